@@ -1,0 +1,400 @@
+#!/usr/bin/env python
+"""Benchmark of the SSD layer forward on B300.
+
+Default workload: the Mamba-2-2.7B-shaped layer at L = 8K (batch 1,
+seqlen 8192, 80 heads, headdim 64, dstate 128, 1 group, chunk 256, bf16
+inputs, fp32 state/accumulation/output, init state ~ N(0, 0.1^2)).  One
+"step" is one ssd_chunk_scan_fwd call over that batch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``value`` is tokens/s with inputs resident in
+HBM; each timed step is bracketed by CUDA events on the launching stream and
+preceded (outside the events) by a 256 MiB write that flushes L2.  ``e2e``
+is the same metric through the public call with pinned host buffers: each
+step copies that step's inputs host->device, runs the call and copies y and
+the final states back.  ``--impl reference`` times the fp64 CPU oracle on
+the host cores instead.  With N > 1 (torchrun) every rank runs its own
+replica of the workload (independent problems, no collective on the data
+path) and ``value`` is the sum over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SSD fwd tokens/sec (2.7B-shaped layer, L=8K) & % of roofline, 1xB300"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="l8k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def algorithmic_cost(wl):
+    """Bytes and FLOPs one forward call must move / do (the roofline's
+    numerator).  Bytes: bf16 x, dt, B, C read once, fp32 y written once,
+    fp32 init and final states once, A and D.  FLOPs: the dense Q x Q chunk
+    blocks of the chunked algorithm (C B^T per group; per head the
+    intra-chunk product, the chunk state and the off-diagonal product)."""
+    ntok = wl.batch * wl.seqlen
+    ein = 2 if wl.dtype == "bf16" else 4
+    H, P, N, G, Q = wl.nheads, wl.headdim, wl.dstate, wl.ngroups, wl.chunk
+    per_tok = H * P * ein + H * P * 4 + H * ein + 2 * G * N * ein
+    nseq = wl.batch if wl.nseq == 0 else wl.nseq
+    states = nseq * H * P * N * 4 * (2 if wl.init == "normal" else 1)
+    bytes_ = ntok * per_tok + states + 2 * H * 4
+    flops_per_tok = 2 * G * Q * N + H * (2 * Q * P + 4 * N * P)
+    return bytes_, ntok * flops_per_tok
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "state_space_sequence_05_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(kernel_key)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle on the host cores, on the same workload."""
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+    import oracle
+    from state_space_sequence_05_b300 import inputs as I
+    wl = I.WORKLOADS[args.workload]
+    fi = I.make_forward_inputs(wl)
+    cores = os.cpu_count() or 1
+    ntok = wl.batch * wl.seqlen
+
+    def step():
+        oracle.ssd_scan(fi.x, fi.dt, fi.A, fi.B, fi.C, fi.D, fi.init, fi.cu_seqlens,
+                        nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = ntok / (ms / 1e3)
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f64", "data": "synthetic",
+           "config": {"workload": f"{wl.name}: b{wl.batch} T{wl.seqlen} H{wl.nheads} "
+                      f"P{wl.headdim} N{wl.dstate} G{wl.ngroups} chunk{wl.chunk}"},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": "the full workload per step (all heads, all tokens)"},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import numpy as np
+    import torch
+    import __graft_entry__
+    from state_space_sequence_05_b300 import inputs as I
+    from state_space_sequence_05_b300 import ssd
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        __graft_entry__.build_library()
+    if world > 1:
+        dist.barrier()
+    ssd.load_library()
+
+    wl = I.WORKLOADS[args.workload]
+    fi = I.make_forward_inputs(wl)
+    wl = fi.wl
+    d = {k: I.as_torch(getattr(fi, k), fi.bits.get(k), dev, wl.dtype) for k in ("x", "dt", "B", "C")}
+    A = torch.from_numpy(fi.A).to(dev)
+    D = torch.from_numpy(fi.D).to(dev)
+    init = None if fi.init is None else torch.from_numpy(fi.init).to(dev)
+    cu = None if fi.cu_seqlens is None else torch.from_numpy(fi.cu_seqlens).to(dev)
+    nseq = fi.nseq
+    H, P, N, G = wl.nheads, wl.headdim, wl.dstate, wl.ngroups
+    y = torch.empty((wl.batch, wl.seqlen, H, P), device=dev, dtype=torch.float32)
+    fin = torch.empty((nseq, H, P, N), device=dev, dtype=torch.float32)
+    code = ssd.SSD_DT_BF16 if wl.dtype == "bf16" else ssd.SSD_DT_F32
+    wsb = ssd.ssd_chunk_scan_fwd_workspace_size(wl.batch, wl.seqlen, H, P, N, G, wl.chunk, code,
+                                                cu is not None, nseq)
+    ws = torch.empty(max(wsb, 1), device=dev, dtype=torch.uint8)
+    status = torch.zeros(1, device=dev, dtype=torch.int32)
+    flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        ssd.ssd_chunk_scan_fwd(d["x"], d["dt"], A, d["B"], d["C"], D, wl.chunk, init, cu, y=y,
+                               final_states=fin, workspace=ws, dev_status=status, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())} after warm-up")
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = ssd.kernel_launches()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = ssd.kernel_launches() - launches0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ntok = wl.batch * wl.seqlen
+    value = ntok * world / (ms / 1e3)
+
+    peaks, peak_src = load_peaks()
+    bytes_, flops = algorithmic_cost(wl)
+    gbs = bytes_ / (ms / 1e3) / 1e9
+    tflops = flops / (ms / 1e3) / 1e12
+    kernel_key = f"ssd_fwd/{wl.name}"
+    roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_from_profiles(kernel_key),
+                "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)",
+                "algorithmic_bytes": bytes_, "algorithmic_flops": flops,
+                "tensor_tflops": tflops,
+                "tensor_frac_of_burst": tflops / peaks["bf16_tflops"],
+                "roofline_time_us": 1e6 * max(bytes_ / (peaks["hbm_gbs"] * 1e9),
+                                              flops / (peaks["bf16_tflops"] * 1e12)),
+                "measured_us": ms * 1e3,
+                "timed": "whole ssd_chunk_scan_fwd call, CUDA events on its stream"}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, fi, wl, dev, A, D, call_kwargs=dict(chunk=wl.chunk, ws=ws,
+                                                                     status=status))
+        if world > 1:
+            t = torch.tensor([e2e["_ms"]], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["_ms"] = float(t.item())
+        e2e["value"] = ntok * world / (e2e.pop("_ms") / 1e3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(fi, wl)
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": wl.dtype, "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
+               "config": {"workload": f"{wl.name}: b{wl.batch} T{wl.seqlen} H{H} P{P} N{N} "
+                                      f"G{G} chunk{wl.chunk}, bf16 in / fp32 state+y, "
+                                      f"init {wl.init}",
+                          "global_batch": wl.batch * world, "seq_len": wl.seqlen,
+                          "parallelism": "replicas" if world > 1 else "single GPU",
+                          "l2": "flushed before every timed step (256 MiB write outside the events)"},
+               "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
+               "launches_per_step": launches / max(1, args.steps),
+               "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
+               "e2e": e2e, "cpu_baseline": cpu,
+               "pages_claim": "SSD 2-8x faster than Mamba's fused selective scan (A100), context only"}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def measure_e2e(args, fi, wl, dev, A, D, call_kwargs):
+    """Public call with pinned host buffers; H2D of the step's inputs and D2H
+    of y and the final states inside the timed region."""
+    import torch
+    from state_space_sequence_05_b300 import inputs as I
+    from state_space_sequence_05_b300 import ssd
+    host = {k: I.as_torch(getattr(fi, k), fi.bits.get(k), "cpu", wl.dtype).pin_memory()
+            for k in ("x", "dt", "B", "C")}
+    host_init = None if fi.init is None else torch.from_numpy(fi.init).pin_memory()
+    host_cu = None if fi.cu_seqlens is None else torch.from_numpy(fi.cu_seqlens).pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    dinit = None if host_init is None else torch.empty_like(host_init, device=dev)
+    dcu = None if host_cu is None else torch.empty_like(host_cu, device=dev)
+    H, P, N = wl.nheads, wl.headdim, wl.dstate
+    y = torch.empty((wl.batch, wl.seqlen, H, P), device=dev, dtype=torch.float32)
+    fin = torch.empty((fi.nseq, H, P, N), device=dev, dtype=torch.float32)
+    y_h = torch.empty(y.shape, dtype=torch.float32).pin_memory()
+    fin_h = torch.empty(fin.shape, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d += 0 if host_init is None else host_init.numel() * 4
+    h2d += 0 if host_cu is None else host_cu.numel() * 4
+    d2h = (y.numel() + fin.numel()) * 4
+
+    def step():
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        if dinit is not None:
+            dinit.copy_(host_init, non_blocking=True)
+        if dcu is not None:
+            dcu.copy_(host_cu, non_blocking=True)
+        ssd.ssd_chunk_scan_fwd(dbuf["x"], dbuf["dt"], A, dbuf["B"], dbuf["C"], D,
+                               call_kwargs["chunk"], dinit, dcu, y=y, final_states=fin,
+                               workspace=call_kwargs["ws"], dev_status=call_kwargs["status"],
+                               stream=stream)
+        y_h.copy_(y, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 20))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return {"_ms": s.elapsed_time(e) / n, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def cpu_baseline(fi, wl):
+    """The fp64 oracle as it stands, on all host cores, over the full workload."""
+    import oracle
+    cores = os.cpu_count() or 1
+    oracle.build()
+    ts = []
+    for _ in range(2):
+        t0 = time.perf_counter()
+        oracle.ssd_scan(fi.x, fi.dt, fi.A, fi.B, fi.C, fi.D, fi.init, fi.cu_seqlens,
+                        nthreads=cores)
+        ts.append(time.perf_counter() - t0)
+    t = min(ts)
+    ntok = wl.batch * wl.seqlen
+    return {"value": ntok / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"full {wl.name} workload ({ntok} tokens x {wl.nheads} heads), best of 2"}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+/*
+ * ssd.h -- C ABI of the B300 (sm_103a) SSD layer library, libssd_b300.so.
+ *
+ * The library computes the Structured State Space Duality (SSD) layer of
+ * Mamba-2, forward only, on one GPU:
+ *
+ *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * x_t B_t^T      (state P x N)
+ *     y_t = h_t C_t + D_h * x_t
+ *
+ * per head h, with A_h one scalar per head and B, C shared by the heads of a
+ * group.  Sources: the recurrence "h_t = A_t h_{t-1} + B_t x_t,
+ * y_t = C_t^T h_t" ("Mamba-2는 왜 Transformer와 닮았는가", bdev.io, section
+ * "문제: 선형 복잡도만으로는 충분하지 않다"); ZOH A-bar = exp(dt A),
+ * B-bar ~= dt B and the skip term D x ("20.1 상태 공간 모델 (SSM)",
+ * sungeuns.github.io, sec. 1 and the loop of sec. 5); scalar-times-identity
+ * A and heads sharing B/C ("Transformers are SSMs Review",
+ * dimensionstp.github.io, sec. 3-2 (3) and (5)); the chunked algorithm --
+ * intra-chunk quadratic blocks, chunk states, state passing, off-diagonal
+ * output -- (same review, sec. 3-2 (4)); varlen packing with the state cut
+ * at sequence boundaries (same review, sec. 3-2 (6)).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library keeps no pointer after a call returns and allocates no device
+ *    or host memory.
+ *  - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream).  Results are complete when the
+ *    stream reaches the point after the call.
+ *  - Argument checks run on the host before anything is launched; a failing
+ *    check returns SSD_ERR_INVALID or SSD_ERR_UNSUPPORTED and launches
+ *    nothing.  A launch failure returns SSD_ERR_CUDA.
+ *  - Errors that only the device can see (an invalid cu_seqlens array, a
+ *    bounded wait that expired) are written to *dev_status when it is not
+ *    NULL: the library clears it at the start of the call and a kernel
+ *    stores the SSD_ERR_* code there.  Read it after synchronising.
+ *  - Layouts are dense row-major (C order) with the shapes given below.
+ *    x, B, C and y must be 16-byte aligned.
+ *  - Head h reads group g(h) = floor(h * ngroups / nheads); nheads must be
+ *    a multiple of ngroups.
+ */
+#ifndef SSD_B300_H
+#define SSD_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID = 1,      /* bad pointer, size or layout */
+    SSD_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels handle */
+    SSD_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    SSD_ERR_TIMEOUT = 4       /* device: a bounded inter-block wait expired */
+} ssd_status_t;
+
+typedef enum {
+    SSD_DT_F32 = 0,   /* x, dt, B, C as float32 */
+    SSD_DT_BF16 = 1   /* x, dt, B, C as bfloat16 */
+} ssd_dtype_t;
+
+/*
+ * ssd_chunk_scan_fwd -- SSD layer forward over whole sequences.
+ *
+ * Inputs (`in_dtype` elements unless stated):
+ *   x   [ntok, nheads, headdim]     ntok = batch * seqlen
+ *   dt  [ntok, nheads]              step sizes, already positive
+ *   A   [nheads] float32            per-head decay rate (A <= 0 in practice)
+ *   B   [ntok, ngroups, dstate]
+ *   C   [ntok, ngroups, dstate]
+ *   D   [nheads] float32 or NULL    skip weight; NULL means 0
+ *   init_states float32 [nseq_or_batch, nheads, headdim, dstate] or NULL
+ *               (NULL means a zero state for every sequence)
+ *   cu_seqlens  int32 [nseq + 1] DEVICE array or NULL.  NULL: `batch`
+ *               independent rows of `seqlen` tokens.  Otherwise `batch`
+ *               must be 1 and the nseq sequences are the packed token
+ *               ranges [cu_seqlens[s], cu_seqlens[s+1]); cu_seqlens[0] = 0,
+ *               non-decreasing, cu_seqlens[nseq] = seqlen.  The state is
+ *               reset (or set from init_states[s]) at every sequence start.
+ *               A malformed array is detected on the device: nothing is
+ *               computed and *dev_status receives SSD_ERR_INVALID.
+ * Outputs (float32):
+ *   y            [ntok, nheads, headdim]
+ *   final_states [nseq_or_batch, nheads, headdim, dstate] or NULL
+ * Scratch:
+ *   workspace / workspace_bytes: device memory of at least
+ *   ssd_chunk_scan_fwd_workspace_size(...) bytes, 256-byte aligned, owned by
+ *   the caller; its contents on entry do not matter.  Calls that overlap in
+ *   time must not share a workspace.
+ * Supported: chunk_size in {64, 128, 256}; headdim in [1, 128] and
+ *   dstate in {16, 32, 64, 128, 256} for float32 inputs; for bfloat16
+ *   inputs headdim == 64 and dstate == 128 run on the tcgen05 tensor-core
+ *   kernel and the other shapes of the float32 list on the CUDA-core
+ *   kernels.  The result does not depend on chunk_size beyond rounding: the
+ *   chunked algorithm is an exact reordering of the recurrence.
+ */
+ssd_status_t ssd_chunk_scan_fwd(
+    const void *x, const void *dt, const float *A, const void *B, const void *C,
+    const float *D, int batch, int seqlen, int nheads, int headdim, int dstate,
+    int ngroups, int chunk_size, ssd_dtype_t in_dtype, const float *init_states,
+    const int32_t *cu_seqlens, int nseq, float *y, float *final_states,
+    void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Bytes of workspace ssd_chunk_scan_fwd needs for these arguments (0 is a
+ * valid answer).  nseq is ignored unless cu_seqlens will be passed
+ * (`varlen` != 0).  Returns (size_t)-1 for arguments ssd_chunk_scan_fwd
+ * would reject.
+ */
+size_t ssd_chunk_scan_fwd_workspace_size(int batch, int seqlen, int nheads, int headdim,
+                                         int dstate, int ngroups, int chunk_size,
+                                         ssd_dtype_t in_dtype, int varlen, int nseq);
+
+/*
+ * ssd_state_update -- one decode step for one new token per batch row, in
+ * place: the loop body of the recurrence applied to a stored state
+ * ("Transformers are SSMs Review", sec. 1-1: constant-size recurrent state
+ * for autoregressive inference; "20.1 상태 공간 모델 (SSM)", sec. 5 loop).
+ *
+ *   state [batch, nheads, headdim, dstate] float32, read and overwritten
+ *   x  [batch, nheads, headdim]   dt [batch, nheads]   (in_dtype)
+ *   A  [nheads] float32           D [nheads] float32 or NULL
+ *   B, C [batch, ngroups, dstate] (in_dtype)
+ *   y  [batch, nheads, headdim] float32 output
+ * Supported: dstate in {16, 32, 64, 128, 256}, headdim >= 1.  state must be
+ * 16-byte aligned.  No workspace.
+ */
+ssd_status_t ssd_state_update(float *state, const void *x, const void *dt, const float *A,
+                              const void *B, const void *C, const float *D, int batch,
+                              int nheads, int headdim, int dstate, int ngroups,
+                              ssd_dtype_t in_dtype, float *y, void *stream);
+
+/* Short English text for a status code (static storage). */
+const char *ssd_status_string(ssd_status_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ssd_version(void);
+
+/*
+ * Number of CUDA kernels this library has launched in this process so far
+ * (all entry points, all devices).  A diagnostic for callers that account
+ * for launches; it never resets.
+ */
+uint64_t ssd_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_B300_H */

@@ -1,0 +1,156 @@
+// ssd_api.cu -- the extern "C" boundary of libssd_b300.so: argument checks,
+// workspace sizing and dispatch to the kernels.  See include/ssd.h for the
+// contract of each entry point.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "ssd.h"
+#include "ssd_internal.h"
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+}  // namespace
+
+void ssd::count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+
+using ssd::FwdArgs;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dstate_ok(int n) { return n == 16 || n == 32 || n == 64 || n == 128 || n == 256; }
+
+// Shape/pointer checks shared by the forward entry point and its workspace
+// query.  Pointers are checked only when `check_ptrs`.
+ssd_status_t check_fwd(const FwdArgs& a, bool check_ptrs) {
+  if (a.dtype != SSD_DT_F32 && a.dtype != SSD_DT_BF16) return SSD_ERR_INVALID;
+  if (a.batch < 0 || a.seqlen < 0 || a.H <= 0 || a.P <= 0 || a.N <= 0 || a.G <= 0)
+    return SSD_ERR_INVALID;
+  if (a.H % a.G != 0) return SSD_ERR_INVALID;
+  if ((long long)a.batch * a.seqlen >= (1LL << 31)) return SSD_ERR_UNSUPPORTED;
+  if (a.Q != 64 && a.Q != 128 && a.Q != 256) return SSD_ERR_UNSUPPORTED;
+  if (a.P > 128 || !dstate_ok(a.N)) return SSD_ERR_UNSUPPORTED;
+  if (a.cu) {
+    if (a.batch != 1 || a.nseq < 0) return SSD_ERR_INVALID;
+    if (a.nseq == 0 && a.seqlen != 0) return SSD_ERR_INVALID;
+  }
+  if (!check_ptrs) return SSD_OK;
+  const long long ntok = (long long)a.batch * a.seqlen;
+  if (ntok > 0 && (!a.x || !a.dt || !a.B || !a.C || !a.y)) return SSD_ERR_INVALID;
+  if (!a.A) return SSD_ERR_INVALID;
+  if (!aligned16(a.x) || !aligned16(a.B) || !aligned16(a.C) || !aligned16(a.y))
+    return SSD_ERR_INVALID;
+  if (!aligned16(a.init) || !aligned16(a.final_states)) return SSD_ERR_INVALID;
+  return SSD_OK;
+}
+
+size_t fwd_workspace(const FwdArgs& a) {
+  if (a.nseq == 0) return 0;
+  if (ssd::tc_supported(a)) return ssd::tc_workspace_bytes(a);
+  return ssd::simt_workspace_bytes(a);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ssd_status_string(ssd_status_t s) {
+  switch (s) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_INVALID: return "invalid argument";
+    case SSD_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case SSD_ERR_CUDA: return "CUDA runtime error";
+    case SSD_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int ssd_version(void) { return 100; }
+
+uint64_t ssd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t ssd_chunk_scan_fwd_workspace_size(int batch, int seqlen, int nheads, int headdim,
+                                         int dstate, int ngroups, int chunk_size,
+                                         ssd_dtype_t in_dtype, int varlen, int nseq) {
+  static const int32_t kDummy = 0;
+  FwdArgs a{};
+  a.batch = batch;
+  a.seqlen = seqlen;
+  a.H = nheads;
+  a.P = headdim;
+  a.N = dstate;
+  a.G = ngroups;
+  a.Q = chunk_size;
+  a.dtype = in_dtype;
+  a.cu = varlen ? &kDummy : nullptr;  // only its presence matters here
+  a.nseq = varlen ? nseq : batch;
+  if (check_fwd(a, false) != SSD_OK) return (size_t)-1;
+  return fwd_workspace(a);
+}
+
+ssd_status_t ssd_chunk_scan_fwd(const void* x, const void* dt, const float* A, const void* B,
+                                const void* C, const float* D, int batch, int seqlen,
+                                int nheads, int headdim, int dstate, int ngroups, int chunk_size,
+                                ssd_dtype_t in_dtype, const float* init_states,
+                                const int32_t* cu_seqlens, int nseq, float* y,
+                                float* final_states, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, void* stream) {
+  FwdArgs a{};
+  a.x = x;
+  a.dt = dt;
+  a.A = A;
+  a.B = B;
+  a.C = C;
+  a.D = D;
+  a.batch = batch;
+  a.seqlen = seqlen;
+  a.H = nheads;
+  a.P = headdim;
+  a.N = dstate;
+  a.G = ngroups;
+  a.Q = chunk_size;
+  a.dtype = in_dtype;
+  a.init = init_states;
+  a.cu = cu_seqlens;
+  a.nseq = cu_seqlens ? nseq : batch;
+  a.y = y;
+  a.final_states = final_states;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  a.dev_status = dev_status;
+  a.stream = static_cast<cudaStream_t>(stream);
+  ssd_status_t st = check_fwd(a, true);
+  if (st != SSD_OK) return st;
+  const size_t need = fwd_workspace(a);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return SSD_ERR_INVALID;
+  if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), a.stream) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  if (a.nseq == 0) return SSD_OK;
+  return ssd::tc_supported(a) ? ssd::tc_forward(a) : ssd::simt_forward(a);
+}
+
+ssd_status_t ssd_state_update(float* state, const void* x, const void* dt, const float* A,
+                              const void* B, const void* C, const float* D, int batch,
+                              int nheads, int headdim, int dstate, int ngroups,
+                              ssd_dtype_t in_dtype, float* y, void* stream) {
+  if (in_dtype != SSD_DT_F32 && in_dtype != SSD_DT_BF16) return SSD_ERR_INVALID;
+  if (batch < 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 || ngroups <= 0)
+    return SSD_ERR_INVALID;
+  if (nheads % ngroups != 0) return SSD_ERR_INVALID;
+  if (!dstate_ok(dstate)) return SSD_ERR_UNSUPPORTED;
+  if ((long long)batch * nheads >= (1LL << 31)) return SSD_ERR_UNSUPPORTED;
+  if (batch == 0) return SSD_OK;
+  if (!state || !x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID;
+  if (!aligned16(state) || !aligned16(B) || !aligned16(C)) return SSD_ERR_INVALID;
+  return ssd::decode_step(state, x, dt, A, B, C, D, batch, nheads, headdim, dstate, ngroups,
+                          in_dtype, y, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// ssd_internal.h -- declarations shared between the library's translation
+// units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ssd.h"
+
+namespace ssd {
+
+struct FwdArgs {
+  const void* x;
+  const void* dt;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  int batch, seqlen, H, P, N, G, Q;
+  ssd_dtype_t dtype;
+  const float* init;
+  const int32_t* cu;
+  int nseq;  // sequences: cu ? nseq : batch
+  float* y;
+  float* final_states;
+  void* ws;
+  size_t ws_bytes;
+  int32_t* dev_status;
+  cudaStream_t stream;
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Launch accounting behind ssd_kernel_launches(): every launch site calls
+// this once per kernel it launches.
+void count_launches(unsigned n);
+
+// Upper bound on the number of `q`-token chunks over all sequences.
+inline long long max_chunks(int batch, int seqlen, int q, bool varlen, int nseq) {
+  long long per = (seqlen + q - 1) / q;
+  return varlen ? per + nseq : (long long)batch * per;
+}
+
+// Sequence plan: offs[0..nseq] chunk offsets plus one status word.
+inline size_t plan_bytes(int nseq) { return align256(sizeof(int32_t) * (size_t(nseq) + 2)); }
+
+// Launch the plan kernel: chunk offsets of `q`-token chunks per sequence
+// into `offs`, with cu_seqlens validation.
+cudaError_t launch_plan(const int32_t* cu, int seqlen_rows, int seqlen_total, int nseq, int q,
+                        int32_t* offs, int32_t* dev_status, cudaStream_t stream);
+
+// CUDA-core (SIMT) chunked forward: any supported shape, fp32 or bf16 in.
+size_t simt_workspace_bytes(const FwdArgs& a);
+ssd_status_t simt_forward(const FwdArgs& a);
+
+// tcgen05 tensor-core forward: bf16 in, headdim 64, dstate 128.
+bool tc_supported(const FwdArgs& a);
+size_t tc_workspace_bytes(const FwdArgs& a);
+ssd_status_t tc_forward(const FwdArgs& a);
+
+// Decode step.
+ssd_status_t decode_step(float* state, const void* x, const void* dt, const float* A,
+                         const void* B, const void* C, const float* D, int batch, int H, int P,
+                         int N, int G, ssd_dtype_t dtype, float* y, cudaStream_t stream);
+
+}  // namespace ssd

@@ -1,0 +1,206 @@
+"""Python binding of libssd_b300.so (ctypes): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this
+module checks tensor placement and dtypes, allocates outputs and the
+workspace with PyTorch, passes raw device pointers and the current CUDA
+stream, and turns status codes into exceptions.  There is no fallback: if
+the library is missing or fails to load, every call raises.
+
+Function names follow the C entry points in include/ssd.h.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssd_b300.so")
+
+SSD_OK, SSD_ERR_INVALID, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT = range(5)
+SSD_DT_F32, SSD_DT_BF16 = 0, 1
+
+# Names and C signatures of every symbol include/ssd.h declares.
+_vp, _fp, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+_ci, _sz = ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "ssd_chunk_scan_fwd": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci, _ci, _ci,
+                                 _ci, _fp, _ip, _ci, _fp, _fp, _vp, _sz, _ip, _vp]),
+    "ssd_chunk_scan_fwd_workspace_size": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci]),
+    "ssd_state_update": (_ci, [_fp, _vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci, _ci,
+                               _fp, _vp]),
+    "ssd_status_string": (ctypes.c_char_p, [_ci]),
+    "ssd_version": (_ci, []),
+    "ssd_kernel_launches": (ctypes.c_uint64, []),
+}
+
+_lib = None
+
+
+class SSDError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the CUDA library (once).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it first (python -m state_space_sequence_05_b300._build "
+            "or __graft_entry__.build()); there is no non-CUDA implementation")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().ssd_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load_library().ssd_version())
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load_library().ssd_kernel_launches())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SSD_DT_BF16
+    if t.dtype == torch.float32:
+        return SSD_DT_F32
+    raise TypeError(f"x/dt/B/C must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need(t, name, device, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def ssd_chunk_scan_fwd_workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups,
+                                      chunk_size, in_dtype, varlen=False, nseq=0) -> int:
+    n = load_library().ssd_chunk_scan_fwd_workspace_size(
+        batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, in_dtype, int(bool(varlen)),
+        nseq)
+    if n == ctypes.c_size_t(-1).value:
+        raise SSDError(SSD_ERR_UNSUPPORTED, "ssd_chunk_scan_fwd_workspace_size")
+    return int(n)
+
+
+def ssd_chunk_scan_fwd(x, dt, A, B, C, D=None, chunk_size=256, init_states=None,
+                       cu_seqlens=None, *, y=None, final_states=None, return_final=True,
+                       workspace=None, dev_status=None, stream=None):
+    """SSD layer forward.  Shapes (device tensors, contiguous):
+
+    x [b, T, H, P], dt [b, T, H], B/C [b, T, G, N] -- all bfloat16 or all
+    float32; A [H] and D [H] float32; init_states [nseq_or_b, H, P, N]
+    float32; cu_seqlens int32 [nseq + 1] (then b must be 1).
+
+    Returns ``(y [b, T, H, P] float32, final_states [nseq_or_b, H, P, N]
+    float32 or None)``.  Raises SSDError on a host-side rejection.  Errors
+    only the device can detect go to ``dev_status`` (an int32 device tensor
+    of one element) when given.
+    """
+    lib = load_library()
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("ssd_chunk_scan_fwd needs CUDA tensors")
+    if x.dim() != 4:
+        raise ValueError("x must be [batch, seqlen, nheads, headdim]")
+    b, T, H, P = x.shape
+    if B.dim() != 4:
+        raise ValueError("B must be [batch, seqlen, ngroups, dstate]")
+    G, N = B.shape[2], B.shape[3]
+    code = _dtype_code(x)
+    _need(x, "x", dev)
+    _need(dt, "dt", dev, x.dtype, (b, T, H))
+    _need(B, "B", dev, x.dtype, (b, T, G, N))
+    _need(C, "C", dev, x.dtype, (b, T, G, N))
+    _need(A, "A", dev, torch.float32, (H,))
+    if D is not None:
+        _need(D, "D", dev, torch.float32, (H,))
+    nseq = b
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", dev, torch.int32)
+        nseq = cu_seqlens.shape[0] - 1
+    if init_states is not None:
+        _need(init_states, "init_states", dev, torch.float32, (nseq, H, P, N))
+    if y is None:
+        y = torch.empty((b, T, H, P), device=dev, dtype=torch.float32)
+    _need(y, "y", dev, torch.float32, (b, T, H, P))
+    if final_states is None and return_final:
+        final_states = torch.empty((nseq, H, P, N), device=dev, dtype=torch.float32)
+    if final_states is not None:
+        _need(final_states, "final_states", dev, torch.float32, (nseq, H, P, N))
+    need = ssd_chunk_scan_fwd_workspace_size(b, T, H, P, N, G, chunk_size, code,
+                                             cu_seqlens is not None, nseq)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.ssd_chunk_scan_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), b, T, H, P,
+                                N, G, chunk_size, code, _ptr(init_states), _ptr(cu_seqlens), nseq,
+                                _ptr(y), _ptr(final_states), _ptr(workspace), ws_bytes,
+                                _ptr(dev_status), _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_chunk_scan_fwd")
+    return y, final_states
+
+
+def ssd_state_update(state, x, dt, A, B, C, D=None, *, y=None, stream=None):
+    """One decode step in place on ``state`` [b, H, P, N] float32.
+
+    x [b, H, P], dt [b, H], B/C [b, G, N] (bfloat16 or float32); A, D [H]
+    float32.  Returns y [b, H, P] float32.
+    """
+    lib = load_library()
+    dev = state.device
+    if dev.type != "cuda":
+        raise ValueError("ssd_state_update needs CUDA tensors")
+    b, H, P, N = state.shape
+    G = B.shape[1]
+    code = _dtype_code(x)
+    _need(state, "state", dev, torch.float32)
+    _need(x, "x", dev, None, (b, H, P))
+    _need(dt, "dt", dev, x.dtype, (b, H))
+    _need(B, "B", dev, x.dtype, (b, G, N))
+    _need(C, "C", dev, x.dtype, (b, G, N))
+    _need(A, "A", dev, torch.float32, (H,))
+    if D is not None:
+        _need(D, "D", dev, torch.float32, (H,))
+    if y is None:
+        y = torch.empty((b, H, P), device=dev, dtype=torch.float32)
+    _need(y, "y", dev, torch.float32, (b, H, P))
+    st = lib.ssd_state_update(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                              b, H, P, N, G, code, _ptr(y), _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_state_update")
+    return y
