@@ -104,6 +104,38 @@ ssd_status_t ssd_chunk_scan_fwd(
     void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * ssd_chunk_scan_fwd_noalloc -- the same forward for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this entry point
+ * exists for the deployment side only.  Some callers cannot call cudaMalloc
+ * or hand over a workspace: a plugin inside a host framework that owns all
+ * device memory and passes in only its inputs and outputs, or a
+ * latency-critical loop in which an allocation (which may synchronise the
+ * device) is not allowed.  This entry point needs neither.
+ *
+ * Arguments, layouts and results are those of ssd_chunk_scan_fwd without
+ * the workspace pair; the caller still passes every input and output.  It
+ * always runs the CUDA-core kernels (fp32 arithmetic), whatever the dtype.
+ * Its scratch memory is one fixed 16 MiB array compiled into the library
+ * (a file-scope __device__ array): every GPU on which the library is loaded
+ * holds those 16 MiB until the process exits.  A problem whose scratch
+ * would exceed 16 MiB is rejected with SSD_ERR_UNSUPPORTED before anything
+ * is launched; the scratch needed is about 4 * nheads * headdim * dstate
+ * bytes per chunk of every sequence.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device
+ * current) and caches it; make that first call before any stream capture.
+ * Every call shares the one array and nothing in it needs to start at zero;
+ * calls whose GPU work overlaps in time (other streams, other threads) race
+ * on it and must be serialised by the caller.  No allocation of any kind is
+ * made, neither by the library nor by any library it calls.
+ */
+ssd_status_t ssd_chunk_scan_fwd_noalloc(
+    const void *x, const void *dt, const float *A, const void *B, const void *C,
+    const float *D, int batch, int seqlen, int nheads, int headdim, int dstate,
+    int ngroups, int chunk_size, ssd_dtype_t in_dtype, const float *init_states,
+    const int32_t *cu_seqlens, int nseq, float *y, float *final_states,
+    int32_t *dev_status, void *stream);
+
+/*
  * Bytes of workspace ssd_chunk_scan_fwd needs for these arguments (0 is a
  * valid answer).  nseq is ignored unless cu_seqlens will be passed
  * (`varlen` != 0).  Returns (size_t)-1 for arguments ssd_chunk_scan_fwd

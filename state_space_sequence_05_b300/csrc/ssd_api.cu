@@ -57,6 +57,10 @@ size_t fwd_workspace(const FwdArgs& a) {
 
 }  // namespace
 
+ssd_status_t ssd::check_fwd_args(const FwdArgs& a, bool check_ptrs) {
+  return check_fwd(a, check_ptrs);
+}
+
 extern "C" {
 
 const char* ssd_status_string(ssd_status_t s) {

@@ -50,6 +50,10 @@ inline size_t plan_bytes(int nseq) { return align256(sizeof(int32_t) * (size_t(n
 cudaError_t launch_plan(const int32_t* cu, int seqlen_rows, int seqlen_total, int nseq, int q,
                         int32_t* offs, int32_t* dev_status, cudaStream_t stream);
 
+// Host-side argument checks of ssd_chunk_scan_fwd (pointers only when
+// `check_ptrs`), shared with the allocation-free entry point.
+ssd_status_t check_fwd_args(const FwdArgs& a, bool check_ptrs);
+
 // CUDA-core (SIMT) chunked forward: any supported shape, fp32 or bf16 in.
 size_t simt_workspace_bytes(const FwdArgs& a);
 ssd_status_t simt_forward(const FwdArgs& a);

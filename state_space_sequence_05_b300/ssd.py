@@ -28,6 +28,8 @@ _ci, _sz = ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "ssd_chunk_scan_fwd": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci, _ci, _ci,
                                  _ci, _fp, _ip, _ci, _fp, _fp, _vp, _sz, _ip, _vp]),
+    "ssd_chunk_scan_fwd_noalloc": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci,
+                                         _ci, _ci, _ci, _fp, _ip, _ci, _fp, _fp, _ip, _vp]),
     "ssd_chunk_scan_fwd_workspace_size": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci]),
     "ssd_state_update": (_ci, [_fp, _vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci, _ci,
                                _fp, _vp]),
