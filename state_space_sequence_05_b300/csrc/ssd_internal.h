@@ -46,9 +46,12 @@ inline long long max_chunks(int batch, int seqlen, int q, bool varlen, int nseq)
 inline size_t plan_bytes(int nseq) { return align256(sizeof(int32_t) * (size_t(nseq) + 2)); }
 
 // Launch the plan kernel: chunk offsets of `q`-token chunks per sequence
-// into `offs`, with cu_seqlens validation.
+// into `offs`, with cu_seqlens validation.  When given, `*ticket` is zeroed
+// and final_states[s] = init[s] (or 0) for sequences without tokens.
 cudaError_t launch_plan(const int32_t* cu, int seqlen_rows, int seqlen_total, int nseq, int q,
-                        int32_t* offs, int32_t* dev_status, cudaStream_t stream);
+                        int32_t* offs, int32_t* dev_status, cudaStream_t stream,
+                        int* ticket = nullptr, const float* init = nullptr,
+                        float* final_states = nullptr, int H = 0, int PN = 0);
 
 // Host-side argument checks of ssd_chunk_scan_fwd (pointers only when
 // `check_ptrs`), shared with the allocation-free entry point.

@@ -64,10 +64,14 @@ __device__ __forceinline__ int block_scan_int_1024(int v, int* buf) {
 
 // Per-sequence chunk offsets.  One block of 1024 threads.  offs[nseq + 1]
 // is the plan status: 0 = valid, else the cu_seqlens array was malformed
-// and every offset is 0 (nothing is computed).
+// and every offset is 0 (nothing is computed).  Optionally zeroes a work
+// ticket and writes final = init (or 0) for sequences with no tokens.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* cu, int seqlen_rows,
                                                     int seqlen_total, int nseq, int q,
-                                                    int32_t* offs, int32_t* dev_status) {
+                                                    int32_t* offs, int32_t* dev_status,
+                                                    int* ticket, const float* init,
+                                                    float* final_states, int H, int PN) {
+  if (ticket && threadIdx.x == 0) *ticket = 0;
   __shared__ int buf[32];
   __shared__ int carry, bad;
   if (threadIdx.x == 0) {
@@ -98,6 +102,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* cu, int seqle
     if (threadIdx.x == 0) report(dev_status, SSD_ERR_INVALID);
   }
   if (threadIdx.x == 0) offs[nseq + 1] = bad;
+  if (final_states && !bad) {
+    const long long per = (long long)H * PN;
+    for (int s = 0; s < nseq; ++s) {
+      if (offs[s + 1] != offs[s]) continue;  // sequence has tokens
+      float* dst = final_states + (long long)s * per;
+      const float* src = init ? init + (long long)s * per : nullptr;
+      for (long long e = threadIdx.x; e < per; e += 1024) dst[e] = src ? src[e] : 0.f;
+    }
+  }
 }
 
 struct ChunkPos {
@@ -389,8 +402,10 @@ ssd_status_t simt_forward_t(const FwdArgs& a) {
 }  // namespace
 
 cudaError_t launch_plan(const int32_t* cu, int seqlen_rows, int seqlen_total, int nseq, int q,
-                        int32_t* offs, int32_t* dev_status, cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(cu, seqlen_rows, seqlen_total, nseq, q, offs, dev_status);
+                        int32_t* offs, int32_t* dev_status, cudaStream_t stream, int* ticket,
+                        const float* init, float* final_states, int H, int PN) {
+  plan_kernel<<<1, 1024, 0, stream>>>(cu, seqlen_rows, seqlen_total, nseq, q, offs, dev_status,
+                                      ticket, init, final_states, H, PN);
   count_launches(1);
   return cudaGetLastError();
 }
