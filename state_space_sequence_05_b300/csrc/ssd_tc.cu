@@ -25,20 +25,35 @@
 // exact reordering of the recurrence), so every chunk_size the API accepts
 // runs with 128-token blocks here.
 //
-// Design (one persistent CTA per SM, 320 threads):
-//   warp 8     TMA producer: per tile loads C (2 x 16 KB), B (2 x 16 KB) and
-//              x (16 KB) into a 2-stage ring with the 128-byte swizzle the
-//              MMA descriptors expect; draws work units from a global ticket.
-//   warp 9     MMA issuer (one thread): C B^T -> TMEM; B^T X' -> TMEM;
-//              C H^T -> TMEM; S X -> TMEM with S read from TMEM.
-//   warps 0-7  CUDA-core math (256 threads, row r = lane of TMEM, column
-//              half hp): cumulative decay, decay weights, the masked S
-//              (written as bf16 pairs over the C B^T accumulator), the
-//              epilogue, and the fp32 state H (registers) with its bf16 copy
-//              in shared memory for the next chunk's C H^T.
-// A work unit is one (sequence, head); the state never leaves the SM
-// between chunks.  Every inter-warp wait is an mbarrier wait bounded in
-// time; on expiry the kernel records SSD_ERR_TIMEOUT and unwinds.
+// Work partition.  Each sequence is cut into segments of kSeg chunks; a
+// work unit is one (sequence, segment, head), handed out in that order by a
+// global ticket, so a unit's predecessor (same sequence and head, previous
+// segment) was always taken earlier by a running CTA.  A unit
+//   1. accumulates its segment's local state H_loc (the decayed sum of its
+//      chunk states, from a zero state) on the tensor cores, walking the
+//      chunks backwards so the decay to the segment end is a running sum --
+//      skipped for the last segment of a sequence;
+//   2. takes the state entering the segment, H_in, from the initial state
+//      (first segment) or from its predecessor's published end state, and
+//      publishes its own end state exp(sum of the segment's dt A) H_in +
+//      H_loc with a release flag: the inter-chunk recurrence carried across
+//      CTAs at segment granularity, i.e. the composition of affine maps
+//      (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2) ("Mamba ... review",
+//      feghi.github.io, sec. 4);
+//   3. runs the forward over its chunks starting from H_in.
+// The state never leaves the SM between the chunks of a segment.
+//
+// Roles (one persistent CTA per SM, 320 threads):
+//   warp 8     TMA producer: C, B, x tiles (128B swizzle) into a 2-stage ring.
+//   warp 9     MMA issuer (one thread): C B^T, B^T (w o X), C H^T and S X
+//              (S read from tensor memory); issues the next chunk's C B^T
+//              ahead of the current chunk's products.
+//   warps 0-7  CUDA-core math (TMEM lane r, column half hp): cumulative
+//              decay, decay mask (built for chunk c+1 while the tensor core
+//              works on chunk c), epilogue, fp32 state in registers,
+//              segment hand-off.
+// Every wait is bounded in time; on expiry the kernel records
+// SSD_ERR_TIMEOUT and unwinds.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -56,38 +71,51 @@ using namespace tc;
 constexpr int kQ = 128;  // chunk tokens = MMA M
 constexpr int kP = 64;   // headdim
 constexpr int kN = 128;  // dstate
+constexpr int kPN = kP * kN;
 constexpr int kStages = 2;
 constexpr int kMathWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 
-constexpr uint32_t kTile = 16384;                 // one 128 x 64 bf16 tile
-constexpr uint32_t kStageBytes = 5 * kTile;       // C0 C1 B0 B1 X
+constexpr uint32_t kTile = 16384;                   // one 128 x 64 bf16 tile
+constexpr uint32_t kStageBytes = 5 * kTile;         // C0 C1 B0 B1 X
+constexpr uint32_t kStageBytesA = 3 * kTile;        // B0 B1 X (segment-state pass)
 constexpr uint32_t kOffXw = kStages * kStageBytes;  // w o X as bf16 hi, lo (2 x 16 KB)
 constexpr uint32_t kOffHt = kOffXw + 2 * kTile;     // H^T as bf16 hi, lo (2 x 16 KB)
 constexpr uint32_t kOffTabs = kOffHt + 2 * kTile;   // c2[128] dt[128] part[8]
 constexpr uint32_t kOffInfo = kOffTabs + 4 * 272;
-constexpr uint32_t kSmemUse = kOffInfo + 128;
-constexpr uint32_t kSmemBytes = kSmemUse + 1024;  // slack for 1024-B alignment
+constexpr uint32_t kSmemUse = kOffInfo + 2 * 64;
+constexpr uint32_t kSmemBytes = kSmemUse + 1024;    // slack for 1024-B alignment
 
 // TMEM columns (fp32 accumulators, 128 lanes).
-constexpr uint32_t kColCB = 0;     // 2 x 128: C B^T, overwritten by bf16 S hi (64) | lo (64)
+constexpr uint32_t kColCB = 0;     // 2 x 128: C B^T, overwritten in place by S (hi/lo pairs)
 constexpr uint32_t kColYD = 256;   // 64: S X
-constexpr uint32_t kColST = 320;   // 64: chunk state (transposed: lane n, column p)
-constexpr uint32_t kColYO = 384;   // 64: C H^T
+constexpr uint32_t kColYO = 320;   // 64: C H^T
+constexpr uint32_t kColST = 384;   // 64: chunk state (lane n, column p)
+constexpr uint32_t kColSA = 448;   // 64: segment-local state (lane n, column p)
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
+// Chunks per segment: 8 chunks (1024 tokens) keep the segment-state pass
+// and the hand-off cheap while giving several units per SM on 8K tokens.
+constexpr int kSeg = 8;
+
+enum : int { kKindA = 0, kKindB = 1, kKindEnd = 2 };
+
 struct TileInfo {
   long long t0;  // first token of the chunk
-  int s, h;      // sequence, head
-  int len;       // valid rows (1..128); 0 = no more work
-  int first, last;
-  int pad;
+  int s, h, sigma, unit;
+  int len;       // valid rows (1..128)
+  int kind;      // kKindA (segment-state pass), kKindB (forward), kKindEnd
+  int idx, cnt;  // position of this chunk among the unit's chunks of its kind
+  int nA;        // chunks in the unit's segment-state pass (0 = none)
+  int last_seg;  // the unit is its sequence's last segment
+  int pad[2];
 };
+static_assert(sizeof(TileInfo) <= 64, "tile info slot");
 
 struct Params {
   const __nv_bfloat16* dt;
@@ -97,10 +125,12 @@ struct Params {
   float* y;
   float* final_states;
   SeqInfo si;
-  const int32_t* offs;  // plan; offs[nseq+1] != 0 => malformed cu_seqlens
+  const int32_t* uoff;  // [nseq + 2]: unit offsets per sequence, then plan status
   int* ticket;
+  int* flags;           // per unit: 1 once its segment end state is published
+  float* slots;         // per unit: segment end state [P][N] fp32
   int32_t* status;
-  int H, G, nunits;
+  int H, G, seg;
 };
 
 __device__ __forceinline__ unsigned long long gtime() {
@@ -128,6 +158,15 @@ __device__ __forceinline__ bool math_sync(uint64_t* bar, uint32_t par) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
   return wait_bar(bar, par);
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -164,7 +203,6 @@ __device__ __forceinline__ void store_split_row(uint8_t* hi_tile, uint8_t* lo_ti
 
 struct Smem {
   uint8_t* base;
-  uint64_t* bars;
   __device__ uint8_t* stage(int s) const { return base + s * kStageBytes; }
   __device__ uint8_t* C(int s, int half) const { return stage(s) + half * kTile; }
   __device__ uint8_t* B(int s, int half) const { return stage(s) + (2 + half) * kTile; }
@@ -181,8 +219,15 @@ struct Smem {
 
 // barrier indices
 enum {
-  kFull0 = 0, kFull1, kEmpty0, kEmpty1, kCbFull0, kCbFull1, kCbsEmpty0, kCbsEmpty1,
-  kXsReady, kSReady, kHReady, kAccFull, kAccEmpty, kSync0, kSync1, kSync2, kMmaDone,
+  kFull0 = 0, kFull1, kEmpty0, kEmpty1,      // TMA stage ring
+  kCbFull0, kCbFull1, kCbEmpty0, kCbEmpty1,  // C B^T / S buffers in TMEM
+  kSFull,                                    // S written (math -> MMA)
+  kXwFull, kXwEmpty,                         // w o X buffer
+  kHFull, kHEmpty,                           // H^T buffer
+  kAccFull, kAccEmpty,                       // Y_diag / Y_off / chunk-state accumulators
+  kAggFull, kAggEmpty,                       // segment-local state accumulator
+  kSyncCum0, kSyncCum1, kSyncHand,           // math-warp rendezvous
+  kMmaDone,
   kNumBars
 };
 
@@ -197,7 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~uintptr_t(1023));
-  sm.bars = bars;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
@@ -208,16 +252,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kEmpty1], 1 + kMathWarps);
     mbar_init(&bars[kCbFull0], 1);
     mbar_init(&bars[kCbFull1], 1);
-    mbar_init(&bars[kCbsEmpty0], 1);
-    mbar_init(&bars[kCbsEmpty1], 1);
-    mbar_init(&bars[kXsReady], kMathWarps);
-    mbar_init(&bars[kSReady], kMathWarps);
-    mbar_init(&bars[kHReady], kMathWarps);
+    mbar_init(&bars[kCbEmpty0], 1);
+    mbar_init(&bars[kCbEmpty1], 1);
+    mbar_init(&bars[kSFull], kMathWarps);
+    mbar_init(&bars[kXwFull], kMathWarps);
+    mbar_init(&bars[kXwEmpty], 1);
+    mbar_init(&bars[kHFull], kMathWarps);
+    mbar_init(&bars[kHEmpty], 1);
     mbar_init(&bars[kAccFull], 1);
     mbar_init(&bars[kAccEmpty], kMathWarps);
-    mbar_init(&bars[kSync0], kMathWarps);
-    mbar_init(&bars[kSync1], kMathWarps);
-    mbar_init(&bars[kSync2], kMathWarps);
+    mbar_init(&bars[kAggFull], 1);
+    mbar_init(&bars[kAggEmpty], kMathWarps);
+    mbar_init(&bars[kSyncCum0], kMathWarps);
+    mbar_init(&bars[kSyncCum1], kMathWarps);
+    mbar_init(&bars[kSyncHand], kMathWarps);
     mbar_init(&bars[kMmaDone], 1);
     abort_sh = 0;
     fence_mbar_init();
@@ -230,11 +278,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  volatile int* abort_v = &abort_sh;
 
   auto fail = [&](int code) {
     report(prm.status, code);
     atomicExch(&abort_sh, 1);
   };
+
+  const int nseq = prm.si.nseq;
+  const int nunits = prm.uoff[nseq];
+  const bool plan_ok = prm.uoff[nseq + 1] == 0;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -242,44 +295,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&map_x);
       prefetch_tmap(&map_b);
       prefetch_tmap(&map_c);
-      const bool plan_ok = prm.offs[prm.si.nseq + 1] == 0;
       uint32_t it = 0;
       bool ok = true;
       while (ok && plan_ok) {
         const int u = atomicAdd(prm.ticket, 1);
-        if (u >= prm.nunits) break;
-        const int s = u / prm.H, h = u % prm.H;
+        if (u >= nunits) break;
+        const int s = upper_index(prm.uoff, nseq, u);
+        const int rem = u - prm.uoff[s];
+        const int sigma = rem / prm.H, h = rem % prm.H;
         const int g = (int)((long long)h * prm.G / prm.H);
         const long long b = prm.si.begin(s), e = prm.si.end(s);
-        const int ntiles = (int)((e - b + kQ - 1) / kQ);
-        for (int t = 0; t < ntiles; ++t, ++it) {
+        const int nt = (int)((e - b + kQ - 1) / kQ);
+        const int tb = sigma * prm.seg, te = min(nt, tb + prm.seg);
+        const int last_seg = te == nt;
+        const int nA = last_seg ? 0 : te - tb, nB = te - tb;
+        for (int k = 0; k < nA + nB; ++k, ++it) {
+          const int kind = k < nA ? kKindA : kKindB;
+          const int t = kind == kKindA ? te - 1 - k : tb + (k - nA);
           const int st = it & 1;
           if (it >= 2 && !wait_bar(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1)) {
             fail(SSD_ERR_TIMEOUT);
             ok = false;
             break;
           }
-          if (*(volatile int*)&abort_sh) { ok = false; break; }
+          if (*abort_v) { ok = false; break; }
           TileInfo* inf = sm.info(st);
           inf->t0 = b + (long long)t * kQ;
           inf->s = s;
           inf->h = h;
+          inf->sigma = sigma;
+          inf->unit = u;
           inf->len = (int)min((long long)kQ, e - inf->t0);
-          inf->first = t == 0;
-          inf->last = t == ntiles - 1;
+          inf->kind = kind;
+          inf->idx = kind == kKindA ? k : k - nA;
+          inf->cnt = kind == kKindA ? nA : nB;
+          inf->nA = nA;
+          inf->last_seg = last_seg;
           const int row = (int)inf->t0;
-          mbar_arrive_expect_tx(&bars[kFull0 + st], kStageBytes);
-          tma_load_2d(sm.C(st, 0), &map_c, &bars[kFull0 + st], g * kN, row);
-          tma_load_2d(sm.C(st, 1), &map_c, &bars[kFull0 + st], g * kN + 64, row);
-          tma_load_2d(sm.B(st, 0), &map_b, &bars[kFull0 + st], g * kN, row);
-          tma_load_2d(sm.B(st, 1), &map_b, &bars[kFull0 + st], g * kN + 64, row);
-          tma_load_2d(sm.X(st), &map_x, &bars[kFull0 + st], h * kP, row);
+          uint64_t* fb = &bars[kFull0 + st];
+          if (kind == kKindB) {
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            tma_load_2d(sm.C(st, 0), &map_c, fb, g * kN, row);
+            tma_load_2d(sm.C(st, 1), &map_c, fb, g * kN + 64, row);
+          } else {
+            mbar_arrive_expect_tx(fb, kStageBytesA);
+          }
+          tma_load_2d(sm.B(st, 0), &map_b, fb, g * kN, row);
+          tma_load_2d(sm.B(st, 1), &map_b, fb, g * kN + 64, row);
+          tma_load_2d(sm.X(st), &map_x, fb, h * kP, row);
         }
       }
       // sentinel: no more work
       const int st = it & 1;
       if (ok && (it < 2 || wait_bar(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1))) {
-        sm.info(st)->len = 0;
+        sm.info(st)->kind = kKindEnd;
         mbar_arrive(&bars[kFull0 + st]);
       } else {
         if (ok) fail(SSD_ERR_TIMEOUT);
@@ -295,45 +364,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idST = idesc_bf16(128, 64, true, true);
       constexpr uint32_t idYO = idesc_bf16(128, 64, false, true);
       constexpr uint32_t idYD = idesc_bf16(128, 64, false, true);
-      uint32_t it = 0;
+      uint32_t it = 0, bt = 0, xu = 0, au = 0;
       bool issued = false;
-      while (true) {
-        const int st = it & 1;
-        if (!wait_bar(&bars[kFull0 + st], (it >> 1) & 1)) { fail(SSD_ERR_TIMEOUT); break; }
-        if (sm.info(st)->len == 0 || *(volatile int*)&abort_sh) break;
-        const uint32_t cbcol = tmem + kColCB + st * 128;
-        if (it >= 2 && !wait_bar(&bars[kCbsEmpty0 + st], ((it >> 1) - 1) & 1)) {
-          fail(SSD_ERR_TIMEOUT);
-          break;
-        }
-        tc_fence_after();
+#define MMA_WAIT(bar, par)            \
+  if (!wait_bar(&bars[bar], (par))) { \
+    fail(SSD_ERR_TIMEOUT);            \
+    break;                            \
+  }
+      // C B^T of ring chunk `rit`, forward-chunk number `rbt`
+      auto issue_cb = [&](uint32_t rit, uint32_t rbt) {
+        const int st = rit & 1;
+        const uint32_t cbcol = tmem + kColCB + (rbt & 1) * 128;
         const uint32_t aC0 = smem_u32(sm.C(st, 0)), aC1 = smem_u32(sm.C(st, 1));
         const uint32_t aB0 = smem_u32(sm.B(st, 0)), aB1 = smem_u32(sm.B(st, 1));
-        const uint32_t aX = smem_u32(sm.X(st));
-        // G = C B^T (both K-major; K = dstate over two 64-wide boxes)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t kb = (k & 3) * 32;
           mma_bf16(cbcol, sdesc_sw128((k < 4 ? aC0 : aC1) + kb, 16, 1024),
                    sdesc_sw128((k < 4 ? aB0 : aB1) + kb, 16, 1024), idCB, k > 0);
         }
-        mma_commit(&bars[kCbFull0 + st]);
-        issued = true;
-        if (it >= 1 && !wait_bar(&bars[kAccEmpty], (it - 1) & 1)) { fail(SSD_ERR_TIMEOUT); break; }
-        if (!wait_bar(&bars[kXsReady], it & 1)) { fail(SSD_ERR_TIMEOUT); break; }
+        mma_commit(&bars[kCbFull0 + (rbt & 1)]);
+      };
+      while (true) {
+        const int st = it & 1;
+        MMA_WAIT(kFull0 + st, (it >> 1) & 1);
+        const TileInfo inf = *sm.info(st);
+        if (inf.kind == kKindEnd || *abort_v) break;
         tc_fence_after();
-        // chunk state S_c^T (n x p) = B^T (w o X): A MN-major (B rows j), B MN-major
+        const uint32_t aB0 = smem_u32(sm.B(st, 0));
+        if (inf.kind == kKindA) {
+          // segment-local state: SA (+)= B^T (w o X), hi and lo halves
+          if (inf.idx == 0 && au >= 1) { MMA_WAIT(kAggEmpty, (au - 1) & 1); }
+          MMA_WAIT(kXwFull, xu & 1);
+          tc_fence_after();
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t aXw = smem_u32(sm.Xw(part));
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t aXw = smem_u32(sm.Xw(part));
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_bf16(tmem + kColST, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
-                     sdesc_sw128(aXw + k * 2048, kTile, 1024), idST, part > 0 || k > 0);
+            for (int k = 0; k < 8; ++k)
+              mma_bf16(tmem + kColSA, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
+                       sdesc_sw128(aXw + k * 2048, kTile, 1024), idST,
+                       inf.idx > 0 || part > 0 || k > 0);
+          }
+          issued = true;
+          mma_commit(&bars[kXwEmpty]);
+          mma_commit(&bars[kEmpty0 + st]);
+          if (inf.idx == inf.cnt - 1) {
+            mma_commit(&bars[kAggFull]);
+            ++au;
+          }
+          ++xu;
+          ++it;
+          continue;
         }
-        if (!wait_bar(&bars[kHReady], it & 1)) { fail(SSD_ERR_TIMEOUT); break; }
+        // forward chunk
+        if (inf.idx == 0) {
+          if (bt >= 2) { MMA_WAIT(kCbEmpty0 + (bt & 1), ((bt >> 1) - 1) & 1); }
+          issue_cb(it, bt);
+          issued = true;
+        }
+        if (inf.idx + 1 < inf.cnt) {
+          // the next chunk's C B^T first, so the math warps can build its
+          // mask while the tensor core runs this chunk's products
+          MMA_WAIT(kFull0 + ((it + 1) & 1), ((it + 1) >> 1) & 1);
+          if (bt + 1 >= 2) { MMA_WAIT(kCbEmpty0 + ((bt + 1) & 1), (((bt + 1) >> 1) - 1) & 1); }
+          tc_fence_after();
+          issue_cb(it + 1, bt + 1);
+          issued = true;
+        }
+        if (bt >= 1) { MMA_WAIT(kAccEmpty, (bt - 1) & 1); }
+        const uint32_t aC0 = smem_u32(sm.C(st, 0)), aC1 = smem_u32(sm.C(st, 1));
+        const uint32_t aX = smem_u32(sm.X(st));
+        // Y_off = C H^T (hi, lo)
+        MMA_WAIT(kHFull, bt & 1);
         tc_fence_after();
-        // Y_off = C H^T: A K-major (C), B MN-major (H^T rows n)
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
           const uint32_t aH = smem_u32(sm.Ht(part));
@@ -344,20 +448,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                      sdesc_sw128(aH + k * 2048, kTile, 1024), idYO, part > 0 || k > 0);
           }
         }
-        if (!wait_bar(&bars[kSReady], it & 1)) { fail(SSD_ERR_TIMEOUT); break; }
+        mma_commit(&bars[kHEmpty]);
+        // chunk state S_c^T = B^T (w o X) (hi, lo)
+        MMA_WAIT(kXwFull, xu & 1);
         tc_fence_after();
-        // Y_diag = S X, S (bf16 pairs) read from TMEM
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t aXw = smem_u32(sm.Xw(part));
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_bf16(tmem + kColST, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
+                     sdesc_sw128(aXw + k * 2048, kTile, 1024), idST, part > 0 || k > 0);
+        }
+        mma_commit(&bars[kXwEmpty]);
+        ++xu;
+        // Y_diag = S X, S (hi, lo) read from TMEM
+        MMA_WAIT(kSFull, bt & 1);
+        tc_fence_after();
+        const uint32_t cbcol = tmem + kColCB + (bt & 1) * 128;
+        // K block k (columns j = 16k .. 16k+15 of S) sits in the 32-column
+        // block k/2: hi pairs at +8 (k%2), lo pairs at +16 + 8 (k%2)
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_bf16_tmem_a(tmem + kColYD, cbcol + part * 64 + k * 8,
+            mma_bf16_tmem_a(tmem + kColYD, cbcol + 32 * (k >> 1) + 16 * part + 8 * (k & 1),
                             sdesc_sw128(aX + k * 2048, kTile, 1024), idYD, part > 0 || k > 0);
         mma_commit(&bars[kAccFull]);
+        mma_commit(&bars[kCbEmpty0 + (bt & 1)]);
         mma_commit(&bars[kEmpty0 + st]);
-        mma_commit(&bars[kCbsEmpty0 + st]);
+        ++bt;
         ++it;
       }
+#undef MMA_WAIT
       if (issued) {
         // every MMA issued must complete before TMEM is released
         mma_commit(&bars[kMmaDone]);
@@ -370,37 +493,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hp = tid >> 7;       // column half
     const int wq = warp & 3;       // lane quarter of this warp
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+    float* c2 = sm.c2();
+    float* dtt = sm.dtt();
+    float* part = sm.part();
+    // use counters: ring chunk, forward chunk, w o X buffer, segment-state
+    // accumulator, and one per math-warp rendezvous barrier
+    uint32_t it = 0, bt = 0, xu = 0, au = 0, ncum = 0, nhand = 0;
     float hreg[32];                // H[p][n = r] for p = 32 hp + q
-#pragma unroll
-    for (int q = 0; q < 32; ++q) hreg[q] = 0.f;
-    uint32_t it = 0;
-    while (true) {
-      const int st = it & 1;
-      if (!wait_bar(&bars[kFull0 + st], (it >> 1) & 1)) { fail(SSD_ERR_TIMEOUT); break; }
-      const TileInfo inf = *sm.info(st);
-      if (inf.len == 0 || *(volatile int*)&abort_sh) break;
-      const int h = inf.h;
-      const float A2 = prm.A[h] * kLog2e;
-      const float Dh = prm.D ? prm.D[h] : 0.f;
-      // -- unit start: load the initial state
-      if (inf.first) {
-        const float* ini = prm.init ? prm.init + ((long long)inf.s * prm.H + h) * (kP * kN)
-                                    : nullptr;
-#pragma unroll
-        for (int q = 0; q < 32; ++q)
-          hreg[q] = ini ? __ldg(ini + (32 * hp + q) * kN + r) : 0.f;
-        store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hreg);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kHReady]);
-      }
-      // -- cumulative decay (log2 domain) over the chunk
-      float* c2 = sm.c2();
-      float* dtt = sm.dtt();
-      float* part = sm.part();
+    uint32_t xpk[16];              // this chunk's x row half, bf16 pairs
+
+    // cumulative log2-decay of a chunk: tables c2[j] = sum_{k<=j} dt_k A log2(e)
+    // and dtt[j] = dt_j (0 beyond the valid rows).
+    auto chunk_cum = [&](const TileInfo& inf, float A2, float& c2_last, float& c2_r,
+                         float& dt_r) -> bool {
       float d = 0.f, v = 0.f;
       if (hp == 0) {
-        if (r < inf.len) d = __bfloat162float(prm.dt[(inf.t0 + r) * prm.H + h]);
+        if (r < inf.len) d = __bfloat162float(prm.dt[(inf.t0 + r) * prm.H + inf.h]);
         v = d * A2;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -409,150 +517,337 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 31) part[wq] = v;
       }
-      if (!math_sync(&bars[kSync0], it & 1)) { fail(SSD_ERR_TIMEOUT); break; }
+      if (!math_sync(&bars[kSyncCum0], ncum & 1)) return false;
       if (hp == 0) {
         float off = 0.f;
         for (int w = 0; w < wq; ++w) off += part[w];
         c2[r] = v + off;
         dtt[r] = d;
       }
-      if (!math_sync(&bars[kSync1], it & 1)) { fail(SSD_ERR_TIMEOUT); break; }
-      const float c2_last = c2[kQ - 1];
-      const float c2_r = c2[r];
-      const float dt_r = dtt[r];
-      // -- X' = w o X (row j = r, p chunks 4hp .. 4hp+3)
-      {
-        const float w = exp2f(c2_last - c2_r) * dt_r;
-        const uint8_t* Xs = sm.X(st);
-        float xw[32];
+      if (!math_sync(&bars[kSyncCum1], ncum & 1)) return false;
+      ++ncum;
+      c2_last = c2[kQ - 1];
+      c2_r = c2[r];
+      dt_r = dtt[r];
+      return true;
+    };
+
+    // The decay mask S of forward chunk number `pbt` (its tables must be
+    // current), written as bf16 hi/lo pairs over its C B^T in TMEM.  Each
+    // 32-column block j in [32 hb, 32 hb + 32) of a row is rewritten in place
+    // as 16 columns of hi pairs followed by 16 columns of lo pairs, so a
+    // thread only ever overwrites TMEM it has just read itself.
+    auto build_mask = [&](uint32_t pbt, float c2r) -> bool {
+      if (!wait_bar(&bars[kCbFull0 + (pbt & 1)], (pbt >> 1) & 1)) return false;
+      tc_fence_after();
+      const uint32_t cbcol = tmem + kColCB + (pbt & 1) * 128 + lane_addr;
+      const int b = 32 * wq;             // first row of this warp's lanes
+      const float c2b = c2[b];
+      const float u = exp2f(c2r - c2b);  // <= 1 for A <= 0
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const int j0 = 64 * hp + 32 * half;
+        uint32_t pkh[16], pkl[16];
+        if (j0 > b + 31) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(Xs + sw128_offset(r, 4 * hp + c));
-          xw[8 * c + 0] = w * bf_lo(xv.x);
-          xw[8 * c + 1] = w * bf_hi(xv.x);
-          xw[8 * c + 2] = w * bf_lo(xv.y);
-          xw[8 * c + 3] = w * bf_hi(xv.y);
-          xw[8 * c + 4] = w * bf_lo(xv.z);
-          xw[8 * c + 5] = w * bf_hi(xv.z);
-          xw[8 * c + 6] = w * bf_lo(xv.w);
-          xw[8 * c + 7] = w * bf_hi(xv.w);
-        }
-        store_split_row(sm.Xw(0), sm.Xw(1), r, hp, xw);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kXsReady]);
-      }
-      // -- S = (C B^T) o exp(cum_i - cum_j) dt_j, causal, written over C B^T
-      {
-        if (!wait_bar(&bars[kCbFull0 + st], (it >> 1) & 1)) { fail(SSD_ERR_TIMEOUT); break; }
-        tc_fence_after();
-        const uint32_t cbcol = tmem + kColCB + st * 128 + lane_addr;
-        const int i = r;
-        const int jbase = 64 * hp;
-        uint32_t pkh[32], pkl[32];   // S hi / lo, bf16 pairs, columns jbase .. jbase+63
-        // this warp's rows are 32 wq .. 32 wq + 31; columns beyond them are 0
-        const bool any = jbase <= 32 * wq + 31;
-        if (any) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float g[32];
-            tmem_ld32(cbcol + jbase + 32 * half, g);
-            tmem_ld_wait();
+          for (int q = 0; q < 16; ++q) pkh[q] = pkl[q] = 0u;
+        } else {
+          float g[32];
+          tmem_ld32(cbcol + j0, g);
+          tmem_ld_wait();
+          if (j0 + 32 <= b) {
+            // strictly below this warp's rows: exp(cum_i - cum_j) =
+            // exp(cum_i - cum_b) exp(cum_b - cum_j), both factors <= 1
+            const float vl = exp2f(c2b - c2[j0 + lane]) * dtt[j0 + lane];
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-              const int j0 = jbase + 32 * half + 2 * q, j1 = j0 + 1;
-              const float s0 = j0 <= i ? g[2 * q] * exp2f(c2_r - c2[j0]) * dtt[j0] : 0.f;
-              const float s1 = j1 <= i ? g[2 * q + 1] * exp2f(c2_r - c2[j1]) * dtt[j1] : 0.f;
-              split2(s0, s1, pkh[16 * half + q], pkl[16 * half + q]);
+              const float v0 = __shfl_sync(0xffffffffu, vl, 2 * q);
+              const float v1 = __shfl_sync(0xffffffffu, vl, 2 * q + 1);
+              split2(g[2 * q] * (u * v0), g[2 * q + 1] * (u * v1), pkh[q], pkl[q]);
+            }
+          } else {
+            // the diagonal block: direct, causal
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const int ja = j0 + 2 * q, jb = ja + 1;
+              const float sa = ja <= r ? g[2 * q] * exp2f(c2r - c2[ja]) * dtt[ja] : 0.f;
+              const float sb = jb <= r ? g[2 * q + 1] * exp2f(c2r - c2[jb]) * dtt[jb] : 0.f;
+              split2(sa, sb, pkh[q], pkl[q]);
             }
           }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) pkh[q] = pkl[q] = 0u;
         }
-        // every C B^T read of this chunk is done before any S write lands
-        tc_fence_before();
-        if (!math_sync(&bars[kSync2], it & 1)) { fail(SSD_ERR_TIMEOUT); break; }
-        tc_fence_after();
-        const uint32_t scol = tmem + kColCB + st * 128 + lane_addr + 32 * hp;
-        uint32_t tmp[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) tmp[q] = pkh[q];
-        tmem_st16(scol, tmp);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) tmp[q] = pkh[16 + q];
-        tmem_st16(scol + 16, tmp);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) tmp[q] = pkl[q];
-        tmem_st16(scol + 64, tmp);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) tmp[q] = pkl[16 + q];
-        tmem_st16(scol + 64 + 16, tmp);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kSReady]);
+        tmem_st16(cbcol + j0, pkh);
+        tmem_st16(cbcol + j0 + 16, pkl);
       }
-      // -- epilogue and state update
-      {
-        if (!wait_bar(&bars[kAccFull], it & 1)) { fail(SSD_ERR_TIMEOUT); break; }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kSFull]);
+      return true;
+    };
+
+    // w o X (w = weight of row r) of the chunk in stage `stg` into the Xw
+    // buffer, keeping x in `xpk` when asked; releases the stage (math side).
+    auto make_xw = [&](int stg, float w, bool keep_x) -> bool {
+      if (xu >= 1 && !wait_bar(&bars[kXwEmpty], (xu - 1) & 1)) return false;
+      const uint8_t* Xs = sm.X(stg);
+      float xw[32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(Xs + sw128_offset(r, 4 * hp + c));
+        if (keep_x) {
+          xpk[4 * c + 0] = xv.x;
+          xpk[4 * c + 1] = xv.y;
+          xpk[4 * c + 2] = xv.z;
+          xpk[4 * c + 3] = xv.w;
+        }
+        xw[8 * c + 0] = w * bf_lo(xv.x);
+        xw[8 * c + 1] = w * bf_hi(xv.x);
+        xw[8 * c + 2] = w * bf_lo(xv.y);
+        xw[8 * c + 3] = w * bf_hi(xv.y);
+        xw[8 * c + 4] = w * bf_lo(xv.z);
+        xw[8 * c + 5] = w * bf_hi(xv.z);
+        xw[8 * c + 6] = w * bf_lo(xv.w);
+        xw[8 * c + 7] = w * bf_hi(xv.w);
+      }
+      store_split_row(sm.Xw(0), sm.Xw(1), r, hp, xw);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[kXwFull]);
+        mbar_arrive(&bars[kEmpty0 + stg]);
+      }
+      ++xu;
+      return true;
+    };
+
+#define MATH_TRY(expr)     \
+  if (!(expr)) {           \
+    fail(SSD_ERR_TIMEOUT); \
+    goto math_done;        \
+  }
+    while (true) {
+      MATH_TRY(wait_bar(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
+      const TileInfo u0 = *sm.info(it & 1);
+      if (u0.kind == kKindEnd || *abort_v) break;
+      const int h = u0.h;
+      const float A2 = prm.A[h] * kLog2e;
+      const float Dh = prm.D ? prm.D[h] : 0.f;
+      const int nA = u0.nA;
+
+      // -------- pass A: segment-local state, chunks walked backwards
+      float later = 0.f;  // sum of the log2-decays of the chunks after this one
+      for (int k = 0; k < nA; ++k) {
+        if (k > 0) MATH_TRY(wait_bar(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
+        const TileInfo inf = *sm.info(it & 1);
+        float c2l, c2r, dtr;
+        MATH_TRY(chunk_cum(inf, A2, c2l, c2r, dtr));
+        const float w = exp2f(c2l - c2r + later) * dtr;
+        later += c2l;
+        MATH_TRY(make_xw(it & 1, w, false));
+        ++it;
+      }
+
+      // -------- segment hand-off
+      float hloc[32];
+      if (nA > 0) {
+        MATH_TRY(wait_bar(&bars[kAggFull], au & 1));
         tc_fence_after();
-        float yd[32], yo[32], sv[32];
-        tmem_ld32(tmem + kColYD + lane_addr + 32 * hp, yd);
-        tmem_ld32(tmem + kColYO + lane_addr + 32 * hp, yo);
-        tmem_ld32(tmem + kColST + lane_addr + 32 * hp, sv);
+        tmem_ld32(tmem + kColSA + lane_addr + 32 * hp, hloc);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kAccEmpty]);
-        // y row i = r
-        if (r < inf.len) {
-          const float ei = exp2f(c2_r);
-          const uint8_t* Xs = sm.X(st);
-          float* yrow = prm.y + ((inf.t0 + r) * prm.H + h) * kP + 32 * hp;
+        if (lane == 0) mbar_arrive(&bars[kAggEmpty]);
+        ++au;
+      }
+      if (u0.sigma == 0) {
+        const float* ini = prm.init ? prm.init + ((long long)u0.s * prm.H + h) * kPN : nullptr;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(Xs + sw128_offset(r, 4 * hp + c));
-            const float xs[8] = {bf_lo(xv.x), bf_hi(xv.x), bf_lo(xv.y), bf_hi(xv.y),
-                                 bf_lo(xv.z), bf_hi(xv.z), bf_lo(xv.w), bf_hi(xv.w)};
-            float4 o0, o1;
-            o0.x = yd[8 * c + 0] + ei * yo[8 * c + 0] + Dh * xs[0];
-            o0.y = yd[8 * c + 1] + ei * yo[8 * c + 1] + Dh * xs[1];
-            o0.z = yd[8 * c + 2] + ei * yo[8 * c + 2] + Dh * xs[2];
-            o0.w = yd[8 * c + 3] + ei * yo[8 * c + 3] + Dh * xs[3];
-            o1.x = yd[8 * c + 4] + ei * yo[8 * c + 4] + Dh * xs[4];
-            o1.y = yd[8 * c + 5] + ei * yo[8 * c + 5] + Dh * xs[5];
-            o1.z = yd[8 * c + 6] + ei * yo[8 * c + 6] + Dh * xs[6];
-            o1.w = yd[8 * c + 7] + ei * yo[8 * c + 7] + Dh * xs[7];
-            __stcs(reinterpret_cast<float4*>(yrow + 8 * c), o0);
-            __stcs(reinterpret_cast<float4*>(yrow + 8 * c + 4), o1);
+        for (int q = 0; q < 32; ++q) hreg[q] = ini ? __ldg(ini + (32 * hp + q) * kN + r) : 0.f;
+      } else {
+        const int pred = u0.unit - prm.H;  // same sequence and head, previous segment
+        if (tid == 0) {
+          const unsigned long long t0 = gtime();
+          while (ld_acquire(prm.flags + pred) == 0) {
+            if (gtime() - t0 > kWaitNs) {
+              fail(SSD_ERR_TIMEOUT);
+              break;
+            }
           }
         }
-        // state: H_c[p][n=r] = exp(cum_last) H_{c-1} + S_c
-        const float a = exp2f(c2_last);
+        MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1));
+        ++nhand;
+        if (*abort_v) goto math_done;
+        const float* src = prm.slots + (long long)pred * kPN;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) hreg[q] = a * hreg[q] + sv[q];
-        if (!inf.last) {
-          store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hreg);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kHReady]);
-        } else if (prm.final_states) {
-          float* fin = prm.final_states + ((long long)inf.s * prm.H + h) * (kP * kN);
-#pragma unroll
-          for (int q = 0; q < 32; ++q) fin[(32 * hp + q) * kN + r] = hreg[q];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kEmpty0 + st]);
+        for (int q = 0; q < 32; ++q) hreg[q] = __ldcg(src + (32 * hp + q) * kN + r);
       }
-      ++it;
+      if (nA > 0) {
+        // publish this segment's end state exp(sum dt A) H_in + H_loc
+        const float aseg = exp2f(later);
+        float* dst = prm.slots + (long long)u0.unit * kPN;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) __stcg(dst + (32 * hp + q) * kN + r, aseg * hreg[q] + hloc[q]);
+        __threadfence();
+        MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1));
+        ++nhand;
+        if (tid == 0) st_release(prm.flags + u0.unit, 1);
+      }
+
+      // -------- pass B: the forward over the segment's chunks from H_in
+      if (bt >= 1) MATH_TRY(wait_bar(&bars[kHEmpty], (bt - 1) & 1));
+      store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hreg);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kHFull]);
+      {
+        MATH_TRY(wait_bar(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
+        TileInfo cur = *sm.info(it & 1);
+        float c2l_cur, c2r_cur, dtr_cur;
+        MATH_TRY(chunk_cum(cur, A2, c2l_cur, c2r_cur, dtr_cur));
+        MATH_TRY(build_mask(bt, c2r_cur));
+        MATH_TRY(make_xw(it & 1, exp2f(c2l_cur - c2r_cur) * dtr_cur, true));
+        const int nB = cur.cnt;
+        for (int t = 0; t < nB; ++t) {
+          const bool more = t + 1 < nB;
+          TileInfo nxt = cur;
+          float c2l_nxt = 0.f, c2r_nxt = 0.f, dtr_nxt = 0.f;
+          if (more) {
+            // the next chunk's decay mask, while the tensor core works on this one
+            MATH_TRY(wait_bar(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1));
+            nxt = *sm.info((it + 1) & 1);
+            MATH_TRY(chunk_cum(nxt, A2, c2l_nxt, c2r_nxt, dtr_nxt));
+            MATH_TRY(build_mask(bt + 1, c2r_nxt));
+          }
+          // this chunk's epilogue and state update
+          MATH_TRY(wait_bar(&bars[kAccFull], bt & 1));
+          tc_fence_after();
+          {
+            float yd[32], yo[32];
+            tmem_ld32(tmem + kColYD + lane_addr + 32 * hp, yd);
+            tmem_ld32(tmem + kColYO + lane_addr + 32 * hp, yo);
+            tmem_ld_wait();
+            if (r < cur.len) {
+              const float ei = exp2f(c2r_cur);
+              float* yrow = prm.y + ((cur.t0 + r) * prm.H + h) * kP + 32 * hp;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                float4 o;
+                o.x = yd[4 * c + 0] + ei * yo[4 * c + 0] + Dh * bf_lo(xpk[2 * c]);
+                o.y = yd[4 * c + 1] + ei * yo[4 * c + 1] + Dh * bf_hi(xpk[2 * c]);
+                o.z = yd[4 * c + 2] + ei * yo[4 * c + 2] + Dh * bf_lo(xpk[2 * c + 1]);
+                o.w = yd[4 * c + 3] + ei * yo[4 * c + 3] + Dh * bf_hi(xpk[2 * c + 1]);
+                __stcs(reinterpret_cast<float4*>(yrow + 4 * c), o);
+              }
+            }
+          }
+          {
+            float sv[32];
+            tmem_ld32(tmem + kColST + lane_addr + 32 * hp, sv);
+            tmem_ld_wait();
+            const float a = exp2f(c2l_cur);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) hreg[q] = a * hreg[q] + sv[q];
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kAccEmpty]);
+          if (more) {
+            MATH_TRY(wait_bar(&bars[kHEmpty], bt & 1));
+            store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hreg);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kHFull]);
+          } else if (cur.last_seg && prm.final_states) {
+            float* fin = prm.final_states + ((long long)cur.s * prm.H + h) * kPN;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) fin[(32 * hp + q) * kN + r] = hreg[q];
+          }
+          ++bt;
+          ++it;
+          if (more) {
+            cur = nxt;
+            c2l_cur = c2l_nxt;
+            c2r_cur = c2r_nxt;
+            dtr_cur = dtr_nxt;
+            MATH_TRY(make_xw(it & 1, exp2f(c2l_cur - c2r_cur) * dtr_cur, true));
+          }
+        }
+      }
     }
+  math_done:;
+#undef MATH_TRY
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == kProducerWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Plan: per sequence the number of work units (segments x heads) as offsets
+// uoff[0..nseq], and uoff[nseq+1] = 0 if cu_seqlens is well formed; zeroes
+// the work ticket and the hand-off flags; final = init (or 0) for sequences
+// without tokens.  One block of 1024 threads.
+__global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* cu, int seqlen_rows,
+                                                       int seqlen_total, int nseq, int seg,
+                                                       int H, int32_t* uoff, int* ticket,
+                                                       int* flags, long long max_units,
+                                                       const float* init, float* final_states,
+                                                       int32_t* dev_status) {
+  __shared__ int buf[32];
+  __shared__ int carry, bad;
+  if (threadIdx.x == 0) {
+    carry = 0;
+    bad = 0;
+    *ticket = 0;
+    if (cu && (cu[0] != 0 || cu[nseq] != seqlen_total)) bad = 1;
+  }
+  for (long long k = threadIdx.x; k < max_units; k += 1024) flags[k] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int base = 0; base < nseq; base += 1024) {
+    const int s = base + threadIdx.x;
+    int n = 0;
+    if (s < nseq) {
+      const long long b = cu ? (long long)cu[s] : (long long)s * seqlen_rows;
+      const long long e = cu ? (long long)cu[s + 1] : (long long)(s + 1) * seqlen_rows;
+      if (e < b || b < 0 || e > seqlen_total) atomicOr(&bad, 1);
+      const long long nt = e > b ? (e - b + kQ - 1) / kQ : 0;
+      n = (int)((nt + seg - 1) / seg) * H;
+    }
+    int v = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += t;
+    }
+    if (lane == 31) buf[wid] = v;
+    __syncthreads();
+    int off = 0;
+    for (int w = 0; w < wid; ++w) off += buf[w];
+    if (s < nseq) uoff[s + 1] = carry + v + off;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry += v + off;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) uoff[0] = 0;
+  __syncthreads();
+  if (bad) {
+    for (int s = threadIdx.x; s <= nseq; s += 1024) uoff[s] = 0;
+    if (threadIdx.x == 0) report(dev_status, SSD_ERR_INVALID);
+  }
+  if (threadIdx.x == 0) uoff[nseq + 1] = bad;
+  __syncthreads();
+  if (final_states && !bad) {
+    const long long per = (long long)H * kPN;
+    for (int s = 0; s < nseq; ++s) {
+      if (uoff[s + 1] != uoff[s]) continue;  // the sequence has tokens
+      float* dst = final_states + (long long)s * per;
+      const float* src = init ? init + (long long)s * per : nullptr;
+      for (long long e = threadIdx.x; e < per; e += 1024) dst[e] = src ? src[e] : 0.f;
+    }
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -600,23 +895,51 @@ int sm_count() {
   return n > 0 ? n : 148;
 }
 
+// Upper bound on the number of work units.
+long long max_units(const FwdArgs& a) {
+  const long long per = ((long long)a.seqlen + kQ - 1) / kQ;
+  if (a.cu) return (((per + a.nseq) + kSeg - 1) / kSeg + a.nseq) * a.H;
+  return (long long)a.batch * ((per + kSeg - 1) / kSeg) * a.H;
+}
+
+struct WsLayout {
+  size_t uoff, ticket, flags, slots, total;
+};
+
+WsLayout ws_layout(const FwdArgs& a) {
+  WsLayout L;
+  const long long mu = max_units(a);
+  L.uoff = 0;
+  L.ticket = L.uoff + plan_bytes(a.nseq);
+  L.flags = L.ticket + 256;
+  L.slots = L.flags + align256(sizeof(int) * (size_t)mu);
+  L.total = L.slots + align256(sizeof(float) * (size_t)mu * kPN);
+  return L;
+}
+
 }  // namespace
 
 bool tc_supported(const FwdArgs& a) {
   return a.dtype == SSD_DT_BF16 && a.P == kP && a.N == kN;
 }
 
-size_t tc_workspace_bytes(const FwdArgs& a) { return plan_bytes(a.nseq) + 256; }
+size_t tc_workspace_bytes(const FwdArgs& a) { return ws_layout(a).total; }
 
 ssd_status_t tc_forward(const FwdArgs& a) {
+  const WsLayout L = ws_layout(a);
   char* ws = static_cast<char*>(a.ws);
-  int32_t* offs = reinterpret_cast<int32_t*>(ws);
-  int* ticket = reinterpret_cast<int*>(ws + plan_bytes(a.nseq));
+  int32_t* uoff = reinterpret_cast<int32_t*>(ws + L.uoff);
+  int* ticket = reinterpret_cast<int*>(ws + L.ticket);
+  int* flags = reinterpret_cast<int*>(ws + L.flags);
+  float* slots = reinterpret_cast<float*>(ws + L.slots);
   const long long ntok = (long long)a.batch * a.seqlen;
-  cudaError_t err = launch_plan(a.cu, a.seqlen, (int)ntok, a.nseq, kQ, offs, a.dev_status,
-                                a.stream, ticket, a.init, a.final_states, a.H, kP * kN);
-  if (err != cudaSuccess) return SSD_ERR_CUDA;
-  if (ntok == 0) return SSD_OK;
+  const long long mu = max_units(a);
+  tc_plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu, a.seqlen, (int)ntok, a.nseq, kSeg, a.H, uoff,
+                                           ticket, flags, mu, a.init, a.final_states,
+                                           a.dev_status);
+  count_launches(1);
+  if (cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
+  if (ntok == 0 || mu == 0) return SSD_OK;
   CUtensorMap mx, mb, mc;
   if (!make_map(&mx, a.x, ntok, (long long)a.H * kP) ||
       !make_map(&mb, a.B, ntok, (long long)a.G * kN) ||
@@ -630,12 +953,14 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   p.y = a.y;
   p.final_states = a.final_states;
   p.si = SeqInfo{a.cu, a.seqlen, a.nseq};
-  p.offs = offs;
+  p.uoff = uoff;
   p.ticket = ticket;
+  p.flags = flags;
+  p.slots = slots;
   p.status = a.dev_status;
   p.H = a.H;
   p.G = a.G;
-  p.nunits = a.nseq * a.H;
+  p.seg = kSeg;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -643,8 +968,7 @@ ssd_status_t tc_forward(const FwdArgs& a) {
                                     (int)kSmemBytes);
   });
   if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
-  const int grid = p.nunits < sm_count() ? p.nunits : sm_count();
-  if (grid <= 0) return SSD_OK;
+  const int grid = (int)(mu < sm_count() ? mu : sm_count());
   ssd_tc_fwd_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(mx, mb, mc, p);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
