@@ -83,8 +83,9 @@ constexpr uint32_t kStageBytes = 5 * kTile;         // C0 C1 B0 B1 X
 constexpr uint32_t kStageBytesA = 3 * kTile;        // B0 B1 X (segment-state pass)
 constexpr uint32_t kOffXw = kStages * kStageBytes;  // w o X as bf16 hi, lo (2 x 16 KB)
 constexpr uint32_t kOffHt = kOffXw + 2 * kTile;     // H^T as bf16 hi, lo (2 x 16 KB)
-constexpr uint32_t kOffTabs = kOffHt + 2 * kTile;   // c2[128] dt[128] part[8]
-constexpr uint32_t kOffInfo = kOffTabs + 4 * 272;
+constexpr uint32_t kOffTabs = kOffHt + 2 * kTile;   // per stage: c2 fp32[128], dt bf16[128]
+constexpr uint32_t kTabBytes = 128 * 4 + 128 * 2;
+constexpr uint32_t kOffInfo = kOffTabs + kStages * kTabBytes;
 constexpr uint32_t kSmemUse = kOffInfo + 2 * 64;
 constexpr uint32_t kSmemBytes = kSmemUse + 1024;    // slack for 1024-B alignment
 
@@ -126,7 +127,7 @@ struct Params {
   float* final_states;
   SeqInfo si;
   const int32_t* uoff;  // [nseq + 2]: unit offsets per sequence, then plan status
-  int* ticket;
+  int* ticket;          // ticket[0]: work ticket; ticket[1]: line of the first expired wait
   int* flags;           // per unit: 1 once its segment end state is published
   float* slots;         // per unit: segment end state [P][N] fp32
   int32_t* status;
@@ -151,13 +152,20 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Warp-collective form: every lane waits and the warp agrees on the result,
+// so a timeout never splits a warp (later warp-synchronous instructions
+// would otherwise strand the lanes that went on).
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity));
+}
+
 // All 8 math warps meet at `bar` (phase parity `par`); bounded.  The math
 // warps synchronise only through mbarriers so that a timed-out warp can
 // leave without stranding the others at a hardware barrier.
 __device__ __forceinline__ bool math_sync(uint64_t* bar, uint32_t par) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  return wait_bar(bar, par);
+  return wait_bar_warp(bar, par);
 }
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -209,9 +217,14 @@ struct Smem {
   __device__ uint8_t* X(int s) const { return stage(s) + 4 * kTile; }
   __device__ uint8_t* Xw(int part) const { return base + kOffXw + part * kTile; }
   __device__ uint8_t* Ht(int part) const { return base + kOffHt + part * kTile; }
-  __device__ float* c2() const { return reinterpret_cast<float*>(base + kOffTabs); }
-  __device__ float* dtt() const { return c2() + 128; }
-  __device__ float* part() const { return c2() + 256; }
+  // cumulative log2-decay of the chunk in stage s: c2[j] = sum_{k<=j} dt_k A log2(e)
+  __device__ float* c2(int s) const {
+    return reinterpret_cast<float*>(base + kOffTabs + s * kTabBytes);
+  }
+  // dt of the chunk in stage s (0 beyond the valid rows)
+  __device__ __nv_bfloat16* dt(int s) const {
+    return reinterpret_cast<__nv_bfloat16*>(base + kOffTabs + s * kTabBytes + 512);
+  }
   __device__ TileInfo* info(int s) const {
     return reinterpret_cast<TileInfo*>(base + kOffInfo) + s;
   }
@@ -221,12 +234,12 @@ struct Smem {
 enum {
   kFull0 = 0, kFull1, kEmpty0, kEmpty1,      // TMA stage ring
   kCbFull0, kCbFull1, kCbEmpty0, kCbEmpty1,  // C B^T / S buffers in TMEM
-  kSFull,                                    // S written (math -> MMA)
+  kSFull0, kSFull1,                          // S written (math -> MMA), per S buffer
   kXwFull, kXwEmpty,                         // w o X buffer
   kHFull, kHEmpty,                           // H^T buffer
   kAccFull, kAccEmpty,                       // Y_diag / Y_off / chunk-state accumulators
   kAggFull, kAggEmpty,                       // segment-local state accumulator
-  kSyncCum0, kSyncCum1, kSyncHand,           // math-warp rendezvous
+  kSyncHand,                                 // math-warp rendezvous
   kMmaDone,
   kNumBars
 };
@@ -246,15 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    mbar_init(&bars[kFull0], 1);
-    mbar_init(&bars[kFull1], 1);
+    mbar_init(&bars[kFull0], 2);  // expect-tx arrival + decay tables written
+    mbar_init(&bars[kFull1], 2);
     mbar_init(&bars[kEmpty0], 1 + kMathWarps);
     mbar_init(&bars[kEmpty1], 1 + kMathWarps);
     mbar_init(&bars[kCbFull0], 1);
     mbar_init(&bars[kCbFull1], 1);
     mbar_init(&bars[kCbEmpty0], 1);
     mbar_init(&bars[kCbEmpty1], 1);
-    mbar_init(&bars[kSFull], kMathWarps);
+    mbar_init(&bars[kSFull0], kMathWarps);
+    mbar_init(&bars[kSFull1], kMathWarps);
     mbar_init(&bars[kXwFull], kMathWarps);
     mbar_init(&bars[kXwEmpty], 1);
     mbar_init(&bars[kHFull], kMathWarps);
@@ -263,8 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kAccEmpty], kMathWarps);
     mbar_init(&bars[kAggFull], 1);
     mbar_init(&bars[kAggEmpty], kMathWarps);
-    mbar_init(&bars[kSyncCum0], kMathWarps);
-    mbar_init(&bars[kSyncCum1], kMathWarps);
     mbar_init(&bars[kSyncHand], kMathWarps);
     mbar_init(&bars[kMmaDone], 1);
     abort_sh = 0;
@@ -280,10 +292,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_sh;
   volatile int* abort_v = &abort_sh;
 
-  auto fail = [&](int code) {
+  auto fail_at = [&](int code, int line) {
     report(prm.status, code);
+    atomicCAS(prm.ticket + 1, 0, line);
     atomicExch(&abort_sh, 1);
   };
+#define fail(code) fail_at((code), __LINE__)
 
   const int nseq = prm.si.nseq;
   const int nunits = prm.uoff[nseq];
@@ -291,48 +305,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // Lane 0 draws work and issues the TMA loads; the whole warp then loads
+    // the chunk's dt and writes its cumulative log2-decay table.
     if (lane == 0) {
       prefetch_tmap(&map_x);
       prefetch_tmap(&map_b);
       prefetch_tmap(&map_c);
-      uint32_t it = 0;
-      bool ok = true;
-      while (ok && plan_ok) {
-        const int u = atomicAdd(prm.ticket, 1);
-        if (u >= nunits) break;
-        const int s = upper_index(prm.uoff, nseq, u);
-        const int rem = u - prm.uoff[s];
-        const int sigma = rem / prm.H, h = rem % prm.H;
-        const int g = (int)((long long)h * prm.G / prm.H);
-        const long long b = prm.si.begin(s), e = prm.si.end(s);
-        const int nt = (int)((e - b + kQ - 1) / kQ);
-        const int tb = sigma * prm.seg, te = min(nt, tb + prm.seg);
-        const int last_seg = te == nt;
-        const int nA = last_seg ? 0 : te - tb, nB = te - tb;
-        for (int k = 0; k < nA + nB; ++k, ++it) {
-          const int kind = k < nA ? kKindA : kKindB;
-          const int t = kind == kKindA ? te - 1 - k : tb + (k - nA);
-          const int st = it & 1;
-          if (it >= 2 && !wait_bar(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1)) {
-            fail(SSD_ERR_TIMEOUT);
-            ok = false;
-            break;
-          }
-          if (*abort_v) { ok = false; break; }
+    }
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && plan_ok) {
+      int u = 0;
+      if (lane == 0) u = atomicAdd(prm.ticket, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u >= nunits) break;
+      const int s = upper_index(prm.uoff, nseq, u);
+      const int rem = u - prm.uoff[s];
+      const int sigma = rem / prm.H, h = rem % prm.H;
+      const int g = (int)((long long)h * prm.G / prm.H);
+      const float A2 = prm.A[h] * kLog2e;
+      const long long b = prm.si.begin(s), e = prm.si.end(s);
+      const int nt = (int)((e - b + kQ - 1) / kQ);
+      const int tb = sigma * prm.seg, te = min(nt, tb + prm.seg);
+      const int last_seg = te == nt;
+      const int nA = last_seg ? 0 : te - tb, nB = te - tb;
+      for (int k = 0; k < nA + nB; ++k, ++it) {
+        const int kind = k < nA ? kKindA : kKindB;
+        const int t = kind == kKindA ? te - 1 - k : tb + (k - nA);
+        const int st = it & 1;
+        if (it >= 2 && !wait_bar_warp(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1)) {
+          if (lane == 0) fail(SSD_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        if (__any_sync(0xffffffffu, *abort_v)) { ok = false; break; }
+        const long long t0 = b + (long long)t * kQ;
+        const int len = (int)min((long long)kQ, e - t0);
+        uint64_t* fb = &bars[kFull0 + st];
+        if (lane == 0) {
           TileInfo* inf = sm.info(st);
-          inf->t0 = b + (long long)t * kQ;
+          inf->t0 = t0;
           inf->s = s;
           inf->h = h;
           inf->sigma = sigma;
           inf->unit = u;
-          inf->len = (int)min((long long)kQ, e - inf->t0);
+          inf->len = len;
           inf->kind = kind;
           inf->idx = kind == kKindA ? k : k - nA;
           inf->cnt = kind == kKindA ? nA : nB;
           inf->nA = nA;
           inf->last_seg = last_seg;
-          const int row = (int)inf->t0;
-          uint64_t* fb = &bars[kFull0 + st];
+          const int row = (int)t0;
           if (kind == kKindB) {
             mbar_arrive_expect_tx(fb, kStageBytes);
             tma_load_2d(sm.C(st, 0), &map_c, fb, g * kN, row);
@@ -344,18 +367,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sm.B(st, 1), &map_b, fb, g * kN + 64, row);
           tma_load_2d(sm.X(st), &map_x, fb, h * kP, row);
         }
+        // decay table: lane l owns tokens 4l .. 4l+3
+        __nv_bfloat16 dv[4];
+        float pre[4], run = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = 4 * lane + q;
+          dv[q] = j < len ? prm.dt[(t0 + j) * prm.H + h] : __float2bfloat16(0.f);
+          run += __bfloat162float(dv[q]) * A2;
+          pre[q] = run;
+        }
+        float incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float tv = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += tv;
+        }
+        const float excl = incl - run;
+        float* c2t = sm.c2(st);
+        __nv_bfloat16* dtt = sm.dt(st);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          c2t[4 * lane + q] = excl + pre[q];
+          dtt[4 * lane + q] = dv[q];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fb);
       }
-      // sentinel: no more work
-      const int st = it & 1;
-      if (ok && (it < 2 || wait_bar(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1))) {
+    }
+    // sentinel: no more work
+    const int st = it & 1;
+    if (ok && (it < 2 || wait_bar_warp(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1))) {
+      if (lane == 0) {
         sm.info(st)->kind = kKindEnd;
         mbar_arrive(&bars[kFull0 + st]);
-      } else {
-        if (ok) fail(SSD_ERR_TIMEOUT);
-        // aborting: loads still in flight must land before the CTA may exit
-        for (uint32_t k = (it >= 2 ? it - 2 : 0); k < it; ++k)
-          (void)wait_bar(&bars[kFull0 + (k & 1)], (k >> 1) & 1);
+        mbar_arrive(&bars[kFull0 + st]);
       }
+    } else if (lane == 0) {
+      if (ok) fail(SSD_ERR_TIMEOUT);
+      // aborting: loads still in flight must land before the CTA may exit
+      for (uint32_t k = (it >= 2 ? it - 2 : 0); k < it; ++k)
+        (void)wait_bar(&bars[kFull0 + (k & 1)], (k >> 1) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -463,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars[kXwEmpty]);
         ++xu;
         // Y_diag = S X, S (hi, lo) read from TMEM
-        MMA_WAIT(kSFull, bt & 1);
+        MMA_WAIT(kSFull0 + (bt & 1), (bt >> 1) & 1);
         tc_fence_after();
         const uint32_t cbcol = tmem + kColCB + (bt & 1) * 128;
         // K block k (columns j = 16k .. 16k+15 of S) sits in the 32-column
@@ -493,42 +545,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hp = tid >> 7;       // column half
     const int wq = warp & 3;       // lane quarter of this warp
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
-    float* c2 = sm.c2();
-    float* dtt = sm.dtt();
-    float* part = sm.part();
     // use counters: ring chunk, forward chunk, w o X buffer, segment-state
     // accumulator, and one per math-warp rendezvous barrier
-    uint32_t it = 0, bt = 0, xu = 0, au = 0, ncum = 0, nhand = 0;
+    uint32_t it = 0, bt = 0, xu = 0, au = 0, nhand = 0;
     float hreg[32];                // H[p][n = r] for p = 32 hp + q
     uint32_t xpk[16];              // this chunk's x row half, bf16 pairs
 
-    // cumulative log2-decay of a chunk: tables c2[j] = sum_{k<=j} dt_k A log2(e)
-    // and dtt[j] = dt_j (0 beyond the valid rows).
-    auto chunk_cum = [&](const TileInfo& inf, float A2, float& c2_last, float& c2_r,
-                         float& dt_r) -> bool {
-      float d = 0.f, v = 0.f;
-      if (hp == 0) {
-        if (r < inf.len) d = __bfloat162float(prm.dt[(inf.t0 + r) * prm.H + inf.h]);
-        v = d * A2;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float t = __shfl_up_sync(0xffffffffu, v, o);
-          if (lane >= o) v += t;
-        }
-        if (lane == 31) part[wq] = v;
-      }
-      if (!math_sync(&bars[kSyncCum0], ncum & 1)) return false;
-      if (hp == 0) {
-        float off = 0.f;
-        for (int w = 0; w < wq; ++w) off += part[w];
-        c2[r] = v + off;
-        dtt[r] = d;
-      }
-      if (!math_sync(&bars[kSyncCum1], ncum & 1)) return false;
-      ++ncum;
-      c2_last = c2[kQ - 1];
-      c2_r = c2[r];
-      dt_r = dtt[r];
+    // Arrival number `use` (0, 1, ...) of this warp on a barrier that all 8
+    // math warps arrive on.  Arrivals carry no phase, so a warp first waits
+    // for the barrier's previous phase to complete: without that, a warp
+    // running a chunk ahead could complete a phase in place of a slower one.
+    auto arrive_seq = [&](int bar, uint32_t use) -> bool {
+      if (use >= 1 && !wait_bar_warp(&bars[bar], (use - 1) & 1)) return false;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[bar]);
       return true;
     };
 
@@ -537,8 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 32-column block j in [32 hb, 32 hb + 32) of a row is rewritten in place
     // as 16 columns of hi pairs followed by 16 columns of lo pairs, so a
     // thread only ever overwrites TMEM it has just read itself.
-    auto build_mask = [&](uint32_t pbt, float c2r) -> bool {
-      if (!wait_bar(&bars[kCbFull0 + (pbt & 1)], (pbt >> 1) & 1)) return false;
+    auto build_mask = [&](uint32_t pbt, int stg, float c2r) -> bool {
+      const float* c2 = sm.c2(stg);
+      const __nv_bfloat16* dtt = sm.dt(stg);
+      if (!wait_bar_warp(&bars[kCbFull0 + (pbt & 1)], (pbt >> 1) & 1)) return false;
       tc_fence_after();
       const uint32_t cbcol = tmem + kColCB + (pbt & 1) * 128 + lane_addr;
       const int b = 32 * wq;             // first row of this warp's lanes
@@ -558,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j0 + 32 <= b) {
             // strictly below this warp's rows: exp(cum_i - cum_j) =
             // exp(cum_i - cum_b) exp(cum_b - cum_j), both factors <= 1
-            const float vl = exp2f(c2b - c2[j0 + lane]) * dtt[j0 + lane];
+            const float vl = exp2f(c2b - c2[j0 + lane]) * __bfloat162float(dtt[j0 + lane]);
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
               const float v0 = __shfl_sync(0xffffffffu, vl, 2 * q);
@@ -570,8 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
               const int ja = j0 + 2 * q, jb = ja + 1;
-              const float sa = ja <= r ? g[2 * q] * exp2f(c2r - c2[ja]) * dtt[ja] : 0.f;
-              const float sb = jb <= r ? g[2 * q + 1] * exp2f(c2r - c2[jb]) * dtt[jb] : 0.f;
+              const float sa =
+                  ja <= r ? g[2 * q] * exp2f(c2r - c2[ja]) * __bfloat162float(dtt[ja]) : 0.f;
+              const float sb =
+                  jb <= r ? g[2 * q + 1] * exp2f(c2r - c2[jb]) * __bfloat162float(dtt[jb]) : 0.f;
               split2(sa, sb, pkh[q], pkl[q]);
             }
           }
@@ -581,15 +615,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kSFull]);
-      return true;
+      // one "S ready" barrier per S buffer: the math warps can get a chunk
+      // ahead of the MMA (the next C B^T is issued before this S is used),
+      // never two
+      return arrive_seq(kSFull0 + (pbt & 1), pbt >> 1);
     };
 
     // w o X (w = weight of row r) of the chunk in stage `stg` into the Xw
     // buffer, keeping x in `xpk` when asked; releases the stage (math side).
-    auto make_xw = [&](int stg, float w, bool keep_x) -> bool {
-      if (xu >= 1 && !wait_bar(&bars[kXwEmpty], (xu - 1) & 1)) return false;
+    auto make_xw = [&](uint32_t pit, float w, bool keep_x) -> bool {
+      const int stg = pit & 1;
+      if (xu >= 1 && !wait_bar_warp(&bars[kXwEmpty], (xu - 1) & 1)) return false;
       const uint8_t* Xs = sm.X(stg);
       float xw[32];
 #pragma unroll
@@ -612,13 +648,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       store_split_row(sm.Xw(0), sm.Xw(1), r, hp, xw);
       fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[kXwFull]);
-        mbar_arrive(&bars[kEmpty0 + stg]);
-      }
+      if (!arrive_seq(kXwFull, xu)) return false;
+      if (!arrive_seq(kEmpty0 + stg, pit >> 1)) return false;
       ++xu;
       return true;
+    };
+
+    // this thread's decay values of the chunk in stage `stg`
+    auto chunk_vals = [&](int stg, float& c2l, float& c2r, float& dtr) {
+      const float* c2 = sm.c2(stg);
+      c2l = c2[kQ - 1];
+      c2r = c2[r];
+      dtr = __bfloat162float(sm.dt(stg)[r]);
     };
 
 #define MATH_TRY(expr)     \
@@ -627,37 +668,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     goto math_done;        \
   }
     while (true) {
-      MATH_TRY(wait_bar(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
+      MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
       const TileInfo u0 = *sm.info(it & 1);
-      if (u0.kind == kKindEnd || *abort_v) break;
+      if (u0.kind == kKindEnd || __any_sync(0xffffffffu, *abort_v)) break;
       const int h = u0.h;
-      const float A2 = prm.A[h] * kLog2e;
       const float Dh = prm.D ? prm.D[h] : 0.f;
       const int nA = u0.nA;
 
       // -------- pass A: segment-local state, chunks walked backwards
       float later = 0.f;  // sum of the log2-decays of the chunks after this one
       for (int k = 0; k < nA; ++k) {
-        if (k > 0) MATH_TRY(wait_bar(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
+        if (k > 0) MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
         const TileInfo inf = *sm.info(it & 1);
         float c2l, c2r, dtr;
-        MATH_TRY(chunk_cum(inf, A2, c2l, c2r, dtr));
+        chunk_vals(it & 1, c2l, c2r, dtr);
         const float w = exp2f(c2l - c2r + later) * dtr;
         later += c2l;
-        MATH_TRY(make_xw(it & 1, w, false));
+        MATH_TRY(make_xw(it, w, false));
         ++it;
       }
 
       // -------- segment hand-off
       float hloc[32];
       if (nA > 0) {
-        MATH_TRY(wait_bar(&bars[kAggFull], au & 1));
+        MATH_TRY(wait_bar_warp(&bars[kAggFull], au & 1));
         tc_fence_after();
         tmem_ld32(tmem + kColSA + lane_addr + 32 * hp, hloc);
         tmem_ld_wait();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kAggEmpty]);
+        MATH_TRY(arrive_seq(kAggEmpty, au));
         ++au;
       }
       if (u0.sigma == 0) {
@@ -677,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1));
         ++nhand;
-        if (*abort_v) goto math_done;
+        if (__any_sync(0xffffffffu, *abort_v)) goto math_done;
         const float* src = prm.slots + (long long)pred * kPN;
 #pragma unroll
         for (int q = 0; q < 32; ++q) hreg[q] = __ldcg(src + (32 * hp + q) * kN + r);
@@ -695,18 +734,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // -------- pass B: the forward over the segment's chunks from H_in
-      if (bt >= 1) MATH_TRY(wait_bar(&bars[kHEmpty], (bt - 1) & 1));
+      if (bt >= 1) MATH_TRY(wait_bar_warp(&bars[kHEmpty], (bt - 1) & 1));
       store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hreg);
       fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kHFull]);
+      MATH_TRY(arrive_seq(kHFull, bt));
       {
-        MATH_TRY(wait_bar(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
+        MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
         TileInfo cur = *sm.info(it & 1);
         float c2l_cur, c2r_cur, dtr_cur;
-        MATH_TRY(chunk_cum(cur, A2, c2l_cur, c2r_cur, dtr_cur));
-        MATH_TRY(build_mask(bt, c2r_cur));
-        MATH_TRY(make_xw(it & 1, exp2f(c2l_cur - c2r_cur) * dtr_cur, true));
+        chunk_vals(it & 1, c2l_cur, c2r_cur, dtr_cur);
+        MATH_TRY(build_mask(bt, it & 1, c2r_cur));
+        MATH_TRY(make_xw(it, exp2f(c2l_cur - c2r_cur) * dtr_cur, true));
         const int nB = cur.cnt;
         for (int t = 0; t < nB; ++t) {
           const bool more = t + 1 < nB;
@@ -714,13 +752,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           float c2l_nxt = 0.f, c2r_nxt = 0.f, dtr_nxt = 0.f;
           if (more) {
             // the next chunk's decay mask, while the tensor core works on this one
-            MATH_TRY(wait_bar(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1));
+            MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1));
             nxt = *sm.info((it + 1) & 1);
-            MATH_TRY(chunk_cum(nxt, A2, c2l_nxt, c2r_nxt, dtr_nxt));
-            MATH_TRY(build_mask(bt + 1, c2r_nxt));
+            chunk_vals((it + 1) & 1, c2l_nxt, c2r_nxt, dtr_nxt);
+            MATH_TRY(build_mask(bt + 1, (it + 1) & 1, c2r_nxt));
           }
           // this chunk's epilogue and state update
-          MATH_TRY(wait_bar(&bars[kAccFull], bt & 1));
+          MATH_TRY(wait_bar_warp(&bars[kAccFull], bt & 1));
           tc_fence_after();
           {
             float yd[32], yo[32];
@@ -750,14 +788,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 32; ++q) hreg[q] = a * hreg[q] + sv[q];
           }
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kAccEmpty]);
+          MATH_TRY(arrive_seq(kAccEmpty, bt));
           if (more) {
-            MATH_TRY(wait_bar(&bars[kHEmpty], bt & 1));
+            MATH_TRY(wait_bar_warp(&bars[kHEmpty], bt & 1));
             store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hreg);
             fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kHFull]);
+            MATH_TRY(arrive_seq(kHFull, bt + 1));
           } else if (cur.last_seg && prm.final_states) {
             float* fin = prm.final_states + ((long long)cur.s * prm.H + h) * kPN;
 #pragma unroll
@@ -770,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             c2l_cur = c2l_nxt;
             c2r_cur = c2r_nxt;
             dtr_cur = dtr_nxt;
-            MATH_TRY(make_xw(it & 1, exp2f(c2l_cur - c2r_cur) * dtr_cur, true));
+            MATH_TRY(make_xw(it, exp2f(c2l_cur - c2r_cur) * dtr_cur, true));
           }
         }
       }
@@ -779,6 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef MATH_TRY
   }
 
+#undef fail
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -800,7 +837,8 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* cu, int se
   if (threadIdx.x == 0) {
     carry = 0;
     bad = 0;
-    *ticket = 0;
+    ticket[0] = 0;
+    ticket[1] = 0;
     if (cu && (cu[0] != 0 || cu[nseq] != seqlen_total)) bad = 1;
   }
   for (long long k = threadIdx.x; k < max_units; k += 1024) flags[k] = 0;

@@ -32,12 +32,19 @@ def to_device(fi: I.ForwardInputs, device="cuda"):
     return d
 
 
-def run_gpu(fi: I.ForwardInputs, chunk=None, use_D=True, dev_status=None, device="cuda"):
+def run_gpu(fi: I.ForwardInputs, chunk=None, use_D=True, device="cuda"):
+    """Run the forward through the binding; the device status must stay 0
+    (a bounded wait that expired would report SSD_ERR_TIMEOUT there)."""
+    import torch
     from state_space_sequence_05_b300 import ssd
     d = to_device(fi, device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
     y, fin = ssd.ssd_chunk_scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"],
                                     d["D"] if use_D else None, chunk or fi.wl.chunk, d["init"],
-                                    d["cu"], dev_status=dev_status)
+                                    d["cu"], dev_status=status)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st == 0, f"device status {st} ({ssd.status_string(st)})"
     return y, fin
 
 
