@@ -94,7 +94,8 @@ constexpr uint32_t kColCB = 0;     // 2 x 128: C B^T, overwritten in place by S 
 constexpr uint32_t kColYD = 256;   // 64: S X
 constexpr uint32_t kColYO = 320;   // 64: C H^T
 constexpr uint32_t kColST = 384;   // 64: chunk state (lane n, column p)
-constexpr uint32_t kColSA = 448;   // 64: segment-local state (lane n, column p)
+constexpr uint32_t kColSA = 448;   // 64: segment-local state; during a forward pass the
+                                   // running fp32 state H (lane n, column p)
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -177,6 +178,14 @@ __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// 2^x on the special-function unit (ex2.approx.ftz: relative error ~2^-22,
+// flushes subnormal results to zero, which every use here tolerates).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
@@ -237,7 +246,8 @@ enum {
   kSFull0, kSFull1,                          // S written (math -> MMA), per S buffer
   kXwFull, kXwEmpty,                         // w o X buffer
   kHFull, kHEmpty,                           // H^T buffer
-  kAccFull, kAccEmpty,                       // Y_diag / Y_off / chunk-state accumulators
+  kAccFull,                                  // Y_diag, Y_off, chunk state ready
+  kStFree, kYoFree, kYdFree,                 // each accumulator read (math -> MMA)
   kAggFull, kAggEmpty,                       // segment-local state accumulator
   kSyncHand,                                 // math-warp rendezvous
   kMmaDone,
@@ -274,7 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kHFull], kMathWarps);
     mbar_init(&bars[kHEmpty], 1);
     mbar_init(&bars[kAccFull], 1);
-    mbar_init(&bars[kAccEmpty], kMathWarps);
+    mbar_init(&bars[kStFree], kMathWarps);
+    mbar_init(&bars[kYoFree], kMathWarps);
+    mbar_init(&bars[kYdFree], kMathWarps);
     mbar_init(&bars[kAggFull], 1);
     mbar_init(&bars[kAggEmpty], kMathWarps);
     mbar_init(&bars[kSyncHand], kMathWarps);
@@ -305,95 +317,155 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    // Lane 0 draws work and issues the TMA loads; the whole warp then loads
-    // the chunk's dt and writes its cumulative log2-decay table.
+    // Walks the ring one chunk at a time: a work unit (ticket), then its
+    // segment-state chunks (backwards), then its forward chunks.  Lane 0
+    // issues the TMA loads; the whole warp writes the chunk's decay tables.
+    // The dt values of the next chunk are loaded one chunk ahead so their
+    // latency overlaps the current chunk's hand-over.
     if (lane == 0) {
       prefetch_tmap(&map_x);
       prefetch_tmap(&map_b);
       prefetch_tmap(&map_c);
     }
+    struct PUnit {
+      long long b, e;
+      int u, s, h, sigma, g, nA, nB, last_seg, tb, te;
+      float A2;
+    };
+    auto draw = [&](PUnit& X) -> bool {
+      int v = 0;
+      if (lane == 0) v = atomicAdd(prm.ticket, 1);
+      v = __shfl_sync(0xffffffffu, v, 0);
+      if (v >= nunits) return false;
+      X.u = v;
+      X.s = upper_index(prm.uoff, nseq, v);
+      const int rem = v - prm.uoff[X.s];
+      X.sigma = rem / prm.H;
+      X.h = rem % prm.H;
+      X.g = (int)((long long)X.h * prm.G / prm.H);
+      X.A2 = prm.A[X.h] * kLog2e;
+      X.b = prm.si.begin(X.s);
+      X.e = prm.si.end(X.s);
+      const int nt = (int)((X.e - X.b + kQ - 1) / kQ);
+      X.tb = X.sigma * prm.seg;
+      X.te = min(nt, X.tb + prm.seg);
+      X.last_seg = X.te == nt;
+      X.nA = X.last_seg ? 0 : X.te - X.tb;
+      X.nB = X.te - X.tb;
+      return true;
+    };
+    // first token, kind and valid rows of chunk k of unit X
+    auto tile_of = [&](const PUnit& X, int k, long long& t0, int& kind, int& len) {
+      kind = k < X.nA ? kKindA : kKindB;
+      const int t = kind == kKindA ? X.te - 1 - k : X.tb + (k - X.nA);
+      t0 = X.b + (long long)t * kQ;
+      len = (int)min((long long)kQ, X.e - t0);
+    };
     uint32_t it = 0;
     bool ok = true;
-    while (ok && plan_ok) {
-      int u = 0;
-      if (lane == 0) u = atomicAdd(prm.ticket, 1);
-      u = __shfl_sync(0xffffffffu, u, 0);
-      if (u >= nunits) break;
-      const int s = upper_index(prm.uoff, nseq, u);
-      const int rem = u - prm.uoff[s];
-      const int sigma = rem / prm.H, h = rem % prm.H;
-      const int g = (int)((long long)h * prm.G / prm.H);
-      const float A2 = prm.A[h] * kLog2e;
-      const long long b = prm.si.begin(s), e = prm.si.end(s);
-      const int nt = (int)((e - b + kQ - 1) / kQ);
-      const int tb = sigma * prm.seg, te = min(nt, tb + prm.seg);
-      const int last_seg = te == nt;
-      const int nA = last_seg ? 0 : te - tb, nB = te - tb;
-      for (int k = 0; k < nA + nB; ++k, ++it) {
-        const int kind = k < nA ? kKindA : kKindB;
-        const int t = kind == kKindA ? te - 1 - k : tb + (k - nA);
-        const int st = it & 1;
-        if (it >= 2 && !wait_bar_warp(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1)) {
-          if (lane == 0) fail(SSD_ERR_TIMEOUT);
-          ok = false;
-          break;
-        }
-        if (__any_sync(0xffffffffu, *abort_v)) { ok = false; break; }
-        const long long t0 = b + (long long)t * kQ;
-        const int len = (int)min((long long)kQ, e - t0);
-        uint64_t* fb = &bars[kFull0 + st];
-        if (lane == 0) {
-          TileInfo* inf = sm.info(st);
-          inf->t0 = t0;
-          inf->s = s;
-          inf->h = h;
-          inf->sigma = sigma;
-          inf->unit = u;
-          inf->len = len;
-          inf->kind = kind;
-          inf->idx = kind == kKindA ? k : k - nA;
-          inf->cnt = kind == kKindA ? nA : nB;
-          inf->nA = nA;
-          inf->last_seg = last_seg;
-          const int row = (int)t0;
-          if (kind == kKindB) {
-            mbar_arrive_expect_tx(fb, kStageBytes);
-            tma_load_2d(sm.C(st, 0), &map_c, fb, g * kN, row);
-            tma_load_2d(sm.C(st, 1), &map_c, fb, g * kN + 64, row);
-          } else {
-            mbar_arrive_expect_tx(fb, kStageBytesA);
-          }
-          tma_load_2d(sm.B(st, 0), &map_b, fb, g * kN, row);
-          tma_load_2d(sm.B(st, 1), &map_b, fb, g * kN + 64, row);
-          tma_load_2d(sm.X(st), &map_x, fb, h * kP, row);
-        }
-        // decay table: lane l owns tokens 4l .. 4l+3
-        __nv_bfloat16 dv[4];
-        float pre[4], run = 0.f;
+    PUnit U;
+    int k = 0;
+    bool have = plan_ok && draw(U);
+    long long nt0 = 0;
+    int nkind = 0, nlen = 0;
+    __nv_bfloat16 dpre[4];
+    auto load_dt = [&](const PUnit& X, long long t0, int len) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int j = 4 * lane + q;
-          dv[q] = j < len ? prm.dt[(t0 + j) * prm.H + h] : __float2bfloat16(0.f);
-          run += __bfloat162float(dv[q]) * A2;
-          pre[q] = run;
-        }
-        float incl = run;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float tv = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += tv;
-        }
-        const float excl = incl - run;
-        float* c2t = sm.c2(st);
-        __nv_bfloat16* dtt = sm.dt(st);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          c2t[4 * lane + q] = excl + pre[q];
-          dtt[4 * lane + q] = dv[q];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(fb);
+      for (int q = 0; q < 4; ++q) {
+        const int j = 4 * lane + q;
+        dpre[q] = j < len ? prm.dt[(t0 + j) * prm.H + X.h] : __float2bfloat16(0.f);
       }
+    };
+    if (have) {
+      tile_of(U, 0, nt0, nkind, nlen);
+      load_dt(U, nt0, nlen);
+    }
+    while (have) {
+      const PUnit C = U;
+      const int ck = k;
+      const long long t0 = nt0;
+      const int kind = nkind, len = nlen;
+      __nv_bfloat16 dv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dv[q] = dpre[q];
+      // advance, and start the next chunk's dt loads
+      if (++k >= U.nA + U.nB) {
+        k = 0;
+        have = draw(U);
+      }
+      if (have) {
+        tile_of(U, k, nt0, nkind, nlen);
+        load_dt(U, nt0, nlen);
+        if (lane == 0) {
+          // the next chunk's tiles into L2 while this one waits for its slot
+          const int nrow = (int)nt0;
+          if (nkind == kKindB) {
+            tma_prefetch_2d(&map_c, U.g * kN, nrow);
+            tma_prefetch_2d(&map_c, U.g * kN + 64, nrow);
+          }
+          tma_prefetch_2d(&map_b, U.g * kN, nrow);
+          tma_prefetch_2d(&map_b, U.g * kN + 64, nrow);
+          tma_prefetch_2d(&map_x, U.h * kP, nrow);
+        }
+      }
+      // hand this chunk over through stage it & 1
+      const int st = it & 1;
+      if (it >= 2 && !wait_bar_warp(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1)) {
+        if (lane == 0) fail(SSD_ERR_TIMEOUT);
+        ok = false;
+        break;
+      }
+      if (__any_sync(0xffffffffu, *abort_v)) { ok = false; break; }
+      uint64_t* fb = &bars[kFull0 + st];
+      if (lane == 0) {
+        TileInfo* inf = sm.info(st);
+        inf->t0 = t0;
+        inf->s = C.s;
+        inf->h = C.h;
+        inf->sigma = C.sigma;
+        inf->unit = C.u;
+        inf->len = len;
+        inf->kind = kind;
+        inf->idx = kind == kKindA ? ck : ck - C.nA;
+        inf->cnt = kind == kKindA ? C.nA : C.nB;
+        inf->nA = C.nA;
+        inf->last_seg = C.last_seg;
+        const int row = (int)t0;
+        if (kind == kKindB) {
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          tma_load_2d(sm.C(st, 0), &map_c, fb, C.g * kN, row);
+          tma_load_2d(sm.C(st, 1), &map_c, fb, C.g * kN + 64, row);
+        } else {
+          mbar_arrive_expect_tx(fb, kStageBytesA);
+        }
+        tma_load_2d(sm.B(st, 0), &map_b, fb, C.g * kN, row);
+        tma_load_2d(sm.B(st, 1), &map_b, fb, C.g * kN + 64, row);
+        tma_load_2d(sm.X(st), &map_x, fb, C.h * kP, row);
+      }
+      // decay table: lane l owns tokens 4l .. 4l+3
+      float pre[4], run = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        run += __bfloat162float(dv[q]) * C.A2;
+        pre[q] = run;
+      }
+      float incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float tv = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += tv;
+      }
+      const float excl = incl - run;
+      float* c2t = sm.c2(st);
+      __nv_bfloat16* dtt = sm.dt(st);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        c2t[4 * lane + q] = excl + pre[q];
+        dtt[4 * lane + q] = dv[q];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fb);
+      ++it;
     }
     // sentinel: no more work
     const int st = it & 1;
@@ -406,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (lane == 0) {
       if (ok) fail(SSD_ERR_TIMEOUT);
       // aborting: loads still in flight must land before the CTA may exit
-      for (uint32_t k = (it >= 2 ? it - 2 : 0); k < it; ++k)
-        (void)wait_bar(&bars[kFull0 + (k & 1)], (k >> 1) & 1);
+      for (uint32_t q = (it >= 2 ? it - 2 : 0); q < it; ++q)
+        (void)wait_bar(&bars[kFull0 + (q & 1)], (q >> 1) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -437,6 +509,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&bars[kCbFull0 + (rbt & 1)]);
       };
+      // B^T (w o X) with the hi and lo halves of w o X into accumulator `col`
+      auto issue_state = [&](uint32_t col, uint32_t aB0, bool acc) {
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t aXw = smem_u32(sm.Xw(part));
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_bf16(col, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
+                     sdesc_sw128(aXw + k * 2048, kTile, 1024), idST, acc || part > 0 || k > 0);
+        }
+      };
       while (true) {
         const int st = it & 1;
         MMA_WAIT(kFull0 + st, (it >> 1) & 1);
@@ -445,19 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t aB0 = smem_u32(sm.B(st, 0));
         if (inf.kind == kKindA) {
-          // segment-local state: SA (+)= B^T (w o X), hi and lo halves
+          // segment-local state: SA (+)= B^T (w o X)
           if (inf.idx == 0 && au >= 1) { MMA_WAIT(kAggEmpty, (au - 1) & 1); }
           MMA_WAIT(kXwFull, xu & 1);
           tc_fence_after();
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint32_t aXw = smem_u32(sm.Xw(part));
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_bf16(tmem + kColSA, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
-                       sdesc_sw128(aXw + k * 2048, kTile, 1024), idST,
-                       inf.idx > 0 || part > 0 || k > 0);
-          }
+          issue_state(tmem + kColSA, aB0, inf.idx > 0);
           issued = true;
           mma_commit(&bars[kXwEmpty]);
           mma_commit(&bars[kEmpty0 + st]);
@@ -469,63 +544,85 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++it;
           continue;
         }
-        // forward chunk
+        // forward chunk: C B^T of this chunk if not issued ahead, then --
+        // in whatever order their inputs become ready -- the next chunk's
+        // C B^T (so the math warps can build its mask early), the chunk
+        // state, C H^T and S X.  Nothing waits behind an input that is late.
         if (inf.idx == 0) {
           if (bt >= 2) { MMA_WAIT(kCbEmpty0 + (bt & 1), ((bt >> 1) - 1) & 1); }
           issue_cb(it, bt);
           issued = true;
         }
-        if (inf.idx + 1 < inf.cnt) {
-          // the next chunk's C B^T first, so the math warps can build its
-          // mask while the tensor core runs this chunk's products
-          MMA_WAIT(kFull0 + ((it + 1) & 1), ((it + 1) >> 1) & 1);
-          if (bt + 1 >= 2) { MMA_WAIT(kCbEmpty0 + ((bt + 1) & 1), (((bt + 1) >> 1) - 1) & 1); }
-          tc_fence_after();
-          issue_cb(it + 1, bt + 1);
-          issued = true;
-        }
-        if (bt >= 1) { MMA_WAIT(kAccEmpty, (bt - 1) & 1); }
         const uint32_t aC0 = smem_u32(sm.C(st, 0)), aC1 = smem_u32(sm.C(st, 1));
         const uint32_t aX = smem_u32(sm.X(st));
-        // Y_off = C H^T (hi, lo)
-        MMA_WAIT(kHFull, bt & 1);
-        tc_fence_after();
+        bool need_cb = inf.idx + 1 < inf.cnt;
+        bool need_st = true, need_yo = true, need_yd = true;
+        const unsigned long long tw = gtime();
+        bool timed_out = false;
+        while (need_cb || need_st || need_yo || need_yd) {
+          bool progressed = false;
+          if (need_cb && mbar_test_wait(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1) &&
+              (bt + 1 < 2 ||
+               mbar_test_wait(&bars[kCbEmpty0 + ((bt + 1) & 1)], (((bt + 1) >> 1) - 1) & 1))) {
+            tc_fence_after();
+            issue_cb(it + 1, bt + 1);
+            need_cb = false;
+            progressed = true;
+          }
+          if (need_st && (bt < 1 || mbar_test_wait(&bars[kStFree], (bt - 1) & 1)) &&
+              mbar_test_wait(&bars[kXwFull], xu & 1)) {
+            // chunk state S_c^T = B^T (w o X)
+            tc_fence_after();
+            issue_state(tmem + kColST, aB0, false);
+            mma_commit(&bars[kXwEmpty]);
+            ++xu;
+            need_st = false;
+            progressed = true;
+          }
+          if (need_yo && (bt < 1 || mbar_test_wait(&bars[kYoFree], (bt - 1) & 1)) &&
+              mbar_test_wait(&bars[kHFull], bt & 1)) {
+            // Y_off = C H^T (hi, lo)
+            tc_fence_after();
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t aH = smem_u32(sm.Ht(part));
+            for (int part = 0; part < 2; ++part) {
+              const uint32_t aH = smem_u32(sm.Ht(part));
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t kb = (k & 3) * 32;
-            mma_bf16(tmem + kColYO, sdesc_sw128((k < 4 ? aC0 : aC1) + kb, 16, 1024),
-                     sdesc_sw128(aH + k * 2048, kTile, 1024), idYO, part > 0 || k > 0);
+              for (int k = 0; k < 8; ++k) {
+                const uint32_t kb = (k & 3) * 32;
+                mma_bf16(tmem + kColYO, sdesc_sw128((k < 4 ? aC0 : aC1) + kb, 16, 1024),
+                         sdesc_sw128(aH + k * 2048, kTile, 1024), idYO, part > 0 || k > 0);
+              }
+            }
+            mma_commit(&bars[kHEmpty]);
+            need_yo = false;
+            progressed = true;
+          }
+          if (need_yd && (bt < 1 || mbar_test_wait(&bars[kYdFree], (bt - 1) & 1)) &&
+              mbar_test_wait(&bars[kSFull0 + (bt & 1)], (bt >> 1) & 1)) {
+            // Y_diag = S X, S (hi, lo) read from TMEM.  K block k (columns
+            // j = 16k .. 16k+15 of S) sits in the 32-column block k/2: hi
+            // pairs at +8 (k%2), lo pairs at +16 + 8 (k%2)
+            tc_fence_after();
+            const uint32_t cbcol = tmem + kColCB + (bt & 1) * 128;
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                mma_bf16_tmem_a(tmem + kColYD, cbcol + 32 * (k >> 1) + 16 * part + 8 * (k & 1),
+                                sdesc_sw128(aX + k * 2048, kTile, 1024), idYD,
+                                part > 0 || k > 0);
+            need_yd = false;
+            progressed = true;
+          }
+          if (!progressed && (*abort_v || gtime() - tw > kWaitNs)) {
+            timed_out = true;
+            break;
           }
         }
-        mma_commit(&bars[kHEmpty]);
-        // chunk state S_c^T = B^T (w o X) (hi, lo)
-        MMA_WAIT(kXwFull, xu & 1);
-        tc_fence_after();
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t aXw = smem_u32(sm.Xw(part));
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_bf16(tmem + kColST, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
-                     sdesc_sw128(aXw + k * 2048, kTile, 1024), idST, part > 0 || k > 0);
+        if (timed_out) {
+          fail(SSD_ERR_TIMEOUT);
+          break;
         }
-        mma_commit(&bars[kXwEmpty]);
-        ++xu;
-        // Y_diag = S X, S (hi, lo) read from TMEM
-        MMA_WAIT(kSFull0 + (bt & 1), (bt >> 1) & 1);
-        tc_fence_after();
-        const uint32_t cbcol = tmem + kColCB + (bt & 1) * 128;
-        // K block k (columns j = 16k .. 16k+15 of S) sits in the 32-column
-        // block k/2: hi pairs at +8 (k%2), lo pairs at +16 + 8 (k%2)
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_bf16_tmem_a(tmem + kColYD, cbcol + 32 * (k >> 1) + 16 * part + 8 * (k & 1),
-                            sdesc_sw128(aX + k * 2048, kTile, 1024), idYD, part > 0 || k > 0);
         mma_commit(&bars[kAccFull]);
         mma_commit(&bars[kCbEmpty0 + (bt & 1)]);
         mma_commit(&bars[kEmpty0 + st]);
@@ -546,15 +643,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;       // lane quarter of this warp
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
     // use counters: ring chunk, forward chunk, w o X buffer, segment-state
-    // accumulator, and one per math-warp rendezvous barrier
+    // accumulator, hand-off rendezvous
     uint32_t it = 0, bt = 0, xu = 0, au = 0, nhand = 0;
-    float hreg[32];                // H[p][n = r] for p = 32 hp + q
-    uint32_t xpk[16];              // this chunk's x row half, bf16 pairs
+    float hreg[32];                // state entering a segment: H[p][n = r], p = 32 hp + q
 
     // Arrival number `use` (0, 1, ...) of this warp on a barrier that all 8
     // math warps arrive on.  Arrivals carry no phase, so a warp first waits
-    // for the barrier's previous phase to complete: without that, a warp
-    // running a chunk ahead could complete a phase in place of a slower one.
+    // for the barrier's previous phase to complete.
     auto arrive_seq = [&](int bar, uint32_t use) -> bool {
       if (use >= 1 && !wait_bar_warp(&bars[bar], (use - 1) & 1)) return false;
       __syncwarp();
@@ -562,20 +657,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    // The decay mask S of forward chunk number `pbt` (its tables must be
-    // current), written as bf16 hi/lo pairs over its C B^T in TMEM.  Each
-    // 32-column block j in [32 hb, 32 hb + 32) of a row is rewritten in place
-    // as 16 columns of hi pairs followed by 16 columns of lo pairs, so a
-    // thread only ever overwrites TMEM it has just read itself.
+    // this thread's decay values of the chunk in stage `stg`
+    auto chunk_vals = [&](int stg, float& c2l, float& c2r, float& dtr) {
+      const float* c2 = sm.c2(stg);
+      c2l = c2[kQ - 1];
+      c2r = c2[r];
+      dtr = __bfloat162float(sm.dt(stg)[r]);
+    };
+
+    // The decay mask S of forward chunk number `pbt`, written as bf16 hi/lo
+    // pairs over its C B^T in TMEM.  Each 32-column block j in
+    // [32 hb, 32 hb + 32) of a row is rewritten in place as 16 columns of hi
+    // pairs followed by 16 columns of lo pairs, so a thread only overwrites
+    // TMEM it has just read itself.
     auto build_mask = [&](uint32_t pbt, int stg, float c2r) -> bool {
       const float* c2 = sm.c2(stg);
       const __nv_bfloat16* dtt = sm.dt(stg);
       if (!wait_bar_warp(&bars[kCbFull0 + (pbt & 1)], (pbt >> 1) & 1)) return false;
       tc_fence_after();
       const uint32_t cbcol = tmem + kColCB + (pbt & 1) * 128 + lane_addr;
-      const int b = 32 * wq;             // first row of this warp's lanes
+      const int b = 32 * wq;                // first row of this warp's lanes
       const float c2b = c2[b];
-      const float u = exp2f(c2r - c2b);  // <= 1 for A <= 0
+      const float u = fast_exp2(c2r - c2b);  // <= 1 for A <= 0
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         const int j0 = 64 * hp + 32 * half;
@@ -590,7 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j0 + 32 <= b) {
             // strictly below this warp's rows: exp(cum_i - cum_j) =
             // exp(cum_i - cum_b) exp(cum_b - cum_j), both factors <= 1
-            const float vl = exp2f(c2b - c2[j0 + lane]) * __bfloat162float(dtt[j0 + lane]);
+            // column factor exp(cum_b - cum_j) dt_j, computed by lane j - j0
+            // and broadcast; the row factor u is this thread's own
+            const float vl = fast_exp2(c2b - c2[j0 + lane]) * __bfloat162float(dtt[j0 + lane]);
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
               const float v0 = __shfl_sync(0xffffffffu, vl, 2 * q);
@@ -603,9 +708,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 16; ++q) {
               const int ja = j0 + 2 * q, jb = ja + 1;
               const float sa =
-                  ja <= r ? g[2 * q] * exp2f(c2r - c2[ja]) * __bfloat162float(dtt[ja]) : 0.f;
+                  ja <= r ? g[2 * q] * fast_exp2(c2r - c2[ja]) * __bfloat162float(dtt[ja]) : 0.f;
               const float sb =
-                  jb <= r ? g[2 * q + 1] * exp2f(c2r - c2[jb]) * __bfloat162float(dtt[jb]) : 0.f;
+                  jb <= r ? g[2 * q + 1] * fast_exp2(c2r - c2[jb]) * __bfloat162float(dtt[jb])
+                          : 0.f;
               split2(sa, sb, pkh[q], pkl[q]);
             }
           }
@@ -621,45 +727,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       return arrive_seq(kSFull0 + (pbt & 1), pbt >> 1);
     };
 
-    // w o X (w = weight of row r) of the chunk in stage `stg` into the Xw
-    // buffer, keeping x in `xpk` when asked; releases the stage (math side).
-    auto make_xw = [&](uint32_t pit, float w, bool keep_x) -> bool {
-      const int stg = pit & 1;
-      if (xu >= 1 && !wait_bar_warp(&bars[kXwEmpty], (xu - 1) & 1)) return false;
+    // w o X (w = weight of row r) of the chunk in stage `stg` as hi/lo bf16
+    // pairs; also returns this thread's x row half as raw bf16 pairs.
+    auto compute_xw = [&](int stg, float w, uint32_t (&ph)[16], uint32_t (&pl)[16],
+                          uint32_t (&xk)[16]) {
       const uint8_t* Xs = sm.X(stg);
-      float xw[32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const uint4 xv = *reinterpret_cast<const uint4*>(Xs + sw128_offset(r, 4 * hp + c));
-        if (keep_x) {
-          xpk[4 * c + 0] = xv.x;
-          xpk[4 * c + 1] = xv.y;
-          xpk[4 * c + 2] = xv.z;
-          xpk[4 * c + 3] = xv.w;
-        }
-        xw[8 * c + 0] = w * bf_lo(xv.x);
-        xw[8 * c + 1] = w * bf_hi(xv.x);
-        xw[8 * c + 2] = w * bf_lo(xv.y);
-        xw[8 * c + 3] = w * bf_hi(xv.y);
-        xw[8 * c + 4] = w * bf_lo(xv.z);
-        xw[8 * c + 5] = w * bf_hi(xv.z);
-        xw[8 * c + 6] = w * bf_lo(xv.w);
-        xw[8 * c + 7] = w * bf_hi(xv.w);
+        xk[4 * c + 0] = xv.x;
+        xk[4 * c + 1] = xv.y;
+        xk[4 * c + 2] = xv.z;
+        xk[4 * c + 3] = xv.w;
+        split2(w * bf_lo(xv.x), w * bf_hi(xv.x), ph[4 * c + 0], pl[4 * c + 0]);
+        split2(w * bf_lo(xv.y), w * bf_hi(xv.y), ph[4 * c + 1], pl[4 * c + 1]);
+        split2(w * bf_lo(xv.z), w * bf_hi(xv.z), ph[4 * c + 2], pl[4 * c + 2]);
+        split2(w * bf_lo(xv.w), w * bf_hi(xv.w), ph[4 * c + 3], pl[4 * c + 3]);
       }
-      store_split_row(sm.Xw(0), sm.Xw(1), r, hp, xw);
+    };
+    // the Xw buffer once the tensor core has read its previous contents
+    auto store_xw = [&](const uint32_t (&ph)[16], const uint32_t (&pl)[16]) -> bool {
+      if (xu >= 1 && !wait_bar_warp(&bars[kXwEmpty], (xu - 1) & 1)) return false;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t off = sw128_offset(r, 4 * hp + c);
+        *reinterpret_cast<uint4*>(sm.Xw(0) + off) =
+            make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+        *reinterpret_cast<uint4*>(sm.Xw(1) + off) =
+            make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+      }
       fence_proxy_async_smem();
       if (!arrive_seq(kXwFull, xu)) return false;
-      if (!arrive_seq(kEmpty0 + stg, pit >> 1)) return false;
       ++xu;
       return true;
     };
-
-    // this thread's decay values of the chunk in stage `stg`
-    auto chunk_vals = [&](int stg, float& c2l, float& c2r, float& dtr) {
-      const float* c2 = sm.c2(stg);
-      c2l = c2[kQ - 1];
-      c2r = c2[r];
-      dtr = __bfloat162float(sm.dt(stg)[r]);
+    // the math warps are done reading the stage of ring chunk `pit`
+    auto release_stage = [&](uint32_t pit) -> bool {
+      return arrive_seq(kEmpty0 + (pit & 1), pit >> 1);
     };
 
 #define MATH_TRY(expr)     \
@@ -674,36 +778,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = u0.h;
       const float Dh = prm.D ? prm.D[h] : 0.f;
       const int nA = u0.nA;
+      // the initial state of a sequence's first segment is loaded now so its
+      // latency hides behind the segment-state pass
+      if (u0.sigma == 0) {
+        const float* ini = prm.init ? prm.init + ((long long)u0.s * prm.H + h) * kPN : nullptr;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) hreg[q] = ini ? __ldg(ini + (32 * hp + q) * kN + r) : 0.f;
+      }
 
       // -------- pass A: segment-local state, chunks walked backwards
       float later = 0.f;  // sum of the log2-decays of the chunks after this one
       for (int k = 0; k < nA; ++k) {
         if (k > 0) MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
-        const TileInfo inf = *sm.info(it & 1);
         float c2l, c2r, dtr;
         chunk_vals(it & 1, c2l, c2r, dtr);
-        const float w = exp2f(c2l - c2r + later) * dtr;
+        const float w = fast_exp2(c2l - c2r + later) * dtr;
         later += c2l;
-        MATH_TRY(make_xw(it, w, false));
+        uint32_t ph[16], pl[16], xk[16];
+        compute_xw(it & 1, w, ph, pl, xk);
+        MATH_TRY(release_stage(it));
+        MATH_TRY(store_xw(ph, pl));
         ++it;
       }
 
       // -------- segment hand-off
-      float hloc[32];
-      if (nA > 0) {
-        MATH_TRY(wait_bar_warp(&bars[kAggFull], au & 1));
-        tc_fence_after();
-        tmem_ld32(tmem + kColSA + lane_addr + 32 * hp, hloc);
-        tmem_ld_wait();
-        tc_fence_before();
-        MATH_TRY(arrive_seq(kAggEmpty, au));
-        ++au;
-      }
-      if (u0.sigma == 0) {
-        const float* ini = prm.init ? prm.init + ((long long)u0.s * prm.H + h) * kPN : nullptr;
-#pragma unroll
-        for (int q = 0; q < 32; ++q) hreg[q] = ini ? __ldg(ini + (32 * hp + q) * kN + r) : 0.f;
-      } else {
+      if (u0.sigma != 0) {
         const int pred = u0.unit - prm.H;  // same sequence and head, previous segment
         if (tid == 0) {
           const unsigned long long t0 = gtime();
@@ -722,91 +821,137 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 32; ++q) hreg[q] = __ldcg(src + (32 * hp + q) * kN + r);
       }
       if (nA > 0) {
-        // publish this segment's end state exp(sum dt A) H_in + H_loc
-        const float aseg = exp2f(later);
+        // this segment's end state exp(sum dt A) H_in + H_loc; the release
+        // flag follows once the first forward chunk is queued
+        MATH_TRY(wait_bar_warp(&bars[kAggFull], au & 1));
+        tc_fence_after();
+        float hloc[32];
+        tmem_ld32(tmem + kColSA + lane_addr + 32 * hp, hloc);
+        tmem_ld_wait();
+        const float aseg = fast_exp2(later);
         float* dst = prm.slots + (long long)u0.unit * kPN;
 #pragma unroll
         for (int q = 0; q < 32; ++q) __stcg(dst + (32 * hp + q) * kN + r, aseg * hreg[q] + hloc[q]);
-        __threadfence();
-        MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1));
-        ++nhand;
-        if (tid == 0) st_release(prm.flags + u0.unit, 1);
       }
-
-      // -------- pass B: the forward over the segment's chunks from H_in
+      // the running state H_in goes to TMEM (over the segment-local state)
+      // and, split into bf16 hi/lo, to the B operand of C H^T
+      tmem_st32(tmem + kColSA + lane_addr + 32 * hp, hreg);
+      tmem_st_wait();
+      tc_fence_before();
+      if (nA > 0) {
+        MATH_TRY(arrive_seq(kAggEmpty, au));
+        ++au;
+      }
       if (bt >= 1) MATH_TRY(wait_bar_warp(&bars[kHEmpty], (bt - 1) & 1));
       store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hreg);
       fence_proxy_async_smem();
       MATH_TRY(arrive_seq(kHFull, bt));
+
+      // -------- pass B: the forward over the segment's chunks from H_in
       {
         MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
-        TileInfo cur = *sm.info(it & 1);
+        const TileInfo* ci = sm.info(it & 1);
+        long long t0_cur = ci->t0;
+        int len_cur = ci->len;
+        const int nB = ci->cnt;
+        const int s_seq = ci->s, last_seg = ci->last_seg;
         float c2l_cur, c2r_cur, dtr_cur;
         chunk_vals(it & 1, c2l_cur, c2r_cur, dtr_cur);
         MATH_TRY(build_mask(bt, it & 1, c2r_cur));
-        MATH_TRY(make_xw(it, exp2f(c2l_cur - c2r_cur) * dtr_cur, true));
-        const int nB = cur.cnt;
+        uint32_t xk[16];   // this chunk's x row half (bf16 pairs) for the skip term
+        uint32_t xkn[16];  // the next chunk's
+        {
+          uint32_t ph[16], pl[16];
+          compute_xw(it & 1, fast_exp2(c2l_cur - c2r_cur) * dtr_cur, ph, pl, xk);
+          MATH_TRY(release_stage(it));
+          MATH_TRY(store_xw(ph, pl));
+        }
+        if (nA > 0) {
+          __threadfence();
+          MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1));
+          ++nhand;
+          if (tid == 0) st_release(prm.flags + u0.unit, 1);
+        }
         for (int t = 0; t < nB; ++t) {
           const bool more = t + 1 < nB;
-          TileInfo nxt = cur;
+          long long t0_nxt = 0;
+          int len_nxt = 0;
           float c2l_nxt = 0.f, c2r_nxt = 0.f, dtr_nxt = 0.f;
           if (more) {
-            // the next chunk's decay mask, while the tensor core works on this one
+            // the next chunk's mask while the tensor core works on this one
             MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1));
-            nxt = *sm.info((it + 1) & 1);
+            const TileInfo* ni = sm.info((it + 1) & 1);
+            t0_nxt = ni->t0;
+            len_nxt = ni->len;
             chunk_vals((it + 1) & 1, c2l_nxt, c2r_nxt, dtr_nxt);
             MATH_TRY(build_mask(bt + 1, (it + 1) & 1, c2r_nxt));
           }
-          // this chunk's epilogue and state update
+          // this chunk: the state first (it feeds the next chunk's C H^T)
           MATH_TRY(wait_bar_warp(&bars[kAccFull], bt & 1));
           tc_fence_after();
+          {
+            float sv[32], hv[32];
+            tmem_ld32(tmem + kColST + lane_addr + 32 * hp, sv);
+            tmem_ld32(tmem + kColSA + lane_addr + 32 * hp, hv);
+            tmem_ld_wait();
+            tc_fence_before();
+            MATH_TRY(arrive_seq(kStFree, bt));
+            const float a = fast_exp2(c2l_cur);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) hv[q] = a * hv[q] + sv[q];
+            if (more) {
+              tmem_st32(tmem + kColSA + lane_addr + 32 * hp, hv);
+              MATH_TRY(wait_bar_warp(&bars[kHEmpty], bt & 1));
+              store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hv);
+              fence_proxy_async_smem();
+              tmem_st_wait();
+              tc_fence_before();
+              MATH_TRY(arrive_seq(kHFull, bt + 1));
+            } else if (last_seg && prm.final_states) {
+              float* fin = prm.final_states + ((long long)s_seq * prm.H + h) * kPN;
+#pragma unroll
+              for (int q = 0; q < 32; ++q) fin[(32 * hp + q) * kN + r] = hv[q];
+            }
+          }
+          if (more) {
+            // the next chunk's w o X: its chunk-state MMA can start now
+            uint32_t ph[16], pl[16];
+            compute_xw((it + 1) & 1, fast_exp2(c2l_nxt - c2r_nxt) * dtr_nxt, ph, pl, xkn);
+            MATH_TRY(release_stage(it + 1));
+            MATH_TRY(store_xw(ph, pl));
+          }
           {
             float yd[32], yo[32];
             tmem_ld32(tmem + kColYD + lane_addr + 32 * hp, yd);
             tmem_ld32(tmem + kColYO + lane_addr + 32 * hp, yo);
             tmem_ld_wait();
-            if (r < cur.len) {
-              const float ei = exp2f(c2r_cur);
-              float* yrow = prm.y + ((cur.t0 + r) * prm.H + h) * kP + 32 * hp;
+            tc_fence_before();
+            MATH_TRY(arrive_seq(kYoFree, bt));
+            MATH_TRY(arrive_seq(kYdFree, bt));
+            if (r < len_cur) {
+              const float ei = fast_exp2(c2r_cur);
+              float* yrow = prm.y + ((t0_cur + r) * prm.H + h) * kP + 32 * hp;
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
                 float4 o;
-                o.x = yd[4 * c + 0] + ei * yo[4 * c + 0] + Dh * bf_lo(xpk[2 * c]);
-                o.y = yd[4 * c + 1] + ei * yo[4 * c + 1] + Dh * bf_hi(xpk[2 * c]);
-                o.z = yd[4 * c + 2] + ei * yo[4 * c + 2] + Dh * bf_lo(xpk[2 * c + 1]);
-                o.w = yd[4 * c + 3] + ei * yo[4 * c + 3] + Dh * bf_hi(xpk[2 * c + 1]);
+                o.x = yd[4 * c + 0] + ei * yo[4 * c + 0] + Dh * bf_lo(xk[2 * c]);
+                o.y = yd[4 * c + 1] + ei * yo[4 * c + 1] + Dh * bf_hi(xk[2 * c]);
+                o.z = yd[4 * c + 2] + ei * yo[4 * c + 2] + Dh * bf_lo(xk[2 * c + 1]);
+                o.w = yd[4 * c + 3] + ei * yo[4 * c + 3] + Dh * bf_hi(xk[2 * c + 1]);
                 __stcs(reinterpret_cast<float4*>(yrow + 4 * c), o);
               }
             }
           }
-          {
-            float sv[32];
-            tmem_ld32(tmem + kColST + lane_addr + 32 * hp, sv);
-            tmem_ld_wait();
-            const float a = exp2f(c2l_cur);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) hreg[q] = a * hreg[q] + sv[q];
-          }
-          tc_fence_before();
-          MATH_TRY(arrive_seq(kAccEmpty, bt));
-          if (more) {
-            MATH_TRY(wait_bar_warp(&bars[kHEmpty], bt & 1));
-            store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hreg);
-            fence_proxy_async_smem();
-            MATH_TRY(arrive_seq(kHFull, bt + 1));
-          } else if (cur.last_seg && prm.final_states) {
-            float* fin = prm.final_states + ((long long)cur.s * prm.H + h) * kPN;
-#pragma unroll
-            for (int q = 0; q < 32; ++q) fin[(32 * hp + q) * kN + r] = hreg[q];
-          }
           ++bt;
           ++it;
           if (more) {
-            cur = nxt;
+            t0_cur = t0_nxt;
+            len_cur = len_nxt;
             c2l_cur = c2l_nxt;
             c2r_cur = c2r_nxt;
             dtr_cur = dtr_nxt;
-            MATH_TRY(make_xw(it, exp2f(c2l_cur - c2r_cur) * dtr_cur, true));
+#pragma unroll
+            for (int q = 0; q < 16; ++q) xk[q] = xkn[q];
           }
         }
       }
