@@ -46,6 +46,7 @@ def parse_args():
     ap.add_argument("--workload", default="l8k")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     return ap.parse_args()
 
 
@@ -155,21 +156,46 @@ def dist_init():
     return world, rank, local
 
 
+def oracle_sample(fi, wl, max_tokens):
+    """A bounded sample of the workload for the CPU oracle: all heads, the
+    first `max_tokens` tokens of batch row 0 (for packed sequences, the first
+    whole sequences up to that many tokens).  Returns the oracle's arguments
+    and the number of tokens in the sample."""
+    if fi.cu_seqlens is None:
+        t = min(wl.seqlen, max_tokens)
+        init = None if fi.init is None else fi.init[:1]
+        return (fi.x[:1, :t], fi.dt[:1, :t], fi.A, fi.B[:1, :t], fi.C[:1, :t], fi.D, init,
+                None), t
+    cu = fi.cu_seqlens
+    k = 1
+    while k < fi.nseq and cu[k + 1] <= max_tokens:
+        k += 1
+    t = int(cu[k])
+    init = None if fi.init is None else fi.init[:k]
+    return (fi.x[:, :t], fi.dt[:, :t], fi.A, fi.B[:, :t], fi.C[:, :t], fi.D, init,
+            cu[:k + 1].copy()), t
+
+
+REFERENCE_SAMPLE_TOKENS = 2048
+
+
 def run_reference(args, world, rank):
-    """The fp64 CPU oracle on the host cores, on the same workload."""
+    """The fp64 CPU oracle on the host cores: each step runs it on a bounded
+    sample of the same workload (all heads, the first 2048 tokens), and the
+    metric is the sample's tokens per second."""
     if rank != 0:
         return
-    import numpy as np  # noqa: F401
     import oracle
     from state_space_sequence_05_b300 import inputs as I
     wl = I.WORKLOADS[args.workload]
     fi = I.make_forward_inputs(wl)
+    wl = fi.wl
+    oracle.build()
     cores = os.cpu_count() or 1
-    ntok = wl.batch * wl.seqlen
+    sample, ntok = oracle_sample(fi, wl, REFERENCE_SAMPLE_TOKENS)
 
     def step():
-        oracle.ssd_scan(fi.x, fi.dt, fi.A, fi.B, fi.C, fi.D, fi.init, fi.cu_seqlens,
-                        nthreads=cores)
+        oracle.ssd_scan(*sample, nthreads=cores)
 
     for _ in range(args.warmup):
         step()
@@ -180,17 +206,28 @@ def run_reference(args, world, rank):
         times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
     value = ntok / (ms / 1e3)
+    what = (f"first {ntok} tokens x all {wl.nheads} heads of the workload per step, "
+            f"{cores} threads over (sequence, head) units")
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-           "dtype": "f64", "data": "synthetic",
-           "config": {"workload": f"{wl.name}: b{wl.batch} T{wl.seqlen} H{wl.nheads} "
-                      f"P{wl.headdim} N{wl.dstate} G{wl.ngroups} chunk{wl.chunk}"},
+           "dtype": "f64", "data": "synthetic (seeded PCG64)",
+           "config": workload_config(wl, 1),
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                            "sample": "the full workload per step (all heads, all tokens)"},
+                            "sample": what},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
+
+
+def workload_config(wl, world):
+    return {"workload": f"{wl.name}: b{wl.batch} T{wl.seqlen} H{wl.nheads} P{wl.headdim} "
+                        f"N{wl.dstate} G{wl.ngroups} chunk{wl.chunk}, {wl.dtype} in / fp32 "
+                        f"state+y, init {wl.init}" + (f", {wl.nseq} packed sequences"
+                                                     if wl.nseq else ""),
+            "global_batch": wl.batch * world, "seq_len": wl.seqlen,
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "flushed before every timed step (256 MiB write outside the events)"}
 
 
 def main():
@@ -302,6 +339,10 @@ def main():
             e2e["_ms"] = float(t.item())
         e2e["value"] = ntok * world / (e2e.pop("_ms") / 1e3)
 
+    decode = None
+    if not args.no_decode:
+        decode = measure_decode(dev, peaks)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(fi, wl)
@@ -311,16 +352,11 @@ def main():
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                "dtype": wl.dtype, "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
-               "config": {"workload": f"{wl.name}: b{wl.batch} T{wl.seqlen} H{H} P{P} N{N} "
-                                      f"G{G} chunk{wl.chunk}, bf16 in / fp32 state+y, "
-                                      f"init {wl.init}",
-                          "global_batch": wl.batch * world, "seq_len": wl.seqlen,
-                          "parallelism": "replicas" if world > 1 else "single GPU",
-                          "l2": "flushed before every timed step (256 MiB write outside the events)"},
+               "config": workload_config(wl, world),
                "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
                "launches_per_step": launches / max(1, args.steps),
                "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
-               "e2e": e2e, "cpu_baseline": cpu,
+               "e2e": e2e, "cpu_baseline": cpu, "decode": decode,
                "pages_claim": "SSD 2-8x faster than Mamba's fused selective scan (A100), context only"}
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -380,20 +416,96 @@ def measure_e2e(args, fi, wl, dev, A, D, call_kwargs):
 
 
 def cpu_baseline(fi, wl):
-    """The fp64 oracle as it stands, on all host cores, over the full workload."""
+    """The fp64 oracle as it stands, on all host cores, over a bounded sample
+    of the workload (all heads, up to 8192 tokens: the whole L = 8K layer)."""
     import oracle
     cores = os.cpu_count() or 1
     oracle.build()
+    sample, ntok = oracle_sample(fi, wl, 8192)
     ts = []
     for _ in range(2):
         t0 = time.perf_counter()
-        oracle.ssd_scan(fi.x, fi.dt, fi.A, fi.B, fi.C, fi.D, fi.init, fi.cu_seqlens,
-                        nthreads=cores)
+        oracle.ssd_scan(*sample, nthreads=cores)
         ts.append(time.perf_counter() - t0)
     t = min(ts)
-    ntok = wl.batch * wl.seqlen
     return {"value": ntok / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"full {wl.name} workload ({ntok} tokens x {wl.nheads} heads), best of 2"}
+            "sample": f"first {ntok} tokens x all {wl.nheads} heads of {wl.name}, best of 2, "
+                      f"{cores} threads over (sequence, head) units"}
+
+
+def measure_decode(dev, peaks, name="decode_b256"):
+    """ssd_state_update over the decode workload: 128 consecutive steps on a
+    resident fp32 state (671 MB, larger than L2, so no flush is needed).
+    Each step is timed with CUDA events (median reported); the same 128 steps
+    are then replayed from one CUDA graph."""
+    import torch
+    from state_space_sequence_05_b300 import inputs as I
+    from state_space_sequence_05_b300 import ssd
+    wl = I.DECODE_WORKLOADS[name]
+    dec = I.make_decode_inputs(wl)
+    b, H, P, N, G = wl.batch, wl.nheads, wl.headdim, wl.dstate, wl.ngroups
+    state = torch.from_numpy(dec.state0).to(dev)
+    A = torch.from_numpy(dec.A).to(dev)
+    D = torch.from_numpy(dec.D).to(dev)
+    toks = []
+    for k in range(wl.steps):
+        t = I.make_decode_token(wl, dec, k)
+        toks.append({n: I.as_torch(getattr(t, n), t.bits.get(n), dev, wl.dtype)
+                     for n in ("x", "dt", "B", "C")})
+    y = torch.empty((b, H, P), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def step(k):
+        t = toks[k]
+        ssd.ssd_state_update(state, t["x"], t["dt"], A, t["B"], t["C"], D, y=y, stream=stream)
+
+    for k in range(3):
+        step(k)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(wl.steps)]
+    l0 = ssd.kernel_launches()
+    for k in range(wl.steps):
+        ev[k][0].record(stream)
+        step(k)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    launches = ssd.kernel_launches() - l0
+    us = [1e3 * s.elapsed_time(e) for s, e in ev]
+    med = statistics.median(us)
+    graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for k in range(wl.steps):
+                    t = toks[k]
+                    ssd.ssd_state_update(state, t["x"], t["dt"], A, t["B"], t["C"], D, y=y,
+                                         stream=side)
+        stream.wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        g.replay()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        graph_us = 1e3 * s0.elapsed_time(s1) / wl.steps
+    except RuntimeError as e:  # graph capture unsupported: report the eager number only
+        graph_us = f"capture failed: {e}".splitlines()[0][:120]
+    ein = 2 if wl.dtype == "bf16" else 4
+    bytes_ = (2 * b * H * P * N * 4 + b * H * P * (ein + 4) + b * H * ein
+              + 2 * b * G * N * ein + 2 * H * 4)
+    gbs = bytes_ / (med * 1e-6) / 1e9
+    return {"workload": f"{name}: b{b} H{H} P{P} N{N} G{G}, {wl.steps} steps, {wl.dtype} in, "
+                        "fp32 state in place",
+            "us_per_step_median": med, "us_per_step_min": min(us),
+            "tokens_per_s": b / (med * 1e-6), "graph_us_per_step": graph_us,
+            "algorithmic_bytes_per_step": bytes_, "achieved_gbs": gbs,
+            "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+            "gpu_launches": launches}
 
 
 if __name__ == "__main__":

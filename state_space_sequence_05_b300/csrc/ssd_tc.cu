@@ -43,14 +43,15 @@
 //   3. runs the forward over its chunks starting from H_in.
 // The state never leaves the SM between the chunks of a segment.
 //
-// Roles (one persistent CTA per SM, 320 threads):
-//   warp 8     TMA producer: C, B, x tiles (128B swizzle) into a 2-stage ring.
-//   warp 9     MMA issuer (one thread): C B^T, B^T (w o X), C H^T and S X
+// Roles (one persistent CTA per SM, 576 threads):
+//   warp 16    TMA producer: C, B, x tiles (128B swizzle) into a 2-stage ring,
+//              and the chunk's cumulative decay table.
+//   warp 17    MMA issuer (one thread): C B^T, B^T (w o X), C H^T and S X
 //              (S read from tensor memory); issues the next chunk's C B^T
 //              ahead of the current chunk's products.
-//   warps 0-7  CUDA-core math (TMEM lane r, column half hp): cumulative
-//              decay, decay mask (built for chunk c+1 while the tensor core
-//              works on chunk c), epilogue, fp32 state in registers,
+//   warps 0-15 CUDA-core math (TMEM lane quarter w % 4, column quarter
+//              w / 4): decay mask (built for chunk c+1 while the tensor core
+//              works on chunk c), w o X, fp32 state in registers, epilogue,
 //              segment hand-off.
 // Every wait is bounded in time; on expiry the kernel records
 // SSD_ERR_TIMEOUT and unwinds.
@@ -73,10 +74,10 @@ constexpr int kP = 64;   // headdim
 constexpr int kN = 128;  // dstate
 constexpr int kPN = kP * kN;
 constexpr int kStages = 2;
-constexpr int kMathWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kMathWarps = 16;
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 576;
 
 constexpr uint32_t kTile = 16384;                   // one 128 x 64 bf16 tile
 constexpr uint32_t kStageBytes = 5 * kTile;         // C0 C1 B0 B1 X
@@ -92,10 +93,11 @@ constexpr uint32_t kSmemBytes = kSmemUse + 1024;    // slack for 1024-B alignmen
 // TMEM columns (fp32 accumulators, 128 lanes).
 constexpr uint32_t kColCB = 0;     // 2 x 128: C B^T, overwritten in place by S (hi/lo pairs)
 constexpr uint32_t kColYD = 256;   // 64: S X
-constexpr uint32_t kColYO = 320;   // 64: C H^T
-constexpr uint32_t kColST = 384;   // 64: chunk state (lane n, column p)
-constexpr uint32_t kColSA = 448;   // 64: segment-local state; during a forward pass the
-                                   // running fp32 state H (lane n, column p)
+constexpr uint32_t kColST = 320;   // 64: chunk state (lane n, column p)
+constexpr uint32_t kColYO = 384;   // 128: C H_hi^T | C H_lo^T
+constexpr uint32_t kColSA = 384;   // 128: segment-local state from the hi | lo halves of
+                                   // w o X (shares the columns of C H^T: the two are
+                                   // never live at once)
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -133,6 +135,7 @@ struct Params {
   float* slots;         // per unit: segment end state [P][N] fp32
   int32_t* status;
   int H, G, seg;
+  int y_v8;             // y is 32-byte aligned: 32-byte stores
 };
 
 __device__ __forceinline__ unsigned long long gtime() {
@@ -201,23 +204,6 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   lo = pack_bf2(a - ha, b - hb);
 }
 
-// Write 32 fp32 values (one row's half) as hi and lo bf16 rows in two
-// 128B-swizzled tiles, 16-byte chunks 4*hp .. 4*hp+3 of row `row`.
-__device__ __forceinline__ void store_split_row(uint8_t* hi_tile, uint8_t* lo_tile, int row,
-                                                int hp, const float* v) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint4 h4, l4;
-    split2(v[8 * c + 0], v[8 * c + 1], h4.x, l4.x);
-    split2(v[8 * c + 2], v[8 * c + 3], h4.y, l4.y);
-    split2(v[8 * c + 4], v[8 * c + 5], h4.z, l4.z);
-    split2(v[8 * c + 6], v[8 * c + 7], h4.w, l4.w);
-    const uint32_t off = sw128_offset(row, 4 * hp + c);
-    *reinterpret_cast<uint4*>(hi_tile + off) = h4;
-    *reinterpret_cast<uint4*>(lo_tile + off) = l4;
-  }
-}
-
 struct Smem {
   uint8_t* base;
   __device__ uint8_t* stage(int s) const { return base + s * kStageBytes; }
@@ -248,7 +234,7 @@ enum {
   kHFull, kHEmpty,                           // H^T buffer
   kAccFull,                                  // Y_diag, Y_off, chunk state ready
   kStFree, kYoFree, kYdFree,                 // each accumulator read (math -> MMA)
-  kAggFull, kAggEmpty,                       // segment-local state accumulator
+  kAggFull,                                  // segment-local state accumulated
   kSyncHand,                                 // math-warp rendezvous
   kMmaDone,
   kNumBars
@@ -288,7 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kYoFree], kMathWarps);
     mbar_init(&bars[kYdFree], kMathWarps);
     mbar_init(&bars[kAggFull], 1);
-    mbar_init(&bars[kAggEmpty], kMathWarps);
     mbar_init(&bars[kSyncHand], kMathWarps);
     mbar_init(&bars[kMmaDone], 1);
     abort_sh = 0;
@@ -486,7 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idCB = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idST = idesc_bf16(128, 64, true, true);
-      constexpr uint32_t idYO = idesc_bf16(128, 64, false, true);
+      constexpr uint32_t idSA = idesc_bf16(128, 128, true, true);
+      constexpr uint32_t idYO = idesc_bf16(128, 128, false, true);
       constexpr uint32_t idYD = idesc_bf16(128, 64, false, true);
       uint32_t it = 0, bt = 0, xu = 0, au = 0;
       bool issued = false;
@@ -528,11 +514,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t aB0 = smem_u32(sm.B(st, 0));
         if (inf.kind == kKindA) {
-          // segment-local state: SA (+)= B^T (w o X)
-          if (inf.idx == 0 && au >= 1) { MMA_WAIT(kAggEmpty, (au - 1) & 1); }
+          // segment-local state: SA (+)= B^T [w o X hi | w o X lo], one N = 128
+          // product per K step (the two halves are summed when SA is read).
+          // SA shares its columns with C H^T: the last forward chunk's must
+          // have been read.
+          if (inf.idx == 0 && bt >= 1) { MMA_WAIT(kYoFree, (bt - 1) & 1); }
           MMA_WAIT(kXwFull, xu & 1);
           tc_fence_after();
-          issue_state(tmem + kColSA, aB0, inf.idx > 0);
+          {
+            const uint32_t aXw = smem_u32(sm.Xw(0));
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_bf16(tmem + kColSA, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
+                       sdesc_sw128(aXw + k * 2048, kTile, 1024), idSA, inf.idx > 0 || k > 0);
+          }
           issued = true;
           mma_commit(&bars[kXwEmpty]);
           mma_commit(&bars[kEmpty0 + st]);
@@ -581,16 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (need_yo && (bt < 1 || mbar_test_wait(&bars[kYoFree], (bt - 1) & 1)) &&
               mbar_test_wait(&bars[kHFull], bt & 1)) {
-            // Y_off = C H^T (hi, lo)
+            // [Y_off_hi | Y_off_lo] = C [H_hi | H_lo]^T: the two 64-column
+            // halves of the B operand are the hi and lo tiles, kTile apart
             tc_fence_after();
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const uint32_t aH = smem_u32(sm.Ht(part));
+            {
+              const uint32_t aH = smem_u32(sm.Ht(0));
 #pragma unroll
               for (int k = 0; k < 8; ++k) {
                 const uint32_t kb = (k & 3) * 32;
                 mma_bf16(tmem + kColYO, sdesc_sw128((k < 4 ? aC0 : aC1) + kb, 16, 1024),
-                         sdesc_sw128(aH + k * 2048, kTile, 1024), idYO, part > 0 || k > 0);
+                         sdesc_sw128(aH + k * 2048, kTile, 1024), idYO, k > 0);
               }
             }
             mma_commit(&bars[kHEmpty]);
@@ -599,16 +594,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (need_yd && (bt < 1 || mbar_test_wait(&bars[kYdFree], (bt - 1) & 1)) &&
               mbar_test_wait(&bars[kSFull0 + (bt & 1)], (bt >> 1) & 1)) {
-            // Y_diag = S X, S (hi, lo) read from TMEM.  K block k (columns
-            // j = 16k .. 16k+15 of S) sits in the 32-column block k/2: hi
-            // pairs at +8 (k%2), lo pairs at +16 + 8 (k%2)
+            // Y_diag = S X, S (hi, lo) read from TMEM: K block k (columns
+            // j = 16k .. 16k+15 of S) holds 8 columns of hi pairs, then 8 of
+            // lo pairs
             tc_fence_after();
             const uint32_t cbcol = tmem + kColCB + (bt & 1) * 128;
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
               for (int k = 0; k < 8; ++k)
-                mma_bf16_tmem_a(tmem + kColYD, cbcol + 32 * (k >> 1) + 16 * part + 8 * (k & 1),
+                mma_bf16_tmem_a(tmem + kColYD, cbcol + 16 * k + 8 * part,
                                 sdesc_sw128(aX + k * 2048, kTile, 1024), idYD,
                                 part > 0 || k > 0);
             need_yd = false;
@@ -638,16 +633,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ math warps
-    const int r = tid & 127;       // TMEM lane: token row i / state row n / token j
-    const int hp = tid >> 7;       // column half
-    const int wq = warp & 3;       // lane quarter of this warp
+    // Warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 (a warp may only
+    // touch its own lane quarter) and takes column quarter cq = w / 4: one
+    // 32-column block of the 128 x 128 mask, and columns 16 cq .. 16 cq + 15
+    // of every 64-wide (headdim) tile.
+    const int wq = warp & 3;
+    const int cq = warp >> 2;
+    const int r = 32 * wq + lane;  // TMEM lane: token row i / state row n / token j
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
     // use counters: ring chunk, forward chunk, w o X buffer, segment-state
     // accumulator, hand-off rendezvous
     uint32_t it = 0, bt = 0, xu = 0, au = 0, nhand = 0;
-    float hreg[32];                // state entering a segment: H[p][n = r], p = 32 hp + q
+    float hreg[16];  // fp32 state H[p][n = r], p = 16 cq + q
 
-    // Arrival number `use` (0, 1, ...) of this warp on a barrier that all 8
+    // Arrival number `use` (0, 1, ...) of this warp on a barrier that all
     // math warps arrive on.  Arrivals carry no phase, so a warp first waits
     // for the barrier's previous phase to complete.
     auto arrive_seq = [&](int bar, uint32_t use) -> bool {
@@ -666,58 +665,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // The decay mask S of forward chunk number `pbt`, written as bf16 hi/lo
-    // pairs over its C B^T in TMEM.  Each 32-column block j in
-    // [32 hb, 32 hb + 32) of a row is rewritten in place as 16 columns of hi
-    // pairs followed by 16 columns of lo pairs, so a thread only overwrites
-    // TMEM it has just read itself.
+    // pairs over its C B^T in TMEM.  Each 16-column block j in [16 k, 16 k +
+    // 16) of a row (the MMA's K block k) is rewritten in place as 8 columns
+    // of hi pairs followed by 8 columns of lo pairs, so a thread only
+    // overwrites TMEM it has just read itself.  This warp owns blocks 2 cq
+    // and 2 cq + 1 of its rows.
     auto build_mask = [&](uint32_t pbt, int stg, float c2r) -> bool {
       const float* c2 = sm.c2(stg);
       const __nv_bfloat16* dtt = sm.dt(stg);
       if (!wait_bar_warp(&bars[kCbFull0 + (pbt & 1)], (pbt >> 1) & 1)) return false;
       tc_fence_after();
       const uint32_t cbcol = tmem + kColCB + (pbt & 1) * 128 + lane_addr;
-      const int b = 32 * wq;                // first row of this warp's lanes
-      const float c2b = c2[b];
-      const float u = fast_exp2(c2r - c2b);  // <= 1 for A <= 0
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        const int j0 = 64 * hp + 32 * half;
-        uint32_t pkh[16], pkl[16];
-        if (j0 > b + 31) {
+      const int b = 32 * wq;   // first row of this warp's lanes
+      const int j0 = 32 * cq;  // first column of this warp's two blocks
+      if (j0 > b) {
+        // strictly above the diagonal: causal zeros
+        uint32_t z[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) pkh[q] = pkl[q] = 0u;
-        } else {
-          float g[32];
-          tmem_ld32(cbcol + j0, g);
+        for (int q = 0; q < 16; ++q) z[q] = 0u;
+        tmem_st16(cbcol + j0, z);
+        tmem_st16(cbcol + j0 + 16, z);
+      } else if (j0 < b) {
+        // strictly below this warp's rows: exp(cum_i - cum_j) =
+        // exp(cum_i - cum_b) exp(cum_b - cum_j), both factors <= 1.  The
+        // column factor exp(cum_b - cum_j) dt_j is computed by lane j - j0
+        // and broadcast; the row factor u is this thread's own.
+        const float c2b = c2[b];
+        const float u = fast_exp2(c2r - c2b);
+        const float vl = fast_exp2(c2b - c2[j0 + lane]) * __bfloat162float(dtt[j0 + lane]);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float g[16];
+          tmem_ld16(cbcol + j0 + 16 * half, g);
           tmem_ld_wait();
-          if (j0 + 32 <= b) {
-            // strictly below this warp's rows: exp(cum_i - cum_j) =
-            // exp(cum_i - cum_b) exp(cum_b - cum_j), both factors <= 1
-            // column factor exp(cum_b - cum_j) dt_j, computed by lane j - j0
-            // and broadcast; the row factor u is this thread's own
-            const float vl = fast_exp2(c2b - c2[j0 + lane]) * __bfloat162float(dtt[j0 + lane]);
+          tie16(g);
+          uint32_t pk[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const float v0 = __shfl_sync(0xffffffffu, vl, 2 * q);
-              const float v1 = __shfl_sync(0xffffffffu, vl, 2 * q + 1);
-              split2(g[2 * q] * (u * v0), g[2 * q + 1] * (u * v1), pkh[q], pkl[q]);
-            }
-          } else {
-            // the diagonal block: direct, causal
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const int ja = j0 + 2 * q, jb = ja + 1;
-              const float sa =
-                  ja <= r ? g[2 * q] * fast_exp2(c2r - c2[ja]) * __bfloat162float(dtt[ja]) : 0.f;
-              const float sb =
-                  jb <= r ? g[2 * q + 1] * fast_exp2(c2r - c2[jb]) * __bfloat162float(dtt[jb])
-                          : 0.f;
-              split2(sa, sb, pkh[q], pkl[q]);
-            }
+          for (int q = 0; q < 8; ++q) {
+            const float v0 = __shfl_sync(0xffffffffu, vl, 16 * half + 2 * q);
+            const float v1 = __shfl_sync(0xffffffffu, vl, 16 * half + 2 * q + 1);
+            split2(g[2 * q] * v0 * u, g[2 * q + 1] * v1 * u, pk[q], pk[8 + q]);
           }
+          tmem_st16(cbcol + j0 + 16 * half, pk);
         }
-        tmem_st16(cbcol + j0, pkh);
-        tmem_st16(cbcol + j0 + 16, pkl);
+      } else {
+        // the diagonal block: direct, causal
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float g[16];
+          tmem_ld16(cbcol + j0 + 16 * half, g);
+          tmem_ld_wait();
+          tie16(g);
+          uint32_t pk[16];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int ja = j0 + 16 * half + 4 * m;
+            const float4 cc = *reinterpret_cast<const float4*>(c2 + ja);
+            const uint2 dd = *reinterpret_cast<const uint2*>(dtt + ja);
+            const float s0 = ja <= r ? g[4 * m] * fast_exp2(c2r - cc.x) * bf_lo(dd.x) : 0.f;
+            const float s1 = ja + 1 <= r ? g[4 * m + 1] * fast_exp2(c2r - cc.y) * bf_hi(dd.x) : 0.f;
+            const float s2 = ja + 2 <= r ? g[4 * m + 2] * fast_exp2(c2r - cc.z) * bf_lo(dd.y) : 0.f;
+            const float s3 = ja + 3 <= r ? g[4 * m + 3] * fast_exp2(c2r - cc.w) * bf_hi(dd.y) : 0.f;
+            split2(s0, s1, pk[2 * m], pk[8 + 2 * m]);
+            split2(s2, s3, pk[2 * m + 1], pk[8 + 2 * m + 1]);
+          }
+          tmem_st16(cbcol + j0 + 16 * half, pk);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -728,13 +741,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // w o X (w = weight of row r) of the chunk in stage `stg` as hi/lo bf16
-    // pairs; also returns this thread's x row half as raw bf16 pairs.
-    auto compute_xw = [&](int stg, float w, uint32_t (&ph)[16], uint32_t (&pl)[16],
-                          uint32_t (&xk)[16]) {
+    // pairs, this thread's 16 columns; also returns them as raw bf16 pairs.
+    auto compute_xw = [&](int stg, float w, uint32_t (&ph)[8], uint32_t (&pl)[8],
+                          uint32_t (&xk)[8]) {
       const uint8_t* Xs = sm.X(stg);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(Xs + sw128_offset(r, 4 * hp + c));
+      for (int c = 0; c < 2; ++c) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(Xs + sw128_offset(r, 2 * cq + c));
         xk[4 * c + 0] = xv.x;
         xk[4 * c + 1] = xv.y;
         xk[4 * c + 2] = xv.z;
@@ -746,11 +759,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     // the Xw buffer once the tensor core has read its previous contents
-    auto store_xw = [&](const uint32_t (&ph)[16], const uint32_t (&pl)[16]) -> bool {
+    auto store_xw = [&](const uint32_t (&ph)[8], const uint32_t (&pl)[8]) -> bool {
       if (xu >= 1 && !wait_bar_warp(&bars[kXwEmpty], (xu - 1) & 1)) return false;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t off = sw128_offset(r, 4 * hp + c);
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t off = sw128_offset(r, 2 * cq + c);
         *reinterpret_cast<uint4*>(sm.Xw(0) + off) =
             make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
         *reinterpret_cast<uint4*>(sm.Xw(1) + off) =
@@ -764,6 +777,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the math warps are done reading the stage of ring chunk `pit`
     auto release_stage = [&](uint32_t pit) -> bool {
       return arrive_seq(kEmpty0 + (pit & 1), pit >> 1);
+    };
+    // H^T (hi, lo) for C H^T: row n = r, this thread's 16 columns p
+    auto store_ht = [&]() {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint4 h4, l4;
+        split2(hreg[8 * c + 0], hreg[8 * c + 1], h4.x, l4.x);
+        split2(hreg[8 * c + 2], hreg[8 * c + 3], h4.y, l4.y);
+        split2(hreg[8 * c + 4], hreg[8 * c + 5], h4.z, l4.z);
+        split2(hreg[8 * c + 6], hreg[8 * c + 7], h4.w, l4.w);
+        const uint32_t off = sw128_offset(r, 2 * cq + c);
+        *reinterpret_cast<uint4*>(sm.Ht(0) + off) = h4;
+        *reinterpret_cast<uint4*>(sm.Ht(1) + off) = l4;
+      }
+      fence_proxy_async_smem();
     };
 
 #define MATH_TRY(expr)     \
@@ -783,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u0.sigma == 0) {
         const float* ini = prm.init ? prm.init + ((long long)u0.s * prm.H + h) * kPN : nullptr;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) hreg[q] = ini ? __ldg(ini + (32 * hp + q) * kN + r) : 0.f;
+        for (int q = 0; q < 16; ++q) hreg[q] = ini ? __ldg(ini + (16 * cq + q) * kN + r) : 0.f;
       }
 
       // -------- pass A: segment-local state, chunks walked backwards
@@ -794,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         chunk_vals(it & 1, c2l, c2r, dtr);
         const float w = fast_exp2(c2l - c2r + later) * dtr;
         later += c2l;
-        uint32_t ph[16], pl[16], xk[16];
+        uint32_t ph[8], pl[8], xk[8];
         compute_xw(it & 1, w, ph, pl, xk);
         MATH_TRY(release_stage(it));
         MATH_TRY(store_xw(ph, pl));
@@ -818,33 +846,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, *abort_v)) goto math_done;
         const float* src = prm.slots + (long long)pred * kPN;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) hreg[q] = __ldcg(src + (32 * hp + q) * kN + r);
+        for (int q = 0; q < 16; ++q) hreg[q] = __ldcg(src + (16 * cq + q) * kN + r);
       }
       if (nA > 0) {
-        // this segment's end state exp(sum dt A) H_in + H_loc; the release
-        // flag follows once the first forward chunk is queued
+        // this segment's end state exp(sum dt A) H_in + H_loc, H_loc the sum
+        // of SA's hi and lo halves; the release flag follows once the first
+        // forward chunk is queued
         MATH_TRY(wait_bar_warp(&bars[kAggFull], au & 1));
         tc_fence_after();
-        float hloc[32];
-        tmem_ld32(tmem + kColSA + lane_addr + 32 * hp, hloc);
+        float ha[16], hb[16];
+        tmem_ld16(tmem + kColSA + lane_addr + 16 * cq, ha);
+        tmem_ld16(tmem + kColSA + lane_addr + 64 + 16 * cq, hb);
         tmem_ld_wait();
+        tie16(ha);
+        tie16(hb);
+        // SA is read: the first C H^T may overwrite it once H^T is in place
+        tc_fence_before();
         const float aseg = fast_exp2(later);
         float* dst = prm.slots + (long long)u0.unit * kPN;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) __stcg(dst + (32 * hp + q) * kN + r, aseg * hreg[q] + hloc[q]);
-      }
-      // the running state H_in goes to TMEM (over the segment-local state)
-      // and, split into bf16 hi/lo, to the B operand of C H^T
-      tmem_st32(tmem + kColSA + lane_addr + 32 * hp, hreg);
-      tmem_st_wait();
-      tc_fence_before();
-      if (nA > 0) {
-        MATH_TRY(arrive_seq(kAggEmpty, au));
+        for (int q = 0; q < 16; ++q)
+          __stcg(dst + (16 * cq + q) * kN + r, aseg * hreg[q] + (ha[q] + hb[q]));
         ++au;
       }
+      // the running state H_in, split into bf16 hi/lo, to the B operand of C H^T
       if (bt >= 1) MATH_TRY(wait_bar_warp(&bars[kHEmpty], (bt - 1) & 1));
-      store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hreg);
-      fence_proxy_async_smem();
+      store_ht();
       MATH_TRY(arrive_seq(kHFull, bt));
 
       // -------- pass B: the forward over the segment's chunks from H_in
@@ -858,10 +885,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float c2l_cur, c2r_cur, dtr_cur;
         chunk_vals(it & 1, c2l_cur, c2r_cur, dtr_cur);
         MATH_TRY(build_mask(bt, it & 1, c2r_cur));
-        uint32_t xk[16];   // this chunk's x row half (bf16 pairs) for the skip term
-        uint32_t xkn[16];  // the next chunk's
+        uint32_t xk[8];   // this chunk's x (bf16 pairs, this thread's 16 columns)
+        uint32_t xkn[8];  // the next chunk's
         {
-          uint32_t ph[16], pl[16];
+          uint32_t ph[8], pl[8];
           compute_xw(it & 1, fast_exp2(c2l_cur - c2r_cur) * dtr_cur, ph, pl, xk);
           MATH_TRY(release_stage(it));
           MATH_TRY(store_xw(ph, pl));
@@ -890,55 +917,66 @@ __global__ void __launch_bounds__(kThreads, 1)
           MATH_TRY(wait_bar_warp(&bars[kAccFull], bt & 1));
           tc_fence_after();
           {
-            float sv[32], hv[32];
-            tmem_ld32(tmem + kColST + lane_addr + 32 * hp, sv);
-            tmem_ld32(tmem + kColSA + lane_addr + 32 * hp, hv);
+            float sv[16];
+            tmem_ld16(tmem + kColST + lane_addr + 16 * cq, sv);
             tmem_ld_wait();
+            tie16(sv);
             tc_fence_before();
             MATH_TRY(arrive_seq(kStFree, bt));
             const float a = fast_exp2(c2l_cur);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) hv[q] = a * hv[q] + sv[q];
+            for (int q = 0; q < 16; ++q) hreg[q] = a * hreg[q] + sv[q];
             if (more) {
-              tmem_st32(tmem + kColSA + lane_addr + 32 * hp, hv);
               MATH_TRY(wait_bar_warp(&bars[kHEmpty], bt & 1));
-              store_split_row(sm.Ht(0), sm.Ht(1), r, hp, hv);
-              fence_proxy_async_smem();
-              tmem_st_wait();
-              tc_fence_before();
+              store_ht();
               MATH_TRY(arrive_seq(kHFull, bt + 1));
             } else if (last_seg && prm.final_states) {
               float* fin = prm.final_states + ((long long)s_seq * prm.H + h) * kPN;
 #pragma unroll
-              for (int q = 0; q < 32; ++q) fin[(32 * hp + q) * kN + r] = hv[q];
+              for (int q = 0; q < 16; ++q) fin[(16 * cq + q) * kN + r] = hreg[q];
             }
           }
           if (more) {
             // the next chunk's w o X: its chunk-state MMA can start now
-            uint32_t ph[16], pl[16];
+            uint32_t ph[8], pl[8];
             compute_xw((it + 1) & 1, fast_exp2(c2l_nxt - c2r_nxt) * dtr_nxt, ph, pl, xkn);
             MATH_TRY(release_stage(it + 1));
             MATH_TRY(store_xw(ph, pl));
           }
           {
-            float yd[32], yo[32];
-            tmem_ld32(tmem + kColYD + lane_addr + 32 * hp, yd);
-            tmem_ld32(tmem + kColYO + lane_addr + 32 * hp, yo);
-            tmem_ld_wait();
-            tc_fence_before();
-            MATH_TRY(arrive_seq(kYoFree, bt));
-            MATH_TRY(arrive_seq(kYdFree, bt));
-            if (r < len_cur) {
-              const float ei = fast_exp2(c2r_cur);
-              float* yrow = prm.y + ((t0_cur + r) * prm.H + h) * kP + 32 * hp;
+            // epilogue, in two 8-column halves: y = Y_diag + exp(cum_i)
+            // (Y_off_hi + Y_off_lo) + D x
+            const float ei = fast_exp2(c2r_cur);
+            float* yrow = prm.y + ((t0_cur + r) * prm.H + h) * kP + 16 * cq;
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                float4 o;
-                o.x = yd[4 * c + 0] + ei * yo[4 * c + 0] + Dh * bf_lo(xk[2 * c]);
-                o.y = yd[4 * c + 1] + ei * yo[4 * c + 1] + Dh * bf_hi(xk[2 * c]);
-                o.z = yd[4 * c + 2] + ei * yo[4 * c + 2] + Dh * bf_lo(xk[2 * c + 1]);
-                o.w = yd[4 * c + 3] + ei * yo[4 * c + 3] + Dh * bf_hi(xk[2 * c + 1]);
-                __stcs(reinterpret_cast<float4*>(yrow + 4 * c), o);
+            for (int half = 0; half < 2; ++half) {
+              float yd[8], yh[8], yl[8];
+              tmem_ld8(tmem + kColYD + lane_addr + 16 * cq + 8 * half, yd);
+              tmem_ld8(tmem + kColYO + lane_addr + 16 * cq + 8 * half, yh);
+              tmem_ld8(tmem + kColYO + lane_addr + 64 + 16 * cq + 8 * half, yl);
+              tmem_ld_wait();
+              tie8(yd);
+              tie8(yh);
+              tie8(yl);
+              if (half == 1) {
+                tc_fence_before();
+                MATH_TRY(arrive_seq(kYoFree, bt));
+                MATH_TRY(arrive_seq(kYdFree, bt));
+              }
+              if (r < len_cur) {
+                float o[8];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  const uint32_t xw = xk[4 * half + c];
+                  o[2 * c] = yd[2 * c] + ei * (yh[2 * c] + yl[2 * c]) + Dh * bf_lo(xw);
+                  o[2 * c + 1] = yd[2 * c + 1] + ei * (yh[2 * c + 1] + yl[2 * c + 1]) + Dh * bf_hi(xw);
+                }
+                if (prm.y_v8) {
+                  st_global_cs_v8(yrow + 8 * half, o);
+                } else {
+                  __stcs(reinterpret_cast<float4*>(yrow + 8 * half), make_float4(o[0], o[1], o[2], o[3]));
+                  __stcs(reinterpret_cast<float4*>(yrow + 8 * half + 4), make_float4(o[4], o[5], o[6], o[7]));
+                }
               }
             }
           }
@@ -951,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             c2r_cur = c2r_nxt;
             dtr_cur = dtr_nxt;
 #pragma unroll
-            for (int q = 0; q < 16; ++q) xk[q] = xkn[q];
+            for (int q = 0; q < 8; ++q) xk[q] = xkn[q];
           }
         }
       }
@@ -1144,6 +1182,7 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   p.H = a.H;
   p.G = a.G;
   p.seg = kSeg;
+  p.y_v8 = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
