@@ -235,6 +235,7 @@ enum {
   kAccFull,                                  // Y_diag, Y_off, chunk state ready
   kStFree, kYoFree, kYdFree,                 // each accumulator read (math -> MMA)
   kAggFull,                                  // segment-local state accumulated
+  kYRead,                                    // staged y tiles read by their TMA stores
   kSyncHand,                                 // math-warp rendezvous
   kMmaDone,
   kNumBars
@@ -243,7 +244,8 @@ enum {
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_tc_fwd_kernel(const __grid_constant__ CUtensorMap map_x,
                       const __grid_constant__ CUtensorMap map_b,
-                      const __grid_constant__ CUtensorMap map_c, Params prm) {
+                      const __grid_constant__ CUtensorMap map_c,
+                      const __grid_constant__ CUtensorMap map_y, Params prm) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[kNumBars];
   __shared__ uint32_t tmem_base_sh;
@@ -276,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kAggFull], 1);
     mbar_init(&bars[kSyncHand], kMathWarps);
     mbar_init(&bars[kMmaDone], 1);
+    mbar_init(&bars[kYRead], kMathWarps);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -311,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&map_x);
       prefetch_tmap(&map_b);
       prefetch_tmap(&map_c);
+      prefetch_tmap(&map_y);
     }
     struct PUnit {
       long long b, e;
@@ -609,9 +613,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             need_yd = false;
             progressed = true;
           }
-          if (!progressed && (*abort_v || gtime() - tw > kWaitNs)) {
-            timed_out = true;
-            break;
+          if (!progressed) {
+            if (*abort_v || gtime() - tw > kWaitNs) {
+              timed_out = true;
+              break;
+            }
+            // nothing ready: sleep on the input that usually comes next
+            // rather than spin, so the math warps sharing this warp's
+            // scheduler keep its issue slots
+            if (need_yd)
+              (void)mbar_try_wait_hint(&bars[kYdFree], (bt - 1) & 1, 200);
+            else if (need_st)
+              (void)mbar_try_wait_hint(&bars[kXwFull], xu & 1, 200);
+            else if (need_yo)
+              (void)mbar_try_wait_hint(&bars[kHFull], bt & 1, 200);
+            else
+              (void)mbar_try_wait_hint(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1, 200);
           }
         }
         if (timed_out) {
@@ -644,6 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // use counters: ring chunk, forward chunk, w o X buffer, segment-state
     // accumulator, hand-off rendezvous
     uint32_t it = 0, bt = 0, xu = 0, au = 0, nhand = 0;
+    uint32_t ny = 0;     // epilogues whose staged y this warp has released
+    bool ypend = false;  // a y tile staged in the w o X buffer may still be read
     float hreg[16];  // fp32 state H[p][n = r], p = 16 cq + q
 
     // Arrival number `use` (0, 1, ...) of this warp on a barrier that all
@@ -670,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of hi pairs followed by 8 columns of lo pairs, so a thread only
     // overwrites TMEM it has just read itself.  This warp owns blocks 2 cq
     // and 2 cq + 1 of its rows.
-    auto build_mask = [&](uint32_t pbt, int stg, float c2r) -> bool {
+    auto build_mask = [&](uint32_t pbt, int stg, float c2r, float Dh) -> bool {
       const float* c2 = sm.c2(stg);
       const __nv_bfloat16* dtt = sm.dt(stg);
       if (!wait_bar_warp(&bars[kCbFull0 + (pbt & 1)], (pbt >> 1) & 1)) return false;
@@ -693,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c2b = c2[b];
         const float u = fast_exp2(c2r - c2b);
         const float vl = fast_exp2(c2b - c2[j0 + lane]) * __bfloat162float(dtt[j0 + lane]);
-#pragma unroll
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           float g[16];
           tmem_ld16(cbcol + j0 + 16 * half, g);
@@ -710,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // the diagonal block: direct, causal
-#pragma unroll
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           float g[16];
           tmem_ld16(cbcol + j0 + 16 * half, g);
@@ -719,6 +738,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
+            // keeps the table loads of one group of 4 columns together
+            // (hoisting all of them costs registers the warp does not have)
+            asm volatile("" ::: "memory");
             const int ja = j0 + 16 * half + 4 * m;
             const float4 cc = *reinterpret_cast<const float4*>(c2 + ja);
             const uint2 dd = *reinterpret_cast<const uint2*>(dtt + ja);
@@ -726,8 +748,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float s1 = ja + 1 <= r ? g[4 * m + 1] * fast_exp2(c2r - cc.y) * bf_hi(dd.x) : 0.f;
             const float s2 = ja + 2 <= r ? g[4 * m + 2] * fast_exp2(c2r - cc.z) * bf_lo(dd.y) : 0.f;
             const float s3 = ja + 3 <= r ? g[4 * m + 3] * fast_exp2(c2r - cc.w) * bf_hi(dd.y) : 0.f;
-            split2(s0, s1, pk[2 * m], pk[8 + 2 * m]);
-            split2(s2, s3, pk[2 * m + 1], pk[8 + 2 * m + 1]);
+            // the skip term D x rides on the diagonal: S[i][i] + D
+            const int dq = r - ja;
+            const float d0 = dq == 0 ? Dh : 0.f, d1 = dq == 1 ? Dh : 0.f;
+            const float d2 = dq == 2 ? Dh : 0.f, d3 = dq == 3 ? Dh : 0.f;
+            split2(s0 + d0, s1 + d1, pk[2 * m], pk[8 + 2 * m]);
+            split2(s2 + d2, s3 + d3, pk[2 * m + 1], pk[8 + 2 * m + 1]);
           }
           tmem_st16(cbcol + j0 + 16 * half, pk);
         }
@@ -741,17 +767,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // w o X (w = weight of row r) of the chunk in stage `stg` as hi/lo bf16
-    // pairs, this thread's 16 columns; also returns them as raw bf16 pairs.
-    auto compute_xw = [&](int stg, float w, uint32_t (&ph)[8], uint32_t (&pl)[8],
-                          uint32_t (&xk)[8]) {
+    // pairs, this thread's 16 columns.
+    auto compute_xw = [&](int stg, float w, uint32_t (&ph)[8], uint32_t (&pl)[8]) {
       const uint8_t* Xs = sm.X(stg);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const uint4 xv = *reinterpret_cast<const uint4*>(Xs + sw128_offset(r, 2 * cq + c));
-        xk[4 * c + 0] = xv.x;
-        xk[4 * c + 1] = xv.y;
-        xk[4 * c + 2] = xv.z;
-        xk[4 * c + 3] = xv.w;
         split2(w * bf_lo(xv.x), w * bf_hi(xv.x), ph[4 * c + 0], pl[4 * c + 0]);
         split2(w * bf_lo(xv.y), w * bf_hi(xv.y), ph[4 * c + 1], pl[4 * c + 1]);
         split2(w * bf_lo(xv.z), w * bf_hi(xv.z), ph[4 * c + 2], pl[4 * c + 2]);
@@ -761,6 +782,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the Xw buffer once the tensor core has read its previous contents
     auto store_xw = [&](const uint32_t (&ph)[8], const uint32_t (&pl)[8]) -> bool {
       if (xu >= 1 && !wait_bar_warp(&bars[kXwEmpty], (xu - 1) & 1)) return false;
+      if (ypend) {
+        // the buffer also stages the previous chunk's y for its TMA stores:
+        // every warp's store must have read it
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        if (!arrive_seq(kYRead, ny)) return false;
+        if (!wait_bar_warp(&bars[kYRead], ny & 1)) return false;
+        ++ny;
+        ypend = false;
+      }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const uint32_t off = sw128_offset(r, 2 * cq + c);
@@ -801,15 +832,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
     while (true) {
       MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
-      const TileInfo u0 = *sm.info(it & 1);
-      if (u0.kind == kKindEnd || __any_sync(0xffffffffu, *abort_v)) break;
-      const int h = u0.h;
+      const TileInfo* u0p = sm.info(it & 1);
+      if (u0p->kind == kKindEnd || __any_sync(0xffffffffu, *abort_v)) break;
+      const int h = u0p->h;
+      const int nA = u0p->nA;
+      const int u_unit = u0p->unit, u_sigma = u0p->sigma, u_s = u0p->s;
       const float Dh = prm.D ? prm.D[h] : 0.f;
-      const int nA = u0.nA;
       // the initial state of a sequence's first segment is loaded now so its
       // latency hides behind the segment-state pass
-      if (u0.sigma == 0) {
-        const float* ini = prm.init ? prm.init + ((long long)u0.s * prm.H + h) * kPN : nullptr;
+      if (u_sigma == 0) {
+        const float* ini = prm.init ? prm.init + ((long long)u_s * prm.H + h) * kPN : nullptr;
 #pragma unroll
         for (int q = 0; q < 16; ++q) hreg[q] = ini ? __ldg(ini + (16 * cq + q) * kN + r) : 0.f;
       }
@@ -822,16 +854,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         chunk_vals(it & 1, c2l, c2r, dtr);
         const float w = fast_exp2(c2l - c2r + later) * dtr;
         later += c2l;
-        uint32_t ph[8], pl[8], xk[8];
-        compute_xw(it & 1, w, ph, pl, xk);
+        uint32_t ph[8], pl[8];
+        compute_xw(it & 1, w, ph, pl);
         MATH_TRY(release_stage(it));
         MATH_TRY(store_xw(ph, pl));
         ++it;
       }
 
       // -------- segment hand-off
-      if (u0.sigma != 0) {
-        const int pred = u0.unit - prm.H;  // same sequence and head, previous segment
+      if (u_sigma != 0) {
+        const int pred = u_unit - prm.H;  // same sequence and head, previous segment
         if (tid == 0) {
           const unsigned long long t0 = gtime();
           while (ld_acquire(prm.flags + pred) == 0) {
@@ -863,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // SA is read: the first C H^T may overwrite it once H^T is in place
         tc_fence_before();
         const float aseg = fast_exp2(later);
-        float* dst = prm.slots + (long long)u0.unit * kPN;
+        float* dst = prm.slots + (long long)u_unit * kPN;
 #pragma unroll
         for (int q = 0; q < 16; ++q)
           __stcg(dst + (16 * cq + q) * kN + r, aseg * hreg[q] + (ha[q] + hb[q]));
@@ -884,12 +916,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s_seq = ci->s, last_seg = ci->last_seg;
         float c2l_cur, c2r_cur, dtr_cur;
         chunk_vals(it & 1, c2l_cur, c2r_cur, dtr_cur);
-        MATH_TRY(build_mask(bt, it & 1, c2r_cur));
-        uint32_t xk[8];   // this chunk's x (bf16 pairs, this thread's 16 columns)
-        uint32_t xkn[8];  // the next chunk's
+        MATH_TRY(build_mask(bt, it & 1, c2r_cur, Dh));
         {
           uint32_t ph[8], pl[8];
-          compute_xw(it & 1, fast_exp2(c2l_cur - c2r_cur) * dtr_cur, ph, pl, xk);
+          compute_xw(it & 1, fast_exp2(c2l_cur - c2r_cur) * dtr_cur, ph, pl);
           MATH_TRY(release_stage(it));
           MATH_TRY(store_xw(ph, pl));
         }
@@ -897,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __threadfence();
           MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1));
           ++nhand;
-          if (tid == 0) st_release(prm.flags + u0.unit, 1);
+          if (tid == 0) st_release(prm.flags + u_unit, 1);
         }
         for (int t = 0; t < nB; ++t) {
           const bool more = t + 1 < nB;
@@ -911,11 +941,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             t0_nxt = ni->t0;
             len_nxt = ni->len;
             chunk_vals((it + 1) & 1, c2l_nxt, c2r_nxt, dtr_nxt);
-            MATH_TRY(build_mask(bt + 1, (it + 1) & 1, c2r_nxt));
+            MATH_TRY(build_mask(bt + 1, (it + 1) & 1, c2r_nxt, Dh));
           }
-          // this chunk: the state first (it feeds the next chunk's C H^T)
+          // this chunk's accumulators: read and release them first so the
+          // tensor core can start the next chunk's products
           MATH_TRY(wait_bar_warp(&bars[kAccFull], bt & 1));
           tc_fence_after();
+          const float ei = fast_exp2(c2r_cur);
+          float* yrow = prm.y + ((t0_cur + r) * prm.H + h) * kP + 16 * cq;
+          // y = Y_diag + exp(cum_i) (Y_off_hi + Y_off_lo), 8 columns (D x is
+          // part of Y_diag: D sits on the diagonal of S).
+          // A warp whose 32 rows are all valid stages its 32 x 16 tile in
+          // the w o X buffer (free from the chunk-state product's end to the
+          // next chunk's w o X; 64B-swizzled rows, 2 KB per warp) and writes
+          // it with one TMA store; rows of a ragged last chunk are stored
+          // directly.
+          const bool tma_y = 32 * wq + 32 <= len_cur;
+          uint8_t* ytile = sm.Xw(0) + warp * 2048;
+          auto emit_y = [&](int half, const float (&yd)[8], const float (&yh)[8],
+                            const float (&yl)[8]) {
+            float o[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) o[c] = yd[c] + ei * (yh[c] + yl[c]);
+            if (tma_y) {
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const int chunk = 2 * half + c;
+                *reinterpret_cast<float4*>(ytile + lane * 64 + 16 * (chunk ^ ((lane >> 1) & 3))) =
+                    make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+              }
+            } else if (r < len_cur) {
+              if (prm.y_v8) {
+                st_global_cs_v8(yrow + 8 * half, o);
+              } else {
+                __stcs(reinterpret_cast<float4*>(yrow + 8 * half), make_float4(o[0], o[1], o[2], o[3]));
+                __stcs(reinterpret_cast<float4*>(yrow + 8 * half + 4), make_float4(o[4], o[5], o[6], o[7]));
+              }
+            }
+          };
           {
             float sv[16];
             tmem_ld16(tmem + kColST + lane_addr + 16 * cq, sv);
@@ -923,62 +986,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             tie16(sv);
             tc_fence_before();
             MATH_TRY(arrive_seq(kStFree, bt));
+            // the state (it feeds the next chunk's C H^T)
             const float a = fast_exp2(c2l_cur);
 #pragma unroll
             for (int q = 0; q < 16; ++q) hreg[q] = a * hreg[q] + sv[q];
-            if (more) {
-              MATH_TRY(wait_bar_warp(&bars[kHEmpty], bt & 1));
-              store_ht();
-              MATH_TRY(arrive_seq(kHFull, bt + 1));
-            } else if (last_seg && prm.final_states) {
-              float* fin = prm.final_states + ((long long)s_seq * prm.H + h) * kPN;
+          }
+          if (more) {
+            MATH_TRY(wait_bar_warp(&bars[kHEmpty], bt & 1));
+            store_ht();
+            MATH_TRY(arrive_seq(kHFull, bt + 1));
+          } else if (last_seg && prm.final_states) {
+            float* fin = prm.final_states + ((long long)s_seq * prm.H + h) * kPN;
 #pragma unroll
-              for (int q = 0; q < 16; ++q) fin[(16 * cq + q) * kN + r] = hreg[q];
+            for (int q = 0; q < 16; ++q) fin[(16 * cq + q) * kN + r] = hreg[q];
+          }
+          {
+            float yd[8], yh[8], yl[8];
+            tmem_ld8(tmem + kColYD + lane_addr + 16 * cq, yd);
+            tmem_ld8(tmem + kColYO + lane_addr + 16 * cq, yh);
+            tmem_ld8(tmem + kColYO + lane_addr + 64 + 16 * cq, yl);
+            tmem_ld_wait();
+            tie8(yd);
+            tie8(yh);
+            tie8(yl);
+            emit_y(0, yd, yh, yl);
+          }
+          {
+            float yd[8], yh[8], yl[8];
+            tmem_ld8(tmem + kColYD + lane_addr + 16 * cq + 8, yd);
+            tmem_ld8(tmem + kColYO + lane_addr + 16 * cq + 8, yh);
+            tmem_ld8(tmem + kColYO + lane_addr + 64 + 16 * cq + 8, yl);
+            tmem_ld_wait();
+            tie8(yd);
+            tie8(yh);
+            tie8(yl);
+            tc_fence_before();
+            MATH_TRY(arrive_seq(kYoFree, bt));
+            MATH_TRY(arrive_seq(kYdFree, bt));
+            emit_y(1, yd, yh, yl);
+          }
+          if (tma_y) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&map_y, ytile, h * kP + 16 * cq, (int)(t0_cur + 32 * wq));
+              bulk_commit();
             }
           }
+          ypend = true;
           if (more) {
             // the next chunk's w o X: its chunk-state MMA can start now
             uint32_t ph[8], pl[8];
-            compute_xw((it + 1) & 1, fast_exp2(c2l_nxt - c2r_nxt) * dtr_nxt, ph, pl, xkn);
+            compute_xw((it + 1) & 1, fast_exp2(c2l_nxt - c2r_nxt) * dtr_nxt, ph, pl);
             MATH_TRY(release_stage(it + 1));
             MATH_TRY(store_xw(ph, pl));
-          }
-          {
-            // epilogue, in two 8-column halves: y = Y_diag + exp(cum_i)
-            // (Y_off_hi + Y_off_lo) + D x
-            const float ei = fast_exp2(c2r_cur);
-            float* yrow = prm.y + ((t0_cur + r) * prm.H + h) * kP + 16 * cq;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              float yd[8], yh[8], yl[8];
-              tmem_ld8(tmem + kColYD + lane_addr + 16 * cq + 8 * half, yd);
-              tmem_ld8(tmem + kColYO + lane_addr + 16 * cq + 8 * half, yh);
-              tmem_ld8(tmem + kColYO + lane_addr + 64 + 16 * cq + 8 * half, yl);
-              tmem_ld_wait();
-              tie8(yd);
-              tie8(yh);
-              tie8(yl);
-              if (half == 1) {
-                tc_fence_before();
-                MATH_TRY(arrive_seq(kYoFree, bt));
-                MATH_TRY(arrive_seq(kYdFree, bt));
-              }
-              if (r < len_cur) {
-                float o[8];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                  const uint32_t xw = xk[4 * half + c];
-                  o[2 * c] = yd[2 * c] + ei * (yh[2 * c] + yl[2 * c]) + Dh * bf_lo(xw);
-                  o[2 * c + 1] = yd[2 * c + 1] + ei * (yh[2 * c + 1] + yl[2 * c + 1]) + Dh * bf_hi(xw);
-                }
-                if (prm.y_v8) {
-                  st_global_cs_v8(yrow + 8 * half, o);
-                } else {
-                  __stcs(reinterpret_cast<float4*>(yrow + 8 * half), make_float4(o[0], o[1], o[2], o[3]));
-                  __stcs(reinterpret_cast<float4*>(yrow + 8 * half + 4), make_float4(o[4], o[5], o[6], o[7]));
-                }
-              }
-            }
           }
           ++bt;
           ++it;
@@ -988,13 +1049,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             c2l_cur = c2l_nxt;
             c2r_cur = c2r_nxt;
             dtr_cur = dtr_nxt;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) xk[q] = xkn[q];
           }
         }
       }
     }
-  math_done:;
+  math_done:
+    // y tiles still being written must land before the CTA exits
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
 #undef MATH_TRY
   }
 
@@ -1105,6 +1167,20 @@ bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// y as a 2D fp32 tensor [tokens][H * P]; a box is 16 columns x 32 rows,
+// 64B-swizzled (one math warp's tile).
+bool make_map_y(CUtensorMap* m, float* ptr, long long rows, long long cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n = 0;
   static std::once_flag once;
@@ -1161,10 +1237,11 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   count_launches(1);
   if (cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
   if (ntok == 0 || mu == 0) return SSD_OK;
-  CUtensorMap mx, mb, mc;
+  CUtensorMap mx, mb, mc, my;
   if (!make_map(&mx, a.x, ntok, (long long)a.H * kP) ||
       !make_map(&mb, a.B, ntok, (long long)a.G * kN) ||
-      !make_map(&mc, a.C, ntok, (long long)a.G * kN))
+      !make_map(&mc, a.C, ntok, (long long)a.G * kN) ||
+      !make_map_y(&my, a.y, ntok, (long long)a.H * kP))
     return SSD_ERR_CUDA;
   Params p;
   p.dt = static_cast<const __nv_bfloat16*>(a.dt);
@@ -1191,7 +1268,7 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   });
   if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
   const int grid = (int)(mu < sm_count() ? mu : sm_count());
-  ssd_tc_fwd_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(mx, mb, mc, p);
+  ssd_tc_fwd_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(mx, mb, mc, my, p);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
