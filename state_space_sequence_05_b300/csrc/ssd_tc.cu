@@ -665,11 +665,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ypend = false;  // a y tile staged in the w o X buffer may still be read
     float hreg[16];  // fp32 state H[p][n = r], p = 16 cq + q
 
-    // Arrival number `use` (0, 1, ...) of this warp on a barrier that all
-    // math warps arrive on.  Arrivals carry no phase, so a warp first waits
-    // for the barrier's previous phase to complete.
+    // This warp's arrival number `use` (0, 1, ...) on a barrier that all
+    // math warps arrive on.  Arrivals carry no phase, so a warp must never
+    // arrive twice before the others arrived once; on every such barrier
+    // that holds by construction: between two arrivals a warp waits on a
+    // phase that cannot complete before the first arrival's phase did (the
+    // tensor core's next use of the buffer, the next TMA fill of the stage,
+    // or, for kYRead, the phase itself).
     auto arrive_seq = [&](int bar, uint32_t use) -> bool {
-      if (use >= 1 && !wait_bar_warp(&bars[bar], (use - 1) & 1)) return false;
+      (void)use;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[bar]);
       return true;
@@ -704,58 +708,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 16; ++q) z[q] = 0u;
         tmem_st16(cbcol + j0, z);
         tmem_st16(cbcol + j0 + 16, z);
-      } else if (j0 < b) {
-        // strictly below this warp's rows: exp(cum_i - cum_j) =
-        // exp(cum_i - cum_b) exp(cum_b - cum_j), both factors <= 1.  The
-        // column factor exp(cum_b - cum_j) dt_j is computed by lane j - j0
-        // and broadcast; the row factor u is this thread's own.
-        const float c2b = c2[b];
-        const float u = fast_exp2(c2r - c2b);
-        const float vl = fast_exp2(c2b - c2[j0 + lane]) * __bfloat162float(dtt[j0 + lane]);
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          float g[16];
-          tmem_ld16(cbcol + j0 + 16 * half, g);
-          tmem_ld_wait();
-          tie16(g);
-          uint32_t pk[16];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float v0 = __shfl_sync(0xffffffffu, vl, 16 * half + 2 * q);
-            const float v1 = __shfl_sync(0xffffffffu, vl, 16 * half + 2 * q + 1);
-            split2(g[2 * q] * v0 * u, g[2 * q + 1] * v1 * u, pk[q], pk[8 + q]);
-          }
-          tmem_st16(cbcol + j0 + 16 * half, pk);
-        }
       } else {
-        // the diagonal block: direct, causal
+        // exp(cum_i - cum_j) = exp(cum_i - cum_b) exp(cum_b - cum_j): the
+        // row factor u is this thread's own, the column factor
+        // exp(cum_b - cum_j) dt_j is computed by lane j - j0 and broadcast.
+        // Below the diagonal both factors are <= 1.  On the diagonal block
+        // the column factor is >= 1, so the factored form is used only when
+        // the block's whole decay keeps both inside fp32's range (almost
+        // always); otherwise each entry takes its own exponential.
+        const float c2b = c2[b];
+        const bool diag = j0 == b;
+        const bool direct = diag && !(fabsf(c2b - c2[b + 31]) < 120.f);
+        if (!direct) {
+          const float u = fast_exp2(c2r - c2b);
+          const float vl = fast_exp2(c2b - c2[j0 + lane]) * __bfloat162float(dtt[j0 + lane]);
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          float g[16];
-          tmem_ld16(cbcol + j0 + 16 * half, g);
-          tmem_ld_wait();
-          tie16(g);
-          uint32_t pk[16];
+          for (int half = 0; half < 2; ++half) {
+            float g[16];
+            tmem_ld16(cbcol + j0 + 16 * half, g);
+            tmem_ld_wait();
+            tie16(g);
+            uint32_t pk[16];
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            // keeps the table loads of one group of 4 columns together
-            // (hoisting all of them costs registers the warp does not have)
-            asm volatile("" ::: "memory");
-            const int ja = j0 + 16 * half + 4 * m;
-            const float4 cc = *reinterpret_cast<const float4*>(c2 + ja);
-            const uint2 dd = *reinterpret_cast<const uint2*>(dtt + ja);
-            const float s0 = ja <= r ? g[4 * m] * fast_exp2(c2r - cc.x) * bf_lo(dd.x) : 0.f;
-            const float s1 = ja + 1 <= r ? g[4 * m + 1] * fast_exp2(c2r - cc.y) * bf_hi(dd.x) : 0.f;
-            const float s2 = ja + 2 <= r ? g[4 * m + 2] * fast_exp2(c2r - cc.z) * bf_lo(dd.y) : 0.f;
-            const float s3 = ja + 3 <= r ? g[4 * m + 3] * fast_exp2(c2r - cc.w) * bf_hi(dd.y) : 0.f;
-            // the skip term D x rides on the diagonal: S[i][i] + D
-            const int dq = r - ja;
-            const float d0 = dq == 0 ? Dh : 0.f, d1 = dq == 1 ? Dh : 0.f;
-            const float d2 = dq == 2 ? Dh : 0.f, d3 = dq == 3 ? Dh : 0.f;
-            split2(s0 + d0, s1 + d1, pk[2 * m], pk[8 + 2 * m]);
-            split2(s2 + d2, s3 + d3, pk[2 * m + 1], pk[8 + 2 * m + 1]);
+            for (int q = 0; q < 8; ++q) {
+              const float v0 = __shfl_sync(0xffffffffu, vl, 16 * half + 2 * q);
+              const float v1 = __shfl_sync(0xffffffffu, vl, 16 * half + 2 * q + 1);
+              float s0 = g[2 * q] * v0 * u, s1 = g[2 * q + 1] * v1 * u;
+              if (diag) {
+                // causal; the skip term D x rides on the diagonal: S[i][i] + D
+                const int ja = j0 + 16 * half + 2 * q;
+                s0 = ja < r ? s0 : (ja == r ? s0 + Dh : 0.f);
+                s1 = ja + 1 < r ? s1 : (ja + 1 == r ? s1 + Dh : 0.f);
+              }
+              split2(s0, s1, pk[q], pk[8 + q]);
+            }
+            tmem_st16(cbcol + j0 + 16 * half, pk);
           }
-          tmem_st16(cbcol + j0 + 16 * half, pk);
+        } else {
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            float g[16];
+            tmem_ld16(cbcol + j0 + 16 * half, g);
+            tmem_ld_wait();
+            tie16(g);
+            uint32_t pk[16];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              // keeps the table loads of one group of 4 columns together
+              // (hoisting all of them costs registers the warp does not have)
+              asm volatile("" ::: "memory");
+              const int ja = j0 + 16 * half + 4 * m;
+              const float4 cc = *reinterpret_cast<const float4*>(c2 + ja);
+              const uint2 dd = *reinterpret_cast<const uint2*>(dtt + ja);
+              const float s0 = ja <= r ? g[4 * m] * fast_exp2(c2r - cc.x) * bf_lo(dd.x) : 0.f;
+              const float s1 = ja + 1 <= r ? g[4 * m + 1] * fast_exp2(c2r - cc.y) * bf_hi(dd.x) : 0.f;
+              const float s2 = ja + 2 <= r ? g[4 * m + 2] * fast_exp2(c2r - cc.z) * bf_lo(dd.y) : 0.f;
+              const float s3 = ja + 3 <= r ? g[4 * m + 3] * fast_exp2(c2r - cc.w) * bf_hi(dd.y) : 0.f;
+              const int dq = r - ja;
+              const float d0 = dq == 0 ? Dh : 0.f, d1 = dq == 1 ? Dh : 0.f;
+              const float d2 = dq == 2 ? Dh : 0.f, d3 = dq == 3 ? Dh : 0.f;
+              split2(s0 + d0, s1 + d1, pk[2 * m], pk[8 + 2 * m]);
+              split2(s2 + d2, s3 + d3, pk[2 * m + 1], pk[8 + 2 * m + 1]);
+            }
+            tmem_st16(cbcol + j0 + 16 * half, pk);
+          }
         }
       }
       tmem_st_wait();
