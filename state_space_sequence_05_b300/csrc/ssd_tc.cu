@@ -84,11 +84,14 @@ constexpr uint32_t kStageBytes = 5 * kTile;         // C0 C1 B0 B1 X
 constexpr uint32_t kStageBytesA = 3 * kTile;        // B0 B1 X (segment-state pass)
 constexpr uint32_t kOffXw = kStages * kStageBytes;  // w o X as bf16 hi, lo (2 x 16 KB)
 constexpr uint32_t kOffHt = kOffXw + 2 * kTile;     // H^T as bf16 hi, lo (2 x 16 KB)
-constexpr uint32_t kOffTabs = kOffHt + 2 * kTile;   // per stage: c2 fp32[128], dt bf16[128]
-constexpr uint32_t kTabBytes = 128 * 4 + 128 * 2;
+// per stage: c2 fp32[128], E fp32[128], dt bf16[128]
+constexpr uint32_t kOffTabs = kOffHt + 2 * kTile;
+constexpr uint32_t kTabBytes = 128 * 4 + 128 * 4 + 128 * 2;
 constexpr uint32_t kOffInfo = kOffTabs + kStages * kTabBytes;
-constexpr uint32_t kSmemUse = kOffInfo + 2 * 64;
-constexpr uint32_t kSmemBytes = kSmemUse + 1024;    // slack for 1024-B alignment
+constexpr uint32_t kOffBars = kOffInfo + 2 * 64;
+// (barriers, then the TMEM base address and the abort flag)
+constexpr uint32_t kBarBytes = 32 * 8;
+constexpr uint32_t kSmemBytes = kOffBars + kBarBytes + 16;
 
 // TMEM columns (fp32 accumulators, 128 lanes).
 constexpr uint32_t kColCB = 0;     // 2 x 128: C B^T, overwritten in place by S (hi/lo pairs)
@@ -117,7 +120,8 @@ struct TileInfo {
   int idx, cnt;  // position of this chunk among the unit's chunks of its kind
   int nA;        // chunks in the unit's segment-state pass (0 = none)
   int last_seg;  // the unit is its sequence's last segment
-  int pad[2];
+  int ez;        // the E table is finite: |cum_last| log2(e) < 120
+  int pad;
 };
 static_assert(sizeof(TileInfo) <= 64, "tile info slot");
 
@@ -191,17 +195,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
-// v ~= hi + lo with hi = bf16(v), lo = bf16(v - hi); packs two such pairs.
+// v ~= hi + lo: hi = v with its low 16 bits cleared (bf16 by truncation),
+// lo = v - hi (exact in fp32) truncated to bf16 the same way; |v - hi - lo|
+// < 2^-14 |v|.  Packs the hi and lo halves of two values (a in the low 16
+// bits, as __floats2bfloat162_rn(a, b) would).
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float ha = __low2float(h), hb = __high2float(h);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = pack_bf2(a - ha, b - hb);
+  const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+  hi = __byte_perm(ua, ub, 0x7632);
+  const float la = a - __uint_as_float(ua & 0xffff0000u);
+  const float lb = b - __uint_as_float(ub & 0xffff0000u);
+  lo = __byte_perm(__float_as_uint(la), __float_as_uint(lb), 0x7632);
 }
 
 struct Smem {
@@ -216,9 +220,13 @@ struct Smem {
   __device__ float* c2(int s) const {
     return reinterpret_cast<float*>(base + kOffTabs + s * kTabBytes);
   }
+  // E[j] = exp(-cum_j) dt_j of the chunk in stage s (0 beyond the valid rows)
+  __device__ float* E(int s) const {
+    return reinterpret_cast<float*>(base + kOffTabs + s * kTabBytes + 512);
+  }
   // dt of the chunk in stage s (0 beyond the valid rows)
   __device__ __nv_bfloat16* dt(int s) const {
-    return reinterpret_cast<__nv_bfloat16*>(base + kOffTabs + s * kTabBytes + 512);
+    return reinterpret_cast<__nv_bfloat16*>(base + kOffTabs + s * kTabBytes + 1024);
   }
   __device__ TileInfo* info(int s) const {
     return reinterpret_cast<TileInfo*>(base + kOffInfo) + s;
@@ -240,21 +248,27 @@ enum {
   kMmaDone,
   kNumBars
 };
+static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
 
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_tc_fwd_kernel(const __grid_constant__ CUtensorMap map_x,
                       const __grid_constant__ CUtensorMap map_b,
                       const __grid_constant__ CUtensorMap map_c,
                       const __grid_constant__ CUtensorMap map_y, Params prm) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bars[kNumBars];
-  __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_sh;
-  Smem sm;
-  sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                       ~uintptr_t(1023));
+  // All shared memory is dynamic: the tiles need 1024-byte alignment and
+  // there is no room for a padding slack, so the base must come aligned.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (tid == 0) report(prm.status, SSD_ERR_UNSUPPORTED);
+    return;
+  }
+  Smem sm;
+  sm.base = smem_raw;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + kOffBars);
+  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem_raw + kOffBars + kBarBytes);
+  int* abort_p = reinterpret_cast<int*>(smem_raw + kOffBars + kBarBytes + 4);
 
   if (tid == 0) {
     mbar_init(&bars[kFull0], 2);  // expect-tx arrival + decay tables written
@@ -279,23 +293,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kSyncHand], kMathWarps);
     mbar_init(&bars[kMmaDone], 1);
     mbar_init(&bars[kYRead], kMathWarps);
-    abort_sh = 0;
+    *abort_p = 0;
     fence_mbar_init();
   }
   if (warp == kProducerWarp) {
-    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_alloc(tmem_base_p, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_base_sh;
-  volatile int* abort_v = &abort_sh;
+  const uint32_t tmem = *tmem_base_p;
+  volatile int* abort_v = abort_p;
 
   auto fail_at = [&](int code, int line) {
     report(prm.status, code);
     atomicCAS(prm.ticket + 1, 0, line);
-    atomicExch(&abort_sh, 1);
+    atomicExch(abort_p, 1);
   };
 #define fail(code) fail_at((code), __LINE__)
 
@@ -446,12 +460,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float excl = incl - run;
       float* c2t = sm.c2(st);
+      float* Et = sm.E(st);
       __nv_bfloat16* dtt = sm.dt(st);
+      // E[j] = exp(-cum_j) dt_j lets the mask and w o X use one table for
+      // every column: exp(cum_i - cum_j) dt_j = exp(cum_i) E[j].  Valid
+      // while the chunk's whole decay keeps both factors inside fp32
+      const float tot = __shfl_sync(0xffffffffu, incl, 31);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        c2t[4 * lane + q] = excl + pre[q];
+        const float cq2 = excl + pre[q];
+        c2t[4 * lane + q] = cq2;
+        Et[4 * lane + q] = fast_exp2(-cq2) * __bfloat162float(dv[q]);
         dtt[4 * lane + q] = dv[q];
       }
+      if (lane == 0) sm.info(st)->ez = fabsf(tot) < 120.f;
       __syncwarp();
       if (lane == 0) mbar_arrive(fb);
       ++it;
@@ -693,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of hi pairs followed by 8 columns of lo pairs, so a thread only
     // overwrites TMEM it has just read itself.  This warp owns blocks 2 cq
     // and 2 cq + 1 of its rows.
-    auto build_mask = [&](uint32_t pbt, int stg, float c2r, float Dh) -> bool {
+    auto build_mask = [&](uint32_t pbt, int stg, float c2r, float Dh, bool ez) -> bool {
       const float* c2 = sm.c2(stg);
       const __nv_bfloat16* dtt = sm.dt(stg);
       if (!wait_bar_warp(&bars[kCbFull0 + (pbt & 1)], (pbt >> 1) & 1)) return false;
@@ -708,6 +730,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 16; ++q) z[q] = 0u;
         tmem_st16(cbcol + j0, z);
         tmem_st16(cbcol + j0 + 16, z);
+      } else if (ez) {
+        // S[i][j] = G[i][j] exp(cum_i) E[j], E from the chunk's table
+        const float ei = fast_exp2(c2r);
+        const float* Et = sm.E(stg);
+        const bool diag = j0 == b;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          float g[16];
+          tmem_ld16(cbcol + j0 + 16 * half, g);
+          tmem_ld_wait();
+          tie16(g);
+          uint32_t pk[16];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int ja = j0 + 16 * half + 4 * m;
+            const float4 e4 = *reinterpret_cast<const float4*>(Et + ja);
+            float sv[4] = {g[4 * m] * (ei * e4.x), g[4 * m + 1] * (ei * e4.y),
+                           g[4 * m + 2] * (ei * e4.z), g[4 * m + 3] * (ei * e4.w)};
+            if (diag) {
+              // causal; the skip term D x rides on the diagonal: S[i][i] + D
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                sv[k] = ja + k < r ? sv[k] : (ja + k == r ? sv[k] + Dh : 0.f);
+            }
+            split2(sv[0], sv[1], pk[2 * m], pk[8 + 2 * m]);
+            split2(sv[2], sv[3], pk[2 * m + 1], pk[8 + 2 * m + 1]);
+          }
+          tmem_st16(cbcol + j0 + 16 * half, pk);
+        }
       } else {
         // exp(cum_i - cum_j) = exp(cum_i - cum_b) exp(cum_b - cum_j): the
         // row factor u is this thread's own, the column factor
@@ -922,20 +973,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       store_ht();
       MATH_TRY(arrive_seq(kHFull, bt));
 
-      // -------- pass B: the forward over the segment's chunks from H_in
+      // -------- pass B: the forward over the segment's chunks from H_in.
+      // Chunk t's mask is built two chunks ahead (at the end of iteration
+      // t - 2) and its w o X one chunk ahead, so the tensor core has chunk
+      // t+1's inputs while the math warps finish chunk t.  The values of a
+      // chunk needed after its stage is handed back (first token, length,
+      // decay, exp(cum)) are kept in registers.
       {
         MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
         const TileInfo* ci = sm.info(it & 1);
-        long long t0_cur = ci->t0;
-        int len_cur = ci->len;
         const int nB = ci->cnt;
         const int s_seq = ci->s, last_seg = ci->last_seg;
-        float c2l_cur, c2r_cur, dtr_cur;
-        chunk_vals(it & 1, c2l_cur, c2r_cur, dtr_cur);
-        MATH_TRY(build_mask(bt, it & 1, c2r_cur, Dh));
+        long long t0_cur = ci->t0;
+        int len_cur = ci->len;
+        float a_cur, ei_cur;
         {
+          float c2l, c2r, dtr;
+          chunk_vals(it & 1, c2l, c2r, dtr);
+          a_cur = fast_exp2(c2l);
+          ei_cur = fast_exp2(c2r);
+          MATH_TRY(build_mask(bt, it & 1, c2r, Dh, sm.info(it & 1)->ez != 0));
           uint32_t ph[8], pl[8];
-          compute_xw(it & 1, fast_exp2(c2l_cur - c2r_cur) * dtr_cur, ph, pl);
+          compute_xw(it & 1, fast_exp2(c2l - c2r) * dtr, ph, pl);
           MATH_TRY(release_stage(it));
           MATH_TRY(store_xw(ph, pl));
         }
@@ -945,25 +1004,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nhand;
           if (tid == 0) st_release(prm.flags + u_unit, 1);
         }
+        if (nB > 1) {
+          MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1));
+          float c2l, c2r, dtr;
+          chunk_vals((it + 1) & 1, c2l, c2r, dtr);
+          MATH_TRY(build_mask(bt + 1, (it + 1) & 1, c2r, Dh, sm.info((it + 1) & 1)->ez != 0));
+        }
+        long long t0_nxt = 0;
+        int len_nxt = 0;
+        float a_nxt = 0.f, ei_nxt = 0.f;
         for (int t = 0; t < nB; ++t) {
           const bool more = t + 1 < nB;
-          long long t0_nxt = 0;
-          int len_nxt = 0;
-          float c2l_nxt = 0.f, c2r_nxt = 0.f, dtr_nxt = 0.f;
-          if (more) {
-            // the next chunk's mask while the tensor core works on this one
-            MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1));
-            const TileInfo* ni = sm.info((it + 1) & 1);
-            t0_nxt = ni->t0;
-            len_nxt = ni->len;
-            chunk_vals((it + 1) & 1, c2l_nxt, c2r_nxt, dtr_nxt);
-            MATH_TRY(build_mask(bt + 1, (it + 1) & 1, c2r_nxt, Dh));
-          }
           // this chunk's accumulators: read and release them first so the
           // tensor core can start the next chunk's products
           MATH_TRY(wait_bar_warp(&bars[kAccFull], bt & 1));
           tc_fence_after();
-          const float ei = fast_exp2(c2r_cur);
+          const float ei = ei_cur;
           float* yrow = prm.y + ((t0_cur + r) * prm.H + h) * kP + 16 * cq;
           // y = Y_diag + exp(cum_i) (Y_off_hi + Y_off_lo), 8 columns (D x is
           // part of Y_diag: D sits on the diagonal of S).
@@ -1003,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             MATH_TRY(arrive_seq(kStFree, bt));
             // the state (it feeds the next chunk's C H^T)
-            const float a = fast_exp2(c2l_cur);
+            const float a = a_cur;
 #pragma unroll
             for (int q = 0; q < 16; ++q) hreg[q] = a * hreg[q] + sv[q];
           }
@@ -1051,21 +1107,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ypend = true;
           if (more) {
-            // the next chunk's w o X: its chunk-state MMA can start now
+            // chunk t+1 (its stage is still held): its values, and its w o X
+            // so its chunk-state product can start
+            const TileInfo* ni = sm.info((it + 1) & 1);
+            t0_nxt = ni->t0;
+            len_nxt = ni->len;
+            float c2l, c2r, dtr;
+            chunk_vals((it + 1) & 1, c2l, c2r, dtr);
+            a_nxt = fast_exp2(c2l);
+            ei_nxt = fast_exp2(c2r);
             uint32_t ph[8], pl[8];
-            compute_xw((it + 1) & 1, fast_exp2(c2l_nxt - c2r_nxt) * dtr_nxt, ph, pl);
+            compute_xw((it + 1) & 1, fast_exp2(c2l - c2r) * dtr, ph, pl);
             MATH_TRY(release_stage(it + 1));
             MATH_TRY(store_xw(ph, pl));
           }
+          if (t + 2 < nB) {
+            // chunk t+2's mask, in the stage chunk t has handed back
+            MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 2) & 1)], ((it + 2) >> 1) & 1));
+            float c2l, c2r, dtr;
+            chunk_vals((it + 2) & 1, c2l, c2r, dtr);
+            MATH_TRY(build_mask(bt + 2, (it + 2) & 1, c2r, Dh, sm.info((it + 2) & 1)->ez != 0));
+          }
           ++bt;
           ++it;
-          if (more) {
-            t0_cur = t0_nxt;
-            len_cur = len_nxt;
-            c2l_cur = c2l_nxt;
-            c2r_cur = c2r_nxt;
-            dtr_cur = dtr_nxt;
-          }
+          t0_cur = t0_nxt;
+          len_cur = len_nxt;
+          a_cur = a_nxt;
+          ei_cur = ei_nxt;
         }
       }
     }
