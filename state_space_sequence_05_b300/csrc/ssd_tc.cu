@@ -25,7 +25,7 @@
 // exact reordering of the recurrence), so every chunk_size the API accepts
 // runs with 128-token blocks here.
 //
-// Work partition.  Each sequence is cut into segments of kSeg chunks; a
+// Work partition.  Each sequence is cut into segments of 4-12 chunks; a
 // work unit is one (sequence, segment, head), handed out in that order by a
 // global ticket, so a unit's predecessor (same sequence and head, previous
 // segment) was always taken earlier by a running CTA.  A unit
@@ -106,9 +106,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
-// Chunks per segment: 8 chunks (1024 tokens) keep the segment-state pass
-// and the hand-off cheap while giving several units per SM on 8K tokens.
-constexpr int kSeg = 8;
+// Chunks per segment.  Dense batches take the length in [kSegMin, kSegMax]
+// that best fills the SMs with whole waves of units (see choose_seg);
+// packed sequences, whose lengths live on the device, take kSegVarlen.
+constexpr int kSegMin = 4, kSegMax = 12, kSegVarlen = 8;
 
 enum : int { kKindA = 0, kKindB = 1, kKindEnd = 2 };
 
@@ -1276,11 +1277,32 @@ int sm_count() {
   return n > 0 ? n : 148;
 }
 
-// Upper bound on the number of work units.
+// Segment length for a call: dense batches pick, among kSegMin..kSegMax,
+// the one whose units fill the SMs in the fewest chunk-steps (waves x
+// chunks per unit), preferring longer segments on a tie.
+int choose_seg(const FwdArgs& a) {
+  if (a.cu) return kSegVarlen;
+  const long long nt = ((long long)a.seqlen + kQ - 1) / kQ;
+  const long long nsm = sm_count();
+  int best = kSegMax;
+  long long best_cost = -1;
+  for (int sg = kSegMax; sg >= kSegMin; --sg) {
+    const long long units = (long long)a.batch * ((nt + sg - 1) / sg) * a.H;
+    const long long cost = ((units + nsm - 1) / nsm) * (nt < sg ? nt : sg);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = sg;
+    }
+  }
+  return best;
+}
+
+// Upper bound on the number of work units for any segment length a call
+// may choose.
 long long max_units(const FwdArgs& a) {
   const long long per = ((long long)a.seqlen + kQ - 1) / kQ;
-  if (a.cu) return (((per + a.nseq) + kSeg - 1) / kSeg + a.nseq) * a.H;
-  return (long long)a.batch * ((per + kSeg - 1) / kSeg) * a.H;
+  if (a.cu) return (((per + a.nseq) + kSegVarlen - 1) / kSegVarlen + a.nseq) * a.H;
+  return (long long)a.batch * ((per + kSegMin - 1) / kSegMin) * a.H;
 }
 
 struct WsLayout {
@@ -1315,7 +1337,8 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   float* slots = reinterpret_cast<float*>(ws + L.slots);
   const long long ntok = (long long)a.batch * a.seqlen;
   const long long mu = max_units(a);
-  tc_plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu, a.seqlen, (int)ntok, a.nseq, kSeg, a.H, uoff,
+  const int seg = choose_seg(a);
+  tc_plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu, a.seqlen, (int)ntok, a.nseq, seg, a.H, uoff,
                                            ticket, flags, mu, a.init, a.final_states,
                                            a.dev_status);
   count_launches(1);
@@ -1342,7 +1365,7 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   p.status = a.dev_status;
   p.H = a.H;
   p.G = a.G;
-  p.seg = kSeg;
+  p.seg = seg;
   p.y_v8 = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;

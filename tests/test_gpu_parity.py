@@ -247,3 +247,51 @@ def test_decode_steps_equal_forward():
     torch.cuda.synchronize()
     assert_close(torch.stack(ys, 1).cpu().numpy(), y.cpu().numpy(), 1e-2, "decode vs fwd y")
     assert_close(state.cpu().numpy(), fin.cpu().numpy(), 1e-2, "decode vs fwd state")
+
+
+def _with_decay(fi, A, dt_per_head, rng):
+    """The same inputs with A and dt replaced: dt[h] ~ dt_per_head[h] x (1 +/- 10%),
+    rounded to bf16 like every bf16 input."""
+    A = np.asarray(A, np.float32)
+    b, T, H = fi.dt.shape
+    dt = (np.asarray(dt_per_head, np.float32)[None, None, :] *
+          (1.0 + 0.1 * rng.uniform(-1, 1, (b, T, H)))).astype(np.float32)
+    fi.A = A
+    fi.bits["dt"], fi.dt = I.bf16_round(dt)
+    return fi
+
+
+def test_decay_regimes_on_the_tensor_path():
+    """One head per decay regime of the tensor-core mask: a chunk whose whole
+    decay fits the exp(-cum) dt table (dt 0.03), chunks too strong for the
+    table but with 32-token blocks that still factor (dt 0.08), blocks whose
+    own decay needs one exponential per entry (dt 0.3), and a nearly
+    undamped head (dt 1e-3).  A = -16 on every head."""
+    wl = I.small_workload(batch=2, seqlen=700, nheads=4, ngroups=2, chunk=128, seed=21)
+    fi = _with_decay(I.make_forward_inputs(wl), [-16.0] * 4, [0.03, 0.08, 0.3, 1e-3],
+                     np.random.default_rng(21))
+    _check_full(fi)
+
+
+def test_zero_decay_is_linear_attention_on_gpu():
+    """A = 0: no decay at all (the mask is the causal C B^T dt)."""
+    wl = I.small_workload(batch=1, seqlen=600, nheads=4, ngroups=1, chunk=128, seed=22)
+    fi = _with_decay(I.make_forward_inputs(wl), [0.0] * 4, [0.01, 0.02, 0.05, 0.1],
+                     np.random.default_rng(22))
+    _check_full(fi)
+
+
+@pytest.mark.parametrize("batch,T", [(3, 1500), (1, 4096), (6, 640)])
+def test_segment_lengths_chosen_per_shape(batch, T):
+    """Dense batches pick their segment length from the SM count and the
+    shape; each pick must give the same function."""
+    wl = I.small_workload(batch=batch, seqlen=T, nheads=8, ngroups=2, chunk=256,
+                          seed=400 + T)
+    fi = I.make_forward_inputs(wl)
+    heads = [0, 5]
+    y, fin = run_gpu(fi)
+    ref = oracle_heads(fi, heads)
+    y_np, f_np = y.cpu().numpy(), fin.cpu().numpy()
+    for (s, h), (yr, fr) in ref.items():
+        assert_close(gpu_seq(fi, y_np, s, h), yr, TOL["bf16"], f"y s{s} h{h}")
+        assert_close(f_np[s, h], fr, TOL["bf16"], f"final s{s} h{h}")
