@@ -314,6 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 #define fail(code) fail_at((code), __LINE__)
 
+  // the plan kernel's results (unit offsets, ticket, flags) are ready past
+  // this point (a no-op when the launch was not programmatic)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int nseq = prm.si.nseq;
   const int nunits = prm.uoff[nseq];
   const bool plan_ok = prm.uoff[nseq + 1] == 0;
@@ -1162,6 +1165,9 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* cu, int se
                                                        int* flags, long long max_units,
                                                        const float* init, float* final_states,
                                                        int32_t* dev_status) {
+  // the forward kernel may be scheduled now; it waits for this grid's
+  // completion before it reads anything written here
+  asm volatile("griddepcontrol.launch_dependents;");
   __shared__ int buf[32];
   __shared__ int carry, bad;
   if (threadIdx.x == 0) {
@@ -1338,17 +1344,14 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   const long long ntok = (long long)a.batch * a.seqlen;
   const long long mu = max_units(a);
   const int seg = choose_seg(a);
-  tc_plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu, a.seqlen, (int)ntok, a.nseq, seg, a.H, uoff,
-                                           ticket, flags, mu, a.init, a.final_states,
-                                           a.dev_status);
-  count_launches(1);
-  if (cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
-  if (ntok == 0 || mu == 0) return SSD_OK;
+  // everything the host prepares comes before the first launch, so the two
+  // kernels reach the GPU back to back
   CUtensorMap mx, mb, mc, my;
-  if (!make_map(&mx, a.x, ntok, (long long)a.H * kP) ||
-      !make_map(&mb, a.B, ntok, (long long)a.G * kN) ||
-      !make_map(&mc, a.C, ntok, (long long)a.G * kN) ||
-      !make_map_y(&my, a.y, ntok, (long long)a.H * kP))
+  const bool work = ntok > 0 && mu > 0;
+  if (work && (!make_map(&mx, a.x, ntok, (long long)a.H * kP) ||
+               !make_map(&mb, a.B, ntok, (long long)a.G * kN) ||
+               !make_map(&mc, a.C, ntok, (long long)a.G * kN) ||
+               !make_map_y(&my, a.y, ntok, (long long)a.H * kP)))
     return SSD_ERR_CUDA;
   Params p;
   p.dt = static_cast<const __nv_bfloat16*>(a.dt);
@@ -1374,8 +1377,28 @@ ssd_status_t tc_forward(const FwdArgs& a) {
                                     (int)kSmemBytes);
   });
   if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
+  tc_plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu, a.seqlen, (int)ntok, a.nseq, seg, a.H, uoff,
+                                           ticket, flags, mu, a.init, a.final_states,
+                                           a.dev_status);
+  count_launches(1);
+  if (cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
+  if (!work) return SSD_OK;
   const int grid = (int)(mu < sm_count() ? mu : sm_count());
-  ssd_tc_fwd_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(mx, mb, mc, my, p);
+  // Programmatic dependent launch: the forward kernel may start while the
+  // plan kernel runs; it waits for the plan's results (griddepcontrol.wait)
+  // after its own set-up (barriers, tensor memory, tensor-map prefetch).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, ssd_tc_fwd_kernel, mx, mb, mc, my, p) != cudaSuccess)
+    return SSD_ERR_CUDA;
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
