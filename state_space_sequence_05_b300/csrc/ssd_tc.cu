@@ -240,6 +240,7 @@ enum {
   kCbFull0, kCbFull1, kCbEmpty0, kCbEmpty1,  // C B^T / S buffers in TMEM
   kSFull0, kSFull1,                          // S written (math -> MMA), per S buffer
   kXwFull, kXwEmpty,                         // w o X buffer
+  kXwFull1, kXwEmpty1,                       // pass A's second w o X buffer (the H^T tiles)
   kHFull, kHEmpty,                           // H^T buffer
   kAccFull,                                  // Y_diag, Y_off, chunk state ready
   kStFree, kYoFree, kYdFree,                 // each accumulator read (math -> MMA)
@@ -284,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kSFull1], kMathWarps);
     mbar_init(&bars[kXwFull], kMathWarps);
     mbar_init(&bars[kXwEmpty], 1);
+    mbar_init(&bars[kXwFull1], kMathWarps);
+    mbar_init(&bars[kXwEmpty1], 1);
     mbar_init(&bars[kHFull], kMathWarps);
     mbar_init(&bars[kHEmpty], 1);
     mbar_init(&bars[kAccFull], 1);
@@ -504,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idSA = idesc_bf16(128, 128, true, true);
       constexpr uint32_t idYO = idesc_bf16(128, 128, false, true);
       constexpr uint32_t idYD = idesc_bf16(128, 64, false, true);
-      uint32_t it = 0, bt = 0, xu = 0, au = 0;
+      uint32_t it = 0, bt = 0, xu = 0, xu1 = 0, au = 0;
       bool issued = false;
 #define MMA_WAIT(bar, par)            \
   if (!wait_bar(&bars[bar], (par))) { \
@@ -548,24 +551,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           // product per K step (the two halves are summed when SA is read).
           // SA shares its columns with C H^T: the last forward chunk's must
           // have been read.
+          // The chunks alternate between the w o X tiles and the H^T tiles
+          // (H^T is not needed before the hand-off), so one chunk's w o X is
+          // written while the tensor core reads the previous one.
           if (inf.idx == 0 && bt >= 1) { MMA_WAIT(kYoFree, (bt - 1) & 1); }
-          MMA_WAIT(kXwFull, xu & 1);
+          const int xb = inf.idx & 1;
+          if (xb == 0) {
+            MMA_WAIT(kXwFull, xu & 1);
+          } else {
+            MMA_WAIT(kXwFull1, xu1 & 1);
+          }
           tc_fence_after();
           {
-            const uint32_t aXw = smem_u32(sm.Xw(0));
+            const uint32_t aXw = smem_u32(xb == 0 ? sm.Xw(0) : sm.Ht(0));
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               mma_bf16(tmem + kColSA, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
                        sdesc_sw128(aXw + k * 2048, kTile, 1024), idSA, inf.idx > 0 || k > 0);
           }
           issued = true;
-          mma_commit(&bars[kXwEmpty]);
+          mma_commit(&bars[xb == 0 ? kXwEmpty : kXwEmpty1]);
           mma_commit(&bars[kEmpty0 + st]);
           if (inf.idx == inf.cnt - 1) {
             mma_commit(&bars[kAggFull]);
             ++au;
           }
-          ++xu;
+          if (xb == 0) ++xu; else ++xu1;
           ++it;
           continue;
         }
@@ -686,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
     // use counters: ring chunk, forward chunk, w o X buffer, segment-state
     // accumulator, hand-off rendezvous
-    uint32_t it = 0, bt = 0, xu = 0, au = 0, nhand = 0;
+    uint32_t it = 0, bt = 0, xu = 0, xu1 = 0, au = 0, nhand = 0;
     uint32_t ny = 0;     // epilogues whose staged y this warp has released
     bool ypend = false;  // a y tile staged in the w o X buffer may still be read
     float hreg[16];  // fp32 state H[p][n = r], p = 16 cq + q
@@ -876,6 +887,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++xu;
       return true;
     };
+    // pass A's second w o X buffer: the H^T tiles, free until the hand-off
+    // (the last forward chunk's C H^T has completed: its accumulators were
+    // waited for)
+    auto store_xw1 = [&](const uint32_t (&ph)[8], const uint32_t (&pl)[8]) -> bool {
+      if (xu1 >= 1 && !wait_bar_warp(&bars[kXwEmpty1], (xu1 - 1) & 1)) return false;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t off = sw128_offset(r, 2 * cq + c);
+        *reinterpret_cast<uint4*>(sm.Ht(0) + off) =
+            make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+        *reinterpret_cast<uint4*>(sm.Ht(1) + off) =
+            make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      if (!arrive_seq(kXwFull1, xu1)) return false;
+      ++xu1;
+      return true;
+    };
     // the math warps are done reading the stage of ring chunk `pit`
     auto release_stage = [&](uint32_t pit) -> bool {
       return arrive_seq(kEmpty0 + (pit & 1), pit >> 1);
@@ -928,7 +957,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph[8], pl[8];
         compute_xw(it & 1, w, ph, pl);
         MATH_TRY(release_stage(it));
-        MATH_TRY(store_xw(ph, pl));
+        if ((k & 1) == 0) {
+          MATH_TRY(store_xw(ph, pl));
+        } else {
+          MATH_TRY(store_xw1(ph, pl));
+        }
         ++it;
       }
 
