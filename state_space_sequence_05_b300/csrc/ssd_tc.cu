@@ -406,17 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (have) {
         tile_of(U, k, nt0, nkind, nlen);
         load_dt(U, nt0, nlen);
-        if (lane == 0) {
-          // the next chunk's tiles into L2 while this one waits for its slot
-          const int nrow = (int)nt0;
-          if (nkind == kKindB) {
-            tma_prefetch_2d(&map_c, U.g * kN, nrow);
-            tma_prefetch_2d(&map_c, U.g * kN + 64, nrow);
-          }
-          tma_prefetch_2d(&map_b, U.g * kN, nrow);
-          tma_prefetch_2d(&map_b, U.g * kN + 64, nrow);
-          tma_prefetch_2d(&map_x, U.h * kP, nrow);
-        }
       }
       // hand this chunk over through stage it & 1
       const int st = it & 1;
@@ -451,6 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sm.B(st, 0), &map_b, fb, C.g * kN, row);
         tma_load_2d(sm.B(st, 1), &map_b, fb, C.g * kN + 64, row);
         tma_load_2d(sm.X(st), &map_x, fb, C.h * kP, row);
+        // the next chunk's x into L2, queued behind this chunk's loads (its
+        // C and B tiles are shared by every head and are usually there
+        // already)
+        if (have) tma_prefetch_2d(&map_x, U.h * kP, (int)nt0);
       }
       // decay table: lane l owns tokens 4l .. 4l+3
       float pre[4], run = 0.f;
