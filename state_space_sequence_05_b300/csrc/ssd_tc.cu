@@ -29,10 +29,11 @@
 // work unit is one (sequence, segment, head), handed out in that order by a
 // global ticket, so a unit's predecessor (same sequence and head, previous
 // segment) was always taken earlier by a running CTA.  A unit
-//   1. accumulates its segment's local state H_loc (the decayed sum of its
-//      chunk states, from a zero state) on the tensor cores, walking the
-//      chunks backwards so the decay to the segment end is a running sum --
-//      skipped for the last segment of a sequence;
+//   1. computes each chunk's state S_c = B^T (w o X) on the tensor cores,
+//      walking the chunks backwards, keeps them in a per-CTA scratch (L2-
+//      resident; every thread reloads only what it stored) and folds them
+//      into the segment-local state H_loc, the decayed sum of its chunk
+//      states from a zero state;
 //   2. takes the state entering the segment, H_in, from the initial state
 //      (first segment) or from its predecessor's published end state, and
 //      publishes its own end state exp(sum of the segment's dt A) H_in +
@@ -40,8 +41,9 @@
 //      CTAs at segment granularity, i.e. the composition of affine maps
 //      (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2) ("Mamba ... review",
 //      feghi.github.io, sec. 4);
-//   3. runs the forward over its chunks starting from H_in.
-// The state never leaves the SM between the chunks of a segment.
+//   3. runs the forward over its chunks starting from H_in, with
+//      H_c = exp(cum_last) H_{c-1} + S_c from the kept chunk states.
+// The running state never leaves the SM between the chunks of a segment.
 //
 // Roles (one persistent CTA per SM, 576 threads):
 //   warp 16    TMA producer: C, B, x tiles (128B swizzle) into a 2-stage ring,
@@ -96,11 +98,11 @@ constexpr uint32_t kSmemBytes = kOffBars + kBarBytes + 16;
 // TMEM columns (fp32 accumulators, 128 lanes).
 constexpr uint32_t kColCB = 0;     // 2 x 128: C B^T, overwritten in place by S (hi/lo pairs)
 constexpr uint32_t kColYD = 256;   // 64: S X
-constexpr uint32_t kColST = 320;   // 64: chunk state (lane n, column p)
 constexpr uint32_t kColYO = 384;   // 128: C H_hi^T | C H_lo^T
-constexpr uint32_t kColSA = 384;   // 128: segment-local state from the hi | lo halves of
-                                   // w o X (shares the columns of C H^T: the two are
-                                   // never live at once)
+// The segment-state pass puts each chunk's state product B^T [w o X hi |
+// w o X lo] (lane n, columns p of the hi half, then of the lo half) in the
+// columns of the two S buffers, alternating: S is not live during that pass.
+constexpr uint32_t kColSA = 0;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -110,6 +112,7 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 // that best fills the SMs with whole waves of units (see choose_seg);
 // packed sequences, whose lengths live on the device, take kSegVarlen.
 constexpr int kSegMin = 4, kSegMax = 12, kSegVarlen = 8;
+constexpr int kStSlots = kSegMax > kSegVarlen ? kSegMax : kSegVarlen;  // chunks per unit, at most
 
 enum : int { kKindA = 0, kKindB = 1, kKindEnd = 2 };
 
@@ -138,6 +141,7 @@ struct Params {
   int* ticket;          // ticket[0]: work ticket; ticket[1]: line of the first expired wait
   int* flags;           // per unit: 1 once its segment end state is published
   float* slots;         // per unit: segment end state [P][N] fp32
+  float* stbuf;         // per CTA: the current unit's chunk states, kStSlots x [P][N] fp32
   int32_t* status;
   int H, G, seg;
   int y_v8;             // y is 32-byte aligned: 32-byte stores
@@ -243,8 +247,8 @@ enum {
   kXwFull1, kXwEmpty1,                       // pass A's second w o X buffer (the H^T tiles)
   kHFull, kHEmpty,                           // H^T buffer
   kAccFull,                                  // Y_diag, Y_off, chunk state ready
-  kStFree, kYoFree, kYdFree,                 // each accumulator read (math -> MMA)
-  kAggFull,                                  // segment-local state accumulated
+  kYoFree, kYdFree,                          // each accumulator read (math -> MMA)
+  kSaFull0, kSaFull1, kSaFree0, kSaFree1,    // segment-state chunk products in TMEM
   kYRead,                                    // staged y tiles read by their TMA stores
   kSyncHand,                                 // math-warp rendezvous
   kMmaDone,
@@ -290,10 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kHFull], kMathWarps);
     mbar_init(&bars[kHEmpty], 1);
     mbar_init(&bars[kAccFull], 1);
-    mbar_init(&bars[kStFree], kMathWarps);
     mbar_init(&bars[kYoFree], kMathWarps);
     mbar_init(&bars[kYdFree], kMathWarps);
-    mbar_init(&bars[kAggFull], 1);
+    mbar_init(&bars[kSaFull0], 1);
+    mbar_init(&bars[kSaFull1], 1);
+    mbar_init(&bars[kSaFree0], kMathWarps);
+    mbar_init(&bars[kSaFree1], kMathWarps);
     mbar_init(&bars[kSyncHand], kMathWarps);
     mbar_init(&bars[kMmaDone], 1);
     mbar_init(&bars[kYRead], kMathWarps);
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       X.tb = X.sigma * prm.seg;
       X.te = min(nt, X.tb + prm.seg);
       X.last_seg = X.te == nt;
-      X.nA = X.last_seg ? 0 : X.te - X.tb;
+      X.nA = X.te - X.tb;  // every unit keeps its chunk states (pass A)
       X.nB = X.te - X.tb;
       return true;
     };
@@ -496,11 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idCB = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idST = idesc_bf16(128, 64, true, true);
       constexpr uint32_t idSA = idesc_bf16(128, 128, true, true);
       constexpr uint32_t idYO = idesc_bf16(128, 128, false, true);
       constexpr uint32_t idYD = idesc_bf16(128, 64, false, true);
-      uint32_t it = 0, bt = 0, xu = 0, xu1 = 0, au = 0;
+      uint32_t it = 0, bt = 0, xu = 0, xu1 = 0, sa = 0;
       bool issued = false;
 #define MMA_WAIT(bar, par)            \
   if (!wait_bar(&bars[bar], (par))) { \
@@ -521,17 +526,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&bars[kCbFull0 + (rbt & 1)]);
       };
-      // B^T (w o X) with the hi and lo halves of w o X into accumulator `col`
-      auto issue_state = [&](uint32_t col, uint32_t aB0, bool acc) {
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t aXw = smem_u32(sm.Xw(part));
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_bf16(col, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
-                     sdesc_sw128(aXw + k * 2048, kTile, 1024), idST, acc || part > 0 || k > 0);
-        }
-      };
       while (true) {
         const int st = it & 1;
         MMA_WAIT(kFull0 + st, (it >> 1) & 1);
@@ -540,55 +534,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t aB0 = smem_u32(sm.B(st, 0));
         if (inf.kind == kKindA) {
-          // segment-local state: SA (+)= B^T [w o X hi | w o X lo], one N = 128
-          // product per K step (the two halves are summed when SA is read).
-          // SA shares its columns with C H^T: the last forward chunk's must
-          // have been read.
-          // The chunks alternate between the w o X tiles and the H^T tiles
-          // (H^T is not needed before the hand-off), so one chunk's w o X is
-          // written while the tensor core reads the previous one.
-          if (inf.idx == 0 && bt >= 1) { MMA_WAIT(kYoFree, (bt - 1) & 1); }
+          // segment-state pass: this chunk's state B^T [w o X hi | w o X lo],
+          // one N = 128 product per K step, into the S columns (alternating
+          // between the two S buffers); the math warps sum the halves and
+          // keep the result.  The chunks also alternate between the w o X
+          // tiles and the H^T tiles (H^T is not needed before the hand-off),
+          // so one chunk's w o X is written while the tensor core reads the
+          // previous one.
+          if (inf.idx == 0) {
+            // the previous unit's last S X products read the S columns
+            if (bt >= 1) { MMA_WAIT(kCbEmpty0 + ((bt - 1) & 1), ((bt - 1) >> 1) & 1); }
+            if (bt >= 2) { MMA_WAIT(kCbEmpty0 + ((bt - 2) & 1), ((bt - 2) >> 1) & 1); }
+          }
           const int xb = inf.idx & 1;
           if (xb == 0) {
             MMA_WAIT(kXwFull, xu & 1);
           } else {
             MMA_WAIT(kXwFull1, xu1 & 1);
           }
+          if (sa >= 2) { MMA_WAIT(kSaFree0 + (sa & 1), ((sa >> 1) - 1) & 1); }
           tc_fence_after();
           {
             const uint32_t aXw = smem_u32(xb == 0 ? sm.Xw(0) : sm.Ht(0));
+            const uint32_t dcol = tmem + kColSA + (sa & 1) * 128;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              mma_bf16(tmem + kColSA, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
-                       sdesc_sw128(aXw + k * 2048, kTile, 1024), idSA, inf.idx > 0 || k > 0);
+              mma_bf16(dcol, sdesc_sw128(aB0 + k * 2048, kTile, 1024),
+                       sdesc_sw128(aXw + k * 2048, kTile, 1024), idSA, k > 0);
           }
           issued = true;
           mma_commit(&bars[xb == 0 ? kXwEmpty : kXwEmpty1]);
           mma_commit(&bars[kEmpty0 + st]);
-          if (inf.idx == inf.cnt - 1) {
-            mma_commit(&bars[kAggFull]);
-            ++au;
-          }
+          mma_commit(&bars[kSaFull0 + (sa & 1)]);
           if (xb == 0) ++xu; else ++xu1;
+          ++sa;
           ++it;
           continue;
         }
         // forward chunk: C B^T of this chunk if not issued ahead, then --
         // in whatever order their inputs become ready -- the next chunk's
-        // C B^T (so the math warps can build its mask early), the chunk
-        // state, C H^T and S X.  Nothing waits behind an input that is late.
+        // C B^T (so the math warps can build its mask early), C H^T and S X.
+        // The chunk state needs no product here: the segment-state pass
+        // kept it.  Nothing waits behind an input that is late.
         if (inf.idx == 0) {
           if (bt >= 2) { MMA_WAIT(kCbEmpty0 + (bt & 1), ((bt >> 1) - 1) & 1); }
+          // the segment-state products in the S columns have been read
+          if (sa >= 1) { MMA_WAIT(kSaFree0 + ((sa - 1) & 1), ((sa - 1) >> 1) & 1); }
+          if (sa >= 2) { MMA_WAIT(kSaFree0 + ((sa - 2) & 1), ((sa - 2) >> 1) & 1); }
           issue_cb(it, bt);
           issued = true;
         }
         const uint32_t aC0 = smem_u32(sm.C(st, 0)), aC1 = smem_u32(sm.C(st, 1));
         const uint32_t aX = smem_u32(sm.X(st));
         bool need_cb = inf.idx + 1 < inf.cnt;
-        bool need_st = true, need_yo = true, need_yd = true;
+        bool need_yo = true, need_yd = true;
         const unsigned long long tw = gtime();
         bool timed_out = false;
-        while (need_cb || need_st || need_yo || need_yd) {
+        while (need_cb || need_yo || need_yd) {
           bool progressed = false;
           if (need_cb && mbar_test_wait(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1) &&
               (bt + 1 < 2 ||
@@ -596,16 +598,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_cb(it + 1, bt + 1);
             need_cb = false;
-            progressed = true;
-          }
-          if (need_st && (bt < 1 || mbar_test_wait(&bars[kStFree], (bt - 1) & 1)) &&
-              mbar_test_wait(&bars[kXwFull], xu & 1)) {
-            // chunk state S_c^T = B^T (w o X)
-            tc_fence_after();
-            issue_state(tmem + kColST, aB0, false);
-            mma_commit(&bars[kXwEmpty]);
-            ++xu;
-            need_st = false;
             progressed = true;
           }
           if (need_yo && (bt < 1 || mbar_test_wait(&bars[kYoFree], (bt - 1) & 1)) &&
@@ -653,8 +645,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // scheduler keep its issue slots
             if (need_yd)
               (void)mbar_try_wait_hint(&bars[kYdFree], (bt - 1) & 1, 200);
-            else if (need_st)
-              (void)mbar_try_wait_hint(&bars[kXwFull], xu & 1, 200);
             else if (need_yo)
               (void)mbar_try_wait_hint(&bars[kHFull], bt & 1, 200);
             else
@@ -690,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
     // use counters: ring chunk, forward chunk, w o X buffer, segment-state
     // accumulator, hand-off rendezvous
-    uint32_t it = 0, bt = 0, xu = 0, xu1 = 0, au = 0, nhand = 0;
+    uint32_t it = 0, bt = 0, xu = 0, xu1 = 0, sa_m = 0, nhand = 0;
     uint32_t ny = 0;     // epilogues whose staged y this warp has released
     bool ypend = false;  // a y tile staged in the w o X buffer may still be read
     float hreg[16];  // fp32 state H[p][n = r], p = 16 cq + q
@@ -930,6 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = u0p->h;
       const int nA = u0p->nA;
       const int u_unit = u0p->unit, u_sigma = u0p->sigma, u_s = u0p->s;
+      const int u_last = u0p->last_seg;
       const float Dh = prm.D ? prm.D[h] : 0.f;
       // the initial state of a sequence's first segment is loaded now so its
       // latency hides behind the segment-state pass
@@ -939,24 +930,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 16; ++q) hreg[q] = ini ? __ldg(ini + (16 * cq + q) * kN + r) : 0.f;
       }
 
-      // -------- pass A: segment-local state, chunks walked backwards
-      float later = 0.f;  // sum of the log2-decays of the chunks after this one
+      // -------- pass A: the segment's chunk states, chunks walked backwards.
+      // Each chunk's state S_c (B^T (w o X) with the chunk-local weights w_j
+      // = exp(cum_last - cum_j) dt_j) is read back from TMEM, kept in this
+      // CTA's scratch (global memory, L2-resident; each thread reloads only
+      // what it stored) for the forward pass, and folded into the segment-
+      // local state H_loc = sum_c exp(sum of the later chunks' dt A) S_c.
+      float hloc[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) hloc[q] = 0.f;
+      float later = 0.f;  // sum of the log2-decays of the chunks folded so far
+      float* stb = prm.stbuf + (long long)blockIdx.x * kStSlots * kPN + (16 * cq) * kN + r;
+      // fold pass-A chunk `kk` (its product is in S-column buffer `sa_m & 1`)
+      auto fold = [&](int kk, float c2l_kk) -> bool {
+        if (!wait_bar_warp(&bars[kSaFull0 + (sa_m & 1)], (sa_m >> 1) & 1)) return false;
+        tc_fence_after();
+        float hi[16], lo[16];
+        const uint32_t col = tmem + kColSA + (sa_m & 1) * 128 + lane_addr + 16 * cq;
+        tmem_ld16(col, hi);
+        tmem_ld16(col + 64, lo);
+        tmem_ld_wait();
+        tie16(hi);
+        tie16(lo);
+        tc_fence_before();
+        if (!arrive_seq(kSaFree0 + (sa_m & 1), sa_m >> 1)) return false;
+        ++sa_m;
+        const float wl = fast_exp2(later);
+        float* dst = stb + (long long)(nA - 1 - kk) * kPN;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float sc = hi[q] + lo[q];
+          __stcg(dst + q * kN, sc);
+          hloc[q] += wl * sc;
+        }
+        later += c2l_kk;
+        return true;
+      };
+      float c2l_prev = 0.f;
       for (int k = 0; k < nA; ++k) {
         if (k > 0) MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
         float c2l, c2r, dtr;
         chunk_vals(it & 1, c2l, c2r, dtr);
-        const float w = fast_exp2(c2l - c2r + later) * dtr;
-        later += c2l;
         uint32_t ph[8], pl[8];
-        compute_xw(it & 1, w, ph, pl);
+        compute_xw(it & 1, fast_exp2(c2l - c2r) * dtr, ph, pl);
         MATH_TRY(release_stage(it));
         if ((k & 1) == 0) {
           MATH_TRY(store_xw(ph, pl));
         } else {
           MATH_TRY(store_xw1(ph, pl));
         }
+        // the previous chunk's product, read while this one's is computed
+        if (k > 0) MATH_TRY(fold(k - 1, c2l_prev));
+        c2l_prev = c2l;
         ++it;
       }
+      if (nA > 0) MATH_TRY(fold(nA - 1, c2l_prev));
 
       // -------- segment hand-off
       if (u_sigma != 0) {
@@ -977,26 +1005,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 16; ++q) hreg[q] = __ldcg(src + (16 * cq + q) * kN + r);
       }
-      if (nA > 0) {
-        // this segment's end state exp(sum dt A) H_in + H_loc, H_loc the sum
-        // of SA's hi and lo halves; the release flag follows once the first
-        // forward chunk is queued
-        MATH_TRY(wait_bar_warp(&bars[kAggFull], au & 1));
-        tc_fence_after();
-        float ha[16], hb[16];
-        tmem_ld16(tmem + kColSA + lane_addr + 16 * cq, ha);
-        tmem_ld16(tmem + kColSA + lane_addr + 64 + 16 * cq, hb);
-        tmem_ld_wait();
-        tie16(ha);
-        tie16(hb);
-        // SA is read: the first C H^T may overwrite it once H^T is in place
-        tc_fence_before();
+      if (!u_last) {
+        // this segment's end state exp(sum dt A) H_in + H_loc; the release
+        // flag follows once the first forward chunk is queued
         const float aseg = fast_exp2(later);
         float* dst = prm.slots + (long long)u_unit * kPN;
 #pragma unroll
         for (int q = 0; q < 16; ++q)
-          __stcg(dst + (16 * cq + q) * kN + r, aseg * hreg[q] + (ha[q] + hb[q]));
-        ++au;
+          __stcg(dst + (16 * cq + q) * kN + r, aseg * hreg[q] + hloc[q]);
       }
       // the running state H_in, split into bf16 hi/lo, to the B operand of C H^T
       if (bt >= 1) MATH_TRY(wait_bar_warp(&bars[kHEmpty], (bt - 1) & 1));
@@ -1005,10 +1021,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // -------- pass B: the forward over the segment's chunks from H_in.
       // Chunk t's mask is built two chunks ahead (at the end of iteration
-      // t - 2) and its w o X one chunk ahead, so the tensor core has chunk
-      // t+1's inputs while the math warps finish chunk t.  The values of a
-      // chunk needed after its stage is handed back (first token, length,
-      // decay, exp(cum)) are kept in registers.
+      // t - 2).  The values of a chunk needed after its stage is handed back
+      // (first token, length, decay, exp(cum)) are kept in registers; its
+      // state product comes from the scratch the segment-state pass filled.
       {
         MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
         const TileInfo* ci = sm.info(it & 1);
@@ -1023,12 +1038,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           a_cur = fast_exp2(c2l);
           ei_cur = fast_exp2(c2r);
           MATH_TRY(build_mask(bt, it & 1, c2r, Dh, sm.info(it & 1)->ez != 0));
-          uint32_t ph[8], pl[8];
-          compute_xw(it & 1, fast_exp2(c2l - c2r) * dtr, ph, pl);
           MATH_TRY(release_stage(it));
-          MATH_TRY(store_xw(ph, pl));
         }
-        if (nA > 0) {
+        if (!u_last) {
           __threadfence();
           MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1));
           ++nhand;
@@ -1045,8 +1057,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         float a_nxt = 0.f, ei_nxt = 0.f;
         for (int t = 0; t < nB; ++t) {
           const bool more = t + 1 < nB;
-          // this chunk's accumulators: read and release them first so the
-          // tensor core can start the next chunk's products
+          // this chunk's state product, from the segment-state pass (loaded
+          // first: its latency hides behind the wait for the accumulators)
+          float sv[16];
+          {
+            const float* srcs = stb + (long long)t * kPN;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) sv[q] = __ldcg(srcs + q * kN);
+          }
+          // this chunk's accumulators
           MATH_TRY(wait_bar_warp(&bars[kAccFull], bt & 1));
           tc_fence_after();
           const float ei = ei_cur;
@@ -1054,12 +1073,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // y = Y_diag + exp(cum_i) (Y_off_hi + Y_off_lo), 8 columns (D x is
           // part of Y_diag: D sits on the diagonal of S).
           // A warp whose 32 rows are all valid stages its 32 x 16 tile in
-          // the w o X buffer (free from the chunk-state product's end to the
-          // next chunk's w o X; 64B-swizzled rows, 2 KB per warp) and writes
-          // it with one TMA store; rows of a ragged last chunk are stored
-          // directly.
+          // the w o X buffer (unused during a forward pass; 64B-swizzled
+          // rows, 2 KB per warp, each warp its own) and writes it with one
+          // TMA store; rows of a ragged last chunk are stored directly.
           const bool tma_y = 32 * wq + 32 <= len_cur;
           uint8_t* ytile = sm.Xw(0) + warp * 2048;
+          if (tma_y) {
+            // this warp's previous tile must have been read by its store
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+          }
           auto emit_y = [&](int half, const float (&yd)[8], const float (&yh)[8],
                             const float (&yl)[8]) {
             float o[8];
@@ -1081,18 +1104,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           };
-          {
-            float sv[16];
-            tmem_ld16(tmem + kColST + lane_addr + 16 * cq, sv);
-            tmem_ld_wait();
-            tie16(sv);
-            tc_fence_before();
-            MATH_TRY(arrive_seq(kStFree, bt));
-            // the state (it feeds the next chunk's C H^T)
-            const float a = a_cur;
+          // the state (it feeds the next chunk's C H^T)
 #pragma unroll
-            for (int q = 0; q < 16; ++q) hreg[q] = a * hreg[q] + sv[q];
-          }
+          for (int q = 0; q < 16; ++q) hreg[q] = a_cur * hreg[q] + sv[q];
           if (more) {
             MATH_TRY(wait_bar_warp(&bars[kHEmpty], bt & 1));
             store_ht();
@@ -1137,8 +1151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ypend = true;
           if (more) {
-            // chunk t+1 (its stage is still held): its values, and its w o X
-            // so its chunk-state product can start
+            // chunk t+1 (its stage is still held; its mask is built): its
+            // values, then the stage goes back to the producer
             const TileInfo* ni = sm.info((it + 1) & 1);
             t0_nxt = ni->t0;
             len_nxt = ni->len;
@@ -1146,10 +1160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             chunk_vals((it + 1) & 1, c2l, c2r, dtr);
             a_nxt = fast_exp2(c2l);
             ei_nxt = fast_exp2(c2r);
-            uint32_t ph[8], pl[8];
-            compute_xw((it + 1) & 1, fast_exp2(c2l - c2r) * dtr, ph, pl);
             MATH_TRY(release_stage(it + 1));
-            MATH_TRY(store_xw(ph, pl));
           }
           if (t + 2 < nB) {
             // chunk t+2's mask, in the stage chunk t has handed back
@@ -1338,7 +1349,7 @@ long long max_units(const FwdArgs& a) {
 }
 
 struct WsLayout {
-  size_t uoff, ticket, flags, slots, total;
+  size_t uoff, ticket, flags, slots, stbuf, total;
 };
 
 WsLayout ws_layout(const FwdArgs& a) {
@@ -1348,7 +1359,8 @@ WsLayout ws_layout(const FwdArgs& a) {
   L.ticket = L.uoff + plan_bytes(a.nseq);
   L.flags = L.ticket + 256;
   L.slots = L.flags + align256(sizeof(int) * (size_t)mu);
-  L.total = L.slots + align256(sizeof(float) * (size_t)mu * kPN);
+  L.stbuf = L.slots + align256(sizeof(float) * (size_t)mu * kPN);
+  L.total = L.stbuf + align256(sizeof(float) * (size_t)sm_count() * kStSlots * kPN);
   return L;
 }
 
@@ -1367,6 +1379,7 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   int* ticket = reinterpret_cast<int*>(ws + L.ticket);
   int* flags = reinterpret_cast<int*>(ws + L.flags);
   float* slots = reinterpret_cast<float*>(ws + L.slots);
+  float* stbuf = reinterpret_cast<float*>(ws + L.stbuf);
   const long long ntok = (long long)a.batch * a.seqlen;
   const long long mu = max_units(a);
   const int seg = choose_seg(a);
@@ -1391,6 +1404,7 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   p.ticket = ticket;
   p.flags = flags;
   p.slots = slots;
+  p.stbuf = stbuf;
   p.status = a.dev_status;
   p.H = a.H;
   p.G = a.G;
