@@ -97,7 +97,7 @@ constexpr uint32_t kSmemBytes = kOffBars + kBarBytes + 16;
 
 // TMEM columns (fp32 accumulators, 128 lanes).
 constexpr uint32_t kColCB = 0;     // 2 x 128: C B^T, overwritten in place by S (hi/lo pairs)
-constexpr uint32_t kColYD = 256;   // 64: S X
+constexpr uint32_t kColYD = 256;   // 2 x 64: S X, double-buffered by forward chunk
 constexpr uint32_t kColYO = 384;   // 128: C H_hi^T | C H_lo^T
 // The segment-state pass puts each chunk's state product B^T [w o X hi |
 // w o X lo] (lane n, columns p of the hi half, then of the lo half) in the
@@ -247,7 +247,7 @@ enum {
   kXwFull1, kXwEmpty1,                       // pass A's second w o X buffer (the H^T tiles)
   kHFull, kHEmpty,                           // H^T buffer
   kAccFull,                                  // Y_diag, Y_off, chunk state ready
-  kYoFree, kYdFree,                          // each accumulator read (math -> MMA)
+  kYoFree, kYdFree0, kYdFree1,               // each accumulator read (math -> MMA)
   kSaFull0, kSaFull1, kSaFree0, kSaFree1,    // segment-state chunk products in TMEM
   kYRead,                                    // staged y tiles read by their TMA stores
   kSyncHand,                                 // math-warp rendezvous
@@ -295,7 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kHEmpty], 1);
     mbar_init(&bars[kAccFull], 1);
     mbar_init(&bars[kYoFree], kMathWarps);
-    mbar_init(&bars[kYdFree], kMathWarps);
+    mbar_init(&bars[kYdFree0], kMathWarps);
+    mbar_init(&bars[kYdFree1], kMathWarps);
     mbar_init(&bars[kSaFull0], 1);
     mbar_init(&bars[kSaFull1], 1);
     mbar_init(&bars[kSaFree0], kMathWarps);
@@ -618,7 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             need_yo = false;
             progressed = true;
           }
-          if (need_yd && (bt < 1 || mbar_test_wait(&bars[kYdFree], (bt - 1) & 1)) &&
+          if (need_yd &&
+              (bt < 2 || mbar_test_wait(&bars[kYdFree0 + (bt & 1)], ((bt >> 1) - 1) & 1)) &&
               mbar_test_wait(&bars[kSFull0 + (bt & 1)], (bt >> 1) & 1)) {
             // Y_diag = S X, S (hi, lo) read from TMEM: K block k (columns
             // j = 16k .. 16k+15 of S) holds 8 columns of hi pairs, then 8 of
@@ -629,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int part = 0; part < 2; ++part)
 #pragma unroll
               for (int k = 0; k < 8; ++k)
-                mma_bf16_tmem_a(tmem + kColYD, cbcol + 16 * k + 8 * part,
+                mma_bf16_tmem_a(tmem + kColYD + (bt & 1) * 64, cbcol + 16 * k + 8 * part,
                                 sdesc_sw128(aX + k * 2048, kTile, 1024), idYD,
                                 part > 0 || k > 0);
             need_yd = false;
@@ -644,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // rather than spin, so the math warps sharing this warp's
             // scheduler keep its issue slots
             if (need_yd)
-              (void)mbar_try_wait_hint(&bars[kYdFree], (bt - 1) & 1, 200);
+              (void)mbar_try_wait_hint(&bars[kSFull0 + (bt & 1)], (bt >> 1) & 1, 200);
             else if (need_yo)
               (void)mbar_try_wait_hint(&bars[kHFull], bt & 1, 200);
             else
@@ -1118,7 +1120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           {
             float yd[8], yh[8], yl[8];
-            tmem_ld8(tmem + kColYD + lane_addr + 16 * cq, yd);
+            tmem_ld8(tmem + kColYD + (bt & 1) * 64 + lane_addr + 16 * cq, yd);
             tmem_ld8(tmem + kColYO + lane_addr + 16 * cq, yh);
             tmem_ld8(tmem + kColYO + lane_addr + 64 + 16 * cq, yl);
             tmem_ld_wait();
@@ -1129,7 +1131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           {
             float yd[8], yh[8], yl[8];
-            tmem_ld8(tmem + kColYD + lane_addr + 16 * cq + 8, yd);
+            tmem_ld8(tmem + kColYD + (bt & 1) * 64 + lane_addr + 16 * cq + 8, yd);
             tmem_ld8(tmem + kColYO + lane_addr + 16 * cq + 8, yh);
             tmem_ld8(tmem + kColYO + lane_addr + 64 + 16 * cq + 8, yl);
             tmem_ld_wait();
@@ -1138,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tie8(yl);
             tc_fence_before();
             MATH_TRY(arrive_seq(kYoFree, bt));
-            MATH_TRY(arrive_seq(kYdFree, bt));
+            MATH_TRY(arrive_seq(kYdFree0 + (bt & 1), bt >> 1));
             emit_y(1, yd, yh, yl);
           }
           if (tma_y) {
