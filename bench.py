@@ -41,7 +41,7 @@ def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="l8k")
     ap.add_argument("--no-e2e", action="store_true")
@@ -278,21 +278,15 @@ def main():
         ssd.ssd_chunk_scan_fwd(d["x"], d["dt"], A, d["B"], d["C"], D, wl.chunk, init, cu, y=y,
                                final_states=fin, workspace=ws, dev_status=status, stream=stream)
 
+    # the clock sampler starts first, so the warm-up also covers its start
+    sampler = ClockSampler(dev.index)
+    sampler.start()
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         call()
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise SystemExit(f"device status {int(status.item())} after warm-up")
-
-    sampler = ClockSampler(dev.index)
-    sampler.start()
-    time.sleep(0.3)
-    # the GPU idled while the sampler started: two more untimed calls bring
-    # its clocks back before the timed region
-    for _ in range(2):
-        flush.zero_()
-        call()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:

@@ -13,12 +13,14 @@
 //   y          = Y_diag + exp(cum_i) Y_off + D_h x
 //   H_c        = exp(cum_last) H_{c-1} + S_c   (state passing)
 //
+// D_h x is folded into Y_diag: D_h sits on the diagonal of S.
+//
 // Precision: x, B and C arrive in bf16 and are used as they are.  The three
 // operands the kernel derives (S, w o X and H) are fp32 values; each is
-// written as a pair of bf16 numbers hi = bf16(v), lo = bf16(v - hi) and both
-// halves are multiplied into the same fp32 accumulator, so the products see
-// about 16 mantissa bits instead of 8.  (A single bf16 rounding of these
-// operands alone costs up to ~2.6e-2 of RMS(y) in max error.)
+// written as a pair of bf16 numbers, hi = v truncated to bf16 and lo = (v -
+// hi) truncated to bf16 (|v - hi - lo| < 2^-14 |v|), and both halves are
+// multiplied into the same fp32 accumulator.  (A single bf16 rounding of any
+// one of these operands costs about 1-5e-2 of RMS(y) in max error.)
 //
 // The chunk length is fixed at 128 = the tcgen05 tile height M.  Any chunk
 // size gives the same function up to rounding (the decomposition is an
@@ -1109,6 +1111,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the state (it feeds the next chunk's C H^T)
 #pragma unroll
           for (int q = 0; q < 16; ++q) hreg[q] = a_cur * hreg[q] + sv[q];
+          // this chunk state's lines are dead now (each 128-byte line is one
+          // p row of this warp's 32 n): drop them from L2 unwritten, so the
+          // scratch never costs DRAM write bandwidth
+          __syncwarp();
+          if (lane < 16) discard_l2_line(stb - lane + (long long)t * kPN + lane * kN);
           if (more) {
             MATH_TRY(wait_bar_warp(&bars[kHEmpty], bt & 1));
             store_ht();

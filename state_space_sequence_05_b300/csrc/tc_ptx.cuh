@@ -317,6 +317,12 @@ __device__ __forceinline__ void st_global_cs_v8(float* p, const float* v) {
                : "memory");
 }
 
+// Drops a 128-byte line from L2 without writing it back (its contents become
+// undefined); for scratch whose last reader is done with it.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128B-swizzled
 // tile whose rows are 128 bytes (the layout TMA writes with SWIZZLE_128B).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c) {
