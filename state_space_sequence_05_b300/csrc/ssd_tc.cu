@@ -426,6 +426,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__any_sync(0xffffffffu, *abort_v)) { ok = false; break; }
       uint64_t* fb = &bars[kFull0 + st];
       if (lane == 0) {
+        // the loads first (x, from DRAM, the slowest), the tile info after:
+        // the consumers read it only once this warp's table arrival lands
+        const int row = (int)t0;
+        mbar_arrive_expect_tx(fb, kind == kKindB ? kStageBytes : kStageBytesA);
+        tma_load_2d(sm.X(st), &map_x, fb, C.h * kP, row);
+        tma_load_2d(sm.B(st, 0), &map_b, fb, C.g * kN, row);
+        tma_load_2d(sm.B(st, 1), &map_b, fb, C.g * kN + 64, row);
+        if (kind == kKindB) {
+          tma_load_2d(sm.C(st, 0), &map_c, fb, C.g * kN, row);
+          tma_load_2d(sm.C(st, 1), &map_c, fb, C.g * kN + 64, row);
+        }
+        // the next chunk's x into L2, queued behind this chunk's loads (its
+        // C and B tiles are shared by every head and are usually there
+        // already)
+        if (have) tma_prefetch_2d(&map_x, U.h * kP, (int)nt0);
         TileInfo* inf = sm.info(st);
         inf->t0 = t0;
         inf->s = C.s;
@@ -438,21 +453,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         inf->cnt = kind == kKindA ? C.nA : C.nB;
         inf->nA = C.nA;
         inf->last_seg = C.last_seg;
-        const int row = (int)t0;
-        if (kind == kKindB) {
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          tma_load_2d(sm.C(st, 0), &map_c, fb, C.g * kN, row);
-          tma_load_2d(sm.C(st, 1), &map_c, fb, C.g * kN + 64, row);
-        } else {
-          mbar_arrive_expect_tx(fb, kStageBytesA);
-        }
-        tma_load_2d(sm.B(st, 0), &map_b, fb, C.g * kN, row);
-        tma_load_2d(sm.B(st, 1), &map_b, fb, C.g * kN + 64, row);
-        tma_load_2d(sm.X(st), &map_x, fb, C.h * kP, row);
-        // the next chunk's x into L2, queued behind this chunk's loads (its
-        // C and B tiles are shared by every head and are usually there
-        // already)
-        if (have) tma_prefetch_2d(&map_x, U.h * kP, (int)nt0);
       }
       // decay table: lane l owns tokens 4l .. 4l+3
       float pre[4], run = 0.f;
