@@ -21,6 +21,9 @@ Contents, all fp64:
   result, pinned against :func:`ssd_scan` in the tests.
 * :func:`linear_attention` -- the A = 0 special case, causal linear attention
   as a masked matrix product ("Transformers are SSMs Review", sec. 3-2 (2)).
+* :func:`s6_scan` -- the Mamba-1 selective scan (a decay per channel and
+  state), the sequential loop of "20.1 상태 공간 모델 (SSM)", sec. 5, in C;
+  :func:`s6_brute_force` restates it with explicit products of the decays.
 
 Readings shared by every function here (the pages leave them open): head h
 uses group ``floor(h*G/H)``; ``D`` is one scalar per head; a missing initial
@@ -65,6 +68,8 @@ def load_library(path):
     lib.oracle_ssd_scan.restype = ci
     lib.oracle_ssd_step.argtypes = [dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, dp]
     lib.oracle_ssd_step.restype = ci
+    lib.oracle_s6_scan.argtypes = [dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, dp, dp, dp, ci]
+    lib.oracle_s6_scan.restype = ci
     return lib
 
 
@@ -142,6 +147,72 @@ def ssd_step(state, x, dt, A, B, C, D=None, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_ssd_step rejected its arguments (rc={rc})")
     return y, st
+
+
+def s6_scan(x, dt, A, B, C, D=None, init=None, nthreads=None, lib=None):
+    """Mamba-1 selective scan, sequential fp64 loop.  Shapes:
+
+    x, dt [b, L, Dm]; A [Dm, N]; B, C [b, L, N]; D [Dm]; init [b, Dm, N].
+    Per channel d and state n: h = exp(dt_t[d] A[d,n]) h + dt_t[d] B_t[n] x_t[d],
+    y_t[d] = sum_n h[n] C_t[n] + D[d] x_t[d].  Returns ``(y [b,L,Dm],
+    final [b,Dm,N])`` as float64 arrays.
+    """
+    lib = lib or _load()
+    x, dt, A, B, C, D, init = map(_f64, (x, dt, A, B, C, D, init))
+    b, L, Dm = x.shape
+    N = A.shape[1]
+    assert dt.shape == (b, L, Dm) and A.shape == (Dm, N)
+    assert B.shape == (b, L, N) and C.shape == (b, L, N)
+    if D is not None:
+        assert D.shape == (Dm,)
+    if init is not None:
+        assert init.shape == (b, Dm, N)
+    y = np.empty((b, L, Dm), np.float64)
+    final = np.empty((b, Dm, N), np.float64)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = lib.oracle_s6_scan(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), b, L, Dm, N,
+                            _ptr(init), _ptr(y), _ptr(final), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_s6_scan rejected its arguments (rc={rc})")
+    return y, final
+
+
+def s6_brute_force(x, dt, A, B, C, D=None, init=None):
+    """The selective scan written out, pure Python, tiny inputs only:
+
+    y_i[d] = sum_n C_i[n] * ( sum_{j<=i} (prod_{k=j+1..i} exp(dt_k[d] A[d,n]))
+                               * dt_j[d] B_j[n] x_j[d]
+                              + (prod_{k<=i} exp(dt_k[d] A[d,n])) init[d,n] )
+             + D[d] x_i[d]
+    """
+    import math
+    x, dt, A, B, C, D, init = map(_f64, (x, dt, A, B, C, D, init))
+    b, L, Dm = x.shape
+    N = A.shape[1]
+    y = np.zeros((b, L, Dm))
+    for bi in range(b):
+        for d in range(Dm):
+            for i in range(L):
+                acc = 0.0
+                for n in range(N):
+                    a = [math.exp(float(dt[bi, k, d]) * float(A[d, n])) for k in range(L)]
+                    hn = 0.0
+                    for j in range(i + 1):
+                        dec = 1.0
+                        for k in range(j + 1, i + 1):
+                            dec *= a[k]
+                        hn += dec * float(dt[bi, j, d]) * float(B[bi, j, n]) * float(x[bi, j, d])
+                    if init is not None:
+                        dec = 1.0
+                        for k in range(i + 1):
+                            dec *= a[k]
+                        hn += dec * float(init[bi, d, n])
+                    acc += float(C[bi, i, n]) * hn
+                if D is not None:
+                    acc += float(D[d]) * float(x[bi, i, d])
+                y[bi, i, d] = acc
+    return y
 
 
 def _group_of(H, G):

@@ -1,6 +1,8 @@
 /*
  * ssd_oracle.c -- TEST INFRASTRUCTURE ONLY.  Plain, slow, fp64 CPU oracle of
- * the selective state-space recurrence that the SSD layer forward computes.
+ * the selective state-space recurrence that the SSD layer forward computes,
+ * and (oracle_s6_scan, at the end) of the Mamba-1 selective scan with a
+ * decay per channel and state.
  * Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg may
  * load this library.  It shares no code, header or constant with the CUDA
  * library; it does not include include/ssd.h.
@@ -188,4 +190,94 @@ int oracle_ssd_step(double *state, const double *x, const double *dt,
         }
     }
     return 0;
+}
+
+/*
+ * Selective scan with a decay per (channel, state): the S6 layer of Mamba-1,
+ * the sequential loop of "20.1 상태 공간 모델 (SSM)" (sungeuns.github.io),
+ * sec. 5 (Selective SSM forward), with an optional initial state added.
+ * Per batch row b, channel d in [0, Dm), state n in [0, N), fp64:
+ *
+ *     dA_t[d,n] = exp(dt_t[d] * A[d,n])                 (ZOH decay, A-bar)
+ *     h_t[d,n]  = dA_t[d,n] * h_{t-1}[d,n] + dt_t[d] * B_t[n] * x_t[d]
+ *     y_t[d]    = sum_n h_t[d,n] * C_t[n] + D[d] * x_t[d]
+ *
+ * The input term is dt B x (B-bar ~= dt B, the same section, sec. 1); y_t
+ * reads the updated state, as the loop does.  B and C are shared by all
+ * channels; dt is per channel.
+ * Layouts: x, dt, y [batch, seqlen, Dm]; A [Dm, N]; B, C [batch, seqlen, N];
+ * D [Dm] or NULL (0); init, final [batch, Dm, N] (init NULL: zero state).
+ */
+typedef struct {
+    const double *x, *dt, *A, *B, *C, *D, *init;
+    int batch, L, Dm, N;
+    double *y, *final_states;
+    int nthreads, tid;
+} s6_job;
+
+static void *s6_worker(void *arg) {
+    const s6_job *J = (const s6_job *)arg;
+    const int L = J->L, Dm = J->Dm, N = J->N;
+    double *h = (double *)malloc((size_t)N * sizeof(double));
+    if (!h) return (void *)1;
+    const int64_t units = (int64_t)J->batch * Dm;
+    for (int64_t u = J->tid; u < units; u += J->nthreads) {
+        const int b = (int)(u / Dm), d = (int)(u % Dm);
+        const double *Ad = J->A + (size_t)d * N;
+        const double Dd = J->D ? J->D[d] : 0.0;
+        for (int n = 0; n < N; ++n)
+            h[n] = J->init ? J->init[((size_t)b * Dm + d) * N + n] : 0.0;
+        for (int t = 0; t < L; ++t) {
+            const size_t bt = (size_t)b * L + t;
+            const double dtt = J->dt[bt * Dm + d];
+            const double xt = J->x[bt * Dm + d];
+            const double *Bt = J->B + bt * N;
+            const double *Ct = J->C + bt * N;
+            double acc = 0.0;
+            for (int n = 0; n < N; ++n) {
+                const double dA = exp(dtt * Ad[n]);
+                h[n] = dA * h[n] + dtt * Bt[n] * xt;
+                acc += h[n] * Ct[n];
+            }
+            J->y[bt * Dm + d] = acc + Dd * xt;
+        }
+        if (J->final_states)
+            memcpy(J->final_states + ((size_t)b * Dm + d) * N, h, (size_t)N * sizeof(double));
+    }
+    free(h);
+    return NULL;
+}
+
+/* Returns 0 on success, -1 on bad arguments, -2 on allocation failure. */
+int oracle_s6_scan(const double *x, const double *dt, const double *A, const double *B,
+                   const double *C, const double *D, int batch, int seqlen, int Dm, int N,
+                   const double *init, double *y, double *final_states, int nthreads) {
+    if (!x || !dt || !A || !B || !C || !y) return -1;
+    if (batch < 0 || seqlen < 0 || Dm <= 0 || N <= 0) return -1;
+    if (nthreads < 1) nthreads = 1;
+    s6_job *jobs = (s6_job *)calloc((size_t)nthreads, sizeof(s6_job));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs); free(th);
+        return -2;
+    }
+    for (int i = 0; i < nthreads; ++i) {
+        s6_job J = {x, dt, A, B, C, D, init, batch, seqlen, Dm, N, y, final_states, nthreads, i};
+        jobs[i] = J;
+    }
+    int rc = 0, started = 0;
+    for (int i = 1; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, s6_worker, &jobs[i]) != 0) break;
+        started = i;
+    }
+    if (s6_worker(&jobs[0]) != NULL) rc = -2;
+    for (int i = 1; i <= started; ++i) {
+        void *ret = NULL;
+        pthread_join(th[i], &ret);
+        if (ret != NULL) rc = -2;
+    }
+    for (int i = started + 1; i < nthreads; ++i)
+        if (s6_worker(&jobs[i]) != NULL) rc = -2;
+    free(jobs); free(th);
+    return rc;
 }

@@ -30,6 +30,15 @@ MUTANTS = {
     "init_index_transposed": ("memcpy(state, J->init + ((size_t)s * H + h) * PN",
                               "memcpy(state, J->init + ((size_t)h * J->nseq + s) * PN"),
     "decode_decay_missing": ("*e = a * *e + dtt * xt[p] * Bt[n];", "*e = *e + dtt * xt[p] * Bt[n];"),
+    # the selective scan (a decay per channel and state)
+    "s6_decay_of_state_0": ("const double dA = exp(dtt * Ad[n]);", "const double dA = exp(dtt * Ad[0]);"),
+    "s6_A_transposed": ("const double dA = exp(dtt * Ad[n]);",
+                        "const double dA = exp(dtt * J->A[(size_t)n * Dm + d]);"),
+    "s6_drop_dt_on_input": ("h[n] = dA * h[n] + dtt * Bt[n] * xt;", "h[n] = dA * h[n] + Bt[n] * xt;"),
+    "s6_y_before_update": ("                h[n] = dA * h[n] + dtt * Bt[n] * xt;\n                acc += h[n] * Ct[n];",
+                           "                acc += h[n] * Ct[n];\n                h[n] = dA * h[n] + dtt * Bt[n] * xt;"),
+    "s6_drop_skip_term": ("J->y[bt * Dm + d] = acc + Dd * xt;", "J->y[bt * Dm + d] = acc;"),
+    "s6_init_ignored": ("h[n] = J->init ? J->init[((size_t)b * Dm + d) * N + n] : 0.0;", "h[n] = 0.0;"),
 }
 
 
@@ -77,6 +86,19 @@ def _pins(lib):
         if oracle.rel_err(yt, yq[:, t]) > 1e-12:
             failed.append("decode_vs_quadratic")
             break
+    # selective scan vs its explicit-products restatement (distinct A per
+    # channel and state, Dm != N so a transposed A reads other values)
+    b6, L6, Dm, N6 = 2, 7, 3, 4
+    x6 = rng.standard_normal((b6, L6, Dm))
+    dt6 = rng.uniform(0.05, 0.6, (b6, L6, Dm))
+    A6 = -rng.uniform(0.2, 3.0, (Dm, N6))
+    B6 = rng.standard_normal((b6, L6, N6))
+    C6 = rng.standard_normal((b6, L6, N6))
+    D6 = rng.standard_normal(Dm)
+    i6 = rng.standard_normal((b6, Dm, N6))
+    y6, _ = oracle.s6_scan(x6, dt6, A6, B6, C6, D6, i6, lib=lib)
+    if oracle.rel_err(y6, oracle.s6_brute_force(x6, dt6, A6, B6, C6, D6, i6)) > 1e-12:
+        failed.append("s6_explicit_products")
     return failed
 
 
