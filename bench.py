@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-s6", action="store_true",
+                    help="skip the Mamba-1 selective-scan comparison")
     return ap.parse_args()
 
 
@@ -342,6 +344,10 @@ def main():
     if not args.no_decode:
         decode = measure_decode(dev, peaks)
 
+    s6 = None
+    if not args.no_s6 and wl.name == "l8k":
+        s6 = measure_s6(dev, peaks, ms * 1e3, flush)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(fi, wl)
@@ -356,7 +362,7 @@ def main():
                "launches_per_step": launches / max(1, args.steps),
                "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
                "step_ms_max": max(step_ms), "step_ms_first5": [round(v, 4) for v in step_ms[:5]],
-               "e2e": e2e, "cpu_baseline": cpu, "decode": decode,
+               "e2e": e2e, "cpu_baseline": cpu, "decode": decode, "s6": s6,
                "pages_claim": "SSD 2-8x faster than Mamba's fused selective scan (A100), context only"}
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -506,6 +512,71 @@ def measure_decode(dev, peaks, name="decode_b256"):
             "algorithmic_bytes_per_step": bytes_, "achieved_gbs": gbs,
             "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
             "gpu_launches": launches}
+
+
+# Special-function unit: 16 ex2 results per SM per clock (4 per sub-partition).
+MUFU_EX2_PER_SM_CLK = 16
+N_SMS = 148
+SM_MAX_MHZ = 2032
+
+
+def measure_s6(dev, peaks, ssd_us, flush, names=("s6_l8k_n16", "s6_l8k_n128"), reps=5):
+    """The Mamba-1 selective scan (a decay per channel and state) on two
+    workloads with the SSD layer workload's tokens (8192) and channels (80 x 64
+    = 5120): Mamba-1's usual 16 states and SSD's 128.  Median of `reps` calls,
+    L2 flushed before each.  Its bound is the special-function unit: one
+    exponential per (token, channel, state); `ssd_speedup` is this time over
+    the SSD layer forward's on this run."""
+    import torch
+    from state_space_sequence_05_b300 import inputs as I
+    from state_space_sequence_05_b300 import ssd
+    out = {}
+    stream = torch.cuda.current_stream()
+    for name in names:
+        f = I.make_s6_inputs(I.S6_WORKLOADS[name])
+        w = f.wl
+        d = {k: I.as_torch(getattr(f, k), f.bits.get(k), dev, w.dtype) for k in ("x", "dt", "B", "C")}
+        A = torch.from_numpy(f.A).to(dev)
+        D = torch.from_numpy(f.D).to(dev)
+        ini = None if f.init is None else torch.from_numpy(f.init).to(dev)
+        y = torch.empty((w.batch, w.seqlen, w.dmodel), device=dev, dtype=torch.float32)
+        fin = torch.empty((w.batch, w.dmodel, w.dstate), device=dev, dtype=torch.float32)
+
+        def call():
+            ssd.ssd_selective_scan_fwd(d["x"], d["dt"], A, d["B"], d["C"], D, ini, y=y,
+                                       final_states=fin, stream=stream)
+
+        for _ in range(2):
+            flush.zero_()
+            call()
+        torch.cuda.synchronize()
+        us = []
+        l0 = ssd.kernel_launches()
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us.append(1e3 * e0.elapsed_time(e1))
+        launches = ssd.kernel_launches() - l0
+        med = statistics.median(us)
+        b, L, Dm, N = w.batch, w.seqlen, w.dmodel, w.dstate
+        es = 2 if w.dtype == "bf16" else 4
+        exps = b * L * Dm * N
+        peak = N_SMS * MUFU_EX2_PER_SM_CLK * SM_MAX_MHZ * 1e6
+        bytes_ = (b * L * Dm * (2 * es + 4) + 2 * b * L * N * es + Dm * N * 4 + Dm * 4
+                  + 2 * b * Dm * N * 4)
+        out[name] = {
+            "workload": f"b{b} L{L} Dm{Dm} N{N} {w.dtype} in, fp32 y and states",
+            "us_median": med, "us_min": min(us), "tokens_per_s": b * L / (med * 1e-6),
+            "roofline": {"bound": "alu", "unit": "ex2/s", "achieved": exps / (med * 1e-6),
+                         "peak": peak, "frac": exps / (med * 1e-6) / peak,
+                         "peak_source": "148 SMs x 16 ex2 per SM per clock x 2032 MHz"},
+            "hbm_frac": bytes_ / (med * 1e-6) / 1e9 / peaks["hbm_gbs"],
+            "ssd_speedup": med / ssd_us, "gpu_launches": launches}
+    return out
 
 
 if __name__ == "__main__":

@@ -164,6 +164,34 @@ ssd_status_t ssd_state_update(float *state, const void *x, const void *dt, const
                               int nheads, int headdim, int dstate, int ngroups,
                               ssd_dtype_t in_dtype, float *y, void *stream);
 
+/*
+ * ssd_selective_scan_fwd -- the Mamba-1 selective scan (S6) forward, with a
+ * decay per channel and state: the sequential loop of "20.1 상태 공간 모델
+ * (SSM)" (sungeuns.github.io), sec. 5 (Selective SSM forward), with an
+ * optional initial state.  Per batch row, channel d and state n:
+ *
+ *     h_t[d,n] = exp(dt_t[d] * A[d,n]) * h_{t-1}[d,n] + dt_t[d] * B_t[n] * x_t[d]
+ *     y_t[d]   = sum_n h_t[d,n] * C_t[n] + D[d] * x_t[d]
+ *
+ * This is the layer that SSD restricts (A the same scalar for every state
+ * of a head); the library offers it so the two can be compared on the same
+ * GPU.  Inputs (`in_dtype` unless stated):
+ *   x, dt  [batch, seqlen, dmodel]   (dt already positive)
+ *   A      [dmodel, dstate] float32
+ *   B, C   [batch, seqlen, dstate]   (shared by every channel; 16-byte aligned)
+ *   D      [dmodel] float32 or NULL (0)
+ *   init_states float32 [batch, dmodel, dstate] or NULL (zero state)
+ * Outputs (float32): y [batch, seqlen, dmodel]; final_states
+ *   [batch, dmodel, dstate] or NULL.
+ * Supported: dstate in {16, 32, 64, 128, 256}, batch <= 65535.  One kernel
+ * launch, no workspace; the other conventions are those above.
+ */
+ssd_status_t ssd_selective_scan_fwd(const void *x, const void *dt, const float *A, const void *B,
+                                    const void *C, const float *D, const float *init_states,
+                                    int batch, int seqlen, int dmodel, int dstate,
+                                    ssd_dtype_t in_dtype, float *y, float *final_states,
+                                    void *stream);
+
 /* Short English text for a status code (static storage). */
 const char *ssd_status_string(ssd_status_t status);
 

@@ -157,4 +157,21 @@ ssd_status_t ssd_state_update(float* state, const void* x, const void* dt, const
                           in_dtype, y, static_cast<cudaStream_t>(stream));
 }
 
+ssd_status_t ssd_selective_scan_fwd(const void* x, const void* dt, const float* A, const void* B,
+                                    const void* C, const float* D, const float* init_states,
+                                    int batch, int seqlen, int dmodel, int dstate,
+                                    ssd_dtype_t in_dtype, float* y, float* final_states,
+                                    void* stream) {
+  if (in_dtype != SSD_DT_F32 && in_dtype != SSD_DT_BF16) return SSD_ERR_INVALID;
+  if (batch < 0 || seqlen < 0 || dmodel <= 0 || dstate <= 0) return SSD_ERR_INVALID;
+  if (!dstate_ok(dstate) || batch > 65535) return SSD_ERR_UNSUPPORTED;
+  if ((long long)batch * seqlen * dmodel >= (1LL << 40)) return SSD_ERR_UNSUPPORTED;
+  if (batch == 0) return SSD_OK;
+  if (!A) return SSD_ERR_INVALID;
+  if (seqlen > 0 && (!x || !dt || !B || !C || !y)) return SSD_ERR_INVALID;
+  if (!aligned16(B) || !aligned16(C)) return SSD_ERR_INVALID;
+  return ssd::s6_forward(x, dt, A, B, C, D, init_states, batch, seqlen, dmodel, dstate,
+                         in_dtype, y, final_states, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -66,6 +66,12 @@ bool tc_supported(const FwdArgs& a);
 size_t tc_workspace_bytes(const FwdArgs& a);
 ssd_status_t tc_forward(const FwdArgs& a);
 
+// Mamba-1 selective scan (a decay per channel and state), one launch.
+ssd_status_t s6_forward(const void* x, const void* dt, const float* A, const void* B,
+                        const void* C, const float* D, const float* init, int batch, int L,
+                        int Dm, int N, ssd_dtype_t dtype, float* y, float* final_states,
+                        cudaStream_t stream);
+
 // Decode step.
 ssd_status_t decode_step(float* state, const void* x, const void* dt, const float* A,
                          const void* B, const void* C, const float* D, int batch, int H, int P,

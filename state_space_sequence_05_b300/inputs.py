@@ -22,6 +22,12 @@ the rounded values.  A, D and the initial state stay fp32.
 
 Draw order from ``numpy.random.Generator(PCG64(seed))``: (varlen lengths),
 x, dt noise, B, C, A, D, dt bias u_h, initial state.
+
+The Mamba-1 selective scan (a decay per channel d and state n) uses the same
+recipe per channel instead of per head, except A[d, n] = -exp(A_log) with
+A_log ~ N(0, 1) elementwise, the parameterisation of the selective-SSM
+example in "20.1 상태 공간 모델 (SSM)", sec. 5.  Draw order: x, dt noise, B,
+C, A_log, D, dt bias u_d, initial state.
 """
 from __future__ import annotations
 
@@ -228,3 +234,62 @@ def as_torch(arr_f32: np.ndarray, bits: Optional[np.ndarray], device, dtype: str
     else:
         t = torch.from_numpy(np.ascontiguousarray(arr_f32, dtype=np.float32))
     return t.to(device)
+
+
+@dataclass(frozen=True)
+class S6Workload:
+    """Shape and dtype of one selective-scan problem."""
+    name: str
+    batch: int
+    seqlen: int
+    dmodel: int
+    dstate: int
+    dtype: str             # "f32" or "bf16": dtype of x, dt, B, C
+    init: str              # "zero" or "normal"
+    seed: int = 1010
+
+
+# The long workloads have the token count and channel count (80 heads x 64)
+# of the SSD layer workload, with Mamba-1's usual state size and with SSD's.
+S6_WORKLOADS = {
+    "s6_tiny_fp32": S6Workload("s6_tiny_fp32", 2, 128, 64, 16, "f32", "normal", 1010),
+    "s6_l8k_n16": S6Workload("s6_l8k_n16", 1, 8192, 5120, 16, "bf16", "normal", 1011),
+    "s6_l8k_n128": S6Workload("s6_l8k_n128", 1, 8192, 5120, 128, "bf16", "normal", 1012),
+}
+
+
+@dataclass
+class S6Inputs:
+    wl: S6Workload
+    x: np.ndarray          # [b, L, Dm]
+    dt: np.ndarray         # [b, L, Dm]
+    A: np.ndarray          # [Dm, N]
+    B: np.ndarray          # [b, L, N]
+    C: np.ndarray          # [b, L, N]
+    D: np.ndarray          # [Dm]
+    init: Optional[np.ndarray]   # [b, Dm, N] or None
+    bits: dict = field(default_factory=dict)
+
+
+def make_s6_inputs(wl: S6Workload, seed: Optional[int] = None) -> S6Inputs:
+    rng = np.random.Generator(np.random.PCG64(wl.seed if seed is None else seed))
+    b, L, Dm, N = wl.batch, wl.seqlen, wl.dmodel, wl.dstate
+    x = rng.standard_normal((b, L, Dm), dtype=np.float32)
+    noise = rng.standard_normal((b, L, Dm), dtype=np.float32) * np.float32(0.5)
+    Bm = rng.standard_normal((b, L, N), dtype=np.float32)
+    Cm = rng.standard_normal((b, L, N), dtype=np.float32)
+    A = (-np.exp(rng.standard_normal((Dm, N)))).astype(np.float32)
+    D = rng.standard_normal(Dm).astype(np.float32)
+    u = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), Dm))
+    dt = _softplus(noise.astype(np.float64) + _softplus_inv(u)[None, None, :]).astype(np.float32)
+    init = (rng.standard_normal((b, Dm, N), dtype=np.float32) * np.float32(0.1)
+            if wl.init == "normal" else None)
+    bits = {}
+    if wl.dtype == "bf16":
+        bits["x"], x = bf16_round(x)
+        bits["dt"], dt = bf16_round(dt)
+        bits["B"], Bm = bf16_round(Bm)
+        bits["C"], Cm = bf16_round(Cm)
+    elif wl.dtype != "f32":
+        raise ValueError(f"unknown dtype {wl.dtype}")
+    return S6Inputs(wl, x, dt, A, Bm, Cm, D, init, bits)

@@ -33,6 +33,8 @@ SIGNATURES = {
     "ssd_chunk_scan_fwd_workspace_size": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci]),
     "ssd_state_update": (_ci, [_fp, _vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci, _ci,
                                _fp, _vp]),
+    "ssd_selective_scan_fwd": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _ci, _ci, _ci, _ci, _ci,
+                                     _fp, _fp, _vp]),
     "ssd_status_string": (ctypes.c_char_p, [_ci]),
     "ssd_version": (_ci, []),
     "ssd_kernel_launches": (ctypes.c_uint64, []),
@@ -206,3 +208,47 @@ def ssd_state_update(state, x, dt, A, B, C, D=None, *, y=None, stream=None):
     if st != SSD_OK:
         raise SSDError(st, "ssd_state_update")
     return y
+
+
+def ssd_selective_scan_fwd(x, dt, A, B, C, D=None, init_states=None, *, y=None,
+                           final_states=None, return_final=True, stream=None):
+    """Mamba-1 selective scan (a decay per channel and state).  Shapes
+    (device tensors, contiguous):
+
+    x, dt [b, L, Dm] and B, C [b, L, N] -- all bfloat16 or all float32;
+    A [Dm, N], D [Dm] and init_states [b, Dm, N] float32.
+
+    Returns ``(y [b, L, Dm] float32, final_states [b, Dm, N] float32 or
+    None)``.  Raises SSDError on a host-side rejection.
+    """
+    lib = load_library()
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("ssd_selective_scan_fwd needs CUDA tensors")
+    if x.dim() != 3 or A.dim() != 2:
+        raise ValueError("x must be [batch, seqlen, dmodel] and A [dmodel, dstate]")
+    b, L, Dm = x.shape
+    N = A.shape[1]
+    code = _dtype_code(x)
+    _need(x, "x", dev)
+    _need(dt, "dt", dev, x.dtype, (b, L, Dm))
+    _need(B, "B", dev, x.dtype, (b, L, N))
+    _need(C, "C", dev, x.dtype, (b, L, N))
+    _need(A, "A", dev, torch.float32, (Dm, N))
+    if D is not None:
+        _need(D, "D", dev, torch.float32, (Dm,))
+    if init_states is not None:
+        _need(init_states, "init_states", dev, torch.float32, (b, Dm, N))
+    if y is None:
+        y = torch.empty((b, L, Dm), device=dev, dtype=torch.float32)
+    _need(y, "y", dev, torch.float32, (b, L, Dm))
+    if final_states is None and return_final:
+        final_states = torch.empty((b, Dm, N), device=dev, dtype=torch.float32)
+    if final_states is not None:
+        _need(final_states, "final_states", dev, torch.float32, (b, Dm, N))
+    st = lib.ssd_selective_scan_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                    _ptr(init_states), b, L, Dm, N, code, _ptr(y),
+                                    _ptr(final_states), _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_selective_scan_fwd")
+    return y, final_states
