@@ -108,13 +108,13 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []   # (arrival time, line)
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -123,9 +123,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def count_since(self, t0):
+        return sum(1 for t, _ in self.lines if t >= t0)
+
+    def stop(self, t0=None):
+        """Summary of the samples that arrived after time t0 (all if None)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -135,7 +139,9 @@ class ClockSampler:
             self.proc.kill()
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
+        for ta, l in self.lines:
+            if t0 is not None and ta < t0:
+                continue
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -287,6 +293,12 @@ def main():
         flush.zero_()
         call()
     torch.cuda.synchronize()
+    # the sampler is running (its first sample has arrived) before timing
+    tw = time.time()
+    while sampler.proc is not None and not sampler.lines and time.time() - tw < 10:
+        flush.zero_()
+        call()
+        torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise SystemExit(f"device status {int(status.item())} after warm-up")
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -294,6 +306,7 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    t_timed = time.time()
     launches0 = ssd.kernel_launches()
     for i in range(args.steps):
         flush.zero_()
@@ -304,7 +317,18 @@ def main():
     launches = ssd.kernel_launches() - launches0
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
+    # A short timed region may see no sample (one every 20 ms): the same
+    # calls continue, untimed, until 5 samples have arrived since the timed
+    # region began (at most 2 s); the summary covers exactly those samples.
+    in_region = sampler.count_since(t_timed)
+    te = time.time()
+    while (sampler.proc is not None and sampler.count_since(t_timed) < 5
+           and time.time() - te < 2):
+        flush.zero_()
+        call()
+        torch.cuda.synchronize()
+    clocks = sampler.stop(t_timed)
+    clocks["samples_in_timed_region"] = in_region
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = statistics.mean(step_ms)
     if world > 1:
