@@ -104,6 +104,46 @@ ssd_status_t ssd_chunk_scan_fwd(
     void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * Fused epilogue options of ssd_chunk_scan_fwd_ex: the steps on either side
+ * of the SSD layer in a Mamba block, done inside the forward kernel so that
+ * neither the positive dt nor the ungated y makes a round trip through HBM.
+ *  - dt_softplus != 0: the layer uses softplus(dt + dt_bias[h]) in place of
+ *    dt, where softplus(v) = log(1 + exp(v)); dt_bias [nheads] float32 or
+ *    NULL (0).  The step size of the selective SSM is a softplus of a
+ *    projection ("20.1 상태 공간 모델 (SSM)", sungeuns.github.io, sec. 2 and
+ *    the sec. 5 loop); dt then holds the projection without its bias.
+ *  - z != NULL: y is multiplied by silu(z) = z / (1 + exp(-z)) elementwise;
+ *    z [ntok, nheads, headdim] in `in_dtype`, 16-byte aligned.  The block's
+ *    second branch is a gate multiplied into the SSM output (the Mamba paper
+ *    review, feghi.github.io, sec. 5); the pages do not name the gate's
+ *    nonlinearity, SiLU is the reading taken here.
+ *  - y_bf16 != 0: y is written as bfloat16 (round to nearest even), halving
+ *    the largest output stream; `y` then points to bfloat16 storage.
+ * Zero-initialised options (or a NULL pointer) select none of them.
+ */
+typedef struct {
+    const float *dt_bias;
+    int dt_softplus;
+    const void *z;
+    int y_bf16;
+} ssd_fwd_epilogue_t;
+
+/*
+ * ssd_chunk_scan_fwd_ex -- ssd_chunk_scan_fwd with the fused epilogue
+ * options above (`epilogue` may be NULL).  Same arguments, layouts and errors;
+ * `y` is float32 or, with y_bf16, bfloat16.  Any option set requires the
+ * tensor-core configuration (bfloat16 inputs, headdim 64, dstate 128);
+ * other shapes return SSD_ERR_UNSUPPORTED and launch nothing.
+ */
+ssd_status_t ssd_chunk_scan_fwd_ex(
+    const void *x, const void *dt, const float *A, const void *B, const void *C,
+    const float *D, int batch, int seqlen, int nheads, int headdim, int dstate,
+    int ngroups, int chunk_size, ssd_dtype_t in_dtype, const float *init_states,
+    const int32_t *cu_seqlens, int nseq, void *y, float *final_states,
+    void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream,
+    const ssd_fwd_epilogue_t *epilogue);
+
+/*
  * ssd_chunk_scan_fwd_noalloc -- the same forward for callers that cannot
  * allocate device memory.  The pages have no counterpart: this entry point
  * exists for the deployment side only.  Some callers cannot call cudaMalloc

@@ -21,6 +21,9 @@ Contents, all fp64:
   result, pinned against :func:`ssd_scan` in the tests.
 * :func:`linear_attention` -- the A = 0 special case, causal linear attention
   as a masked matrix product ("Transformers are SSMs Review", sec. 3-2 (2)).
+* :func:`softplus`, :func:`silu_gate` -- the elementwise steps either side
+  of the layer in a Mamba block (positive step size, output gate), for the
+  fused-epilogue options.
 * :func:`s6_scan` -- the Mamba-1 selective scan (a decay per channel and
   state), the sequential loop of "20.1 상태 공간 모델 (SSM)", sec. 5, in C;
   :func:`s6_brute_force` restates it with explicit products of the decays.
@@ -363,6 +366,24 @@ def linear_attention(x, dt, B, C):
             Wm = np.tril(C[bi, :, g, :] @ B[bi, :, g, :].T) * dt[bi, None, :, h]
             y[bi, :, h, :] = Wm @ x[bi, :, h, :]
     return y
+
+
+def softplus(v):
+    """softplus(v) = log(1 + exp(v)), fp64: the step size of the selective SSM
+    is a softplus of a projection, which keeps it positive ("20.1 상태 공간
+    모델 (SSM)", sec. 2, and the same page's sec. 5 loop)."""
+    return np.logaddexp(0.0, np.asarray(v, dtype=np.float64))
+
+
+def silu_gate(y, z):
+    """y * silu(z), silu(z) = z / (1 + exp(-z)), fp64: the Mamba block's
+    second branch is a gate multiplied into the SSM output (the Mamba paper
+    review, sec. 5).  The page does not name the gate's nonlinearity; SiLU
+    is the reading taken.  exp(-z) overflowing to inf gives the correct limit
+    0 for very negative z."""
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return np.asarray(y, dtype=np.float64) * (z / (1.0 + np.exp(-z)))
 
 
 def rel_err(got, ref):

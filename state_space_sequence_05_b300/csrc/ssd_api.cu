@@ -104,6 +104,20 @@ ssd_status_t ssd_chunk_scan_fwd(const void* x, const void* dt, const float* A, c
                                 const int32_t* cu_seqlens, int nseq, float* y,
                                 float* final_states, void* workspace, size_t workspace_bytes,
                                 int32_t* dev_status, void* stream) {
+  return ssd_chunk_scan_fwd_ex(x, dt, A, B, C, D, batch, seqlen, nheads, headdim, dstate, ngroups,
+                               chunk_size, in_dtype, init_states, cu_seqlens, nseq, y,
+                               final_states, workspace, workspace_bytes, dev_status, stream,
+                               nullptr);
+}
+
+ssd_status_t ssd_chunk_scan_fwd_ex(const void* x, const void* dt, const float* A, const void* B,
+                                   const void* C, const float* D, int batch, int seqlen,
+                                   int nheads, int headdim, int dstate, int ngroups,
+                                   int chunk_size, ssd_dtype_t in_dtype, const float* init_states,
+                                   const int32_t* cu_seqlens, int nseq, void* y,
+                                   float* final_states, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_status, void* stream,
+                                   const ssd_fwd_epilogue_t* epilogue) {
   FwdArgs a{};
   a.x = x;
   a.dt = dt;
@@ -122,14 +136,26 @@ ssd_status_t ssd_chunk_scan_fwd(const void* x, const void* dt, const float* A, c
   a.init = init_states;
   a.cu = cu_seqlens;
   a.nseq = cu_seqlens ? nseq : batch;
-  a.y = y;
+  a.y = static_cast<float*>(y);
   a.final_states = final_states;
+  if (epilogue) {
+    a.dt_bias = epilogue->dt_bias;
+    a.dt_softplus = epilogue->dt_softplus != 0;
+    a.z = epilogue->z;
+    a.y_bf16 = epilogue->y_bf16 != 0;
+  }
   a.ws = workspace;
   a.ws_bytes = workspace_bytes;
   a.dev_status = dev_status;
   a.stream = static_cast<cudaStream_t>(stream);
   ssd_status_t st = check_fwd(a, true);
   if (st != SSD_OK) return st;
+  const bool fused = a.dt_softplus || a.z || a.y_bf16;
+  if (fused) {
+    // the fused epilogue exists on the tensor-core kernel only
+    if (!ssd::tc_supported(a)) return SSD_ERR_UNSUPPORTED;
+    if (!aligned16(a.z)) return SSD_ERR_INVALID;
+  }
   const size_t need = fwd_workspace(a);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))

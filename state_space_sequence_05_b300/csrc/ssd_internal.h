@@ -22,8 +22,13 @@ struct FwdArgs {
   const float* init;
   const int32_t* cu;
   int nseq;  // sequences: cu ? nseq : batch
-  float* y;
+  float* y;  // bfloat16 storage when y_bf16
   float* final_states;
+  // fused epilogue options (ssd_fwd_epilogue_t); zero = none
+  const float* dt_bias;
+  int dt_softplus;
+  const void* z;
+  int y_bf16;
   void* ws;
   size_t ws_bytes;
   int32_t* dev_status;

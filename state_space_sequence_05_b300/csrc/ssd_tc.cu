@@ -90,7 +90,7 @@ constexpr uint32_t kOffXw = kStages * kStageBytes;  // w o X as bf16 hi, lo (2 x
 constexpr uint32_t kOffHt = kOffXw + 2 * kTile;     // H^T as bf16 hi, lo (2 x 16 KB)
 // per stage: c2 fp32[128], E fp32[128], dt bf16[128]
 constexpr uint32_t kOffTabs = kOffHt + 2 * kTile;
-constexpr uint32_t kTabBytes = 128 * 4 + 128 * 4 + 128 * 2;
+constexpr uint32_t kTabBytes = 128 * 4 + 128 * 4 + 128 * 2;  // c2, E, dt (bf16)
 constexpr uint32_t kOffInfo = kOffTabs + kStages * kTabBytes;
 constexpr uint32_t kOffBars = kOffInfo + 2 * 64;
 // (barriers, then the TMEM base address and the abort flag)
@@ -149,6 +149,15 @@ struct Params {
   int y_v8;             // y is 32-byte aligned: 32-byte stores
 };
 
+// Fused epilogue options (ssd_fwd_epilogue_t), read by the epilogue kernel
+// variant only.
+struct EpiParams {
+  const float* dt_bias;         // [H] or null
+  const __nv_bfloat16* z;       // [tokens, H * kP] or null: y *= silu(z)
+  int dt_softplus;              // dt = softplus(dt + dt_bias[h]) in the tables
+  int y_bf16;                   // y stored as bf16 (round to nearest even)
+};
+
 __device__ __forceinline__ unsigned long long gtime() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -201,6 +210,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+// two floats rounded to bf16 (to nearest, ties to even), a in the low half
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // v ~= hi + lo: hi = v with its low 16 bits cleared (bf16 by truncation),
@@ -227,7 +241,11 @@ struct Smem {
   __device__ float* c2(int s) const {
     return reinterpret_cast<float*>(base + kOffTabs + s * kTabBytes);
   }
-  // E[j] = exp(-cum_j) dt_j of the chunk in stage s (0 beyond the valid rows)
+  // E[j] = exp(-cum_j) dt_j of the chunk in stage s (0 beyond the valid
+  // rows).  In the fused-epilogue variant, whose dt is an fp32 softplus, the
+  // slot holds E only when the tile info's `ez` is set (the chunk's decay
+  // range keeps E finite) and dt_j itself otherwise; the bf16 dt table below
+  // is then unused.
   __device__ float* E(int s) const {
     return reinterpret_cast<float*>(base + kOffTabs + s * kTabBytes + 512);
   }
@@ -258,11 +276,15 @@ enum {
 };
 static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
 
+// kEpi: the fused-epilogue variant (dt = softplus(dt + dt_bias), y *=
+// silu(z), bf16 y); it stores y directly instead of through the TMA staging
+// tiles.  The plain variant carries none of that code.
+template <bool kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_tc_fwd_kernel(const __grid_constant__ CUtensorMap map_x,
                       const __grid_constant__ CUtensorMap map_b,
                       const __grid_constant__ CUtensorMap map_c,
-                      const __grid_constant__ CUtensorMap map_y, Params prm) {
+                      const __grid_constant__ CUtensorMap map_y, Params prm, EpiParams ep) {
   // All shared memory is dynamic: the tiles need 1024-byte alignment and
   // there is no room for a padding slack, so the base must come aligned.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -404,9 +426,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ck = k;
       const long long t0 = nt0;
       const int kind = nkind, len = nlen;
-      __nv_bfloat16 dv[4];
+      float dv[4];
+      __nv_bfloat16 dpre_cur[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) dv[q] = dpre[q];
+      for (int q = 0; q < 4; ++q) {
+        dpre_cur[q] = dpre[q];
+        dv[q] = __bfloat162float(dpre[q]);
+      }
+      if constexpr (kEpi) if (ep.dt_softplus) {
+        // dt = softplus(dt + dt_bias[h]) on the valid rows (padding rows stay 0)
+        const float bias = ep.dt_bias ? ep.dt_bias[C.h] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float v = dv[q] + bias;
+          dv[q] = 4 * lane + q < len ? (v > 20.f ? v : log1pf(expf(v))) : 0.f;
+        }
+      }
       // advance, and start the next chunk's dt loads
       if (++k >= U.nA + U.nB) {
         k = 0;
@@ -458,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float pre[4], run = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        run += __bfloat162float(dv[q]) * C.A2;
+        run += dv[q] * C.A2;
         pre[q] = run;
       }
       float incl = run;
@@ -470,19 +505,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float excl = incl - run;
       float* c2t = sm.c2(st);
       float* Et = sm.E(st);
-      __nv_bfloat16* dtt = sm.dt(st);
       // E[j] = exp(-cum_j) dt_j lets the mask and w o X use one table for
       // every column: exp(cum_i - cum_j) dt_j = exp(cum_i) E[j].  Valid
       // while the chunk's whole decay keeps both factors inside fp32
       const float tot = __shfl_sync(0xffffffffu, incl, 31);
+      const bool ez = fabsf(tot) < 120.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float cq2 = excl + pre[q];
         c2t[4 * lane + q] = cq2;
-        Et[4 * lane + q] = fast_exp2(-cq2) * __bfloat162float(dv[q]);
-        dtt[4 * lane + q] = dv[q];
+        if constexpr (kEpi) {
+          Et[4 * lane + q] = ez ? fast_exp2(-cq2) * dv[q] : dv[q];
+        } else {
+          Et[4 * lane + q] = fast_exp2(-cq2) * dv[q];
+          sm.dt(st)[4 * lane + q] = dpre_cur[q];
+        }
       }
-      if (lane == 0) sm.info(st)->ez = fabsf(tot) < 120.f;
+      if (lane == 0) sm.info(st)->ez = ez;
       __syncwarp();
       if (lane == 0) mbar_arrive(fb);
       ++it;
@@ -703,12 +742,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    // this thread's decay values of the chunk in stage `stg`
-    auto chunk_vals = [&](int stg, float& c2l, float& c2r, float& dtr) {
+    // this thread's decay values of the chunk in stage `stg`: the chunk's
+    // total and row r's cumulative log2-decay, and row r's dt (the plain
+    // variant) or E-table entry (the fused-epilogue variant)
+    auto chunk_vals = [&](int stg, float& c2l, float& c2r, float& er) {
       const float* c2 = sm.c2(stg);
       c2l = c2[kQ - 1];
       c2r = c2[r];
-      dtr = __bfloat162float(sm.dt(stg)[r]);
+      if constexpr (kEpi)
+        er = sm.E(stg)[r];
+      else
+        er = __bfloat162float(sm.dt(stg)[r]);
     };
 
     // The decay mask S of forward chunk number `pbt`, written as bf16 hi/lo
@@ -719,7 +763,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and 2 cq + 1 of its rows.
     auto build_mask = [&](uint32_t pbt, int stg, float c2r, float Dh, bool ez) -> bool {
       const float* c2 = sm.c2(stg);
-      const __nv_bfloat16* dtt = sm.dt(stg);
       if (!wait_bar_warp(&bars[kCbFull0 + (pbt & 1)], (pbt >> 1) & 1)) return false;
       tc_fence_after();
       const uint32_t cbcol = tmem + kColCB + (pbt & 1) * 128 + lane_addr;
@@ -774,7 +817,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool direct = diag && !(fabsf(c2b - c2[b + 31]) < 120.f);
         if (!direct) {
           const float u = fast_exp2(c2r - c2b);
-          const float vl = fast_exp2(c2b - c2[j0 + lane]) * __bfloat162float(dtt[j0 + lane]);
+          // the chunk is not `ez` (in the fused-epilogue variant its E slot holds dt)
+          const float dtj = kEpi ? sm.E(stg)[j0 + lane] : __bfloat162float(sm.dt(stg)[j0 + lane]);
+          const float vl = fast_exp2(c2b - c2[j0 + lane]) * dtj;
 #pragma unroll 1
           for (int half = 0; half < 2; ++half) {
             float g[16];
@@ -812,11 +857,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               asm volatile("" ::: "memory");
               const int ja = j0 + 16 * half + 4 * m;
               const float4 cc = *reinterpret_cast<const float4*>(c2 + ja);
-              const uint2 dd = *reinterpret_cast<const uint2*>(dtt + ja);
-              const float s0 = ja <= r ? g[4 * m] * fast_exp2(c2r - cc.x) * bf_lo(dd.x) : 0.f;
-              const float s1 = ja + 1 <= r ? g[4 * m + 1] * fast_exp2(c2r - cc.y) * bf_hi(dd.x) : 0.f;
-              const float s2 = ja + 2 <= r ? g[4 * m + 2] * fast_exp2(c2r - cc.z) * bf_lo(dd.y) : 0.f;
-              const float s3 = ja + 3 <= r ? g[4 * m + 3] * fast_exp2(c2r - cc.w) * bf_hi(dd.y) : 0.f;
+              float dd[4];
+              if constexpr (kEpi) {
+                // the chunk is not `ez`: its E slot holds dt
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dd[q] = sm.E(stg)[ja + q];
+              } else {
+                const uint2 db = *reinterpret_cast<const uint2*>(sm.dt(stg) + ja);
+                dd[0] = bf_lo(db.x);
+                dd[1] = bf_hi(db.x);
+                dd[2] = bf_lo(db.y);
+                dd[3] = bf_hi(db.y);
+              }
+              const float s0 = ja <= r ? g[4 * m] * fast_exp2(c2r - cc.x) * dd[0] : 0.f;
+              const float s1 = ja + 1 <= r ? g[4 * m + 1] * fast_exp2(c2r - cc.y) * dd[1] : 0.f;
+              const float s2 = ja + 2 <= r ? g[4 * m + 2] * fast_exp2(c2r - cc.z) * dd[2] : 0.f;
+              const float s3 = ja + 3 <= r ? g[4 * m + 3] * fast_exp2(c2r - cc.w) * dd[3] : 0.f;
               const int dq = r - ja;
               const float d0 = dq == 0 ? Dh : 0.f, d1 = dq == 1 ? Dh : 0.f;
               const float d2 = dq == 2 ? Dh : 0.f, d3 = dq == 3 ? Dh : 0.f;
@@ -973,10 +1029,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       float c2l_prev = 0.f;
       for (int k = 0; k < nA; ++k) {
         if (k > 0) MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
-        float c2l, c2r, dtr;
-        chunk_vals(it & 1, c2l, c2r, dtr);
+        float c2l, c2r, er;
+        chunk_vals(it & 1, c2l, c2r, er);
         uint32_t ph[8], pl[8];
-        compute_xw(it & 1, fast_exp2(c2l - c2r) * dtr, ph, pl);
+        // w_r = exp(cum_last - cum_r) dt_r, from E (= exp(-cum_r) dt_r) when
+        // the chunk's table holds it, else from dt_r
+        float wr;
+        if constexpr (kEpi)
+          wr = fast_exp2(c2l - (sm.info(it & 1)->ez ? 0.f : c2r)) * er;
+        else
+          wr = fast_exp2(c2l - c2r) * er;
+        compute_xw(it & 1, wr, ph, pl);
         MATH_TRY(release_stage(it));
         if ((k & 1) == 0) {
           MATH_TRY(store_xw(ph, pl));
@@ -1037,8 +1100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int len_cur = ci->len;
         float a_cur, ei_cur;
         {
-          float c2l, c2r, dtr;
-          chunk_vals(it & 1, c2l, c2r, dtr);
+          float c2l, c2r, er;
+          chunk_vals(it & 1, c2l, c2r, er);
           a_cur = fast_exp2(c2l);
           ei_cur = fast_exp2(c2r);
           MATH_TRY(build_mask(bt, it & 1, c2r, Dh, sm.info(it & 1)->ez != 0));
@@ -1052,8 +1115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (nB > 1) {
           MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1));
-          float c2l, c2r, dtr;
-          chunk_vals((it + 1) & 1, c2l, c2r, dtr);
+          float c2l, c2r, er;
+          chunk_vals((it + 1) & 1, c2l, c2r, er);
           MATH_TRY(build_mask(bt + 1, (it + 1) & 1, c2r, Dh, sm.info((it + 1) & 1)->ez != 0));
         }
         long long t0_nxt = 0;
@@ -1069,6 +1132,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 16; ++q) sv[q] = __ldcg(srcs + q * kN);
           }
+          // the gate values of this thread's 16 outputs (epilogue variant)
+          uint4 zv[2];
+          if constexpr (kEpi) {
+            if (ep.z && r < len_cur) {
+              const uint4* zs = reinterpret_cast<const uint4*>(
+                  ep.z + (t0_cur + r) * ((long long)prm.H * kP) + h * kP + 16 * cq);
+              zv[0] = __ldg(zs);
+              zv[1] = __ldg(zs + 1);
+            } else {
+              zv[0] = make_uint4(0u, 0u, 0u, 0u);
+              zv[1] = zv[0];
+            }
+          }
           // this chunk's accumulators
           MATH_TRY(wait_bar_warp(&bars[kAccFull], bt & 1));
           tc_fence_after();
@@ -1080,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the w o X buffer (unused during a forward pass; 64B-swizzled
           // rows, 2 KB per warp, each warp its own) and writes it with one
           // TMA store; rows of a ragged last chunk are stored directly.
-          const bool tma_y = 32 * wq + 32 <= len_cur;
+          const bool tma_y = !kEpi && 32 * wq + 32 <= len_cur;
           uint8_t* ytile = sm.Xw(0) + warp * 2048;
           if (tma_y) {
             // this warp's previous tile must have been read by its store
@@ -1092,7 +1168,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             float o[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) o[c] = yd[c] + ei * (yh[c] + yl[c]);
-            if (tma_y) {
+            if constexpr (kEpi) {
+              if (r < len_cur) {
+                if (ep.z) {
+                  // gate: y * silu(z) = y * z / (1 + exp(-z))
+                  const uint32_t zw[4] = {zv[half].x, zv[half].y, zv[half].z, zv[half].w};
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) {
+                    const float zc = (c & 1) ? bf_hi(zw[c >> 1]) : bf_lo(zw[c >> 1]);
+                    o[c] *= zc / (1.f + fast_exp2(-zc * kLog2e));
+                  }
+                }
+                if (ep.y_bf16) {
+                  uint4 w;
+                  w.x = pack_bf16(o[0], o[1]);
+                  w.y = pack_bf16(o[2], o[3]);
+                  w.z = pack_bf16(o[4], o[5]);
+                  w.w = pack_bf16(o[6], o[7]);
+                  __stcs(reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(prm.y) +
+                                                  ((t0_cur + r) * prm.H + h) * kP + 16 * cq) + half, w);
+                } else if (prm.y_v8) {
+                  st_global_cs_v8(yrow + 8 * half, o);
+                } else {
+                  __stcs(reinterpret_cast<float4*>(yrow + 8 * half), make_float4(o[0], o[1], o[2], o[3]));
+                  __stcs(reinterpret_cast<float4*>(yrow + 8 * half + 4), make_float4(o[4], o[5], o[6], o[7]));
+                }
+              }
+            } else if (tma_y) {
 #pragma unroll
               for (int c = 0; c < 2; ++c) {
                 const int chunk = 2 * half + c;
@@ -1165,8 +1267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const TileInfo* ni = sm.info((it + 1) & 1);
             t0_nxt = ni->t0;
             len_nxt = ni->len;
-            float c2l, c2r, dtr;
-            chunk_vals((it + 1) & 1, c2l, c2r, dtr);
+            float c2l, c2r, er;
+            chunk_vals((it + 1) & 1, c2l, c2r, er);
             a_nxt = fast_exp2(c2l);
             ei_nxt = fast_exp2(c2r);
             MATH_TRY(release_stage(it + 1));
@@ -1174,8 +1276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t + 2 < nB) {
             // chunk t+2's mask, in the stage chunk t has handed back
             MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 2) & 1)], ((it + 2) >> 1) & 1));
-            float c2l, c2r, dtr;
-            chunk_vals((it + 2) & 1, c2l, c2r, dtr);
+            float c2l, c2r, er;
+            chunk_vals((it + 2) & 1, c2l, c2r, er);
             MATH_TRY(build_mask(bt + 2, (it + 2) & 1, c2r, Dh, sm.info((it + 2) & 1)->ez != 0));
           }
           ++bt;
@@ -1396,10 +1498,13 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   // kernels reach the GPU back to back
   CUtensorMap mx, mb, mc, my;
   const bool work = ntok > 0 && mu > 0;
+  // the fused-epilogue variant stores y directly (its map is never read)
+  const bool epi = a.z != nullptr || a.y_bf16 || a.dt_softplus;
   if (work && (!make_map(&mx, a.x, ntok, (long long)a.H * kP) ||
                !make_map(&mb, a.B, ntok, (long long)a.G * kN) ||
                !make_map(&mc, a.C, ntok, (long long)a.G * kN) ||
-               !make_map_y(&my, a.y, ntok, (long long)a.H * kP)))
+               (epi ? !make_map(&my, a.x, ntok, (long long)a.H * kP)
+                    : !make_map_y(&my, a.y, ntok, (long long)a.H * kP))))
     return SSD_ERR_CUDA;
   Params p;
   p.dt = static_cast<const __nv_bfloat16*>(a.dt);
@@ -1408,6 +1513,11 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   p.init = a.init;
   p.y = a.y;
   p.final_states = a.final_states;
+  EpiParams ep;
+  ep.dt_bias = a.dt_bias;
+  ep.dt_softplus = a.dt_softplus;
+  ep.z = static_cast<const __nv_bfloat16*>(a.z);
+  ep.y_bf16 = a.y_bf16;
   p.si = SeqInfo{a.cu, a.seqlen, a.nseq};
   p.uoff = uoff;
   p.ticket = ticket;
@@ -1422,8 +1532,11 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(ssd_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSmemBytes);
+    attr_err = cudaFuncSetAttribute(ssd_tc_fwd_kernel<false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(ssd_tc_fwd_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   });
   if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
   tc_plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu, a.seqlen, (int)ntok, a.nseq, seg, a.H, uoff,
@@ -1446,8 +1559,10 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, ssd_tc_fwd_kernel, mx, mb, mc, my, p) != cudaSuccess)
-    return SSD_ERR_CUDA;
+  const cudaError_t le =
+      epi ? cudaLaunchKernelEx(&cfg, ssd_tc_fwd_kernel<true>, mx, mb, mc, my, p, ep)
+          : cudaLaunchKernelEx(&cfg, ssd_tc_fwd_kernel<false>, mx, mb, mc, my, p, ep);
+  if (le != cudaSuccess) return SSD_ERR_CUDA;
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

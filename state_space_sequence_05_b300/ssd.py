@@ -25,9 +25,19 @@ SSD_DT_F32, SSD_DT_BF16 = 0, 1
 # Names and C signatures of every symbol include/ssd.h declares.
 _vp, _fp, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
 _ci, _sz = ctypes.c_int, ctypes.c_size_t
+
+
+class FwdEpilogue(ctypes.Structure):
+    """ssd_fwd_epilogue_t: the fused epilogue options of ssd_chunk_scan_fwd_ex."""
+    _fields_ = [("dt_bias", ctypes.c_void_p), ("dt_softplus", ctypes.c_int),
+                ("z", ctypes.c_void_p), ("y_bf16", ctypes.c_int)]
+
 SIGNATURES = {
     "ssd_chunk_scan_fwd": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci, _ci, _ci,
                                  _ci, _fp, _ip, _ci, _fp, _fp, _vp, _sz, _ip, _vp]),
+    "ssd_chunk_scan_fwd_ex": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci, _ci,
+                                    _ci, _ci, _fp, _ip, _ci, _vp, _fp, _vp, _sz, _ip, _vp,
+                                    ctypes.POINTER(FwdEpilogue)]),
     "ssd_chunk_scan_fwd_noalloc": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci,
                                          _ci, _ci, _ci, _fp, _ip, _ci, _fp, _fp, _ip, _vp]),
     "ssd_chunk_scan_fwd_workspace_size": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci]),
@@ -122,17 +132,23 @@ def ssd_chunk_scan_fwd_workspace_size(batch, seqlen, nheads, headdim, dstate, ng
 
 def ssd_chunk_scan_fwd(x, dt, A, B, C, D=None, chunk_size=256, init_states=None,
                        cu_seqlens=None, *, y=None, final_states=None, return_final=True,
-                       workspace=None, dev_status=None, stream=None):
+                       workspace=None, dev_status=None, stream=None, dt_bias=None,
+                       dt_softplus=False, z=None, y_dtype=torch.float32):
     """SSD layer forward.  Shapes (device tensors, contiguous):
 
     x [b, T, H, P], dt [b, T, H], B/C [b, T, G, N] -- all bfloat16 or all
     float32; A [H] and D [H] float32; init_states [nseq_or_b, H, P, N]
     float32; cu_seqlens int32 [nseq + 1] (then b must be 1).
 
-    Returns ``(y [b, T, H, P] float32, final_states [nseq_or_b, H, P, N]
-    float32 or None)``.  Raises SSDError on a host-side rejection.  Errors
-    only the device can detect go to ``dev_status`` (an int32 device tensor
-    of one element) when given.
+    Fused epilogue (ssd_chunk_scan_fwd_ex; tensor-core shapes only):
+    ``dt_softplus`` uses softplus(dt + dt_bias) for dt (dt_bias [H] float32
+    or None); ``z`` [b, T, H, P] multiplies y by silu(z); ``y_dtype``
+    torch.bfloat16 writes y as bf16.
+
+    Returns ``(y [b, T, H, P], final_states [nseq_or_b, H, P, N] float32 or
+    None)``.  Raises SSDError on a host-side rejection.  Errors only the
+    device can detect go to ``dev_status`` (an int32 device tensor of one
+    element) when given.
     """
     lib = load_library()
     dev = x.device
@@ -158,9 +174,16 @@ def ssd_chunk_scan_fwd(x, dt, A, B, C, D=None, chunk_size=256, init_states=None,
         nseq = cu_seqlens.shape[0] - 1
     if init_states is not None:
         _need(init_states, "init_states", dev, torch.float32, (nseq, H, P, N))
+    if y_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("y_dtype must be torch.float32 or torch.bfloat16")
+    if dt_bias is not None:
+        _need(dt_bias, "dt_bias", dev, torch.float32, (H,))
+    if z is not None:
+        _need(z, "z", dev, x.dtype, (b, T, H, P))
+    fused = bool(dt_softplus) or z is not None or y_dtype == torch.bfloat16
     if y is None:
-        y = torch.empty((b, T, H, P), device=dev, dtype=torch.float32)
-    _need(y, "y", dev, torch.float32, (b, T, H, P))
+        y = torch.empty((b, T, H, P), device=dev, dtype=y_dtype)
+    _need(y, "y", dev, y_dtype, (b, T, H, P))
     if final_states is None and return_final:
         final_states = torch.empty((nseq, H, P, N), device=dev, dtype=torch.float32)
     if final_states is not None:
@@ -170,12 +193,24 @@ def ssd_chunk_scan_fwd(x, dt, A, B, C, D=None, chunk_size=256, init_states=None,
     if workspace is None and need > 0:
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.ssd_chunk_scan_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), b, T, H, P,
-                                N, G, chunk_size, code, _ptr(init_states), _ptr(cu_seqlens), nseq,
-                                _ptr(y), _ptr(final_states), _ptr(workspace), ws_bytes,
-                                _ptr(dev_status), _stream_handle(stream))
+    if fused:
+        epi = FwdEpilogue(None if dt_bias is None else dt_bias.data_ptr(), int(bool(dt_softplus)),
+                          None if z is None else z.data_ptr(), int(y_dtype == torch.bfloat16))
+        st = lib.ssd_chunk_scan_fwd_ex(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), b, T,
+                                       H, P, N, G, chunk_size, code, _ptr(init_states),
+                                       _ptr(cu_seqlens), nseq, _ptr(y), _ptr(final_states),
+                                       _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                       _stream_handle(stream), ctypes.byref(epi))
+        where = "ssd_chunk_scan_fwd_ex"
+    else:
+        st = lib.ssd_chunk_scan_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), b, T,
+                                    H, P, N, G, chunk_size, code, _ptr(init_states),
+                                    _ptr(cu_seqlens), nseq, _ptr(y), _ptr(final_states),
+                                    _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                    _stream_handle(stream))
+        where = "ssd_chunk_scan_fwd"
     if st != SSD_OK:
-        raise SSDError(st, "ssd_chunk_scan_fwd")
+        raise SSDError(st, where)
     return y, final_states
 
 

@@ -259,3 +259,32 @@ def test_inputs_generator_recipe():
     lens = np.diff(vl.cu_seqlens)
     assert len(lens) == 64 and lens.min() >= 64 and lens.max() < 8192
     assert vl.x.shape[1] == vl.cu_seqlens[-1]
+
+
+def test_softplus_pins():
+    # softplus(0) = ln 2; softplus(v) - softplus(-v) = v; softplus(v) -> v for
+    # large v and -> exp(v) for very negative v
+    import math
+    assert oracle.softplus(0.0) == pytest.approx(math.log(2.0), rel=1e-15)
+    v = np.linspace(-30, 30, 121)
+    assert np.allclose(oracle.softplus(v) - oracle.softplus(-v), v, rtol=0, atol=1e-12)
+    assert oracle.softplus(50.0) == pytest.approx(50.0, rel=1e-15)
+    assert oracle.softplus(-40.0) == pytest.approx(math.exp(-40.0), rel=1e-12)
+    assert np.allclose(oracle.softplus(v), np.log1p(np.exp(v)), rtol=1e-13, atol=0)
+
+
+def test_silu_gate_pins():
+    # silu(0) = 0; silu(z) - silu(-z) = z; silu(z) -> z for large z, -> 0 for
+    # very negative z; the gate scales y linearly
+    z = np.linspace(-20, 20, 81)
+    one = np.ones_like(z)
+    assert oracle.silu_gate(1.0, 0.0) == 0.0
+    assert np.allclose(oracle.silu_gate(one, z) - oracle.silu_gate(one, -z), z, rtol=0, atol=1e-12)
+    assert oracle.silu_gate(1.0, 40.0) == pytest.approx(40.0, rel=1e-15)
+    assert abs(oracle.silu_gate(1.0, -40.0)) < 1e-15
+    assert np.allclose(oracle.silu_gate(3.0 * one, z), 3.0 * oracle.silu_gate(one, z), rtol=1e-15)
+    # silu(z) = z * sigmoid(z), with sigmoid(z) = (1 + tanh(z / 2)) / 2 (valid where
+    # the tanh form keeps its relative precision)
+    zz = np.linspace(-8, 20, 57)
+    assert np.allclose(oracle.silu_gate(np.ones_like(zz), zz), zz * 0.5 * (1 + np.tanh(zz / 2)),
+                       rtol=1e-12, atol=0)
