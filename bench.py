@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-epilogue", action="store_true",
+                    help="skip the fused-epilogue variant of the forward")
     ap.add_argument("--no-s6", action="store_true",
                     help="skip the Mamba-1 selective-scan comparison")
     return ap.parse_args()
@@ -368,6 +370,10 @@ def main():
     if not args.no_decode:
         decode = measure_decode(dev, peaks)
 
+    epilogue = None
+    if not args.no_epilogue and wl.cu_seqlens is None and wl.dtype == "bf16":
+        epilogue = measure_epilogue(fi, wl, dev, d, A, D, init, ws, flush, peaks)
+
     s6 = None
     if not args.no_s6 and wl.name == "l8k":
         s6 = measure_s6(dev, peaks, ms * 1e3, flush)
@@ -386,7 +392,7 @@ def main():
                "launches_per_step": launches / max(1, args.steps),
                "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
                "step_ms_max": max(step_ms), "step_ms_first5": [round(v, 4) for v in step_ms[:5]],
-               "e2e": e2e, "cpu_baseline": cpu, "decode": decode, "s6": s6,
+               "e2e": e2e, "cpu_baseline": cpu, "decode": decode, "epilogue": epilogue, "s6": s6,
                "pages_claim": "SSD 2-8x faster than Mamba's fused selective scan (A100), context only"}
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -535,6 +541,58 @@ def measure_decode(dev, peaks, name="decode_b256"):
             "tokens_per_s": b / (med * 1e-6), "graph_us_per_step": graph_us,
             "algorithmic_bytes_per_step": bytes_, "achieved_gbs": gbs,
             "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+            "gpu_launches": launches}
+
+
+def measure_epilogue(fi, wl, dev, d, A, D, init, ws, flush, peaks, reps=20):
+    """The same forward with every fused-epilogue option (ssd_chunk_scan_fwd_ex):
+    dt = softplus(dt + dt_bias) in the kernel, y *= silu(z), bf16 y.  The
+    extra inputs (a raw dt, a bias, z) are seeded; median of `reps` calls, L2
+    flushed before each.  Algorithmic bytes: x, dt, B, C, z read once (bf16),
+    bf16 y written once, fp32 states."""
+    import numpy as np
+    import torch
+    from state_space_sequence_05_b300 import inputs as I
+    from state_space_sequence_05_b300 import ssd
+    b, T, H, P, N, G = wl.batch, wl.seqlen, wl.nheads, wl.headdim, wl.dstate, wl.ngroups
+    rng = np.random.Generator(np.random.PCG64(wl.seed + 77))
+    dt_bits, _ = I.bf16_round(rng.standard_normal((b, T, H), dtype=np.float32) * np.float32(0.5)
+                              - np.float32(2.0))
+    z_bits, _ = I.bf16_round(rng.standard_normal((b, T, H, P), dtype=np.float32))
+    dt_raw = I.as_torch(None, dt_bits, dev, "bf16")
+    z = I.as_torch(None, z_bits, dev, "bf16")
+    bias = torch.from_numpy(rng.uniform(-2.0, 1.0, H).astype(np.float32)).to(dev)
+    y = torch.empty((b, T, H, P), device=dev, dtype=torch.bfloat16)
+    fin = torch.empty((b, H, P, N), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        ssd.ssd_chunk_scan_fwd(d["x"], dt_raw, A, d["B"], d["C"], D, wl.chunk, init, y=y,
+                               final_states=fin, workspace=ws, dt_bias=bias, dt_softplus=True,
+                               z=z, y_dtype=torch.bfloat16, stream=stream)
+
+    for _ in range(3):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    us = []
+    l0 = ssd.kernel_launches()
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us.append(1e3 * e0.elapsed_time(e1))
+    launches = ssd.kernel_launches() - l0
+    med = statistics.median(us)
+    ntok = b * T
+    bytes_ = (ntok * H * P * (2 + 2 + 2) + ntok * H * 2 + 2 * ntok * G * N * 2 + 2 * H * 4
+              + (2 if init is not None else 1) * b * H * P * N * 4)
+    return {"workload": f"{wl.name} with dt softplus(dt + bias), y * silu(z), bf16 y",
+            "us_median": med, "us_min": min(us), "tokens_per_s": ntok / (med * 1e-6),
+            "algorithmic_bytes": bytes_, "hbm_frac": bytes_ / (med * 1e-6) / 1e9 / peaks["hbm_gbs"],
             "gpu_launches": launches}
 
 
