@@ -371,7 +371,7 @@ def main():
         decode = measure_decode(dev, peaks)
 
     epilogue = None
-    if not args.no_epilogue and wl.cu_seqlens is None and wl.dtype == "bf16":
+    if not args.no_epilogue and fi.cu_seqlens is None and wl.dtype == "bf16":
         epilogue = measure_epilogue(fi, wl, dev, d, A, D, init, ws, flush, peaks)
 
     s6 = None
