@@ -108,6 +108,7 @@ constexpr uint32_t kColSA = 0;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
 // Chunks per segment.  Dense batches take the length in [kSegMin, kSegMax]
@@ -209,6 +210,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// log2 on the special-function unit (lg2.approx.ftz: absolute error ~2^-22
+// near 1)
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 // two floats rounded to bf16 (to nearest, ties to even), a in the low half
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -284,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ssd_tc_fwd_kernel(const __grid_constant__ CUtensorMap map_x,
                       const __grid_constant__ CUtensorMap map_b,
                       const __grid_constant__ CUtensorMap map_c,
-                      const __grid_constant__ CUtensorMap map_y, Params prm, EpiParams ep) {
+                      const __grid_constant__ CUtensorMap map_y,
+                      const __grid_constant__ CUtensorMap map_z, Params prm, EpiParams ep) {
   // All shared memory is dynamic: the tiles need 1024-byte alignment and
   // there is no room for a padding slack, so the base must come aligned.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -434,12 +444,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         dv[q] = __bfloat162float(dpre[q]);
       }
       if constexpr (kEpi) if (ep.dt_softplus) {
-        // dt = softplus(dt + dt_bias[h]) on the valid rows (padding rows stay 0)
+        // dt = softplus(dt + dt_bias[h]) on the valid rows (padding rows stay
+        // 0): softplus(v) = max(v, 0) + log(1 + e), e = exp(-|v|) in (0, 1];
+        // log(1 + e) = ln 2 * log2(1 + e), or e itself once e < 2^-12 (the
+        // next term, e^2 / 2, is below 2^-13 e)
         const float bias = ep.dt_bias ? ep.dt_bias[C.h] : 0.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float v = dv[q] + bias;
-          dv[q] = 4 * lane + q < len ? (v > 20.f ? v : log1pf(expf(v))) : 0.f;
+          const float e = fast_exp2(-fabsf(v) * kLog2e);
+          const float l1p = e < 0x1p-12f ? e : kLn2 * fast_log2(1.f + e);
+          dv[q] = 4 * lane + q < len ? fmaxf(v, 0.f) + l1p : 0.f;
         }
       }
       // advance, and start the next chunk's dt loads
@@ -476,6 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // C and B tiles are shared by every head and are usually there
         // already)
         if (have) tma_prefetch_2d(&map_x, U.h * kP, (int)nt0);
+        // the gate's z tile of a forward chunk, into L2 long before its epilogue
+        if constexpr (kEpi)
+          if (ep.z && kind == kKindB) tma_prefetch_2d(&map_z, C.h * kP, row);
         TileInfo* inf = sm.info(st);
         inf->t0 = t0;
         inf->s = C.s;
@@ -1154,9 +1172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // part of Y_diag: D sits on the diagonal of S).
           // A warp whose 32 rows are all valid stages its 32 x 16 tile in
           // the w o X buffer (unused during a forward pass; 64B-swizzled
-          // rows, 2 KB per warp, each warp its own) and writes it with one
-          // TMA store; rows of a ragged last chunk are stored directly.
-          const bool tma_y = !kEpi && 32 * wq + 32 <= len_cur;
+          // fp32 rows, 2 KB per warp, each warp its own; or plain 32-byte
+          // rows of a bf16 y) and writes it with one TMA store; rows of a
+          // ragged last chunk are stored directly.
+          const bool tma_y = 32 * wq + 32 <= len_cur;
           uint8_t* ytile = sm.Xw(0) + warp * 2048;
           if (tma_y) {
             // this warp's previous tile must have been read by its store
@@ -1169,32 +1188,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 8; ++c) o[c] = yd[c] + ei * (yh[c] + yl[c]);
             if constexpr (kEpi) {
-              if (r < len_cur) {
-                if (ep.z) {
-                  // gate: y * silu(z) = y * z / (1 + exp(-z))
-                  const uint32_t zw[4] = {zv[half].x, zv[half].y, zv[half].z, zv[half].w};
+              if (ep.z) {
+                // gate: y * silu(z) = y * z / (1 + exp(-z))
+                const uint32_t zw[4] = {zv[half].x, zv[half].y, zv[half].z, zv[half].w};
 #pragma unroll
-                  for (int c = 0; c < 8; ++c) {
-                    const float zc = (c & 1) ? bf_hi(zw[c >> 1]) : bf_lo(zw[c >> 1]);
-                    o[c] *= zc / (1.f + fast_exp2(-zc * kLog2e));
-                  }
-                }
-                if (ep.y_bf16) {
-                  uint4 w;
-                  w.x = pack_bf16(o[0], o[1]);
-                  w.y = pack_bf16(o[2], o[3]);
-                  w.z = pack_bf16(o[4], o[5]);
-                  w.w = pack_bf16(o[6], o[7]);
-                  __stcs(reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(prm.y) +
-                                                  ((t0_cur + r) * prm.H + h) * kP + 16 * cq) + half, w);
-                } else if (prm.y_v8) {
-                  st_global_cs_v8(yrow + 8 * half, o);
-                } else {
-                  __stcs(reinterpret_cast<float4*>(yrow + 8 * half), make_float4(o[0], o[1], o[2], o[3]));
-                  __stcs(reinterpret_cast<float4*>(yrow + 8 * half + 4), make_float4(o[4], o[5], o[6], o[7]));
+                for (int c = 0; c < 8; ++c) {
+                  const float zc = (c & 1) ? bf_hi(zw[c >> 1]) : bf_lo(zw[c >> 1]);
+                  o[c] *= zc / (1.f + fast_exp2(-zc * kLog2e));
                 }
               }
-            } else if (tma_y) {
+              if (ep.y_bf16) {
+                uint4 w;
+                w.x = pack_bf16(o[0], o[1]);
+                w.y = pack_bf16(o[2], o[3]);
+                w.z = pack_bf16(o[4], o[5]);
+                w.w = pack_bf16(o[6], o[7]);
+                if (tma_y) {
+                  *reinterpret_cast<uint4*>(ytile + lane * 32 + 16 * half) = w;
+                } else if (r < len_cur) {
+                  __stcs(reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(prm.y) +
+                                                  ((t0_cur + r) * prm.H + h) * kP + 16 * cq) + half, w);
+                }
+                return;
+              }
+            }
+            if (tma_y) {
 #pragma unroll
               for (int c = 0; c < 2; ++c) {
                 const int chunk = 2 * half + c;
@@ -1420,6 +1438,20 @@ bool make_map_y(CUtensorMap* m, float* ptr, long long rows, long long cols) {
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 y (the fused-epilogue option): a box is 16 columns (32 bytes) x 32
+// rows, unswizzled.
+bool make_map_y_bf16(CUtensorMap* m, void* ptr, long long rows, long long cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n = 0;
   static std::once_flag once;
@@ -1496,15 +1528,16 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   const int seg = choose_seg(a);
   // everything the host prepares comes before the first launch, so the two
   // kernels reach the GPU back to back
-  CUtensorMap mx, mb, mc, my;
+  CUtensorMap mx, mb, mc, my, mz;
   const bool work = ntok > 0 && mu > 0;
-  // the fused-epilogue variant stores y directly (its map is never read)
   const bool epi = a.z != nullptr || a.y_bf16 || a.dt_softplus;
   if (work && (!make_map(&mx, a.x, ntok, (long long)a.H * kP) ||
                !make_map(&mb, a.B, ntok, (long long)a.G * kN) ||
                !make_map(&mc, a.C, ntok, (long long)a.G * kN) ||
-               (epi ? !make_map(&my, a.x, ntok, (long long)a.H * kP)
-                    : !make_map_y(&my, a.y, ntok, (long long)a.H * kP))))
+               (a.y_bf16 ? !make_map_y_bf16(&my, a.y, ntok, (long long)a.H * kP)
+                         : !make_map_y(&my, a.y, ntok, (long long)a.H * kP)) ||
+               // z is only prefetched through its map (x stands in when absent)
+               !make_map(&mz, a.z ? a.z : a.x, ntok, (long long)a.H * kP)))
     return SSD_ERR_CUDA;
   Params p;
   p.dt = static_cast<const __nv_bfloat16*>(a.dt);
@@ -1560,8 +1593,8 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t le =
-      epi ? cudaLaunchKernelEx(&cfg, ssd_tc_fwd_kernel<true>, mx, mb, mc, my, p, ep)
-          : cudaLaunchKernelEx(&cfg, ssd_tc_fwd_kernel<false>, mx, mb, mc, my, p, ep);
+      epi ? cudaLaunchKernelEx(&cfg, ssd_tc_fwd_kernel<true>, mx, mb, mc, my, mz, p, ep)
+          : cudaLaunchKernelEx(&cfg, ssd_tc_fwd_kernel<false>, mx, mb, mc, my, mz, p, ep);
   if (le != cudaSuccess) return SSD_ERR_CUDA;
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
