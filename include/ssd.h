@@ -205,6 +205,41 @@ ssd_status_t ssd_state_update(float *state, const void *x, const void *dt, const
                               ssd_dtype_t in_dtype, float *y, void *stream);
 
 /*
+ * Context (sequence) parallelism: one sequence cut into R consecutive slices,
+ * one per device.  Each device runs ssd_chunk_scan_fwd on its slice from a
+ * zero state and keeps the slice's end state S_r (final_states) and its
+ * total log-decay a_r (ssd_segment_decay); the devices exchange these (an
+ * all-gather, the caller's collective); ssd_segment_combine composes the
+ * slices' affine maps h -> exp(a_r) h + S_r into the state entering each
+ * slice; a second ssd_chunk_scan_fwd from that state gives the exact y and
+ * end state of the slice.  The composition rule (a2, b2) o (a1, b1) =
+ * (a2 a1, a2 b1 + b2) is that of the Mamba paper review (feghi.github.io,
+ * sec. 4); passing states between blocks of the sequence is the SSD
+ * review's chunked algorithm (dimensionstp.github.io, sec. 3-2 (4)) at the
+ * scale of whole slices.
+ *
+ * ssd_segment_decay -- decay[b, h] = A[h] * sum_t dt[b, t, h] over the
+ *   slice.  dt [batch, seqlen, nheads] (in_dtype), A [nheads] float32,
+ *   decay [batch, nheads] float32.  One launch, no workspace.
+ */
+ssd_status_t ssd_segment_decay(const void *dt, const float *A, int batch, int seqlen, int nheads,
+                               ssd_dtype_t in_dtype, float *decay, void *stream);
+
+/*
+ * ssd_segment_combine -- the states entering R consecutive slices:
+ *   states_in[0] = init_states (NULL: zero), states_in[r + 1] =
+ *   exp(decay[r]) * states_in[r] + states[r], elementwise over
+ *   [batch, nheads, headdim, dstate].
+ *   decay [R, batch, nheads], states [R, batch, nheads, headdim, dstate],
+ *   init_states [batch, nheads, headdim, dstate] or NULL, states_in
+ *   [R + 1, batch, nheads, headdim, dstate], all float32.  states_in[R] is
+ *   the end state of the whole sequence.  One launch, no workspace.
+ */
+ssd_status_t ssd_segment_combine(const float *decay, const float *states,
+                                 const float *init_states, int nsegments, int batch, int nheads,
+                                 int headdim, int dstate, float *states_in, void *stream);
+
+/*
  * ssd_selective_scan_fwd -- the Mamba-1 selective scan (S6) forward, with a
  * decay per channel and state: the sequential loop of "20.1 상태 공간 모델
  * (SSM)" (sungeuns.github.io), sec. 5 (Selective SSM forward), with an

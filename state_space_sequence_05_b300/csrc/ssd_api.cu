@@ -183,6 +183,30 @@ ssd_status_t ssd_state_update(float* state, const void* x, const void* dt, const
                           in_dtype, y, static_cast<cudaStream_t>(stream));
 }
 
+ssd_status_t ssd_segment_decay(const void* dt, const float* A, int batch, int seqlen, int nheads,
+                               ssd_dtype_t in_dtype, float* decay, void* stream) {
+  if (in_dtype != SSD_DT_F32 && in_dtype != SSD_DT_BF16) return SSD_ERR_INVALID;
+  if (batch < 0 || seqlen < 0 || nheads <= 0) return SSD_ERR_INVALID;
+  if ((long long)batch * nheads >= (1LL << 31) || (long long)batch * seqlen >= (1LL << 31))
+    return SSD_ERR_UNSUPPORTED;
+  if (batch == 0) return SSD_OK;
+  if (!A || !decay || (seqlen > 0 && !dt)) return SSD_ERR_INVALID;
+  return ssd::segment_decay(dt, A, batch, seqlen, nheads, in_dtype, decay,
+                            static_cast<cudaStream_t>(stream));
+}
+
+ssd_status_t ssd_segment_combine(const float* decay, const float* states,
+                                 const float* init_states, int nsegments, int batch, int nheads,
+                                 int headdim, int dstate, float* states_in, void* stream) {
+  if (nsegments < 0 || batch < 0 || nheads <= 0 || headdim <= 0 || dstate <= 0)
+    return SSD_ERR_INVALID;
+  if ((long long)batch * nheads >= (1LL << 31)) return SSD_ERR_UNSUPPORTED;
+  if (batch == 0) return SSD_OK;
+  if (!states_in || (nsegments > 0 && (!decay || !states))) return SSD_ERR_INVALID;
+  return ssd::segment_combine(decay, states, init_states, nsegments, batch, nheads, headdim,
+                              dstate, states_in, static_cast<cudaStream_t>(stream));
+}
+
 ssd_status_t ssd_selective_scan_fwd(const void* x, const void* dt, const float* A, const void* B,
                                     const void* C, const float* D, const float* init_states,
                                     int batch, int seqlen, int dmodel, int dstate,

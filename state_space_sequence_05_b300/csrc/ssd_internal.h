@@ -77,6 +77,13 @@ ssd_status_t s6_forward(const void* x, const void* dt, const float* A, const voi
                         int Dm, int N, ssd_dtype_t dtype, float* y, float* final_states,
                         cudaStream_t stream);
 
+// Context parallelism: per-slice log-decay sums and the composition of the
+// slices' affine state maps.
+ssd_status_t segment_decay(const void* dt, const float* A, int batch, int T, int H,
+                           ssd_dtype_t dtype, float* a, cudaStream_t stream);
+ssd_status_t segment_combine(const float* a, const float* S, const float* init, int R, int batch,
+                             int H, int P, int N, float* h_in, cudaStream_t stream);
+
 // Decode step.
 ssd_status_t decode_step(float* state, const void* x, const void* dt, const float* A,
                          const void* B, const void* C, const float* D, int batch, int H, int P,

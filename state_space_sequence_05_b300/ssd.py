@@ -45,6 +45,8 @@ SIGNATURES = {
                                _fp, _vp]),
     "ssd_selective_scan_fwd": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _ci, _ci, _ci, _ci, _ci,
                                      _fp, _fp, _vp]),
+    "ssd_segment_decay": (_ci, [_vp, _fp, _ci, _ci, _ci, _ci, _fp, _vp]),
+    "ssd_segment_combine": (_ci, [_fp, _fp, _fp, _ci, _ci, _ci, _ci, _ci, _fp, _vp]),
     "ssd_status_string": (ctypes.c_char_p, [_ci]),
     "ssd_version": (_ci, []),
     "ssd_kernel_launches": (ctypes.c_uint64, []),
@@ -287,3 +289,47 @@ def ssd_selective_scan_fwd(x, dt, A, B, C, D=None, init_states=None, *, y=None,
     if st != SSD_OK:
         raise SSDError(st, "ssd_selective_scan_fwd")
     return y, final_states
+
+
+def ssd_segment_decay(dt, A, *, out=None, stream=None):
+    """Total log-decay of a slice, A[h] * sum_t dt[b, t, h]: dt [b, T, H]
+    (bfloat16 or float32), A [H] float32.  Returns [b, H] float32."""
+    lib = load_library()
+    dev = dt.device
+    if dev.type != "cuda" or dt.dim() != 3:
+        raise ValueError("dt must be a CUDA tensor [batch, seqlen, nheads]")
+    b, T, H = dt.shape
+    code = _dtype_code(dt)
+    _need(dt, "dt", dev)
+    _need(A, "A", dev, torch.float32, (H,))
+    if out is None:
+        out = torch.empty((b, H), device=dev, dtype=torch.float32)
+    _need(out, "out", dev, torch.float32, (b, H))
+    st = lib.ssd_segment_decay(_ptr(dt), _ptr(A), b, T, H, code, _ptr(out), _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_segment_decay")
+    return out
+
+
+def ssd_segment_combine(decay, states, init_states=None, *, out=None, stream=None):
+    """States entering R consecutive slices: decay [R, b, H], states [R, b,
+    H, P, N] (each slice's end state from a zero start), init_states [b, H,
+    P, N] or None.  Returns [R + 1, b, H, P, N] float32: out[0] = init,
+    out[r + 1] = exp(decay[r]) out[r] + states[r]."""
+    lib = load_library()
+    dev = states.device
+    if dev.type != "cuda" or states.dim() != 5:
+        raise ValueError("states must be a CUDA tensor [R, batch, nheads, headdim, dstate]")
+    R, b, H, P, N = states.shape
+    _need(states, "states", dev, torch.float32)
+    _need(decay, "decay", dev, torch.float32, (R, b, H))
+    if init_states is not None:
+        _need(init_states, "init_states", dev, torch.float32, (b, H, P, N))
+    if out is None:
+        out = torch.empty((R + 1, b, H, P, N), device=dev, dtype=torch.float32)
+    _need(out, "out", dev, torch.float32, (R + 1, b, H, P, N))
+    st = lib.ssd_segment_combine(_ptr(decay), _ptr(states), _ptr(init_states), R, b, H, P, N,
+                                 _ptr(out), _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_segment_combine")
+    return out
