@@ -5,8 +5,8 @@ this package.  The CUDA library and its Python binding never import it.
 """
 from .oracle import (brute_force, build, chunked_reference, linear_attention,
                      quadratic_form, rel_err, s6_brute_force, s6_scan, silu_gate, softplus,
-                     ssd_scan, ssd_step)
+                     ssd_bwd, ssd_scan, ssd_step)
 
 __all__ = ["brute_force", "build", "chunked_reference", "linear_attention",
            "quadratic_form", "rel_err", "s6_brute_force", "s6_scan", "silu_gate", "softplus",
-           "ssd_scan", "ssd_step"]
+           "ssd_bwd", "ssd_scan", "ssd_step"]

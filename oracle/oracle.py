@@ -24,6 +24,8 @@ Contents, all fp64:
 * :func:`softplus`, :func:`silu_gate` -- the elementwise steps either side
   of the layer in a Mamba block (positive step size, output gate), for the
   fused-epilogue options.
+* :func:`ssd_bwd` -- the backward of the layer (reverse-mode, in C),
+  pinned by finite differences of :func:`ssd_scan`.
 * :func:`s6_scan` -- the Mamba-1 selective scan (a decay per channel and
   state), the sequential loop of "20.1 상태 공간 모델 (SSM)", sec. 5, in C;
   :func:`s6_brute_force` restates it with explicit products of the decays.
@@ -73,6 +75,9 @@ def load_library(path):
     lib.oracle_ssd_step.restype = ci
     lib.oracle_s6_scan.argtypes = [dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, dp, dp, dp, ci]
     lib.oracle_s6_scan.restype = ci
+    lib.oracle_ssd_bwd.argtypes = [dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, dp, dp, dp,
+                                   dp, dp, dp, dp, dp, dp, dp]
+    lib.oracle_ssd_bwd.restype = ci
     return lib
 
 
@@ -150,6 +155,27 @@ def ssd_step(state, x, dt, A, B, C, D=None, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_ssd_step rejected its arguments (rc={rc})")
     return y, st
+
+
+def ssd_bwd(x, dt, A, B, C, D, init, dy, dfinal=None, lib=None):
+    """Backward of the SSD layer, batch mode, fp64 (reverse-mode derivative
+    of the recurrence of :func:`ssd_scan`, for dL/dy = dy and dL/dfinal =
+    dfinal).  Returns a dict with dx, ddt, dA, dB, dC, dD, dinit, shaped like
+    x, dt, A, B, C, A and the states."""
+    lib = lib or _load()
+    x, dt, A, B, C, D, init, dy, dfinal = map(_f64, (x, dt, A, B, C, D, init, dy, dfinal))
+    b, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    out = {"dx": np.empty_like(x), "ddt": np.empty_like(dt), "dA": np.empty(H),
+           "dB": np.empty_like(B), "dC": np.empty_like(C), "dD": np.empty(H),
+           "dinit": np.empty((b, H, P, N))}
+    rc = lib.oracle_ssd_bwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), b, T, H, P, N, G,
+                            _ptr(init), _ptr(dy), _ptr(dfinal), _ptr(out["dx"]), _ptr(out["ddt"]),
+                            _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+                            _ptr(out["dinit"]))
+    if rc != 0:
+        raise ValueError(f"oracle_ssd_bwd rejected its arguments (rc={rc})")
+    return out
 
 
 def s6_scan(x, dt, A, B, C, D=None, init=None, nthreads=None, lib=None):

@@ -281,3 +281,105 @@ int oracle_s6_scan(const double *x, const double *dt, const double *A, const dou
     free(jobs); free(th);
     return rc;
 }
+
+/*
+ * Backward of the SSD layer (reverse-mode derivative of the recurrence at
+ * the top of this file), fp64, single-threaded.  For a scalar loss L with
+ * dL/dy = dy and dL/dfinal = dfinal (NULL: 0), with G_t = dL/dh_t:
+ *
+ *     G_{T-1} = dfinal + dy_{T-1} C_{T-1}^T;  G_{t-1} = a_t G_t + dy_{t-1} C_{t-1}^T
+ *     dx_t[p] = dt_t sum_n G_t[p,n] B_t[n] + D dy_t[p]
+ *     dB_t[n] += dt_t sum_p G_t[p,n] x_t[p]          (summed over the group's heads)
+ *     dC_t[n] += sum_p dy_t[p] h_t[p,n]              (summed over the group's heads)
+ *     ddt_t    = sum_{p,n} G_t[p,n] (A a_t h_{t-1}[p,n] + x_t[p] B_t[n])
+ *     dA      += sum_t dt_t a_t sum_{p,n} G_t[p,n] h_{t-1}[p,n]
+ *     dD      += sum_t sum_p dy_t[p] x_t[p]
+ *     dinit    = a_0 G_0                               (= dL/dh_{-1})
+ *
+ * with a_t = exp(dt_t A), h_{-1} = init (or 0).  Batch mode only.  Layouts as
+ * the forward: dy, dx [batch*seqlen, H, P]; ddt [batch*seqlen, H]; dB, dC
+ * [batch*seqlen, G, N]; dA, dD [H]; dfinal, dinit [batch, H, P, N].  dD and
+ * dinit may be NULL.  Returns 0, -1 (bad arguments) or -2 (allocation).
+ */
+int oracle_ssd_bwd(const double *x, const double *dt, const double *A, const double *B,
+                   const double *C, const double *D, int batch, int seqlen, int H, int P, int N,
+                   int G, const double *init, const double *dy, const double *dfinal,
+                   double *dx, double *ddt, double *dA, double *dB, double *dC, double *dD,
+                   double *dinit) {
+    if (!x || !dt || !A || !B || !C || !dy || !dx || !ddt || !dA || !dB || !dC) return -1;
+    if (batch < 0 || seqlen < 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G) return -1;
+    const size_t PN = (size_t)P * N;
+    const size_t ntok = (size_t)batch * seqlen;
+    double *hs = (double *)malloc((size_t)(seqlen + 1) * PN * sizeof(double));
+    double *Gs = (double *)malloc(PN * sizeof(double));
+    if (!hs || !Gs) {
+        free(hs); free(Gs);
+        return -2;
+    }
+    memset(dA, 0, (size_t)H * sizeof(double));
+    if (dD) memset(dD, 0, (size_t)H * sizeof(double));
+    memset(dB, 0, ntok * G * N * sizeof(double));
+    memset(dC, 0, ntok * G * N * sizeof(double));
+    for (int b = 0; b < batch; ++b) {
+        for (int h = 0; h < H; ++h) {
+            const int g = (int)(((int64_t)h * G) / H);
+            const double Ah = A[h];
+            const double Dh = D ? D[h] : 0.0;
+            /* forward: hs[t + 1] = h_t, hs[0] = h_{-1} */
+            for (size_t e = 0; e < PN; ++e)
+                hs[e] = init ? init[((size_t)b * H + h) * PN + e] : 0.0;
+            for (int t = 0; t < seqlen; ++t) {
+                const size_t bt = (size_t)b * seqlen + t;
+                const double dtt = dt[bt * H + h], a = exp(dtt * Ah);
+                const double *xt = x + (bt * H + h) * P;
+                const double *Bt = B + (bt * G + g) * N;
+                for (int p = 0; p < P; ++p)
+                    for (int n = 0; n < N; ++n)
+                        hs[(t + 1) * PN + p * N + n] =
+                            a * hs[t * PN + p * N + n] + dtt * xt[p] * Bt[n];
+            }
+            /* backward */
+            for (size_t e = 0; e < PN; ++e)
+                Gs[e] = dfinal ? dfinal[((size_t)b * H + h) * PN + e] : 0.0;
+            for (int t = seqlen - 1; t >= 0; --t) {
+                const size_t bt = (size_t)b * seqlen + t;
+                const double dtt = dt[bt * H + h], a = exp(dtt * Ah);
+                const double *xt = x + (bt * H + h) * P;
+                const double *dyt = dy + (bt * H + h) * P;
+                const double *Bt = B + (bt * G + g) * N;
+                const double *Ct = C + (bt * G + g) * N;
+                const double *ht = hs + (t + 1) * PN, *hp = hs + t * PN;
+                for (int p = 0; p < P; ++p)
+                    for (int n = 0; n < N; ++n) Gs[p * N + n] += dyt[p] * Ct[n];
+                double s_h = 0.0, s_xb = 0.0;
+                for (int p = 0; p < P; ++p) {
+                    double acc = 0.0;
+                    for (int n = 0; n < N; ++n) {
+                        const double gv = Gs[p * N + n];
+                        acc += gv * Bt[n];
+                        s_h += gv * hp[p * N + n];
+                        s_xb += gv * xt[p] * Bt[n];
+                    }
+                    dx[(bt * H + h) * P + p] = dtt * acc + Dh * dyt[p];
+                    if (dD) dD[h] += dyt[p] * xt[p];
+                }
+                for (int n = 0; n < N; ++n) {
+                    double gb = 0.0, gc = 0.0;
+                    for (int p = 0; p < P; ++p) {
+                        gb += Gs[p * N + n] * xt[p];
+                        gc += dyt[p] * ht[p * N + n];
+                    }
+                    dB[(bt * G + g) * N + n] += dtt * gb;
+                    dC[(bt * G + g) * N + n] += gc;
+                }
+                ddt[bt * H + h] = Ah * a * s_h + s_xb;
+                dA[h] += dtt * a * s_h;
+                for (size_t e = 0; e < PN; ++e) Gs[e] *= a;
+            }
+            if (dinit) memcpy(dinit + ((size_t)b * H + h) * PN, Gs, PN * sizeof(double));
+        }
+    }
+    free(hs);
+    free(Gs);
+    return 0;
+}

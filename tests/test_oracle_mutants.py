@@ -39,6 +39,11 @@ MUTANTS = {
                            "                acc += h[n] * Ct[n];\n                h[n] = dA * h[n] + dtt * Bt[n] * xt;"),
     "s6_drop_skip_term": ("J->y[bt * Dm + d] = acc + Dd * xt;", "J->y[bt * Dm + d] = acc;"),
     "s6_init_ignored": ("h[n] = J->init ? J->init[((size_t)b * Dm + d) * N + n] : 0.0;", "h[n] = 0.0;"),
+    # the backward
+    "bwd_adjoint_not_decayed": ("for (size_t e = 0; e < PN; ++e) Gs[e] *= a;", "for (size_t e = 0; e < PN; ++e) Gs[e] *= 1.0;"),
+    "bwd_dA_uses_h_t": ("s_h += gv * hp[p * N + n];", "s_h += gv * ht[p * N + n];"),
+    "bwd_dC_uses_h_prev": ("gc += dyt[p] * ht[p * N + n];", "gc += dyt[p] * hp[p * N + n];"),
+    "bwd_dx_drops_dt": ("dx[(bt * H + h) * P + p] = dtt * acc + Dh * dyt[p];", "dx[(bt * H + h) * P + p] = acc + Dh * dyt[p];"),
 }
 
 
@@ -99,6 +104,32 @@ def _pins(lib):
     y6, _ = oracle.s6_scan(x6, dt6, A6, B6, C6, D6, i6, lib=lib)
     if oracle.rel_err(y6, oracle.s6_brute_force(x6, dt6, A6, B6, C6, D6, i6)) > 1e-12:
         failed.append("s6_explicit_products")
+    # backward: each gradient against a directional central difference of the
+    # forward, L = sum(y dy) + sum(final dfinal)
+    b, T, H, P, N, G = 2, 5, 4, 2, 3, 2
+    v = dict(x=rng.standard_normal((b, T, H, P)), dt=rng.uniform(0.05, 0.6, (b, T, H)),
+             A=-rng.uniform(0.2, 2.0, H), B=rng.standard_normal((b, T, G, N)),
+             C=rng.standard_normal((b, T, G, N)), D=rng.standard_normal(H),
+             init=rng.standard_normal((b, H, P, N)))
+    dy = rng.standard_normal((b, T, H, P))
+    dfin = rng.standard_normal((b, H, P, N))
+
+    def loss(w):
+        yy, ff = oracle.ssd_scan(w["x"], w["dt"], w["A"], w["B"], w["C"], w["D"], w["init"], lib=lib)
+        return float(np.sum(yy * dy) + np.sum(ff * dfin))
+
+    gr = oracle.ssd_bwd(v["x"], v["dt"], v["A"], v["B"], v["C"], v["D"], v["init"], dy, dfin, lib=lib)
+    for name, gname in (("x", "dx"), ("dt", "ddt"), ("A", "dA"), ("B", "dB"), ("C", "dC"),
+                        ("D", "dD"), ("init", "dinit")):
+        d = rng.standard_normal(v[name].shape)
+        wp = {k: a.copy() for k, a in v.items()}
+        wm = {k: a.copy() for k, a in v.items()}
+        wp[name] += 1e-6 * d
+        wm[name] -= 1e-6 * d
+        fd = (loss(wp) - loss(wm)) / 2e-6
+        if abs(float(np.sum(gr[gname] * d)) - fd) > 1e-6 * max(1.0, abs(fd)):
+            failed.append(f"bwd_{gname}")
+            break
     return failed
 
 
