@@ -49,6 +49,7 @@ def parse_args():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-epilogue", action="store_true",
                     help="skip the fused-epilogue variant of the forward")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward pass")
     ap.add_argument("--no-s6", action="store_true",
                     help="skip the Mamba-1 selective-scan comparison")
     return ap.parse_args()
@@ -377,6 +378,10 @@ def main():
     if not args.no_epilogue and fi.cu_seqlens is None and wl.dtype == "bf16":
         epilogue = measure_epilogue(fi, wl, dev, d, A, D, init, ws, flush, peaks)
 
+    backward = None
+    if not args.no_bwd and fi.cu_seqlens is None:
+        backward = measure_backward(fi, wl, dev, d, A, D, init, peaks)
+
     s6 = None
     if not args.no_s6 and wl.name == "l8k":
         s6 = measure_s6(dev, peaks, ms * 1e3, flush)
@@ -395,7 +400,7 @@ def main():
                "launches_per_step": launches / max(1, args.steps),
                "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
                "step_ms_max": max(step_ms), "step_ms_first5": [round(v, 4) for v in step_ms[:5]],
-               "e2e": e2e, "cpu_baseline": cpu, "decode": decode, "epilogue": epilogue, "s6": s6,
+               "e2e": e2e, "cpu_baseline": cpu, "decode": decode, "epilogue": epilogue, "backward": backward, "s6": s6,
                "pages_claim": "SSD 2-8x faster than Mamba's fused selective scan (A100), context only"}
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -601,6 +606,50 @@ def measure_epilogue(fi, wl, dev, d, A, D, init, ws, flush, peaks, reps=20):
             "us_median": med, "us_min": min(us), "tokens_per_s": ntok / (med * 1e-6),
             "algorithmic_bytes": bytes_, "hbm_frac": bytes_ / (med * 1e-6) / 1e9 / peaks["hbm_gbs"],
             "gpu_launches": launches}
+
+
+def measure_backward(fi, wl, dev, d, A, D, init, peaks, reps=3):
+    """ssd_chunk_scan_bwd on the same layer with a seeded fp32 dL/dy: median of
+    `reps` calls (inputs larger than L2).  Algorithmic bytes: x, dt, B, C
+    (input dtype) and dy read once; dx, ddt, dB, dC, dinit and the two
+    per-head sums written once."""
+    import numpy as np
+    import torch
+    from state_space_sequence_05_b300 import ssd
+    b, T, H, P, N, G = wl.batch, wl.seqlen, wl.nheads, wl.headdim, wl.dstate, wl.ngroups
+    rng = np.random.Generator(np.random.PCG64(wl.seed + 99))
+    dy = torch.from_numpy(rng.standard_normal((b, T, H, P), dtype=np.float32)).to(dev)
+    ws = torch.empty(ssd.load_library().ssd_chunk_scan_bwd_workspace_size(
+        b, T, H, P, N, G, ssd.SSD_DT_BF16 if wl.dtype == "bf16" else ssd.SSD_DT_F32),
+        device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        ssd.ssd_chunk_scan_bwd(d["x"], d["dt"], A, d["B"], d["C"], D, init, dy, workspace=ws,
+                               stream=stream)
+
+    call()
+    torch.cuda.synchronize()
+    us = []
+    l0 = ssd.kernel_launches()
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us.append(1e3 * e0.elapsed_time(e1))
+    med = statistics.median(us)
+    es = 2 if wl.dtype == "bf16" else 4
+    ntok = b * T
+    bytes_ = (ntok * H * P * (es + 4 + 4) + ntok * H * (es + 4) + 2 * ntok * G * N * (es + 4)
+              + b * H * P * N * 4 * (2 if init is not None else 1) + 3 * H * 4)
+    gbs = bytes_ / (med * 1e-6) / 1e9
+    return {"workload": f"{wl.name}, fp32 dL/dy, no dL/dfinal", "us_median": med,
+            "tokens_per_s": ntok / (med * 1e-6), "algorithmic_bytes": bytes_,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"]},
+            "gpu_launches": ssd.kernel_launches() - l0}
 
 
 # Special-function unit: 16 ex2 results per SM per clock (4 per sub-partition).

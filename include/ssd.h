@@ -205,6 +205,36 @@ ssd_status_t ssd_state_update(float *state, const void *x, const void *dt, const
                               ssd_dtype_t in_dtype, float *y, void *stream);
 
 /*
+ * ssd_chunk_scan_bwd -- backward of ssd_chunk_scan_fwd (batch mode): the
+ * gradients of a loss L given dL/dy and dL/dfinal, the reverse-mode
+ * derivative of the recurrence above (the state gradient G_t = dL/dh_t runs
+ * backwards: G_t = dy_t C_t^T + exp(dt_{t+1} A) G_{t+1}).
+ *
+ * Inputs: x, dt, A, B, C, D, init_states as for the forward (D and
+ *   init_states may be NULL); dy [ntok, nheads, headdim] float32; dfinal
+ *   [batch, nheads, headdim, dstate] float32 or NULL (0).
+ * Outputs (float32, caller-owned, all overwritten):
+ *   dx [ntok, nheads, headdim]; ddt [ntok, nheads]; dA [nheads];
+ *   dB, dC [ntok, ngroups, dstate]; dD [nheads] or NULL; dinit [batch,
+ *   nheads, headdim, dstate] or NULL.
+ * Workspace: ssd_chunk_scan_bwd_workspace_size(...) bytes, 256-byte
+ *   aligned: one stored state every 64 steps and the 64 states of one
+ *   chunk, per (batch row, head).
+ * Supported: headdim * dstate <= 16384, either input dtype; no cu_seqlens.
+ * All arithmetic is fp32.  One kernel launch plus the zeroing of dA, dB, dC
+ * and dD.
+ */
+size_t ssd_chunk_scan_bwd_workspace_size(int batch, int seqlen, int nheads, int headdim,
+                                         int dstate, int ngroups, ssd_dtype_t in_dtype);
+ssd_status_t ssd_chunk_scan_bwd(const void *x, const void *dt, const float *A, const void *B,
+                                const void *C, const float *D, int batch, int seqlen, int nheads,
+                                int headdim, int dstate, int ngroups, ssd_dtype_t in_dtype,
+                                const float *init_states, const float *dy, const float *dfinal,
+                                float *dx, float *ddt, float *dA, float *dB, float *dC, float *dD,
+                                float *dinit, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/*
  * Context (sequence) parallelism: one sequence cut into R consecutive slices,
  * one per device.  Each device runs ssd_chunk_scan_fwd on its slice from a
  * zero state and keeps the slice's end state S_r (final_states) and its

@@ -183,6 +183,74 @@ ssd_status_t ssd_state_update(float* state, const void* x, const void* dt, const
                           in_dtype, y, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+// shapes of the backward: batch mode, P * N up to 16384 (the state and its
+// adjoint live in shared memory)
+ssd_status_t check_bwd(ssd_dtype_t dtype, int batch, int seqlen, int H, int P, int N, int G) {
+  if (dtype != SSD_DT_F32 && dtype != SSD_DT_BF16) return SSD_ERR_INVALID;
+  if (batch < 0 || seqlen < 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G) return SSD_ERR_INVALID;
+  if ((long long)P * N > 16384 || (long long)batch * H >= (1LL << 31) ||
+      (long long)batch * seqlen >= (1LL << 31))
+    return SSD_ERR_UNSUPPORTED;
+  return SSD_OK;
+}
+
+}  // namespace
+
+size_t ssd_chunk_scan_bwd_workspace_size(int batch, int seqlen, int nheads, int headdim,
+                                         int dstate, int ngroups, ssd_dtype_t in_dtype) {
+  if (check_bwd(in_dtype, batch, seqlen, nheads, headdim, dstate, ngroups) != SSD_OK)
+    return (size_t)-1;
+  return ssd::bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate);
+}
+
+ssd_status_t ssd_chunk_scan_bwd(const void* x, const void* dt, const float* A, const void* B,
+                                const void* C, const float* D, int batch, int seqlen, int nheads,
+                                int headdim, int dstate, int ngroups, ssd_dtype_t in_dtype,
+                                const float* init_states, const float* dy, const float* dfinal,
+                                float* dx, float* ddt, float* dA, float* dB, float* dC, float* dD,
+                                float* dinit, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  ssd_status_t st = check_bwd(in_dtype, batch, seqlen, nheads, headdim, dstate, ngroups);
+  if (st != SSD_OK) return st;
+  if (batch == 0) return SSD_OK;
+  if (!A || !dA) return SSD_ERR_INVALID;
+  if (seqlen > 0 && (!x || !dt || !B || !C || !dy || !dx || !ddt || !dB || !dC))
+    return SSD_ERR_INVALID;
+  const size_t need = ssd::bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate);
+  if (seqlen > 0 && (workspace == nullptr || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return SSD_ERR_INVALID;
+  ssd::BwdArgs a{};
+  a.x = x;
+  a.dt = dt;
+  a.B = B;
+  a.C = C;
+  a.A = A;
+  a.D = D;
+  a.init = init_states;
+  a.dy = dy;
+  a.dfinal = dfinal;
+  a.dx = dx;
+  a.ddt = ddt;
+  a.dA = dA;
+  a.dB = dB;
+  a.dC = dC;
+  a.dD = dD;
+  a.dinit = dinit;
+  a.batch = batch;
+  a.seqlen = seqlen;
+  a.H = nheads;
+  a.P = headdim;
+  a.N = dstate;
+  a.G = ngroups;
+  a.dtype = in_dtype;
+  a.ws = workspace;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return ssd::bwd(a);
+}
+
 ssd_status_t ssd_segment_decay(const void* dt, const float* A, int batch, int seqlen, int nheads,
                                ssd_dtype_t in_dtype, float* decay, void* stream) {
   if (in_dtype != SSD_DT_F32 && in_dtype != SSD_DT_BF16) return SSD_ERR_INVALID;

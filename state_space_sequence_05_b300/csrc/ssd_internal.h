@@ -77,6 +77,19 @@ ssd_status_t s6_forward(const void* x, const void* dt, const float* A, const voi
                         int Dm, int N, ssd_dtype_t dtype, float* y, float* final_states,
                         cudaStream_t stream);
 
+// Backward of the forward (batch mode).
+struct BwdArgs {
+  const void *x, *dt, *B, *C;
+  const float *A, *D, *init, *dy, *dfinal;
+  float *dx, *ddt, *dA, *dB, *dC, *dD, *dinit;
+  int batch, seqlen, H, P, N, G;
+  ssd_dtype_t dtype;
+  void* ws;
+  cudaStream_t stream;
+};
+size_t bwd_workspace_bytes(int batch, int T, int H, int P, int N);
+ssd_status_t bwd(const BwdArgs& a);
+
 // Context parallelism: per-slice log-decay sums and the composition of the
 // slices' affine state maps.
 ssd_status_t segment_decay(const void* dt, const float* A, int batch, int T, int H,

@@ -45,6 +45,9 @@ SIGNATURES = {
                                _fp, _vp]),
     "ssd_selective_scan_fwd": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _ci, _ci, _ci, _ci, _ci,
                                      _fp, _fp, _vp]),
+    "ssd_chunk_scan_bwd_workspace_size": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci, _ci]),
+    "ssd_chunk_scan_bwd": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci, _ci, _ci,
+                                 _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _vp, _sz, _vp]),
     "ssd_segment_decay": (_ci, [_vp, _fp, _ci, _ci, _ci, _ci, _fp, _vp]),
     "ssd_segment_combine": (_ci, [_fp, _fp, _fp, _ci, _ci, _ci, _ci, _ci, _fp, _vp]),
     "ssd_status_string": (ctypes.c_char_p, [_ci]),
@@ -333,3 +336,50 @@ def ssd_segment_combine(decay, states, init_states=None, *, out=None, stream=Non
     if st != SSD_OK:
         raise SSDError(st, "ssd_segment_combine")
     return out
+
+
+def ssd_chunk_scan_bwd(x, dt, A, B, C, D, init_states, dy, dfinal=None, *, workspace=None,
+                       want_dD=True, want_dinit=True, stream=None):
+    """Backward of the forward (batch mode).  x, dt, A, B, C, D, init_states
+    as for ssd_chunk_scan_fwd; dy [b, T, H, P] float32; dfinal [b, H, P, N]
+    float32 or None.  Returns a dict of float32 gradients dx, ddt, dA, dB, dC
+    and (unless disabled) dD and dinit."""
+    lib = load_library()
+    dev = x.device
+    if dev.type != "cuda" or x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be [b, T, H, P] and B [b, T, G, N], on a CUDA device")
+    b, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    code = _dtype_code(x)
+    _need(x, "x", dev)
+    _need(dt, "dt", dev, x.dtype, (b, T, H))
+    _need(B, "B", dev, x.dtype, (b, T, G, N))
+    _need(C, "C", dev, x.dtype, (b, T, G, N))
+    _need(A, "A", dev, torch.float32, (H,))
+    _need(dy, "dy", dev, torch.float32, (b, T, H, P))
+    if D is not None:
+        _need(D, "D", dev, torch.float32, (H,))
+    if init_states is not None:
+        _need(init_states, "init_states", dev, torch.float32, (b, H, P, N))
+    if dfinal is not None:
+        _need(dfinal, "dfinal", dev, torch.float32, (b, H, P, N))
+    f32 = dict(device=dev, dtype=torch.float32)
+    g = {"dx": torch.empty((b, T, H, P), **f32), "ddt": torch.empty((b, T, H), **f32),
+         "dA": torch.empty((H,), **f32), "dB": torch.empty((b, T, G, N), **f32),
+         "dC": torch.empty((b, T, G, N), **f32),
+         "dD": torch.empty((H,), **f32) if want_dD else None,
+         "dinit": torch.empty((b, H, P, N), **f32) if want_dinit else None}
+    need = lib.ssd_chunk_scan_bwd_workspace_size(b, T, H, P, N, G, code)
+    if need == ctypes.c_size_t(-1).value:
+        raise SSDError(SSD_ERR_UNSUPPORTED, "ssd_chunk_scan_bwd_workspace_size")
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.ssd_chunk_scan_bwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), b, T, H, P,
+                                N, G, code, _ptr(init_states), _ptr(dy), _ptr(dfinal),
+                                _ptr(g["dx"]), _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]),
+                                _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dinit"]), _ptr(workspace),
+                                ws_bytes, _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_chunk_scan_bwd")
+    return g
