@@ -13,14 +13,16 @@
 //     ddt_t = <G_t, A a_t h_{t-1} + x_t B_t^T>,  dA = sum_t dt_t a_t <G_t, h_{t-1}>,
 //     dD = sum_t <dy_t, x_t>,  dinit = a_0 G_0.
 //
-// Design: one block per (batch row, head), the running state and the adjoint
-// in shared memory (P*N floats each).  The states h_t are needed in reverse
+// Design: the rows p of the state never mix (h_t[p,:] and G_t[p,:] evolve on
+// their own), so the work is cut into blocks of (batch row, head, slice of
+// kRows state rows), the slice's state and adjoint in shared memory.  Sums
+// over p (dB, dC, ddt, dA, dD) add up the slices with atomics (the entry
+// point zeroes them first).  The states h_t are needed in reverse
 // order: a first forward sweep stores every kCk-th state in the workspace;
 // then, chunk by chunk from the end, the chunk's kCk states are recomputed
 // from its checkpoint into the workspace and the adjoint walks the chunk
 // backwards.  Sums over a row of the state go to warps, sums over a column to
-// threads; dB and dC, shared by the heads of a group, are accumulated with
-// atomics (the entry point zeroes them first).  All arithmetic is fp32.
+// threads.  All arithmetic is fp32.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -33,14 +35,15 @@ namespace {
 
 constexpr int kBwdThreads = 256;
 constexpr int kBwdWarps = kBwdThreads / 32;
-constexpr int kCk = 64;  // steps between stored states
+constexpr int kCk = 64;   // steps between stored states
+constexpr int kRows = 8;  // state rows per block
 
 struct BwdParams {
   const void *x, *dt, *B, *C;
   const float *A, *D, *init, *dy, *dfinal;
   float *dx, *ddt, *dA, *dB, *dC, *dD, *dinit;
-  float* ws;  // per (b, h): (nck + 1) stored states, then kCk chunk states
-  int T, H, P, N, G, nck;
+  float* ws;  // per (b, h, slice): (nck + 1) stored states, then kCk chunk states
+  int T, H, P, N, G, nck, nslice;
 };
 
 template <bool BF16>
@@ -57,11 +60,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_kernel(BwdParams p) {
-  const int bh = blockIdx.x;
+  const int bh = blockIdx.x / p.nslice;
+  const int slice = blockIdx.x % p.nslice;
   const int b = bh / p.H, h = bh % p.H;
   const int g = (int)((long long)h * p.G / p.H);
-  const int P = p.P, N = p.N, H = p.H, G = p.G;
-  const int PN = P * N;
+  const int N = p.N, H = p.H, G = p.G, Pf = p.P;
+  const int p0 = slice * kRows;                 // first state row of this block
+  const int P = min(kRows, Pf - p0);            // rows of this block
+  const int PN = P * N;                         // state elements of this block
+  const long long soff = ((long long)bh * Pf + p0) * N;  // its offset in a [b, H, P, N] state
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   extern __shared__ float bwd_smem[];
@@ -76,15 +83,15 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_kernel(BwdParams p) {
   const float Ah = p.A[h];
   const float Dh = p.D ? p.D[h] : 0.f;
   const long long tok0 = (long long)b * p.T;
-  float* ck = p.ws + (long long)bh * (p.nck + 1 + kCk) * PN;  // stored states
-  float* hs = ck + (long long)(p.nck + 1) * PN;               // one chunk's states
+  float* ck = p.ws + (long long)blockIdx.x * (p.nck + 1 + kCk) * (kRows * N);  // stored states
+  float* hs = ck + (long long)(p.nck + 1) * PN;                                // one chunk's states
 
   // inputs of step t into shared memory (callers synchronise around it)
   auto load_step = [&](int t, bool backward) {
     const long long bt = tok0 + t;
     for (int i = tid; i < P; i += kBwdThreads) {
-      xs[i] = ldin<BF16>(p.x, (bt * H + h) * P + i);
-      if (backward) dys[i] = p.dy[(bt * H + h) * P + i];
+      xs[i] = ldin<BF16>(p.x, (bt * H + h) * Pf + p0 + i);
+      if (backward) dys[i] = p.dy[(bt * H + h) * Pf + p0 + i];
     }
     for (int i = tid; i < N; i += kBwdThreads) {
       Bs[i] = ldin<BF16>(p.B, (bt * G + g) * N + i);
@@ -106,7 +113,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_kernel(BwdParams p) {
 
   // 1. forward sweep, storing the state before every kCk-th step
   for (int e = tid; e < PN; e += kBwdThreads) {
-    const float v = p.init ? p.init[(long long)bh * PN + e] : 0.f;
+    const float v = p.init ? p.init[soff + e] : 0.f;
     hsm[e] = v;
     ck[e] = v;
   }
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_kernel(BwdParams p) {
 
   // 2. the adjoint, chunk by chunk from the end
   for (int e = tid; e < PN; e += kBwdThreads)
-    Gsm[e] = p.dfinal ? p.dfinal[(long long)bh * PN + e] : 0.f;
+    Gsm[e] = p.dfinal ? p.dfinal[soff + e] : 0.f;
   float dA_acc = 0.f, dD_acc = 0.f;  // thread 0's running sums
   for (int c = p.nck - 1; c >= 0; --c) {
     const int t0 = c * kCk;
@@ -159,7 +166,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_kernel(BwdParams p) {
         float acc = 0.f;
         for (int n = lane; n < N; n += 32) acc += Gsm[pp * N + n] * Bs[n];
         acc = warp_sum(acc);
-        if (lane == 0) p.dx[(bt * H + h) * P + pp] = dtt * acc + Dh * dys[pp];
+        if (lane == 0) p.dx[(bt * H + h) * Pf + p0 + pp] = dtt * acc + Dh * dys[pp];
       }
       // dB_t[n] += dt_t sum_p G_t[p,n] x_t[p], dC_t[n] += sum_p dy_t[p] h_t[p,n]
       for (int n = tid; n < N; n += kBwdThreads) {
@@ -177,7 +184,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_kernel(BwdParams p) {
           sh += red[w];
           sxb += red[kBwdWarps + w];
         }
-        p.ddt[bt * H + h] = Ah * a * sh + sxb;
+        atomicAdd(p.ddt + bt * H + h, Ah * a * sh + sxb);
         dA_acc += dtt * a * sh;
         float xd = 0.f;
         for (int pp = 0; pp < P; ++pp) xd += dys[pp] * xs[pp];
@@ -189,22 +196,23 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_kernel(BwdParams p) {
     }
   }
   if (p.dinit)
-    for (int e = tid; e < PN; e += kBwdThreads) p.dinit[(long long)bh * PN + e] = Gsm[e];
+    for (int e = tid; e < PN; e += kBwdThreads) p.dinit[soff + e] = Gsm[e];
   if (tid == 0) {
     atomicAdd(p.dA + h, dA_acc);
     if (p.dD) atomicAdd(p.dD + h, dD_acc);
   }
 }
 
-size_t smem_bytes(int P, int N) {
-  return sizeof(float) * ((size_t)2 * P * N + 2 * P + 2 * N + 2 * kBwdWarps);
+size_t smem_bytes(int N) {
+  return sizeof(float) * ((size_t)2 * kRows * N + 2 * kRows + 2 * N + 2 * kBwdWarps);
 }
 
 }  // namespace
 
 size_t bwd_workspace_bytes(int batch, int T, int H, int P, int N) {
   const long long nck = ((long long)T + kCk - 1) / kCk;
-  return sizeof(float) * (size_t)batch * H * (size_t)(nck + 1 + kCk) * P * N;
+  const long long nslice = (P + kRows - 1) / kRows;
+  return sizeof(float) * (size_t)batch * H * nslice * (size_t)(nck + 1 + kCk) * kRows * N;
 }
 
 ssd_status_t bwd(const BwdArgs& a) {
@@ -232,9 +240,11 @@ ssd_status_t bwd(const BwdArgs& a) {
   p.N = a.N;
   p.G = a.G;
   p.nck = (a.seqlen + kCk - 1) / kCk;
+  p.nslice = (a.P + kRows - 1) / kRows;
   const long long ntok = (long long)a.batch * a.seqlen;
   // the accumulated gradients start at zero
   if (cudaMemsetAsync(a.dA, 0, sizeof(float) * a.H, a.stream) != cudaSuccess ||
+      (ntok > 0 && cudaMemsetAsync(a.ddt, 0, sizeof(float) * ntok * a.H, a.stream) != cudaSuccess) ||
       (a.dD && cudaMemsetAsync(a.dD, 0, sizeof(float) * a.H, a.stream) != cudaSuccess) ||
       (ntok > 0 &&
        (cudaMemsetAsync(a.dB, 0, sizeof(float) * ntok * a.G * a.N, a.stream) != cudaSuccess ||
@@ -251,13 +261,13 @@ ssd_status_t bwd(const BwdArgs& a) {
     }
     return SSD_OK;
   }
-  const size_t smem = smem_bytes(a.P, a.N);
+  const size_t smem = smem_bytes(a.N);
   auto k = a.dtype == SSD_DT_BF16 ? ssd_bwd_kernel<true> : ssd_bwd_kernel<false>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess)
     return SSD_ERR_CUDA;
-  k<<<a.batch * a.H, kBwdThreads, smem, a.stream>>>(p);
+  k<<<a.batch * a.H * p.nslice, kBwdThreads, smem, a.stream>>>(p);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
