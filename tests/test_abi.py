@@ -96,3 +96,48 @@ def test_binding_fails_loudly_without_library(tmp_path):
             ssd.load_library(str(tmp_path / "nope.so"))
     finally:
         ssd._lib = saved
+
+
+def test_host_side_rejections_of_the_other_entry_points(lib):
+    """The fused-epilogue forward, the backward, the context-parallel steps and
+    the selective scan check their arguments on the host before any CUDA call
+    (so this runs without a GPU)."""
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    E = ssd.FwdEpilogue
+
+    def fwd_ex(epi, dtype=0, P=16, N=16, z=None):
+        e = E(None, epi.get("softplus", 0), z, epi.get("bf16", 0))
+        return lib.ssd_chunk_scan_fwd_ex(fake, fake, fake, fake, fake, None, 1, 16, 2, P, N, 1, 64,
+                                         dtype, None, None, 0, fake, None, None, 0, None, None,
+                                         ctypes.byref(e))
+    # the fused epilogue exists on the tensor-core shapes only
+    assert fwd_ex({"softplus": 1}) == ssd.SSD_ERR_UNSUPPORTED
+    assert fwd_ex({"bf16": 1}, dtype=0, P=64, N=128) == ssd.SSD_ERR_UNSUPPORTED
+    # z must be 16-byte aligned
+    assert fwd_ex({}, dtype=1, P=64, N=128, z=odd) == ssd.SSD_ERR_INVALID
+
+    def bwd(dtype=0, H=2, P=16, N=16, G=1, ws=None, ws_bytes=0):
+        return lib.ssd_chunk_scan_bwd(fake, fake, fake, fake, fake, None, 1, 16, H, P, N, G, dtype,
+                                      None, fake, None, fake, fake, fake, fake, fake, None, None,
+                                      ws, ws_bytes, None)
+    assert bwd(dtype=7) == ssd.SSD_ERR_INVALID
+    assert bwd(H=3, G=2) == ssd.SSD_ERR_INVALID
+    assert bwd(P=129, N=128) == ssd.SSD_ERR_UNSUPPORTED
+    assert bwd() == ssd.SSD_ERR_INVALID                                   # no workspace
+    need = lib.ssd_chunk_scan_bwd_workspace_size(1, 16, 2, 16, 16, 1, 0)
+    assert 0 < need < (1 << 30)
+    assert bwd(ws=fake, ws_bytes=need - 1) == ssd.SSD_ERR_INVALID         # too small
+    assert lib.ssd_chunk_scan_bwd_workspace_size(1, 16, 2, 129, 128, 1, 0) == ctypes.c_size_t(-1).value
+
+    assert lib.ssd_segment_decay(fake, fake, 1, 16, 0, 0, fake, None) == ssd.SSD_ERR_INVALID
+    assert lib.ssd_segment_decay(None, fake, 1, 16, 2, 0, fake, None) == ssd.SSD_ERR_INVALID
+    assert lib.ssd_segment_combine(fake, None, None, 2, 1, 2, 4, 4, fake, None) == ssd.SSD_ERR_INVALID
+    assert lib.ssd_segment_combine(fake, fake, None, 2, 1, 2, 0, 4, fake, None) == ssd.SSD_ERR_INVALID
+
+    def s6(batch=1, N=16, x=fake):
+        return lib.ssd_selective_scan_fwd(x, fake, fake, fake, fake, None, None, batch, 16, 8, N,
+                                          0, fake, None, None)
+    assert s6(N=24) == ssd.SSD_ERR_UNSUPPORTED
+    assert s6(batch=70000) == ssd.SSD_ERR_UNSUPPORTED
+    assert s6(x=None) == ssd.SSD_ERR_INVALID
