@@ -203,8 +203,10 @@ __global__ void __launch_bounds__(kBwdThreads) ssd_bwd_kernel(BwdParams p) {
   }
 }
 
-size_t smem_bytes(int N) {
-  return sizeof(float) * ((size_t)2 * kRows * N + 2 * kRows + 2 * N + 2 * kBwdWarps);
+// shared memory of a block holding `rows` state rows (the kernel's layout:
+// state, adjoint, x, dy, B, C, block-sum partials)
+size_t smem_bytes(int rows, int N) {
+  return sizeof(float) * ((size_t)2 * rows * N + 2 * rows + 2 * N + 2 * kBwdWarps);
 }
 
 }  // namespace
@@ -261,7 +263,7 @@ ssd_status_t bwd(const BwdArgs& a) {
     }
     return SSD_OK;
   }
-  const size_t smem = smem_bytes(a.N);
+  const size_t smem = smem_bytes(a.P < kRows ? a.P : kRows, a.N);
   auto k = a.dtype == SSD_DT_BF16 ? ssd_bwd_kernel<true> : ssd_bwd_kernel<false>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
