@@ -310,6 +310,20 @@ int ssd_version(void);
  */
 uint64_t ssd_kernel_launches(void);
 
+/*
+ * Test hook, not for production use.  Sets, for later calls of
+ * ssd_chunk_scan_fwd on the tensor-core path (bf16, headdim 64, dstate 128,
+ * no fused-epilogue options), the bound on every device-side wait in
+ * nanoseconds (0 restores the default of 2 s) and a work unit that never
+ * publishes its segment end state (-1: none).  With a held unit, the unit
+ * that waits for it gives up after `wait_ns`, the call records
+ * SSD_ERR_TIMEOUT in dev_status, and the kernel returns with its tensor
+ * memory freed; the output of that call is undefined.  Work units are
+ * numbered sequence by sequence, segment by segment, head by head.  The
+ * setting is process-wide and not synchronised with calls in flight.
+ */
+void ssd_test_set_forward_wait(unsigned long long wait_ns, int hold_unit);
+
 #ifdef __cplusplus
 }
 #endif

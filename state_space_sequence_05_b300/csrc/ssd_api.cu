@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <cstdlib>
 
 #include "ssd.h"
 #include "ssd_internal.h"
@@ -12,6 +13,10 @@
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+// Test hook (ssd_test_set_forward_wait): bound on every device wait of the
+// pipelined tensor-core forward and a unit that never publishes its state.
+std::atomic<unsigned long long> g_wait_ns{0};
+std::atomic<int> g_hold_unit{-1};
 
 }  // namespace
 
@@ -49,9 +54,21 @@ ssd_status_t check_fwd(const FwdArgs& a, bool check_ptrs) {
   return SSD_OK;
 }
 
+// Which tensor-core forward runs the plain (no fused-epilogue) calls: the
+// first kernel unless SSD_TC_PIPELINED=1 selects the pipelined one.
+bool legacy_tc() {
+  const char* e = getenv("SSD_TC_PIPELINED");
+  return !(e && e[0] == '1');
+}
+
 size_t fwd_workspace(const FwdArgs& a) {
   if (a.nseq == 0) return 0;
-  if (ssd::tc_supported(a)) return ssd::tc_workspace_bytes(a);
+  // the tensor-core shapes run on the pipelined kernel, or on the fused-
+  // epilogue kernel when epilogue options are given: enough for either
+  if (ssd::tc_supported(a)) {
+    const size_t t1 = ssd::tc_workspace_bytes(a), t2 = ssd::tc2_workspace_bytes(a);
+    return t1 > t2 ? t1 : t2;
+  }
   return ssd::simt_workspace_bytes(a);
 }
 
@@ -163,7 +180,16 @@ ssd_status_t ssd_chunk_scan_fwd_ex(const void* x, const void* dt, const float* A
   if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), a.stream) != cudaSuccess)
     return SSD_ERR_CUDA;
   if (a.nseq == 0) return SSD_OK;
+  if (ssd::tc2_supported(a) && !legacy_tc()) {
+    const unsigned long long w = g_wait_ns.load(std::memory_order_relaxed);
+    return ssd::tc2_forward(a, w ? w : 2000000000ull, g_hold_unit.load(std::memory_order_relaxed));
+  }
   return ssd::tc_supported(a) ? ssd::tc_forward(a) : ssd::simt_forward(a);
+}
+
+void ssd_test_set_forward_wait(unsigned long long wait_ns, int hold_unit) {
+  g_wait_ns.store(wait_ns, std::memory_order_relaxed);
+  g_hold_unit.store(hold_unit, std::memory_order_relaxed);
 }
 
 ssd_status_t ssd_state_update(float* state, const void* x, const void* dt, const float* A,

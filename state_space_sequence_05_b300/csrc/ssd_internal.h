@@ -71,6 +71,14 @@ bool tc_supported(const FwdArgs& a);
 size_t tc_workspace_bytes(const FwdArgs& a);
 ssd_status_t tc_forward(const FwdArgs& a);
 
+// Pipelined tcgen05 forward (the same shapes, no fused-epilogue options).
+// Every device wait is bounded by `wait_ns`; `hold_unit` >= 0 names a work
+// unit that never publishes its segment end state (a test hook: its
+// successor's wait runs out and the call reports SSD_ERR_TIMEOUT).
+bool tc2_supported(const FwdArgs& a);
+size_t tc2_workspace_bytes(const FwdArgs& a);
+ssd_status_t tc2_forward(const FwdArgs& a, unsigned long long wait_ns, int hold_unit);
+
 // Mamba-1 selective scan (a decay per channel and state), one launch.
 ssd_status_t s6_forward(const void* x, const void* dt, const float* A, const void* B,
                         const void* C, const float* D, const float* init, int batch, int L,

@@ -66,7 +66,9 @@
 
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
+#include "ssd_tc_host.h"
 #include "tc_ptx.cuh"
+#include "tc_util.cuh"
 
 namespace ssd {
 namespace {
@@ -109,13 +111,9 @@ constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
-// Chunks per segment.  Dense batches take the length in [kSegMin, kSegMax]
-// that best fills the SMs with whole waves of units (see choose_seg);
-// packed sequences, whose lengths live on the device, take kSegVarlen.
-constexpr int kSegMin = 4, kSegMax = 12, kSegVarlen = 8;
-constexpr int kStSlots = kSegMax > kSegVarlen ? kSegMax : kSegVarlen;  // chunks per unit, at most
+// Chunks per unit, at most (segment lengths: see tc_choose_seg).
+constexpr int kStSlots = kTcSegMax > kTcSegVarlen ? kTcSegMax : kTcSegVarlen;
 
 enum : int { kKindA = 0, kKindB = 1, kKindEnd = 2 };
 
@@ -158,85 +156,6 @@ struct EpiParams {
   int dt_softplus;              // dt = softplus(dt + dt_bias[h]) in the tables
   int y_bf16;                   // y stored as bf16 (round to nearest even)
 };
-
-__device__ __forceinline__ unsigned long long gtime() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded mbarrier wait: polls until `parity` completes or kWaitNs passes.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = gtime();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (gtime() - t0 > kWaitNs) return false;
-  }
-}
-
-// Warp-collective form: every lane waits and the warp agrees on the result,
-// so a timeout never splits a warp (later warp-synchronous instructions
-// would otherwise strand the lanes that went on).
-__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, wait_bar(bar, parity));
-}
-
-// All 8 math warps meet at `bar` (phase parity `par`); bounded.  The math
-// warps synchronise only through mbarriers so that a timed-out warp can
-// leave without stranding the others at a hardware barrier.
-__device__ __forceinline__ bool math_sync(uint64_t* bar, uint32_t par) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  return wait_bar_warp(bar, par);
-}
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release(int* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// 2^x on the special-function unit (ex2.approx.ftz: relative error ~2^-22,
-// flushes subnormal results to zero, which every use here tolerates).
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// log2 on the special-function unit (lg2.approx.ftz: absolute error ~2^-22
-// near 1)
-__device__ __forceinline__ float fast_log2(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-// two floats rounded to bf16 (to nearest, ties to even), a in the low half
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// v ~= hi + lo: hi = v with its low 16 bits cleared (bf16 by truncation),
-// lo = v - hi (exact in fp32) truncated to bf16 the same way; |v - hi - lo|
-// < 2^-14 |v|.  Packs the hi and lo halves of two values (a in the low 16
-// bits, as __floats2bfloat162_rn(a, b) would).
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
-  hi = __byte_perm(ua, ub, 0x7632);
-  const float la = a - __uint_as_float(ua & 0xffff0000u);
-  const float lb = b - __uint_as_float(ub & 0xffff0000u);
-  lo = __byte_perm(__float_as_uint(la), __float_as_uint(lb), 0x7632);
-}
 
 struct Smem {
   uint8_t* base;
@@ -1321,189 +1240,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Plan: per sequence the number of work units (segments x heads) as offsets
-// uoff[0..nseq], and uoff[nseq+1] = 0 if cu_seqlens is well formed; zeroes
-// the work ticket and the hand-off flags; final = init (or 0) for sequences
-// without tokens.  One block of 1024 threads.
-__global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* cu, int seqlen_rows,
-                                                       int seqlen_total, int nseq, int seg,
-                                                       int H, int32_t* uoff, int* ticket,
-                                                       int* flags, long long max_units,
-                                                       const float* init, float* final_states,
-                                                       int32_t* dev_status) {
-  // the forward kernel may be scheduled now; it waits for this grid's
-  // completion before it reads anything written here
-  asm volatile("griddepcontrol.launch_dependents;");
-  __shared__ int buf[32];
-  __shared__ int carry, bad;
-  if (threadIdx.x == 0) {
-    carry = 0;
-    bad = 0;
-    ticket[0] = 0;
-    ticket[1] = 0;
-    if (cu && (cu[0] != 0 || cu[nseq] != seqlen_total)) bad = 1;
-  }
-  for (long long k = threadIdx.x; k < max_units; k += 1024) flags[k] = 0;
-  __syncthreads();
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int base = 0; base < nseq; base += 1024) {
-    const int s = base + threadIdx.x;
-    int n = 0;
-    if (s < nseq) {
-      const long long b = cu ? (long long)cu[s] : (long long)s * seqlen_rows;
-      const long long e = cu ? (long long)cu[s + 1] : (long long)(s + 1) * seqlen_rows;
-      if (e < b || b < 0 || e > seqlen_total) atomicOr(&bad, 1);
-      const long long nt = e > b ? (e - b + kQ - 1) / kQ : 0;
-      n = (int)((nt + seg - 1) / seg) * H;
-    }
-    int v = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += t;
-    }
-    if (lane == 31) buf[wid] = v;
-    __syncthreads();
-    int off = 0;
-    for (int w = 0; w < wid; ++w) off += buf[w];
-    if (s < nseq) uoff[s + 1] = carry + v + off;
-    __syncthreads();
-    if (threadIdx.x == 1023) carry += v + off;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) uoff[0] = 0;
-  __syncthreads();
-  if (bad) {
-    for (int s = threadIdx.x; s <= nseq; s += 1024) uoff[s] = 0;
-    if (threadIdx.x == 0) report(dev_status, SSD_ERR_INVALID);
-  }
-  if (threadIdx.x == 0) uoff[nseq + 1] = bad;
-  __syncthreads();
-  if (final_states && !bad) {
-    const long long per = (long long)H * kPN;
-    for (int s = 0; s < nseq; ++s) {
-      if (uoff[s + 1] != uoff[s]) continue;  // the sequence has tokens
-      float* dst = final_states + (long long)s * per;
-      const float* src = init ? init + (long long)s * per : nullptr;
-      for (long long e = threadIdx.x; e < per; e += 1024) dst[e] = src ? src[e] : 0.f;
-    }
-  }
-}
-
-// --------------------------------------------------------------------------
-// host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// 2-D bf16 map over a [rows, cols] row-major matrix, 64 x 128 boxes, 128B swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, 128};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// y as a 2D fp32 tensor [tokens][H * P]; a box is 16 columns x 32 rows,
-// 64B-swizzled (one math warp's tile).
-bool make_map_y(CUtensorMap* m, float* ptr, long long rows, long long cols) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
-  cuuint32_t box[2] = {16, 32};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// bf16 y (the fused-epilogue option): a box is 16 columns (32 bytes) x 32
-// rows, unswizzled.
-bool make_map_y_bf16(CUtensorMap* m, void* ptr, long long rows, long long cols) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {16, 32};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int sm_count() {
-  static int n = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  });
-  return n > 0 ? n : 148;
-}
-
-// Segment length for a call: dense batches pick, among kSegMin..kSegMax,
-// the one whose units fill the SMs in the fewest chunk-steps (waves x
-// chunks per unit), preferring longer segments on a tie.
-int choose_seg(const FwdArgs& a) {
-  if (a.cu) return kSegVarlen;
-  const long long nt = ((long long)a.seqlen + kQ - 1) / kQ;
-  const long long nsm = sm_count();
-  int best = kSegMax;
-  long long best_cost = -1;
-  for (int sg = kSegMax; sg >= kSegMin; --sg) {
-    const long long units = (long long)a.batch * ((nt + sg - 1) / sg) * a.H;
-    const long long cost = ((units + nsm - 1) / nsm) * (nt < sg ? nt : sg);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = sg;
-    }
-  }
-  return best;
-}
-
-// Upper bound on the number of work units for any segment length a call
-// may choose.
-long long max_units(const FwdArgs& a) {
-  const long long per = ((long long)a.seqlen + kQ - 1) / kQ;
-  if (a.cu) return (((per + a.nseq) + kSegVarlen - 1) / kSegVarlen + a.nseq) * a.H;
-  return (long long)a.batch * ((per + kSegMin - 1) / kSegMin) * a.H;
-}
-
 struct WsLayout {
   size_t uoff, ticket, flags, slots, stbuf, total;
 };
 
 WsLayout ws_layout(const FwdArgs& a) {
   WsLayout L;
-  const long long mu = max_units(a);
+  const long long mu = tc_max_units(a);
   L.uoff = 0;
   L.ticket = L.uoff + plan_bytes(a.nseq);
   L.flags = L.ticket + 256;
   L.slots = L.flags + align256(sizeof(int) * (size_t)mu);
   L.stbuf = L.slots + align256(sizeof(float) * (size_t)mu * kPN);
-  L.total = L.stbuf + align256(sizeof(float) * (size_t)sm_count() * kStSlots * kPN);
+  L.total = L.stbuf + align256(sizeof(float) * (size_t)tc_sm_count() * kStSlots * kPN);
   return L;
 }
 
@@ -1524,20 +1273,20 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   float* slots = reinterpret_cast<float*>(ws + L.slots);
   float* stbuf = reinterpret_cast<float*>(ws + L.stbuf);
   const long long ntok = (long long)a.batch * a.seqlen;
-  const long long mu = max_units(a);
-  const int seg = choose_seg(a);
+  const long long mu = tc_max_units(a);
+  const int seg = tc_choose_seg(a);
   // everything the host prepares comes before the first launch, so the two
   // kernels reach the GPU back to back
   CUtensorMap mx, mb, mc, my, mz;
   const bool work = ntok > 0 && mu > 0;
   const bool epi = a.z != nullptr || a.y_bf16 || a.dt_softplus;
-  if (work && (!make_map(&mx, a.x, ntok, (long long)a.H * kP) ||
-               !make_map(&mb, a.B, ntok, (long long)a.G * kN) ||
-               !make_map(&mc, a.C, ntok, (long long)a.G * kN) ||
-               (a.y_bf16 ? !make_map_y_bf16(&my, a.y, ntok, (long long)a.H * kP)
-                         : !make_map_y(&my, a.y, ntok, (long long)a.H * kP)) ||
+  if (work && (!tc_make_map_bf16(&mx, a.x, ntok, (long long)a.H * kP) ||
+               !tc_make_map_bf16(&mb, a.B, ntok, (long long)a.G * kN) ||
+               !tc_make_map_bf16(&mc, a.C, ntok, (long long)a.G * kN) ||
+               (a.y_bf16 ? !tc_make_map_y_bf16(&my, a.y, ntok, (long long)a.H * kP)
+                         : !tc_make_map_y_f32(&my, a.y, ntok, (long long)a.H * kP)) ||
                // z is only prefetched through its map (x stands in when absent)
-               !make_map(&mz, a.z ? a.z : a.x, ntok, (long long)a.H * kP)))
+               !tc_make_map_bf16(&mz, a.z ? a.z : a.x, ntok, (long long)a.H * kP)))
     return SSD_ERR_CUDA;
   Params p;
   p.dt = static_cast<const __nv_bfloat16*>(a.dt);
@@ -1572,13 +1321,9 @@ ssd_status_t tc_forward(const FwdArgs& a) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   });
   if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
-  tc_plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu, a.seqlen, (int)ntok, a.nseq, seg, a.H, uoff,
-                                           ticket, flags, mu, a.init, a.final_states,
-                                           a.dev_status);
-  count_launches(1);
-  if (cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
+  if (tc_launch_plan(a, seg, uoff, ticket, flags, mu) != cudaSuccess) return SSD_ERR_CUDA;
   if (!work) return SSD_OK;
-  const int grid = (int)(mu < sm_count() ? mu : sm_count());
+  const int grid = (int)(mu < tc_sm_count() ? mu : tc_sm_count());
   // Programmatic dependent launch: the forward kernel may start while the
   // plan kernel runs; it waits for the plan's results (griddepcontrol.wait)
   // after its own set-up (barriers, tensor memory, tensor-map prefetch).

@@ -1,0 +1,51 @@
+// ssd_tc_host.h -- host-side pieces shared by the tensor-core forward
+// kernels (not part of the public ABI): TMA tensor maps, the plan kernel that
+// lays out the work units, and the choice of segment length.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssd_internal.h"
+
+namespace ssd {
+
+// Tokens per chunk of the tensor-core kernels (the tcgen05 tile height M).
+constexpr int kTcChunk = 128;
+// Chunks per segment: dense batches take a length in [kTcSegMin, kTcSegMax]
+// (see tc_choose_seg); packed sequences, whose lengths live on the device,
+// take kTcSegVarlen.
+constexpr int kTcSegMin = 4, kTcSegMax = 12, kTcSegVarlen = 8;
+
+// SMs of the current device (queried once).
+int tc_sm_count();
+
+// Segment length for a call: dense batches pick, among kTcSegMin..kTcSegMax,
+// the one whose units fill the SMs in the fewest chunk-steps (waves x chunks
+// per unit), preferring longer segments on a tie.
+int tc_choose_seg(const FwdArgs& a);
+
+// Upper bound on the number of work units (sequence, segment, head) for any
+// segment length a call may choose.
+long long tc_max_units(const FwdArgs& a);
+
+// 2-D bf16 map over a row-major [rows, cols] matrix, 64-column x 128-row
+// boxes, 128-byte swizzle (the operand tiles of the MMAs).
+bool tc_make_map_bf16(CUtensorMap* m, const void* ptr, long long rows, long long cols);
+// y as a 2-D fp32 tensor [tokens][H * P]: 16-column x 32-row boxes, 64-byte
+// swizzle (one math warp's staged tile).
+bool tc_make_map_y_f32(CUtensorMap* m, float* ptr, long long rows, long long cols);
+// bf16 y: 16-column (32-byte) x 32-row boxes, unswizzled.
+bool tc_make_map_y_bf16(CUtensorMap* m, void* ptr, long long rows, long long cols);
+
+// Plan kernel: per sequence the number of work units (segments of `seg`
+// chunks x H heads) as offsets uoff[0..nseq], and uoff[nseq+1] = 0 if
+// cu_seqlens is well formed (else SSD_ERR_INVALID in dev_status and no
+// units); zeroes the work ticket (ticket[0..1]) and the first `max_units`
+// hand-off flags; final = init (or 0) for sequences without tokens.  It
+// allows its dependent launch to start early (programmatic dependent launch).
+cudaError_t tc_launch_plan(const FwdArgs& a, int seg, int32_t* uoff, int* ticket, int* flags,
+                           long long max_units);
+
+}  // namespace ssd

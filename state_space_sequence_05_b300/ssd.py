@@ -53,6 +53,7 @@ SIGNATURES = {
     "ssd_status_string": (ctypes.c_char_p, [_ci]),
     "ssd_version": (_ci, []),
     "ssd_kernel_launches": (ctypes.c_uint64, []),
+    "ssd_test_set_forward_wait": (None, [ctypes.c_ulonglong, _ci]),
 }
 
 _lib = None
@@ -93,6 +94,12 @@ def version() -> int:
 def kernel_launches() -> int:
     """Kernels the library has launched in this process so far."""
     return int(load_library().ssd_kernel_launches())
+
+
+def test_set_forward_wait(wait_ns: int = 0, hold_unit: int = -1) -> None:
+    """Test hook: bound on every device wait of the tensor-core forward (ns,
+    0 = default) and a work unit that never publishes its state (-1 = none)."""
+    load_library().ssd_test_set_forward_wait(int(wait_ns), int(hold_unit))
 
 
 def _ptr(t: Optional[torch.Tensor]):
