@@ -162,11 +162,19 @@ ssd_status_t ssd_chunk_scan_fwd_ex(
  * is launched; the scratch needed is about 4 * nheads * headdim * dstate
  * bytes per chunk of every sequence.  The first call on a device looks up
  * the array's device address (cudaGetSymbolAddress, with that device
- * current) and caches it; make that first call before any stream capture.
- * Every call shares the one array and nothing in it needs to start at zero;
- * calls whose GPU work overlaps in time (other streams, other threads) race
- * on it and must be serialised by the caller.  No allocation of any kind is
- * made, neither by the library nor by any library it calls.
+ * current) and caches it.  With lazy module loading (the CUDA default) that
+ * first lookup is also when the driver loads the library's device code on
+ * that device and reserves the 16 MiB: a one-time step that may
+ * synchronise the device.  Make the first call during set-up -- before any
+ * stream capture and outside latency-critical loops; from then on the
+ * memory stays reserved until the process exits.  The cached address
+ * belongs to the device's current context: do not use this entry point
+ * across a cudaDeviceReset (or anything else that destroys and recreates
+ * the primary context) in the same process.  Every call shares the one
+ * array and nothing in it needs to start at zero; calls whose GPU work
+ * overlaps in time (other streams, other threads) race on it and must be
+ * serialised by the caller.  After that first call no allocation of any
+ * kind is made, neither by the library nor by any library it calls.
  */
 ssd_status_t ssd_chunk_scan_fwd_noalloc(
     const void *x, const void *dt, const float *A, const void *B, const void *C,

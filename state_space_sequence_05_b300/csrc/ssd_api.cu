@@ -180,11 +180,11 @@ ssd_status_t ssd_chunk_scan_fwd_ex(const void* x, const void* dt, const float* A
   if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), a.stream) != cudaSuccess)
     return SSD_ERR_CUDA;
   if (a.nseq == 0) return SSD_OK;
-  if (ssd::tc2_supported(a) && !legacy_tc()) {
-    const unsigned long long w = g_wait_ns.load(std::memory_order_relaxed);
-    return ssd::tc2_forward(a, w ? w : 2000000000ull, g_hold_unit.load(std::memory_order_relaxed));
-  }
-  return ssd::tc_supported(a) ? ssd::tc_forward(a) : ssd::simt_forward(a);
+  const unsigned long long w = g_wait_ns.load(std::memory_order_relaxed);
+  const unsigned long long wait_ns = w ? w : 2000000000ull;
+  const int hold = g_hold_unit.load(std::memory_order_relaxed);
+  if (ssd::tc2_supported(a) && !legacy_tc()) return ssd::tc2_forward(a, wait_ns, hold);
+  return ssd::tc_supported(a) ? ssd::tc_forward(a, wait_ns, hold) : ssd::simt_forward(a);
 }
 
 void ssd_test_set_forward_wait(unsigned long long wait_ns, int hold_unit) {

@@ -66,10 +66,14 @@ ssd_status_t check_fwd_args(const FwdArgs& a, bool check_ptrs);
 size_t simt_workspace_bytes(const FwdArgs& a);
 ssd_status_t simt_forward(const FwdArgs& a);
 
-// tcgen05 tensor-core forward: bf16 in, headdim 64, dstate 128.
+// tcgen05 tensor-core forward: bf16 in, headdim 64, dstate 128, with the
+// fused-epilogue options.  Every device wait is bounded by `wait_ns`;
+// `hold_unit` >= 0 names a work unit that never publishes its segment end
+// state (a test hook: its successor's wait runs out and the call reports
+// SSD_ERR_TIMEOUT).
 bool tc_supported(const FwdArgs& a);
 size_t tc_workspace_bytes(const FwdArgs& a);
-ssd_status_t tc_forward(const FwdArgs& a);
+ssd_status_t tc_forward(const FwdArgs& a, unsigned long long wait_ns, int hold_unit);
 
 // Pipelined tcgen05 forward (the same shapes, no fused-epilogue options).
 // Every device wait is bounded by `wait_ns`; `hold_unit` >= 0 names a work

@@ -146,6 +146,8 @@ struct Params {
   int32_t* status;
   int H, G, seg;
   int y_v8;             // y is 32-byte aligned: 32-byte stores
+  unsigned long long wait_ns;  // bound on every wait
+  int hold_unit;        // test hook: this unit never publishes its end state (-1: none)
 };
 
 // Fused epilogue options (ssd_fwd_epilogue_t), read by the epilogue kernel
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // hand this chunk over through stage it & 1
       const int st = it & 1;
-      if (it >= 2 && !wait_bar_warp(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1)) {
+      if (it >= 2 && !wait_bar_warp(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1, prm.wait_ns)) {
         if (lane == 0) fail(SSD_ERR_TIMEOUT);
         ok = false;
         break;
@@ -465,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // sentinel: no more work
     const int st = it & 1;
-    if (ok && (it < 2 || wait_bar_warp(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1))) {
+    if (ok && (it < 2 || wait_bar_warp(&bars[kEmpty0 + st], ((it >> 1) - 1) & 1, prm.wait_ns))) {
       if (lane == 0) {
         sm.info(st)->kind = kKindEnd;
         mbar_arrive(&bars[kFull0 + st]);
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) fail(SSD_ERR_TIMEOUT);
       // aborting: loads still in flight must land before the CTA may exit
       for (uint32_t q = (it >= 2 ? it - 2 : 0); q < it; ++q)
-        (void)wait_bar(&bars[kFull0 + (q & 1)], (q >> 1) & 1);
+        (void)wait_bar(&bars[kFull0 + (q & 1)], (q >> 1) & 1, prm.wait_ns);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -487,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, bt = 0, xu = 0, xu1 = 0, sa = 0;
       bool issued = false;
 #define MMA_WAIT(bar, par)            \
-  if (!wait_bar(&bars[bar], (par))) { \
+  if (!wait_bar(&bars[bar], (par), prm.wait_ns)) { \
     fail(SSD_ERR_TIMEOUT);            \
     break;                            \
   }
@@ -616,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             progressed = true;
           }
           if (!progressed) {
-            if (*abort_v || gtime() - tw > kWaitNs) {
+            if (*abort_v || gtime() - tw > prm.wait_ns) {
               timed_out = true;
               break;
             }
@@ -645,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (issued) {
         // every MMA issued must complete before TMEM is released
         mma_commit(&bars[kMmaDone]);
-        if (!wait_bar(&bars[kMmaDone], 0)) fail(SSD_ERR_TIMEOUT);
+        if (!wait_bar(&bars[kMmaDone], 0, prm.wait_ns)) fail(SSD_ERR_TIMEOUT);
       }
     }
   } else {
@@ -700,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and 2 cq + 1 of its rows.
     auto build_mask = [&](uint32_t pbt, int stg, float c2r, float Dh, bool ez) -> bool {
       const float* c2 = sm.c2(stg);
-      if (!wait_bar_warp(&bars[kCbFull0 + (pbt & 1)], (pbt >> 1) & 1)) return false;
+      if (!wait_bar_warp(&bars[kCbFull0 + (pbt & 1)], (pbt >> 1) & 1, prm.wait_ns)) return false;
       tc_fence_after();
       const uint32_t cbcol = tmem + kColCB + (pbt & 1) * 128 + lane_addr;
       const int b = 32 * wq;   // first row of this warp's lanes
@@ -843,14 +845,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // the Xw buffer once the tensor core has read its previous contents
     auto store_xw = [&](const uint32_t (&ph)[8], const uint32_t (&pl)[8]) -> bool {
-      if (xu >= 1 && !wait_bar_warp(&bars[kXwEmpty], (xu - 1) & 1)) return false;
+      if (xu >= 1 && !wait_bar_warp(&bars[kXwEmpty], (xu - 1) & 1, prm.wait_ns)) return false;
       if (ypend) {
         // the buffer also stages the previous chunk's y for its TMA stores:
         // every warp's store must have read it
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
         if (!arrive_seq(kYRead, ny)) return false;
-        if (!wait_bar_warp(&bars[kYRead], ny & 1)) return false;
+        if (!wait_bar_warp(&bars[kYRead], ny & 1, prm.wait_ns)) return false;
         ++ny;
         ypend = false;
       }
@@ -871,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (the last forward chunk's C H^T has completed: its accumulators were
     // waited for)
     auto store_xw1 = [&](const uint32_t (&ph)[8], const uint32_t (&pl)[8]) -> bool {
-      if (xu1 >= 1 && !wait_bar_warp(&bars[kXwEmpty1], (xu1 - 1) & 1)) return false;
+      if (xu1 >= 1 && !wait_bar_warp(&bars[kXwEmpty1], (xu1 - 1) & 1, prm.wait_ns)) return false;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const uint32_t off = sw128_offset(r, 2 * cq + c);
@@ -911,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     goto math_done;        \
   }
     while (true) {
-      MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
+      MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1, prm.wait_ns));
       const TileInfo* u0p = sm.info(it & 1);
       if (u0p->kind == kKindEnd || __any_sync(0xffffffffu, *abort_v)) break;
       const int h = u0p->h;
@@ -940,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* stb = prm.stbuf + (long long)blockIdx.x * kStSlots * kPN + (16 * cq) * kN + r;
       // fold pass-A chunk `kk` (its product is in S-column buffer `sa_m & 1`)
       auto fold = [&](int kk, float c2l_kk) -> bool {
-        if (!wait_bar_warp(&bars[kSaFull0 + (sa_m & 1)], (sa_m >> 1) & 1)) return false;
+        if (!wait_bar_warp(&bars[kSaFull0 + (sa_m & 1)], (sa_m >> 1) & 1, prm.wait_ns)) return false;
         tc_fence_after();
         float hi[16], lo[16];
         const uint32_t col = tmem + kColSA + (sa_m & 1) * 128 + lane_addr + 16 * cq;
@@ -965,7 +967,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       float c2l_prev = 0.f;
       for (int k = 0; k < nA; ++k) {
-        if (k > 0) MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
+        if (k > 0) MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1, prm.wait_ns));
         float c2l, c2r, er;
         chunk_vals(it & 1, c2l, c2r, er);
         uint32_t ph[8], pl[8];
@@ -996,13 +998,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
           const unsigned long long t0 = gtime();
           while (ld_acquire(prm.flags + pred) == 0) {
-            if (gtime() - t0 > kWaitNs) {
+            if (gtime() - t0 > prm.wait_ns) {
               fail(SSD_ERR_TIMEOUT);
               break;
             }
           }
         }
-        MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1));
+        MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1, prm.wait_ns));
         ++nhand;
         if (__any_sync(0xffffffffu, *abort_v)) goto math_done;
         const float* src = prm.slots + (long long)pred * kPN;
@@ -1019,7 +1021,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __stcg(dst + (16 * cq + q) * kN + r, aseg * hreg[q] + hloc[q]);
       }
       // the running state H_in, split into bf16 hi/lo, to the B operand of C H^T
-      if (bt >= 1) MATH_TRY(wait_bar_warp(&bars[kHEmpty], (bt - 1) & 1));
+      if (bt >= 1) MATH_TRY(wait_bar_warp(&bars[kHEmpty], (bt - 1) & 1, prm.wait_ns));
       store_ht();
       MATH_TRY(arrive_seq(kHFull, bt));
 
@@ -1029,7 +1031,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (first token, length, decay, exp(cum)) are kept in registers; its
       // state product comes from the scratch the segment-state pass filled.
       {
-        MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1));
+        MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], (it >> 1) & 1, prm.wait_ns));
         const TileInfo* ci = sm.info(it & 1);
         const int nB = ci->cnt;
         const int s_seq = ci->s, last_seg = ci->last_seg;
@@ -1046,12 +1048,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!u_last) {
           __threadfence();
-          MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1));
+          MATH_TRY(math_sync(&bars[kSyncHand], nhand & 1, prm.wait_ns));
           ++nhand;
-          if (tid == 0) st_release(prm.flags + u_unit, 1);
+          if (tid == 0 && u_unit != prm.hold_unit) st_release(prm.flags + u_unit, 1);
         }
         if (nB > 1) {
-          MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1));
+          MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1, prm.wait_ns));
           float c2l, c2r, er;
           chunk_vals((it + 1) & 1, c2l, c2r, er);
           MATH_TRY(build_mask(bt + 1, (it + 1) & 1, c2r, Dh, sm.info((it + 1) & 1)->ez != 0));
@@ -1083,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // this chunk's accumulators
-          MATH_TRY(wait_bar_warp(&bars[kAccFull], bt & 1));
+          MATH_TRY(wait_bar_warp(&bars[kAccFull], bt & 1, prm.wait_ns));
           tc_fence_after();
           const float ei = ei_cur;
           float* yrow = prm.y + ((t0_cur + r) * prm.H + h) * kP + 16 * cq;
@@ -1156,7 +1158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane < 16) discard_l2_line(stb - lane + (long long)t * kPN + lane * kN);
           if (more) {
-            MATH_TRY(wait_bar_warp(&bars[kHEmpty], bt & 1));
+            MATH_TRY(wait_bar_warp(&bars[kHEmpty], bt & 1, prm.wait_ns));
             store_ht();
             MATH_TRY(arrive_seq(kHFull, bt + 1));
           } else if (last_seg && prm.final_states) {
@@ -1212,7 +1214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (t + 2 < nB) {
             // chunk t+2's mask, in the stage chunk t has handed back
-            MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 2) & 1)], ((it + 2) >> 1) & 1));
+            MATH_TRY(wait_bar_warp(&bars[kFull0 + ((it + 2) & 1)], ((it + 2) >> 1) & 1, prm.wait_ns));
             float c2l, c2r, er;
             chunk_vals((it + 2) & 1, c2l, c2r, er);
             MATH_TRY(build_mask(bt + 2, (it + 2) & 1, c2r, Dh, sm.info((it + 2) & 1)->ez != 0));
@@ -1264,7 +1266,7 @@ bool tc_supported(const FwdArgs& a) {
 
 size_t tc_workspace_bytes(const FwdArgs& a) { return ws_layout(a).total; }
 
-ssd_status_t tc_forward(const FwdArgs& a) {
+ssd_status_t tc_forward(const FwdArgs& a, unsigned long long wait_ns, int hold_unit) {
   const WsLayout L = ws_layout(a);
   char* ws = static_cast<char*>(a.ws);
   int32_t* uoff = reinterpret_cast<int32_t*>(ws + L.uoff);
@@ -1311,6 +1313,8 @@ ssd_status_t tc_forward(const FwdArgs& a) {
   p.G = a.G;
   p.seg = seg;
   p.y_v8 = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
+  p.wait_ns = wait_ns;
+  p.hold_unit = hold_unit;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {

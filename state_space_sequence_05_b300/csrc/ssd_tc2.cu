@@ -46,16 +46,24 @@
 //      granularity;
 //   B. runs the forward over its chunks from H_in with the kept chunk states.
 //
-// Roles (one persistent CTA per SM, 576 threads):
-//   warp 16    producer: TMA loads of C, B, x tiles (128-byte swizzle) into a
-//              2-stage ring, the chunk's decay tables, and -- as soon as a
-//              forward chunk's tiles land -- its C B^T product.
+// Shared memory holds two rings that turn over at different rates: C/B slots
+// (a chunk's C and B tiles; in the segment-state pass the C half holds the
+// chunk's w o X instead) are handed back once the chunk's C B^T and C H^T
+// products have read them -- early, since the state chain needs no
+// product of the forward pass -- and x slots (with the chunk's decay
+// tables) once its S' X product has.
+//
+// Roles (one persistent CTA per SM, 608 threads):
+//   warp 16    producer: TMA loads of C, B, x tiles (128-byte swizzle) and
+//              the chunk's decay tables.
 //   warp 17    MMA issuer (the whole warp; one elected lane issues): the
-//              chunk-state products and each forward chunk's accumulator.
+//              chunk-state products, C H^T and S' X.
+//   warp 18    C B^T issuer: each forward chunk's C B^T as soon as its tiles
+//              land.
 //   warps 0-15 CUDA-core math (tensor-memory lane quarter w % 4, column
 //              quarter w / 4): w o X (bf16 hi/lo), the decay mask S' (in
-//              place over G in tensor memory), the fp32 running state, the
-//              epilogue.
+//              place over G in tensor memory), the fp32 running state chain,
+//              the epilogue.
 // Every wait is bounded; on expiry the kernel records SSD_ERR_TIMEOUT and
 // unwinds with all tensor memory freed.
 #include <cuda.h>
@@ -81,26 +89,29 @@ constexpr int kPN = kP * kN;
 constexpr int kMathWarps = 16;
 constexpr int kProducerWarp = 16;
 constexpr int kMmaWarp = 17;
-constexpr int kThreads = 576;
+constexpr int kGWarp = 18;
+constexpr int kThreads = 608;
 
-constexpr uint32_t kTile = 16384;                  // 128 rows x 128 bytes (bf16)
-constexpr uint32_t kStageBytes = 5 * kTile;        // C0 C1 B0 B1 X
-constexpr uint32_t kStageBytesA = 3 * kTile;       // B0 B1 X (segment-state pass)
-constexpr uint32_t kOffXw = 2 * kStageBytes;       // w o X, bf16 hi then lo
-constexpr uint32_t kOffHt = kOffXw + 2 * kTile;    // H^T, bf16 hi then lo
-constexpr uint32_t kOffTabs = kOffHt + 2 * kTile;  // per stage: c2, E (fp32), dt (bf16)
+constexpr uint32_t kTile = 16384;              // 128 rows x 128 bytes (bf16)
+constexpr int kCB = 2;                         // C/B slots: C0 C1 B0 B1 (64 KB)
+constexpr int kXS = 3;                         // x slots (16 KB) with decay tables
+constexpr uint32_t kCBBytes = 4 * kTile;
+constexpr uint32_t kOffX = kCB * kCBBytes;     // x slots
+constexpr uint32_t kOffHt = kOffX + kXS * kTile;  // H^T, bf16 hi then lo
+constexpr uint32_t kOffTabs = kOffHt + 2 * kTile; // per x slot: c2, E (fp32), dt (bf16)
 constexpr uint32_t kTabBytes = 128 * 4 + 128 * 4 + 128 * 2;
-constexpr uint32_t kOffInfo = kOffTabs + 2 * kTabBytes;
-constexpr uint32_t kOffBars = kOffInfo + 2 * 64;
-constexpr uint32_t kBarBytes = 20 * 8;
+constexpr uint32_t kOffInfo = kOffTabs + kXS * kTabBytes;
+constexpr uint32_t kOffBars = kOffInfo + kXS * 64;
+constexpr uint32_t kBarBytes = 32 * 8;
 constexpr uint32_t kSmemBytes = kOffBars + kBarBytes + 16;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
+static_assert(kOffTabs % 16 == 0 && kOffBars % 8 == 0, "alignment");
 
 // Tensor memory columns (128 lanes x 512 columns of 32 bits).
 //   S buffers (2 x 128): G = C B^T, overwritten in place by S' (hi/lo pairs).
 //   accumulators (2 x 128): a chunk-state product [B^T (w o X)_hi |
 //   B^T (w o X)_lo] (lane n, column p of each half) in the segment-state
-//   pass, or a forward accumulator [S' X + C H_hi^T | C H_lo^T] (lane i,
+//   pass, or a forward accumulator [C H_hi^T + S' X | C H_lo^T] (lane i,
 //   column p of each half).
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColAcc = 256;
@@ -146,44 +157,53 @@ struct Params {
 
 // barrier indices
 enum {
-  kFull0 = 0, kFull1, kEmpty0, kEmpty1,   // TMA stage ring
-  kGFull0, kGFull1,                       // C B^T in S buffer b (producer's MMA commit)
-  kSFull0, kSFull1, kSFree0, kSFree1,     // S' written (math) / S buffer read by Acc (MMA)
-  kXwFull, kXwFree, kHtFull, kHtFree,     // w o X and H^T operand tiles
-  kAccFull0, kAccFull1, kAccFree0, kAccFree1,  // accumulators (state products, forward)
-  kSync,                                  // math-warp rendezvous (hand-off)
-  kMmaDone,                               // both issuers' last products
+  kCbFull0 = 0, kCbFull1,             // C/B slot loaded (TMA)
+  kCbEmpty0, kCbEmpty1,               // C/B slot read (producer's and MMA issuer's commits)
+  kXFull0, kXFull1, kXFull2,          // x slot loaded (TMA) and its tables written
+  kXEmpty0, kXEmpty1, kXEmpty2,       // x slot done with (math warps + MMA commit)
+  kWxFull0, kWxFull1,                 // w o X written into C/B slot (segment-state pass)
+  kGFull0, kGFull1,                   // C B^T in S buffer (producer's commit)
+  kSFull0, kSFull1, kSFree0, kSFree1, // S' written (math) / S buffer read by S' X
+  kHtFull, kHtFree,                   // H^T operand tiles
+  kAccFull0, kAccFull1, kAccFree0, kAccFree1,
+  kSync,                              // math-warp rendezvous
+  kMmaDone,                           // both issuers' last products
   kNumBars
 };
 static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
 
 struct Smem {
   uint8_t* base;
-  __device__ uint8_t* stage(int s) const { return base + s * kStageBytes; }
-  __device__ uint8_t* C(int s, int half) const { return stage(s) + half * kTile; }
-  __device__ uint8_t* B(int s, int half) const { return stage(s) + (2 + half) * kTile; }
-  __device__ uint8_t* X(int s) const { return stage(s) + 4 * kTile; }
-  __device__ uint8_t* Xw() const { return base + kOffXw; }
+  __device__ uint8_t* C(int cb, int half) const { return base + cb * kCBBytes + half * kTile; }
+  __device__ uint8_t* B(int cb, int half) const { return base + cb * kCBBytes + (2 + half) * kTile; }
+  // w o X of a segment-state chunk, hi then lo, in its slot's C half
+  __device__ uint8_t* W(int cb) const { return base + cb * kCBBytes; }
+  __device__ uint8_t* X(int xs) const { return base + kOffX + xs * kTile; }
   __device__ uint8_t* Ht() const { return base + kOffHt; }
-  // cumulative log2-decay of the chunk in stage s: c2[j] = sum_{k<=j} dt_k A log2(e)
-  __device__ float* c2(int s) const {
-    return reinterpret_cast<float*>(base + kOffTabs + s * kTabBytes);
+  // cumulative log2-decay of the chunk in x slot xs: c2[j] = sum_{k<=j} dt_k A log2(e)
+  __device__ float* c2(int xs) const {
+    return reinterpret_cast<float*>(base + kOffTabs + xs * kTabBytes);
   }
   // E[j] = exp(-cum_j) dt_j (0 beyond the valid rows; may be inf where unused)
-  __device__ float* E(int s) const {
-    return reinterpret_cast<float*>(base + kOffTabs + s * kTabBytes + 512);
+  __device__ float* E(int xs) const {
+    return reinterpret_cast<float*>(base + kOffTabs + xs * kTabBytes + 512);
   }
-  // dt of the chunk in stage s (0 beyond the valid rows)
-  __device__ __nv_bfloat16* dt(int s) const {
-    return reinterpret_cast<__nv_bfloat16*>(base + kOffTabs + s * kTabBytes + 1024);
+  // dt of the chunk (0 beyond the valid rows)
+  __device__ __nv_bfloat16* dt(int xs) const {
+    return reinterpret_cast<__nv_bfloat16*>(base + kOffTabs + xs * kTabBytes + 1024);
   }
-  __device__ TileInfo* info(int s) const {
-    return reinterpret_cast<TileInfo*>(base + kOffInfo) + s;
+  __device__ TileInfo* info(int xs) const {
+    return reinterpret_cast<TileInfo*>(base + kOffInfo) + xs;
   }
 };
 
 // Parity of the completion of use `u` of a barrier that completes once per use.
 __device__ __forceinline__ uint32_t par_of(uint32_t u) { return u & 1u; }
+// Ring position of chunk number `it`: the C/B slot it % 2 (use it / 2 of
+// that slot's barriers), the x slot it % 3 (use it / 3).
+__device__ __forceinline__ uint32_t cb_par(uint32_t it) { return (it >> 1) & 1u; }
+__device__ __forceinline__ int x_slot(uint32_t it) { return (int)(it % 3u); }
+__device__ __forceinline__ uint32_t x_par(uint32_t it) { return (it / 3u) & 1u; }
 // For a pair of barriers alternating between two buffers: parity of use `u`
 // on barrier (u & 1).
 __device__ __forceinline__ uint32_t par2_of(uint32_t u) { return (u >> 1) & 1u; }
@@ -207,24 +227,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const unsigned long long wns = prm.wait_ns;
 
   if (tid == 0) {
-    mbar_init(&bars[kFull0], 2);  // expect-tx arrival + decay tables written
-    mbar_init(&bars[kFull1], 2);
-    mbar_init(&bars[kEmpty0], 1 + kMathWarps);
-    mbar_init(&bars[kEmpty1], 1 + kMathWarps);
-    mbar_init(&bars[kGFull0], 1);
-    mbar_init(&bars[kGFull1], 1);
-    mbar_init(&bars[kSFull0], kMathWarps);
-    mbar_init(&bars[kSFull1], kMathWarps);
-    mbar_init(&bars[kSFree0], 1);
-    mbar_init(&bars[kSFree1], 1);
-    mbar_init(&bars[kXwFull], kMathWarps);
-    mbar_init(&bars[kXwFree], 1);
+    for (int b = 0; b < kCB; ++b) {
+      mbar_init(&bars[kCbFull0 + b], 1);   // expect-tx arrival
+      mbar_init(&bars[kCbEmpty0 + b], 2);  // producer (G product or plain) + MMA issuer
+      mbar_init(&bars[kWxFull0 + b], kMathWarps);
+      mbar_init(&bars[kGFull0 + b], 1);
+      mbar_init(&bars[kSFull0 + b], kMathWarps);
+      mbar_init(&bars[kSFree0 + b], 1);
+      mbar_init(&bars[kAccFull0 + b], 1);
+      mbar_init(&bars[kAccFree0 + b], kMathWarps);
+    }
+    for (int b = 0; b < kXS; ++b) {
+      mbar_init(&bars[kXFull0 + b], 2);               // expect-tx arrival + tables written
+      mbar_init(&bars[kXEmpty0 + b], kMathWarps + 1);  // math warps + MMA issuer
+    }
     mbar_init(&bars[kHtFull], kMathWarps);
     mbar_init(&bars[kHtFree], 1);
-    mbar_init(&bars[kAccFull0], 1);
-    mbar_init(&bars[kAccFull1], 1);
-    mbar_init(&bars[kAccFree0], kMathWarps);
-    mbar_init(&bars[kAccFree1], kMathWarps);
     mbar_init(&bars[kSync], kMathWarps);
     mbar_init(&bars[kMmaDone], 2);
     *abort_p = 0;
@@ -254,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nunits = prm.uoff[nseq];
   const bool plan_ok = prm.uoff[nseq + 1] == 0;
 
-  // C B^T: 128 x 128 x 128 from the stage's C and B tiles (both K-major).
+  // C B^T: 128 x 128 x 128 from the slot's C and B tiles (both K-major).
   constexpr uint32_t idG = idesc_bf16(128, 128, false, false);
   // chunk states: B^T (MN-major, M = n) times [w o X hi | lo] (MN-major, N = 128).
   constexpr uint32_t idSt = idesc_bf16(128, 128, true, true);
@@ -262,13 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // S' (tensor memory) times X (MN-major, N = 64) into the first half.
   constexpr uint32_t idCH = idesc_bf16(128, 128, false, true);
   constexpr uint32_t idSX = idesc_bf16(128, 64, false, true);
+  constexpr uint64_t kT16 = kTile >> 4;  // one tile, in descriptor address units
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    // Walks the ring one chunk at a time: a work unit (ticket), then its
-    // segment-state chunks (backwards), then its forward chunks.  Lane 0
-    // issues the TMA loads; the whole warp writes the chunk's decay tables;
-    // lane 0 then issues a forward chunk's C B^T once its tiles have landed.
+    // Walks the chunks of each work unit (ticket): its segment-state chunks
+    // (backwards), then its forward chunks.  Lane 0 issues the TMA loads;
+    // the whole warp writes the chunk's decay tables; one lane issues a
+    // forward chunk's C B^T once its tiles have landed.
     if (lane == 0) {
       prefetch_tmap(&map_x);
       prefetch_tmap(&map_b);
@@ -300,16 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       X.n = X.te - X.tb;
       return true;
     };
-    // first token, kind and valid rows of chunk k of unit X: the segment-
-    // state chunks (backwards), then the forward chunks
     auto tile_of = [&](const PUnit& X, int k, long long& t0, int& kind, int& len) {
       kind = k < X.n ? kKindA : kKindB;
       const int t = kind == kKindA ? X.te - 1 - k : X.tb + (k - X.n);
       t0 = X.b + (long long)t * kQ;
       len = (int)min((long long)kQ, X.e - t0);
     };
-    uint32_t it = 0, gu = 0;
-    bool ok = true, issued = false;
+    uint32_t it = 0;
+    bool ok = true;
     PUnit U;
     int k = 0;
     bool have = plan_ok && draw(U);
@@ -338,7 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         dcur[q] = dpre[q];
         dv[q] = __bfloat162float(dpre[q]);
       }
-      // advance, and start the next chunk's dt loads
       if (++k >= 2 * U.n) {
         k = 0;
         have = draw(U);
@@ -347,27 +363,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_of(U, k, nt0, nkind, nlen);
         load_dt(U, nt0, nlen);
       }
-      const int st = it & 1;
-      if (it >= 2 && !wait_bar_warp(&bars[kEmpty0 + st], par2_of(it - 2), wns)) {
+      const int cb = it & 1, xs = x_slot(it);
+      bool good = it < kCB || wait_bar_warp(&bars[kCbEmpty0 + cb], cb_par(it - kCB), wns);
+      if (good && it >= kXS) good = wait_bar_warp(&bars[kXEmpty0 + xs], x_par(it - kXS), wns);
+      if (!good) {
         if (lane == 0) fail(SSD_ERR_TIMEOUT);
         ok = false;
         break;
       }
       if (__any_sync(0xffffffffu, *abort_v)) { ok = false; break; }
-      uint64_t* fb = &bars[kFull0 + st];
+      uint64_t* fcb = &bars[kCbFull0 + cb];
+      uint64_t* fx = &bars[kXFull0 + xs];
       if (lane == 0) {
         const int row = (int)t0;
-        mbar_arrive_expect_tx(fb, kind == kKindB ? kStageBytes : kStageBytesA);
-        tma_load_2d(sm.X(st), &map_x, fb, C.h * kP, row);
-        tma_load_2d(sm.B(st, 0), &map_b, fb, C.g * kN, row);
-        tma_load_2d(sm.B(st, 1), &map_b, fb, C.g * kN + 64, row);
+        mbar_arrive_expect_tx(fx, kTile);
+        tma_load_2d(sm.X(xs), &map_x, fx, C.h * kP, row);
+        mbar_arrive_expect_tx(fcb, kind == kKindB ? 4 * kTile : 2 * kTile);
+        tma_load_2d(sm.B(cb, 0), &map_b, fcb, C.g * kN, row);
+        tma_load_2d(sm.B(cb, 1), &map_b, fcb, C.g * kN + 64, row);
         if (kind == kKindB) {
-          tma_load_2d(sm.C(st, 0), &map_c, fb, C.g * kN, row);
-          tma_load_2d(sm.C(st, 1), &map_c, fb, C.g * kN + 64, row);
+          tma_load_2d(sm.C(cb, 0), &map_c, fcb, C.g * kN, row);
+          tma_load_2d(sm.C(cb, 1), &map_c, fcb, C.g * kN + 64, row);
         }
         // the next chunk's x into L2 behind this chunk's loads
         if (have) tma_prefetch_2d(&map_x, U.h * kP, (int)nt0);
-        TileInfo* inf = sm.info(st);
+        TileInfo* inf = sm.info(xs);
         inf->t0 = t0;
         inf->s = C.s;
         inf->h = C.h;
@@ -392,63 +412,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane >= o) incl += tv;
       }
       const float excl = incl - run;
-      float* c2t = sm.c2(st);
-      float* Et = sm.E(st);
+      float* c2t = sm.c2(xs);
+      float* Et = sm.E(xs);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float cq2 = excl + pre[q];
         c2t[4 * lane + q] = cq2;
         Et[4 * lane + q] = 4 * lane + q < len ? fast_exp2(-cq2) * dv[q] : 0.f;
-        sm.dt(st)[4 * lane + q] = dcur[q];
+        sm.dt(xs)[4 * lane + q] = dcur[q];
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(fb);
-      if (kind == kKindB) {
-        // C B^T of this forward chunk into S buffer gu & 1, once its tiles
-        // have landed and the buffer's previous S' has been read
-        bool good = wait_bar_warp(fb, par2_of(it), wns);
-        if (good && gu >= 2) good = wait_bar_warp(&bars[kSFree0 + (gu & 1)], par2_of(gu - 2), wns);
-        if (!good) {
-          if (lane == 0) fail(SSD_ERR_TIMEOUT);
-          ok = false;
-          ++it;
-          break;
-        }
-        tc_fence_after();
-        if (elect_one()) {
-          const uint32_t sbase = smem_u32(smem_raw) + st * kStageBytes;
-          const uint64_t dC0 = sdesc_sw128(sbase, 16, 1024);
-          const uint64_t dB0 = sdesc_sw128(sbase + 2 * kTile, 16, 1024);
-          const uint32_t d = tmem + kColS + (gu & 1) * 128;
-          // K steps of 32 bytes inside each 64-column half tile (C0/B0, then C1/B1)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16(d, dC0 + (kk >> 2) * (kTile >> 4) + (kk & 3) * 2,
-                     dB0 + (kk >> 2) * (kTile >> 4) + (kk & 3) * 2, idG, kk > 0);
-          mma_commit(&bars[kGFull0 + (gu & 1)]);
-        }
-        __syncwarp();
-        issued = true;
-        ++gu;
-      }
+      if (lane == 0) mbar_arrive(fx);
       ++it;
     }
-    // sentinel: no more work
-    const int st = it & 1;
-    if (ok && (it < 2 || wait_bar_warp(&bars[kEmpty0 + st], par2_of(it - 2), wns))) {
+    // sentinel: no more work (in the next x slot)
+    const int xs = x_slot(it);
+    if (ok && (it < kXS || wait_bar_warp(&bars[kXEmpty0 + xs], x_par(it - kXS), wns))) {
       if (lane == 0) {
-        sm.info(st)->kind = kKindEnd;
-        mbar_arrive(&bars[kFull0 + st]);
-        mbar_arrive(&bars[kFull0 + st]);
+        sm.info(xs)->kind = kKindEnd;
+        mbar_arrive(&bars[kXFull0 + xs]);
+        mbar_arrive(&bars[kXFull0 + xs]);
       }
     } else if (lane == 0) {
       if (ok) fail(SSD_ERR_TIMEOUT);
       // aborting: loads still in flight must land before the CTA may exit
-      for (uint32_t q = (it >= 2 ? it - 2 : 0); q < it; ++q)
-        (void)wait_bar(&bars[kFull0 + (q & 1)], par2_of(q), wns);
+      for (uint32_t q = (it >= kXS ? it - kXS : 0); q < it; ++q)
+        (void)wait_bar(&bars[kXFull0 + x_slot(q)], x_par(q), wns);
+      for (uint32_t q = (it >= kCB ? it - kCB : 0); q < it; ++q)
+        (void)wait_bar(&bars[kCbFull0 + (q & 1)], cb_par(q), wns);
+    }
+  } else if (warp == kGWarp) {
+    // ------------------------------------------------------------ C B^T issuer
+    // Follows the chunks through the x slots (the tile info): each forward
+    // chunk's C B^T once its C/B slot has landed and its S buffer is free;
+    // it also gives the C/B slot its first release arrival (for a segment-
+    // state chunk at once, for a forward chunk when C B^T has read it).
+    uint32_t it = 0, gu = 0;
+    bool issued = false;
+    while (true) {
+      const int cb = it & 1, xs = x_slot(it);
+      bool good = wait_bar_warp(&bars[kXFull0 + xs], x_par(it), wns);
+      if (!good) {
+        if (lane == 0) fail(SSD_ERR_TIMEOUT);
+        break;
+      }
+      const int kind = sm.info(xs)->kind;
+      if (kind == kKindEnd || *abort_v) break;
+      if (kind == kKindB) {
+        good = wait_bar_warp(&bars[kCbFull0 + cb], cb_par(it), wns);
+        if (good && gu >= 2) good = wait_bar_warp(&bars[kSFree0 + (gu & 1)], par2_of(gu - 2), wns);
+        if (!good) {
+          if (lane == 0) fail(SSD_ERR_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t dC0 = sdesc_sw128(smem_u32(sm.C(cb, 0)), 16, 1024);
+          const uint64_t dB0 = sdesc_sw128(smem_u32(sm.B(cb, 0)), 16, 1024);
+          const uint32_t d = tmem + kColS + (gu & 1) * 128;
+          // K steps of 32 bytes inside each 64-column half tile
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16(d, dC0 + (kk >> 2) * kT16 + (kk & 3) * 2,
+                     dB0 + (kk >> 2) * kT16 + (kk & 3) * 2, idG, kk > 0);
+          mma_commit(&bars[kGFull0 + (gu & 1)]);
+          mma_commit(&bars[kCbEmpty0 + cb]);
+        }
+        __syncwarp();
+        issued = true;
+        ++gu;
+      } else if (lane == 0) {
+        mbar_arrive(&bars[kCbEmpty0 + cb]);
+      }
+      ++it;
     }
     if (lane == 0) {
-      // this thread's products must complete before tensor memory is freed
+      // this warp's products must complete before tensor memory is freed
       if (issued) mma_commit(&bars[kMmaDone]);
       else mbar_arrive(&bars[kMmaDone]);
     }
@@ -456,20 +495,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop (waits and bookkeeping are warp-uniform,
     // so descriptors live in uniform registers); one elected lane issues.
-    // Shared-memory descriptors are built once per tile and advanced by
-    // constant offsets (a descriptor's address field is bytes >> 4).
-    const uint32_t sbase = smem_u32(smem_raw);
-    // stage 0 descriptors; stage 1 is kStageBytes further (no arrays indexed
-    // at run time: they would live in local memory)
-    const uint64_t dB0 = sdesc_sw128(sbase + 2 * kTile, kTile, 1024);  // MN-major B^T
-    const uint64_t dX0 = sdesc_sw128(sbase + 4 * kTile, kTile, 1024);  // MN-major x
-    const uint64_t dC0 = sdesc_sw128(sbase, 16, 1024);                 // K-major C
-    constexpr uint64_t kS16 = kStageBytes >> 4;
-    // [hi | lo] operands: two 64-column MN blocks one tile apart
-    const uint64_t dXw = sdesc_sw128(sbase + kOffXw, kTile, 1024);
-    const uint64_t dHt = sdesc_sw128(sbase + kOffHt, kTile, 1024);
-    constexpr uint64_t kT16 = kTile >> 4;  // one tile, in descriptor address units
-    uint32_t it = 0, xu = 0, hu = 0, gu = 0, au = 0;
+    // Descriptors are built once per buffer and advanced by constant
+    // offsets (a descriptor's address field is bytes >> 4).
+    const uint64_t dC0 = sdesc_sw128(smem_u32(sm.C(0, 0)), 16, 1024);       // K-major C
+    const uint64_t dBt0 = sdesc_sw128(smem_u32(sm.B(0, 0)), kTile, 1024);   // MN-major B^T
+    const uint64_t dW0 = sdesc_sw128(smem_u32(sm.W(0)), kTile, 1024);       // [w o X hi | lo]
+    const uint64_t dX0 = sdesc_sw128(smem_u32(sm.X(0)), kTile, 1024);       // MN-major x
+    const uint64_t dHt = sdesc_sw128(smem_u32(sm.Ht()), kTile, 1024);       // [H hi | lo]^T
+    constexpr uint64_t kCB16 = kCBBytes >> 4;
+    uint32_t it = 0, hu = 0, gu = 0, au = 0;
+    uint32_t wa0 = 0, wa1 = 0;  // segment-state chunks that used C/B slot 0 / 1
     bool issued = false;
 #define MMA_WAIT(bar, par)                      \
   if (!wait_bar_warp(&bars[bar], (par), wns)) { \
@@ -477,67 +512,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     goto mma_done;                              \
   }
     while (true) {
-      MMA_WAIT(kFull0 + (it & 1), par2_of(it));
-      if (sm.info(it & 1)->kind == kKindEnd || *abort_v) break;
-      const int n = sm.info(it & 1)->cnt;
-      // ---- segment-state pass: S_c = B^T [w o X hi | lo] per chunk, the
-      // w o X tiles alternating between the w o X and H^T buffers (H^T is
-      // not live before the hand-off)
+      MMA_WAIT(kXFull0 + x_slot(it), x_par(it));
+      if (sm.info(x_slot(it))->kind == kKindEnd || *abort_v) break;
+      const int n = sm.info(x_slot(it))->cnt;
+      // ---- segment-state pass: S_c = B^T [w o X hi | lo] per chunk
       for (int k = 0; k < n; ++k) {
-        if (k > 0) { MMA_WAIT(kFull0 + (it & 1), par2_of(it)); }
-        const int st = it & 1;
-        const bool use_xw = (k & 1) == 0;
-        if (use_xw) {
-          MMA_WAIT(kXwFull, par_of(xu));
-        } else {
-          MMA_WAIT(kHtFull, par_of(hu));
-        }
+        const int cb = it & 1, xs = x_slot(it);
+        uint32_t& wa = cb ? wa1 : wa0;
+        MMA_WAIT(kCbFull0 + cb, cb_par(it));
+        MMA_WAIT(kWxFull0 + cb, par_of(wa));
+        ++wa;
         if (au >= 2) { MMA_WAIT(kAccFree0 + (au & 1), par2_of(au - 2)); }
         tc_fence_after();
         if (elect_one()) {
           const uint32_t d = tmem + kColAcc + (au & 1) * 128;
-          const uint64_t dw = use_xw ? dXw : dHt;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16(d, dB0 + st * kS16 + kk * 128, dw + kk * 128, idSt, kk > 0);
-          mma_commit(&bars[use_xw ? kXwFree : kHtFree]);
-          mma_commit(&bars[kEmpty0 + st]);
+            mma_bf16(d, dBt0 + cb * kCB16 + kk * 128, dW0 + cb * kCB16 + kk * 128, idSt, kk > 0);
           mma_commit(&bars[kAccFull0 + (au & 1)]);
+          mma_commit(&bars[kCbEmpty0 + cb]);
+          mma_commit(&bars[kXEmpty0 + xs]);
         }
         __syncwarp();
         issued = true;
-        if (use_xw) ++xu; else ++hu;
         ++au;
         ++it;
       }
-      // ---- forward chunks: [S' X + C H_hi^T | C H_lo^T]
+      // ---- forward chunks: [C H_hi^T + S' X | C H_lo^T]
       for (int t = 0; t < n; ++t) {
-        MMA_WAIT(kFull0 + (it & 1), par2_of(it));
-        const int st = it & 1;
-        MMA_WAIT(kSFull0 + (gu & 1), par2_of(gu));
+        const int cb = it & 1, xs = x_slot(it);
+        MMA_WAIT(kCbFull0 + cb, cb_par(it));
         MMA_WAIT(kHtFull, par_of(hu));
         if (au >= 2) { MMA_WAIT(kAccFree0 + (au & 1), par2_of(au - 2)); }
         tc_fence_after();
+        const uint32_t d = tmem + kColAcc + (au & 1) * 128;
         if (elect_one()) {
-          const uint32_t d = tmem + kColAcc + (au & 1) * 128;
-          const uint32_t scol = tmem + kColS + (gu & 1) * 128;
           // C (K-major: K steps of 32 bytes inside each 64-column half tile)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16(d, dC0 + st * kS16 + (kk >> 2) * kT16 + (kk & 3) * 2, dHt + kk * 128, idCH, kk > 0);
+            mma_bf16(d, dC0 + cb * kCB16 + (kk >> 2) * kT16 + (kk & 3) * 2, dHt + kk * 128, idCH,
+                     kk > 0);
+          mma_commit(&bars[kHtFree]);
+          mma_commit(&bars[kCbEmpty0 + cb]);
+        }
+        __syncwarp();
+        MMA_WAIT(kXFull0 + xs, x_par(it));
+        MMA_WAIT(kSFull0 + (gu & 1), par2_of(gu));
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t scol = tmem + kColS + (gu & 1) * 128;
           // S' from tensor memory: K block kk (columns j = 16 kk .. 16 kk + 15)
           // holds 8 columns of hi pairs, then 8 of lo pairs
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_bf16_tmem_a(d, scol + 16 * kk + 8 * part, dX0 + st * kS16 + kk * 128, idSX, true);
+              mma_bf16_tmem_a(d, scol + 16 * kk + 8 * part, dX0 + xs * kT16 + kk * 128, idSX, true);
           mma_commit(&bars[kAccFull0 + (au & 1)]);
-          mma_commit(&bars[kHtFree]);
           mma_commit(&bars[kSFree0 + (gu & 1)]);
-          mma_commit(&bars[kEmpty0 + st]);
+          mma_commit(&bars[kXEmpty0 + xs]);
         }
         __syncwarp();
+        issued = true;
         ++gu;
         ++hu;
         ++au;
@@ -561,15 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cq = warp >> 2;
     const int r = 32 * q + lane;  // tensor-memory lane: token row i / state row n
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-    uint32_t it = 0, xu = 0, hu = 0, gu = 0, au = 0, nsync = 0;
+    uint32_t it = 0, hu = 0, gu = 0, au = 0, nsync = 0;
     // fp32 running state: pair k holds H[p][n = r] for p = 16 cq + 2k, 2k + 1
     f2 h2[8];
     // this thread's 16 values of a chunk state in the CTA's scratch: 64
     // contiguous bytes per thread (slot 0; slots are kPN floats apart)
     float* const stb = prm.stbuf + (long long)blockIdx.x * kStSlots * kPN + tid * 16;
-    // the same 64 bytes staged in shared memory (the w o X buffer, idle in
-    // the forward chunks) by cp.async
-    uint8_t* const sts = sm.Xw() + tid * 64;
 
     auto arrive = [&](int bar) {
       __syncwarp();
@@ -579,11 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one 16-byte work item of w o X (items k = 0..1023: 8 values of row
     // j = k / 8), weight w_j = exp2(wl - c2_j) dt_j, written as bf16 hi and
     // lo tiles at `dst`
-    auto wx_item = [&](int stg, int k, float wl, uint8_t* dst) {
+    auto wx_item = [&](int xs, int k, float wl, uint8_t* dst) {
       const int j = k >> 3, c = k & 7;
       const uint32_t off = sw128_offset(j, c);
-      const uint4 xv = *reinterpret_cast<const uint4*>(sm.X(stg) + off);
-      const float w = fast_exp2(wl - sm.c2(stg)[j]) * __bfloat162float(sm.dt(stg)[j]);
+      const uint4 xv = *reinterpret_cast<const uint4*>(sm.X(xs) + off);
+      const float w = fast_exp2(wl - sm.c2(xs)[j]) * __bfloat162float(sm.dt(xs)[j]);
       const f2 ww{w, w};
       uint4 hi, lo;
       split2p(mul2(bf2(xv.x), ww), hi.x, lo.x);
@@ -599,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 32 cq..), in two 16-column halves, each rewritten as one K block: 8
     // columns of hi pairs followed by 8 of lo pairs.  Blocks above the
     // diagonal become zeros.
-    auto build_mask = [&](uint32_t pgu, int stg, float c2r, float Dh) -> bool {
+    auto build_mask = [&](uint32_t pgu, int xs, float c2r, float Dh) -> bool {
       const int gb = pgu & 1;
       if (!wait_bar_warp(&bars[kGFull0 + gb], par2_of(pgu), wns)) return false;
       tc_fence_after();
@@ -626,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2 v[8];
           if (fast) {
             // every row's factor is exp(cum_i): S' = G E_j
-            const float4* E4 = reinterpret_cast<const float4*>(sm.E(stg) + j0);
+            const float4* E4 = reinterpret_cast<const float4*>(sm.E(xs) + j0);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
               const float4 e = E4[m];
@@ -635,8 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             // some rows decayed below 2^-60: exp2(c2_i - m_i - c2_j) dt_j per entry
-            const float4* c4 = reinterpret_cast<const float4*>(sm.c2(stg) + j0);
-            const uint2* d2 = reinterpret_cast<const uint2*>(sm.dt(stg) + j0);
+            const float4* c4 = reinterpret_cast<const float4*>(sm.c2(xs) + j0);
+            const uint2* d2 = reinterpret_cast<const uint2*>(sm.dt(xs) + j0);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
               const float4 cc = c4[m];
@@ -746,19 +779,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane < 16) discard_l2_line(stb - tid * 16 + (long long)slot * kPN + warp * 512 + lane * 32);
     };
-    // stage scratch slot `slot` (this thread's 64 bytes) in shared memory
-    auto stage_slot = [&](int slot) {
-      const float* src = stb + (long long)slot * kPN;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) cp_async16(sts + 16 * c, src + 4 * c);
-      cp_async_commit();
-    };
-    // the staged state, once its copy has landed
-    auto staged_state = [&](f2 (&sv)[8]) {
-      cp_async_wait_all();
+    // this thread's 16 values of the chunk state in scratch slot `slot`
+    auto load_slot = [&](int slot, f2 (&sv)[8]) {
+      const float4* src = reinterpret_cast<const float4*>(stb + (long long)slot * kPN);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const float4 t = *reinterpret_cast<const float4*>(sts + 16 * c);
+        const float4 t = __ldcg(src + c);
         sv[2 * c] = f2{t.x, t.y};
         sv[2 * c + 1] = f2{t.z, t.w};
       }
@@ -770,14 +796,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     goto math_done;        \
   }
     while (true) {
-      MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], par2_of(it), wns));
-      if (sm.info(it & 1)->kind == kKindEnd || __any_sync(0xffffffffu, *abort_v)) break;
-      const TileInfo u0 = *sm.info(it & 1);
+      MATH_TRY(wait_bar_warp(&bars[kXFull0 + x_slot(it)], x_par(it), wns));
+      if (sm.info(x_slot(it))->kind == kKindEnd || __any_sync(0xffffffffu, *abort_v)) break;
+      const TileInfo u0 = *sm.info(x_slot(it));
       const int h = u0.h, n = u0.cnt;
-      // the w o X buffer held the previous unit's staged chunk states: every
-      // math warp must be done with them before it is rewritten
-      MATH_TRY(math_sync(&bars[kSync], par_of(nsync), wns));
-      ++nsync;
       const float Dh = prm.D ? prm.D[h] : 0.f;
       // the initial state of a sequence's first segment: into L2 now, read at
       // the hand-off
@@ -788,7 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -------- segment-state pass: each chunk's state S_c (chunk-local
       // weights w_j = exp(cum_last - cum_j) dt_j), chunks walked backwards,
       // kept in scratch slot (its index in the segment) and folded into
-      // H_loc = sum_c exp(sum of the later chunks' dt A) S_c
+      // H_loc = sum_c exp(sum of the later chunks' dt A) S_c.  The w o X
+      // tiles go into the C half of the chunk's C/B slot.
       f2 hloc[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) hloc[k] = f2{0.f, 0.f};
@@ -807,28 +830,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       float c2l_prev = 0.f;
       for (int k = 0; k < n; ++k) {
-        if (k > 0) MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], par2_of(it), wns));
-        const int stg = it & 1;
-        const float c2l = sm.c2(stg)[kQ - 1];
-        const bool use_xw = (k & 1) == 0;
-        if (use_xw) {
-          if (xu >= 1) MATH_TRY(wait_bar_warp(&bars[kXwFree], par_of(xu - 1), wns));
-        } else {
-          if (hu >= 1) MATH_TRY(wait_bar_warp(&bars[kHtFree], par_of(hu - 1), wns));
-        }
-        uint8_t* dst = use_xw ? sm.Xw() : sm.Ht();
-        wx_item(stg, tid, c2l, dst);
-        wx_item(stg, tid + 512, c2l, dst);
+        const int cb = it & 1, xs = x_slot(it);
+        if (k > 0) MATH_TRY(wait_bar_warp(&bars[kXFull0 + xs], x_par(it), wns));
+        // the slot's B tile has landed, and with it the slot is free of its
+        // previous chunk: w o X may be written into its C half
+        MATH_TRY(wait_bar_warp(&bars[kCbFull0 + cb], cb_par(it), wns));
+        const float c2l = sm.c2(xs)[kQ - 1];
+        wx_item(xs, tid, c2l, sm.W(cb));
+        wx_item(xs, tid + 512, c2l, sm.W(cb));
         fence_proxy_async_smem();
-        arrive(use_xw ? kXwFull : kHtFull);
-        if (use_xw) ++xu; else ++hu;
-        arrive(kEmpty0 + stg);
+        arrive(kWxFull0 + cb);
+        arrive(kXEmpty0 + xs);
         // the previous chunk's product, read while this one's is computed
         if (k > 0) MATH_TRY(fold(k - 1, c2l_prev));
         c2l_prev = c2l;
         ++it;
       }
       MATH_TRY(fold(n - 1, c2l_prev));
+
+      // -------- the first forward chunk's mask does not need the incoming
+      // state: build it while the predecessor may still be publishing
+      const int xs0 = x_slot(it);
+      MATH_TRY(wait_bar_warp(&bars[kXFull0 + xs0], x_par(it), wns));
+      MATH_TRY(build_mask(gu, xs0, sm.c2(xs0)[r], Dh));
+      ++gu;
 
       // -------- segment hand-off
       if (u0.sigma == 0) {
@@ -876,49 +901,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the state entering the segment feeds the first chunk's C H^T
       MATH_TRY(put_ht());
 
-      // -------- forward chunks.  Iteration t: the mask of chunk t, then the
-      // state after chunk t-1 (H^T for chunk t's C H^T) and chunk t-1's y.
-      float a_prev = 0.f, f_prev = 0.f;
-      long long t0_prev = 0;
-      int len_prev = 0;
+      // -------- forward chunks.  Iteration t: the state after chunk t (H^T
+      // for chunk t + 1's C H^T), the mask of chunk t + 1, chunk t's y.
+      f2 sv[8];
+      load_slot(0, sv);
       for (int t = 0; t < n; ++t) {
-        // the previous chunk's state, from scratch (in flight during the mask)
-        if (t > 0) stage_slot(t - 1);
-        MATH_TRY(wait_bar_warp(&bars[kFull0 + (it & 1)], par2_of(it), wns));
-        const int stg = it & 1;
-        const float c2l = sm.c2(stg)[kQ - 1];
-        const float c2r = sm.c2(stg)[r];
-        const long long t0 = sm.info(stg)->t0;
-        const int len = sm.info(stg)->len;
-        // the mask (its C B^T was issued when the tiles landed)
-        MATH_TRY(build_mask(gu, stg, c2r, Dh));
-        ++gu;
-        arrive(kEmpty0 + stg);
-        if (t > 0) {
-          f2 sv[8];
-          staged_state(sv);
+        const int xs = x_slot(it);
+        // this chunk's values (its x slot is full: its mask was built)
+        const float a = fast_exp2(sm.c2(xs)[kQ - 1]);
+        const float f = fast_exp2(fmaxf(sm.c2(xs)[r], kDeep));
+        const long long t0 = sm.info(xs)->t0;
+        const int len = sm.info(xs)->len;
+        arrive(kXEmpty0 + xs);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) h2[k] = fma2(f2{a_prev, a_prev}, h2[k], sv[k]);
-          discard_slot(t - 1);
+        for (int k = 0; k < 8; ++k) h2[k] = fma2(f2{a, a}, h2[k], sv[k]);
+        discard_slot(t);
+        if (t + 1 < n) {
+          load_slot(t + 1, sv);  // in flight during the mask and the epilogue
           MATH_TRY(put_ht());
-          MATH_TRY(epilogue(f_prev, t0_prev, len_prev, h));
-        }
-        a_prev = fast_exp2(c2l);
-        f_prev = fast_exp2(fmaxf(c2r, kDeep));
-        t0_prev = t0;
-        len_prev = len;
-        ++it;
-      }
-      {
-        // the state after the last chunk (the sequence's final state when
-        // this is its last segment) and the last chunk's y
-        stage_slot(n - 1);
-        f2 sv[8];
-        staged_state(sv);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) h2[k] = fma2(f2{a_prev, a_prev}, h2[k], sv[k]);
-        discard_slot(n - 1);
-        if (u0.last_seg && prm.final_states) {
+          const int xn = x_slot(it + 1);
+          MATH_TRY(wait_bar_warp(&bars[kXFull0 + xn], x_par(it + 1), wns));
+          MATH_TRY(build_mask(gu, xn, sm.c2(xn)[r], Dh));
+          ++gu;
+        } else if (u0.last_seg && prm.final_states) {
+          // the sequence's final state
           float* fin = prm.final_states + ((long long)u0.s * prm.H + h) * kPN;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -926,7 +932,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fin[(16 * cq + 2 * k + 1) * kN + r] = h2[k].y;
           }
         }
-        MATH_TRY(epilogue(f_prev, t0_prev, len_prev, h));
+        MATH_TRY(epilogue(f, t0, len, h));
+        ++it;
       }
     }
   math_done:;

@@ -288,3 +288,29 @@ def test_silu_gate_pins():
     zz = np.linspace(-8, 20, 57)
     assert np.allclose(oracle.silu_gate(np.ones_like(zz), zz), zz * 0.5 * (1 + np.tanh(zz / 2)),
                        rtol=1e-12, atol=0)
+
+
+# ---- the tolerance metric itself ---------------------------------------------
+
+def test_rel_err_hand_computed_values():
+    """rel_err = max |got - ref| / RMS(ref), with values worked by hand: a
+    wrong denominator (max |ref| instead of the RMS, a sum, a broadcast slip)
+    or a missing absolute value changes these numbers."""
+    # max diff 1 (at the last entry); RMS(ref) = sqrt((1 + 4 + 16) / 3) = sqrt(7)
+    assert oracle.rel_err([1.0, 2.0, 3.0], [1.0, 2.0, 4.0]) == pytest.approx(1.0 / np.sqrt(7.0), rel=1e-15)
+    # the diff is negative: |got - ref| must be taken; RMS(ref) = sqrt((9 + 16) / 2)
+    assert oracle.rel_err([3.0, 2.5], [3.0, 4.0]) == pytest.approx(1.5 / np.sqrt(12.5), rel=1e-15)
+    # max != RMS: ref = [0, 0, 0, 10] has RMS 5 and max 10
+    assert oracle.rel_err([0.0, 0.0, 1.0, 10.0], [0.0, 0.0, 0.0, 10.0]) == pytest.approx(0.2, rel=1e-15)
+    # 2-D inputs: the max and the RMS run over every element
+    ref = np.array([[1.0, -1.0], [1.0, -1.0]])
+    got = ref + np.array([[0.0, 0.0], [0.0, 0.5]])
+    assert oracle.rel_err(got, ref) == pytest.approx(0.5, rel=1e-15)
+
+
+def test_rel_err_edge_cases():
+    assert oracle.rel_err(np.zeros(0), np.zeros(0)) == 0.0
+    assert oracle.rel_err(np.zeros((3, 0)), np.zeros((3, 0))) == 0.0
+    # a zero reference: the absolute difference is reported
+    assert oracle.rel_err([0.25, 0.0], [0.0, 0.0]) == 0.25
+    assert oracle.rel_err([1.0, 2.0], [1.0, 2.0]) == 0.0
