@@ -12,8 +12,13 @@ Prints one JSON line (rank 0).  ``value`` is tokens/s with inputs resident in
 HBM; each timed step is bracketed by CUDA events on the launching stream and
 preceded (outside the events) by a 256 MiB write that flushes L2.  ``e2e``
 is the same metric through the public call with pinned host buffers: each
-step copies that step's inputs host->device, runs the call and copies y and
-the final states back.  ``--impl reference`` times the fp64 CPU oracle on
+step copies that step's inputs host->device, runs the forward and copies y
+and the final states back -- for a batch-1 sequence in four slices carried
+by their states, so the copies in, the calls and the copies out overlap on
+three streams (the one-stream time is reported beside it).
+``other_workloads`` times the forward on the 4 x 2K, 64K and packed
+varlen workloads.  Clocks are sampled through NVML about every millisecond
+during the timed calls.  ``--impl reference`` times the fp64 CPU oracle on
 the host cores instead.  With N > 1 (torchrun) every rank runs its own
 replica of the workload (independent problems, no collective on the data
 path) and ``value`` is the sum over ranks divided by the slowest rank's time.
@@ -52,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward pass")
     ap.add_argument("--no-s6", action="store_true",
                     help="skip the Mamba-1 selective-scan comparison")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the l2k_b4 / l64k / varlen64 forward measurements")
     return ap.parse_args()
 
 
@@ -81,7 +88,7 @@ def load_peaks():
 
 
 # the device code of the forward kernel whose DRAM traffic profiles/traffic.json records
-FORWARD_KERNEL_SOURCES = ("ssd_tc.cu", "tc_ptx.cuh", "ssd_common.cuh")
+FORWARD_KERNEL_SOURCES = ("ssd_tc.cu", "tc_ptx.cuh", "tc_util.cuh", "ssd_common.cuh")
 
 
 def source_hash():
@@ -105,62 +112,129 @@ def traffic_from_profiles(kernel_key):
     return e.get("dram_bytes_per_launch")
 
 
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes):
+    the SM clock, its maximum and the active clock event reasons."""
+    CLOCK_SM = 1
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
+
+    def __init__(self, index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        self.get_reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _clock(self, fn):
+        v = self.ct.c_uint()
+        if fn(self.h, self.ct.c_int(self.CLOCK_SM), self.ct.byref(v)) != 0:
+            raise RuntimeError("clock query failed")
+        return float(v.value)
+
+    def sm_mhz(self):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo)
+
+    def max_sm_mhz(self):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def reasons(self):
+        v = self.ct.c_ulonglong()
+        if self.get_reasons(self.h, self.ct.byref(v)) != 0:
+            raise RuntimeError("reason query failed")
+        return {n for b, n in self.REASONS.items() if v.value & b}
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """SM clock, its maximum and the clock event (throttle) reasons, sampled
+    about every millisecond while the timed calls run: NVML queries from a
+    thread (read-only; no setting of the GPU is touched), or nvidia-smi
+    every 20 ms when NVML is unavailable."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.lines = []   # (arrival time, line)
+        self.nvml = None
+        self.samples = []   # (time, sm MHz, max MHz, set of reason names)
+        self.running = False
 
     def start(self):
+        try:
+            self.nvml = _Nvml(self.index)
+            self.smax = self.nvml.max_sm_mhz()
+            self.running = True
+            self.t = threading.Thread(target=self._poll_nvml, daemon=True)
+            self.t.start()
+            return
+        except Exception:
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t = threading.Thread(target=self._read_smi, daemon=True)
             self.t.start()
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def _read(self):
+    def _poll_nvml(self):
+        while self.running:
+            try:
+                sm, reasons = self.nvml.sm_mhz(), self.nvml.reasons()
+            except Exception:
+                break
+            self.samples.append((time.time(), sm, self.smax, reasons))
+            time.sleep(0.001)
+
+    def _read_smi(self):
         for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
-
-    def count_since(self, t0):
-        return sum(1 for t, _ in self.lines if t >= t0)
-
-    def stop(self, t0=None):
-        """Summary of the samples that arrived after time t0 (all if None)."""
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ta, l in self.lines:
-            if t0 is not None and ta < t0:
-                continue
-            f = [x.strip() for x in l.split(",")]
+            f = [x.strip() for x in line.strip().split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
+                sm, smax = float(f[1]), float(f[2])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            self.samples.append((time.time(), sm, smax,
+                                 {n for n, v in zip(self.NAMES, f[5:9])
+                                  if v.lower().startswith("active")}))
+
+    @property
+    def available(self):
+        return self.nvml is not None or self.proc is not None
+
+    def count_between(self, t0, t1=None):
+        return sum(1 for t, *_ in self.samples if t >= t0 and (t1 is None or t <= t1))
+
+    def stop(self, t0=None, t1=None):
+        """Summary of the samples taken between times t0 and t1."""
+        if not self.available:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock query unavailable"]}
+        self.running = False
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sel = [x for x in self.samples
+               if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
+        sm = [x[1] for x in sel]
+        reasons = set().union(*[x[3] for x in sel]) if sel else set()
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": sel[-1][2] if sel else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "source": "NVML, ~1 ms" if self.nvml is not None else "nvidia-smi, 20 ms"}
 
 
 def dist_init():
@@ -299,12 +373,6 @@ def main():
         flush.zero_()
         call()
     torch.cuda.synchronize()
-    # the sampler is running (its first sample has arrived) before timing
-    tw = time.time()
-    while sampler.proc is not None and not sampler.lines and time.time() - tw < 10:
-        flush.zero_()
-        call()
-        torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise SystemExit(f"device status {int(status.item())} after warm-up")
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -320,21 +388,12 @@ def main():
         call()
         ends[i].record(stream)
     torch.cuda.synchronize()
+    t_end = time.time()
     launches = ssd.kernel_launches() - launches0
     if world > 1:
         dist.barrier()
-    # A short timed region may see no sample (one every 20 ms): the same
-    # calls continue, untimed, until 5 samples have arrived since the timed
-    # region began (at most 2 s); the summary covers exactly those samples.
-    in_region = sampler.count_since(t_timed)
-    te = time.time()
-    while (sampler.proc is not None and sampler.count_since(t_timed) < 5
-           and time.time() - te < 2):
-        flush.zero_()
-        call()
-        torch.cuda.synchronize()
-    clocks = sampler.stop(t_timed)
-    clocks["samples_in_timed_region"] = in_region
+    clocks = sampler.stop(t_timed, t_end)
+    clocks["samples_in_timed_region"] = clocks.get("samples", 0)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = statistics.mean(step_ms)
     if world > 1:
@@ -362,13 +421,20 @@ def main():
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(args, fi, wl, dev, A, D, call_kwargs=dict(chunk=wl.chunk, ws=ws,
-                                                                     status=status))
-        if world > 1:
-            t = torch.tensor([e2e["_ms"]], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e["_ms"] = float(t.item())
-        e2e["value"] = ntok * world / (e2e.pop("_ms") / 1e3)
+        kw = dict(chunk=wl.chunk, ws=ws, status=status)
+        e2e_serial = measure_e2e(args, fi, wl, dev, A, D, call_kwargs=kw)
+        e2e = e2e_serial
+        if wl.batch == 1 and fi.cu_seqlens is None and wl.seqlen >= 4 * 128:
+            e2e = measure_e2e_overlapped(args, fi, wl, dev, A, D, call_kwargs=kw)
+        for r in (e2e, e2e_serial):
+            if world > 1:
+                t = torch.tensor([r["_ms"]], device=dev)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                r["_ms"] = float(t.item())
+            r["value"] = ntok * world / (r.pop("_ms") / 1e3)
+        if e2e is not e2e_serial:
+            e2e["serial"] = {"value": e2e_serial["value"], "unit": "tokens/s",
+                             "how": "one stream: all inputs in, one call, y and final out"}
 
     decode = None
     if not args.no_decode:
@@ -386,6 +452,10 @@ def main():
     if not args.no_s6 and wl.name == "l8k":
         s6 = measure_s6(dev, peaks, ms * 1e3, flush)
 
+    others = None
+    if not args.no_other_workloads and wl.name == "l8k":
+        others = {n: measure_workload(n, dev, peaks, flush) for n in ("l2k_b4", "l64k", "varlen64")}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(fi, wl)
@@ -394,13 +464,16 @@ def main():
         out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-               "dtype": wl.dtype, "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
+               "dtype": wl.dtype,
+               "data": "synthetic, seeded PCG64: x, B, C ~ N(0,1); A_h = -exp(U(ln 1, ln 16)); "
+                       "dt = softplus(N(0, 0.5^2) + per-head bias); bf16-rounded inputs",
                "config": workload_config(wl, world),
                "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
                "launches_per_step": launches / max(1, args.steps),
                "step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
                "step_ms_max": max(step_ms), "step_ms_first5": [round(v, 4) for v in step_ms[:5]],
-               "e2e": e2e, "cpu_baseline": cpu, "decode": decode, "epilogue": epilogue, "backward": backward, "s6": s6,
+               "e2e": e2e, "cpu_baseline": cpu, "other_workloads": others, "decode": decode,
+               "epilogue": epilogue, "backward": backward, "s6": s6,
                "pages_claim": "SSD 2-8x faster than Mamba's fused selective scan (A100), context only"}
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -457,6 +530,142 @@ def measure_e2e(args, fi, wl, dev, A, D, call_kwargs):
     torch.cuda.synchronize()
     return {"_ms": s.elapsed_time(e) / n, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def measure_e2e_overlapped(args, fi, wl, dev, A, D, call_kwargs, pieces=4):
+    """The public call with pinned host buffers, the sequence streamed in
+    `pieces` consecutive slices: slice k+1's inputs go host->device on one
+    stream while slice k is computed on a second and slice k-1's y comes back
+    on a third.  Each slice starts from the previous slice's final state (the
+    recurrence carried across calls), so the result is the one-call result.
+    Batch-1 dense workloads only (a slice of [1, T, ...] is contiguous)."""
+    import torch
+    from state_space_sequence_05_b300 import inputs as I
+    from state_space_sequence_05_b300 import ssd
+    T, H, P, N = wl.seqlen, wl.nheads, wl.headdim, wl.dstate
+    q = 128
+    cuts = [0] + [((T * k // pieces) // q) * q for k in range(1, pieces)] + [T]
+    host = {k: I.as_torch(getattr(fi, k), fi.bits.get(k), "cpu", wl.dtype).pin_memory()
+            for k in ("x", "dt", "B", "C")}
+    host_init = None if fi.init is None else torch.from_numpy(fi.init).pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    dinit = None if host_init is None else torch.empty_like(host_init, device=dev)
+    y = torch.empty((1, T, H, P), device=dev, dtype=torch.float32)
+    fins = [torch.empty((1, H, P, N), device=dev, dtype=torch.float32) for _ in range(2)]
+    y_h = torch.empty(y.shape, dtype=torch.float32).pin_memory()
+    fin_h = torch.empty((1, H, P, N), dtype=torch.float32).pin_memory()
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d += 0 if host_init is None else host_init.numel() * 4
+    d2h = (y.numel() + fin_h.numel()) * 4
+
+    def step():
+        ev_in = [torch.cuda.Event() for _ in range(pieces)]
+        ev_run = [torch.cuda.Event() for _ in range(pieces)]
+        # the previous step's reads of these buffers must be done: its calls
+        # read dbuf, its device->host copies read y
+        s_in.wait_stream(s_run)
+        s_run.wait_stream(s_out)
+        with torch.cuda.stream(s_in):
+            if dinit is not None:
+                dinit.copy_(host_init, non_blocking=True)
+            for k in range(pieces):
+                a, b = cuts[k], cuts[k + 1]
+                for n in host:
+                    dbuf[n][:, a:b].copy_(host[n][:, a:b], non_blocking=True)
+                ev_in[k].record(s_in)
+        for k in range(pieces):
+            a, b = cuts[k], cuts[k + 1]
+            s_run.wait_event(ev_in[k])
+            sl = {n: dbuf[n][:, a:b] for n in dbuf}
+            init = dinit if k == 0 else fins[(k - 1) % 2]
+            ssd.ssd_chunk_scan_fwd(sl["x"], sl["dt"], A, sl["B"], sl["C"], D,
+                                   call_kwargs["chunk"], init, None, y=y[:, a:b],
+                                   final_states=fins[k % 2], workspace=call_kwargs["ws"],
+                                   dev_status=call_kwargs["status"], stream=s_run)
+            ev_run[k].record(s_run)
+        s_out.wait_stream(s_in)
+        with torch.cuda.stream(s_out):
+            for k in range(pieces):
+                a, b = cuts[k], cuts[k + 1]
+                s_out.wait_event(ev_run[k])
+                y_h[:, a:b].copy_(y[:, a:b], non_blocking=True)
+            fin_h.copy_(fins[(pieces - 1) % 2], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 20))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(s_in)
+    for _ in range(n):
+        step()
+    s_out.wait_stream(s_run)
+    e.record(s_out)
+    torch.cuda.synchronize()
+    return {"_ms": s.elapsed_time(e) / n, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n,
+            "how": f"{pieces} slices with the state carried between calls; host->device, "
+                   f"compute and device->host on three streams"}
+
+
+def measure_workload(name, dev, peaks, flush, steps=20, warmup=5):
+    """The forward on another named workload: time per call (CUDA events,
+    L2 flushed before each), tokens/s and the fraction of the HBM roofline."""
+    import torch
+    from state_space_sequence_05_b300 import inputs as I
+    from state_space_sequence_05_b300 import ssd
+    fi = I.make_forward_inputs(I.WORKLOADS[name])
+    wl = fi.wl
+    d = {k: I.as_torch(getattr(fi, k), fi.bits.get(k), dev, wl.dtype) for k in ("x", "dt", "B", "C")}
+    A = torch.from_numpy(fi.A).to(dev)
+    D = torch.from_numpy(fi.D).to(dev)
+    init = None if fi.init is None else torch.from_numpy(fi.init).to(dev)
+    cu = None if fi.cu_seqlens is None else torch.from_numpy(fi.cu_seqlens).to(dev)
+    H, P, N, G = wl.nheads, wl.headdim, wl.dstate, wl.ngroups
+    y = torch.empty((wl.batch, wl.seqlen, H, P), device=dev, dtype=torch.float32)
+    fin = torch.empty((fi.nseq, H, P, N), device=dev, dtype=torch.float32)
+    code = ssd.SSD_DT_BF16 if wl.dtype == "bf16" else ssd.SSD_DT_F32
+    wsb = ssd.ssd_chunk_scan_fwd_workspace_size(wl.batch, wl.seqlen, H, P, N, G, wl.chunk, code,
+                                                cu is not None, fi.nseq)
+    ws = torch.empty(max(wsb, 1), device=dev, dtype=torch.uint8)
+    status = torch.zeros(1, device=dev, dtype=torch.int32)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        ssd.ssd_chunk_scan_fwd(d["x"], d["dt"], A, d["B"], d["C"], D, wl.chunk, init, cu, y=y,
+                               final_states=fin, workspace=ws, dev_status=status, stream=stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    ts = []
+    l0 = ssd.kernel_launches()
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    launches = (ssd.kernel_launches() - l0) / steps
+    st = int(status.item())
+    us = [1e3 * a.elapsed_time(b) for a, b in ts]
+    mean_us = statistics.mean(us)
+    bytes_, flops = algorithmic_cost(wl)
+    ntok = wl.batch * wl.seqlen
+    out = {"workload": workload_config(wl, 1)["workload"], "tokens": ntok, "us_per_call": mean_us,
+           "us_median": statistics.median(us), "tokens_per_s": ntok / (mean_us / 1e6),
+           "algorithmic_bytes": bytes_,
+           "roofline_frac": bytes_ / (mean_us / 1e6) / 1e9 / peaks["hbm_gbs"],
+           "roofline_time_us": 1e6 * max(bytes_ / (peaks["hbm_gbs"] * 1e9),
+                                         flops / (peaks["bf16_tflops"] * 1e12)),
+           "launches_per_call": launches, "device_status": st}
+    del d, y, fin, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def cpu_baseline(fi, wl):
