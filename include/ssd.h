@@ -243,14 +243,40 @@ ssd_status_t ssd_chunk_scan_bwd(const void *x, const void *dt, const float *A, c
                                 void *stream);
 
 /*
+ * ssd_chunk_scan_states -- the state at the end of each sequence, without
+ * the outputs: the segment-state and state-passing steps of the chunked
+ * forward ("Transformers are SSMs Review", dimensionstp.github.io, sec. 3-2
+ * (4): chunk states, then the recurrence over chunks; sec. 3-2 (6): only the
+ * boundary states cross between pieces of a sequence).
+ *   Arguments, layouts and checks as for ssd_chunk_scan_fwd, less C, D and y:
+ *   final_states [nseq_or_batch, nheads, headdim, dstate] float32 (required)
+ *   receives the state after each sequence from init_states (NULL: zero).
+ *   Scratch: workspace of at least ssd_chunk_scan_states_workspace_size(...)
+ *   bytes, 256-byte aligned, owned by the caller.
+ *   The tensor-core configuration (bfloat16, headdim 64, dstate 128) runs the
+ *   segment-state and state-passing kernels only; other shapes run the
+ *   CUDA-core forward with y kept in the workspace and dropped.
+ *   Returns SSD_OK, SSD_ERR_INVALID, SSD_ERR_UNSUPPORTED or SSD_ERR_CUDA;
+ *   errors only the device can see go to *dev_status as for the forward.
+ */
+size_t ssd_chunk_scan_states_workspace_size(int batch, int seqlen, int nheads, int headdim,
+                                            int dstate, int ngroups, int chunk_size,
+                                            ssd_dtype_t in_dtype, int varlen, int nseq);
+ssd_status_t ssd_chunk_scan_states(
+    const void *x, const void *dt, const float *A, const void *B, int batch, int seqlen,
+    int nheads, int headdim, int dstate, int ngroups, int chunk_size, ssd_dtype_t in_dtype,
+    const float *init_states, const int32_t *cu_seqlens, int nseq, float *final_states,
+    void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
  * Context (sequence) parallelism: one sequence cut into R consecutive slices,
- * one per device.  Each device runs ssd_chunk_scan_fwd on its slice from a
+ * one per device.  Each device runs ssd_chunk_scan_states on its slice from a
  * zero state and keeps the slice's end state S_r (final_states) and its
  * total log-decay a_r (ssd_segment_decay); the devices exchange these (an
  * all-gather, the caller's collective); ssd_segment_combine composes the
  * slices' affine maps h -> exp(a_r) h + S_r into the state entering each
- * slice; a second ssd_chunk_scan_fwd from that state gives the exact y and
- * end state of the slice.  The composition rule (a2, b2) o (a1, b1) =
+ * slice; ssd_chunk_scan_fwd from that state gives the exact y and end state
+ * of the slice.  The composition rule (a2, b2) o (a1, b1) =
  * (a2 a1, a2 b1 + b2) is that of the Mamba paper review (feghi.github.io,
  * sec. 4); passing states between blocks of the sequence is the SSD
  * review's chunked algorithm (dimensionstp.github.io, sec. 3-2 (4)) at the

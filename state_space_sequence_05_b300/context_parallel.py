@@ -3,19 +3,22 @@
 One sequence is cut into consecutive slices, one per rank of a
 ``torch.distributed`` group, in rank order.  Every rank
 
-1. runs its slice from a zero state (``ssd_chunk_scan_fwd``) and keeps the
-   slice's end state S_r, and computes the slice's total log-decay a_r
+1. computes the state its slice leaves from a zero state, S_r, with the
+   states-only pass (``ssd_chunk_scan_states``: segment states and state
+   passing, no outputs), and the slice's total log-decay a_r
    (``ssd_segment_decay``);
 2. all-gathers (a_r, S_r) from every rank: the one exchange step;
 3. composes the earlier slices' affine maps h -> exp(a_k) h + S_k into the
    state entering its own slice (``ssd_segment_combine``; the composition
    rule (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2) of the Mamba paper review,
    sec. 4);
-4. runs its slice again from that state: the exact y and end state.
+4. runs the forward over its slice from that state: the exact y and end
+   state.
 
 The result equals the single-device forward up to rounding (the recurrence
-is linear in its initial state).  Each rank does two forward passes over its
-slice, so R ranks finish a sequence about R / 2 times faster than one.
+is linear in its initial state).  Each rank does one states-only pass and
+one forward over its slice ("Transformers are SSMs Review" sec. 3-2 (6):
+only the boundary states move between the pieces).
 
 This module marshals arguments and calls the collective; every step of the
 computation runs in the library's kernels.  ``ops`` replaces those kernels
@@ -32,11 +35,13 @@ import torch
 @dataclass
 class CPOps:
     """The per-rank device steps: forward(x, dt, A, B, C, D, chunk_size,
-    init) -> (y, final); decay(dt, A) -> [b, H]; combine(decay [R, b, H],
-    states [R, b, H, P, N], init) -> [R + 1, b, H, P, N]."""
+    init) -> (y, final); states(x, dt, A, B, chunk_size) -> final from a
+    zero state; decay(dt, A) -> [b, H]; combine(decay [R, b, H], states
+    [R, b, H, P, N], init) -> [R + 1, b, H, P, N]."""
     forward: Callable
     decay: Callable
     combine: Callable
+    states: Optional[Callable] = None
 
 
 def cuda_ops() -> CPOps:
@@ -45,7 +50,10 @@ def cuda_ops() -> CPOps:
     def forward(x, dt, A, B, C, D, chunk_size, init):
         return ssd.ssd_chunk_scan_fwd(x, dt, A, B, C, D, chunk_size, init)
 
-    return CPOps(forward, ssd.ssd_segment_decay, ssd.ssd_segment_combine)
+    def states(x, dt, A, B, chunk_size):
+        return ssd.ssd_chunk_scan_states(x, dt, A, B, chunk_size)
+
+    return CPOps(forward, ssd.ssd_segment_decay, ssd.ssd_segment_combine, states)
 
 
 def ssd_forward_context_parallel(x, dt, A, B, C, D=None, chunk_size=256, init_states=None,
@@ -66,8 +74,11 @@ def ssd_forward_context_parallel(x, dt, A, B, C, D=None, chunk_size=256, init_st
     if world == 1:
         return ops.forward(x, dt, A, B, C, D, chunk_size, init_states)
     rank = dist.get_rank(group)
-    # 1. this slice from a zero state (D does not enter the state)
-    _, S = ops.forward(x, dt, A, B, C, None, chunk_size, None)
+    # 1. the state this slice leaves from a zero state (D does not enter it)
+    if ops.states is not None:
+        S = ops.states(x, dt, A, B, chunk_size)
+    else:
+        _, S = ops.forward(x, dt, A, B, C, None, chunk_size, None)
     a = ops.decay(dt, A)
     # 2. the exchange
     S_all = [torch.empty_like(S) for _ in range(world)]

@@ -2,6 +2,7 @@
 // workspace sizing and dispatch to the kernels.  See include/ssd.h for the
 // contract of each entry point.
 #include <cuda_runtime.h>
+#include <string.h>
 #include <stdint.h>
 
 #include <atomic>
@@ -54,20 +55,28 @@ ssd_status_t check_fwd(const FwdArgs& a, bool check_ptrs) {
   return SSD_OK;
 }
 
-// Which tensor-core forward runs the plain (no fused-epilogue) calls: the
-// first kernel unless SSD_TC_PIPELINED=1 selects the pipelined one.
-bool legacy_tc() {
-  const char* e = getenv("SSD_TC_PIPELINED");
-  return !(e && e[0] == '1');
+// Which tensor-core forward runs the plain (no fused-epilogue) calls:
+// SSD_TC_KERNEL=split (the default: segment states, state passing, outputs
+// as three kernels), =fused (one kernel with the segment hand-off inside) or
+// =pipelined (the fused design with a deeper operand pipeline).
+enum class TcKernel { kSplit, kFused, kPipelined };
+TcKernel tc_kernel() {
+  const char* e = getenv("SSD_TC_KERNEL");
+  if (e && strcmp(e, "fused") == 0) return TcKernel::kFused;
+  if (e && strcmp(e, "pipelined") == 0) return TcKernel::kPipelined;
+  return TcKernel::kSplit;
 }
 
 size_t fwd_workspace(const FwdArgs& a) {
   if (a.nseq == 0) return 0;
-  // the tensor-core shapes run on the pipelined kernel, or on the fused-
-  // epilogue kernel when epilogue options are given: enough for either
+  // any of the tensor-core kernels may run a tensor-core shape (the fused-
+  // epilogue options always take the fused kernel): enough for each
   if (ssd::tc_supported(a)) {
-    const size_t t1 = ssd::tc_workspace_bytes(a), t2 = ssd::tc2_workspace_bytes(a);
-    return t1 > t2 ? t1 : t2;
+    size_t w = ssd::tc_workspace_bytes(a);
+    const size_t t2 = ssd::tc2_workspace_bytes(a), t3 = ssd::tc3_workspace_bytes(a);
+    if (t2 > w) w = t2;
+    if (t3 > w) w = t3;
+    return w;
   }
   return ssd::simt_workspace_bytes(a);
 }
@@ -183,7 +192,9 @@ ssd_status_t ssd_chunk_scan_fwd_ex(const void* x, const void* dt, const float* A
   const unsigned long long w = g_wait_ns.load(std::memory_order_relaxed);
   const unsigned long long wait_ns = w ? w : 2000000000ull;
   const int hold = g_hold_unit.load(std::memory_order_relaxed);
-  if (ssd::tc2_supported(a) && !legacy_tc()) return ssd::tc2_forward(a, wait_ns, hold);
+  const TcKernel k = tc_kernel();
+  if (k == TcKernel::kSplit && ssd::tc3_supported(a)) return ssd::tc3_forward(a, wait_ns, hold);
+  if (k == TcKernel::kPipelined && ssd::tc2_supported(a)) return ssd::tc2_forward(a, wait_ns, hold);
   return ssd::tc_supported(a) ? ssd::tc_forward(a, wait_ns, hold) : ssd::simt_forward(a);
 }
 
@@ -275,6 +286,95 @@ ssd_status_t ssd_chunk_scan_bwd(const void* x, const void* dt, const float* A, c
   a.ws = workspace;
   a.stream = static_cast<cudaStream_t>(stream);
   return ssd::bwd(a);
+}
+
+namespace {
+
+// The forward's arguments for a states-only call: C and y are not read by
+// the segment-state kernels; the CUDA-core path computes y into scratch
+// (with B standing in for C, whose values then do not matter).
+FwdArgs states_args(const void* x, const void* dt, const float* A, const void* B, int batch,
+                    int seqlen, int nheads, int headdim, int dstate, int ngroups, int chunk_size,
+                    ssd_dtype_t in_dtype, const float* init_states, const int32_t* cu_seqlens,
+                    int nseq, float* final_states) {
+  FwdArgs a{};
+  a.x = x;
+  a.dt = dt;
+  a.A = A;
+  a.B = B;
+  a.C = B;
+  a.batch = batch;
+  a.seqlen = seqlen;
+  a.H = nheads;
+  a.P = headdim;
+  a.N = dstate;
+  a.G = ngroups;
+  a.Q = chunk_size;
+  a.dtype = in_dtype;
+  a.init = init_states;
+  a.cu = cu_seqlens;
+  a.nseq = cu_seqlens ? nseq : batch;
+  a.final_states = final_states;
+  return a;
+}
+
+// Scratch of a states-only call: the split tensor-core kernels' workspace,
+// or the CUDA-core forward's plus room for the dropped y.
+size_t states_workspace(const FwdArgs& a, size_t* y_offset) {
+  if (a.nseq == 0) return 0;
+  if (ssd::tc3_supported(a)) return ssd::tc3_workspace_bytes(a);
+  const size_t w = ssd::align256(ssd::simt_workspace_bytes(a));
+  *y_offset = w;
+  return w + ssd::align256(sizeof(float) * (size_t)a.batch * a.seqlen * a.H * a.P);
+}
+
+}  // namespace
+
+size_t ssd_chunk_scan_states_workspace_size(int batch, int seqlen, int nheads, int headdim,
+                                            int dstate, int ngroups, int chunk_size,
+                                            ssd_dtype_t in_dtype, int varlen, int nseq) {
+  static const int32_t kDummy = 0;
+  FwdArgs a = states_args(nullptr, nullptr, nullptr, nullptr, batch, seqlen, nheads, headdim,
+                          dstate, ngroups, chunk_size, in_dtype, nullptr,
+                          varlen ? &kDummy : nullptr, nseq, nullptr);
+  if (check_fwd(a, false) != SSD_OK) return (size_t)-1;
+  size_t yoff = 0;
+  return states_workspace(a, &yoff);
+}
+
+ssd_status_t ssd_chunk_scan_states(const void* x, const void* dt, const float* A, const void* B,
+                                   int batch, int seqlen, int nheads, int headdim, int dstate,
+                                   int ngroups, int chunk_size, ssd_dtype_t in_dtype,
+                                   const float* init_states, const int32_t* cu_seqlens, int nseq,
+                                   float* final_states, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_status, void* stream) {
+  FwdArgs a = states_args(x, dt, A, B, batch, seqlen, nheads, headdim, dstate, ngroups,
+                          chunk_size, in_dtype, init_states, cu_seqlens, nseq, final_states);
+  a.dev_status = dev_status;
+  a.stream = static_cast<cudaStream_t>(stream);
+  ssd_status_t st = check_fwd(a, false);
+  if (st != SSD_OK) return st;
+  const long long ntok = (long long)a.batch * a.seqlen;
+  if (!final_states || !A) return SSD_ERR_INVALID;
+  if (ntok > 0 && (!x || !dt || !B)) return SSD_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(B) || !aligned16(init_states) || !aligned16(final_states))
+    return SSD_ERR_INVALID;
+  size_t yoff = 0;
+  const size_t need = states_workspace(a, &yoff);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return SSD_ERR_INVALID;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), a.stream) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  if (a.nseq == 0) return SSD_OK;
+  const unsigned long long w = g_wait_ns.load(std::memory_order_relaxed);
+  const unsigned long long wait_ns = w ? w : 2000000000ull;
+  if (ssd::tc3_supported(a)) return ssd::tc3_states(a, wait_ns);
+  a.y = reinterpret_cast<float*>(static_cast<char*>(workspace) + yoff);
+  a.ws_bytes = yoff;
+  return ssd::simt_forward(a);
 }
 
 ssd_status_t ssd_segment_decay(const void* dt, const float* A, int batch, int seqlen, int nheads,

@@ -83,6 +83,19 @@ bool tc2_supported(const FwdArgs& a);
 size_t tc2_workspace_bytes(const FwdArgs& a);
 ssd_status_t tc2_forward(const FwdArgs& a, unsigned long long wait_ns, int hold_unit);
 
+// Three-kernel tcgen05 forward (segment states, state passing, outputs; the
+// same shapes, no fused-epilogue options).  Every device wait is bounded by
+// `wait_ns`; `hold_unit` >= 0 names a work unit whose first decay mask is
+// never published (a test hook: the MMA issuer's wait runs out and the call
+// reports SSD_ERR_TIMEOUT).
+bool tc3_supported(const FwdArgs& a);
+size_t tc3_workspace_bytes(const FwdArgs& a);
+ssd_status_t tc3_forward(const FwdArgs& a, unsigned long long wait_ns, int hold_unit);
+// The segment-state and state-passing kernels alone: final_states (and the
+// segments' entering states in the workspace) without y.  Same workspace
+// as tc3_forward; a.C, a.D and a.y are not used.
+ssd_status_t tc3_states(const FwdArgs& a, unsigned long long wait_ns);
+
 // Mamba-1 selective scan (a decay per channel and state), one launch.
 ssd_status_t s6_forward(const void* x, const void* dt, const float* A, const void* B,
                         const void* C, const float* D, const float* init, int batch, int L,

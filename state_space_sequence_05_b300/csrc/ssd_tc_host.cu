@@ -16,7 +16,8 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* cu, int se
                                                        int H, int32_t* uoff, int* ticket,
                                                        int* flags, long long max_units,
                                                        const float* init, float* final_states,
-                                                       int PN, int32_t* dev_status) {
+                                                       int PN, int32_t* dev_status,
+                                                       int32_t* coff) {
   // the forward kernel may be scheduled now; it waits for this grid's
   // completion before it reads anything written here
   asm volatile("griddepcontrol.launch_dependents;");
@@ -25,42 +26,51 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* cu, int se
   if (threadIdx.x == 0) {
     carry = 0;
     bad = 0;
-    ticket[0] = 0;
-    ticket[1] = 0;
+    for (int k = 0; k < 4; ++k) ticket[k] = 0;
     if (cu && (cu[0] != 0 || cu[nseq] != seqlen_total)) bad = 1;
   }
   for (long long k = threadIdx.x; k < max_units; k += 1024) flags[k] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int base = 0; base < nseq; base += 1024) {
-    const int s = base + threadIdx.x;
-    int n = 0;
-    if (s < nseq) {
-      const long long b = cu ? (long long)cu[s] : (long long)s * seqlen_rows;
-      const long long e = cu ? (long long)cu[s + 1] : (long long)(s + 1) * seqlen_rows;
-      if (e < b || b < 0 || e > seqlen_total) atomicOr(&bad, 1);
-      const long long nt = e > b ? (e - b + kTcChunk - 1) / kTcChunk : 0;
-      n = (int)((nt + seg - 1) / seg) * H;
-    }
-    int v = n;
+  // pass 0: units per sequence into uoff; pass 1 (when coff is given):
+  // chunks per sequence into coff
+  for (int pass = 0; pass < (coff ? 2 : 1); ++pass) {
+    int32_t* offs = pass == 0 ? uoff : coff;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < nseq; base += 1024) {
+      const int s = base + threadIdx.x;
+      int n = 0;
+      if (s < nseq) {
+        const long long b = cu ? (long long)cu[s] : (long long)s * seqlen_rows;
+        const long long e = cu ? (long long)cu[s + 1] : (long long)(s + 1) * seqlen_rows;
+        if (e < b || b < 0 || e > seqlen_total) atomicOr(&bad, 1);
+        const long long nt = e > b ? (e - b + kTcChunk - 1) / kTcChunk : 0;
+        n = pass == 0 ? (int)((nt + seg - 1) / seg) * H : (int)nt;
+      }
+      int v = n;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += t;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+      }
+      if (lane == 31) buf[wid] = v;
+      __syncthreads();
+      int off = 0;
+      for (int w = 0; w < wid; ++w) off += buf[w];
+      if (s < nseq) offs[s + 1] = carry + v + off;
+      __syncthreads();
+      if (threadIdx.x == 1023) carry += v + off;
+      __syncthreads();
     }
-    if (lane == 31) buf[wid] = v;
-    __syncthreads();
-    int off = 0;
-    for (int w = 0; w < wid; ++w) off += buf[w];
-    if (s < nseq) uoff[s + 1] = carry + v + off;
-    __syncthreads();
-    if (threadIdx.x == 1023) carry += v + off;
+    if (threadIdx.x == 0) offs[0] = 0;
     __syncthreads();
   }
-  if (threadIdx.x == 0) uoff[0] = 0;
-  __syncthreads();
   if (bad) {
-    for (int s = threadIdx.x; s <= nseq; s += 1024) uoff[s] = 0;
+    for (int s = threadIdx.x; s <= nseq; s += 1024) {
+      uoff[s] = 0;
+      if (coff) coff[s] = 0;
+    }
     if (threadIdx.x == 0) report(dev_status, SSD_ERR_INVALID);
   }
   if (threadIdx.x == 0) uoff[nseq + 1] = bad;
@@ -175,11 +185,11 @@ long long tc_max_units(const FwdArgs& a) {
 }
 
 cudaError_t tc_launch_plan(const FwdArgs& a, int seg, int32_t* uoff, int* ticket, int* flags,
-                           long long max_units) {
+                           long long max_units, int32_t* coff) {
   const long long ntok = (long long)a.batch * a.seqlen;
   tc_plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu, a.seqlen, (int)ntok, a.nseq, seg, a.H, uoff,
                                            ticket, flags, max_units, a.init, a.final_states,
-                                           a.P * a.N, a.dev_status);
+                                           a.P * a.N, a.dev_status, coff);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -42,10 +42,11 @@ bool tc_make_map_y_bf16(CUtensorMap* m, void* ptr, long long rows, long long col
 // Plan kernel: per sequence the number of work units (segments of `seg`
 // chunks x H heads) as offsets uoff[0..nseq], and uoff[nseq+1] = 0 if
 // cu_seqlens is well formed (else SSD_ERR_INVALID in dev_status and no
-// units); zeroes the work ticket (ticket[0..1]) and the first `max_units`
-// hand-off flags; final = init (or 0) for sequences without tokens.  It
+// units); zeroes the work tickets (ticket[0..3]) and the first `max_units`
+// hand-off flags; final = init (or 0) for sequences without tokens; when
+// `coff` is given, the chunk offsets per sequence there (coff[0..nseq]).  It
 // allows its dependent launch to start early (programmatic dependent launch).
 cudaError_t tc_launch_plan(const FwdArgs& a, int seg, int32_t* uoff, int* ticket, int* flags,
-                           long long max_units);
+                           long long max_units, int32_t* coff = nullptr);
 
 }  // namespace ssd

@@ -357,6 +357,24 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Copies `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global memory into shared memory with one bulk request, completing on
+// `bar` (its expected transaction count must include the bytes).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Brings `bytes` (a multiple of 16, from a 16-byte aligned p) into L2 with
+// one bulk request.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Drops a 128-byte line from L2 without writing it back (its contents become
 // undefined); for scratch whose last reader is done with it.
 __device__ __forceinline__ void discard_l2_line(const void* p) {

@@ -41,6 +41,10 @@ SIGNATURES = {
     "ssd_chunk_scan_fwd_noalloc": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci,
                                          _ci, _ci, _ci, _fp, _ip, _ci, _fp, _fp, _ip, _vp]),
     "ssd_chunk_scan_fwd_workspace_size": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci]),
+    "ssd_chunk_scan_states_workspace_size": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci,
+                                                   _ci]),
+    "ssd_chunk_scan_states": (_ci, [_vp, _vp, _fp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _fp,
+                                    _ip, _ci, _fp, _vp, _sz, _ip, _vp]),
     "ssd_state_update": (_ci, [_fp, _vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci, _ci,
                                _fp, _vp]),
     "ssd_selective_scan_fwd": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _ci, _ci, _ci, _ci, _ci,
@@ -224,6 +228,49 @@ def ssd_chunk_scan_fwd(x, dt, A, B, C, D=None, chunk_size=256, init_states=None,
     if st != SSD_OK:
         raise SSDError(st, where)
     return y, final_states
+
+
+def ssd_chunk_scan_states(x, dt, A, B, chunk_size=256, init_states=None, cu_seqlens=None, *,
+                          final_states=None, workspace=None, dev_status=None, stream=None):
+    """The state at the end of each sequence without the outputs
+    (ssd_chunk_scan_states): shapes as for ``ssd_chunk_scan_fwd`` (no C, D,
+    y).  Returns ``final_states [nseq_or_b, H, P, N]`` float32."""
+    lib = load_library()
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("ssd_chunk_scan_states needs CUDA tensors")
+    if x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be [batch, seqlen, nheads, headdim], B [batch, seqlen, ngroups, dstate]")
+    b, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    code = _dtype_code(x)
+    _need(x, "x", dev)
+    _need(dt, "dt", dev, x.dtype, (b, T, H))
+    _need(B, "B", dev, x.dtype, (b, T, G, N))
+    _need(A, "A", dev, torch.float32, (H,))
+    nseq = b
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", dev, torch.int32)
+        nseq = cu_seqlens.shape[0] - 1
+    if init_states is not None:
+        _need(init_states, "init_states", dev, torch.float32, (nseq, H, P, N))
+    if final_states is None:
+        final_states = torch.empty((nseq, H, P, N), device=dev, dtype=torch.float32)
+    _need(final_states, "final_states", dev, torch.float32, (nseq, H, P, N))
+    need = lib.ssd_chunk_scan_states_workspace_size(b, T, H, P, N, G, chunk_size, code,
+                                                    int(cu_seqlens is not None), nseq)
+    if need == ctypes.c_size_t(-1).value:
+        raise SSDError(SSD_ERR_UNSUPPORTED, "ssd_chunk_scan_states_workspace_size")
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.ssd_chunk_scan_states(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), b, T, H, P, N, G,
+                                   chunk_size, code, _ptr(init_states), _ptr(cu_seqlens), nseq,
+                                   _ptr(final_states), _ptr(workspace), ws_bytes,
+                                   _ptr(dev_status), _stream_handle(stream))
+    if st != SSD_OK:
+        raise SSDError(st, "ssd_chunk_scan_states")
+    return final_states
 
 
 def ssd_state_update(state, x, dt, A, B, C, D=None, *, y=None, stream=None):

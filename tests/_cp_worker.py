@@ -19,6 +19,13 @@ def oracle_ops():
                                  None if init is None else init.numpy())
         return torch.from_numpy(y), torch.from_numpy(fin)
 
+    def states(x, dt, A, B, chunk_size):
+        # the state a slice leaves from a zero state: the recurrence's final
+        # state, whose value does not depend on C
+        zeros = np.zeros(B.shape, dtype=B.numpy().dtype)
+        _, fin = oracle.ssd_scan(x.numpy(), dt.numpy(), A.numpy(), B.numpy(), zeros, None, None)
+        return torch.from_numpy(fin)
+
     def decay(dt, A):
         return dt.double().sum(dim=1) * A.double()
 
@@ -31,7 +38,7 @@ def oracle_ops():
             out[r + 1] = torch.exp(a[r])[:, :, None, None] * out[r] + S[r]
         return out
 
-    return CPOps(forward, decay, combine)
+    return CPOps(forward, decay, combine, states)
 
 
 def run(rank, world, port, data_path, out_prefix):

@@ -3,10 +3,12 @@ library through its binding, run the oracle (whole problem or sampled
 heads), and compare with the tolerance metric max|diff| <= tol * RMS(ref).
 
 Tolerances: 1e-4 for float32 inputs, 1e-2 for bfloat16 inputs (fp32 state
-and accumulation).  The pages give none; these are the stated targets of the
-build, applied to y and, separately, to the final states.
+and accumulation).  The pages give none; these are the targets the library
+is held to, applied to y and, separately, to the final states.
 """
 from __future__ import annotations
+
+import functools
 
 import numpy as np
 
@@ -51,6 +53,14 @@ def run_gpu(fi: I.ForwardInputs, chunk=None, use_D=True, device="cuda"):
 def oracle_full(fi: I.ForwardInputs, use_D=True):
     return oracle.ssd_scan(fi.x, fi.dt, fi.A, fi.B, fi.C, fi.D if use_D else None, fi.init,
                            cu_seqlens=fi.cu_seqlens)
+
+
+@functools.lru_cache(maxsize=4)
+def oracle_workload(name: str):
+    """The whole-problem oracle of a named workload, computed once per test
+    session (several kernels are checked against it)."""
+    fi = I.make_forward_inputs(I.WORKLOADS[name])
+    return oracle_full(fi)
 
 
 def oracle_heads(fi: I.ForwardInputs, heads, seqs=None):

@@ -8,7 +8,8 @@ import pytest
 import oracle
 from state_space_sequence_05_b300 import inputs as I
 
-from _helpers import TOL, assert_close, gpu_seq, oracle_full, oracle_heads, run_gpu, to_device
+from _helpers import (TOL, assert_close, gpu_seq, oracle_full, oracle_heads, oracle_workload,
+                      run_gpu, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -181,7 +182,11 @@ def _check_all(name):
     """The whole workload against the whole-problem oracle (fp64, all host
     threads): every batch row or packed sequence, every head."""
     fi = I.make_forward_inputs(I.WORKLOADS[name])
-    return _check_full(fi)
+    y, fin = run_gpu(fi)
+    y_ref, fin_ref = oracle_workload(name)
+    tol = TOL[fi.wl.dtype]
+    assert_close(y.cpu().numpy(), y_ref, tol, "y")
+    assert_close(fin.cpu().numpy(), fin_ref, tol, "final")
 
 
 def test_l2k_b4_all_heads():

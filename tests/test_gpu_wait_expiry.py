@@ -1,12 +1,14 @@
 """The bounded device waits of the tensor-core forward run out cleanly.
 
-Every wait in the kernel (an mbarrier phase, a predecessor's hand-off flag)
+Every wait in the kernels (an mbarrier phase, a predecessor's hand-off flag)
 gives up after a time limit, records SSD_ERR_TIMEOUT in dev_status and lets
 the kernel unwind with its tensor memory freed -- no trap, no fault.  Here a
-test hook shortens the limit to 2 ms and holds back one work unit's hand-off
-flag (the segment end state it should publish), so the unit waiting for it
-runs out.  The call must return, report the timeout, and leave the context
-usable: the next call on the same stream, with the hook off, is exact.
+test hook shortens the limit to 2 ms and holds back one signal of work unit
+0: in the fused and pipelined kernels its hand-off flag (the segment end
+state it should publish), so the unit waiting for it runs out; in the split
+kernels its first decay mask, so the MMA issuer waiting for it runs out.
+The call must return, report the timeout, and leave the context usable: the
+next call on the same stream, with the hook off, is exact.
 """
 import os
 
@@ -28,10 +30,10 @@ def _lib():
     __graft_entry__.build()
 
 
-@pytest.fixture(params=["first", "pipelined"])
+@pytest.fixture(params=["fused", "pipelined", "split"])
 def kernel(request, monkeypatch):
-    """Both tensor-core forward kernels take the hook."""
-    monkeypatch.setenv("SSD_TC_PIPELINED", "1" if request.param == "pipelined" else "0")
+    """Every tensor-core forward takes the hook."""
+    monkeypatch.setenv("SSD_TC_KERNEL", request.param)
     return request.param
 
 
