@@ -214,7 +214,12 @@ size_t smem_bytes(int rows, int N) {
 size_t bwd_workspace_bytes(int batch, int T, int H, int P, int N) {
   const long long nck = ((long long)T + kCk - 1) / kCk;
   const long long nslice = (P + kRows - 1) / kRows;
-  return sizeof(float) * (size_t)batch * H * nslice * (size_t)(nck + 1 + kCk) * kRows * N;
+  const size_t steps = sizeof(float) * (size_t)batch * H * nslice * (size_t)(nck + 1 + kCk) * kRows * N;
+  // either backward may run a supported shape (the chunked one needs 16-byte
+  // aligned state arguments)
+  if (!bwd_chunked_supported(P, N)) return steps;
+  const size_t chunked = bwd_chunked_workspace_bytes(batch, T, H, P, N);
+  return chunked > steps ? chunked : steps;
 }
 
 ssd_status_t bwd(const BwdArgs& a) {
@@ -252,6 +257,10 @@ ssd_status_t bwd(const BwdArgs& a) {
        (cudaMemsetAsync(a.dB, 0, sizeof(float) * ntok * a.G * a.N, a.stream) != cudaSuccess ||
         cudaMemsetAsync(a.dC, 0, sizeof(float) * ntok * a.G * a.N, a.stream) != cudaSuccess)))
     return SSD_ERR_CUDA;
+  auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  if (a.seqlen > 0 && bwd_chunked_supported(a.P, a.N) && a16(a.init) && a16(a.dfinal) &&
+      a16(a.dinit))
+    return bwd_chunked(a);
   if (a.seqlen == 0) {
     // no steps: dinit = dL/dfinal
     if (a.dinit) {

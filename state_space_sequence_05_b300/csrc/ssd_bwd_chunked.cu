@@ -1,0 +1,687 @@
+// ssd_bwd_chunked.cu -- chunked backward of the SSD layer forward for
+// headdim <= 64 and dstate <= 128 (batch mode): the gradients of a loss L
+// with respect to x, dt, A, B, C, D and the initial state, given dL/dy and
+// dL/dfinal, through the forward's chunked form ("Transformers are SSMs
+// Review", sec. 3-2 (4)) instead of a walk over every step.
+//
+// Forward, per chunk c of 64 tokens (cum_i = sum_{k<=i} dt_k A chunk-local,
+// L_ij = exp(cum_i - cum_j) for j <= i, G_ij = C_i . B_j, M_ij = G_ij L_ij dt_j,
+// w_j = exp(cum_last - cum_j) dt_j, H_c the state entering the chunk):
+//
+//   y_i      = sum_j M_ij x_j + exp(cum_i) H_c C_i + D x_i
+//   H_{c+1}  = exp(cum_last) H_c + sum_j w_j x_j B_j^T
+//
+// Backward.  The adjoint of the state leaving chunk c, dH_{c+1}, runs
+// backwards over chunks like the forward state runs forwards:
+//
+//   dH_c = exp(cum_last) dH_{c+1} + sum_i exp(cum_i) dy_i C_i^T,
+//
+// starting from dL/dfinal after the last chunk; dinit = dH_0.  Within a
+// chunk, with dS_ij = dy_i . x_j and dG_ij = dS_ij L_ij dt_j:
+//
+//   dx_j  = sum_i M_ij dy_i + w_j dH_{c+1} B_j + D dy_j
+//   dC_i  = sum_j dG_ij B_j + exp(cum_i) H_c^T dy_i
+//   dB_j  = sum_i dG_ij C_i + w_j dH_{c+1}^T x_j
+//   dD    = sum_i dy_i . x_i
+//
+// and the decay terms through dcum_k = dL/dcum_k (chunk-local):
+//
+//   dcum_i += sum_j dS_ij M_ij + exp(cum_i) C_i . (H_c^T dy_i)      (row i)
+//   dcum_j -= sum_i dS_ij M_ij + w_j x_j . (dH_{c+1} B_j)           (column j)
+//   dcum_last += exp(cum_last) <dH_{c+1}, H_c> + sum_j w_j x_j . (dH_{c+1} B_j)
+//   ddt_j = sum_i dS_ij G_ij L_ij + exp(cum_last - cum_j) x_j . (dH_{c+1} B_j)
+//           + A sum_{k>=j} dcum_k
+//   dA    = sum_j dt_j sum_{k>=j} dcum_k          (over every chunk)
+//
+// Kernels (all fp32 arithmetic):
+//   bwd_outer_kernel<F>  per (chunk, head): the chunk state sum_j w_j x_j B_j^T
+//                        and exp(cum_last);
+//   bwd_outer_kernel<R>  per (chunk, head): sum_i exp(cum_i) dy_i C_i^T;
+//   bwd_pass_kernel      per (row, head, state element): the states entering
+//                        each chunk (forwards) / the adjoints leaving each
+//                        chunk (backwards), in place; dinit;
+//   bwd_grad_kernel      per (chunk, group, slice of up to 8 of the group's
+//                        heads): every gradient above.  C B^T is formed once
+//                        per block; dB and dC (shared by a group's heads) are
+//                        summed over the slice in registers and then with
+//                        atomics, like dA and dD, into buffers the entry
+//                        point zeroed.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "ssd.h"
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kQb = 64;     // chunk length
+constexpr int kThr = 256;   // threads per block
+constexpr int kPmax = 64;   // headdim of this path, at most
+constexpr int kNmax = 128;  // dstate of this path, at most
+constexpr int kNT = 32;     // dstate columns per tile of H / dH in the gradient kernel
+
+struct BP {
+  const void *x, *dt, *B, *C;
+  const float *A, *D, *init, *dy, *dfinal;
+  float *dx, *ddt, *dA, *dB, *dC, *dD, *dinit;
+  float* st;   // [chunks][H][P N]: chunk states, then the states entering each chunk
+  float* ad;   // [chunks][H][P N]: local adjoint sums, then the adjoints leaving each chunk
+  float* dec;  // [chunks][H]: exp(cum_last)
+  int T, H, P, N, G, nc;  // nc: chunks per batch row
+};
+
+template <bool BF16>
+__device__ __forceinline__ float ldin(const void* p, long long i) {
+  if (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+  return reinterpret_cast<const float*>(p)[i];
+}
+
+// Where chunk `c` (global index) lies: batch row, first token, valid rows.
+struct Chunk {
+  int b, t0, len;
+  long long tok0;  // global index of its first token
+};
+__device__ __forceinline__ Chunk chunk_of(const BP& p, int c) {
+  Chunk k;
+  k.b = c / p.nc;
+  k.t0 = (c % p.nc) * kQb;
+  k.len = min(kQb, p.T - k.t0);
+  k.tok0 = (long long)k.b * p.T + k.t0;
+  return k;
+}
+
+// cum[j] = sum_{k<=j} dt_k A (j < 64; dt = 0 past the valid rows) and dts[j]
+// = dt_j, by threads 0..63 (two warp scans).  Ends with a block barrier.
+template <bool BF16>
+__device__ __forceinline__ void chunk_cum(const BP& p, const Chunk& k, int h, float Ah, float* cum,
+                                          float* dts, float* wsum) {
+  const int t = threadIdx.x;
+  if (t < kQb) {
+    const float d = t < k.len ? ldin<BF16>(p.dt, (k.tok0 + t) * p.H + h) : 0.f;
+    float v = d * Ah;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, v, o);
+      if ((t & 31) >= o) v += u;
+    }
+    if ((t & 31) == 31) wsum[t >> 5] = v;
+    cum[t] = v;
+    dts[t] = d;
+  }
+  __syncthreads();
+  if (t >= 32 && t < kQb) cum[t] += wsum[0];
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- outer sums
+// MODE 0: out = sum_j w_j x_j B_j^T, w_j = exp(cum_last - cum_j) dt_j, into p.st,
+//         and exp(cum_last) into p.dec.
+// MODE 1: out = sum_i exp(cum_i) dy_i C_i^T into p.ad.
+constexpr size_t kOuterSmem = sizeof(float) * (kQb * kPmax + kQb * kNmax);
+
+template <bool BF16, int MODE>
+__global__ void __launch_bounds__(kThr) bwd_outer_kernel(BP p) {
+  extern __shared__ float osm[];
+  float* us = osm;                   // [64][P] weighted x (or dy) rows
+  float* vs = osm + kQb * kPmax;     // [64][N] B (or C) rows
+  __shared__ float cum[kQb], dts[kQb], wsum[2];
+  const int c = blockIdx.x, h = blockIdx.y;
+  const Chunk k = chunk_of(p, c);
+  const int g = (int)((long long)h * p.G / p.H);
+  const int P = p.P, N = p.N;
+  chunk_cum<BF16>(p, k, h, p.A[h], cum, dts, wsum);
+  const float last = cum[k.len - 1];
+  for (int e = threadIdx.x; e < kQb * P; e += kThr) {
+    const int j = e / P, q = e % P;
+    float v = 0.f;
+    if (j < k.len) {
+      const long long i = ((k.tok0 + j) * p.H + h) * P + q;
+      v = MODE == 0 ? expf(last - cum[j]) * dts[j] * ldin<BF16>(p.x, i)
+                    : expf(cum[j]) * p.dy[i];
+    }
+    us[j * P + q] = v;
+  }
+  const void* vsrc = MODE == 0 ? p.B : p.C;
+  for (int e = threadIdx.x; e < kQb * N; e += kThr) {
+    const int j = e / N, n = e % N;
+    vs[j * N + n] = j < k.len ? ldin<BF16>(vsrc, ((k.tok0 + j) * p.G + g) * N + n) : 0.f;
+  }
+  __syncthreads();
+  // thread (tp, tn): rows p = tp + 16 a, columns n = tn + 16 b
+  const int tp = threadIdx.x >> 4, tn = threadIdx.x & 15;
+  float acc[4][8];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int bb = 0; bb < 8; ++bb) acc[a][bb] = 0.f;
+  for (int j = 0; j < k.len; ++j) {
+    float u[4], v[8];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) u[a] = tp + 16 * a < P ? us[j * P + tp + 16 * a] : 0.f;
+#pragma unroll
+    for (int bb = 0; bb < 8; ++bb) v[bb] = tn + 16 * bb < N ? vs[j * N + tn + 16 * bb] : 0.f;
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb) acc[a][bb] = fmaf(u[a], v[bb], acc[a][bb]);
+  }
+  float* out = (MODE == 0 ? p.st : p.ad) + ((long long)c * p.H + h) * (long long)(P * N);
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int bb = 0; bb < 8; ++bb) {
+      const int q = tp + 16 * a, n = tn + 16 * bb;
+      if (q < P && n < N) out[q * N + n] = acc[a][bb];
+    }
+  if (MODE == 0 && threadIdx.x == 0) p.dec[(long long)c * p.H + h] = expf(last);
+}
+
+// ---------------------------------------------------------------- passes
+// FORWARD: st[c] <- state entering chunk c (from init); the state after the
+// row's last chunk is not needed.  BACKWARD: ad[c] <- adjoint leaving chunk c
+// (from dL/dfinal after the last chunk); dinit <- adjoint entering chunk 0.
+template <bool FORWARD>
+__global__ void __launch_bounds__(kThr) bwd_pass_kernel(BP p) {
+  // one thread per float4 of a state; the chunks' values are independent
+  // loads, issued eight at a time ahead of the recurrence
+  const int PN = p.P * p.N;
+  const int e4 = blockIdx.x * kThr + threadIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  if (4 * e4 >= PN) return;
+  const long long sh = ((long long)b * p.H + h) * PN + 4 * e4;
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (FORWARD && p.init) v = *reinterpret_cast<const float4*>(p.init + sh);
+  if (!FORWARD && p.dfinal) v = *reinterpret_cast<const float4*>(p.dfinal + sh);
+  float* buf = FORWARD ? p.st : p.ad;
+  for (int i0 = 0; i0 < p.nc; i0 += 8) {
+    float4 s[8];
+    float d[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (i0 + u < p.nc) {
+        const int c = b * p.nc + (FORWARD ? i0 + u : p.nc - 1 - (i0 + u));
+        s[u] = __ldcg(reinterpret_cast<const float4*>(buf + ((long long)c * p.H + h) * PN + 4 * e4));
+        d[u] = p.dec[(long long)c * p.H + h];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (i0 + u < p.nc) {
+        const int c = b * p.nc + (FORWARD ? i0 + u : p.nc - 1 - (i0 + u));
+        __stcg(reinterpret_cast<float4*>(buf + ((long long)c * p.H + h) * PN + 4 * e4), v);
+        v.x = fmaf(d[u], v.x, s[u].x);
+        v.y = fmaf(d[u], v.y, s[u].y);
+        v.z = fmaf(d[u], v.z, s[u].z);
+        v.w = fmaf(d[u], v.w, s[u].w);
+      }
+    }
+  }
+  if (!FORWARD && p.dinit) *reinterpret_cast<float4*>(p.dinit + sh) = v;
+}
+
+// ---------------------------------------------------------------- gradients
+constexpr int kHS = 8;          // heads of a group per gradient block
+constexpr int kPP = kPmax + 1;  // padded row pitches
+constexpr int kNP = kNmax + 1;
+constexpr int kQP = kQb + 1;
+constexpr int kTP = kNT + 1;
+constexpr size_t kGradSmem = sizeof(float) * (2 * kQb * kPP + 2 * kQb * kNP + 3 * kQb * kQP +
+                                              2 * kPmax * kTP + 8 * kQb);
+
+__device__ __forceinline__ float half_warp_sum(float v) {
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One block per (chunk, group, slice of kHS heads of the group): C B^T once,
+// then head after head the gradients above; dB and dC of the slice's heads
+// stay in registers and are added to global memory once.
+template <bool BF16>
+__global__ void __launch_bounds__(kThr) bwd_grad_kernel(BP p) {
+  extern __shared__ float sm[];
+  float* xs = sm;                  // [64][P+1] x rows
+  float* dys = xs + kQb * kPP;     // [64][P+1] dy rows
+  float* bs = dys + kQb * kPP;     // [64][N+1] B rows
+  float* cs = bs + kQb * kNP;      // [64][N+1] C rows
+  float* gs = cs + kQb * kNP;      // [64][65] G = C B^T
+  float* mm = gs + kQb * kQP;      // [64][65] M
+  float* gg = mm + kQb * kQP;      // [64][65] dG
+  float* hs = gg + kQb * kQP;      // [P][33] tile of H_c
+  float* dhs = hs + kPmax * kTP;   // [P][33] tile of dH_{c+1}
+  float* cum = dhs + kPmax * kTP;  // [64]
+  float* dts = cum + kQb;          // [64] dt
+  float* ec = dts + kQb;           // [64] exp(cum_i)
+  float* wt = ec + kQb;            // [64] w_j
+  float* dcum = wt + kQb;          // [64] dL/dcum
+  float* ddd = dcum + kQb;         // [64] direct dt terms
+  float* red = ddd + kQb;          // [64] block reductions
+  __shared__ float wsum[2];
+  const int c = blockIdx.x, g = blockIdx.y;
+  const Chunk k = chunk_of(p, c);
+  const int P = p.P, N = p.N, len = k.len;
+  const int hpg = p.H / p.G;
+  const int hb = g * hpg + blockIdx.z * kHS;
+  const int nh = min(kHS, hpg - blockIdx.z * kHS);
+  const int t = threadIdx.x;
+  const int ti = t >> 4, tj = t & 15;
+
+  for (int e = t; e < kQb * N; e += kThr) {
+    const int j = e / N, n = e % N;
+    const bool ok = j < len;
+    const long long i = ((k.tok0 + j) * p.G + g) * N + n;
+    bs[j * kNP + n] = ok ? ldin<BF16>(p.B, i) : 0.f;
+    cs[j * kNP + n] = ok ? ldin<BF16>(p.C, i) : 0.f;
+  }
+  __syncthreads();
+  // G = C B^T; rows i = ti + 16 r, columns j = tj + 16 s
+  {
+    float gacc[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2) gacc[r][s2] = 0.f;
+    for (int n = 0; n < N; ++n) {
+      float a[4], b[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = cs[(ti + 16 * r) * kNP + n];
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2) b[s2] = bs[(tj + 16 * s2) * kNP + n];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) gacc[r][s2] = fmaf(a[r], b[s2], gacc[r][s2]);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2) gs[(ti + 16 * r) * kQP + tj + 16 * s2] = gacc[r][s2];
+  }
+  // dB (rows j = ti + 16 r) and dC (rows i = ti + 16 r), columns n = tj + 16 s,
+  // summed over the slice's heads
+  float dca[4][8], dba[4][8];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2) dca[r][s2] = dba[r][s2] = 0.f;
+
+  for (int hh = 0; hh < nh; ++hh) {
+    const int h = hb + hh;
+    const float Ah = p.A[h];
+    const float Dh = p.D ? p.D[h] : 0.f;
+    __syncthreads();  // the previous head's tiles and tables are no longer read
+    chunk_cum<BF16>(p, k, h, Ah, cum, dts, wsum);
+    const float last = cum[len - 1];
+    if (t < kQb) {
+      ec[t] = expf(cum[t]);
+      wt[t] = expf(last - cum[t]) * dts[t];
+      dcum[t] = 0.f;
+      ddd[t] = 0.f;
+    }
+    for (int e = t; e < kQb * P; e += kThr) {
+      const int j = e / P, q = e % P;
+      const bool ok = j < len;
+      const long long i = ((k.tok0 + j) * p.H + h) * P + q;
+      xs[j * kPP + q] = ok ? ldin<BF16>(p.x, i) : 0.f;
+      dys[j * kPP + q] = ok ? p.dy[i] : 0.f;
+    }
+    __syncthreads();
+
+    // ---- dS = dY X^T; M, dG and the decay terms of the quadratic form
+    {
+      float sacc[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) sacc[r][s2] = 0.f;
+      for (int q = 0; q < P; ++q) {
+        float a[4], b[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) a[r] = dys[(ti + 16 * r) * kPP + q];
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) b[s2] = xs[(tj + 16 * s2) * kPP + q];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int s2 = 0; s2 < 4; ++s2) sacc[r][s2] = fmaf(a[r], b[s2], sacc[r][s2]);
+      }
+      float rowT[4] = {0.f, 0.f, 0.f, 0.f}, colT[4] = {0.f, 0.f, 0.f, 0.f},
+            colU[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = ti + 16 * r;
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) {
+          const int j = tj + 16 * s2;
+          float Mv = 0.f, dGv = 0.f;
+          if (j <= i && i < len) {
+            const float L = expf(cum[i] - cum[j]);
+            const float GL = gs[i * kQP + j] * L;
+            Mv = GL * dts[j];
+            dGv = sacc[r][s2] * L * dts[j];
+            const float T = sacc[r][s2] * Mv;
+            rowT[r] += T;
+            colT[s2] += T;
+            colU[s2] += sacc[r][s2] * GL;
+          }
+          mm[i * kQP + j] = Mv;
+          gg[i * kQP + j] = dGv;
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float v = half_warp_sum(rowT[r]);
+        if (tj == 0) atomicAdd(&dcum[ti + 16 * r], v);
+      }
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2) {
+        atomicAdd(&dcum[tj + 16 * s2], -colT[s2]);
+        atomicAdd(&ddd[tj + 16 * s2], colU[s2]);
+      }
+    }
+    __syncthreads();
+
+    // ---- dX (intra) = M^T dY; rows j = ti + 16 r, columns q = tj + 16 s
+    float dxa[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2) dxa[r][s2] = 0.f;
+    for (int i = 0; i < len; ++i) {
+      float a[4], b[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = mm[i * kQP + ti + 16 * r];
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2) b[s2] = tj + 16 * s2 < P ? dys[i * kPP + tj + 16 * s2] : 0.f;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) dxa[r][s2] = fmaf(a[r], b[s2], dxa[r][s2]);
+    }
+    // ---- dC += dG B, dB += dG^T C
+    for (int jj = 0; jj < len; ++jj) {
+      float a[4], a2[4], b[8], c2[8];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        a[r] = gg[(ti + 16 * r) * kQP + jj];
+        a2[r] = gg[jj * kQP + ti + 16 * r];
+      }
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2) {
+        b[s2] = bs[jj * kNP + tj + 16 * s2];
+        c2[s2] = cs[jj * kNP + tj + 16 * s2];
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+          dca[r][s2] = fmaf(a[r], b[s2], dca[r][s2]);
+          dba[r][s2] = fmaf(a2[r], c2[s2], dba[r][s2]);
+        }
+    }
+
+    // ---- state terms, over tiles of 32 dstate columns:
+    //   V = B dH^T (rows j, columns q), W = X dH, Z = dY H (rows, columns n), <dH, H>
+    const float* Hc = p.st + ((long long)c * p.H + h) * (long long)(P * N);
+    const float* dHc = p.ad + ((long long)c * p.H + h) * (long long)(P * N);
+    float va[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2) va[r][s2] = 0.f;
+    float hdot = 0.f, zc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < kNmax / kNT; ++m) {
+      const int n0 = m * kNT;
+      if (n0 >= N) break;
+      const int nt = min(kNT, N - n0);
+      __syncthreads();
+      for (int e = t; e < P * kNT; e += kThr) {
+        const int q = e / kNT, nn = e % kNT;
+        const bool ok = nn < nt;
+        const float hv = ok ? __ldcg(Hc + (long long)q * N + n0 + nn) : 0.f;
+        const float dv = ok ? __ldcg(dHc + (long long)q * N + n0 + nn) : 0.f;
+        hs[q * kTP + nn] = hv;
+        dhs[q * kTP + nn] = dv;
+        hdot = fmaf(hv, dv, hdot);
+      }
+      __syncthreads();
+      for (int nn = 0; nn < nt; ++nn) {
+        float a[4], b[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) a[r] = bs[(ti + 16 * r) * kNP + n0 + nn];
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) b[s2] = tj + 16 * s2 < P ? dhs[(tj + 16 * s2) * kTP + nn] : 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int s2 = 0; s2 < 4; ++s2) va[r][s2] = fmaf(a[r], b[s2], va[r][s2]);
+      }
+      float wa[4][2], za[4][2];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) wa[r][0] = wa[r][1] = za[r][0] = za[r][1] = 0.f;
+      for (int q = 0; q < P; ++q) {
+        float xa[4], ya[4], dh[2], hh2[2];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          xa[r] = xs[(ti + 16 * r) * kPP + q];
+          ya[r] = dys[(ti + 16 * r) * kPP + q];
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          dh[u] = dhs[q * kTP + tj + 16 * u];
+          hh2[u] = hs[q * kTP + tj + 16 * u];
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            wa[r][u] = fmaf(xa[r], dh[u], wa[r][u]);
+            za[r][u] = fmaf(ya[r], hh2[u], za[r][u]);
+          }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = ti + 16 * r;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int s2 = 2 * m + u;
+          if (s2 < 8 && n0 + tj + 16 * u < N) {
+            dba[r][s2] = fmaf(wt[row], wa[r][u], dba[r][s2]);
+            const float zz = ec[row] * za[r][u];
+            dca[r][s2] += zz;
+            zc[r] = fmaf(zz, cs[row * kNP + n0 + tj + 16 * u], zc[r]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float v = half_warp_sum(zc[r]);
+      if (tj == 0) atomicAdd(&dcum[ti + 16 * r], v);
+    }
+    float wv_sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int j = ti + 16 * r;
+      float vj = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2)
+        if (tj + 16 * s2 < P) vj = fmaf(xs[j * kPP + tj + 16 * s2], va[r][s2], vj);
+      vj = half_warp_sum(vj);
+      if (tj == 0 && j < len) {
+        atomicAdd(&dcum[j], -wt[j] * vj);
+        atomicAdd(&ddd[j], expf(last - cum[j]) * vj);
+        wv_sum = fmaf(wt[j], vj, wv_sum);
+      }
+    }
+    // dx = M^T dy + w_j dH B_j + D dy
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int j = ti + 16 * r;
+      if (j < len) {
+        float* dst = p.dx + ((k.tok0 + j) * p.H + h) * P;
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) {
+          const int q = tj + 16 * s2;
+          if (q < P) dst[q] = dxa[r][s2] + wt[j] * va[r][s2] + Dh * dys[j * kPP + q];
+        }
+      }
+    }
+    // block sums: <dH, H>, sum_j w_j v_j, dD
+    float dd = 0.f;
+    for (int e = t; e < len * P; e += kThr)
+      dd = fmaf(dys[(e / P) * kPP + e % P], xs[(e / P) * kPP + e % P], dd);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      hdot += __shfl_xor_sync(0xffffffffu, hdot, o);
+      wv_sum += __shfl_xor_sync(0xffffffffu, wv_sum, o);
+      dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    }
+    if ((t & 31) == 0) {
+      red[t >> 5] = hdot;
+      red[8 + (t >> 5)] = wv_sum;
+      red[16 + (t >> 5)] = dd;
+    }
+    __syncthreads();
+    if (t == 0) {
+      float a = 0.f, b = 0.f, d2 = 0.f;
+      for (int w = 0; w < kThr / 32; ++w) {
+        a += red[w];
+        b += red[8 + w];
+        d2 += red[16 + w];
+      }
+      dcum[len - 1] += expf(last) * a + b;
+      if (p.dD) atomicAdd(p.dD + h, d2);
+    }
+    __syncthreads();
+    // ddt_j = direct terms + A sum_{k>=j} dcum_k; dA += sum_j dt_j sum_{k>=j} dcum_k
+    if (t < 32) {
+      // reverse inclusive scan over the 64 entries, two per lane (lane l owns
+      // entries 63 - 2l and 62 - 2l, the later one first)
+      const int j1 = kQb - 1 - 2 * t, j2 = j1 - 1;
+      const float a1 = dcum[j1], a2 = dcum[j2];
+      float v = a1 + a2;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (t >= o) v += u;
+      }
+      const float r2 = v;       // sum over k >= j2
+      const float r1 = v - a2;  // sum over k >= j1
+      float da = 0.f;
+      if (j1 < len) {
+        p.ddt[(k.tok0 + j1) * p.H + h] = ddd[j1] + Ah * r1;
+        da = fmaf(dts[j1], r1, da);
+      }
+      if (j2 < len) {
+        p.ddt[(k.tok0 + j2) * p.H + h] = ddd[j2] + Ah * r2;
+        da = fmaf(dts[j2], r2, da);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
+      if (t == 0) atomicAdd(p.dA + h, da);
+    }
+  }
+  // dB, dC of the slice's heads
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int j = ti + 16 * r;
+    if (j < len) {
+      float* db = p.dB + ((k.tok0 + j) * p.G + g) * N;
+      float* dc = p.dC + ((k.tok0 + j) * p.G + g) * N;
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2) {
+        const int n = tj + 16 * s2;
+        if (n < N) {
+          atomicAdd(db + n, dba[r][s2]);
+          atomicAdd(dc + n, dca[r][s2]);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+bool bwd_chunked_supported(int P, int N) {
+  // the state passes move float4s
+  return P >= 1 && P <= kPmax && N >= 1 && N <= kNmax && (P * N) % 4 == 0;
+}
+
+size_t bwd_chunked_workspace_bytes(int batch, int T, int H, int P, int N) {
+  const long long nch = (long long)batch * ((T + kQb - 1) / kQb);
+  return 2 * align256(sizeof(float) * (size_t)nch * H * P * N) +
+         align256(sizeof(float) * (size_t)nch * H);
+}
+
+ssd_status_t bwd_chunked(const BwdArgs& a) {
+  BP p;
+  p.x = a.x;
+  p.dt = a.dt;
+  p.B = a.B;
+  p.C = a.C;
+  p.A = a.A;
+  p.D = a.D;
+  p.init = a.init;
+  p.dy = a.dy;
+  p.dfinal = a.dfinal;
+  p.dx = a.dx;
+  p.ddt = a.ddt;
+  p.dA = a.dA;
+  p.dB = a.dB;
+  p.dC = a.dC;
+  p.dD = a.dD;
+  p.dinit = a.dinit;
+  p.T = a.seqlen;
+  p.H = a.H;
+  p.P = a.P;
+  p.N = a.N;
+  p.G = a.G;
+  p.nc = (a.seqlen + kQb - 1) / kQb;
+  const long long nch = (long long)a.batch * p.nc;
+  char* ws = static_cast<char*>(a.ws);
+  const size_t sbytes = align256(sizeof(float) * (size_t)nch * a.H * a.P * a.N);
+  p.st = reinterpret_cast<float*>(ws);
+  p.ad = reinterpret_cast<float*>(ws + sbytes);
+  p.dec = reinterpret_cast<float*>(ws + 2 * sbytes);
+  const bool bf = a.dtype == SSD_DT_BF16;
+  const dim3 cgrid((unsigned)nch, a.H);
+  const dim3 pgrid((unsigned)((a.P * a.N / 4 + kThr - 1) / kThr), a.H, a.batch);
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    if (cudaFuncSetAttribute(bwd_grad_kernel<true>, at, (int)kGradSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_grad_kernel<false>, at, (int)kGradSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_outer_kernel<true, 0>, at, (int)kOuterSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_outer_kernel<true, 1>, at, (int)kOuterSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_outer_kernel<false, 0>, at, (int)kOuterSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_outer_kernel<false, 1>, at, (int)kOuterSmem) != cudaSuccess)
+      attr_err = cudaGetLastError();
+  });
+  if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
+  if (bf) {
+    bwd_outer_kernel<true, 0><<<cgrid, kThr, kOuterSmem, a.stream>>>(p);
+    bwd_outer_kernel<true, 1><<<cgrid, kThr, kOuterSmem, a.stream>>>(p);
+  } else {
+    bwd_outer_kernel<false, 0><<<cgrid, kThr, kOuterSmem, a.stream>>>(p);
+    bwd_outer_kernel<false, 1><<<cgrid, kThr, kOuterSmem, a.stream>>>(p);
+  }
+  bwd_pass_kernel<true><<<pgrid, kThr, 0, a.stream>>>(p);
+  bwd_pass_kernel<false><<<pgrid, kThr, 0, a.stream>>>(p);
+  const int hpg = a.H / a.G;
+  const dim3 ggrid((unsigned)nch, a.G, (unsigned)((hpg + kHS - 1) / kHS));
+  if (bf)
+    bwd_grad_kernel<true><<<ggrid, kThr, kGradSmem, a.stream>>>(p);
+  else
+    bwd_grad_kernel<false><<<ggrid, kThr, kGradSmem, a.stream>>>(p);
+  count_launches(5);
+  return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // namespace ssd

@@ -114,6 +114,12 @@ struct BwdArgs {
 };
 size_t bwd_workspace_bytes(int batch, int T, int H, int P, int N);
 ssd_status_t bwd(const BwdArgs& a);
+// The chunked backward (headdim <= 64, dstate <= 128); `bwd` takes it for
+// those shapes after zeroing the summed gradients, and the step-by-step
+// backward otherwise.
+bool bwd_chunked_supported(int P, int N);
+size_t bwd_chunked_workspace_bytes(int batch, int T, int H, int P, int N);
+ssd_status_t bwd_chunked(const BwdArgs& a);
 
 // Context parallelism: per-slice log-decay sums and the composition of the
 // slices' affine state maps.

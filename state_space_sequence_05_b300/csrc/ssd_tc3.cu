@@ -131,17 +131,6 @@ struct UnitPlan {
   }
 };
 
-// dt of tokens t0 + 4 lane .. t0 + 4 lane + 3 of a chunk (0 past the valid
-// rows), issued a chunk ahead so that the loads are in flight meanwhile.
-__device__ __forceinline__ void load_dt(const __nv_bfloat16* dt_g, int H, int h, long long t0,
-                                        int len, int lane, __nv_bfloat16 (&d)[4]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int j = 4 * lane + q;
-    d[q] = j < len ? dt_g[(t0 + j) * H + h] : __float2bfloat16(0.f);
-  }
-}
-
 // Chunk-local cumulative log2-decay of a chunk from its dt (lane l owns
 // tokens 4l .. 4l+3; dt is 0 past the valid rows, so c2 stays flat there).
 // Writes c2[128], dt[128] and, when E is given, E[j] = exp2(-c2_j) dt_j.
@@ -175,28 +164,48 @@ __device__ __forceinline__ void decay_tables(const __nv_bfloat16 (&d)[4], int le
 // memory: c2 fp32[128], E fp32[128], dt bf16[128].
 constexpr uint32_t kTabBytes = 512 + 512 + 256;
 
-// One warp per (chunk, head) of the call: the chunk's decay tables into
-// tabs[(global chunk) H + h], so that the persistent kernels fetch them with
-// one bulk copy per chunk.
+// One block per (chunk, tile of 8 heads): the tile's dt read row by row
+// (16-byte runs) into shared memory transposed, then one warp per head writes
+// its decay tables into tabs[(global chunk) H + h], so that the persistent
+// kernels fetch them with one bulk copy per chunk.
+constexpr int kTabHeads = 8;
+constexpr int kTabRow = kQ + 8;  // padded row of the transposed dt tile
 __global__ void __launch_bounds__(256)
     ssd_chunk_tables_kernel(const int32_t* uoff, const int32_t* coff, SeqInfo si, int H,
                             const __nv_bfloat16* dt, const float* A, uint8_t* tabs) {
+  __shared__ __align__(16) __nv_bfloat16 dts[kTabHeads * kTabRow];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int nseq = si.nseq;
   if (uoff[nseq + 1] != 0) return;
-  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= (long long)coff[nseq] * H) return;
-  const int gc = (int)(w / H), h = (int)(w % H);
+  const int gc = blockIdx.x;
+  if (gc >= coff[nseq]) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = upper_index(coff, nseq, gc);
   const long long t0 = si.begin(s) + (long long)(gc - coff[s]) * kQ;
   const int len = (int)min((long long)kQ, si.end(s) - t0);
-  __nv_bfloat16 d[4];
-  load_dt(dt, H, h, t0, len, lane, d);
-  uint8_t* tb = tabs + w * kTabBytes;
-  decay_tables(d, len, A[h] * kLog2e, reinterpret_cast<float*>(tb), reinterpret_cast<float*>(tb + 512),
-               reinterpret_cast<__nv_bfloat16*>(tb + 1024), lane);
+  {
+    const int h0 = blockIdx.y * kTabHeads;
+    const int nh = min(kTabHeads, H - h0);
+    for (int e = threadIdx.x; e < kQ * nh; e += blockDim.x) {
+      const int j = e / nh, hh = e % nh;
+      dts[hh * kTabRow + j] = j < len ? dt[(t0 + j) * H + h0 + hh] : __float2bfloat16(0.f);
+    }
+    __syncthreads();
+    for (int hh = warp; hh < nh; hh += blockDim.x >> 5) {
+      const uint2 v = *reinterpret_cast<const uint2*>(dts + hh * kTabRow + 4 * lane);
+      __nv_bfloat16 d[4];
+      d[0] = __ushort_as_bfloat16((unsigned short)(v.x & 0xffffu));
+      d[1] = __ushort_as_bfloat16((unsigned short)(v.x >> 16));
+      d[2] = __ushort_as_bfloat16((unsigned short)(v.y & 0xffffu));
+      d[3] = __ushort_as_bfloat16((unsigned short)(v.y >> 16));
+      const int h = h0 + hh;
+      uint8_t* tb = tabs + ((long long)gc * H + h) * kTabBytes;
+      decay_tables(d, len, A[h] * kLog2e, reinterpret_cast<float*>(tb),
+                   reinterpret_cast<float*>(tb + 512), reinterpret_cast<__nv_bfloat16*>(tb + 1024),
+                   lane);
+    }
+  }
 }
 
 // One 16-byte work item of w o X (items k = 0..1023: 8 values of row j =
@@ -230,9 +239,10 @@ constexpr uint32_t kIdSX = idesc_bf16(128, 64, false, true);
 // ============================================================== kernel 1
 namespace k1 {
 constexpr int kStages = 3;
-constexpr uint32_t kStageBytes = 3 * kTile;         // x, B (n 0..63), B (n 64..127)
-constexpr uint32_t kOffW = kStages * kStageBytes;   // 2 buffers x (hi, lo)
-constexpr uint32_t kOffTabs = kOffW + 4 * kTile;    // per stage: the chunk's decay tables
+// A stage: the x tile (overwritten in place by w o X hi), w o X lo, B (n 0..63),
+// B (n 64..127).  [hi | lo] is the N = 128 operand of the state product.
+constexpr uint32_t kStageBytes = 4 * kTile;
+constexpr uint32_t kOffTabs = kStages * kStageBytes;  // per stage: the chunk's decay tables
 constexpr uint32_t kOffInfo = kOffTabs + kStages * kTabBytes;
 constexpr uint32_t kOffBars = kOffInfo + kStages * 64;
 constexpr uint32_t kBarBytes = 16 * 8;
@@ -241,13 +251,12 @@ static_assert(kSmemBytes <= 232448, "shared memory per block");
 constexpr uint32_t kTmemCols = 256;  // two accumulators [hi | lo] x 128 columns
 
 enum {
-  kFull0 = 0, kFull1, kFull2,          // stage loaded (TMA) and its tables written
-  kEmpty0 = 3, kEmpty1, kEmpty2,       // stage read (math warps + MMA commit)
-  kWxFull0 = 6, kWxFull1,              // w o X written (math warps)
-  kWxFree0 = 8, kWxFree1,              // w o X read (MMA commit)
-  kAccFull0 = 10, kAccFull1,           // unit's product complete (MMA commit)
-  kAccFree0 = 12, kAccFree1,           // unit's product read (math warps)
-  kMmaDone = 14,
+  kFull0 = 0, kFull1, kFull2,          // stage loaded (TMA: tiles and tables)
+  kEmpty0 = 3, kEmpty1, kEmpty2,       // stage's state product done (MMA commit)
+  kWxFull0 = 6, kWxFull1, kWxFull2,    // w o X written in the stage (math warps)
+  kAccFull0 = 9, kAccFull1,            // unit's product complete (MMA commit)
+  kAccFree0 = 11, kAccFree1,           // unit's product read (math warps)
+  kMmaDone = 13,
   kNumBars
 };
 static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
@@ -274,8 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   uint8_t* const sb = smem_raw;
   auto X = [&](int st) { return sb + st * kStageBytes; };
-  auto Bt = [&](int st) { return sb + st * kStageBytes + kTile; };
-  auto W = [&](int wb) { return sb + kOffW + wb * 2 * kTile; };
+  auto Bt = [&](int st) { return sb + st * kStageBytes + 2 * kTile; };
   auto c2 = [&](int st) { return reinterpret_cast<float*>(sb + kOffTabs + st * kTabBytes); };
   auto dtt = [&](int st) {
     return reinterpret_cast<__nv_bfloat16*>(sb + kOffTabs + st * kTabBytes + 1024);
@@ -288,12 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int b = 0; b < kStages; ++b) {
-      mbar_init(&bars[kFull0 + b], 1);                // expect-tx arrival (tiles, tables)
-      mbar_init(&bars[kEmpty0 + b], kMathWarps + 1);  // math warps + MMA commit
+      mbar_init(&bars[kFull0 + b], 1);   // expect-tx arrival (tiles, tables)
+      mbar_init(&bars[kEmpty0 + b], 1);  // MMA commit
+      mbar_init(&bars[kWxFull0 + b], kMathWarps);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars[kWxFull0 + b], kMathWarps);
-      mbar_init(&bars[kWxFree0 + b], 1);
       mbar_init(&bars[kAccFull0 + b], 1);
       mbar_init(&bars[kAccFree0 + b], kMathWarps);
     }
@@ -412,9 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     const uint64_t dBt0 = sdesc_sw128(smem_u32(Bt(0)), kTile, 1024);  // MN-major B^T
-    const uint64_t dW0 = sdesc_sw128(smem_u32(W(0)), kTile, 1024);    // [w o X hi | lo]
+    const uint64_t dW0 = sdesc_sw128(smem_u32(X(0)), kTile, 1024);    // [w o X hi | lo]
     constexpr uint64_t kSt16 = kStageBytes >> 4;
-    constexpr uint64_t kW16 = (2 * kTile) >> 4;
     uint32_t it = 0, uc = 0;
     bool issued = false;
 #define MMA_WAIT(bar, par)                      \
@@ -427,8 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       MMA_WAIT(kFull0 + st, (it / kStages) & 1u);
       const TileInfo inf = *info(st);
       if (inf.kind == kKindEnd || *abort_v) break;
-      const int wb = it & 1;
-      MMA_WAIT(kWxFull0 + wb, (it >> 1) & 1u);
+      MMA_WAIT(kWxFull0 + st, (it / kStages) & 1u);
       const int ab = uc & 1;
       if (inf.first && uc >= 2) { MMA_WAIT(kAccFree0 + ab, ((uc >> 1) - 1) & 1u); }
       tc_fence_after();
@@ -436,10 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + ab * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(d, dBt0 + st * kSt16 + kk * 128, dW0 + wb * kW16 + kk * 128, kIdSt,
+          mma_bf16(d, dBt0 + st * kSt16 + kk * 128, dW0 + st * kSt16 + kk * 128, kIdSt,
                    !(inf.first && kk == 0));
         mma_commit(&bars[kEmpty0 + st]);
-        mma_commit(&bars[kWxFree0 + wb]);
         if (inf.last) mma_commit(&bars[kAccFull0 + ab]);
       }
       __syncwarp();
@@ -500,15 +504,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo inf = *info(st);
       if (inf.kind == kKindEnd || __any_sync(0xffffffffu, *abort_v)) break;
       if (inf.first) later = 0.f;
-      const int wb = it & 1;
-      if (it >= 2) MATH_TRY(wait_bar_warp(&bars[kWxFree0 + wb], ((it >> 1) - 1) & 1u, wns));
       const float c2l = c2(st)[kQ - 1];
       const float wl = later + c2l;
-      wx_item(X(st), c2(st), dtt(st), tid, wl, W(wb));
-      wx_item(X(st), c2(st), dtt(st), tid + 512, wl, W(wb));
+      // w o X hi over the x tile in place (each item is read, then rewritten,
+      // by the same thread), lo into the next tile
+      wx_item(X(st), c2(st), dtt(st), tid, wl, X(st));
+      wx_item(X(st), c2(st), dtt(st), tid + 512, wl, X(st));
       fence_proxy_async_smem();
-      arrive(kWxFull0 + wb);
-      arrive(kEmpty0 + st);
+      arrive(kWxFull0 + st);
       later += c2l;
       if (pending) {
         MATH_TRY(readout());
@@ -1310,9 +1313,8 @@ ssd_status_t states_pass(const FwdArgs& a, unsigned long long wait_ns, int hold_
     const __nv_bfloat16* dtp = static_cast<const __nv_bfloat16*>(a.dt);
     const float* Ap = a.A;
     void* args[] = {&cuoff, &ccoff, &si, &H, &dtp, &Ap, &tabs};
-    const long long threads = max_tc_chunks(a) * a.H * 32;
-    const unsigned blocks = (unsigned)((threads + 255) / 256);
-    if (launch_pdl(reinterpret_cast<const void*>(ssd_chunk_tables_kernel), dim3(blocks), dim3(256),
+    const dim3 blocks((unsigned)max_tc_chunks(a), (unsigned)((a.H + kTabHeads - 1) / kTabHeads));
+    if (launch_pdl(reinterpret_cast<const void*>(ssd_chunk_tables_kernel), blocks, dim3(256),
                    0, a.stream, args) != cudaSuccess)
       return SSD_ERR_CUDA;
   }

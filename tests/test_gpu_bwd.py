@@ -69,3 +69,40 @@ def test_bwd_without_optional_inputs():
     _check(I.small_workload(batch=1, seqlen=64, nheads=2, headdim=4, dstate=32, ngroups=1,
                             chunk=64, dtype="f32", init="zero", seed=63),
            use_D=False, use_init=False, use_dfinal=False, seed=2)
+
+
+def test_bwd_l8k_shape_sampled_heads():
+    """The metric's layer length (b1 T8192 H80 P64 N128, bf16, init, D):
+    128 chunks of the chunked backward.  The fp64 oracle walks one head at a
+    time (≈0.7 s per head at 8192 steps on one host thread), so four heads
+    are checked: their per-head gradients (dx, ddt, dA, dD, dinit) from the
+    full 80-head call, and every gradient, dB and dC included, from a call
+    on those four heads alone."""
+    import torch
+    from state_space_sequence_05_b300 import ssd
+    fi = I.make_forward_inputs(I.WORKLOADS["l8k"])
+    d = to_device(fi)
+    b, T, H, P = fi.x.shape
+    rng = np.random.Generator(np.random.PCG64(905))
+    dy = rng.standard_normal((b, T, H, P)).astype(np.float32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    g_all = ssd.ssd_chunk_scan_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"],
+                                   t(dy))
+    heads = [0, 27, 53, 79]
+    hsel = lambda v, ax: np.ascontiguousarray(np.take(v, heads, axis=ax))
+    xs, dts, As, Ds = hsel(fi.x, 2), hsel(fi.dt, 2), fi.A[heads], fi.D[heads]
+    inits, dys = hsel(fi.init, 1), hsel(dy, 2)
+    # the bf16 inputs keep their exact values on the device slice
+    dsl = {k: torch.index_select(d[k], 2, torch.tensor(heads, device="cuda")).contiguous()
+           for k in ("x", "dt")}
+    g_sub = ssd.ssd_chunk_scan_bwd(dsl["x"], dsl["dt"], t(As), d["B"], d["C"], t(Ds), t(inits),
+                                   t(dys))
+    torch.cuda.synchronize()
+    ref = oracle.ssd_bwd(xs, dts, As, fi.B, fi.C, Ds, inits, dys, None)
+    for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dinit"):
+        e = oracle.rel_err(g_sub[k].cpu().numpy(), ref[k])
+        assert e <= TOL_BWD, f"{k} (four heads): max|diff|/RMS = {e:.3e}"
+    per_head_axis = {"dx": 2, "ddt": 2, "dA": 0, "dD": 0, "dinit": 1}
+    for k, ax in per_head_axis.items():
+        e = oracle.rel_err(hsel(g_all[k].cpu().numpy(), ax), ref[k])
+        assert e <= TOL_BWD, f"{k} (full call, sampled heads): max|diff|/RMS = {e:.3e}"
