@@ -17,7 +17,10 @@ and the final states back -- for a batch-1 sequence in four slices carried
 by their states, so the copies in, the calls and the copies out overlap on
 three streams (the one-stream time is reported beside it).
 ``other_workloads`` times the forward on the 4 x 2K, 64K and packed
-varlen workloads.  Clocks are sampled through NVML about every millisecond
+varlen workloads; ``tc_kernel_variants`` the same l8k call on the split and
+pipelined tensor-core forwards; ``states_only`` the states-only pass
+(final states without y), whole and on a 4096-token slice against the
+forward on that slice.  Clocks are sampled through NVML about every millisecond
 during the timed calls.  ``--impl reference`` times the fp64 CPU oracle on
 the host cores instead.  With N > 1 (torchrun) every rank runs its own
 replica of the workload (independent problems, no collective on the data
@@ -57,6 +60,8 @@ def parse_args():
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward pass")
     ap.add_argument("--no-s6", action="store_true",
                     help="skip the Mamba-1 selective-scan comparison")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the other tensor-core forwards and the states-only pass")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the l2k_b4 / l64k / varlen64 forward measurements")
     return ap.parse_args()
@@ -456,6 +461,11 @@ def main():
     if not args.no_other_workloads and wl.name == "l8k":
         others = {n: measure_workload(n, dev, peaks, flush) for n in ("l2k_b4", "l64k", "varlen64")}
 
+    variants = states = None
+    if not args.no_variants and wl.name == "l8k":
+        variants = measure_variants(call, status, flush, ntok, bytes_, peaks, ms * 1e3)
+        states = measure_states(d, A, wl, flush, ntok, ms * 1e3)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(fi, wl)
@@ -474,10 +484,76 @@ def main():
                "step_ms_max": max(step_ms), "step_ms_first5": [round(v, 4) for v in step_ms[:5]],
                "e2e": e2e, "cpu_baseline": cpu, "other_workloads": others, "decode": decode,
                "epilogue": epilogue, "backward": backward, "s6": s6,
+               "tc_kernel_variants": variants, "states_only": states,
                "pages_claim": "SSD 2-8x faster than Mamba's fused selective scan (A100), context only"}
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def _timed_median(fn, flush, reps, warmup=3):
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    us = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us.append(1e3 * e0.elapsed_time(e1))
+    return statistics.median(us)
+
+
+def measure_variants(call, status, flush, ntok, bytes_, peaks, default_us, reps=20):
+    """The same l8k call on the other tensor-core forwards (SSD_TC_KERNEL):
+    the split kernels and the pipelined fused kernel; median of `reps`
+    calls, L2 flushed before each."""
+    out = {"default": {"kernel": "fused", "us_median_of_main_run": default_us}}
+    prev = os.environ.get("SSD_TC_KERNEL")
+    try:
+        for k in ("split", "pipelined"):
+            os.environ["SSD_TC_KERNEL"] = k
+            med = _timed_median(call, flush, reps)
+            if int(status.item()) != 0:
+                raise SystemExit(f"device status {int(status.item())} on the {k} kernel")
+            gbs = bytes_ / (med * 1e-6) / 1e9
+            out[k] = {"us_median": med, "tokens_per_s": ntok / (med * 1e-6),
+                      "roofline_frac": gbs / peaks["hbm_gbs"]}
+    finally:
+        if prev is None:
+            os.environ.pop("SSD_TC_KERNEL", None)
+        else:
+            os.environ["SSD_TC_KERNEL"] = prev
+    return out
+
+
+def measure_states(d, A, wl, flush, ntok, forward_us, reps=20):
+    """ssd_chunk_scan_states (each sequence's final state without y) on the
+    l8k layer and on a 4096-token slice of it: context parallelism's first
+    pass per rank, against the forward on the same slice."""
+    import torch
+    from state_space_sequence_05_b300 import ssd
+    fin = torch.empty((wl.batch, wl.nheads, wl.headdim, wl.dstate), device=d["x"].device)
+    full = _timed_median(lambda: ssd.ssd_chunk_scan_states(d["x"], d["dt"], A, d["B"], wl.chunk,
+                                                           final_states=fin), flush, reps)
+    sl = {k: d[k][:, :4096].contiguous() for k in ("x", "dt", "B", "C")}
+    st_slice = _timed_median(lambda: ssd.ssd_chunk_scan_states(sl["x"], sl["dt"], A, sl["B"],
+                                                               wl.chunk, final_states=fin),
+                             flush, reps)
+    fw_slice = _timed_median(lambda: ssd.ssd_chunk_scan_fwd(sl["x"], sl["dt"], A, sl["B"],
+                                                            sl["C"], None, wl.chunk, None),
+                             flush, reps)
+    return {"l8k_us_median": full, "l8k_tokens_per_s": ntok / (full * 1e-6),
+            "vs_forward": full / forward_us,
+            "slice_4096": {"states_only_us": st_slice, "forward_us": fw_slice},
+            "how": "final states only (segment states and state passing; no y), median of "
+                   f"{reps} calls, L2 flushed before each"}
 
 
 def measure_e2e(args, fi, wl, dev, A, D, call_kwargs):

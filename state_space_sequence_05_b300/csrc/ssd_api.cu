@@ -56,15 +56,16 @@ ssd_status_t check_fwd(const FwdArgs& a, bool check_ptrs) {
 }
 
 // Which tensor-core forward runs the plain (no fused-epilogue) calls:
-// SSD_TC_KERNEL=split (the default: segment states, state passing, outputs
-// as three kernels), =fused (one kernel with the segment hand-off inside) or
-// =pipelined (the fused design with a deeper operand pipeline).
-enum class TcKernel { kSplit, kFused, kPipelined };
+// SSD_TC_KERNEL=fused (the default: one kernel with the segment hand-off
+// inside), =split (decay tables, segment states, state passing and outputs
+// as separate kernels) or =pipelined (the fused design with a deeper
+// operand pipeline).
+enum class TcKernel { kFused, kSplit, kPipelined };
 TcKernel tc_kernel() {
   const char* e = getenv("SSD_TC_KERNEL");
-  if (e && strcmp(e, "fused") == 0) return TcKernel::kFused;
+  if (e && strcmp(e, "split") == 0) return TcKernel::kSplit;
   if (e && strcmp(e, "pipelined") == 0) return TcKernel::kPipelined;
-  return TcKernel::kSplit;
+  return TcKernel::kFused;
 }
 
 size_t fwd_workspace(const FwdArgs& a) {
