@@ -117,17 +117,47 @@ __device__ __forceinline__ void chunk_cum(const BP& p, const Chunk& k, int h, fl
   __syncthreads();
 }
 
+// ---------------------------------------------------------------- warp MMA
+// Operands of the tensor-core products are fp32 values split into bf16 hi =
+// rn(v) and lo = rn(v - hi) (|v - hi - lo| <= 2^-18 |v|); a product of two
+// split operands is taken as hi.hi + hi.lo + lo.hi, of a split operand and an
+// exact bf16 one as hi.b + lo.b, both accumulated in fp32.
+__device__ __forceinline__ void split_rn(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+// D (16 x 8, fp32) += A (16 x 16, bf16, row-major fragment) B (16 x 8, bf16)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t ld32(const __nv_bfloat16* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
+}
+
 // ---------------------------------------------------------------- outer sums
 // MODE 0: out = sum_j w_j x_j B_j^T, w_j = exp(cum_last - cum_j) dt_j, into p.st,
 //         and exp(cum_last) into p.dec.
 // MODE 1: out = sum_i exp(cum_i) dy_i C_i^T into p.ad.
-constexpr size_t kOuterSmem = sizeof(float) * (kQb * kPmax + kQb * kNmax);
+// A (P x 64 tokens) = the weighted rows transposed, B (64 tokens x N) = B or
+// C, on the tensor cores: warp w takes output rows 16 (w % 4).. and columns
+// 64 (w / 4).. (eight 16 x 8 tiles).
+constexpr int kJP = kQb + 8;  // padded pitch (bf16) of a transposed operand row
+constexpr size_t kOuterSmem = sizeof(__nv_bfloat16) * 2 * (kPmax * kJP + kNmax * kJP);
 
 template <bool BF16, int MODE>
 __global__ void __launch_bounds__(kThr) bwd_outer_kernel(BP p) {
-  extern __shared__ float osm[];
-  float* us = osm;                   // [64][P] weighted x (or dy) rows
-  float* vs = osm + kQb * kPmax;     // [64][N] B (or C) rows
+  extern __shared__ __align__(16) unsigned char osm_raw[];
+  __nv_bfloat16* uh = reinterpret_cast<__nv_bfloat16*>(osm_raw);  // [64 p][72]: hi
+  __nv_bfloat16* ul = uh + kPmax * kJP;                            // lo
+  __nv_bfloat16* vh = ul + kPmax * kJP;                            // [128 n][72]: hi
+  __nv_bfloat16* vl = vh + kNmax * kJP;                            // lo (float32 inputs)
   __shared__ float cum[kQb], dts[kQb], wsum[2];
   const int c = blockIdx.x, h = blockIdx.y;
   const Chunk k = chunk_of(p, c);
@@ -135,48 +165,67 @@ __global__ void __launch_bounds__(kThr) bwd_outer_kernel(BP p) {
   const int P = p.P, N = p.N;
   chunk_cum<BF16>(p, k, h, p.A[h], cum, dts, wsum);
   const float last = cum[k.len - 1];
-  for (int e = threadIdx.x; e < kQb * P; e += kThr) {
-    const int j = e / P, q = e % P;
+  for (int e = threadIdx.x; e < kQb * kPmax; e += kThr) {
+    const int j = e / kPmax, q = e % kPmax;
     float v = 0.f;
-    if (j < k.len) {
+    if (j < k.len && q < P) {
       const long long i = ((k.tok0 + j) * p.H + h) * P + q;
       v = MODE == 0 ? expf(last - cum[j]) * dts[j] * ldin<BF16>(p.x, i)
                     : expf(cum[j]) * p.dy[i];
     }
-    us[j * P + q] = v;
+    split_rn(v, uh[q * kJP + j], ul[q * kJP + j]);
   }
   const void* vsrc = MODE == 0 ? p.B : p.C;
-  for (int e = threadIdx.x; e < kQb * N; e += kThr) {
-    const int j = e / N, n = e % N;
-    vs[j * N + n] = j < k.len ? ldin<BF16>(vsrc, ((k.tok0 + j) * p.G + g) * N + n) : 0.f;
+  for (int e = threadIdx.x; e < kQb * kNmax; e += kThr) {
+    const int j = e / kNmax, n = e % kNmax;
+    const float v = (j < k.len && n < N) ? ldin<BF16>(vsrc, ((k.tok0 + j) * p.G + g) * N + n) : 0.f;
+    if (BF16) {
+      vh[n * kJP + j] = __float2bfloat16_rn(v);  // exact
+    } else {
+      split_rn(v, vh[n * kJP + j], vl[n * kJP + j]);
+    }
   }
   __syncthreads();
-  // thread (tp, tn): rows p = tp + 16 a, columns n = tn + 16 b
-  const int tp = threadIdx.x >> 4, tn = threadIdx.x & 15;
-  float acc[4][8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;  // fragment row group and column pair
+  const int r0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);
+  float acc[8][4];
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 #pragma unroll
-    for (int bb = 0; bb < 8; ++bb) acc[a][bb] = 0.f;
-  for (int j = 0; j < k.len; ++j) {
-    float u[4], v[8];
+  for (int k0 = 0; k0 < kQb; k0 += 16) {
+    uint32_t ah[4], al[4];
+    const int ra = (r0 + gq) * kJP + k0 + 2 * tq, rb = ra + 8 * kJP;
+    ah[0] = ld32(uh + ra);
+    ah[1] = ld32(uh + rb);
+    ah[2] = ld32(uh + ra + 8);
+    ah[3] = ld32(uh + rb + 8);
+    al[0] = ld32(ul + ra);
+    al[1] = ld32(ul + rb);
+    al[2] = ld32(ul + ra + 8);
+    al[3] = ld32(ul + rb + 8);
 #pragma unroll
-    for (int a = 0; a < 4; ++a) u[a] = tp + 16 * a < P ? us[j * P + tp + 16 * a] : 0.f;
-#pragma unroll
-    for (int bb = 0; bb < 8; ++bb) v[bb] = tn + 16 * bb < N ? vs[j * N + tn + 16 * bb] : 0.f;
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int bb = 0; bb < 8; ++bb) acc[a][bb] = fmaf(u[a], v[bb], acc[a][bb]);
+    for (int t = 0; t < 8; ++t) {
+      const int nb = (n0 + 8 * t + gq) * kJP + k0 + 2 * tq;
+      const uint32_t b0 = ld32(vh + nb), b1 = ld32(vh + nb + 8);
+      mma16816(acc[t], ah, b0, b1);
+      mma16816(acc[t], al, b0, b1);
+      if (!BF16) mma16816(acc[t], ah, ld32(vl + nb), ld32(vl + nb + 8));
+    }
   }
   float* out = (MODE == 0 ? p.st : p.ad) + ((long long)c * p.H + h) * (long long)(P * N);
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int t = 0; t < 8; ++t) {
+    const int n = n0 + 8 * t + 2 * tq;
 #pragma unroll
-    for (int bb = 0; bb < 8; ++bb) {
-      const int q = tp + 16 * a, n = tn + 16 * bb;
-      if (q < P && n < N) out[q * N + n] = acc[a][bb];
+    for (int hf = 0; hf < 2; ++hf) {
+      const int q = r0 + gq + 8 * hf;
+      if (q < P) {
+        if (n < N) out[q * N + n] = acc[t][2 * hf];
+        if (n + 1 < N) out[q * N + n + 1] = acc[t][2 * hf + 1];
+      }
     }
+  }
   if (MODE == 0 && threadIdx.x == 0) p.dec[(long long)c * p.H + h] = expf(last);
 }
 
