@@ -54,6 +54,7 @@
 
 #include "ssd.h"
 #include "ssd_internal.h"
+#include "tc_ptx.cuh"
 
 namespace ssd {
 namespace {
@@ -655,6 +656,493 @@ __global__ void __launch_bounds__(kThr) bwd_grad_kernel(BP p) {
   }
 }
 
+// ---------------------------------------------------------------- gradients, tensor cores
+// bf16 inputs with headdim and dstate multiples of 8: the products of the
+// gradient kernel above on warp MMAs.  Per block the operands live in shared
+// memory once, as bf16 (exact for the bf16 inputs x, B, C; hi/lo pairs for
+// the fp32 dy, H_c, dH_{c+1}, M and dG), padded to the full 64 x 64 and
+// 64 x 128 tiles with zeros; ldmatrix reads them in either orientation.  Warp
+// tiles (8 warps): dS and C B^T: rows 16 (w % 4), columns 32 (w / 4);
+// dx = M^T dy + w B dH^T: rows 16 (w % 4), columns 32 (w / 4); dC and dB
+// (with the state terms dy H and x dH): rows 16 (w % 4), columns 64 (w / 4).
+// C B^T stays in registers for the slice's heads, dB and dC likewise.  Blocks
+// of M and dG that the causal mask zeroes are skipped.
+constexpr int kAP = kQb + 8;    // pitch (bf16) of the 64 x 64 tiles
+constexpr int kBP = kNmax + 8;  // pitch (bf16) of the 64 x 128 tiles
+constexpr size_t kT64 = sizeof(__nv_bfloat16) * kQb * kAP;
+constexpr size_t kT128 = sizeof(__nv_bfloat16) * kQb * kBP;
+constexpr size_t kGradMmaSmem = 6 * kT128 + 7 * kT64 + sizeof(float) * (8 * kQb + 32);
+
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t a) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t a) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+
+// Per-lane row/column offsets of the four 8 x 8 matrices of an ldmatrix.x4:
+// pattern X for a left operand stored [m][k] and a right operand stored
+// [k][n]; pattern Y for a left operand stored [k][m] and a right operand
+// stored [n][k].
+struct LaneOff {
+  int rx, cx, ry, cy;
+};
+__device__ __forceinline__ LaneOff lane_off(int lane) {
+  LaneOff o;
+  o.rx = (lane & 7) + ((lane >> 3) & 1) * 8;
+  o.cx = (lane >> 4) * 8;
+  o.ry = (lane & 7) + (lane >> 4) * 8;
+  o.cy = ((lane >> 3) & 1) * 8;
+  return o;
+}
+
+// acc[t] (16 x 8, t < NT) += A (16 x K) B (K x 8 NT) for k in [kb, ke) (steps
+// of 16): A's rows m0.., stored [m][k] (TA false) or [k][m]; B's columns
+// n0.., stored [n][k] (TB false) or [k][n].  ALO / BLO: the operand is a
+// hi/lo pair (lo at al / bl), else exact in bf16.  Shared addresses in bytes.
+template <int NT, int PA, bool TA, bool ALO, int PB, bool TB, bool BLO>
+__device__ __forceinline__ void warp_mma(float (&acc)[NT][4], uint32_t ah_s, uint32_t al_s, int m0,
+                                         uint32_t bh_s, uint32_t bl_s, int n0, int kb, int ke,
+                                         const LaneOff& o) {
+  for (int k0 = kb; k0 < ke; k0 += 16) {
+    const uint32_t aoff = TA ? 2u * ((k0 + o.ry) * PA + m0 + o.cy) : 2u * ((m0 + o.rx) * PA + k0 + o.cx);
+    uint32_t ah[4], al[4];
+    if (TA) {
+      ldsm4t(ah, ah_s + aoff);
+      if (ALO) ldsm4t(al, al_s + aoff);
+    } else {
+      ldsm4(ah, ah_s + aoff);
+      if (ALO) ldsm4(al, al_s + aoff);
+    }
+#pragma unroll
+    for (int u = 0; u < NT / 2; ++u) {
+      const int nb = n0 + 16 * u;
+      const uint32_t boff = TB ? 2u * ((k0 + o.rx) * PB + nb + o.cx) : 2u * ((nb + o.ry) * PB + k0 + o.cy);
+      uint32_t bh[4], bl[4];
+      if (TB) {
+        ldsm4t(bh, bh_s + boff);
+        if (BLO) ldsm4t(bl, bl_s + boff);
+      } else {
+        ldsm4(bh, bh_s + boff);
+        if (BLO) ldsm4(bl, bl_s + boff);
+      }
+      mma16816(acc[2 * u], ah, bh[0], bh[1]);
+      mma16816(acc[2 * u + 1], ah, bh[2], bh[3]);
+      if (ALO) {
+        mma16816(acc[2 * u], al, bh[0], bh[1]);
+        mma16816(acc[2 * u + 1], al, bh[2], bh[3]);
+      }
+      if (BLO) {
+        mma16816(acc[2 * u], ah, bl[0], bl[1]);
+        mma16816(acc[2 * u + 1], ah, bl[2], bl[3]);
+      }
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+
+// four fp32 values -> hi/lo bf16 quadruples (8 bytes each) at dh / dl
+__device__ __forceinline__ void store_split4(__nv_bfloat16* dh, __nv_bfloat16* dl, float4 v) {
+  __nv_bfloat16 h0, h1, h2, h3, l0, l1, l2, l3;
+  split_rn(v.x, h0, l0);
+  split_rn(v.y, h1, l1);
+  split_rn(v.z, h2, l2);
+  split_rn(v.w, h3, l3);
+  *reinterpret_cast<uint2*>(dh) = make_uint2(pack_bf2(h0, h1), pack_bf2(h2, h3));
+  *reinterpret_cast<uint2*>(dl) = make_uint2(pack_bf2(l0, l1), pack_bf2(l2, l3));
+}
+
+__device__ __forceinline__ float bf_at(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+__global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
+  extern __shared__ __align__(16) unsigned char gsm_raw[];
+  __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(gsm_raw);  // [64 j][136] B (exact)
+  __nv_bfloat16* Cs = Bs + kQb * kBP;                              // [64 i][136] C (exact)
+  __nv_bfloat16* Hh = Cs + kQb * kBP;                              // [64 q][136] H_c hi
+  __nv_bfloat16* Hl = Hh + kQb * kBP;                              //               lo
+  __nv_bfloat16* Dh = Hl + kQb * kBP;                              // [64 q][136] dH_{c+1} hi
+  __nv_bfloat16* Dl = Dh + kQb * kBP;                              //               lo
+  __nv_bfloat16* Xs = Dl + kQb * kBP;                              // [64 j][72] x (exact)
+  __nv_bfloat16* Yh = Xs + kQb * kAP;                              // [64 i][72] dy hi
+  __nv_bfloat16* Yl = Yh + kQb * kAP;                              //            lo
+  __nv_bfloat16* Mh = Yl + kQb * kAP;                              // [64 i][72] M hi
+  __nv_bfloat16* Ml = Mh + kQb * kAP;                              //            lo
+  __nv_bfloat16* Gh = Ml + kQb * kAP;                              // [64 i][72] dG hi
+  __nv_bfloat16* Gl = Gh + kQb * kAP;                              //            lo
+  float* cum = reinterpret_cast<float*>(Gl + kQb * kAP);           // [64]
+  float* dts = cum + kQb;                                          // [64] dt
+  float* ec = dts + kQb;                                           // [64] exp(cum_i)
+  float* wt = ec + kQb;                                            // [64] w_j
+  float* el = wt + kQb;                                            // [64] exp(cum_last - cum_j)
+  float* dcum = el + kQb;                                          // [64] dL/dcum
+  float* ddd = dcum + kQb;                                         // [64] direct dt terms
+  float* red = ddd + kQb;                                          // [64] block reductions
+  __shared__ float wsum[2];
+  const int c = blockIdx.x, g = blockIdx.y;
+  const Chunk k = chunk_of(p, c);
+  const int P = p.P, N = p.N, len = k.len;
+  const int hpg = p.H / p.G;
+  const int hb = g * hpg + blockIdx.z * kHS;
+  const int nh = min(kHS, hpg - blockIdx.z * kHS);
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int gq = lane >> 2, tq = lane & 3;
+  const LaneOff lo = lane_off(lane);
+  const int kq = (P + 15) & ~15;  // k extent over headdim
+  const int kn = (N + 15) & ~15;  // k extent over dstate
+  const uint32_t sBs = tc::smem_u32(Bs), sCs = tc::smem_u32(Cs), sHh = tc::smem_u32(Hh),
+                 sHl = tc::smem_u32(Hl), sDh = tc::smem_u32(Dh), sDl = tc::smem_u32(Dl),
+                 sXs = tc::smem_u32(Xs), sYh = tc::smem_u32(Yh), sYl = tc::smem_u32(Yl),
+                 sMh = tc::smem_u32(Mh), sMl = tc::smem_u32(Ml), sGh = tc::smem_u32(Gh),
+                 sGl = tc::smem_u32(Gl);
+  // warp tiles
+  const int r16 = 16 * (w & 3);  // rows of every product
+  const int c32 = 32 * (w >> 2);  // columns of dS / C B^T and of dx
+  const int c64 = 64 * (w >> 2);  // columns of dC / dB
+
+  // ---- B, C rows of the chunk (zero past the valid rows and dstate)
+  {
+    const __nv_bfloat16* Bg = reinterpret_cast<const __nv_bfloat16*>(p.B);
+    const __nv_bfloat16* Cg = reinterpret_cast<const __nv_bfloat16*>(p.C);
+    uint4 vb[4], vc[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e8 = t + kThr * r, j = e8 >> 4, n = (e8 & 15) * 8;
+      const bool ok = j < len && n < N;
+      const long long i = ((k.tok0 + j) * p.G + g) * N + n;
+      vb[r] = ok ? *reinterpret_cast<const uint4*>(Bg + i) : make_uint4(0, 0, 0, 0);
+      vc[r] = ok ? *reinterpret_cast<const uint4*>(Cg + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e8 = t + kThr * r, j = e8 >> 4, n = (e8 & 15) * 8;
+      *reinterpret_cast<uint4*>(Bs + j * kBP + n) = vb[r];
+      *reinterpret_cast<uint4*>(Cs + j * kBP + n) = vc[r];
+    }
+  }
+  __syncthreads();
+  // G = C B^T at the dS tile's positions
+  float gr[4][4];
+  zero_acc(gr);
+  warp_mma<4, kBP, false, false, kBP, false, false>(gr, sCs, 0, r16, sBs, 0, c32, 0, kn, lo);
+
+  float dca[8][4], dba[8][4];  // dC (rows i), dB (rows j): rows r16.., columns c64..
+  zero_acc(dca);
+  zero_acc(dba);
+
+  for (int hh = 0; hh < nh; ++hh) {
+    const int h = hb + hh;
+    const float Ah = p.A[h];
+    const float Dd = p.D ? p.D[h] : 0.f;
+    const long long sOff = ((long long)c * p.H + h) * (long long)(P * N);
+    __syncthreads();  // the previous head's operands and tables are no longer read
+    // ---- this head's x, dy, H_c, dH_{c+1} into registers
+    uint4 vx[2];
+    float4 vy[4], vh[8], vd[8];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e8 = t + kThr * r, j = e8 >> 3, q = (e8 & 7) * 8;
+      vx[r] = (j < len && q < P)
+                  ? *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.x) +
+                                                    ((k.tok0 + j) * p.H + h) * P + q)
+                  : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e4 = t + kThr * r, i = e4 >> 4, q = (e4 & 15) * 4;
+      vy[r] = (i < len && q < P)
+                  ? *reinterpret_cast<const float4*>(p.dy + ((k.tok0 + i) * p.H + h) * P + q)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int e4 = t + kThr * r, q = e4 >> 5, n = (e4 & 31) * 4;
+      const bool ok = q < P && n < N;
+      vh[r] = ok ? __ldcg(reinterpret_cast<const float4*>(p.st + sOff + q * N + n))
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+      vd[r] = ok ? __ldcg(reinterpret_cast<const float4*>(p.ad + sOff + q * N + n))
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // the next head's operands into L2 meanwhile
+    if (hh + 1 < nh) {
+      const long long nOff = sOff + (long long)(P * N);
+      if (t == 0) {
+        tc::bulk_prefetch_l2(p.st + nOff, (uint32_t)(P * N * 4));
+        tc::bulk_prefetch_l2(p.ad + nOff, (uint32_t)(P * N * 4));
+      } else if (t >= 32 && t < 32 + kQb && t - 32 < len) {
+        const long long row = (k.tok0 + (t - 32)) * p.H + h + 1;
+        tc::prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(p.x) + row * P);
+        tc::prefetch_l2(p.dy + row * P);
+        if (P > 32) tc::prefetch_l2(p.dy + row * P + 32);
+      }
+    }
+    chunk_cum<true>(p, k, h, Ah, cum, dts, wsum);
+    const float last = cum[len - 1];
+    if (t < kQb) {
+      ec[t] = expf(cum[t]);
+      el[t] = expf(last - cum[t]);
+      wt[t] = el[t] * dts[t];
+      dcum[t] = 0.f;
+      ddd[t] = 0.f;
+    }
+    float hdot = 0.f;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e8 = t + kThr * r, j = e8 >> 3, q = (e8 & 7) * 8;
+      *reinterpret_cast<uint4*>(Xs + j * kAP + q) = vx[r];
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e4 = t + kThr * r, i = e4 >> 4, q = (e4 & 15) * 4;
+      store_split4(Yh + i * kAP + q, Yl + i * kAP + q, vy[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int e4 = t + kThr * r, q = e4 >> 5, n = (e4 & 31) * 4;
+      store_split4(Hh + q * kBP + n, Hl + q * kBP + n, vh[r]);
+      store_split4(Dh + q * kBP + n, Dl + q * kBP + n, vd[r]);
+      hdot += vh[r].x * vd[r].x + vh[r].y * vd[r].y + vh[r].z * vd[r].z + vh[r].w * vd[r].w;
+    }
+    __syncthreads();
+
+    // ---- dS = dY X^T; M = G L dt, dG = dS L dt; the decay terms of the
+    //      quadratic form (rows r16.., columns c32..)
+    {
+      float sa[4][4];
+      zero_acc(sa);
+      if (c32 <= r16 + 15)
+        warp_mma<4, kAP, false, true, kAP, false, false>(sa, sYh, sYl, r16, sXs, 0, c32, 0, kq, lo);
+      float rowT[2] = {0.f, 0.f}, colT[4][2], colU[4][2];
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt) {
+        colT[tt][0] = colT[tt][1] = colU[tt][0] = colU[tt][1] = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int i = r16 + gq + 8 * hf;
+          float mv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int j = c32 + 8 * tt + 2 * tq + e;
+            mv[e] = dv[e] = 0.f;
+            if (j <= i && i < len) {
+              const float L = expf(cum[i] - cum[j]);
+              const float s = sa[tt][2 * hf + e];
+              const float GL = gr[tt][2 * hf + e] * L;
+              mv[e] = GL * dts[j];
+              dv[e] = s * L * dts[j];
+              const float T = s * mv[e];
+              rowT[hf] += T;
+              colT[tt][e] += T;
+              colU[tt][e] += s * GL;
+            }
+          }
+          __nv_bfloat16 h0, h1, l0, l1;
+          const int at = i * kAP + c32 + 8 * tt + 2 * tq;
+          split_rn(mv[0], h0, l0);
+          split_rn(mv[1], h1, l1);
+          *reinterpret_cast<uint32_t*>(Mh + at) = pack_bf2(h0, h1);
+          *reinterpret_cast<uint32_t*>(Ml + at) = pack_bf2(l0, l1);
+          split_rn(dv[0], h0, l0);
+          split_rn(dv[1], h1, l1);
+          *reinterpret_cast<uint32_t*>(Gh + at) = pack_bf2(h0, h1);
+          *reinterpret_cast<uint32_t*>(Gl + at) = pack_bf2(l0, l1);
+        }
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float v = rowT[hf];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (tq == 0) atomicAdd(&dcum[r16 + gq + 8 * hf], v);
+      }
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float a = colT[tt][e], b = colU[tt][e];
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            b += __shfl_xor_sync(0xffffffffu, b, o);
+          }
+          if (gq == 0) {
+            const int j = c32 + 8 * tt + 2 * tq + e;
+            atomicAdd(&dcum[j], -a);
+            atomicAdd(&ddd[j], b);
+          }
+        }
+    }
+    __syncthreads();
+
+    // ---- dx = M^T dY + w_j dH B_j + D dy (rows j = r16.., columns q = c32..)
+    float wv_sum = 0.f, dd = 0.f;
+    {
+      float xa[4][4], va[4][4];
+      zero_acc(xa);
+      zero_acc(va);
+      if (c32 < P) {
+        warp_mma<4, kAP, true, true, kAP, true, true>(xa, sMh, sMl, r16, sYh, sYl, c32, r16, kQb, lo);
+        warp_mma<4, kBP, false, false, kBP, false, true>(va, sBs, 0, r16, sDh, sDl, c32, 0, kn, lo);
+      }
+      float vp[2] = {0.f, 0.f};
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int j = r16 + gq + 8 * hf;
+        const float wj = wt[j];
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+          const int q = c32 + 8 * tt + 2 * tq;
+          const int at = j * kAP + q;
+          const float y0 = bf_at(Yh + at) + bf_at(Yl + at);
+          const float y1 = bf_at(Yh + at + 1) + bf_at(Yl + at + 1);
+          const float x0 = bf_at(Xs + at), x1 = bf_at(Xs + at + 1);
+          const float v0 = va[tt][2 * hf], v1 = va[tt][2 * hf + 1];
+          vp[hf] += x0 * v0 + x1 * v1;
+          dd += x0 * y0 + x1 * y1;
+          if (j < len && q < P) {
+            float2 o;
+            o.x = xa[tt][2 * hf] + wj * v0 + Dd * y0;
+            o.y = xa[tt][2 * hf + 1] + wj * v1 + Dd * y1;
+            *reinterpret_cast<float2*>(p.dx + ((k.tok0 + j) * p.H + h) * P + q) = o;
+          }
+        }
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float v = vp[hf];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        const int j = r16 + gq + 8 * hf;
+        if (tq == 0 && j < len) {
+          atomicAdd(&dcum[j], -wt[j] * v);
+          atomicAdd(&ddd[j], el[j] * v);
+          wv_sum = fmaf(wt[j], v, wv_sum);
+        }
+      }
+    }
+
+    // ---- dC += dG B + exp(cum_i) dY H (rows i = r16.., columns n = c64..)
+    if (c64 < N) {
+      warp_mma<8, kAP, false, true, kBP, true, false>(dca, sGh, sGl, r16, sBs, 0, c64, 0, r16 + 16, lo);
+      float za[8][4];
+      zero_acc(za);
+      warp_mma<8, kAP, false, true, kBP, true, true>(za, sYh, sYl, r16, sHh, sHl, c64, 0, kq, lo);
+      float zc[2] = {0.f, 0.f};
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int i = r16 + gq + 8 * hf;
+        const float e = ec[i];
+#pragma unroll
+        for (int tt = 0; tt < 8; ++tt) {
+          const int n = c64 + 8 * tt + 2 * tq;
+          const float z0 = e * za[tt][2 * hf], z1 = e * za[tt][2 * hf + 1];
+          dca[tt][2 * hf] += z0;
+          dca[tt][2 * hf + 1] += z1;
+          zc[hf] += z0 * bf_at(Cs + i * kBP + n) + z1 * bf_at(Cs + i * kBP + n + 1);
+        }
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float v = zc[hf];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (tq == 0) atomicAdd(&dcum[r16 + gq + 8 * hf], v);
+      }
+      // ---- dB += dG^T C + w_j X dH (rows j = r16.., columns n = c64..)
+      warp_mma<8, kAP, true, true, kBP, true, false>(dba, sGh, sGl, r16, sCs, 0, c64, r16, kQb, lo);
+      zero_acc(za);
+      warp_mma<8, kAP, false, false, kBP, true, true>(za, sXs, 0, r16, sDh, sDl, c64, 0, kq, lo);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const float wj = wt[r16 + gq + 8 * hf];
+#pragma unroll
+        for (int tt = 0; tt < 8; ++tt) {
+          dba[tt][2 * hf] = fmaf(wj, za[tt][2 * hf], dba[tt][2 * hf]);
+          dba[tt][2 * hf + 1] = fmaf(wj, za[tt][2 * hf + 1], dba[tt][2 * hf + 1]);
+        }
+      }
+    }
+
+    // ---- block sums: <dH, H>, sum_j w_j v_j, dD
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      hdot += __shfl_xor_sync(0xffffffffu, hdot, o);
+      wv_sum += __shfl_xor_sync(0xffffffffu, wv_sum, o);
+      dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    }
+    if (lane == 0) {
+      red[w] = hdot;
+      red[8 + w] = wv_sum;
+      red[16 + w] = dd;
+    }
+    __syncthreads();
+    if (t == 0) {
+      float a = 0.f, b = 0.f, d2 = 0.f;
+      for (int i = 0; i < kThr / 32; ++i) {
+        a += red[i];
+        b += red[8 + i];
+        d2 += red[16 + i];
+      }
+      dcum[len - 1] += expf(last) * a + b;
+      if (p.dD) atomicAdd(p.dD + h, d2);
+    }
+    __syncthreads();
+    // ddt_j = direct terms + A sum_{k>=j} dcum_k; dA += sum_j dt_j sum_{k>=j} dcum_k
+    if (t < 32) {
+      const int j1 = kQb - 1 - 2 * t, j2 = j1 - 1;
+      const float a1 = dcum[j1], a2 = dcum[j2];
+      float v = a1 + a2;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (t >= o) v += u;
+      }
+      const float r2 = v, r1 = v - a2;
+      float da = 0.f;
+      if (j1 < len) {
+        p.ddt[(k.tok0 + j1) * p.H + h] = ddd[j1] + Ah * r1;
+        da = fmaf(dts[j1], r1, da);
+      }
+      if (j2 < len) {
+        p.ddt[(k.tok0 + j2) * p.H + h] = ddd[j2] + Ah * r2;
+        da = fmaf(dts[j2], r2, da);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
+      if (t == 0) atomicAdd(p.dA + h, da);
+    }
+  }
+  // dB, dC of the slice's heads
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const int j = r16 + gq + 8 * hf;
+    if (j < len) {
+      float* db = p.dB + ((k.tok0 + j) * p.G + g) * N;
+      float* dc = p.dC + ((k.tok0 + j) * p.G + g) * N;
+#pragma unroll
+      for (int tt = 0; tt < 8; ++tt) {
+        const int n = c64 + 8 * tt + 2 * tq;
+        if (n < N) {
+          atomicAdd(reinterpret_cast<float2*>(db + n), make_float2(dba[tt][2 * hf], dba[tt][2 * hf + 1]));
+          atomicAdd(reinterpret_cast<float2*>(dc + n), make_float2(dca[tt][2 * hf], dca[tt][2 * hf + 1]));
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
 
 bool bwd_chunked_supported(int P, int N) {
@@ -706,6 +1194,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   std::call_once(attr_once, [] {
     const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
     if (cudaFuncSetAttribute(bwd_grad_kernel<true>, at, (int)kGradSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_grad_mma_kernel, at, (int)kGradMmaSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_grad_kernel<false>, at, (int)kGradSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_outer_kernel<true, 0>, at, (int)kOuterSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_outer_kernel<true, 1>, at, (int)kOuterSmem) != cudaSuccess ||
@@ -725,7 +1214,14 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   bwd_pass_kernel<false><<<pgrid, kThr, 0, a.stream>>>(p);
   const int hpg = a.H / a.G;
   const dim3 ggrid((unsigned)nch, a.G, (unsigned)((hpg + kHS - 1) / kHS));
-  if (bf)
+  // the tensor-core kernel moves x, B, C (bf16) and dy in 16-byte vectors and
+  // writes dx in pairs
+  const auto al = [](const void* q, uintptr_t m) { return (reinterpret_cast<uintptr_t>(q) & m) == 0; };
+  const bool mma = bf && a.P % 8 == 0 && a.N % 8 == 0 && al(a.x, 15) && al(a.B, 15) &&
+                   al(a.C, 15) && al(a.dy, 15) && al(a.dx, 7) && al(a.dB, 7) && al(a.dC, 7);
+  if (mma)
+    bwd_grad_mma_kernel<<<ggrid, kThr, kGradMmaSmem, a.stream>>>(p);
+  else if (bf)
     bwd_grad_kernel<true><<<ggrid, kThr, kGradSmem, a.stream>>>(p);
   else
     bwd_grad_kernel<false><<<ggrid, kThr, kGradSmem, a.stream>>>(p);

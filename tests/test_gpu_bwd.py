@@ -65,6 +65,21 @@ def test_bwd_bf16_tensor_core_shape():
                             chunk=128, dtype="bf16", seed=62), seed=1)
 
 
+def test_bwd_bf16_mma_padded_tiles():
+    """bf16 on the tensor-core gradient kernel with headdim and dstate below
+    the 64 x 128 tiles (P 24, N 40: zero-padded operands), two groups of
+    three heads and a ragged last chunk."""
+    _check(I.small_workload(batch=2, seqlen=100, nheads=6, headdim=24, dstate=40, ngroups=2,
+                            chunk=64, dtype="bf16", seed=64), seed=3)
+
+
+def test_bwd_bf16_cuda_core_path():
+    """bf16 with a headdim that is no multiple of 8 (P 12): the CUDA-core
+    gradient kernel."""
+    _check(I.small_workload(batch=1, seqlen=90, nheads=2, headdim=12, dstate=24, ngroups=1,
+                            chunk=64, dtype="bf16", seed=65), seed=4)
+
+
 def test_bwd_without_optional_inputs():
     _check(I.small_workload(batch=1, seqlen=64, nheads=2, headdim=4, dstate=32, ngroups=1,
                             chunk=64, dtype="f32", init="zero", seed=63),
