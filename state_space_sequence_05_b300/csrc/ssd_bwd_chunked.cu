@@ -73,6 +73,7 @@ struct BP {
   float* ad;   // [chunks][H][P N]: local adjoint sums, then the adjoints leaving each chunk
   float* dec;  // [chunks][H]: exp(cum_last)
   int T, H, P, N, G, nc;  // nc: chunks per batch row
+  int vec;  // rows of x, dy, B, C move as 16-byte vectors (headdim, dstate multiples of 8)
 };
 
 template <bool BF16>
@@ -138,96 +139,314 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t ld32(const __nv_bfloat16* p) {
-  return *reinterpret_cast<const uint32_t*>(p);
+constexpr int kAP = kQb + 8;    // pitch (bf16) of the 64 x 64 tiles
+constexpr int kBP = kNmax + 8;  // pitch (bf16) of the 64 x 128 tiles
+constexpr size_t kT64 = sizeof(__nv_bfloat16) * kQb * kAP;
+constexpr size_t kT128 = sizeof(__nv_bfloat16) * kQb * kBP;
+
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t a) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
 }
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t a) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+
+// Per-lane row/column offsets of the four 8 x 8 matrices of an ldmatrix.x4:
+// pattern X for a left operand stored [m][k] and a right operand stored
+// [k][n]; pattern Y for a left operand stored [k][m] and a right operand
+// stored [n][k].
+struct LaneOff {
+  int rx, cx, ry, cy;
+};
+__device__ __forceinline__ LaneOff lane_off(int lane) {
+  LaneOff o;
+  o.rx = (lane & 7) + ((lane >> 3) & 1) * 8;
+  o.cx = (lane >> 4) * 8;
+  o.ry = (lane & 7) + (lane >> 4) * 8;
+  o.cy = ((lane >> 3) & 1) * 8;
+  return o;
+}
+
+// acc[t] (16 x 8, t < NT) += A (16 x K) B (K x 8 NT) for k in [kb, ke) (steps
+// of 16): A's rows m0.., stored [m][k] (TA false) or [k][m]; B's columns
+// n0.., stored [n][k] (TB false) or [k][n].  ALO / BLO: the operand is a
+// hi/lo pair (lo at al / bl), else exact in bf16; the hi.hi products go to
+// acc, the hi.lo and lo.hi ones to accl (which may be acc).  Per k-step the
+// fragments are loaded first and the MMAs issued pass by pass, so that two
+// MMAs into one accumulator are NT apart.  Shared addresses in bytes.
+template <int NT, int PA, bool TA, bool ALO, int PB, bool TB, bool BLO>
+__device__ __forceinline__ void warp_mma(float (&acc)[NT][4], float (&accl)[NT][4], uint32_t ah_s,
+                                         uint32_t al_s, int m0, uint32_t bh_s, uint32_t bl_s,
+                                         int n0, int kb, int ke, const LaneOff& o) {
+#pragma unroll 1
+  for (int k0 = kb; k0 < ke; k0 += 16) {
+    const uint32_t aoff = TA ? 2u * ((k0 + o.ry) * PA + m0 + o.cy) : 2u * ((m0 + o.rx) * PA + k0 + o.cx);
+    uint32_t ah[4], al[4], bh[NT / 2][4], bl[NT / 2][4];
+    if (TA) {
+      ldsm4t(ah, ah_s + aoff);
+      if (ALO) ldsm4t(al, al_s + aoff);
+    } else {
+      ldsm4(ah, ah_s + aoff);
+      if (ALO) ldsm4(al, al_s + aoff);
+    }
+#pragma unroll
+    for (int u = 0; u < NT / 2; ++u) {
+      const int nb = n0 + 16 * u;
+      const uint32_t boff = TB ? 2u * ((k0 + o.rx) * PB + nb + o.cx) : 2u * ((nb + o.ry) * PB + k0 + o.cy);
+      if (TB) {
+        ldsm4t(bh[u], bh_s + boff);
+        if (BLO) ldsm4t(bl[u], bl_s + boff);
+      } else {
+        ldsm4(bh[u], bh_s + boff);
+        if (BLO) ldsm4(bl[u], bl_s + boff);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < NT / 2; ++u) {
+      mma16816(acc[2 * u], ah, bh[u][0], bh[u][1]);
+      mma16816(acc[2 * u + 1], ah, bh[u][2], bh[u][3]);
+    }
+    if (ALO) {
+#pragma unroll
+      for (int u = 0; u < NT / 2; ++u) {
+        mma16816(accl[2 * u], al, bh[u][0], bh[u][1]);
+        mma16816(accl[2 * u + 1], al, bh[u][2], bh[u][3]);
+      }
+    }
+    if (BLO) {
+#pragma unroll
+      for (int u = 0; u < NT / 2; ++u) {
+        mma16816(accl[2 * u], ah, bl[u][0], bl[u][1]);
+        mma16816(accl[2 * u + 1], ah, bl[u][2], bl[u][3]);
+      }
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+
+// four fp32 values -> hi/lo bf16 quadruples (8 bytes each) at dh / dl
+__device__ __forceinline__ void store_split4(__nv_bfloat16* dh, __nv_bfloat16* dl, float4 v) {
+  __nv_bfloat16 h0, h1, h2, h3, l0, l1, l2, l3;
+  split_rn(v.x, h0, l0);
+  split_rn(v.y, h1, l1);
+  split_rn(v.z, h2, l2);
+  split_rn(v.w, h3, l3);
+  *reinterpret_cast<uint2*>(dh) = make_uint2(pack_bf2(h0, h1), pack_bf2(h2, h3));
+  *reinterpret_cast<uint2*>(dl) = make_uint2(pack_bf2(l0, l1), pack_bf2(l2, l3));
+}
+
+__device__ __forceinline__ float bf_at(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
 // ---------------------------------------------------------------- outer sums
 // MODE 0: out = sum_j w_j x_j B_j^T, w_j = exp(cum_last - cum_j) dt_j, into p.st,
 //         and exp(cum_last) into p.dec.
 // MODE 1: out = sum_i exp(cum_i) dy_i C_i^T into p.ad.
-// A (P x 64 tokens) = the weighted rows transposed, B (64 tokens x N) = B or
-// C, on the tensor cores: warp w takes output rows 16 (w % 4).. and columns
-// 64 (w / 4).. (eight 16 x 8 tiles).
-constexpr int kJP = kQb + 8;  // padded pitch (bf16) of a transposed operand row
-constexpr size_t kOuterSmem = sizeof(__nv_bfloat16) * 2 * (kPmax * kJP + kNmax * kJP);
+// One block per (chunk, group, slice of up to kHS heads of the group): V (64
+// tokens x N) = the group's B or C rows, staged once; per head U (64 tokens x
+// P) = the weighted rows, and out = U^T V on the tensor cores (transposing
+// loads), warp w taking rows 16 (w % 4).. and columns 64 (w / 4)...  With
+// p.vec the rows move as 16-byte vectors: the next head's U rows are copied
+// asynchronously into a staging buffer (and its dt loaded) while the current
+// head's product runs.
+constexpr int kHS = 8;  // heads of a group per block (outer sums and gradients)
+
+constexpr size_t kStage = sizeof(float) * kQb * kPmax;  // raw U rows of one head
+
+template <bool BF16>
+constexpr size_t outer_smem() {
+  return 2 * kT64 + (BF16 ? 1 : 2) * kT128 + kStage + sizeof(float) * kQb;
+}
 
 template <bool BF16, int MODE>
-__global__ void __launch_bounds__(kThr) bwd_outer_kernel(BP p) {
+__global__ void __launch_bounds__(kThr, 3) bwd_outer_kernel(BP p) {
   extern __shared__ __align__(16) unsigned char osm_raw[];
-  __nv_bfloat16* uh = reinterpret_cast<__nv_bfloat16*>(osm_raw);  // [64 p][72]: hi
-  __nv_bfloat16* ul = uh + kPmax * kJP;                            // lo
-  __nv_bfloat16* vh = ul + kPmax * kJP;                            // [128 n][72]: hi
-  __nv_bfloat16* vl = vh + kNmax * kJP;                            // lo (float32 inputs)
-  __shared__ float cum[kQb], dts[kQb], wsum[2];
-  const int c = blockIdx.x, h = blockIdx.y;
+  __nv_bfloat16* Uh = reinterpret_cast<__nv_bfloat16*>(osm_raw);  // [64 j][72]: hi
+  __nv_bfloat16* Ul = Uh + kQb * kAP;                              // lo
+  __nv_bfloat16* Vh = Ul + kQb * kAP;                              // [64 j][136]: hi (bf16: exact)
+  __nv_bfloat16* Vl = Vh + kQb * kBP;                              // lo (fp32 inputs only)
+  unsigned char* stg = reinterpret_cast<unsigned char*>(Vh + (BF16 ? 1 : 2) * kQb * kBP);
+  // stg: the next head's U rows as loaded, [64 j][P] (x: input dtype, dy: fp32)
+  float* sc = reinterpret_cast<float*>(stg + kStage);  // [64] row weights
+  const int c = blockIdx.x, g = blockIdx.y;
+  const int hpg = p.H / p.G;
+  const int hb = g * hpg + blockIdx.z * kHS;
+  const int nh = min(kHS, hpg - blockIdx.z * kHS);
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const Chunk k = chunk_of(p, c);
-  const int g = (int)((long long)h * p.G / p.H);
-  const int P = p.P, N = p.N;
-  chunk_cum<BF16>(p, k, h, p.A[h], cum, dts, wsum);
-  const float last = cum[k.len - 1];
-  for (int e = threadIdx.x; e < kQb * kPmax; e += kThr) {
-    const int j = e / kPmax, q = e % kPmax;
-    float v = 0.f;
-    if (j < k.len && q < P) {
-      const long long i = ((k.tok0 + j) * p.H + h) * P + q;
-      v = MODE == 0 ? expf(last - cum[j]) * dts[j] * ldin<BF16>(p.x, i)
-                    : expf(cum[j]) * p.dy[i];
-    }
-    split_rn(v, uh[q * kJP + j], ul[q * kJP + j]);
-  }
+  const int P = p.P, N = p.N, len = k.len;
+  const void* usrc = MODE == 0 ? p.x : static_cast<const void*>(p.dy);
   const void* vsrc = MODE == 0 ? p.B : p.C;
-  for (int e = threadIdx.x; e < kQb * kNmax; e += kThr) {
-    const int j = e / kNmax, n = e % kNmax;
-    const float v = (j < k.len && n < N) ? ldin<BF16>(vsrc, ((k.tok0 + j) * p.G + g) * N + n) : 0.f;
-    if (BF16) {
-      vh[n * kJP + j] = __float2bfloat16_rn(v);  // exact
+  constexpr int kUS = kQb * kPmax / 4 / kThr;  // 4
+  constexpr int kVS = kQb * kNmax / 4 / kThr;  // 8
+  (void)kUS;
+
+  // U rows of head h into the staging buffer, 16 bytes per copy (zero past
+  // the valid rows); completes at the next cp.async wait
+  constexpr bool kUB = MODE == 0 && BF16;  // U rows in bf16
+  constexpr int kUE = kUB ? 8 : 4;         // elements per 16 bytes
+  constexpr int kUC = kQb * kPmax / kUE / kThr;
+  const auto stage_u = [&](int h) {
+#pragma unroll
+    for (int r = 0; r < kUC; ++r) {
+      const int e = t + kThr * r, j = e / (kPmax / kUE), q = (e % (kPmax / kUE)) * kUE;
+      const bool ok = j < len && q < P;
+      const long long i = ((k.tok0 + (ok ? j : 0)) * p.H + h) * P + (ok ? q : 0);
+      const void* src = kUB ? static_cast<const void*>(static_cast<const __nv_bfloat16*>(usrc) + i)
+                            : static_cast<const void*>(static_cast<const float*>(usrc) + i);
+      tc::cp_async16_zfill(stg + 16 * e, src, ok);
+    }
+    tc::cp_async_commit();
+  };
+  // warp 0: dt of head h (rows 2 lane, 2 lane + 1) and then the row weights
+  float d0 = 0.f, d1 = 0.f;
+  const auto load_dt = [&](int h) {
+    const int j0 = 2 * lane, j1 = j0 + 1;
+    d0 = j0 < len ? ldin<BF16>(p.dt, (k.tok0 + j0) * p.H + h) : 0.f;
+    d1 = j1 < len ? ldin<BF16>(p.dt, (k.tok0 + j1) * p.H + h) : 0.f;
+  };
+  const auto weights = [&](int h) {
+    const float Ah = p.A[h];
+    const float a1 = d1 * Ah;
+    float s = d0 * Ah + a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += u;
+    }
+    const float cm1 = s, cm0 = s - a1;
+    const float lst = __shfl_sync(0xffffffffu, ((len - 1) & 1) ? cm1 : cm0, (len - 1) >> 1);
+    if (MODE == 0) {
+      sc[2 * lane] = expf(lst - cm0) * d0;
+      sc[2 * lane + 1] = expf(lst - cm1) * d1;
+      if (lane == 0) p.dec[(long long)c * p.H + h] = expf(lst);
     } else {
-      split_rn(v, vh[n * kJP + j], vl[n * kJP + j]);
+      sc[2 * lane] = expf(cm0);
+      sc[2 * lane + 1] = expf(cm1);
+    }
+  };
+
+  // ---- V once (zero past the valid rows and dstate)
+  if (p.vec) {
+    uint2 vb[kVS];
+    float4 vf[kVS];
+#pragma unroll
+    for (int r = 0; r < kVS; ++r) {
+      const int e4 = t + kThr * r, j = e4 >> 5, n = (e4 & 31) * 4;
+      const bool ok = j < len && n < N;
+      const long long i = ((k.tok0 + j) * p.G + g) * N + n;
+      if (BF16)
+        vb[r] = ok ? *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(vsrc) + i)
+                   : make_uint2(0, 0);
+      else
+        vf[r] = ok ? *reinterpret_cast<const float4*>(static_cast<const float*>(vsrc) + i)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    stage_u(hb);
+    if (w == 0) load_dt(hb);
+#pragma unroll
+    for (int r = 0; r < kVS; ++r) {
+      const int e4 = t + kThr * r, j = e4 >> 5, n = (e4 & 31) * 4;
+      if (BF16)
+        *reinterpret_cast<uint2*>(Vh + j * kBP + n) = vb[r];
+      else
+        store_split4(Vh + j * kBP + n, Vl + j * kBP + n, vf[r]);
+    }
+  } else {
+    if (w == 0) load_dt(hb);
+    for (int e = t; e < kQb * kNmax; e += kThr) {
+      const int j = e / kNmax, n = e % kNmax;
+      const float v = (j < len && n < N) ? ldin<BF16>(vsrc, ((k.tok0 + j) * p.G + g) * N + n) : 0.f;
+      if (BF16)
+        Vh[j * kBP + n] = __float2bfloat16_rn(v);  // exact
+      else
+        split_rn(v, Vh[j * kBP + n], Vl[j * kBP + n]);
     }
   }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;  // fragment row group and column pair
-  const int r0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);
-  float acc[8][4];
+
+  const int r16 = 16 * (w & 3), c64 = 64 * (w >> 2);
+  const int gq = lane >> 2, tq = lane & 3;
+  const LaneOff lo = lane_off(lane);
+  for (int hh = 0; hh < nh; ++hh) {
+    const int h = hb + hh;
+    if (w == 0) weights(h);
+    if (p.vec) tc::cp_async_wait_all();
+    __syncthreads();  // weights, staged rows (and V) visible; the previous head's product is done
+    if (p.vec) {
 #pragma unroll
-  for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-#pragma unroll
-  for (int k0 = 0; k0 < kQb; k0 += 16) {
-    uint32_t ah[4], al[4];
-    const int ra = (r0 + gq) * kJP + k0 + 2 * tq, rb = ra + 8 * kJP;
-    ah[0] = ld32(uh + ra);
-    ah[1] = ld32(uh + rb);
-    ah[2] = ld32(uh + ra + 8);
-    ah[3] = ld32(uh + rb + 8);
-    al[0] = ld32(ul + ra);
-    al[1] = ld32(ul + rb);
-    al[2] = ld32(ul + ra + 8);
-    al[3] = ld32(ul + rb + 8);
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int nb = (n0 + 8 * t + gq) * kJP + k0 + 2 * tq;
-      const uint32_t b0 = ld32(vh + nb), b1 = ld32(vh + nb + 8);
-      mma16816(acc[t], ah, b0, b1);
-      mma16816(acc[t], al, b0, b1);
-      if (!BF16) mma16816(acc[t], ah, ld32(vl + nb), ld32(vl + nb + 8));
+      for (int r = 0; r < kQb * kPmax / 4 / kThr; ++r) {
+        const int e4 = t + kThr * r, j = e4 >> 4, q = (e4 & 15) * 4;
+        const float m = sc[j];
+        float4 v;
+        if (kUB) {
+          const uint2 b = *reinterpret_cast<const uint2*>(stg + 2 * (j * kPmax + q));
+          v.x = __uint_as_float(b.x << 16);
+          v.y = __uint_as_float(b.x & 0xffff0000u);
+          v.z = __uint_as_float(b.y << 16);
+          v.w = __uint_as_float(b.y & 0xffff0000u);
+        } else {
+          v = *reinterpret_cast<const float4*>(stg + 4 * (j * kPmax + q));
+        }
+        v.x *= m;
+        v.y *= m;
+        v.z *= m;
+        v.w *= m;
+        store_split4(Uh + j * kAP + q, Ul + j * kAP + q, v);
+      }
+    } else {
+      for (int e = t; e < kQb * kPmax; e += kThr) {
+        const int j = e / kPmax, q = e % kPmax;
+        float v = 0.f;
+        if (j < len && q < P) {
+          const long long i = ((k.tok0 + j) * p.H + h) * P + q;
+          v = sc[j] * (MODE == 0 ? ldin<BF16>(p.x, i) : p.dy[i]);
+        }
+        split_rn(v, Uh[j * kAP + q], Ul[j * kAP + q]);
+      }
     }
-  }
-  float* out = (MODE == 0 ? p.st : p.ad) + ((long long)c * p.H + h) * (long long)(P * N);
+    if (w == 0 && hh + 1 < nh) load_dt(h + 1);
+    __syncthreads();  // U ready; the staging buffer is free
+    if (p.vec && hh + 1 < nh) stage_u(h + 1);
+    float* out = (MODE == 0 ? p.st : p.ad) + ((long long)c * p.H + h) * (long long)(P * N);
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {  // 32 columns at a time
+      const int cb = c64 + 32 * half;
+      float acc[4][4];
+      zero_acc(acc);
+      if (r16 < P && cb < N)
+        warp_mma<4, kAP, true, true, kBP, true, !BF16>(acc, acc, tc::smem_u32(Uh), tc::smem_u32(Ul),
+                                                       r16, tc::smem_u32(Vh), tc::smem_u32(Vl), cb,
+                                                       0, (len + 15) & ~15, lo);
 #pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    const int n = n0 + 8 * t + 2 * tq;
+      for (int tt = 0; tt < 4; ++tt) {
+        const int n = cb + 8 * tt + 2 * tq;
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int q = r0 + gq + 8 * hf;
-      if (q < P) {
-        if (n < N) out[q * N + n] = acc[t][2 * hf];
-        if (n + 1 < N) out[q * N + n + 1] = acc[t][2 * hf + 1];
+        for (int hf = 0; hf < 2; ++hf) {
+          const int q = r16 + gq + 8 * hf;
+          if (q < P) {
+            if (p.vec) {
+              if (n < N) *reinterpret_cast<float2*>(out + q * N + n) = make_float2(acc[tt][2 * hf], acc[tt][2 * hf + 1]);
+            } else {
+              if (n < N) out[q * N + n] = acc[tt][2 * hf];
+              if (n + 1 < N) out[q * N + n + 1] = acc[tt][2 * hf + 1];
+            }
+          }
+        }
       }
     }
   }
-  if (MODE == 0 && threadIdx.x == 0) p.dec[(long long)c * p.H + h] = expf(last);
 }
 
 // ---------------------------------------------------------------- passes
@@ -274,7 +493,6 @@ __global__ void __launch_bounds__(kThr) bwd_pass_kernel(BP p) {
 }
 
 // ---------------------------------------------------------------- gradients
-constexpr int kHS = 8;          // heads of a group per gradient block
 constexpr int kPP = kPmax + 1;  // padded row pitches
 constexpr int kNP = kNmax + 1;
 constexpr int kQP = kQb + 1;
@@ -667,107 +885,10 @@ __global__ void __launch_bounds__(kThr) bwd_grad_kernel(BP p) {
 // (with the state terms dy H and x dH): rows 16 (w % 4), columns 64 (w / 4).
 // C B^T stays in registers for the slice's heads, dB and dC likewise.  Blocks
 // of M and dG that the causal mask zeroes are skipped.
-constexpr int kAP = kQb + 8;    // pitch (bf16) of the 64 x 64 tiles
-constexpr int kBP = kNmax + 8;  // pitch (bf16) of the 64 x 128 tiles
-constexpr size_t kT64 = sizeof(__nv_bfloat16) * kQb * kAP;
-constexpr size_t kT128 = sizeof(__nv_bfloat16) * kQb * kBP;
-constexpr size_t kGradMmaSmem = 6 * kT128 + 7 * kT64 + sizeof(float) * (8 * kQb + 32);
+constexpr int kThrG = 512;  // threads of the tensor-core gradient kernel
+constexpr size_t kGradMmaSmem = 6 * kT128 + 7 * kT64 + sizeof(float) * (8 * kQb + 8 * kThrG);
 
-__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t a) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(a));
-}
-__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t a) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(a));
-}
-
-// Per-lane row/column offsets of the four 8 x 8 matrices of an ldmatrix.x4:
-// pattern X for a left operand stored [m][k] and a right operand stored
-// [k][n]; pattern Y for a left operand stored [k][m] and a right operand
-// stored [n][k].
-struct LaneOff {
-  int rx, cx, ry, cy;
-};
-__device__ __forceinline__ LaneOff lane_off(int lane) {
-  LaneOff o;
-  o.rx = (lane & 7) + ((lane >> 3) & 1) * 8;
-  o.cx = (lane >> 4) * 8;
-  o.ry = (lane & 7) + (lane >> 4) * 8;
-  o.cy = ((lane >> 3) & 1) * 8;
-  return o;
-}
-
-// acc[t] (16 x 8, t < NT) += A (16 x K) B (K x 8 NT) for k in [kb, ke) (steps
-// of 16): A's rows m0.., stored [m][k] (TA false) or [k][m]; B's columns
-// n0.., stored [n][k] (TB false) or [k][n].  ALO / BLO: the operand is a
-// hi/lo pair (lo at al / bl), else exact in bf16.  Shared addresses in bytes.
-template <int NT, int PA, bool TA, bool ALO, int PB, bool TB, bool BLO>
-__device__ __forceinline__ void warp_mma(float (&acc)[NT][4], uint32_t ah_s, uint32_t al_s, int m0,
-                                         uint32_t bh_s, uint32_t bl_s, int n0, int kb, int ke,
-                                         const LaneOff& o) {
-  for (int k0 = kb; k0 < ke; k0 += 16) {
-    const uint32_t aoff = TA ? 2u * ((k0 + o.ry) * PA + m0 + o.cy) : 2u * ((m0 + o.rx) * PA + k0 + o.cx);
-    uint32_t ah[4], al[4];
-    if (TA) {
-      ldsm4t(ah, ah_s + aoff);
-      if (ALO) ldsm4t(al, al_s + aoff);
-    } else {
-      ldsm4(ah, ah_s + aoff);
-      if (ALO) ldsm4(al, al_s + aoff);
-    }
-#pragma unroll
-    for (int u = 0; u < NT / 2; ++u) {
-      const int nb = n0 + 16 * u;
-      const uint32_t boff = TB ? 2u * ((k0 + o.rx) * PB + nb + o.cx) : 2u * ((nb + o.ry) * PB + k0 + o.cy);
-      uint32_t bh[4], bl[4];
-      if (TB) {
-        ldsm4t(bh, bh_s + boff);
-        if (BLO) ldsm4t(bl, bl_s + boff);
-      } else {
-        ldsm4(bh, bh_s + boff);
-        if (BLO) ldsm4(bl, bl_s + boff);
-      }
-      mma16816(acc[2 * u], ah, bh[0], bh[1]);
-      mma16816(acc[2 * u + 1], ah, bh[2], bh[3]);
-      if (ALO) {
-        mma16816(acc[2 * u], al, bh[0], bh[1]);
-        mma16816(acc[2 * u + 1], al, bh[2], bh[3]);
-      }
-      if (BLO) {
-        mma16816(acc[2 * u], ah, bl[0], bl[1]);
-        mma16816(acc[2 * u + 1], ah, bl[2], bl[3]);
-      }
-    }
-  }
-}
-
-template <int NT>
-__device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
-#pragma unroll
-  for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-}
-
-__device__ __forceinline__ uint32_t pack_bf2(__nv_bfloat16 a, __nv_bfloat16 b) {
-  return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
-}
-
-// four fp32 values -> hi/lo bf16 quadruples (8 bytes each) at dh / dl
-__device__ __forceinline__ void store_split4(__nv_bfloat16* dh, __nv_bfloat16* dl, float4 v) {
-  __nv_bfloat16 h0, h1, h2, h3, l0, l1, l2, l3;
-  split_rn(v.x, h0, l0);
-  split_rn(v.y, h1, l1);
-  split_rn(v.z, h2, l2);
-  split_rn(v.w, h3, l3);
-  *reinterpret_cast<uint2*>(dh) = make_uint2(pack_bf2(h0, h1), pack_bf2(h2, h3));
-  *reinterpret_cast<uint2*>(dl) = make_uint2(pack_bf2(l0, l1), pack_bf2(l2, l3));
-}
-
-__device__ __forceinline__ float bf_at(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-
-__global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
+__global__ void __launch_bounds__(kThrG, 1) bwd_grad_mma_kernel(BP p) {
   extern __shared__ __align__(16) unsigned char gsm_raw[];
   __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(gsm_raw);  // [64 j][136] B (exact)
   __nv_bfloat16* Cs = Bs + kQb * kBP;                              // [64 i][136] C (exact)
@@ -789,8 +910,8 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
   float* el = wt + kQb;                                            // [64] exp(cum_last - cum_j)
   float* dcum = el + kQb;                                          // [64] dL/dcum
   float* ddd = dcum + kQb;                                         // [64] direct dt terms
-  float* red = ddd + kQb;                                          // [64] block reductions
-  __shared__ float wsum[2];
+  float* red = ddd + kQb;                                          // [48] block reductions
+  float* grs = red + kQb;  // [8][512] C B^T at each thread's dS fragment positions
   const int c = blockIdx.x, g = blockIdx.y;
   const Chunk k = chunk_of(p, c);
   const int P = p.P, N = p.N, len = k.len;
@@ -802,131 +923,164 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
   const LaneOff lo = lane_off(lane);
   const int kq = (P + 15) & ~15;  // k extent over headdim
   const int kn = (N + 15) & ~15;  // k extent over dstate
-  const uint32_t sBs = tc::smem_u32(Bs), sCs = tc::smem_u32(Cs), sHh = tc::smem_u32(Hh),
-                 sHl = tc::smem_u32(Hl), sDh = tc::smem_u32(Dh), sDl = tc::smem_u32(Dl),
-                 sXs = tc::smem_u32(Xs), sYh = tc::smem_u32(Yh), sYl = tc::smem_u32(Yl),
-                 sMh = tc::smem_u32(Mh), sMl = tc::smem_u32(Ml), sGh = tc::smem_u32(Gh),
-                 sGl = tc::smem_u32(Gl);
-  // warp tiles
-  const int r16 = 16 * (w & 3);  // rows of every product
-  const int c32 = 32 * (w >> 2);  // columns of dS / C B^T and of dx
-  const int c64 = 64 * (w >> 2);  // columns of dC / dB
+  // shared addresses of the operand tiles: one base plus constant offsets
+  const uint32_t sb = tc::smem_u32(gsm_raw);
+  const uint32_t sBs = sb, sCs = sb + kT128, sHh = sb + 2 * kT128, sHl = sb + 3 * kT128,
+                 sDh = sb + 4 * kT128, sDl = sb + 5 * kT128, sXs = sb + 6 * kT128,
+                 sYh = sXs + kT64, sYl = sXs + 2 * kT64, sMh = sXs + 3 * kT64,
+                 sMl = sXs + 4 * kT64, sGh = sXs + 5 * kT64, sGl = sXs + 6 * kT64;
+  // warp tiles: row block rb (every SM sub-partition holds all four), column block cb
+  const int rb = w >> 2, cb = w & 3;
+  const int r16 = 16 * rb;
+  const int c16 = 16 * cb;  // columns of dS / C B^T and of dx
+  const int c32 = 32 * cb;  // columns of dC / dB
+  const __nv_bfloat16* xg = reinterpret_cast<const __nv_bfloat16*>(p.x);
 
-  // ---- B, C rows of the chunk (zero past the valid rows and dstate)
-  {
-    const __nv_bfloat16* Bg = reinterpret_cast<const __nv_bfloat16*>(p.B);
-    const __nv_bfloat16* Cg = reinterpret_cast<const __nv_bfloat16*>(p.C);
-    uint4 vb[4], vc[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e8 = t + kThr * r, j = e8 >> 4, n = (e8 & 15) * 8;
-      const bool ok = j < len && n < N;
-      const long long i = ((k.tok0 + j) * p.G + g) * N + n;
-      vb[r] = ok ? *reinterpret_cast<const uint4*>(Bg + i) : make_uint4(0, 0, 0, 0);
-      vc[r] = ok ? *reinterpret_cast<const uint4*>(Cg + i) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e8 = t + kThr * r, j = e8 >> 4, n = (e8 & 15) * 8;
-      *reinterpret_cast<uint4*>(Bs + j * kBP + n) = vb[r];
-      *reinterpret_cast<uint4*>(Cs + j * kBP + n) = vc[r];
-    }
-  }
-  __syncthreads();
-  // G = C B^T at the dS tile's positions
-  float gr[4][4];
-  zero_acc(gr);
-  warp_mma<4, kBP, false, false, kBP, false, false>(gr, sCs, 0, r16, sBs, 0, c32, 0, kn, lo);
-
-  float dca[8][4], dba[8][4];  // dC (rows i), dB (rows j): rows r16.., columns c64..
-  zero_acc(dca);
-  zero_acc(dba);
-
-  for (int hh = 0; hh < nh; ++hh) {
-    const int h = hb + hh;
-    const float Ah = p.A[h];
-    const float Dd = p.D ? p.D[h] : 0.f;
+  // One head's x, dy, H_c, dH_{c+1} in registers (zero outside the valid
+  // rows, headdim and dstate), loaded a head ahead of their use.
+  uint4 vx;
+  float4 vy[2], vh[4], vd[4];
+  const auto load_head = [&](int h) {
     const long long sOff = ((long long)c * p.H + h) * (long long)(P * N);
-    __syncthreads();  // the previous head's operands and tables are no longer read
-    // ---- this head's x, dy, H_c, dH_{c+1} into registers
-    uint4 vx[2];
-    float4 vy[4], vh[8], vd[8];
+    {
+      const int j = t >> 3, q = (t & 7) * 8;
+      vx = (j < len && q < P) ? *reinterpret_cast<const uint4*>(xg + ((k.tok0 + j) * p.H + h) * P + q)
+                              : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const int e8 = t + kThr * r, j = e8 >> 3, q = (e8 & 7) * 8;
-      vx[r] = (j < len && q < P)
-                  ? *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.x) +
-                                                    ((k.tok0 + j) * p.H + h) * P + q)
-                  : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e4 = t + kThr * r, i = e4 >> 4, q = (e4 & 15) * 4;
+      const int e4 = t + kThrG * r, i = e4 >> 4, q = (e4 & 15) * 4;
       vy[r] = (i < len && q < P)
                   ? *reinterpret_cast<const float4*>(p.dy + ((k.tok0 + i) * p.H + h) * P + q)
                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int e4 = t + kThr * r, q = e4 >> 5, n = (e4 & 31) * 4;
+    for (int r = 0; r < 4; ++r) {
+      const int e4 = t + kThrG * r, q = e4 >> 5, n = (e4 & 31) * 4;
       const bool ok = q < P && n < N;
       vh[r] = ok ? __ldcg(reinterpret_cast<const float4*>(p.st + sOff + q * N + n))
                  : make_float4(0.f, 0.f, 0.f, 0.f);
       vd[r] = ok ? __ldcg(reinterpret_cast<const float4*>(p.ad + sOff + q * N + n))
                  : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    // the next head's operands into L2 meanwhile
-    if (hh + 1 < nh) {
-      const long long nOff = sOff + (long long)(P * N);
-      if (t == 0) {
-        tc::bulk_prefetch_l2(p.st + nOff, (uint32_t)(P * N * 4));
-        tc::bulk_prefetch_l2(p.ad + nOff, (uint32_t)(P * N * 4));
-      } else if (t >= 32 && t < 32 + kQb && t - 32 < len) {
-        const long long row = (k.tok0 + (t - 32)) * p.H + h + 1;
-        tc::prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(p.x) + row * P);
-        tc::prefetch_l2(p.dy + row * P);
-        if (P > 32) tc::prefetch_l2(p.dy + row * P + 32);
-      }
+  };
+  // The operands of head h into L2 (a head before their register loads).
+  const auto prefetch_head = [&](int h) {
+    const long long sOff = ((long long)c * p.H + h) * (long long)(P * N);
+    if (t == 0) {
+      tc::bulk_prefetch_l2(p.st + sOff, (uint32_t)(P * N * 4));
+      tc::bulk_prefetch_l2(p.ad + sOff, (uint32_t)(P * N * 4));
+    } else if (t >= 32 && t < 32 + kQb && t - 32 < len) {
+      const long long row = (k.tok0 + (t - 32)) * p.H + h;
+      tc::prefetch_l2(xg + row * P);
+      tc::prefetch_l2(p.dy + row * P);
+      if (P > 32) tc::prefetch_l2(p.dy + row * P + 32);
     }
-    chunk_cum<true>(p, k, h, Ah, cum, dts, wsum);
-    const float last = cum[len - 1];
-    if (t < kQb) {
-      ec[t] = expf(cum[t]);
-      el[t] = expf(last - cum[t]);
-      wt[t] = el[t] * dts[t];
-      dcum[t] = 0.f;
-      ddd[t] = 0.f;
+  };
+  // Warp 0: the decay tables of head h (lane l holds entries 2l and 2l+1),
+  // dcum and ddd cleared.
+  const auto tables = [&](int h) {
+    const float Ah = p.A[h];
+    const int j0 = 2 * lane, j1 = j0 + 1;
+    const float d0 = j0 < len ? ldin<true>(p.dt, (k.tok0 + j0) * p.H + h) : 0.f;
+    const float d1 = j1 < len ? ldin<true>(p.dt, (k.tok0 + j1) * p.H + h) : 0.f;
+    const float a1 = d1 * Ah;
+    float s = d0 * Ah + a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += u;
     }
-    float hdot = 0.f;
+    const float cm1 = s, cm0 = s - a1;
+    const float lst = __shfl_sync(0xffffffffu, ((len - 1) & 1) ? cm1 : cm0, (len - 1) >> 1);
+    cum[j0] = cm0;
+    cum[j1] = cm1;
+    dts[j0] = d0;
+    dts[j1] = d1;
+    ec[j0] = expf(cm0);
+    ec[j1] = expf(cm1);
+    const float e0 = expf(lst - cm0), e1 = expf(lst - cm1);
+    el[j0] = e0;
+    el[j1] = e1;
+    wt[j0] = e0 * d0;
+    wt[j1] = e1 * d1;
+    dcum[j0] = dcum[j1] = 0.f;
+    ddd[j0] = ddd[j1] = 0.f;
+  };
+
+  // ---- prologue: B, C rows of the chunk; the first head's operands and tables
+  {
+    const __nv_bfloat16* Bg = reinterpret_cast<const __nv_bfloat16*>(p.B);
+    const __nv_bfloat16* Cg = reinterpret_cast<const __nv_bfloat16*>(p.C);
+    uint4 vb[2], vc[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const int e8 = t + kThr * r, j = e8 >> 3, q = (e8 & 7) * 8;
-      *reinterpret_cast<uint4*>(Xs + j * kAP + q) = vx[r];
+      const int e8 = t + kThrG * r, j = e8 >> 4, n = (e8 & 15) * 8;
+      const bool ok = j < len && n < N;
+      const long long i = ((k.tok0 + j) * p.G + g) * N + n;
+      vb[r] = ok ? *reinterpret_cast<const uint4*>(Bg + i) : make_uint4(0, 0, 0, 0);
+      vc[r] = ok ? *reinterpret_cast<const uint4*>(Cg + i) : make_uint4(0, 0, 0, 0);
+    }
+    load_head(hb);
+    if (nh > 1) prefetch_head(hb + 1);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e8 = t + kThrG * r, j = e8 >> 4, n = (e8 & 15) * 8;
+      *reinterpret_cast<uint4*>(Bs + j * kBP + n) = vb[r];
+      *reinterpret_cast<uint4*>(Cs + j * kBP + n) = vc[r];
+    }
+    if (w == 0) tables(hb);
+  }
+  __syncthreads();
+  // G = C B^T at the dS tile's positions (rows r16.., columns c16..)
+  {
+    float gr[2][4];
+    zero_acc(gr);
+    warp_mma<2, kBP, false, false, kBP, false, false>(gr, gr, sCs, 0, r16, sBs, 0, c16, 0, kn, lo);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) grs[e * kThrG + t] = gr[e >> 2][e & 3];
+  }
+
+  float dca[4][4], dba[4][4];  // dC (rows i), dB (rows j): rows r16.., columns c32..
+  zero_acc(dca);
+  zero_acc(dba);
+
+  for (int hh = 0; hh < nh; ++hh) {
+    const int h = hb + hh;
+    const float Dd = p.D ? p.D[h] : 0.f;
+    // ---- operands to shared memory (the previous head's readers passed the
+    //      last barrier)
+    float hdot = 0.f;
+    {
+      const int j = t >> 3, q = (t & 7) * 8;
+      *reinterpret_cast<uint4*>(Xs + j * kAP + q) = vx;
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e4 = t + kThr * r, i = e4 >> 4, q = (e4 & 15) * 4;
+    for (int r = 0; r < 2; ++r) {
+      const int e4 = t + kThrG * r, i = e4 >> 4, q = (e4 & 15) * 4;
       store_split4(Yh + i * kAP + q, Yl + i * kAP + q, vy[r]);
     }
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int e4 = t + kThr * r, q = e4 >> 5, n = (e4 & 31) * 4;
+    for (int r = 0; r < 4; ++r) {
+      const int e4 = t + kThrG * r, q = e4 >> 5, n = (e4 & 31) * 4;
       store_split4(Hh + q * kBP + n, Hl + q * kBP + n, vh[r]);
       store_split4(Dh + q * kBP + n, Dl + q * kBP + n, vd[r]);
       hdot += vh[r].x * vd[r].x + vh[r].y * vd[r].y + vh[r].z * vd[r].z + vh[r].w * vd[r].w;
     }
     __syncthreads();
+    const float last = cum[len - 1];
 
     // ---- dS = dY X^T; M = G L dt, dG = dS L dt; the decay terms of the
-    //      quadratic form (rows r16.., columns c32..)
+    //      quadratic form (rows r16.., columns c16..)
     {
-      float sa[4][4];
+      float sa[2][4], sl[2][4];
       zero_acc(sa);
-      if (c32 <= r16 + 15)
-        warp_mma<4, kAP, false, true, kAP, false, false>(sa, sYh, sYl, r16, sXs, 0, c32, 0, kq, lo);
-      float rowT[2] = {0.f, 0.f}, colT[4][2], colU[4][2];
+      zero_acc(sl);
+      if (cb <= rb)
+        warp_mma<2, kAP, false, true, kAP, false, false>(sa, sl, sYh, sYl, r16, sXs, 0, c16, 0, kq, lo);
+      float rowT[2] = {0.f, 0.f}, colT[2][2], colU[2][2];
 #pragma unroll
-      for (int tt = 0; tt < 4; ++tt) {
+      for (int tt = 0; tt < 2; ++tt) {
         colT[tt][0] = colT[tt][1] = colU[tt][0] = colU[tt][1] = 0.f;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -934,22 +1088,22 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
           float mv[2], dv[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int j = c32 + 8 * tt + 2 * tq + e;
+            const int j = c16 + 8 * tt + 2 * tq + e;
             mv[e] = dv[e] = 0.f;
             if (j <= i && i < len) {
               const float L = expf(cum[i] - cum[j]);
-              const float s = sa[tt][2 * hf + e];
-              const float GL = gr[tt][2 * hf + e] * L;
+              const float sv = sa[tt][2 * hf + e] + sl[tt][2 * hf + e];
+              const float GL = grs[(4 * tt + 2 * hf + e) * kThrG + t] * L;
               mv[e] = GL * dts[j];
-              dv[e] = s * L * dts[j];
-              const float T = s * mv[e];
+              dv[e] = sv * L * dts[j];
+              const float T = sv * mv[e];
               rowT[hf] += T;
               colT[tt][e] += T;
-              colU[tt][e] += s * GL;
+              colU[tt][e] += sv * GL;
             }
           }
           __nv_bfloat16 h0, h1, l0, l1;
-          const int at = i * kAP + c32 + 8 * tt + 2 * tq;
+          const int at = i * kAP + c16 + 8 * tt + 2 * tq;
           split_rn(mv[0], h0, l0);
           split_rn(mv[1], h1, l1);
           *reinterpret_cast<uint32_t*>(Mh + at) = pack_bf2(h0, h1);
@@ -960,41 +1114,43 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
           *reinterpret_cast<uint32_t*>(Gl + at) = pack_bf2(l0, l1);
         }
       }
+      if (cb <= rb) {
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float v = rowT[hf];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        if (tq == 0) atomicAdd(&dcum[r16 + gq + 8 * hf], v);
-      }
-#pragma unroll
-      for (int tt = 0; tt < 4; ++tt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float a = colT[tt][e], b = colU[tt][e];
-#pragma unroll
-          for (int o = 4; o < 32; o <<= 1) {
-            a += __shfl_xor_sync(0xffffffffu, a, o);
-            b += __shfl_xor_sync(0xffffffffu, b, o);
-          }
-          if (gq == 0) {
-            const int j = c32 + 8 * tt + 2 * tq + e;
-            atomicAdd(&dcum[j], -a);
-            atomicAdd(&ddd[j], b);
-          }
+        for (int hf = 0; hf < 2; ++hf) {
+          float v = rowT[hf];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          if (tq == 0) atomicAdd(&dcum[r16 + gq + 8 * hf], v);
         }
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float a = colT[tt][e], b = colU[tt][e];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+              a += __shfl_xor_sync(0xffffffffu, a, o);
+              b += __shfl_xor_sync(0xffffffffu, b, o);
+            }
+            if (gq == 0) {
+              const int j = c16 + 8 * tt + 2 * tq + e;
+              atomicAdd(&dcum[j], -a);
+              atomicAdd(&ddd[j], b);
+            }
+          }
+      }
     }
     __syncthreads();
 
-    // ---- dx = M^T dY + w_j dH B_j + D dy (rows j = r16.., columns q = c32..)
+    // ---- dx = M^T dY + w_j dH B_j + D dy (rows j = r16.., columns q = c16..)
     float wv_sum = 0.f, dd = 0.f;
     {
-      float xa[4][4], va[4][4];
+      float xa[2][4], va[2][4];
       zero_acc(xa);
       zero_acc(va);
-      if (c32 < P) {
-        warp_mma<4, kAP, true, true, kAP, true, true>(xa, sMh, sMl, r16, sYh, sYl, c32, r16, kQb, lo);
-        warp_mma<4, kBP, false, false, kBP, false, true>(va, sBs, 0, r16, sDh, sDl, c32, 0, kn, lo);
+      if (c16 < P) {
+        warp_mma<2, kAP, true, true, kAP, true, true>(xa, xa, sMh, sMl, r16, sYh, sYl, c16, r16, kQb, lo);
+        warp_mma<2, kBP, false, false, kBP, false, true>(va, va, sBs, 0, r16, sDh, sDl, c16, 0, kn, lo);
       }
       float vp[2] = {0.f, 0.f};
 #pragma unroll
@@ -1002,8 +1158,8 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
         const int j = r16 + gq + 8 * hf;
         const float wj = wt[j];
 #pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-          const int q = c32 + 8 * tt + 2 * tq;
+        for (int tt = 0; tt < 2; ++tt) {
+          const int q = c16 + 8 * tt + 2 * tq;
           const int at = j * kAP + q;
           const float y0 = bf_at(Yh + at) + bf_at(Yl + at);
           const float y1 = bf_at(Yh + at + 1) + bf_at(Yl + at + 1);
@@ -1033,21 +1189,22 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
       }
     }
 
-    // ---- dC += dG B + exp(cum_i) dY H (rows i = r16.., columns n = c64..)
-    if (c64 < N) {
-      warp_mma<8, kAP, false, true, kBP, true, false>(dca, sGh, sGl, r16, sBs, 0, c64, 0, r16 + 16, lo);
-      float za[8][4];
-      zero_acc(za);
-      warp_mma<8, kAP, false, true, kBP, true, true>(za, sYh, sYl, r16, sHh, sHl, c64, 0, kq, lo);
+    // ---- dC += dG B + exp(cum_i) dY H; dB += dG^T C + w_j X dH
+    //      (rows r16.., columns n = c32..)
+    if (c32 < N) {
+      warp_mma<4, kAP, false, true, kBP, true, false>(dca, dca, sGh, sGl, r16, sBs, 0, c32, 0, r16 + 16, lo);
+      float ta[4][4];
+      zero_acc(ta);
+      warp_mma<4, kAP, false, true, kBP, true, true>(ta, ta, sYh, sYl, r16, sHh, sHl, c32, 0, kq, lo);
       float zc[2] = {0.f, 0.f};
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int i = r16 + gq + 8 * hf;
         const float e = ec[i];
 #pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-          const int n = c64 + 8 * tt + 2 * tq;
-          const float z0 = e * za[tt][2 * hf], z1 = e * za[tt][2 * hf + 1];
+        for (int tt = 0; tt < 4; ++tt) {
+          const int n = c32 + 8 * tt + 2 * tq;
+          const float z0 = e * ta[tt][2 * hf], z1 = e * ta[tt][2 * hf + 1];
           dca[tt][2 * hf] += z0;
           dca[tt][2 * hf + 1] += z1;
           zc[hf] += z0 * bf_at(Cs + i * kBP + n) + z1 * bf_at(Cs + i * kBP + n + 1);
@@ -1060,22 +1217,25 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
         v += __shfl_xor_sync(0xffffffffu, v, 2);
         if (tq == 0) atomicAdd(&dcum[r16 + gq + 8 * hf], v);
       }
-      // ---- dB += dG^T C + w_j X dH (rows j = r16.., columns n = c64..)
-      warp_mma<8, kAP, true, true, kBP, true, false>(dba, sGh, sGl, r16, sCs, 0, c64, r16, kQb, lo);
-      zero_acc(za);
-      warp_mma<8, kAP, false, false, kBP, true, true>(za, sXs, 0, r16, sDh, sDl, c64, 0, kq, lo);
+      warp_mma<4, kAP, true, true, kBP, true, false>(dba, dba, sGh, sGl, r16, sCs, 0, c32, r16, kQb, lo);
+      zero_acc(ta);
+      warp_mma<4, kAP, false, false, kBP, true, true>(ta, ta, sXs, 0, r16, sDh, sDl, c32, 0, kq, lo);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const float wj = wt[r16 + gq + 8 * hf];
 #pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-          dba[tt][2 * hf] = fmaf(wj, za[tt][2 * hf], dba[tt][2 * hf]);
-          dba[tt][2 * hf + 1] = fmaf(wj, za[tt][2 * hf + 1], dba[tt][2 * hf + 1]);
+        for (int tt = 0; tt < 4; ++tt) {
+          dba[tt][2 * hf] = fmaf(wj, ta[tt][2 * hf], dba[tt][2 * hf]);
+          dba[tt][2 * hf + 1] = fmaf(wj, ta[tt][2 * hf + 1], dba[tt][2 * hf + 1]);
         }
       }
     }
 
-    // ---- block sums: <dH, H>, sum_j w_j v_j, dD
+    // ---- the next head's operands into registers; block sums
+    if (hh + 1 < nh) {
+      load_head(h + 1);
+      if (hh + 2 < nh) prefetch_head(h + 2);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       hdot += __shfl_xor_sync(0xffffffffu, hdot, o);
@@ -1084,32 +1244,37 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
     }
     if (lane == 0) {
       red[w] = hdot;
-      red[8 + w] = wv_sum;
-      red[16 + w] = dd;
+      red[16 + w] = wv_sum;
+      red[32 + w] = dd;
     }
     __syncthreads();
-    if (t == 0) {
-      float a = 0.f, b = 0.f, d2 = 0.f;
-      for (int i = 0; i < kThr / 32; ++i) {
-        a += red[i];
-        b += red[8 + i];
-        d2 += red[16 + i];
+    // ---- warp 0: <dH, H>, sum_j w_j v_j, dD; ddt_j = direct terms + A
+    //      sum_{k>=j} dcum_k; dA += sum_j dt_j sum_{k>=j} dcum_k; then the
+    //      next head's tables
+    if (w == 0) {
+      float a = lane < 16 ? red[lane] : 0.f, b = lane < 16 ? red[16 + lane] : 0.f,
+            d2 = lane < 16 ? red[32 + lane] : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {  // every lane gets the sums
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+        d2 += __shfl_xor_sync(0xffffffffu, d2, o);
       }
-      dcum[len - 1] += expf(last) * a + b;
-      if (p.dD) atomicAdd(p.dD + h, d2);
-    }
-    __syncthreads();
-    // ddt_j = direct terms + A sum_{k>=j} dcum_k; dA += sum_j dt_j sum_{k>=j} dcum_k
-    if (t < 32) {
-      const int j1 = kQb - 1 - 2 * t, j2 = j1 - 1;
-      const float a1 = dcum[j1], a2 = dcum[j2];
+      // reverse inclusive scan, lane l owning entries 63 - 2l and 62 - 2l;
+      // the state terms of the last valid row join it there
+      const int j1 = kQb - 1 - 2 * lane, j2 = j1 - 1;
+      const float extra = expf(last) * a + b;
+      const float a1 = dcum[j1] + (j1 == len - 1 ? extra : 0.f);
+      const float a2 = dcum[j2] + (j2 == len - 1 ? extra : 0.f);
+      if (lane == 0 && p.dD) atomicAdd(p.dD + h, d2);
       float v = a1 + a2;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float u = __shfl_up_sync(0xffffffffu, v, o);
-        if (t >= o) v += u;
+        if (lane >= o) v += u;
       }
       const float r2 = v, r1 = v - a2;
+      const float Ah = p.A[h];
       float da = 0.f;
       if (j1 < len) {
         p.ddt[(k.tok0 + j1) * p.H + h] = ddd[j1] + Ah * r1;
@@ -1121,7 +1286,9 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
-      if (t == 0) atomicAdd(p.dA + h, da);
+      if (lane == 0) atomicAdd(p.dA + h, da);
+      __syncwarp();
+      if (hh + 1 < nh) tables(h + 1);
     }
   }
   // dB, dC of the slice's heads
@@ -1132,8 +1299,8 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_mma_kernel(BP p) {
       float* db = p.dB + ((k.tok0 + j) * p.G + g) * N;
       float* dc = p.dC + ((k.tok0 + j) * p.G + g) * N;
 #pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-        const int n = c64 + 8 * tt + 2 * tq;
+      for (int tt = 0; tt < 4; ++tt) {
+        const int n = c32 + 8 * tt + 2 * tq;
         if (n < N) {
           atomicAdd(reinterpret_cast<float2*>(db + n), make_float2(dba[tt][2 * hf], dba[tt][2 * hf + 1]));
           atomicAdd(reinterpret_cast<float2*>(dc + n), make_float2(dca[tt][2 * hf], dca[tt][2 * hf + 1]));
@@ -1180,14 +1347,15 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   p.N = a.N;
   p.G = a.G;
   p.nc = (a.seqlen + kQb - 1) / kQb;
+  const bool bf = a.dtype == SSD_DT_BF16;
+  const auto al = [](const void* q, uintptr_t m) { return (reinterpret_cast<uintptr_t>(q) & m) == 0; };
+  p.vec = a.P % 8 == 0 && a.N % 8 == 0 && al(a.x, 15) && al(a.B, 15) && al(a.C, 15) && al(a.dy, 15);
   const long long nch = (long long)a.batch * p.nc;
   char* ws = static_cast<char*>(a.ws);
   const size_t sbytes = align256(sizeof(float) * (size_t)nch * a.H * a.P * a.N);
   p.st = reinterpret_cast<float*>(ws);
   p.ad = reinterpret_cast<float*>(ws + sbytes);
   p.dec = reinterpret_cast<float*>(ws + 2 * sbytes);
-  const bool bf = a.dtype == SSD_DT_BF16;
-  const dim3 cgrid((unsigned)nch, a.H);
   const dim3 pgrid((unsigned)((a.P * a.N / 4 + kThr - 1) / kThr), a.H, a.batch);
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1196,31 +1364,30 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
     if (cudaFuncSetAttribute(bwd_grad_kernel<true>, at, (int)kGradSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_grad_mma_kernel, at, (int)kGradMmaSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_grad_kernel<false>, at, (int)kGradSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(bwd_outer_kernel<true, 0>, at, (int)kOuterSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(bwd_outer_kernel<true, 1>, at, (int)kOuterSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(bwd_outer_kernel<false, 0>, at, (int)kOuterSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(bwd_outer_kernel<false, 1>, at, (int)kOuterSmem) != cudaSuccess)
+        cudaFuncSetAttribute(bwd_outer_kernel<true, 0>, at, (int)outer_smem<true>()) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_outer_kernel<true, 1>, at, (int)outer_smem<true>()) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_outer_kernel<false, 0>, at, (int)outer_smem<false>()) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_outer_kernel<false, 1>, at, (int)outer_smem<false>()) != cudaSuccess)
       attr_err = cudaGetLastError();
   });
   if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
+  const int hpg = a.H / a.G;
+  const dim3 ggrid((unsigned)nch, a.G, (unsigned)((hpg + kHS - 1) / kHS));
   if (bf) {
-    bwd_outer_kernel<true, 0><<<cgrid, kThr, kOuterSmem, a.stream>>>(p);
-    bwd_outer_kernel<true, 1><<<cgrid, kThr, kOuterSmem, a.stream>>>(p);
+    bwd_outer_kernel<true, 0><<<ggrid, kThr, outer_smem<true>(), a.stream>>>(p);
+    bwd_outer_kernel<true, 1><<<ggrid, kThr, outer_smem<true>(), a.stream>>>(p);
   } else {
-    bwd_outer_kernel<false, 0><<<cgrid, kThr, kOuterSmem, a.stream>>>(p);
-    bwd_outer_kernel<false, 1><<<cgrid, kThr, kOuterSmem, a.stream>>>(p);
+    bwd_outer_kernel<false, 0><<<ggrid, kThr, outer_smem<false>(), a.stream>>>(p);
+    bwd_outer_kernel<false, 1><<<ggrid, kThr, outer_smem<false>(), a.stream>>>(p);
   }
   bwd_pass_kernel<true><<<pgrid, kThr, 0, a.stream>>>(p);
   bwd_pass_kernel<false><<<pgrid, kThr, 0, a.stream>>>(p);
-  const int hpg = a.H / a.G;
-  const dim3 ggrid((unsigned)nch, a.G, (unsigned)((hpg + kHS - 1) / kHS));
   // the tensor-core kernel moves x, B, C (bf16) and dy in 16-byte vectors and
   // writes dx in pairs
-  const auto al = [](const void* q, uintptr_t m) { return (reinterpret_cast<uintptr_t>(q) & m) == 0; };
   const bool mma = bf && a.P % 8 == 0 && a.N % 8 == 0 && al(a.x, 15) && al(a.B, 15) &&
                    al(a.C, 15) && al(a.dy, 15) && al(a.dx, 7) && al(a.dB, 7) && al(a.dC, 7);
   if (mma)
-    bwd_grad_mma_kernel<<<ggrid, kThr, kGradMmaSmem, a.stream>>>(p);
+    bwd_grad_mma_kernel<<<ggrid, kThrG, kGradMmaSmem, a.stream>>>(p);
   else if (bf)
     bwd_grad_kernel<true><<<ggrid, kThr, kGradSmem, a.stream>>>(p);
   else
