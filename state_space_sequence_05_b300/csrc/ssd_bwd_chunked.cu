@@ -69,6 +69,7 @@ struct BP {
   const void *x, *dt, *B, *C;
   const float *A, *D, *init, *dy, *dfinal;
   float *dx, *ddt, *dA, *dB, *dC, *dD, *dinit;
+  int* status;  // SSD_ERR_TIMEOUT when a device wait runs out (may be null)
   float* st;   // [chunks][H][P N]: chunk states, then the states entering each chunk
   float* ad;   // [chunks][H][P N]: local adjoint sums, then the adjoints leaving each chunk
   float* dec;  // [chunks][H]: exp(cum_last)
@@ -1310,6 +1311,583 @@ __global__ void __launch_bounds__(kThrG, 1) bwd_grad_mma_kernel(BP p) {
   }
 }
 
+// ---------------------------------------------------------------- gradients, tcgen05
+// The gradient kernel on the fifth-generation tensor cores (bf16 inputs,
+// headdim and dstate multiples of 8).  Per block (chunk, group, slice of up
+// to kHS heads of the group), 16 math warps and one MMA warp.  Operands are
+// 128-byte-swizzled bf16 tiles of 64 rows (exact for x, B, C; hi/lo pairs
+// for dy, exp(cum) dy, w x, H_c, dH_{c+1}, M and dG), zero-padded to headdim
+// 64 and dstate 128, read by the MMAs K-major or MN-major as each product
+// needs.  Accumulators (M = 64: row r in TMEM lane 32 (r / 16) + r % 16):
+//   dC (128 columns) += exp(cum) dY H + dG B       summed over the slice's heads
+//   dB (128 columns) += (w o X) dH + dG^T C
+//   S  = dY X^T (the first head's C B^T before it)   V = B dH^T
+//   Xi = M^T dY (D on M's diagonal: + D dy)          U = C H^T
+// Per head: operands -> smem; MMAs dS, V, U, dC, dB; the dS epilogue writes M
+// and dG; MMAs Xi, dC, dB; the epilogue of V, U, Xi writes dx and the decay
+// terms; warp 0 closes ddt and dA.  Every wait is bounded: one that runs out
+// records SSD_ERR_TIMEOUT and the block goes on (its results are then
+// undefined) and waits once more for its last MMAs before freeing TMEM.
+namespace tg {
+constexpr int kMathWarps = 16;
+constexpr int kThreads = 32 * (kMathWarps + 1);
+constexpr int kMathThreads = 32 * kMathWarps;
+constexpr uint32_t kAtom = 8192;  // 64 rows x 128 bytes
+constexpr uint32_t oB = 0, oC = 2 * kAtom, oX = 4 * kAtom, oWXh = 5 * kAtom, oWXl = 6 * kAtom,
+                   oYh = 7 * kAtom, oYl = 8 * kAtom, oEYh = 9 * kAtom, oEYl = 10 * kAtom,
+                   oHh = 11 * kAtom, oHl = 13 * kAtom, oDh = 15 * kAtom, oDl = 17 * kAtom,
+                   oMh = 19 * kAtom, oMl = 20 * kAtom, oGh = 21 * kAtom, oGl = 22 * kAtom,
+                   oTab = 23 * kAtom;
+// tables: two buffers of (cum, dt, exp(cum), w, exp(cum_last - cum)), then
+// dcum, the direct dt terms and the block sums
+constexpr uint32_t kTabFloats = 2 * 5 * kQb + 3 * kQb;
+constexpr uint32_t oBar = oTab + 4 * kTabFloats;
+constexpr uint32_t kSmem = oBar + 64 + 1024;  // + alignment of the tiles to 1024 bytes
+static_assert(kSmem <= 232448, "shared memory per block");
+constexpr uint32_t cDC = 0, cDB = 128, cS = 256, cX = 320, cV = 384, cU = 448;  // TMEM columns
+constexpr uint32_t kIdKK64 = tc::idesc_bf16(64, 64, false, false);
+constexpr uint32_t kIdNN64 = tc::idesc_bf16(64, 64, true, true);
+constexpr uint32_t kIdKN128 = tc::idesc_bf16(64, 128, false, true);
+constexpr uint32_t kIdNN128 = tc::idesc_bf16(64, 128, true, true);
+
+// byte offset of element (r, c) of a 64-row tile made of 64-column atoms
+__device__ __forceinline__ uint32_t swo(int r, int c) {
+  return (uint32_t)(c >> 6) * kAtom + tc::sw128_offset(r, (c & 63) >> 3) + (c & 7) * 2;
+}
+// descriptors: K-major (k-step kk: +32 bytes inside an atom, atoms kAtom
+// apart) and MN-major (k-step kk: +16 rows; 64-element MN blocks kAtom apart)
+__device__ __forceinline__ uint64_t dk(uint32_t s, int kk) {
+  return tc::sdesc_sw128(s + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t dm(uint32_t s, int kk) {
+  return tc::sdesc_sw128(s + kk * 2048, kAtom, 1024);
+}
+// 16 lanes x 16 (x2) / 32 (x4) columns: per thread the m16n8 accumulator
+// fragments of the warp's 16 rows (rows lane/4 and lane/4 + 8, columns
+// 8 b + 2 (lane % 4) + {0, 1} of block b)
+__device__ __forceinline__ void ld_frag2(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void ld_frag4(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// eight fp32 -> hi/lo bf16 (16 bytes each)
+__device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo) {
+  __nv_bfloat16 h[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) split_rn(v[i], h[i], l[i]);
+  hi = make_uint4(pack_bf2(h[0], h[1]), pack_bf2(h[2], h[3]), pack_bf2(h[4], h[5]), pack_bf2(h[6], h[7]));
+  lo = make_uint4(pack_bf2(l[0], l[1]), pack_bf2(l[2], l[3]), pack_bf2(l[4], l[5]), pack_bf2(l[6], l[7]));
+}
+__device__ __forceinline__ float2 bf2_at(const unsigned char* p) {
+  const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+}  // namespace tg
+
+__global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
+  using namespace tg;
+  extern __shared__ unsigned char tsm_raw[];
+  const uint32_t raw_s = tc::smem_u32(tsm_raw);
+  const uint32_t sb = (raw_s + 1023u) & ~1023u;
+  unsigned char* base = tsm_raw + (sb - raw_s);
+  float* tabs = reinterpret_cast<float*>(base + oTab);
+  float* dcum = tabs + 10 * kQb;  // dL/dcum
+  float* ddd = dcum + kQb;        // direct dt terms
+  float* red = ddd + kQb;         // block sums (48)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);  // C B^T, dS, group 1, group 2
+  uint32_t* tptr = reinterpret_cast<uint32_t*>(base + oBar + 32);
+  const int c = blockIdx.x, g = blockIdx.y;
+  const Chunk k = chunk_of(p, c);
+  const int P = p.P, N = p.N, len = k.len;
+  const int hpg = p.H / p.G;
+  const int hb = g * hpg + blockIdx.z * kHS;
+  const int nh = min(kHS, hpg - blockIdx.z * kHS);
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const bool math = w < kMathWarps;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int qd = w & 3, cg = w >> 2;  // math warps: TMEM lane quadrant (rows 16 qd..), column group
+  const int r16 = 16 * qd, c16 = 16 * cg, c32 = 32 * cg;
+  const uint32_t lanebase = (uint32_t)(32 * qd) << 16;
+  const __nv_bfloat16* xg = reinterpret_cast<const __nv_bfloat16*>(p.x);
+  bool ok = true;  // every wait of this thread completed
+
+  // One head's x, dy, H_c, dH_{c+1} in registers (zero outside the valid
+  // rows, headdim and dstate), loaded a head ahead of their use.  Math
+  // thread t: x and dy of row t / 8, columns 8 (t % 8).. (+4 for vy[1]);
+  // float4 r of H and dH at (t + 512 r) / 32, 4 ((t + 512 r) % 32).
+  uint4 vx = make_uint4(0, 0, 0, 0);
+  float4 vy[2], vh[4], vd[4];
+  const auto load_head = [&](int h) {
+    const long long sOff = ((long long)c * p.H + h) * (long long)(P * N);
+    const int j = t >> 3, q = (t & 7) * 8;
+    const bool okr = j < len && q < P;
+    const long long row = ((k.tok0 + j) * p.H + h) * P + q;
+    vx = okr ? *reinterpret_cast<const uint4*>(xg + row) : make_uint4(0, 0, 0, 0);
+    vy[0] = okr ? *reinterpret_cast<const float4*>(p.dy + row) : make_float4(0.f, 0.f, 0.f, 0.f);
+    vy[1] = okr ? *reinterpret_cast<const float4*>(p.dy + row + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e4 = t + kMathThreads * r, qq = e4 >> 5, n = (e4 & 31) * 4;
+      const bool okh = qq < P && n < N;
+      vh[r] = okh ? __ldcg(reinterpret_cast<const float4*>(p.st + sOff + qq * N + n))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      vd[r] = okh ? __ldcg(reinterpret_cast<const float4*>(p.ad + sOff + qq * N + n))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  const auto prefetch_head = [&](int h) {
+    const long long sOff = ((long long)c * p.H + h) * (long long)(P * N);
+    if (t == 0) {
+      tc::bulk_prefetch_l2(p.st + sOff, (uint32_t)(P * N * 4));
+      tc::bulk_prefetch_l2(p.ad + sOff, (uint32_t)(P * N * 4));
+    } else if (t >= 32 && t < 32 + kQb && t - 32 < len) {
+      const long long row = (k.tok0 + (t - 32)) * p.H + h;
+      tc::prefetch_l2(xg + row * P);
+      tc::prefetch_l2(p.dy + row * P);
+      if (P > 32) tc::prefetch_l2(p.dy + row * P + 32);
+    }
+  };
+  // Warp 0: the decay tables of head h into buffer b (lane l: rows 2l, 2l+1).
+  const auto tables = [&](int h, int b) {
+    float* cum = tabs + (5 * b) * kQb;
+    float* dts = cum + kQb;
+    float* ec = dts + kQb;
+    float* wt = ec + kQb;
+    float* el = wt + kQb;
+    const float Ah = p.A[h];
+    const int j0 = 2 * lane, j1 = j0 + 1;
+    const float d0 = j0 < len ? ldin<true>(p.dt, (k.tok0 + j0) * p.H + h) : 0.f;
+    const float d1 = j1 < len ? ldin<true>(p.dt, (k.tok0 + j1) * p.H + h) : 0.f;
+    const float a1 = d1 * Ah;
+    float s = d0 * Ah + a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += u;
+    }
+    const float cm1 = s, cm0 = s - a1;
+    const float lst = __shfl_sync(0xffffffffu, ((len - 1) & 1) ? cm1 : cm0, (len - 1) >> 1);
+    cum[j0] = cm0;
+    cum[j1] = cm1;
+    dts[j0] = d0;
+    dts[j1] = d1;
+    ec[j0] = expf(cm0);
+    ec[j1] = expf(cm1);
+    const float e0 = expf(lst - cm0), e1 = expf(lst - cm1);
+    el[j0] = e0;
+    el[j1] = e1;
+    wt[j0] = e0 * d0;
+    wt[j1] = e1 * d1;
+  };
+
+  // ---- prologue: B, C tiles; the first head's operands and tables; TMEM; C B^T
+  if (math) {
+    const __nv_bfloat16* Bg = reinterpret_cast<const __nv_bfloat16*>(p.B);
+    const __nv_bfloat16* Cg = reinterpret_cast<const __nv_bfloat16*>(p.C);
+    uint4 vb[2], vc[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e8 = t + kMathThreads * r, j = e8 >> 4, n = (e8 & 15) * 8;
+      const bool okb = j < len && n < N;
+      const long long i = ((k.tok0 + j) * p.G + g) * N + n;
+      vb[r] = okb ? *reinterpret_cast<const uint4*>(Bg + i) : make_uint4(0, 0, 0, 0);
+      vc[r] = okb ? *reinterpret_cast<const uint4*>(Cg + i) : make_uint4(0, 0, 0, 0);
+    }
+    load_head(hb);
+    if (nh > 1) prefetch_head(hb + 1);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e8 = t + kMathThreads * r, j = e8 >> 4, n = (e8 & 15) * 8;
+      *reinterpret_cast<uint4*>(base + oB + swo(j, n)) = vb[r];
+      *reinterpret_cast<uint4*>(base + oC + swo(j, n)) = vc[r];
+    }
+    if (w == 0) {
+      tables(hb, 0);
+      dcum[2 * lane] = dcum[2 * lane + 1] = 0.f;
+      ddd[2 * lane] = ddd[2 * lane + 1] = 0.f;
+    }
+    tc::fence_proxy_async_smem();
+  } else {
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tc::mbar_init(&bars[i], 1);
+      tc::fence_mbar_init();
+    }
+    __syncwarp();
+    tc::tmem_alloc(tptr, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tm = *tptr;
+  if (!math) {
+    if (tc::elect_one()) {
+#pragma unroll 1
+      for (int kk = 0; kk < 8; ++kk)
+        tc::mma_bf16(tm + cS, dk(sb + oC, kk), dk(sb + oB, kk), kIdKK64, kk > 0);
+      tc::mma_commit(&bars[0]);
+    }
+    __syncwarp();
+  }
+  float gr[8];  // C B^T at this thread's dS fragment positions
+  if (math) {
+    ok &= tc::mbar_wait(&bars[0], 0);
+    tc::tc_fence_after();
+    ld_frag2(tm + lanebase + cS + c16, gr);
+    tc::tmem_ld_wait();
+    tc::tie8(gr);
+  }
+
+  for (int hh = 0; hh < nh; ++hh) {
+    const int h = hb + hh;
+    const uint32_t par = hh & 1;
+    const float* cum = tabs + (5 * (hh & 1)) * kQb;
+    const float* dts = cum + kQb;
+    const float* ec = dts + kQb;
+    const float* wt = ec + kQb;
+    const float* el = wt + kQb;
+    float hdot = 0.f, dd = 0.f, wv_sum = 0.f;
+    // ---- operands to shared memory
+    if (math) {
+      const int j = t >> 3, q = (t & 7) * 8;
+      const uint32_t o8 = swo(j, q);
+      *reinterpret_cast<uint4*>(base + oX + o8) = vx;
+      float xf[8], yf[8];
+      xf[0] = __uint_as_float(vx.x << 16);
+      xf[1] = __uint_as_float(vx.x & 0xffff0000u);
+      xf[2] = __uint_as_float(vx.y << 16);
+      xf[3] = __uint_as_float(vx.y & 0xffff0000u);
+      xf[4] = __uint_as_float(vx.z << 16);
+      xf[5] = __uint_as_float(vx.z & 0xffff0000u);
+      xf[6] = __uint_as_float(vx.w << 16);
+      xf[7] = __uint_as_float(vx.w & 0xffff0000u);
+      yf[0] = vy[0].x; yf[1] = vy[0].y; yf[2] = vy[0].z; yf[3] = vy[0].w;
+      yf[4] = vy[1].x; yf[5] = vy[1].y; yf[6] = vy[1].z; yf[7] = vy[1].w;
+      const float wj = wt[j], ej = ec[j];
+      float sx[8], sy[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        dd = fmaf(xf[i], yf[i], dd);
+        sx[i] = wj * xf[i];
+        sy[i] = ej * yf[i];
+      }
+      uint4 hi, lo;
+      split8(sx, hi, lo);
+      *reinterpret_cast<uint4*>(base + oWXh + o8) = hi;
+      *reinterpret_cast<uint4*>(base + oWXl + o8) = lo;
+      split8(sy, hi, lo);
+      *reinterpret_cast<uint4*>(base + oEYh + o8) = hi;
+      *reinterpret_cast<uint4*>(base + oEYl + o8) = lo;
+      split8(yf, hi, lo);
+      *reinterpret_cast<uint4*>(base + oYh + o8) = hi;
+      *reinterpret_cast<uint4*>(base + oYl + o8) = lo;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int e4 = t + kMathThreads * r, qq = e4 >> 5, n = (e4 & 31) * 4;
+        const uint32_t o = swo(qq, n);
+        store_split4(reinterpret_cast<__nv_bfloat16*>(base + oHh + o),
+                     reinterpret_cast<__nv_bfloat16*>(base + oHl + o), vh[r]);
+        store_split4(reinterpret_cast<__nv_bfloat16*>(base + oDh + o),
+                     reinterpret_cast<__nv_bfloat16*>(base + oDl + o), vd[r]);
+        hdot += vh[r].x * vd[r].x + vh[r].y * vd[r].y + vh[r].z * vd[r].z + vh[r].w * vd[r].w;
+      }
+      tc::fence_proxy_async_smem();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const float last = cum[len - 1];
+
+    // ---- group 1: dS = dY X^T; V = B dH^T; U = C H^T; dC += (ec o dY) H; dB += (w o X) dH
+    if (!math) {
+      if (tc::elect_one()) {
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) {
+          tc::mma_bf16(tm + cS, dk(sb + oYh, kk), dk(sb + oX, kk), kIdKK64, kk > 0);
+          tc::mma_bf16(tm + cS, dk(sb + oYl, kk), dk(sb + oX, kk), kIdKK64, true);
+        }
+        tc::mma_commit(&bars[1]);
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk) {
+          tc::mma_bf16(tm + cV, dk(sb + oB, kk), dk(sb + oDh, kk), kIdKK64, kk > 0);
+          tc::mma_bf16(tm + cV, dk(sb + oB, kk), dk(sb + oDl, kk), kIdKK64, true);
+          tc::mma_bf16(tm + cU, dk(sb + oC, kk), dk(sb + oHh, kk), kIdKK64, kk > 0);
+          tc::mma_bf16(tm + cU, dk(sb + oC, kk), dk(sb + oHl, kk), kIdKK64, true);
+        }
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) {
+          const bool acc = hh > 0 || kk > 0;
+          tc::mma_bf16(tm + cDC, dk(sb + oEYh, kk), dm(sb + oHh, kk), kIdKN128, acc);
+          tc::mma_bf16(tm + cDC, dk(sb + oEYl, kk), dm(sb + oHh, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDC, dk(sb + oEYh, kk), dm(sb + oHl, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDB, dk(sb + oWXh, kk), dm(sb + oDh, kk), kIdKN128, acc);
+          tc::mma_bf16(tm + cDB, dk(sb + oWXl, kk), dm(sb + oDh, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDB, dk(sb + oWXh, kk), dm(sb + oDl, kk), kIdKN128, true);
+        }
+        tc::mma_commit(&bars[2]);
+      }
+      __syncwarp();
+    } else {
+      // ---- dS epilogue: M = G L dt (+ D on the diagonal), dG = dS L dt;
+      //      the decay terms of the quadratic form (rows r16.., columns c16..)
+      ok &= tc::mbar_wait(&bars[1], par);
+      tc::tc_fence_after();
+      float sa[8];
+      ld_frag2(tm + lanebase + cS + c16, sa);
+      tc::tmem_ld_wait();
+      tc::tie8(sa);
+      const float Dd = p.D ? p.D[h] : 0.f;
+      float rowT[2] = {0.f, 0.f}, colU[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int i = r16 + gq + 8 * hf;
+          float mv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int j = c16 + 8 * tt + 2 * tq + e;
+            const int f = 4 * tt + 2 * hf + e;
+            mv[e] = dv[e] = 0.f;
+            if (j <= i && i < len) {
+              const float L = expf(cum[i] - cum[j]);
+              const float GL = gr[f] * L;
+              mv[e] = GL * dts[j];
+              dv[e] = sa[f] * L * dts[j];
+              rowT[hf] = fmaf(sa[f], mv[e], rowT[hf]);
+              colU[tt][e] = fmaf(sa[f], GL, colU[tt][e]);
+              if (i == j) mv[e] += Dd;
+            }
+          }
+          __nv_bfloat16 h0, h1, l0, l1;
+          const uint32_t o = swo(i, c16 + 8 * tt + 2 * tq);
+          split_rn(mv[0], h0, l0);
+          split_rn(mv[1], h1, l1);
+          *reinterpret_cast<uint32_t*>(base + oMh + o) = pack_bf2(h0, h1);
+          *reinterpret_cast<uint32_t*>(base + oMl + o) = pack_bf2(l0, l1);
+          split_rn(dv[0], h0, l0);
+          split_rn(dv[1], h1, l1);
+          *reinterpret_cast<uint32_t*>(base + oGh + o) = pack_bf2(h0, h1);
+          *reinterpret_cast<uint32_t*>(base + oGl + o) = pack_bf2(l0, l1);
+        }
+      }
+      if (cg <= qd) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float v = rowT[hf];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          if (tq == 0) atomicAdd(&dcum[r16 + gq + 8 * hf], v);
+        }
+        // column j: sum_i dS M = dt_j sum_i dS G L
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float b = colU[tt][e];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+            if (gq == 0) {
+              const int j = c16 + 8 * tt + 2 * tq + e;
+              atomicAdd(&dcum[j], -dts[j] * b);
+              atomicAdd(&ddd[j], b);
+            }
+          }
+      }
+      tc::fence_proxy_async_smem();
+      if (w == 0 && hh + 1 < nh) tables(h + 1, (hh + 1) & 1);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+
+    // ---- group 2: Xi = M^T dY; dC += dG B; dB += dG^T C
+    if (!math) {
+      if (tc::elect_one()) {
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) {
+          tc::mma_bf16(tm + cX, dm(sb + oMh, kk), dm(sb + oYh, kk), kIdNN64, kk > 0);
+          tc::mma_bf16(tm + cX, dm(sb + oMl, kk), dm(sb + oYh, kk), kIdNN64, true);
+          tc::mma_bf16(tm + cX, dm(sb + oMh, kk), dm(sb + oYl, kk), kIdNN64, true);
+          tc::mma_bf16(tm + cDC, dk(sb + oGh, kk), dm(sb + oB, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDC, dk(sb + oGl, kk), dm(sb + oB, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDB, dm(sb + oGh, kk), dm(sb + oC, kk), kIdNN128, true);
+          tc::mma_bf16(tm + cDB, dm(sb + oGl, kk), dm(sb + oC, kk), kIdNN128, true);
+        }
+        tc::mma_commit(&bars[3]);
+      }
+      __syncwarp();
+    } else {
+      // ---- V, U: the state terms of the decay; then dx = Xi + w_j V
+      ok &= tc::mbar_wait(&bars[2], par);
+      tc::tc_fence_after();
+      float va[8], ua[8];
+      ld_frag2(tm + lanebase + cV + c16, va);
+      ld_frag2(tm + lanebase + cU + c16, ua);
+      tc::tmem_ld_wait();
+      tc::tie8(va);
+      tc::tie8(ua);
+      float vp[2] = {0.f, 0.f}, zc[2] = {0.f, 0.f};
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int r = r16 + gq + 8 * hf;
+          const uint32_t o = swo(r, c16 + 8 * tt + 2 * tq);
+          const float2 xv = bf2_at(base + oX + o);
+          const float2 yh = bf2_at(base + oYh + o), yl = bf2_at(base + oYl + o);
+          const int f = 4 * tt + 2 * hf;
+          vp[hf] += xv.x * va[f] + xv.y * va[f + 1];
+          zc[hf] += (yh.x + yl.x) * ua[f] + (yh.y + yl.y) * ua[f + 1];
+        }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float v = vp[hf], z = zc[hf];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        z += __shfl_xor_sync(0xffffffffu, z, 1);
+        z += __shfl_xor_sync(0xffffffffu, z, 2);
+        const int r = r16 + gq + 8 * hf;
+        if (tq == 0 && r < len) {
+          atomicAdd(&dcum[r], ec[r] * z - wt[r] * v);
+          atomicAdd(&ddd[r], el[r] * v);
+          wv_sum = fmaf(wt[r], v, wv_sum);
+        }
+      }
+      ok &= tc::mbar_wait(&bars[3], par);
+      tc::tc_fence_after();
+      float xa[8];
+      ld_frag2(tm + lanebase + cX + c16, xa);
+      tc::tmem_ld_wait();
+      tc::tie8(xa);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int j = r16 + gq + 8 * hf;
+        const float wj = wt[j];
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+          const int q = c16 + 8 * tt + 2 * tq;
+          const int f = 4 * tt + 2 * hf;
+          if (j < len && q < P)
+            *reinterpret_cast<float2*>(p.dx + ((k.tok0 + j) * p.H + h) * P + q) =
+                make_float2(fmaf(wj, va[f], xa[f]), fmaf(wj, va[f + 1], xa[f + 1]));
+        }
+      }
+      // the next head's operands into registers
+      if (hh + 1 < nh) {
+        load_head(h + 1);
+        if (hh + 2 < nh) prefetch_head(h + 2);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        hdot += __shfl_xor_sync(0xffffffffu, hdot, o);
+        wv_sum += __shfl_xor_sync(0xffffffffu, wv_sum, o);
+        dd += __shfl_xor_sync(0xffffffffu, dd, o);
+      }
+      if (lane == 0) {
+        red[w] = hdot;
+        red[16 + w] = wv_sum;
+        red[32 + w] = dd;
+      }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    // ---- warp 0: <dH, H>, sum_j w_j v_j, dD; ddt_j = direct terms + A
+    //      sum_{k>=j} dcum_k; dA += sum_j dt_j sum_{k>=j} dcum_k
+    if (w == 0) {
+      float a = lane < 16 ? red[lane] : 0.f, b = lane < 16 ? red[16 + lane] : 0.f,
+            d2 = lane < 16 ? red[32 + lane] : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+        d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+      }
+      // reverse inclusive scan, lane l owning entries 63 - 2l and 62 - 2l;
+      // the state terms of the last valid row join it there
+      const int j1 = kQb - 1 - 2 * lane, j2 = j1 - 1;
+      const float extra = expf(last) * a + b;
+      const float a1 = dcum[j1] + (j1 == len - 1 ? extra : 0.f);
+      const float a2 = dcum[j2] + (j2 == len - 1 ? extra : 0.f);
+      const float q1 = ddd[j1], q2 = ddd[j2];
+      __syncwarp();
+      dcum[j1] = dcum[j2] = 0.f;
+      ddd[j1] = ddd[j2] = 0.f;
+      if (lane == 0 && p.dD) atomicAdd(p.dD + h, d2);
+      float v = a1 + a2;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      const float r2 = v, r1 = v - a2;
+      const float Ah = p.A[h];
+      float da = 0.f;
+      if (j1 < len) {
+        p.ddt[(k.tok0 + j1) * p.H + h] = q1 + Ah * r1;
+        da = fmaf(dts[j1], r1, da);
+      }
+      if (j2 < len) {
+        p.ddt[(k.tok0 + j2) * p.H + h] = q2 + Ah * r2;
+        da = fmaf(dts[j2], r2, da);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
+      if (lane == 0) atomicAdd(p.dA + h, da);
+    }
+  }
+  // ---- dB, dC of the slice's heads (rows r16.., columns c32..)
+  if (math) {
+    tc::tc_fence_after();
+    float vc[16], vb[16];
+    ld_frag4(tm + lanebase + cDC + c32, vc);
+    ld_frag4(tm + lanebase + cDB + c32, vb);
+    tc::tmem_ld_wait();
+    tc::tie16(vc);
+    tc::tie16(vb);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int j = r16 + gq + 8 * hf;
+      if (j < len) {
+        float* db = p.dB + ((k.tok0 + j) * p.G + g) * N;
+        float* dc = p.dC + ((k.tok0 + j) * p.G + g) * N;
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+          const int n = c32 + 8 * tt + 2 * tq;
+          const int f = 4 * tt + 2 * hf;
+          if (n < N) {
+            atomicAdd(reinterpret_cast<float2*>(db + n), make_float2(vb[f], vb[f + 1]));
+            atomicAdd(reinterpret_cast<float2*>(dc + n), make_float2(vc[f], vc[f + 1]));
+          }
+        }
+      }
+    }
+  }
+  if (!ok && p.status) atomicCAS(p.status, 0, (int)SSD_ERR_TIMEOUT);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (!math) {
+    tc::mbar_wait(&bars[3], (nh - 1) & 1);  // the last MMAs are done (bounded)
+    tc::tmem_dealloc(tm, 512);
+  }
+}
 }  // namespace
 
 bool bwd_chunked_supported(int P, int N) {
@@ -1341,6 +1919,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   p.dC = a.dC;
   p.dD = a.dD;
   p.dinit = a.dinit;
+  p.status = nullptr;
   p.T = a.seqlen;
   p.H = a.H;
   p.P = a.P;
@@ -1363,6 +1942,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
     const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
     if (cudaFuncSetAttribute(bwd_grad_kernel<true>, at, (int)kGradSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_grad_mma_kernel, at, (int)kGradMmaSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_grad_tc_kernel, at, (int)tg::kSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_grad_kernel<false>, at, (int)kGradSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_outer_kernel<true, 0>, at, (int)outer_smem<true>()) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_outer_kernel<true, 1>, at, (int)outer_smem<true>()) != cudaSuccess ||
@@ -1387,7 +1967,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   const bool mma = bf && a.P % 8 == 0 && a.N % 8 == 0 && al(a.x, 15) && al(a.B, 15) &&
                    al(a.C, 15) && al(a.dy, 15) && al(a.dx, 7) && al(a.dB, 7) && al(a.dC, 7);
   if (mma)
-    bwd_grad_mma_kernel<<<ggrid, kThrG, kGradMmaSmem, a.stream>>>(p);
+    bwd_grad_tc_kernel<<<ggrid, tg::kThreads, tg::kSmem, a.stream>>>(p);
   else if (bf)
     bwd_grad_kernel<true><<<ggrid, kThr, kGradSmem, a.stream>>>(p);
   else
