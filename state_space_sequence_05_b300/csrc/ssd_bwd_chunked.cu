@@ -55,6 +55,7 @@
 #include "ssd.h"
 #include "ssd_internal.h"
 #include "tc_ptx.cuh"
+#include "tc_util.cuh"
 
 namespace ssd {
 namespace {
@@ -1338,9 +1339,10 @@ constexpr uint32_t oB = 0, oC = 2 * kAtom, oX = 4 * kAtom, oWXh = 5 * kAtom, oWX
                    oHh = 11 * kAtom, oHl = 13 * kAtom, oDh = 15 * kAtom, oDl = 17 * kAtom,
                    oMh = 19 * kAtom, oMl = 20 * kAtom, oGh = 21 * kAtom, oGl = 22 * kAtom,
                    oTab = 23 * kAtom;
-// tables: two buffers of (cum, dt, exp(cum), w, exp(cum_last - cum)), then
-// dcum, the direct dt terms and the block sums
-constexpr uint32_t kTabFloats = 2 * 5 * kQb + 3 * kQb;
+// tables (floats): two buffers of (log2e cum, exp(cum), w, exp(cum_last -
+// cum)) [64]; per head of the slice dt [8][64], dL/dcum [8][64], the direct
+// dt terms [8][64], and (log2e cum_last, <dH, H>, sum_j w_j v_j, dD) [8][4]
+constexpr uint32_t kTabFloats = 2 * 4 * kQb + 3 * kHS * kQb + 4 * kHS;
 constexpr uint32_t oBar = oTab + 4 * kTabFloats;
 constexpr uint32_t kSmem = oBar + 64 + 1024;  // + alignment of the tiles to 1024 bytes
 static_assert(kSmem <= 232448, "shared memory per block");
@@ -1349,22 +1351,20 @@ constexpr uint32_t kIdKK64 = tc::idesc_bf16(64, 64, false, false);
 constexpr uint32_t kIdNN64 = tc::idesc_bf16(64, 64, true, true);
 constexpr uint32_t kIdKN128 = tc::idesc_bf16(64, 128, false, true);
 constexpr uint32_t kIdNN128 = tc::idesc_bf16(64, 128, true, true);
+constexpr float kLog2e = 1.4426950408889634f;
 
 // byte offset of element (r, c) of a 64-row tile made of 64-column atoms
 __device__ __forceinline__ uint32_t swo(int r, int c) {
   return (uint32_t)(c >> 6) * kAtom + tc::sw128_offset(r, (c & 63) >> 3) + (c & 7) * 2;
 }
-// descriptors: K-major (k-step kk: +32 bytes inside an atom, atoms kAtom
-// apart) and MN-major (k-step kk: +16 rows; 64-element MN blocks kAtom apart)
-__device__ __forceinline__ uint64_t dk(uint32_t s, int kk) {
-  return tc::sdesc_sw128(s + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-}
-__device__ __forceinline__ uint64_t dm(uint32_t s, int kk) {
-  return tc::sdesc_sw128(s + kk * 2048, kAtom, 1024);
-}
-// 16 lanes x 16 (x2) / 32 (x4) columns: per thread the m16n8 accumulator
-// fragments of the warp's 16 rows (rows lane/4 and lane/4 + 8, columns
-// 8 b + 2 (lane % 4) + {0, 1} of block b)
+// descriptor offsets (16-byte units) of k-step kk: K-major +32 bytes inside
+// an atom, atoms kAtom apart; MN-major +16 rows (64-element MN blocks kAtom
+// apart, the descriptor's leading offset)
+__host__ __device__ constexpr uint64_t kof(int kk) { return (uint64_t)((kk >> 2) * (kAtom >> 4) + (kk & 3) * 2); }
+__host__ __device__ constexpr uint64_t mof(int kk) { return (uint64_t)(kk * 128); }
+// 16 lanes x 16 columns: per thread the m16n8 accumulator fragments of the
+// warp's 16 rows (rows lane/4 and lane/4 + 8, columns 8 b + 2 (lane % 4) +
+// {0, 1} of block b = 0, 1)
 __device__ __forceinline__ void ld_frag2(uint32_t taddr, float (&v)[8]) {
   uint32_t r[8];
   asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -1374,6 +1374,7 @@ __device__ __forceinline__ void ld_frag2(uint32_t taddr, float (&v)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
+// the same for 32 columns (blocks b = 0..3)
 __device__ __forceinline__ void ld_frag4(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
@@ -1386,32 +1387,47 @@ __device__ __forceinline__ void ld_frag4(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-// eight fp32 -> hi/lo bf16 (16 bytes each)
-__device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo) {
-  __nv_bfloat16 h[8], l[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) split_rn(v[i], h[i], l[i]);
-  hi = make_uint4(pack_bf2(h[0], h[1]), pack_bf2(h[2], h[3]), pack_bf2(h[4], h[5]), pack_bf2(h[6], h[7]));
-  lo = make_uint4(pack_bf2(l[0], l[1]), pack_bf2(l[2], l[3]), pack_bf2(l[4], l[5]), pack_bf2(l[6], l[7]));
+// a pair of fp32 -> bf16 hi = rn(v), lo = rn(v - hi), packed (x in the low half)
+__device__ __forceinline__ void split2rn(tc::f2 v, uint32_t& hi, uint32_t& lo) {
+  hi = tc::pack_bf16(v.x, v.y);
+  const tc::f2 r = tc::sub2(v, tc::bf2(hi));
+  lo = tc::pack_bf16(r.x, r.y);
 }
-__device__ __forceinline__ float2 bf2_at(const unsigned char* p) {
-  const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
-  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+// eight fp32 (four pairs) -> hi/lo, 16 bytes each
+__device__ __forceinline__ void split8(const tc::f2 (&v)[4], uint4& hi, uint4& lo) {
+  split2rn(v[0], hi.x, lo.x);
+  split2rn(v[1], hi.y, lo.y);
+  split2rn(v[2], hi.z, lo.z);
+  split2rn(v[3], hi.w, lo.w);
+}
+// four fp32 -> hi/lo, 8 bytes each, at byte addresses ph / pl
+__device__ __forceinline__ void split4_at(unsigned char* ph, unsigned char* pl, float4 v) {
+  uint2 hi, lo;
+  split2rn(tc::f2{v.x, v.y}, hi.x, lo.x);
+  split2rn(tc::f2{v.z, v.w}, hi.y, lo.y);
+  *reinterpret_cast<uint2*>(ph) = hi;
+  *reinterpret_cast<uint2*>(pl) = lo;
+}
+__device__ __forceinline__ tc::f2 bf2_at(const unsigned char* p) {
+  return tc::bf2(*reinterpret_cast<const uint32_t*>(p));
 }
 }  // namespace tg
 
 __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   using namespace tg;
+  using tc::f2;
   extern __shared__ unsigned char tsm_raw[];
   const uint32_t raw_s = tc::smem_u32(tsm_raw);
   const uint32_t sb = (raw_s + 1023u) & ~1023u;
   unsigned char* base = tsm_raw + (sb - raw_s);
   float* tabs = reinterpret_cast<float*>(base + oTab);
-  float* dcum = tabs + 10 * kQb;  // dL/dcum
-  float* ddd = dcum + kQb;        // direct dt terms
-  float* red = ddd + kQb;         // block sums (48)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);  // C B^T, dS, group 1, group 2
-  uint32_t* tptr = reinterpret_cast<uint32_t*>(base + oBar + 32);
+  float* dtsH = tabs + 8 * kQb;          // [8][64] dt per head
+  float* dcumH = dtsH + kHS * kQb;       // [8][64] dL/dcum per head
+  float* dddH = dcumH + kHS * kQb;       // [8][64] direct dt terms per head
+  float* hsum = dddH + kHS * kQb;        // [8][4] per head
+  // mbarriers, one phase per head each: C B^T (once), dS, group 1, group 2, Xi
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);
+  uint32_t* tptr = reinterpret_cast<uint32_t*>(base + oBar + 48);
   const int c = blockIdx.x, g = blockIdx.y;
   const Chunk k = chunk_of(p, c);
   const int P = p.P, N = p.N, len = k.len;
@@ -1429,8 +1445,8 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
 
   // One head's x, dy, H_c, dH_{c+1} in registers (zero outside the valid
   // rows, headdim and dstate), loaded a head ahead of their use.  Math
-  // thread t: x and dy of row t / 8, columns 8 (t % 8).. (+4 for vy[1]);
-  // float4 r of H and dH at (t + 512 r) / 32, 4 ((t + 512 r) % 32).
+  // thread t: x and dy of row t / 8, columns 8 (t % 8)..; float4 r of H and
+  // dH at row (t + 512 r) / 32, columns 4 ((t + 512 r) % 32)..
   uint4 vx = make_uint4(0, 0, 0, 0);
   float4 vy[2], vh[4], vd[4];
   const auto load_head = [&](int h) {
@@ -1463,14 +1479,15 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
       if (P > 32) tc::prefetch_l2(p.dy + row * P + 32);
     }
   };
-  // Warp 0: the decay tables of head h into buffer b (lane l: rows 2l, 2l+1).
-  const auto tables = [&](int h, int b) {
-    float* cum = tabs + (5 * b) * kQb;
-    float* dts = cum + kQb;
-    float* ec = dts + kQb;
+  // One warp: the decay tables of slice head hh into buffer hh % 2 (lane l:
+  // rows 2l, 2l+1), its dt and log2e cum_last.
+  const auto tables = [&](int hh) {
+    const int h = hb + hh;
+    float* c2 = tabs + 4 * (hh & 1) * kQb;
+    float* ec = c2 + kQb;
     float* wt = ec + kQb;
     float* el = wt + kQb;
-    const float Ah = p.A[h];
+    const float Ah = p.A[h] * kLog2e;
     const int j0 = 2 * lane, j1 = j0 + 1;
     const float d0 = j0 < len ? ldin<true>(p.dt, (k.tok0 + j0) * p.H + h) : 0.f;
     const float d1 = j1 < len ? ldin<true>(p.dt, (k.tok0 + j1) * p.H + h) : 0.f;
@@ -1483,17 +1500,18 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     }
     const float cm1 = s, cm0 = s - a1;
     const float lst = __shfl_sync(0xffffffffu, ((len - 1) & 1) ? cm1 : cm0, (len - 1) >> 1);
-    cum[j0] = cm0;
-    cum[j1] = cm1;
-    dts[j0] = d0;
-    dts[j1] = d1;
-    ec[j0] = expf(cm0);
-    ec[j1] = expf(cm1);
-    const float e0 = expf(lst - cm0), e1 = expf(lst - cm1);
+    c2[j0] = cm0;
+    c2[j1] = cm1;
+    dtsH[hh * kQb + j0] = d0;
+    dtsH[hh * kQb + j1] = d1;
+    ec[j0] = tc::fast_exp2(cm0);
+    ec[j1] = tc::fast_exp2(cm1);
+    const float e0 = tc::fast_exp2(lst - cm0), e1 = tc::fast_exp2(lst - cm1);
     el[j0] = e0;
     el[j1] = e1;
     wt[j0] = e0 * d0;
     wt[j1] = e1 * d1;
+    if (lane == 0) hsum[4 * hh] = lst;
   };
 
   // ---- prologue: B, C tiles; the first head's operands and tables; TMEM; C B^T
@@ -1517,16 +1535,13 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
       *reinterpret_cast<uint4*>(base + oB + swo(j, n)) = vb[r];
       *reinterpret_cast<uint4*>(base + oC + swo(j, n)) = vc[r];
     }
-    if (w == 0) {
-      tables(hb, 0);
-      dcum[2 * lane] = dcum[2 * lane + 1] = 0.f;
-      ddd[2 * lane] = ddd[2 * lane + 1] = 0.f;
-    }
+    for (int e = t; e < 2 * kHS * kQb + 4 * kHS; e += kMathThreads) dcumH[e] = 0.f;  // dcum, ddd, sums
+    if (w == 0) tables(0);
     tc::fence_proxy_async_smem();
   } else {
     if (lane == 0) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) tc::mbar_init(&bars[i], 1);
+      for (int i = 0; i < 5; ++i) tc::mbar_init(&bars[i], 1);
       tc::fence_mbar_init();
     }
     __syncwarp();
@@ -1537,11 +1552,15 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tm = *tptr;
+  // operand descriptors: one K-major and one MN-major base, the tiles at
+  // constant offsets from it (start-address field, 16-byte units)
+  const uint64_t kd0 = tc::sdesc_sw128(sb, 16, 1024), md0 = tc::sdesc_sw128(sb, kAtom, 1024);
+#define KD(off, kk) (kd0 + ((off) >> 4) + kof(kk))
+#define MD(off, kk) (md0 + ((off) >> 4) + mof(kk))
   if (!math) {
     if (tc::elect_one()) {
-#pragma unroll 1
-      for (int kk = 0; kk < 8; ++kk)
-        tc::mma_bf16(tm + cS, dk(sb + oC, kk), dk(sb + oB, kk), kIdKK64, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tm + cS, KD(oC, kk), KD(oB, kk), kIdKK64, kk > 0);
       tc::mma_commit(&bars[0]);
     }
     __syncwarp();
@@ -1558,35 +1577,28 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   for (int hh = 0; hh < nh; ++hh) {
     const int h = hb + hh;
     const uint32_t par = hh & 1;
-    const float* cum = tabs + (5 * (hh & 1)) * kQb;
-    const float* dts = cum + kQb;
-    const float* ec = dts + kQb;
+    const float* c2 = tabs + 4 * (hh & 1) * kQb;  // log2e cum
+    const float* ec = c2 + kQb;
     const float* wt = ec + kQb;
     const float* el = wt + kQb;
-    float hdot = 0.f, dd = 0.f, wv_sum = 0.f;
+    const float* dts = dtsH + hh * kQb;
+    float* dcum = dcumH + hh * kQb;
+    float* ddd = dddH + hh * kQb;
     // ---- operands to shared memory
     if (math) {
       const int j = t >> 3, q = (t & 7) * 8;
       const uint32_t o8 = swo(j, q);
       *reinterpret_cast<uint4*>(base + oX + o8) = vx;
-      float xf[8], yf[8];
-      xf[0] = __uint_as_float(vx.x << 16);
-      xf[1] = __uint_as_float(vx.x & 0xffff0000u);
-      xf[2] = __uint_as_float(vx.y << 16);
-      xf[3] = __uint_as_float(vx.y & 0xffff0000u);
-      xf[4] = __uint_as_float(vx.z << 16);
-      xf[5] = __uint_as_float(vx.z & 0xffff0000u);
-      xf[6] = __uint_as_float(vx.w << 16);
-      xf[7] = __uint_as_float(vx.w & 0xffff0000u);
-      yf[0] = vy[0].x; yf[1] = vy[0].y; yf[2] = vy[0].z; yf[3] = vy[0].w;
-      yf[4] = vy[1].x; yf[5] = vy[1].y; yf[6] = vy[1].z; yf[7] = vy[1].w;
-      const float wj = wt[j], ej = ec[j];
-      float sx[8], sy[8];
+      const f2 xf[4] = {tc::bf2(vx.x), tc::bf2(vx.y), tc::bf2(vx.z), tc::bf2(vx.w)};
+      const f2 yf[4] = {f2{vy[0].x, vy[0].y}, f2{vy[0].z, vy[0].w}, f2{vy[1].x, vy[1].y},
+                        f2{vy[1].z, vy[1].w}};
+      const f2 wj{wt[j], wt[j]}, ej{ec[j], ec[j]};
+      f2 sx[4], sy[4], dd2{0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        dd = fmaf(xf[i], yf[i], dd);
-        sx[i] = wj * xf[i];
-        sy[i] = ej * yf[i];
+      for (int i = 0; i < 4; ++i) {
+        dd2 = tc::fma2(xf[i], yf[i], dd2);
+        sx[i] = tc::mul2(wj, xf[i]);
+        sy[i] = tc::mul2(ej, yf[i]);
       }
       uint4 hi, lo;
       split8(sx, hi, lo);
@@ -1598,48 +1610,58 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
       split8(yf, hi, lo);
       *reinterpret_cast<uint4*>(base + oYh + o8) = hi;
       *reinterpret_cast<uint4*>(base + oYl + o8) = lo;
+      f2 hd2{0.f, 0.f};
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int e4 = t + kMathThreads * r, qq = e4 >> 5, n = (e4 & 31) * 4;
         const uint32_t o = swo(qq, n);
-        store_split4(reinterpret_cast<__nv_bfloat16*>(base + oHh + o),
-                     reinterpret_cast<__nv_bfloat16*>(base + oHl + o), vh[r]);
-        store_split4(reinterpret_cast<__nv_bfloat16*>(base + oDh + o),
-                     reinterpret_cast<__nv_bfloat16*>(base + oDl + o), vd[r]);
-        hdot += vh[r].x * vd[r].x + vh[r].y * vd[r].y + vh[r].z * vd[r].z + vh[r].w * vd[r].w;
+        split4_at(base + oHh + o, base + oHl + o, vh[r]);
+        split4_at(base + oDh + o, base + oDl + o, vd[r]);
+        hd2 = tc::fma2(f2{vh[r].x, vh[r].y}, f2{vd[r].x, vd[r].y}, hd2);
+        hd2 = tc::fma2(f2{vh[r].z, vh[r].w}, f2{vd[r].z, vd[r].w}, hd2);
       }
       tc::fence_proxy_async_smem();
+      // the block sums <dH, H> and dD of this head
+      float hdot = hd2.x + hd2.y, dd = dd2.x + dd2.y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        hdot += __shfl_xor_sync(0xffffffffu, hdot, o);
+        dd += __shfl_xor_sync(0xffffffffu, dd, o);
+      }
+      if (lane == 0) {
+        atomicAdd(&hsum[4 * hh + 1], hdot);
+        atomicAdd(&hsum[4 * hh + 3], dd);
+      }
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const float last = cum[len - 1];
 
     // ---- group 1: dS = dY X^T; V = B dH^T; U = C H^T; dC += (ec o dY) H; dB += (w o X) dH
     if (!math) {
       if (tc::elect_one()) {
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          tc::mma_bf16(tm + cS, dk(sb + oYh, kk), dk(sb + oX, kk), kIdKK64, kk > 0);
-          tc::mma_bf16(tm + cS, dk(sb + oYl, kk), dk(sb + oX, kk), kIdKK64, true);
+          tc::mma_bf16(tm + cS, KD(oYh, kk), KD(oX, kk), kIdKK64, kk > 0);
+          tc::mma_bf16(tm + cS, KD(oYl, kk), KD(oX, kk), kIdKK64, true);
         }
         tc::mma_commit(&bars[1]);
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk) {
-          tc::mma_bf16(tm + cV, dk(sb + oB, kk), dk(sb + oDh, kk), kIdKK64, kk > 0);
-          tc::mma_bf16(tm + cV, dk(sb + oB, kk), dk(sb + oDl, kk), kIdKK64, true);
-          tc::mma_bf16(tm + cU, dk(sb + oC, kk), dk(sb + oHh, kk), kIdKK64, kk > 0);
-          tc::mma_bf16(tm + cU, dk(sb + oC, kk), dk(sb + oHl, kk), kIdKK64, true);
-        }
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const bool acc = hh > 0 || kk > 0;
-          tc::mma_bf16(tm + cDC, dk(sb + oEYh, kk), dm(sb + oHh, kk), kIdKN128, acc);
-          tc::mma_bf16(tm + cDC, dk(sb + oEYl, kk), dm(sb + oHh, kk), kIdKN128, true);
-          tc::mma_bf16(tm + cDC, dk(sb + oEYh, kk), dm(sb + oHl, kk), kIdKN128, true);
-          tc::mma_bf16(tm + cDB, dk(sb + oWXh, kk), dm(sb + oDh, kk), kIdKN128, acc);
-          tc::mma_bf16(tm + cDB, dk(sb + oWXl, kk), dm(sb + oDh, kk), kIdKN128, true);
-          tc::mma_bf16(tm + cDB, dk(sb + oWXh, kk), dm(sb + oDl, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDC, KD(oEYh, kk), MD(oHh, kk), kIdKN128, acc);
+          tc::mma_bf16(tm + cDC, KD(oEYl, kk), MD(oHh, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDC, KD(oEYh, kk), MD(oHl, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDB, KD(oWXh, kk), MD(oDh, kk), kIdKN128, acc);
+          tc::mma_bf16(tm + cDB, KD(oWXl, kk), MD(oDh, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDB, KD(oWXh, kk), MD(oDl, kk), kIdKN128, true);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          tc::mma_bf16(tm + cV, KD(oB, kk), KD(oDh, kk), kIdKK64, kk > 0);
+          tc::mma_bf16(tm + cV, KD(oB, kk), KD(oDl, kk), kIdKK64, true);
+          tc::mma_bf16(tm + cU, KD(oC, kk), KD(oHh, kk), kIdKK64, kk > 0);
+          tc::mma_bf16(tm + cU, KD(oC, kk), KD(oHl, kk), kIdKK64, true);
         }
         tc::mma_commit(&bars[2]);
       }
@@ -1667,7 +1689,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
             const int f = 4 * tt + 2 * hf + e;
             mv[e] = dv[e] = 0.f;
             if (j <= i && i < len) {
-              const float L = expf(cum[i] - cum[j]);
+              const float L = tc::fast_exp2(c2[i] - c2[j]);
               const float GL = gr[f] * L;
               mv[e] = GL * dts[j];
               dv[e] = sa[f] * L * dts[j];
@@ -1676,18 +1698,17 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
               if (i == j) mv[e] += Dd;
             }
           }
-          __nv_bfloat16 h0, h1, l0, l1;
+          uint32_t mh, ml, gh, gl;
+          split2rn(f2{mv[0], mv[1]}, mh, ml);
+          split2rn(f2{dv[0], dv[1]}, gh, gl);
           const uint32_t o = swo(i, c16 + 8 * tt + 2 * tq);
-          split_rn(mv[0], h0, l0);
-          split_rn(mv[1], h1, l1);
-          *reinterpret_cast<uint32_t*>(base + oMh + o) = pack_bf2(h0, h1);
-          *reinterpret_cast<uint32_t*>(base + oMl + o) = pack_bf2(l0, l1);
-          split_rn(dv[0], h0, l0);
-          split_rn(dv[1], h1, l1);
-          *reinterpret_cast<uint32_t*>(base + oGh + o) = pack_bf2(h0, h1);
-          *reinterpret_cast<uint32_t*>(base + oGl + o) = pack_bf2(l0, l1);
+          *reinterpret_cast<uint32_t*>(base + oMh + o) = mh;
+          *reinterpret_cast<uint32_t*>(base + oMl + o) = ml;
+          *reinterpret_cast<uint32_t*>(base + oGh + o) = gh;
+          *reinterpret_cast<uint32_t*>(base + oGl + o) = gl;
         }
       }
+      tc::fence_proxy_async_smem();
       if (cg <= qd) {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -1711,8 +1732,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
             }
           }
       }
-      tc::fence_proxy_async_smem();
-      if (w == 0 && hh + 1 < nh) tables(h + 1, (hh + 1) & 1);
+      if (w == 4 && hh + 1 < nh) tables(hh + 1);  // a warp whose dS block is masked
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -1721,15 +1741,19 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     // ---- group 2: Xi = M^T dY; dC += dG B; dB += dG^T C
     if (!math) {
       if (tc::elect_one()) {
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          tc::mma_bf16(tm + cX, dm(sb + oMh, kk), dm(sb + oYh, kk), kIdNN64, kk > 0);
-          tc::mma_bf16(tm + cX, dm(sb + oMl, kk), dm(sb + oYh, kk), kIdNN64, true);
-          tc::mma_bf16(tm + cX, dm(sb + oMh, kk), dm(sb + oYl, kk), kIdNN64, true);
-          tc::mma_bf16(tm + cDC, dk(sb + oGh, kk), dm(sb + oB, kk), kIdKN128, true);
-          tc::mma_bf16(tm + cDC, dk(sb + oGl, kk), dm(sb + oB, kk), kIdKN128, true);
-          tc::mma_bf16(tm + cDB, dm(sb + oGh, kk), dm(sb + oC, kk), kIdNN128, true);
-          tc::mma_bf16(tm + cDB, dm(sb + oGl, kk), dm(sb + oC, kk), kIdNN128, true);
+          tc::mma_bf16(tm + cX, MD(oMh, kk), MD(oYh, kk), kIdNN64, kk > 0);
+          tc::mma_bf16(tm + cX, MD(oMl, kk), MD(oYh, kk), kIdNN64, true);
+          tc::mma_bf16(tm + cX, MD(oMh, kk), MD(oYl, kk), kIdNN64, true);
+        }
+        tc::mma_commit(&bars[4]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          tc::mma_bf16(tm + cDC, KD(oGh, kk), MD(oB, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDC, KD(oGl, kk), MD(oB, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDB, MD(oGh, kk), MD(oC, kk), kIdNN128, true);
+          tc::mma_bf16(tm + cDB, MD(oGl, kk), MD(oC, kk), kIdNN128, true);
         }
         tc::mma_commit(&bars[3]);
       }
@@ -1751,12 +1775,13 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
         for (int hf = 0; hf < 2; ++hf) {
           const int r = r16 + gq + 8 * hf;
           const uint32_t o = swo(r, c16 + 8 * tt + 2 * tq);
-          const float2 xv = bf2_at(base + oX + o);
-          const float2 yh = bf2_at(base + oYh + o), yl = bf2_at(base + oYl + o);
+          const f2 xv = bf2_at(base + oX + o);
+          const f2 yv = tc::add2(bf2_at(base + oYh + o), bf2_at(base + oYl + o));
           const int f = 4 * tt + 2 * hf;
           vp[hf] += xv.x * va[f] + xv.y * va[f + 1];
-          zc[hf] += (yh.x + yl.x) * ua[f] + (yh.y + yl.y) * ua[f + 1];
+          zc[hf] += yv.x * ua[f] + yv.y * ua[f + 1];
         }
+      float wv_sum = 0.f;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float v = vp[hf], z = zc[hf];
@@ -1771,7 +1796,16 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
           wv_sum = fmaf(wt[r], v, wv_sum);
         }
       }
-      ok &= tc::mbar_wait(&bars[3], par);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wv_sum += __shfl_xor_sync(0xffffffffu, wv_sum, o);
+      if (lane == 0) atomicAdd(&hsum[4 * hh + 2], wv_sum);
+      // the next head's operands into registers
+      if (hh + 1 < nh) {
+        load_head(h + 1);
+        if (hh + 2 < nh) prefetch_head(h + 2);
+      }
+      // Xi (committed before the products into dC and dB)
+      ok &= tc::mbar_wait(&bars[4], par);
       tc::tc_fence_after();
       float xa[8];
       ld_frag2(tm + lanebase + cX + c16, xa);
@@ -1790,72 +1824,49 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
                 make_float2(fmaf(wj, va[f], xa[f]), fmaf(wj, va[f + 1], xa[f + 1]));
         }
       }
-      // the next head's operands into registers
-      if (hh + 1 < nh) {
-        load_head(h + 1);
-        if (hh + 2 < nh) prefetch_head(h + 2);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        hdot += __shfl_xor_sync(0xffffffffu, hdot, o);
-        wv_sum += __shfl_xor_sync(0xffffffffu, wv_sum, o);
-        dd += __shfl_xor_sync(0xffffffffu, dd, o);
-      }
-      if (lane == 0) {
-        red[w] = hdot;
-        red[16 + w] = wv_sum;
-        red[32 + w] = dd;
-      }
+      // group 2 complete before its operands are overwritten
+      ok &= tc::mbar_wait(&bars[3], par);
     }
     tc::tc_fence_before();
     __syncthreads();
-    // ---- warp 0: <dH, H>, sum_j w_j v_j, dD; ddt_j = direct terms + A
-    //      sum_{k>=j} dcum_k; dA += sum_j dt_j sum_{k>=j} dcum_k
-    if (w == 0) {
-      float a = lane < 16 ? red[lane] : 0.f, b = lane < 16 ? red[16 + lane] : 0.f,
-            d2 = lane < 16 ? red[32 + lane] : 0.f;
+  }
+  tc::tc_fence_after();
+  // ---- per head of the slice (warp hh): ddt_j = direct terms + A
+  //      sum_{k>=j} dcum_k, with the state terms <dH, H> and sum_j w_j v_j
+  //      at the last valid row; dA += sum_j dt_j sum_{k>=j} dcum_k; dD
+  if (math && w < nh) {
+    const int hh = w, h = hb + w;
+    const float* dts = dtsH + hh * kQb;
+    const float* dcum = dcumH + hh * kQb;
+    const float* ddd = dddH + hh * kQb;
+    const float extra = tc::fast_exp2(hsum[4 * hh]) * hsum[4 * hh + 1] + hsum[4 * hh + 2];
+    const int j1 = kQb - 1 - 2 * lane, j2 = j1 - 1;  // lane l: entries 63 - 2l, 62 - 2l
+    const float a1 = dcum[j1] + (j1 == len - 1 ? extra : 0.f);
+    const float a2 = dcum[j2] + (j2 == len - 1 ? extra : 0.f);
+    if (lane == 0 && p.dD) atomicAdd(p.dD + h, hsum[4 * hh + 3]);
+    float v = a1 + a2;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        a += __shfl_xor_sync(0xffffffffu, a, o);
-        b += __shfl_xor_sync(0xffffffffu, b, o);
-        d2 += __shfl_xor_sync(0xffffffffu, d2, o);
-      }
-      // reverse inclusive scan, lane l owning entries 63 - 2l and 62 - 2l;
-      // the state terms of the last valid row join it there
-      const int j1 = kQb - 1 - 2 * lane, j2 = j1 - 1;
-      const float extra = expf(last) * a + b;
-      const float a1 = dcum[j1] + (j1 == len - 1 ? extra : 0.f);
-      const float a2 = dcum[j2] + (j2 == len - 1 ? extra : 0.f);
-      const float q1 = ddd[j1], q2 = ddd[j2];
-      __syncwarp();
-      dcum[j1] = dcum[j2] = 0.f;
-      ddd[j1] = ddd[j2] = 0.f;
-      if (lane == 0 && p.dD) atomicAdd(p.dD + h, d2);
-      float v = a1 + a2;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      const float r2 = v, r1 = v - a2;
-      const float Ah = p.A[h];
-      float da = 0.f;
-      if (j1 < len) {
-        p.ddt[(k.tok0 + j1) * p.H + h] = q1 + Ah * r1;
-        da = fmaf(dts[j1], r1, da);
-      }
-      if (j2 < len) {
-        p.ddt[(k.tok0 + j2) * p.H + h] = q2 + Ah * r2;
-        da = fmaf(dts[j2], r2, da);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
-      if (lane == 0) atomicAdd(p.dA + h, da);
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
     }
+    const float r2 = v, r1 = v - a2;
+    const float Ah = p.A[h];
+    float da = 0.f;
+    if (j1 < len) {
+      p.ddt[(k.tok0 + j1) * p.H + h] = ddd[j1] + Ah * r1;
+      da = fmaf(dts[j1], r1, da);
+    }
+    if (j2 < len) {
+      p.ddt[(k.tok0 + j2) * p.H + h] = ddd[j2] + Ah * r2;
+      da = fmaf(dts[j2], r2, da);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
+    if (lane == 0) atomicAdd(p.dA + h, da);
   }
   // ---- dB, dC of the slice's heads (rows r16.., columns c32..)
   if (math) {
-    tc::tc_fence_after();
     float vc[16], vb[16];
     ld_frag4(tm + lanebase + cDC + c32, vc);
     ld_frag4(tm + lanebase + cDB + c32, vb);
@@ -1888,6 +1899,9 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     tc::tmem_dealloc(tm, 512);
   }
 }
+#undef KD
+#undef MD
+
 }  // namespace
 
 bool bwd_chunked_supported(int P, int N) {
