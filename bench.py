@@ -909,9 +909,11 @@ def measure_backward(fi, wl, dev, d, A, D, init, peaks, reps=3):
         device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream()
 
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
     def call():
         ssd.ssd_chunk_scan_bwd(d["x"], d["dt"], A, d["B"], d["C"], D, init, dy, workspace=ws,
-                               stream=stream)
+                               dev_status=status, stream=stream)
 
     call()
     torch.cuda.synchronize()
@@ -924,6 +926,8 @@ def measure_backward(fi, wl, dev, d, A, D, init, peaks, reps=3):
         e1.record(stream)
         torch.cuda.synchronize()
         us.append(1e3 * e0.elapsed_time(e1))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"backward: device status {int(status.item())}")
     med = statistics.median(us)
     es = 2 if wl.dtype == "bf16" else 4
     ntok = b * T

@@ -226,11 +226,21 @@ ssd_status_t ssd_state_update(float *state, const void *x, const void *dt, const
  *   dB, dC [ntok, ngroups, dstate]; dD [nheads] or NULL; dinit [batch,
  *   nheads, headdim, dstate] or NULL.
  * Workspace: ssd_chunk_scan_bwd_workspace_size(...) bytes, 256-byte
- *   aligned: one stored state every 64 steps and the 64 states of one
- *   chunk, per (batch row, head).
+ *   aligned, owned by the caller.  With headdim <= 64 and dstate <= 128
+ *   (the chunked path, 64-token chunks): the state entering each chunk and
+ *   the adjoint leaving it, [chunks][nheads][headdim][dstate] float32 each,
+ *   and one decay per (chunk, head); other shapes (the step-by-step path):
+ *   one stored state every 64 steps and the 64 states of one chunk, per
+ *   (batch row, head).
  * Supported: headdim * dstate <= 16384, either input dtype; no cu_seqlens.
- * All arithmetic is fp32.  One kernel launch plus the zeroing of dA, dB, dC
- * and dD.
+ * Arithmetic: fp32 accumulation.  On the chunked path the products run on
+ *   tensor cores with each fp32 operand as a pair of bf16 values (hi =
+ *   rn(v), lo = rn(v - hi)): warp MMAs for the chunk states, tcgen05 MMAs
+ *   for the gradients when the inputs are bf16 with headdim and dstate
+ *   multiples of 8 (CUDA cores otherwise).  Five kernel launches (one on the
+ *   step-by-step path) after the zeroing of dA, dB, dC and dD.
+ * dev_status: as for the forward (NULL allowed): a device wait that runs
+ *   out writes SSD_ERR_TIMEOUT there and the outputs are undefined.
  */
 size_t ssd_chunk_scan_bwd_workspace_size(int batch, int seqlen, int nheads, int headdim,
                                          int dstate, int ngroups, ssd_dtype_t in_dtype);
@@ -240,7 +250,7 @@ ssd_status_t ssd_chunk_scan_bwd(const void *x, const void *dt, const float *A, c
                                 const float *init_states, const float *dy, const float *dfinal,
                                 float *dx, float *ddt, float *dA, float *dB, float *dC, float *dD,
                                 float *dinit, void *workspace, size_t workspace_bytes,
-                                void *stream);
+                                int32_t *dev_status, void *stream);
 
 /*
  * ssd_chunk_scan_states -- the state at the end of each sequence, without

@@ -249,7 +249,7 @@ ssd_status_t ssd_chunk_scan_bwd(const void* x, const void* dt, const float* A, c
                                 const float* init_states, const float* dy, const float* dfinal,
                                 float* dx, float* ddt, float* dA, float* dB, float* dC, float* dD,
                                 float* dinit, void* workspace, size_t workspace_bytes,
-                                void* stream) {
+                                int32_t* dev_status, void* stream) {
   ssd_status_t st = check_bwd(in_dtype, batch, seqlen, nheads, headdim, dstate, ngroups);
   if (st != SSD_OK) return st;
   if (batch == 0) return SSD_OK;
@@ -285,6 +285,7 @@ ssd_status_t ssd_chunk_scan_bwd(const void* x, const void* dt, const float* A, c
   a.G = ngroups;
   a.dtype = in_dtype;
   a.ws = workspace;
+  a.dev_status = dev_status;
   a.stream = static_cast<cudaStream_t>(stream);
   return ssd::bwd(a);
 }

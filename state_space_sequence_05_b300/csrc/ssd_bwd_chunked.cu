@@ -33,19 +33,24 @@
 //           + A sum_{k>=j} dcum_k
 //   dA    = sum_j dt_j sum_{k>=j} dcum_k          (over every chunk)
 //
-// Kernels (all fp32 arithmetic):
-//   bwd_outer_kernel<F>  per (chunk, head): the chunk state sum_j w_j x_j B_j^T
-//                        and exp(cum_last);
-//   bwd_outer_kernel<R>  per (chunk, head): sum_i exp(cum_i) dy_i C_i^T;
+// Kernels (fp32 accumulation; the products on tensor cores take fp32
+// operands as bf16 hi/lo pairs, hi = rn(v), lo = rn(v - hi)):
+//   bwd_outer_kernel<F>  per (chunk, group, slice of up to 8 of the group's
+//                        heads): the chunk states sum_j w_j x_j B_j^T and
+//                        exp(cum_last), warp MMAs;
+//   bwd_outer_kernel<R>  the same for sum_i exp(cum_i) dy_i C_i^T;
 //   bwd_pass_kernel      per (row, head, state element): the states entering
 //                        each chunk (forwards) / the adjoints leaving each
 //                        chunk (backwards), in place; dinit;
-//   bwd_grad_kernel      per (chunk, group, slice of up to 8 of the group's
-//                        heads): every gradient above.  C B^T is formed once
-//                        per block; dB and dC (shared by a group's heads) are
-//                        summed over the slice in registers and then with
-//                        atomics, like dA and dD, into buffers the entry
-//                        point zeroed.
+//   bwd_grad_tc_kernel   per (chunk, group, slice of up to 8 heads), bf16
+//                        inputs with headdim and dstate multiples of 8:
+//                        every gradient above on tcgen05 MMAs (M = 64), dB
+//                        and dC summed over the slice in tensor memory;
+//   bwd_grad_kernel      the same on CUDA cores for fp32 inputs and other
+//                        shapes, dB and dC summed over the slice in
+//                        registers.
+// dB, dC, dA and dD are added with atomics into buffers the entry point
+// zeroed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -70,7 +75,7 @@ struct BP {
   const void *x, *dt, *B, *C;
   const float *A, *D, *init, *dy, *dfinal;
   float *dx, *ddt, *dA, *dB, *dC, *dD, *dinit;
-  int* status;  // SSD_ERR_TIMEOUT when a device wait runs out (may be null)
+  int32_t* status;  // SSD_ERR_TIMEOUT when a device wait runs out (may be null)
   float* st;   // [chunks][H][P N]: chunk states, then the states entering each chunk
   float* ad;   // [chunks][H][P N]: local adjoint sums, then the adjoints leaving each chunk
   float* dec;  // [chunks][H]: exp(cum_last)
@@ -249,8 +254,6 @@ __device__ __forceinline__ void store_split4(__nv_bfloat16* dh, __nv_bfloat16* d
   *reinterpret_cast<uint2*>(dh) = make_uint2(pack_bf2(h0, h1), pack_bf2(h2, h3));
   *reinterpret_cast<uint2*>(dl) = make_uint2(pack_bf2(l0, l1), pack_bf2(l2, l3));
 }
-
-__device__ __forceinline__ float bf_at(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
 // ---------------------------------------------------------------- outer sums
 // MODE 0: out = sum_j w_j x_j B_j^T, w_j = exp(cum_last - cum_j) dt_j, into p.st,
@@ -870,442 +873,6 @@ __global__ void __launch_bounds__(kThr) bwd_grad_kernel(BP p) {
         if (n < N) {
           atomicAdd(db + n, dba[r][s2]);
           atomicAdd(dc + n, dca[r][s2]);
-        }
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------- gradients, tensor cores
-// bf16 inputs with headdim and dstate multiples of 8: the products of the
-// gradient kernel above on warp MMAs.  Per block the operands live in shared
-// memory once, as bf16 (exact for the bf16 inputs x, B, C; hi/lo pairs for
-// the fp32 dy, H_c, dH_{c+1}, M and dG), padded to the full 64 x 64 and
-// 64 x 128 tiles with zeros; ldmatrix reads them in either orientation.  Warp
-// tiles (8 warps): dS and C B^T: rows 16 (w % 4), columns 32 (w / 4);
-// dx = M^T dy + w B dH^T: rows 16 (w % 4), columns 32 (w / 4); dC and dB
-// (with the state terms dy H and x dH): rows 16 (w % 4), columns 64 (w / 4).
-// C B^T stays in registers for the slice's heads, dB and dC likewise.  Blocks
-// of M and dG that the causal mask zeroes are skipped.
-constexpr int kThrG = 512;  // threads of the tensor-core gradient kernel
-constexpr size_t kGradMmaSmem = 6 * kT128 + 7 * kT64 + sizeof(float) * (8 * kQb + 8 * kThrG);
-
-__global__ void __launch_bounds__(kThrG, 1) bwd_grad_mma_kernel(BP p) {
-  extern __shared__ __align__(16) unsigned char gsm_raw[];
-  __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(gsm_raw);  // [64 j][136] B (exact)
-  __nv_bfloat16* Cs = Bs + kQb * kBP;                              // [64 i][136] C (exact)
-  __nv_bfloat16* Hh = Cs + kQb * kBP;                              // [64 q][136] H_c hi
-  __nv_bfloat16* Hl = Hh + kQb * kBP;                              //               lo
-  __nv_bfloat16* Dh = Hl + kQb * kBP;                              // [64 q][136] dH_{c+1} hi
-  __nv_bfloat16* Dl = Dh + kQb * kBP;                              //               lo
-  __nv_bfloat16* Xs = Dl + kQb * kBP;                              // [64 j][72] x (exact)
-  __nv_bfloat16* Yh = Xs + kQb * kAP;                              // [64 i][72] dy hi
-  __nv_bfloat16* Yl = Yh + kQb * kAP;                              //            lo
-  __nv_bfloat16* Mh = Yl + kQb * kAP;                              // [64 i][72] M hi
-  __nv_bfloat16* Ml = Mh + kQb * kAP;                              //            lo
-  __nv_bfloat16* Gh = Ml + kQb * kAP;                              // [64 i][72] dG hi
-  __nv_bfloat16* Gl = Gh + kQb * kAP;                              //            lo
-  float* cum = reinterpret_cast<float*>(Gl + kQb * kAP);           // [64]
-  float* dts = cum + kQb;                                          // [64] dt
-  float* ec = dts + kQb;                                           // [64] exp(cum_i)
-  float* wt = ec + kQb;                                            // [64] w_j
-  float* el = wt + kQb;                                            // [64] exp(cum_last - cum_j)
-  float* dcum = el + kQb;                                          // [64] dL/dcum
-  float* ddd = dcum + kQb;                                         // [64] direct dt terms
-  float* red = ddd + kQb;                                          // [48] block reductions
-  float* grs = red + kQb;  // [8][512] C B^T at each thread's dS fragment positions
-  const int c = blockIdx.x, g = blockIdx.y;
-  const Chunk k = chunk_of(p, c);
-  const int P = p.P, N = p.N, len = k.len;
-  const int hpg = p.H / p.G;
-  const int hb = g * hpg + blockIdx.z * kHS;
-  const int nh = min(kHS, hpg - blockIdx.z * kHS);
-  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int gq = lane >> 2, tq = lane & 3;
-  const LaneOff lo = lane_off(lane);
-  const int kq = (P + 15) & ~15;  // k extent over headdim
-  const int kn = (N + 15) & ~15;  // k extent over dstate
-  // shared addresses of the operand tiles: one base plus constant offsets
-  const uint32_t sb = tc::smem_u32(gsm_raw);
-  const uint32_t sBs = sb, sCs = sb + kT128, sHh = sb + 2 * kT128, sHl = sb + 3 * kT128,
-                 sDh = sb + 4 * kT128, sDl = sb + 5 * kT128, sXs = sb + 6 * kT128,
-                 sYh = sXs + kT64, sYl = sXs + 2 * kT64, sMh = sXs + 3 * kT64,
-                 sMl = sXs + 4 * kT64, sGh = sXs + 5 * kT64, sGl = sXs + 6 * kT64;
-  // warp tiles: row block rb (every SM sub-partition holds all four), column block cb
-  const int rb = w >> 2, cb = w & 3;
-  const int r16 = 16 * rb;
-  const int c16 = 16 * cb;  // columns of dS / C B^T and of dx
-  const int c32 = 32 * cb;  // columns of dC / dB
-  const __nv_bfloat16* xg = reinterpret_cast<const __nv_bfloat16*>(p.x);
-
-  // One head's x, dy, H_c, dH_{c+1} in registers (zero outside the valid
-  // rows, headdim and dstate), loaded a head ahead of their use.
-  uint4 vx;
-  float4 vy[2], vh[4], vd[4];
-  const auto load_head = [&](int h) {
-    const long long sOff = ((long long)c * p.H + h) * (long long)(P * N);
-    {
-      const int j = t >> 3, q = (t & 7) * 8;
-      vx = (j < len && q < P) ? *reinterpret_cast<const uint4*>(xg + ((k.tok0 + j) * p.H + h) * P + q)
-                              : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int e4 = t + kThrG * r, i = e4 >> 4, q = (e4 & 15) * 4;
-      vy[r] = (i < len && q < P)
-                  ? *reinterpret_cast<const float4*>(p.dy + ((k.tok0 + i) * p.H + h) * P + q)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e4 = t + kThrG * r, q = e4 >> 5, n = (e4 & 31) * 4;
-      const bool ok = q < P && n < N;
-      vh[r] = ok ? __ldcg(reinterpret_cast<const float4*>(p.st + sOff + q * N + n))
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
-      vd[r] = ok ? __ldcg(reinterpret_cast<const float4*>(p.ad + sOff + q * N + n))
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  };
-  // The operands of head h into L2 (a head before their register loads).
-  const auto prefetch_head = [&](int h) {
-    const long long sOff = ((long long)c * p.H + h) * (long long)(P * N);
-    if (t == 0) {
-      tc::bulk_prefetch_l2(p.st + sOff, (uint32_t)(P * N * 4));
-      tc::bulk_prefetch_l2(p.ad + sOff, (uint32_t)(P * N * 4));
-    } else if (t >= 32 && t < 32 + kQb && t - 32 < len) {
-      const long long row = (k.tok0 + (t - 32)) * p.H + h;
-      tc::prefetch_l2(xg + row * P);
-      tc::prefetch_l2(p.dy + row * P);
-      if (P > 32) tc::prefetch_l2(p.dy + row * P + 32);
-    }
-  };
-  // Warp 0: the decay tables of head h (lane l holds entries 2l and 2l+1),
-  // dcum and ddd cleared.
-  const auto tables = [&](int h) {
-    const float Ah = p.A[h];
-    const int j0 = 2 * lane, j1 = j0 + 1;
-    const float d0 = j0 < len ? ldin<true>(p.dt, (k.tok0 + j0) * p.H + h) : 0.f;
-    const float d1 = j1 < len ? ldin<true>(p.dt, (k.tok0 + j1) * p.H + h) : 0.f;
-    const float a1 = d1 * Ah;
-    float s = d0 * Ah + a1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float u = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += u;
-    }
-    const float cm1 = s, cm0 = s - a1;
-    const float lst = __shfl_sync(0xffffffffu, ((len - 1) & 1) ? cm1 : cm0, (len - 1) >> 1);
-    cum[j0] = cm0;
-    cum[j1] = cm1;
-    dts[j0] = d0;
-    dts[j1] = d1;
-    ec[j0] = expf(cm0);
-    ec[j1] = expf(cm1);
-    const float e0 = expf(lst - cm0), e1 = expf(lst - cm1);
-    el[j0] = e0;
-    el[j1] = e1;
-    wt[j0] = e0 * d0;
-    wt[j1] = e1 * d1;
-    dcum[j0] = dcum[j1] = 0.f;
-    ddd[j0] = ddd[j1] = 0.f;
-  };
-
-  // ---- prologue: B, C rows of the chunk; the first head's operands and tables
-  {
-    const __nv_bfloat16* Bg = reinterpret_cast<const __nv_bfloat16*>(p.B);
-    const __nv_bfloat16* Cg = reinterpret_cast<const __nv_bfloat16*>(p.C);
-    uint4 vb[2], vc[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int e8 = t + kThrG * r, j = e8 >> 4, n = (e8 & 15) * 8;
-      const bool ok = j < len && n < N;
-      const long long i = ((k.tok0 + j) * p.G + g) * N + n;
-      vb[r] = ok ? *reinterpret_cast<const uint4*>(Bg + i) : make_uint4(0, 0, 0, 0);
-      vc[r] = ok ? *reinterpret_cast<const uint4*>(Cg + i) : make_uint4(0, 0, 0, 0);
-    }
-    load_head(hb);
-    if (nh > 1) prefetch_head(hb + 1);
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int e8 = t + kThrG * r, j = e8 >> 4, n = (e8 & 15) * 8;
-      *reinterpret_cast<uint4*>(Bs + j * kBP + n) = vb[r];
-      *reinterpret_cast<uint4*>(Cs + j * kBP + n) = vc[r];
-    }
-    if (w == 0) tables(hb);
-  }
-  __syncthreads();
-  // G = C B^T at the dS tile's positions (rows r16.., columns c16..)
-  {
-    float gr[2][4];
-    zero_acc(gr);
-    warp_mma<2, kBP, false, false, kBP, false, false>(gr, gr, sCs, 0, r16, sBs, 0, c16, 0, kn, lo);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) grs[e * kThrG + t] = gr[e >> 2][e & 3];
-  }
-
-  float dca[4][4], dba[4][4];  // dC (rows i), dB (rows j): rows r16.., columns c32..
-  zero_acc(dca);
-  zero_acc(dba);
-
-  for (int hh = 0; hh < nh; ++hh) {
-    const int h = hb + hh;
-    const float Dd = p.D ? p.D[h] : 0.f;
-    // ---- operands to shared memory (the previous head's readers passed the
-    //      last barrier)
-    float hdot = 0.f;
-    {
-      const int j = t >> 3, q = (t & 7) * 8;
-      *reinterpret_cast<uint4*>(Xs + j * kAP + q) = vx;
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int e4 = t + kThrG * r, i = e4 >> 4, q = (e4 & 15) * 4;
-      store_split4(Yh + i * kAP + q, Yl + i * kAP + q, vy[r]);
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e4 = t + kThrG * r, q = e4 >> 5, n = (e4 & 31) * 4;
-      store_split4(Hh + q * kBP + n, Hl + q * kBP + n, vh[r]);
-      store_split4(Dh + q * kBP + n, Dl + q * kBP + n, vd[r]);
-      hdot += vh[r].x * vd[r].x + vh[r].y * vd[r].y + vh[r].z * vd[r].z + vh[r].w * vd[r].w;
-    }
-    __syncthreads();
-    const float last = cum[len - 1];
-
-    // ---- dS = dY X^T; M = G L dt, dG = dS L dt; the decay terms of the
-    //      quadratic form (rows r16.., columns c16..)
-    {
-      float sa[2][4], sl[2][4];
-      zero_acc(sa);
-      zero_acc(sl);
-      if (cb <= rb)
-        warp_mma<2, kAP, false, true, kAP, false, false>(sa, sl, sYh, sYl, r16, sXs, 0, c16, 0, kq, lo);
-      float rowT[2] = {0.f, 0.f}, colT[2][2], colU[2][2];
-#pragma unroll
-      for (int tt = 0; tt < 2; ++tt) {
-        colT[tt][0] = colT[tt][1] = colU[tt][0] = colU[tt][1] = 0.f;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int i = r16 + gq + 8 * hf;
-          float mv[2], dv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int j = c16 + 8 * tt + 2 * tq + e;
-            mv[e] = dv[e] = 0.f;
-            if (j <= i && i < len) {
-              const float L = expf(cum[i] - cum[j]);
-              const float sv = sa[tt][2 * hf + e] + sl[tt][2 * hf + e];
-              const float GL = grs[(4 * tt + 2 * hf + e) * kThrG + t] * L;
-              mv[e] = GL * dts[j];
-              dv[e] = sv * L * dts[j];
-              const float T = sv * mv[e];
-              rowT[hf] += T;
-              colT[tt][e] += T;
-              colU[tt][e] += sv * GL;
-            }
-          }
-          __nv_bfloat16 h0, h1, l0, l1;
-          const int at = i * kAP + c16 + 8 * tt + 2 * tq;
-          split_rn(mv[0], h0, l0);
-          split_rn(mv[1], h1, l1);
-          *reinterpret_cast<uint32_t*>(Mh + at) = pack_bf2(h0, h1);
-          *reinterpret_cast<uint32_t*>(Ml + at) = pack_bf2(l0, l1);
-          split_rn(dv[0], h0, l0);
-          split_rn(dv[1], h1, l1);
-          *reinterpret_cast<uint32_t*>(Gh + at) = pack_bf2(h0, h1);
-          *reinterpret_cast<uint32_t*>(Gl + at) = pack_bf2(l0, l1);
-        }
-      }
-      if (cb <= rb) {
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float v = rowT[hf];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          if (tq == 0) atomicAdd(&dcum[r16 + gq + 8 * hf], v);
-        }
-#pragma unroll
-        for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float a = colT[tt][e], b = colU[tt][e];
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-              a += __shfl_xor_sync(0xffffffffu, a, o);
-              b += __shfl_xor_sync(0xffffffffu, b, o);
-            }
-            if (gq == 0) {
-              const int j = c16 + 8 * tt + 2 * tq + e;
-              atomicAdd(&dcum[j], -a);
-              atomicAdd(&ddd[j], b);
-            }
-          }
-      }
-    }
-    __syncthreads();
-
-    // ---- dx = M^T dY + w_j dH B_j + D dy (rows j = r16.., columns q = c16..)
-    float wv_sum = 0.f, dd = 0.f;
-    {
-      float xa[2][4], va[2][4];
-      zero_acc(xa);
-      zero_acc(va);
-      if (c16 < P) {
-        warp_mma<2, kAP, true, true, kAP, true, true>(xa, xa, sMh, sMl, r16, sYh, sYl, c16, r16, kQb, lo);
-        warp_mma<2, kBP, false, false, kBP, false, true>(va, va, sBs, 0, r16, sDh, sDl, c16, 0, kn, lo);
-      }
-      float vp[2] = {0.f, 0.f};
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int j = r16 + gq + 8 * hf;
-        const float wj = wt[j];
-#pragma unroll
-        for (int tt = 0; tt < 2; ++tt) {
-          const int q = c16 + 8 * tt + 2 * tq;
-          const int at = j * kAP + q;
-          const float y0 = bf_at(Yh + at) + bf_at(Yl + at);
-          const float y1 = bf_at(Yh + at + 1) + bf_at(Yl + at + 1);
-          const float x0 = bf_at(Xs + at), x1 = bf_at(Xs + at + 1);
-          const float v0 = va[tt][2 * hf], v1 = va[tt][2 * hf + 1];
-          vp[hf] += x0 * v0 + x1 * v1;
-          dd += x0 * y0 + x1 * y1;
-          if (j < len && q < P) {
-            float2 o;
-            o.x = xa[tt][2 * hf] + wj * v0 + Dd * y0;
-            o.y = xa[tt][2 * hf + 1] + wj * v1 + Dd * y1;
-            *reinterpret_cast<float2*>(p.dx + ((k.tok0 + j) * p.H + h) * P + q) = o;
-          }
-        }
-      }
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float v = vp[hf];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        const int j = r16 + gq + 8 * hf;
-        if (tq == 0 && j < len) {
-          atomicAdd(&dcum[j], -wt[j] * v);
-          atomicAdd(&ddd[j], el[j] * v);
-          wv_sum = fmaf(wt[j], v, wv_sum);
-        }
-      }
-    }
-
-    // ---- dC += dG B + exp(cum_i) dY H; dB += dG^T C + w_j X dH
-    //      (rows r16.., columns n = c32..)
-    if (c32 < N) {
-      warp_mma<4, kAP, false, true, kBP, true, false>(dca, dca, sGh, sGl, r16, sBs, 0, c32, 0, r16 + 16, lo);
-      float ta[4][4];
-      zero_acc(ta);
-      warp_mma<4, kAP, false, true, kBP, true, true>(ta, ta, sYh, sYl, r16, sHh, sHl, c32, 0, kq, lo);
-      float zc[2] = {0.f, 0.f};
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int i = r16 + gq + 8 * hf;
-        const float e = ec[i];
-#pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-          const int n = c32 + 8 * tt + 2 * tq;
-          const float z0 = e * ta[tt][2 * hf], z1 = e * ta[tt][2 * hf + 1];
-          dca[tt][2 * hf] += z0;
-          dca[tt][2 * hf + 1] += z1;
-          zc[hf] += z0 * bf_at(Cs + i * kBP + n) + z1 * bf_at(Cs + i * kBP + n + 1);
-        }
-      }
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float v = zc[hf];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        if (tq == 0) atomicAdd(&dcum[r16 + gq + 8 * hf], v);
-      }
-      warp_mma<4, kAP, true, true, kBP, true, false>(dba, dba, sGh, sGl, r16, sCs, 0, c32, r16, kQb, lo);
-      zero_acc(ta);
-      warp_mma<4, kAP, false, false, kBP, true, true>(ta, ta, sXs, 0, r16, sDh, sDl, c32, 0, kq, lo);
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const float wj = wt[r16 + gq + 8 * hf];
-#pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-          dba[tt][2 * hf] = fmaf(wj, ta[tt][2 * hf], dba[tt][2 * hf]);
-          dba[tt][2 * hf + 1] = fmaf(wj, ta[tt][2 * hf + 1], dba[tt][2 * hf + 1]);
-        }
-      }
-    }
-
-    // ---- the next head's operands into registers; block sums
-    if (hh + 1 < nh) {
-      load_head(h + 1);
-      if (hh + 2 < nh) prefetch_head(h + 2);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      hdot += __shfl_xor_sync(0xffffffffu, hdot, o);
-      wv_sum += __shfl_xor_sync(0xffffffffu, wv_sum, o);
-      dd += __shfl_xor_sync(0xffffffffu, dd, o);
-    }
-    if (lane == 0) {
-      red[w] = hdot;
-      red[16 + w] = wv_sum;
-      red[32 + w] = dd;
-    }
-    __syncthreads();
-    // ---- warp 0: <dH, H>, sum_j w_j v_j, dD; ddt_j = direct terms + A
-    //      sum_{k>=j} dcum_k; dA += sum_j dt_j sum_{k>=j} dcum_k; then the
-    //      next head's tables
-    if (w == 0) {
-      float a = lane < 16 ? red[lane] : 0.f, b = lane < 16 ? red[16 + lane] : 0.f,
-            d2 = lane < 16 ? red[32 + lane] : 0.f;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {  // every lane gets the sums
-        a += __shfl_xor_sync(0xffffffffu, a, o);
-        b += __shfl_xor_sync(0xffffffffu, b, o);
-        d2 += __shfl_xor_sync(0xffffffffu, d2, o);
-      }
-      // reverse inclusive scan, lane l owning entries 63 - 2l and 62 - 2l;
-      // the state terms of the last valid row join it there
-      const int j1 = kQb - 1 - 2 * lane, j2 = j1 - 1;
-      const float extra = expf(last) * a + b;
-      const float a1 = dcum[j1] + (j1 == len - 1 ? extra : 0.f);
-      const float a2 = dcum[j2] + (j2 == len - 1 ? extra : 0.f);
-      if (lane == 0 && p.dD) atomicAdd(p.dD + h, d2);
-      float v = a1 + a2;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      const float r2 = v, r1 = v - a2;
-      const float Ah = p.A[h];
-      float da = 0.f;
-      if (j1 < len) {
-        p.ddt[(k.tok0 + j1) * p.H + h] = ddd[j1] + Ah * r1;
-        da = fmaf(dts[j1], r1, da);
-      }
-      if (j2 < len) {
-        p.ddt[(k.tok0 + j2) * p.H + h] = ddd[j2] + Ah * r2;
-        da = fmaf(dts[j2], r2, da);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
-      if (lane == 0) atomicAdd(p.dA + h, da);
-      __syncwarp();
-      if (hh + 1 < nh) tables(h + 1);
-    }
-  }
-  // dB, dC of the slice's heads
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    const int j = r16 + gq + 8 * hf;
-    if (j < len) {
-      float* db = p.dB + ((k.tok0 + j) * p.G + g) * N;
-      float* dc = p.dC + ((k.tok0 + j) * p.G + g) * N;
-#pragma unroll
-      for (int tt = 0; tt < 4; ++tt) {
-        const int n = c32 + 8 * tt + 2 * tq;
-        if (n < N) {
-          atomicAdd(reinterpret_cast<float2*>(db + n), make_float2(dba[tt][2 * hf], dba[tt][2 * hf + 1]));
-          atomicAdd(reinterpret_cast<float2*>(dc + n), make_float2(dca[tt][2 * hf], dca[tt][2 * hf + 1]));
         }
       }
     }
@@ -1933,7 +1500,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   p.dC = a.dC;
   p.dD = a.dD;
   p.dinit = a.dinit;
-  p.status = nullptr;
+  p.status = a.dev_status;
   p.T = a.seqlen;
   p.H = a.H;
   p.P = a.P;
@@ -1955,7 +1522,6 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   std::call_once(attr_once, [] {
     const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
     if (cudaFuncSetAttribute(bwd_grad_kernel<true>, at, (int)kGradSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(bwd_grad_mma_kernel, at, (int)kGradMmaSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_grad_tc_kernel, at, (int)tg::kSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_grad_kernel<false>, at, (int)kGradSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_outer_kernel<true, 0>, at, (int)outer_smem<true>()) != cudaSuccess ||

@@ -110,6 +110,7 @@ struct BwdArgs {
   int batch, seqlen, H, P, N, G;
   ssd_dtype_t dtype;
   void* ws;
+  int32_t* dev_status;  // may be null
   cudaStream_t stream;
 };
 size_t bwd_workspace_bytes(int batch, int T, int H, int P, int N);

@@ -51,7 +51,8 @@ SIGNATURES = {
                                      _fp, _fp, _vp]),
     "ssd_chunk_scan_bwd_workspace_size": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci, _ci]),
     "ssd_chunk_scan_bwd": (_ci, [_vp, _vp, _fp, _vp, _vp, _fp, _ci, _ci, _ci, _ci, _ci, _ci, _ci,
-                                 _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _vp, _sz, _vp]),
+                                 _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _vp, _sz, _ip,
+                                 _vp]),
     "ssd_segment_decay": (_ci, [_vp, _fp, _ci, _ci, _ci, _ci, _fp, _vp]),
     "ssd_segment_combine": (_ci, [_fp, _fp, _fp, _ci, _ci, _ci, _ci, _ci, _fp, _vp]),
     "ssd_status_string": (ctypes.c_char_p, [_ci]),
@@ -393,11 +394,12 @@ def ssd_segment_combine(decay, states, init_states=None, *, out=None, stream=Non
 
 
 def ssd_chunk_scan_bwd(x, dt, A, B, C, D, init_states, dy, dfinal=None, *, workspace=None,
-                       want_dD=True, want_dinit=True, stream=None):
+                       want_dD=True, want_dinit=True, dev_status=None, stream=None):
     """Backward of the forward (batch mode).  x, dt, A, B, C, D, init_states
     as for ssd_chunk_scan_fwd; dy [b, T, H, P] float32; dfinal [b, H, P, N]
-    float32 or None.  Returns a dict of float32 gradients dx, ddt, dA, dB, dC
-    and (unless disabled) dD and dinit."""
+    float32 or None; dev_status an int32 device tensor (or None) that
+    receives device-side errors.  Returns a dict of float32 gradients dx,
+    ddt, dA, dB, dC and (unless disabled) dD and dinit."""
     lib = load_library()
     dev = x.device
     if dev.type != "cuda" or x.dim() != 4 or B.dim() != 4:
@@ -433,7 +435,7 @@ def ssd_chunk_scan_bwd(x, dt, A, B, C, D, init_states, dy, dfinal=None, *, works
                                 N, G, code, _ptr(init_states), _ptr(dy), _ptr(dfinal),
                                 _ptr(g["dx"]), _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]),
                                 _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dinit"]), _ptr(workspace),
-                                ws_bytes, _stream_handle(stream))
+                                ws_bytes, _ptr(dev_status), _stream_handle(stream))
     if st != SSD_OK:
         raise SSDError(st, "ssd_chunk_scan_bwd")
     return g

@@ -120,7 +120,7 @@ def test_host_side_rejections_of_the_other_entry_points(lib):
     def bwd(dtype=0, H=2, P=16, N=16, G=1, ws=None, ws_bytes=0):
         return lib.ssd_chunk_scan_bwd(fake, fake, fake, fake, fake, None, 1, 16, H, P, N, G, dtype,
                                       None, fake, None, fake, fake, fake, fake, fake, None, None,
-                                      ws, ws_bytes, None)
+                                      ws, ws_bytes, None, None)
     assert bwd(dtype=7) == ssd.SSD_ERR_INVALID
     assert bwd(H=3, G=2) == ssd.SSD_ERR_INVALID
     assert bwd(P=129, N=128) == ssd.SSD_ERR_UNSUPPORTED

@@ -40,9 +40,11 @@ def _check(wl, use_D=True, use_init=True, use_dfinal=True, seed=0):
     dfin = rng.standard_normal((b, H, P, N)).astype(np.float32) if use_dfinal else None
     init = fi.init if use_init else None
     t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     g = ssd.ssd_chunk_scan_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"] if use_D else None,
-                               t(init), t(dy), t(dfin))
+                               t(init), t(dy), t(dfin), dev_status=status)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0
     ref = oracle.ssd_bwd(fi.x, fi.dt, fi.A, fi.B, fi.C, fi.D if use_D else None, init, dy, dfin)
     errs = {}
     for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dinit"):
