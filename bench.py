@@ -29,6 +29,7 @@ path) and ``value`` is the sum over ranks divided by the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -64,6 +65,11 @@ def parse_args():
                     help="skip the other tensor-core forwards and the states-only pass")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the l2k_b4 / l64k / varlen64 forward measurements")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the backward on the workload (--steps calls) and print its "
+                         "JSON object (for profiling runs)")
+    ap.add_argument("--bwd-seqlen", type=int, default=0,
+                    help="with --backward-only: the workload's shape at this sequence length")
     return ap.parse_args()
 
 
@@ -348,12 +354,19 @@ def main():
     ssd.load_library()
 
     wl = I.WORKLOADS[args.workload]
+    if args.backward_only and args.bwd_seqlen > 0:
+        wl = dataclasses.replace(wl, name=f"{wl.name}@T{args.bwd_seqlen}", seqlen=args.bwd_seqlen)
     fi = I.make_forward_inputs(wl)
     wl = fi.wl
     d = {k: I.as_torch(getattr(fi, k), fi.bits.get(k), dev, wl.dtype) for k in ("x", "dt", "B", "C")}
     A = torch.from_numpy(fi.A).to(dev)
     D = torch.from_numpy(fi.D).to(dev)
     init = None if fi.init is None else torch.from_numpy(fi.init).to(dev)
+    if args.backward_only:
+        peaks, _ = load_peaks()
+        print(json.dumps({"backward": measure_backward(fi, wl, dev, d, A, D, init, peaks,
+                                                       reps=max(1, args.steps))}), flush=True)
+        return
     cu = None if fi.cu_seqlens is None else torch.from_numpy(fi.cu_seqlens).to(dev)
     nseq = fi.nseq
     H, P, N, G = wl.nheads, wl.headdim, wl.dstate, wl.ngroups
