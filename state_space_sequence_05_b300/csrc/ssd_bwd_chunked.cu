@@ -79,6 +79,7 @@ struct BP {
   float* st;   // [chunks][H][P N]: chunk states, then the states entering each chunk
   float* ad;   // [chunks][H][P N]: local adjoint sums, then the adjoints leaving each chunk
   float* dec;  // [chunks][H]: exp(cum_last)
+  float* tab;  // [chunks][H][144] (tensor-core path): forward weights, adjoint weights, decay
   int T, H, P, N, G, nc;  // nc: chunks per batch row
   int vec;  // rows of x, dy, B, C move as 16-byte vectors (headdim, dstate multiples of 8)
 };
@@ -884,9 +885,10 @@ __global__ void __launch_bounds__(kThr) bwd_grad_kernel(BP p) {
 // headdim and dstate multiples of 8).  Per block (chunk, group, slice of up
 // to kHS heads of the group), 16 math warps and one MMA warp.  Operands are
 // 128-byte-swizzled bf16 tiles of 64 rows (exact for x, B, C; hi/lo pairs
-// for dy, exp(cum) dy, w x, H_c, dH_{c+1}, M and dG), zero-padded to headdim
-// 64 and dstate 128, read by the MMAs K-major or MN-major as each product
-// needs.  Accumulators (M = 64: row r in TMEM lane 32 (r / 16) + r % 16):
+// for dy, exp(cum) dy, w x, H_c, dH_{c+1}, M and dG; H_c and dH_{c+1} as
+// stored by the state scans, transposed: 128 rows of dstate), zero-padded to
+// headdim 64 and dstate 128, read by the MMAs K-major or MN-major as each
+// product needs.  Accumulators (M = 64: row r in TMEM lane 32 (r / 16) + r % 16):
 //   dC (128 columns) += exp(cum) dY H + dG B       summed over the slice's heads
 //   dB (128 columns) += (w o X) dH + dG^T C
 //   S  = dY X^T (the first head's C B^T before it)   V = B dH^T
@@ -918,6 +920,8 @@ constexpr uint32_t kIdKK64 = tc::idesc_bf16(64, 64, false, false);
 constexpr uint32_t kIdNN64 = tc::idesc_bf16(64, 64, true, true);
 constexpr uint32_t kIdKN128 = tc::idesc_bf16(64, 128, false, true);
 constexpr uint32_t kIdNN128 = tc::idesc_bf16(64, 128, true, true);
+constexpr uint32_t kIdKK128 = tc::idesc_bf16(64, 128, false, false);
+constexpr uint32_t kIdKN64 = tc::idesc_bf16(64, 64, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 
 // byte offset of element (r, c) of a 64-row tile made of 64-column atoms
@@ -1012,8 +1016,9 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
 
   // One head's x, dy, H_c, dH_{c+1} in registers (zero outside the valid
   // rows, headdim and dstate), loaded a head ahead of their use.  Math
-  // thread t: x and dy of row t / 8, columns 8 (t % 8)..; float4 r of H and
-  // dH at row (t + 512 r) / 32, columns 4 ((t + 512 r) % 32)..
+  // thread t: x and dy of row t / 8, columns 8 (t % 8)..; float4 r of the
+  // transposed H and dH ([n][q]) at row (t + 512 r) / 16, columns
+  // 4 ((t + 512 r) % 16)..
   uint4 vx = make_uint4(0, 0, 0, 0);
   float4 vy[2], vh[4], vd[4];
   const auto load_head = [&](int h) {
@@ -1026,11 +1031,11 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     vy[1] = okr ? *reinterpret_cast<const float4*>(p.dy + row + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int e4 = t + kMathThreads * r, qq = e4 >> 5, n = (e4 & 31) * 4;
-      const bool okh = qq < P && n < N;
-      vh[r] = okh ? __ldcg(reinterpret_cast<const float4*>(p.st + sOff + qq * N + n))
+      const int e4 = t + kMathThreads * r, n = e4 >> 4, qq = (e4 & 15) * 4;
+      const bool okh = n < N && qq < P;
+      vh[r] = okh ? __ldcg(reinterpret_cast<const float4*>(p.st + sOff + n * P + qq))
                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      vd[r] = okh ? __ldcg(reinterpret_cast<const float4*>(p.ad + sOff + qq * N + n))
+      vd[r] = okh ? __ldcg(reinterpret_cast<const float4*>(p.ad + sOff + n * P + qq))
                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
@@ -1180,8 +1185,8 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
       f2 hd2{0.f, 0.f};
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int e4 = t + kMathThreads * r, qq = e4 >> 5, n = (e4 & 31) * 4;
-        const uint32_t o = swo(qq, n);
+        const int e4 = t + kMathThreads * r, n = e4 >> 4, qq = (e4 & 15) * 4;
+        const uint32_t o = swo(n, qq);
         split4_at(base + oHh + o, base + oHl + o, vh[r]);
         split4_at(base + oDh + o, base + oDl + o, vd[r]);
         hd2 = tc::fma2(f2{vh[r].x, vh[r].y}, f2{vd[r].x, vd[r].y}, hd2);
@@ -1216,19 +1221,19 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const bool acc = hh > 0 || kk > 0;
-          tc::mma_bf16(tm + cDC, KD(oEYh, kk), MD(oHh, kk), kIdKN128, acc);
-          tc::mma_bf16(tm + cDC, KD(oEYl, kk), MD(oHh, kk), kIdKN128, true);
-          tc::mma_bf16(tm + cDC, KD(oEYh, kk), MD(oHl, kk), kIdKN128, true);
-          tc::mma_bf16(tm + cDB, KD(oWXh, kk), MD(oDh, kk), kIdKN128, acc);
-          tc::mma_bf16(tm + cDB, KD(oWXl, kk), MD(oDh, kk), kIdKN128, true);
-          tc::mma_bf16(tm + cDB, KD(oWXh, kk), MD(oDl, kk), kIdKN128, true);
+          tc::mma_bf16(tm + cDC, KD(oEYh, kk), KD(oHh, kk), kIdKK128, acc);
+          tc::mma_bf16(tm + cDC, KD(oEYl, kk), KD(oHh, kk), kIdKK128, true);
+          tc::mma_bf16(tm + cDC, KD(oEYh, kk), KD(oHl, kk), kIdKK128, true);
+          tc::mma_bf16(tm + cDB, KD(oWXh, kk), KD(oDh, kk), kIdKK128, acc);
+          tc::mma_bf16(tm + cDB, KD(oWXl, kk), KD(oDh, kk), kIdKK128, true);
+          tc::mma_bf16(tm + cDB, KD(oWXh, kk), KD(oDl, kk), kIdKK128, true);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          tc::mma_bf16(tm + cV, KD(oB, kk), KD(oDh, kk), kIdKK64, kk > 0);
-          tc::mma_bf16(tm + cV, KD(oB, kk), KD(oDl, kk), kIdKK64, true);
-          tc::mma_bf16(tm + cU, KD(oC, kk), KD(oHh, kk), kIdKK64, kk > 0);
-          tc::mma_bf16(tm + cU, KD(oC, kk), KD(oHl, kk), kIdKK64, true);
+          tc::mma_bf16(tm + cV, KD(oB, kk), MD(oDh, kk), kIdKN64, kk > 0);
+          tc::mma_bf16(tm + cV, KD(oB, kk), MD(oDl, kk), kIdKN64, true);
+          tc::mma_bf16(tm + cU, KD(oC, kk), MD(oHh, kk), kIdKN64, kk > 0);
+          tc::mma_bf16(tm + cU, KD(oC, kk), MD(oHl, kk), kIdKN64, true);
         }
         tc::mma_commit(&bars[2]);
       }
@@ -1469,6 +1474,281 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
 #undef KD
 #undef MD
 
+// ---------------------------------------------------------------- state scans, tcgen05
+// The states entering each chunk (forwards from init) and the adjoints
+// leaving each chunk (backwards from dL/dfinal) for the tcgen05 gradient
+// kernel: one block per (head, batch row, direction) walks the row's chunks
+// in order with the state in registers, so every state is written once.
+// Storage is transposed: st, ad [chunk][head][n][q] (dstate rows of headdim
+// values); dinit [batch][head][q][n].  Per chunk the local sum
+//   forwards:  sum_j B_j (w_j x_j)^T,       w_j = exp(cum_last - cum_j) dt_j
+//   backwards: sum_i C_i (exp(cum_i) dy_i)^T
+// is one M = 128 (n) x N = 128 tcgen05 product over the chunk's 64 tokens:
+// B^T (or C^T) read MN-major, times the weighted rows as [hi | lo] (64
+// columns each, MN-major); the state then becomes exp(cum_last) state + hi +
+// lo.  Warps 0-3 hold the state (row n = TMEM lane n) and write it out
+// through a padded shared-memory stage as coalesced rows, warps 4-7 stage and
+// convert the operands of a two-slot ring, warp 8 issues the MMAs into a
+// double-buffered accumulator.  Every wait is bounded (SSD_ERR_TIMEOUT).
+namespace sc {
+constexpr int kStages = 2;
+constexpr uint32_t kAtom = 8192;        // 64 rows x 128 bytes
+constexpr uint32_t kSlotBytes = 4 * kAtom;  // U hi, U lo (64 tokens x 64 q), V (64 tokens x 128 n)
+constexpr int kThreads = 32 * 9;
+constexpr int kTabF = 144;  // floats per (chunk, head) of the weight table
+constexpr uint32_t oTab = kStages * kSlotBytes;  // [2][64] the slots' row weights
+constexpr uint32_t kStgPitch = 272;              // bytes per staged state row (256 + 16: no bank conflicts)
+constexpr uint32_t oStg = oTab + kStages * 256;  // [128][272 B] the state rows on their way out
+constexpr uint32_t oBar = oStg + 128 * kStgPitch;  // full[2], empty[2], acc full[2], acc free[2]; TMEM base
+constexpr uint32_t kSmem = oBar + 128 + 1024;
+constexpr uint32_t kId = tc::idesc_bf16(128, 128, true, true);
+}  // namespace sc
+
+// The weight table of the tensor-core path, per (chunk, head): the forward
+// weights w_j = exp(cum_last - cum_j) dt_j in [0, 64), the adjoint weights
+// exp(cum_i) in [64, 128), exp(cum_last) at 128 (rows past the chunk's end
+// have dt = 0).  One warp per head, lane l on rows 2l and 2l + 1.
+__global__ void __launch_bounds__(256) bwd_tab_kernel(BP p) {
+  const int c = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 8 + w;
+  if (h >= p.H) return;
+  const Chunk k = chunk_of(p, c);
+  const float Ah2 = p.A[h] * tg::kLog2e;
+  const int j0 = 2 * lane, j1 = j0 + 1;
+  const float d0 = j0 < k.len ? ldin<true>(p.dt, (k.tok0 + j0) * p.H + h) : 0.f;
+  const float d1 = j1 < k.len ? ldin<true>(p.dt, (k.tok0 + j1) * p.H + h) : 0.f;
+  const float a1 = d1 * Ah2;
+  float sum = d0 * Ah2 + a1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float u = __shfl_up_sync(0xffffffffu, sum, o);
+    if (lane >= o) sum += u;
+  }
+  const float cm1 = sum, cm0 = sum - a1;
+  const float lst = __shfl_sync(0xffffffffu, ((k.len - 1) & 1) ? cm1 : cm0, (k.len - 1) >> 1);
+  float* row = p.tab + ((long long)c * p.H + h) * sc::kTabF;
+  row[j0] = tc::fast_exp2(lst - cm0) * d0;
+  row[j1] = tc::fast_exp2(lst - cm1) * d1;
+  row[64 + j0] = tc::fast_exp2(cm0);
+  row[64 + j1] = tc::fast_exp2(cm1);
+  if (lane == 0) row[128] = tc::fast_exp2(lst);
+}
+
+__global__ void __launch_bounds__(sc::kThreads, 2) bwd_scan_kernel(BP p) {
+  using namespace sc;
+  using tc::f2;
+  extern __shared__ unsigned char ssm_raw[];
+  const uint32_t raw_s = tc::smem_u32(ssm_raw);
+  const uint32_t sb = (raw_s + 1023u) & ~1023u;
+  unsigned char* base = ssm_raw + (sb - raw_s);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);
+  uint32_t* tptr = reinterpret_cast<uint32_t*>(base + oBar + 64);
+  const int h = blockIdx.x, b = blockIdx.y, dir = blockIdx.z;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int P = p.P, N = p.N, nc = p.nc;
+  const int g = (int)((long long)h * p.G / p.H);
+  bool ok = true;
+  const auto chunk_at = [&](int s) { return b * nc + (dir == 0 ? s : nc - 1 - s); };
+  const float* tabh = p.tab + (long long)h * kTabF;  // + chunk * H * kTabF
+
+  if (w == 8) {
+    if (lane == 0) {
+      for (int i = 0; i < 2; ++i) tc::mbar_init(&bars[i], 128);  // full: converter threads
+      for (int i = 2; i < 6; ++i) tc::mbar_init(&bars[i], 1);    // empty, acc full: MMA commits
+      for (int i = 6; i < 8; ++i) tc::mbar_init(&bars[i], 128);  // acc free: state threads
+      tc::fence_mbar_init();
+    }
+    __syncwarp();
+    tc::tmem_alloc(tptr, 256);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tm = *tptr;
+
+  if (w >= 4 && w < 8) {
+    // ---- converters: copies of step s into slot s % 3, then w o x (or
+    //      exp(cum) o dy) as hi/lo tiles
+    const int ct = t - 128;
+    const void* vsrc = dir == 0 ? p.B : p.C;
+    const auto issue = [&](int s) {
+      const Chunk k = chunk_of(p, chunk_at(s));
+      unsigned char* st = base + (s % kStages) * kSlotBytes;
+      const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(vsrc);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int e = ct + 128 * r, j = e >> 4, n8 = (e & 15) * 8;
+        const bool okc = j < k.len && n8 < N;
+        const __nv_bfloat16* src = vg + ((k.tok0 + (okc ? j : 0)) * p.G + g) * N + (okc ? n8 : 0);
+        tc::cp_async16_zfill(st + 2 * kAtom + tg::swo(j, n8), src, okc);
+      }
+      if (ct < 16)  // the step's row weights
+        tc::cp_async16(base + oTab + 256 * (s % kStages) + 16 * ct,
+                       tabh + (long long)chunk_at(s) * p.H * kTabF + 64 * dir + 4 * ct);
+      if (dir == 0) {  // x rows (bf16) straight into the hi tile
+        const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int e = ct + 128 * r, j = e >> 3, q8 = (e & 7) * 8;
+          const bool okc = j < k.len && q8 < P;
+          const __nv_bfloat16* src = xg + ((k.tok0 + (okc ? j : 0)) * p.H + h) * P + (okc ? q8 : 0);
+          tc::cp_async16_zfill(st + tg::swo(j, q8), src, okc);
+        }
+      } else {  // dy rows (fp32) as they are over both tiles: row j at 256 j
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int e = ct + 128 * r, j = e >> 4, q4 = (e & 15) * 4;
+          const bool okc = j < k.len && q4 < P;
+          const float* src = p.dy + ((k.tok0 + (okc ? j : 0)) * p.H + h) * P + (okc ? q4 : 0);
+          tc::cp_async16_zfill(st + 16 * e, src, okc);
+        }
+      }
+    };
+    issue(0);
+    tc::cp_async_commit();
+    for (int s = 0; s < nc; ++s) {
+      const int slot = s % kStages;
+      if (s + 1 < nc) {  // the next step's copies into the other slot, once its product is done
+        const int s1 = s + 1;
+        if (s1 >= kStages) ok &= tc::mbar_wait(&bars[2 + s1 % kStages], ((s1 / kStages) - 1) & 1);
+        issue(s1);
+      }
+      tc::cp_async_commit();
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // every converter's copies of step s
+      const float* wrow = reinterpret_cast<const float*>(base + oTab + 256 * slot);
+      unsigned char* st = base + slot * kSlotBytes;
+      if (dir == 0) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int e = ct + 128 * r, j = e >> 3, q8 = (e & 7) * 8;
+          const float wj = wrow[j];
+          const uint32_t o = tg::swo(j, q8);
+          const uint4 xv = *reinterpret_cast<const uint4*>(st + o);
+          const f2 ww{wj, wj};
+          const f2 v[4] = {tc::mul2(tc::bf2(xv.x), ww), tc::mul2(tc::bf2(xv.y), ww),
+                           tc::mul2(tc::bf2(xv.z), ww), tc::mul2(tc::bf2(xv.w), ww)};
+          uint4 hi, lo;
+          tg::split8(v, hi, lo);
+          *reinterpret_cast<uint4*>(st + o) = hi;
+          *reinterpret_cast<uint4*>(st + kAtom + o) = lo;
+        }
+      } else {
+        float4 raw[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) raw[r] = *reinterpret_cast<const float4*>(st + 16 * (ct + 128 * r));
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the raw rows are read before the tiles overwrite them
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int e = ct + 128 * r, j = e >> 4, q4 = (e & 15) * 4;
+          const float wj = wrow[j];
+          const uint32_t o = tg::swo(j, q4);
+          float4 v = raw[r];
+          v.x *= wj;
+          v.y *= wj;
+          v.z *= wj;
+          v.w *= wj;
+          tg::split4_at(st + o, st + kAtom + o, v);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&bars[slot]);
+    }
+  } else if (w == 8) {
+    // ---- MMA warp
+    for (int s = 0; s < nc; ++s) {
+      const int slot = s % kStages, a = s & 1;
+      ok &= tc::mbar_wait(&bars[slot], (s / kStages) & 1);
+      if (s >= 2) ok &= tc::mbar_wait(&bars[6 + a], ((s >> 1) - 1) & 1);
+      tc::tc_fence_after();
+      if (tc::elect_one()) {
+        const uint32_t s0 = sb + slot * kSlotBytes;
+        const uint64_t dv = tc::sdesc_sw128(s0 + 2 * kAtom, kAtom, 1024);  // V^T, MN-major
+        const uint64_t du = tc::sdesc_sw128(s0, kAtom, 1024);              // [U hi | U lo], MN-major
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16(tm + 128 * a, dv + kk * 128, du + kk * 128, kId, kk > 0);
+        tc::mma_commit(&bars[2 + slot]);
+        tc::mma_commit(&bars[4 + a]);
+      }
+      __syncwarp();
+    }
+    if (nc > 0) tc::mbar_wait(&bars[4 + ((nc - 1) & 1)], ((nc - 1) >> 1) & 1);  // last product done
+  } else {
+    // ---- state warps: row n of the transposed state, headdim values
+    const int n = 32 * w + lane;
+    const uint32_t lb = (uint32_t)(32 * w) << 16;
+    float S[kPmax];
+    const float* s0 = dir == 0 ? p.init : p.dfinal;
+#pragma unroll
+    for (int q = 0; q < kPmax; ++q)
+      S[q] = (s0 && q < P && n < N) ? s0[(((long long)b * p.H + h) * P + q) * N + n] : 0.f;
+    float* outb = dir == 0 ? p.st : p.ad;
+    // the chunks' decays, loaded four steps ahead
+    float dcur[4], dnext[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dcur[i] = i < nc ? tabh[(long long)chunk_at(i) * p.H * kTabF + 128] : 1.f;
+    for (int s0 = 0; s0 < nc; s0 += 4) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dnext[i] = s0 + 4 + i < nc ? tabh[(long long)chunk_at(s0 + 4 + i) * p.H * kTabF + 128] : 1.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int s = s0 + i;
+        if (s >= nc) break;
+        const int a = s & 1;
+        const long long c = chunk_at(s);
+        {  // S out: row n into the stage, then rows 2 per warp instruction to global
+          unsigned char* stg = base + oStg;
+          asm volatile("bar.sync 2, 128;" ::: "memory");  // the previous step's rows have left
+#pragma unroll
+          for (int q = 0; q < kPmax; q += 4)
+            *reinterpret_cast<float4*>(stg + n * kStgPitch + 4 * q) =
+                make_float4(S[q], S[q + 1], S[q + 2], S[q + 3]);
+          asm volatile("bar.sync 2, 128;" ::: "memory");
+          float* o = outb + (c * p.H + h) * (long long)N * P;
+#pragma unroll
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const int idx = 128 * i2 + t, row = idx >> 4, c4 = (idx & 15) * 4;
+            if (row < N && c4 < P)
+              *reinterpret_cast<float4*>(o + row * P + c4) =
+                  *reinterpret_cast<const float4*>(stg + row * kStgPitch + 4 * c4);
+          }
+        }
+        const float dec = dcur[i];
+        ok &= tc::mbar_wait(&bars[4 + a], (s >> 1) & 1);
+        tc::tc_fence_after();
+#pragma unroll
+        for (int qb = 0; qb < kPmax; qb += 8) {  // columns qb.. of the hi half, 64 + qb.. of the lo half
+          float vh[8], vl[8];
+          const uint32_t col = tm + lb + 128 * a + qb;
+          tc::tmem_ld8(col, vh);
+          tc::tmem_ld8(col + 64, vl);
+          tc::tmem_ld_wait();
+          tc::tie8(vh);
+          tc::tie8(vl);
+#pragma unroll
+          for (int i2 = 0; i2 < 8; ++i2) S[qb + i2] = fmaf(dec, S[qb + i2], vh[i2] + vl[i2]);
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars[6 + a]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dcur[i] = dnext[i];
+    }
+    if (dir == 1 && p.dinit && n < N) {
+#pragma unroll
+      for (int q = 0; q < kPmax; ++q)
+        if (q < P) p.dinit[(((long long)b * p.H + h) * P + q) * N + n] = S[q];
+    }
+  }
+  if (!ok && p.status) atomicCAS(p.status, 0, (int)SSD_ERR_TIMEOUT);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (w == 8) tc::tmem_dealloc(tm, 256);
+}
+
 }  // namespace
 
 bool bwd_chunked_supported(int P, int N) {
@@ -1479,7 +1759,7 @@ bool bwd_chunked_supported(int P, int N) {
 size_t bwd_chunked_workspace_bytes(int batch, int T, int H, int P, int N) {
   const long long nch = (long long)batch * ((T + kQb - 1) / kQb);
   return 2 * align256(sizeof(float) * (size_t)nch * H * P * N) +
-         align256(sizeof(float) * (size_t)nch * H);
+         align256(sizeof(float) * (size_t)nch * H) + align256(sizeof(float) * (size_t)nch * H * 144);
 }
 
 ssd_status_t bwd_chunked(const BwdArgs& a) {
@@ -1516,6 +1796,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   p.st = reinterpret_cast<float*>(ws);
   p.ad = reinterpret_cast<float*>(ws + sbytes);
   p.dec = reinterpret_cast<float*>(ws + 2 * sbytes);
+  p.tab = reinterpret_cast<float*>(ws + 2 * sbytes + align256(sizeof(float) * (size_t)nch * a.H));
   const dim3 pgrid((unsigned)((a.P * a.N / 4 + kThr - 1) / kThr), a.H, a.batch);
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1523,6 +1804,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
     const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
     if (cudaFuncSetAttribute(bwd_grad_kernel<true>, at, (int)kGradSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_grad_tc_kernel, at, (int)tg::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_scan_kernel, at, (int)sc::kSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_grad_kernel<false>, at, (int)kGradSmem) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_outer_kernel<true, 0>, at, (int)outer_smem<true>()) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_outer_kernel<true, 1>, at, (int)outer_smem<true>()) != cudaSuccess ||
@@ -1533,6 +1815,19 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
   const int hpg = a.H / a.G;
   const dim3 ggrid((unsigned)nch, a.G, (unsigned)((hpg + kHS - 1) / kHS));
+  // The tensor-core path (bf16 inputs, headdim and dstate multiples of 8; x,
+  // B, C and dy move as 16-byte vectors, dx, dB and dC in pairs): the state
+  // scans (transposed states) and the tcgen05 gradient kernel.
+  const bool tcp = bf && a.P % 8 == 0 && a.N % 8 == 0 && al(a.x, 15) && al(a.B, 15) &&
+                   al(a.C, 15) && al(a.dy, 15) && al(a.dx, 7) && al(a.dB, 7) && al(a.dC, 7) &&
+                   al(a.dinit, 3);
+  if (tcp) {
+    bwd_tab_kernel<<<dim3((unsigned)nch, (unsigned)((a.H + 7) / 8)), 256, 0, a.stream>>>(p);
+    bwd_scan_kernel<<<dim3((unsigned)a.H, (unsigned)a.batch, 2), sc::kThreads, sc::kSmem, a.stream>>>(p);
+    bwd_grad_tc_kernel<<<ggrid, tg::kThreads, tg::kSmem, a.stream>>>(p);
+    count_launches(3);
+    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  }
   if (bf) {
     bwd_outer_kernel<true, 0><<<ggrid, kThr, outer_smem<true>(), a.stream>>>(p);
     bwd_outer_kernel<true, 1><<<ggrid, kThr, outer_smem<true>(), a.stream>>>(p);
@@ -1542,13 +1837,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   }
   bwd_pass_kernel<true><<<pgrid, kThr, 0, a.stream>>>(p);
   bwd_pass_kernel<false><<<pgrid, kThr, 0, a.stream>>>(p);
-  // the tensor-core kernel moves x, B, C (bf16) and dy in 16-byte vectors and
-  // writes dx in pairs
-  const bool mma = bf && a.P % 8 == 0 && a.N % 8 == 0 && al(a.x, 15) && al(a.B, 15) &&
-                   al(a.C, 15) && al(a.dy, 15) && al(a.dx, 7) && al(a.dB, 7) && al(a.dC, 7);
-  if (mma)
-    bwd_grad_tc_kernel<<<ggrid, tg::kThreads, tg::kSmem, a.stream>>>(p);
-  else if (bf)
+  if (bf)
     bwd_grad_kernel<true><<<ggrid, kThr, kGradSmem, a.stream>>>(p);
   else
     bwd_grad_kernel<false><<<ggrid, kThr, kGradSmem, a.stream>>>(p);
