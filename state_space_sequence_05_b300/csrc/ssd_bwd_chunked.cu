@@ -59,6 +59,7 @@
 
 #include "ssd.h"
 #include "ssd_internal.h"
+#include "ssd_tc_host.h"
 #include "tc_ptx.cuh"
 #include "tc_util.cuh"
 
@@ -1487,7 +1488,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
 // B^T (or C^T) read MN-major, times the weighted rows as [hi | lo] (64
 // columns each, MN-major); the state then becomes exp(cum_last) state + hi +
 // lo.  Warps 0-3 hold the state (row n = TMEM lane n) and write it out
-// through a padded shared-memory stage as coalesced rows, warps 4-7 stage and
+// through two 128B-swizzled shared-memory tiles with TMA stores, warps 4-7 stage and
 // convert the operands of a two-slot ring, warp 8 issues the MMAs into a
 // double-buffered accumulator.  Every wait is bounded (SSD_ERR_TIMEOUT).
 namespace sc {
@@ -1497,9 +1498,8 @@ constexpr uint32_t kSlotBytes = 4 * kAtom;  // U hi, U lo (64 tokens x 64 q), V 
 constexpr int kThreads = 32 * 9;
 constexpr int kTabF = 144;  // floats per (chunk, head) of the weight table
 constexpr uint32_t oTab = kStages * kSlotBytes;  // [2][64] the slots' row weights
-constexpr uint32_t kStgPitch = 272;              // bytes per staged state row (256 + 16: no bank conflicts)
-constexpr uint32_t oStg = oTab + kStages * 256;  // [128][272 B] the state rows on their way out
-constexpr uint32_t oBar = oStg + 128 * kStgPitch;  // full[2], empty[2], acc full[2], acc free[2]; TMEM base
+constexpr uint32_t oStg = oTab + 1024;  // two [128 rows][32 fp32] 128B-swizzled tiles: the state out
+constexpr uint32_t oBar = oStg + 2 * 16384;  // full[2], empty[2], acc full[2], acc free[2]; TMEM base
 constexpr uint32_t kSmem = oBar + 128 + 1024;
 constexpr uint32_t kId = tc::idesc_bf16(128, 128, true, true);
 }  // namespace sc
@@ -1534,7 +1534,9 @@ __global__ void __launch_bounds__(256) bwd_tab_kernel(BP p) {
   if (lane == 0) row[128] = tc::fast_exp2(lst);
 }
 
-__global__ void __launch_bounds__(sc::kThreads, 2) bwd_scan_kernel(BP p) {
+__global__ void __launch_bounds__(sc::kThreads, 2)
+    bwd_scan_kernel(BP p, const __grid_constant__ CUtensorMap map_st,
+                    const __grid_constant__ CUtensorMap map_ad) {
   using namespace sc;
   using tc::f2;
   extern __shared__ unsigned char ssm_raw[];
@@ -1684,7 +1686,6 @@ __global__ void __launch_bounds__(sc::kThreads, 2) bwd_scan_kernel(BP p) {
 #pragma unroll
     for (int q = 0; q < kPmax; ++q)
       S[q] = (s0 && q < P && n < N) ? s0[(((long long)b * p.H + h) * P + q) * N + n] : 0.f;
-    float* outb = dir == 0 ? p.st : p.ad;
     // the chunks' decays, loaded four steps ahead
     float dcur[4], dnext[4];
 #pragma unroll
@@ -1699,21 +1700,22 @@ __global__ void __launch_bounds__(sc::kThreads, 2) bwd_scan_kernel(BP p) {
         if (s >= nc) break;
         const int a = s & 1;
         const long long c = chunk_at(s);
-        {  // S out: row n into the stage, then rows 2 per warp instruction to global
+        {  // S out: row n into the two swizzled stage tiles, then two TMA stores
           unsigned char* stg = base + oStg;
-          asm volatile("bar.sync 2, 128;" ::: "memory");  // the previous step's rows have left
+          if (t == 0) tc::bulk_wait_read<0>();  // the previous step's stores have read the stage
+          asm volatile("bar.sync 2, 128;" ::: "memory");
 #pragma unroll
           for (int q = 0; q < kPmax; q += 4)
-            *reinterpret_cast<float4*>(stg + n * kStgPitch + 4 * q) =
+            *reinterpret_cast<float4*>(stg + (q >> 5) * 16384 + tc::sw128_offset(n, (q & 31) >> 2)) =
                 make_float4(S[q], S[q + 1], S[q + 2], S[q + 3]);
+          tc::fence_proxy_async_smem();
           asm volatile("bar.sync 2, 128;" ::: "memory");
-          float* o = outb + (c * p.H + h) * (long long)N * P;
-#pragma unroll
-          for (int i2 = 0; i2 < 16; ++i2) {
-            const int idx = 128 * i2 + t, row = idx >> 4, c4 = (idx & 15) * 4;
-            if (row < N && c4 < P)
-              *reinterpret_cast<float4*>(o + row * P + c4) =
-                  *reinterpret_cast<const float4*>(stg + row * kStgPitch + 4 * c4);
+          if (t == 0) {
+            const CUtensorMap* map = dir == 0 ? &map_st : &map_ad;
+            const int row0 = (int)((c * p.H + h) * N);
+            tc::tma_store_2d(map, stg, 0, row0);
+            if (P > 32) tc::tma_store_2d(map, stg + 16384, 32, row0);
+            tc::bulk_commit();
           }
         }
         const float dec = dcur[i];
@@ -1737,6 +1739,7 @@ __global__ void __launch_bounds__(sc::kThreads, 2) bwd_scan_kernel(BP p) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) dcur[i] = dnext[i];
     }
+    if (t == 0) tc::bulk_wait<0>();  // the state stores are complete
     if (dir == 1 && p.dinit && n < N) {
 #pragma unroll
       for (int q = 0; q < kPmax; ++q)
@@ -1823,7 +1826,13 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
                    al(a.dinit, 3);
   if (tcp) {
     bwd_tab_kernel<<<dim3((unsigned)nch, (unsigned)((a.H + 7) / 8)), 256, 0, a.stream>>>(p);
-    bwd_scan_kernel<<<dim3((unsigned)a.H, (unsigned)a.batch, 2), sc::kThreads, sc::kSmem, a.stream>>>(p);
+    CUtensorMap map_st, map_ad;
+    const long long srows = nch * a.H * a.N;
+    if (!tc_make_map_f32_sw128(&map_st, p.st, srows, a.P, a.N) ||
+        !tc_make_map_f32_sw128(&map_ad, p.ad, srows, a.P, a.N))
+      return SSD_ERR_CUDA;
+    bwd_scan_kernel<<<dim3((unsigned)a.H, (unsigned)a.batch, 2), sc::kThreads, sc::kSmem, a.stream>>>(
+        p, map_st, map_ad);
     bwd_grad_tc_kernel<<<ggrid, tg::kThreads, tg::kSmem, a.stream>>>(p);
     count_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;

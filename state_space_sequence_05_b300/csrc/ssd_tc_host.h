@@ -36,6 +36,10 @@ bool tc_make_map_bf16(CUtensorMap* m, const void* ptr, long long rows, long long
 // y as a 2-D fp32 tensor [tokens][H * P]: 16-column x 32-row boxes, 64-byte
 // swizzle (one math warp's staged tile).
 bool tc_make_map_y_f32(CUtensorMap* m, float* ptr, long long rows, long long cols);
+// fp32 [rows][cols]: 32-column (128-byte) x box_rows-row boxes, 128-byte
+// swizzle (the backward's state tiles; box_rows <= 256).
+bool tc_make_map_f32_sw128(CUtensorMap* m, float* ptr, long long rows, long long cols,
+                           int box_rows);
 // bf16 y: 16-column (32-byte) x 32-row boxes, unswizzled.
 bool tc_make_map_y_bf16(CUtensorMap* m, void* ptr, long long rows, long long cols);
 
