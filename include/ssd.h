@@ -228,17 +228,18 @@ ssd_status_t ssd_state_update(float *state, const void *x, const void *dt, const
  * Workspace: ssd_chunk_scan_bwd_workspace_size(...) bytes, 256-byte
  *   aligned, owned by the caller.  With headdim <= 64 and dstate <= 128
  *   (the chunked path, 64-token chunks): the state entering each chunk and
- *   the adjoint leaving it, [chunks][nheads][headdim][dstate] float32 each,
- *   and one decay per (chunk, head); other shapes (the step-by-step path):
- *   one stored state every 64 steps and the 64 states of one chunk, per
- *   (batch row, head).
+ *   the adjoint leaving it, [chunks][nheads] x headdim x dstate float32
+ *   each, and per (chunk, head) its decay and a 144-float weight row; other
+ *   shapes (the step-by-step path): one stored state every 64 steps and the
+ *   64 states of one chunk, per (batch row, head).
  * Supported: headdim * dstate <= 16384, either input dtype; no cu_seqlens.
  * Arithmetic: fp32 accumulation.  On the chunked path the products run on
  *   tensor cores with each fp32 operand as a pair of bf16 values (hi =
- *   rn(v), lo = rn(v - hi)): warp MMAs for the chunk states, tcgen05 MMAs
- *   for the gradients when the inputs are bf16 with headdim and dstate
- *   multiples of 8 (CUDA cores otherwise).  Five kernel launches (one on the
- *   step-by-step path) after the zeroing of dA, dB, dC and dD.
+ *   rn(v), lo = rn(v - hi)).  bf16 inputs with headdim and dstate multiples
+ *   of 8: three launches (a weight table, tcgen05 state scans, the tcgen05
+ *   gradient kernel); other chunked shapes: five (warp-MMA chunk states,
+ *   two state passes, the CUDA-core gradient kernel); the step-by-step
+ *   path: one.  dA, dB, dC and dD are zeroed first.
  * dev_status: as for the forward (NULL allowed): a device wait that runs
  *   out writes SSD_ERR_TIMEOUT there and the outputs are undefined.
  */
