@@ -1087,6 +1087,56 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     if (lane == 0) hsum[4 * hh] = lst;
   };
 
+  // The operands of slice head hh read only by the first MMA group: H_c,
+  // dH_{c+1} (hi/lo), w o x and exp(cum) o dy (hi/lo) from the registers
+  // (x, dy, H, dH of that head) and its tables; the block sums <dH, H> and
+  // dD of the head.  Math threads.
+  const auto store_early = [&](int hh) {
+    const float* ec = tabs + (4 * (hh & 1) + 1) * kQb;
+    const float* wt = ec + kQb;
+    const int j = t >> 3, q = (t & 7) * 8;
+    const uint32_t o8 = swo(j, q);
+    const f2 xf[4] = {tc::bf2(vx.x), tc::bf2(vx.y), tc::bf2(vx.z), tc::bf2(vx.w)};
+    const f2 yf[4] = {f2{vy[0].x, vy[0].y}, f2{vy[0].z, vy[0].w}, f2{vy[1].x, vy[1].y},
+                      f2{vy[1].z, vy[1].w}};
+    const f2 wj{wt[j], wt[j]}, ej{ec[j], ec[j]};
+    f2 sx[4], sy[4], dd2{0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      dd2 = tc::fma2(xf[i], yf[i], dd2);
+      sx[i] = tc::mul2(wj, xf[i]);
+      sy[i] = tc::mul2(ej, yf[i]);
+    }
+    uint4 hi, lo;
+    split8(sx, hi, lo);
+    *reinterpret_cast<uint4*>(base + oWXh + o8) = hi;
+    *reinterpret_cast<uint4*>(base + oWXl + o8) = lo;
+    split8(sy, hi, lo);
+    *reinterpret_cast<uint4*>(base + oEYh + o8) = hi;
+    *reinterpret_cast<uint4*>(base + oEYl + o8) = lo;
+    f2 hd2{0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e4 = t + kMathThreads * r, n = e4 >> 4, qq = (e4 & 15) * 4;
+      const uint32_t o = swo(n, qq);
+      split4_at(base + oHh + o, base + oHl + o, vh[r]);
+      split4_at(base + oDh + o, base + oDl + o, vd[r]);
+      hd2 = tc::fma2(f2{vh[r].x, vh[r].y}, f2{vd[r].x, vd[r].y}, hd2);
+      hd2 = tc::fma2(f2{vh[r].z, vh[r].w}, f2{vd[r].z, vd[r].w}, hd2);
+    }
+    tc::fence_proxy_async_smem();
+    float hdot = hd2.x + hd2.y, dd = dd2.x + dd2.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      hdot += __shfl_xor_sync(0xffffffffu, hdot, o);
+      dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    }
+    if (lane == 0) {
+      atomicAdd(&hsum[4 * hh + 1], hdot);
+      atomicAdd(&hsum[4 * hh + 3], dd);
+    }
+  };
+
   // ---- prologue: B, C tiles; the first head's operands and tables; TMEM; C B^T
   if (math) {
     const __nv_bfloat16* Bg = reinterpret_cast<const __nv_bfloat16*>(p.B);
@@ -1140,6 +1190,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   }
   float gr[8];  // C B^T at this thread's dS fragment positions
   if (math) {
+    store_early(0);
     ok &= tc::mbar_wait(&bars[0], 0);
     tc::tc_fence_after();
     ld_frag2(tm + lanebase + cS + c16, gr);
@@ -1157,54 +1208,19 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     const float* dts = dtsH + hh * kQb;
     float* dcum = dcumH + hh * kQb;
     float* ddd = dddH + hh * kQb;
-    // ---- operands to shared memory
+    // ---- x and dy of this head to shared memory (H, dH, w o x and
+    //      exp(cum) o dy went in while the previous head's second MMA group ran)
     if (math) {
       const int j = t >> 3, q = (t & 7) * 8;
       const uint32_t o8 = swo(j, q);
       *reinterpret_cast<uint4*>(base + oX + o8) = vx;
-      const f2 xf[4] = {tc::bf2(vx.x), tc::bf2(vx.y), tc::bf2(vx.z), tc::bf2(vx.w)};
       const f2 yf[4] = {f2{vy[0].x, vy[0].y}, f2{vy[0].z, vy[0].w}, f2{vy[1].x, vy[1].y},
                         f2{vy[1].z, vy[1].w}};
-      const f2 wj{wt[j], wt[j]}, ej{ec[j], ec[j]};
-      f2 sx[4], sy[4], dd2{0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        dd2 = tc::fma2(xf[i], yf[i], dd2);
-        sx[i] = tc::mul2(wj, xf[i]);
-        sy[i] = tc::mul2(ej, yf[i]);
-      }
       uint4 hi, lo;
-      split8(sx, hi, lo);
-      *reinterpret_cast<uint4*>(base + oWXh + o8) = hi;
-      *reinterpret_cast<uint4*>(base + oWXl + o8) = lo;
-      split8(sy, hi, lo);
-      *reinterpret_cast<uint4*>(base + oEYh + o8) = hi;
-      *reinterpret_cast<uint4*>(base + oEYl + o8) = lo;
       split8(yf, hi, lo);
       *reinterpret_cast<uint4*>(base + oYh + o8) = hi;
       *reinterpret_cast<uint4*>(base + oYl + o8) = lo;
-      f2 hd2{0.f, 0.f};
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int e4 = t + kMathThreads * r, n = e4 >> 4, qq = (e4 & 15) * 4;
-        const uint32_t o = swo(n, qq);
-        split4_at(base + oHh + o, base + oHl + o, vh[r]);
-        split4_at(base + oDh + o, base + oDl + o, vd[r]);
-        hd2 = tc::fma2(f2{vh[r].x, vh[r].y}, f2{vd[r].x, vd[r].y}, hd2);
-        hd2 = tc::fma2(f2{vh[r].z, vh[r].w}, f2{vd[r].z, vd[r].w}, hd2);
-      }
       tc::fence_proxy_async_smem();
-      // the block sums <dH, H> and dD of this head
-      float hdot = hd2.x + hd2.y, dd = dd2.x + dd2.y;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        hdot += __shfl_xor_sync(0xffffffffu, hdot, o);
-        dd += __shfl_xor_sync(0xffffffffu, dd, o);
-      }
-      if (lane == 0) {
-        atomicAdd(&hsum[4 * hh + 1], hdot);
-        atomicAdd(&hsum[4 * hh + 3], dd);
-      }
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -1306,6 +1322,11 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
           }
       }
       if (w == 4 && hh + 1 < nh) tables(hh + 1);  // a warp whose dS block is masked
+      // the next head's x, dy, H, dH into registers (this head's are in shared memory)
+      if (hh + 1 < nh) {
+        load_head(h + 1);
+        if (hh + 2 < nh) prefetch_head(h + 2);
+      }
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -1372,11 +1393,9 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) wv_sum += __shfl_xor_sync(0xffffffffu, wv_sum, o);
       if (lane == 0) atomicAdd(&hsum[4 * hh + 2], wv_sum);
-      // the next head's operands into registers
-      if (hh + 1 < nh) {
-        load_head(h + 1);
-        if (hh + 2 < nh) prefetch_head(h + 2);
-      }
+      // the first group is done with H, dH, w o x and exp(cum) o dy: the next
+      // head's go in now (its tables came with the second barrier)
+      if (hh + 1 < nh) store_early(hh + 1);
       // Xi (committed before the products into dC and dB)
       ok &= tc::mbar_wait(&bars[4], par);
       tc::tc_fence_after();
