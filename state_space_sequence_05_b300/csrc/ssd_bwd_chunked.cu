@@ -910,9 +910,12 @@ constexpr uint32_t oB = 0, oC = 2 * kAtom, oX = 4 * kAtom, oWXh = 5 * kAtom, oWX
                    oMh = 19 * kAtom, oMl = 20 * kAtom, oGh = 21 * kAtom, oGl = 22 * kAtom,
                    oTab = 23 * kAtom;
 // tables (floats): two buffers of (log2e cum, exp(cum), w, exp(cum_last -
-// cum)) [64]; per head of the slice dt [8][64], dL/dcum [8][64], the direct
-// dt terms [8][64], and (log2e cum_last, <dH, H>, sum_j w_j v_j, dD) [8][4]
-constexpr uint32_t kTabFloats = 2 * 4 * kQb + 3 * kHS * kQb + 4 * kHS;
+// cum)) [64]; per head of the slice dt [8][64]; per head the partial decay
+// sums, each slot with one writer: dL/dcum by row and column group [4][64],
+// the direct dt terms by row and column group [4][64] and by column and row
+// group [4][64]; and (log2e cum_last, <dH, H>, sum_j w_j v_j, dD) [8][4]
+constexpr uint32_t kPart = 3 * 4 * kQb;  // partial sums per head
+constexpr uint32_t kTabFloats = 2 * 4 * kQb + kHS * kQb + kHS * kPart + 4 * kHS;
 constexpr uint32_t oBar = oTab + 4 * kTabFloats;
 constexpr uint32_t kSmem = oBar + 64 + 1024;  // + alignment of the tiles to 1024 bytes
 static_assert(kSmem <= 232448, "shared memory per block");
@@ -994,9 +997,8 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   unsigned char* base = tsm_raw + (sb - raw_s);
   float* tabs = reinterpret_cast<float*>(base + oTab);
   float* dtsH = tabs + 8 * kQb;          // [8][64] dt per head
-  float* dcumH = dtsH + kHS * kQb;       // [8][64] dL/dcum per head
-  float* dddH = dcumH + kHS * kQb;       // [8][64] direct dt terms per head
-  float* hsum = dddH + kHS * kQb;        // [8][4] per head
+  float* partH = dtsH + kHS * kQb;       // [8][kPart] partial decay sums per head
+  float* hsum = partH + kHS * kPart;     // [8][4] per head
   // mbarriers, one phase per head each: C B^T (once), dS, group 1, group 2, Xi
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);
   uint32_t* tptr = reinterpret_cast<uint32_t*>(base + oBar + 48);
@@ -1158,7 +1160,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
       *reinterpret_cast<uint4*>(base + oB + swo(j, n)) = vb[r];
       *reinterpret_cast<uint4*>(base + oC + swo(j, n)) = vc[r];
     }
-    for (int e = t; e < 2 * kHS * kQb + 4 * kHS; e += kMathThreads) dcumH[e] = 0.f;  // dcum, ddd, sums
+    for (int e = t; e < (int)(kHS * kPart + 4 * kHS); e += kMathThreads) partH[e] = 0.f;  // partial sums
     if (w == 0) tables(0);
     tc::fence_proxy_async_smem();
   } else {
@@ -1206,8 +1208,9 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     const float* wt = ec + kQb;
     const float* el = wt + kQb;
     const float* dts = dtsH + hh * kQb;
-    float* dcum = dcumH + hh * kQb;
-    float* ddd = dddH + hh * kQb;
+    float* rrow = partH + hh * kPart + cg * kQb;              // dL/dcum, rows, this column group
+    float* drow = partH + hh * kPart + (4 + cg) * kQb;        // direct dt terms, rows
+    float* dcol = partH + hh * kPart + (8 + qd) * kQb;        // direct dt terms, columns, this row group
     // ---- x and dy of this head to shared memory (H, dH, w o x and
     //      exp(cum) o dy went in while the previous head's second MMA group ran)
     if (math) {
@@ -1266,6 +1269,14 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
       tc::tie8(sa);
       const float Dd = p.D ? p.D[h] : 0.f;
       float rowT[2] = {0.f, 0.f}, colU[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      const float c2i[2] = {c2[r16 + gq], c2[r16 + gq + 8]};
+      float c2j[4], dtj[4];
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        const int j = c16 + 8 * (f >> 1) + 2 * tq + (f & 1);
+        c2j[f] = c2[j];
+        dtj[f] = dts[j];
+      }
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt) {
 #pragma unroll
@@ -1278,10 +1289,10 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
             const int f = 4 * tt + 2 * hf + e;
             mv[e] = dv[e] = 0.f;
             if (j <= i && i < len) {
-              const float L = tc::fast_exp2(c2[i] - c2[j]);
+              const float L = tc::fast_exp2(c2i[hf] - c2j[2 * tt + e]);
               const float GL = gr[f] * L;
-              mv[e] = GL * dts[j];
-              dv[e] = sa[f] * L * dts[j];
+              mv[e] = GL * dtj[2 * tt + e];
+              dv[e] = sa[f] * L * dtj[2 * tt + e];
               rowT[hf] = fmaf(sa[f], mv[e], rowT[hf]);
               colU[tt][e] = fmaf(sa[f], GL, colU[tt][e]);
               if (i == j) mv[e] += Dd;
@@ -1298,29 +1309,24 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
         }
       }
       tc::fence_proxy_async_smem();
-      if (cg <= qd) {
+      // partial sums, one writer per slot: rows (quad sums) and columns
+      // (column j: sum_i dS M = dt_j sum_i dS G L; sums over the warp's rows)
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float v = rowT[hf];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          if (tq == 0) atomicAdd(&dcum[r16 + gq + 8 * hf], v);
-        }
-        // column j: sum_i dS M = dt_j sum_i dS G L
-#pragma unroll
-        for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float b = colU[tt][e];
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
-            if (gq == 0) {
-              const int j = c16 + 8 * tt + 2 * tq + e;
-              atomicAdd(&dcum[j], -dts[j] * b);
-              atomicAdd(&ddd[j], b);
-            }
-          }
+      for (int hf = 0; hf < 2; ++hf) {
+        float v = rowT[hf];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (tq == 0) rrow[r16 + gq + 8 * hf] = v;
       }
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float b = colU[tt][e];
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+          if (gq == 0) dcol[c16 + 8 * tt + 2 * tq + e] = b;
+        }
       if (w == 4 && hh + 1 < nh) tables(hh + 1);  // a warp whose dS block is masked
       // the next head's x, dy, H, dH into registers (this head's are in shared memory)
       if (hh + 1 < nh) {
@@ -1384,10 +1390,11 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
         z += __shfl_xor_sync(0xffffffffu, z, 1);
         z += __shfl_xor_sync(0xffffffffu, z, 2);
         const int r = r16 + gq + 8 * hf;
-        if (tq == 0 && r < len) {
-          atomicAdd(&dcum[r], ec[r] * z - wt[r] * v);
-          atomicAdd(&ddd[r], el[r] * v);
-          wv_sum = fmaf(wt[r], v, wv_sum);
+        if (tq == 0) {
+          const bool okr = r < len;
+          rrow[r] += okr ? ec[r] * z - wt[r] * v : 0.f;  // this thread wrote the row's dS part
+          drow[r] = okr ? el[r] * v : 0.f;
+          if (okr) wv_sum = fmaf(wt[r], v, wv_sum);
         }
       }
 #pragma unroll
@@ -1429,12 +1436,26 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   if (math && w < nh) {
     const int hh = w, h = hb + w;
     const float* dts = dtsH + hh * kQb;
-    const float* dcum = dcumH + hh * kQb;
-    const float* ddd = dddH + hh * kQb;
+    const float* part = partH + hh * kPart;
+    // dL/dcum_j and the direct dt terms from the partial sums
+    const auto sums = [&](int j, float& dc, float& dd) {
+      float r = 0.f, d = 0.f, cu = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        r += part[k * kQb + j];
+        d += part[(4 + k) * kQb + j];
+        cu += part[(8 + k) * kQb + j];
+      }
+      dc = r - dts[j] * cu;
+      dd = d + cu;
+    };
     const float extra = tc::fast_exp2(hsum[4 * hh]) * hsum[4 * hh + 1] + hsum[4 * hh + 2];
     const int j1 = kQb - 1 - 2 * lane, j2 = j1 - 1;  // lane l: entries 63 - 2l, 62 - 2l
-    const float a1 = dcum[j1] + (j1 == len - 1 ? extra : 0.f);
-    const float a2 = dcum[j2] + (j2 == len - 1 ? extra : 0.f);
+    float dc1, dd1, dc2, dd2;
+    sums(j1, dc1, dd1);
+    sums(j2, dc2, dd2);
+    const float a1 = dc1 + (j1 == len - 1 ? extra : 0.f);
+    const float a2 = dc2 + (j2 == len - 1 ? extra : 0.f);
     if (lane == 0 && p.dD) atomicAdd(p.dD + h, hsum[4 * hh + 3]);
     float v = a1 + a2;
 #pragma unroll
@@ -1446,11 +1467,11 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     const float Ah = p.A[h];
     float da = 0.f;
     if (j1 < len) {
-      p.ddt[(k.tok0 + j1) * p.H + h] = ddd[j1] + Ah * r1;
+      p.ddt[(k.tok0 + j1) * p.H + h] = dd1 + Ah * r1;
       da = fmaf(dts[j1], r1, da);
     }
     if (j2 < len) {
-      p.ddt[(k.tok0 + j2) * p.H + h] = ddd[j2] + Ah * r2;
+      p.ddt[(k.tok0 + j2) * p.H + h] = dd2 + Ah * r2;
       da = fmaf(dts[j2], r2, da);
     }
 #pragma unroll
