@@ -240,8 +240,9 @@ ssd_status_t ssd_state_update(float *state, const void *x, const void *dt, const
  *   gradient kernel); other chunked shapes: five (warp-MMA chunk states,
  *   two state passes, the CUDA-core gradient kernel); the step-by-step
  *   path: one.  dA, dB, dC and dD are zeroed first.
- * dev_status: as for the forward (NULL allowed): a device wait that runs
- *   out writes SSD_ERR_TIMEOUT there and the outputs are undefined.
+ * dev_status: as for the forward (NULL allowed): zeroed by the call on its
+ *   stream; a device wait that runs out writes SSD_ERR_TIMEOUT there and the
+ *   outputs are undefined.
  */
 size_t ssd_chunk_scan_bwd_workspace_size(int batch, int seqlen, int nheads, int headdim,
                                          int dstate, int ngroups, ssd_dtype_t in_dtype);
@@ -368,6 +369,20 @@ uint64_t ssd_kernel_launches(void);
  * setting is process-wide and not synchronised with calls in flight.
  */
 void ssd_test_set_forward_wait(unsigned long long wait_ns, int hold_unit);
+
+/*
+ * Test hook, not for production use.  Sets, for later calls of
+ * ssd_chunk_scan_bwd on its tensor-core path (bf16, headdim and dstate
+ * multiples of 8, at most 64 and 128), the bound on every mbarrier wait of
+ * the state scans and the gradient kernel in polls (0 restores the default,
+ * 2^22) and one MMA completion that is never signalled: hold 1, the first
+ * dS of gradient block 0; hold 2, the first chunk product of the forward
+ * scan of head 0; 0, none.  The waiting threads give up after `polls`, the
+ * call records SSD_ERR_TIMEOUT in dev_status, the block stops waiting and
+ * frees its tensor memory once its MMAs are done; the gradients of that call
+ * are undefined.  Process-wide, not synchronised with calls in flight.
+ */
+void ssd_test_set_backward_wait(unsigned long long polls, int hold);
 
 #ifdef __cplusplus
 }

@@ -287,6 +287,8 @@ ssd_status_t ssd_chunk_scan_bwd(const void* x, const void* dt, const float* A, c
   a.ws = workspace;
   a.dev_status = dev_status;
   a.stream = static_cast<cudaStream_t>(stream);
+  if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), a.stream) != cudaSuccess)
+    return SSD_ERR_CUDA;
   return ssd::bwd(a);
 }
 

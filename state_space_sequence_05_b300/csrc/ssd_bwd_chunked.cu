@@ -55,6 +55,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "ssd.h"
@@ -77,6 +79,8 @@ struct BP {
   const float *A, *D, *init, *dy, *dfinal;
   float *dx, *ddt, *dA, *dB, *dC, *dD, *dinit;
   int32_t* status;  // SSD_ERR_TIMEOUT when a device wait runs out (may be null)
+  unsigned wait_polls;  // bound on every mbarrier wait of the tcgen05 kernels (polls)
+  int hold;             // test hook: 1 / 2 hold back one MMA completion (gradients / scans)
   float* st;   // [chunks][H][P N]: chunk states, then the states entering each chunk
   float* ad;   // [chunks][H][P N]: local adjoint sums, then the adjoints leaving each chunk
   float* dec;  // [chunks][H]: exp(cum_last)
@@ -988,6 +992,17 @@ __device__ __forceinline__ tc::f2 bf2_at(const unsigned char* p) {
 }
 }  // namespace tg
 
+// A bounded mbarrier wait that gives up at once when an earlier wait of the
+// block ran out (*abort), and raises *abort when it runs out itself: a
+// block whose wait expired unwinds without waiting again.
+__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                      uint32_t polls) {
+  if (*abort) return false;
+  if (tc::mbar_wait(bar, parity, polls)) return true;
+  *abort = 1;
+  return false;
+}
+
 __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   using namespace tg;
   using tc::f2;
@@ -999,9 +1014,11 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   float* dtsH = tabs + 8 * kQb;          // [8][64] dt per head
   float* partH = dtsH + kHS * kQb;       // [8][kPart] partial decay sums per head
   float* hsum = partH + kHS * kPart;     // [8][4] per head
-  // mbarriers, one phase per head each: C B^T (once), dS, group 1, group 2, Xi
+  // mbarriers, one phase per head each: C B^T (once), dS, group 1, group 2,
+  // Xi; then the drain of the last MMAs (once)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);
   uint32_t* tptr = reinterpret_cast<uint32_t*>(base + oBar + 48);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(base + oBar + 52);
   const int c = blockIdx.x, g = blockIdx.y;
   const Chunk k = chunk_of(p, c);
   const int P = p.P, N = p.N, len = k.len;
@@ -1166,7 +1183,8 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   } else {
     if (lane == 0) {
 #pragma unroll
-      for (int i = 0; i < 5; ++i) tc::mbar_init(&bars[i], 1);
+      for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
+      *abort_f = 0;
       tc::fence_mbar_init();
     }
     __syncwarp();
@@ -1193,7 +1211,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   float gr[8];  // C B^T at this thread's dS fragment positions
   if (math) {
     store_early(0);
-    ok &= tc::mbar_wait(&bars[0], 0);
+    ok &= bwait(&bars[0], 0, abort_f, p.wait_polls);
     tc::tc_fence_after();
     ld_frag2(tm + lanebase + cS + c16, gr);
     tc::tmem_ld_wait();
@@ -1237,7 +1255,8 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
           tc::mma_bf16(tm + cS, KD(oYh, kk), KD(oX, kk), kIdKK64, kk > 0);
           tc::mma_bf16(tm + cS, KD(oYl, kk), KD(oX, kk), kIdKK64, true);
         }
-        tc::mma_commit(&bars[1]);
+        if (!(p.hold == 1 && hh == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0))
+          tc::mma_commit(&bars[1]);  // (the test hook holds back the first one of block 0)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const bool acc = hh > 0 || kk > 0;
@@ -1261,7 +1280,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     } else {
       // ---- dS epilogue: M = G L dt (+ D on the diagonal), dG = dS L dt;
       //      the decay terms of the quadratic form (rows r16.., columns c16..)
-      ok &= tc::mbar_wait(&bars[1], par);
+      ok &= bwait(&bars[1], par, abort_f, p.wait_polls);
       tc::tc_fence_after();
       float sa[8];
       ld_frag2(tm + lanebase + cS + c16, sa);
@@ -1360,7 +1379,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
       __syncwarp();
     } else {
       // ---- V, U: the state terms of the decay; then dx = Xi + w_j V
-      ok &= tc::mbar_wait(&bars[2], par);
+      ok &= bwait(&bars[2], par, abort_f, p.wait_polls);
       tc::tc_fence_after();
       float va[8], ua[8];
       ld_frag2(tm + lanebase + cV + c16, va);
@@ -1404,7 +1423,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
       // head's go in now (its tables came with the second barrier)
       if (hh + 1 < nh) store_early(hh + 1);
       // Xi (committed before the products into dC and dB)
-      ok &= tc::mbar_wait(&bars[4], par);
+      ok &= bwait(&bars[4], par, abort_f, p.wait_polls);
       tc::tc_fence_after();
       float xa[8];
       ld_frag2(tm + lanebase + cX + c16, xa);
@@ -1424,7 +1443,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
         }
       }
       // group 2 complete before its operands are overwritten
-      ok &= tc::mbar_wait(&bars[3], par);
+      ok &= bwait(&bars[3], par, abort_f, p.wait_polls);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -1507,8 +1526,10 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   if (!ok && p.status) atomicCAS(p.status, 0, (int)SSD_ERR_TIMEOUT);
   tc::tc_fence_before();
   __syncthreads();
-  if (!math) {
-    tc::mbar_wait(&bars[3], (nh - 1) & 1);  // the last MMAs are done (bounded)
+  if (!math) {  // every MMA of the block complete before its tensor memory is freed
+    if (tc::elect_one()) tc::mma_commit(&bars[5]);
+    __syncwarp();
+    tc::mbar_wait(&bars[5], 0);
     tc::tmem_dealloc(tm, 512);
   }
 }
@@ -1584,7 +1605,8 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
   const uint32_t sb = (raw_s + 1023u) & ~1023u;
   unsigned char* base = ssm_raw + (sb - raw_s);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);
-  uint32_t* tptr = reinterpret_cast<uint32_t*>(base + oBar + 64);
+  uint32_t* tptr = reinterpret_cast<uint32_t*>(base + oBar + 80);  // bars[8]: the drain
+  volatile int* abort_f = reinterpret_cast<volatile int*>(base + oBar + 84);
   const int h = blockIdx.x, b = blockIdx.y, dir = blockIdx.z;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int P = p.P, N = p.N, nc = p.nc;
@@ -1598,6 +1620,8 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
       for (int i = 0; i < 2; ++i) tc::mbar_init(&bars[i], 128);  // full: converter threads
       for (int i = 2; i < 6; ++i) tc::mbar_init(&bars[i], 1);    // empty, acc full: MMA commits
       for (int i = 6; i < 8; ++i) tc::mbar_init(&bars[i], 128);  // acc free: state threads
+      tc::mbar_init(&bars[8], 1);                                // drain of the last MMAs
+      *abort_f = 0;
       tc::fence_mbar_init();
     }
     __syncwarp();
@@ -1653,7 +1677,7 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
       const int slot = s % kStages;
       if (s + 1 < nc) {  // the next step's copies into the other slot, once its product is done
         const int s1 = s + 1;
-        if (s1 >= kStages) ok &= tc::mbar_wait(&bars[2 + s1 % kStages], ((s1 / kStages) - 1) & 1);
+        if (s1 >= kStages) ok &= bwait(&bars[2 + s1 % kStages], ((s1 / kStages) - 1) & 1, abort_f, p.wait_polls);
         issue(s1);
       }
       tc::cp_async_commit();
@@ -1701,8 +1725,8 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
     // ---- MMA warp
     for (int s = 0; s < nc; ++s) {
       const int slot = s % kStages, a = s & 1;
-      ok &= tc::mbar_wait(&bars[slot], (s / kStages) & 1);
-      if (s >= 2) ok &= tc::mbar_wait(&bars[6 + a], ((s >> 1) - 1) & 1);
+      ok &= bwait(&bars[slot], (s / kStages) & 1, abort_f, p.wait_polls);
+      if (s >= 2) ok &= bwait(&bars[6 + a], ((s >> 1) - 1) & 1, abort_f, p.wait_polls);
       tc::tc_fence_after();
       if (tc::elect_one()) {
         const uint32_t s0 = sb + slot * kSlotBytes;
@@ -1712,11 +1736,15 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
         for (int kk = 0; kk < 4; ++kk)
           tc::mma_bf16(tm + 128 * a, dv + kk * 128, du + kk * 128, kId, kk > 0);
         tc::mma_commit(&bars[2 + slot]);
-        tc::mma_commit(&bars[4 + a]);
+        if (!(p.hold == 2 && s == 0 && h == 0 && b == 0 && dir == 0))
+          tc::mma_commit(&bars[4 + a]);  // (the test hook holds back the first one of one block)
       }
       __syncwarp();
     }
-    if (nc > 0) tc::mbar_wait(&bars[4 + ((nc - 1) & 1)], ((nc - 1) >> 1) & 1);  // last product done
+    // every MMA of the block complete before its tensor memory is freed
+    if (tc::elect_one()) tc::mma_commit(&bars[8]);
+    __syncwarp();
+    tc::mbar_wait(&bars[8], 0);
   } else {
     // ---- state warps: row n of the transposed state, headdim values
     const int n = 32 * w + lane;
@@ -1759,7 +1787,7 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
           }
         }
         const float dec = dcur[i];
-        ok &= tc::mbar_wait(&bars[4 + a], (s >> 1) & 1);
+        ok &= bwait(&bars[4 + a], (s >> 1) & 1, abort_f, p.wait_polls);
         tc::tc_fence_after();
 #pragma unroll
         for (int qb = 0; qb < kPmax; qb += 8) {  // columns qb.. of the hi half, 64 + qb.. of the lo half
@@ -1794,6 +1822,12 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
 
 }  // namespace
 
+namespace {
+// Test hook (ssd_test_set_backward_wait).
+std::atomic<unsigned long long> g_bwd_polls{0};
+std::atomic<int> g_bwd_hold{0};
+}  // namespace
+
 bool bwd_chunked_supported(int P, int N) {
   // the state passes move float4s
   return P >= 1 && P <= kPmax && N >= 1 && N <= kNmax && (P * N) % 4 == 0;
@@ -1824,6 +1858,11 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
   p.dD = a.dD;
   p.dinit = a.dinit;
   p.status = a.dev_status;
+  {
+    const unsigned long long polls = g_bwd_polls.load(std::memory_order_relaxed);
+    p.wait_polls = polls == 0 ? (1u << 22) : (unsigned)std::min<unsigned long long>(polls, 1u << 30);
+    p.hold = g_bwd_hold.load(std::memory_order_relaxed);
+  }
   p.T = a.seqlen;
   p.H = a.H;
   p.P = a.P;
@@ -1895,3 +1934,8 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
 }
 
 }  // namespace ssd
+
+extern "C" void ssd_test_set_backward_wait(unsigned long long polls, int hold) {
+  ssd::g_bwd_polls.store(polls, std::memory_order_relaxed);
+  ssd::g_bwd_hold.store(hold, std::memory_order_relaxed);
+}

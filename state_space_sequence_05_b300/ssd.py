@@ -59,6 +59,7 @@ SIGNATURES = {
     "ssd_version": (_ci, []),
     "ssd_kernel_launches": (ctypes.c_uint64, []),
     "ssd_test_set_forward_wait": (None, [ctypes.c_ulonglong, _ci]),
+    "ssd_test_set_backward_wait": (None, [ctypes.c_ulonglong, _ci]),
 }
 
 _lib = None
@@ -105,6 +106,13 @@ def test_set_forward_wait(wait_ns: int = 0, hold_unit: int = -1) -> None:
     """Test hook: bound on every device wait of the tensor-core forward (ns,
     0 = default) and a work unit that never publishes its state (-1 = none)."""
     load_library().ssd_test_set_forward_wait(int(wait_ns), int(hold_unit))
+
+
+def test_set_backward_wait(polls: int = 0, hold: int = 0) -> None:
+    """Test hook: bound on every mbarrier wait of the tensor-core backward
+    (polls, 0 = default) and one MMA completion held back (1: gradient
+    kernel, 2: state scan, 0: none)."""
+    load_library().ssd_test_set_backward_wait(int(polls), int(hold))
 
 
 def _ptr(t: Optional[torch.Tensor]):

@@ -1,4 +1,5 @@
-"""The bounded device waits of the tensor-core forward run out cleanly.
+"""The bounded device waits of the tensor-core forward and backward run out
+cleanly.
 
 Every wait in the kernels (an mbarrier phase, a predecessor's hand-off flag)
 gives up after a time limit, records SSD_ERR_TIMEOUT in dev_status and lets
@@ -60,3 +61,39 @@ def test_held_hand_off_times_out_then_next_call_is_exact(kernel):
     y_ref, f_ref = oracle_full(fi)
     assert_close(y.cpu().numpy(), y_ref, TOL["bf16"], "y after the expired call")
     assert_close(fin.cpu().numpy(), f_ref, TOL["bf16"], "final after the expired call")
+
+
+@pytest.mark.parametrize("hold", [1, 2], ids=["gradients", "state_scan"])
+def test_backward_held_mma_completion_times_out_then_next_call_is_exact(hold):
+    """The tensor-core backward: one MMA completion of the gradient kernel
+    (hold 1) or of the state scans (hold 2) is never signalled, so the
+    threads waiting for it give up after the hook's poll bound and the call
+    reports SSD_ERR_TIMEOUT; the next call, hook off, matches the fp64
+    backward oracle."""
+    import numpy as np
+    import torch
+    import oracle
+    from state_space_sequence_05_b300 import ssd
+    wl = I.small_workload(batch=1, seqlen=192, nheads=2, headdim=64, dstate=128, ngroups=1,
+                          chunk=128, dtype="bf16", seed=33)
+    fi = I.make_forward_inputs(wl)
+    d = to_device(fi)
+    rng = np.random.Generator(np.random.PCG64(933))
+    dy = rng.standard_normal(fi.x.shape).astype(np.float32)
+    dyt = torch.from_numpy(dy).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    args = (d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init"], dyt)
+    try:
+        ssd.test_set_backward_wait(20000, hold)
+        ssd.ssd_chunk_scan_bwd(*args, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == ssd.SSD_ERR_TIMEOUT
+    finally:
+        ssd.test_set_backward_wait(0, 0)
+    g = ssd.ssd_chunk_scan_bwd(*args, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.ssd_bwd(fi.x, fi.dt, fi.A, fi.B, fi.C, fi.D, fi.init, dy, None)
+    for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dinit"):
+        e = oracle.rel_err(g[k].cpu().numpy(), ref[k])
+        assert e <= 1e-3, f"{k} after the expired call: max|diff|/RMS = {e:.3e}"
