@@ -75,6 +75,14 @@ def test_bwd_bf16_mma_padded_tiles():
                             chunk=64, dtype="bf16", seed=64), seed=3)
 
 
+def test_bwd_bf16_tensor_core_head_slices():
+    """The tensor-core path with two batch rows and two groups of ten heads:
+    each group's heads split over two gradient blocks (8 + 2), whose dB and dC
+    meet in global memory; init and dL/dfinal on both state scans."""
+    _check(I.small_workload(batch=2, seqlen=200, nheads=20, headdim=64, dstate=128, ngroups=2,
+                            chunk=128, dtype="bf16", seed=66), seed=5)
+
+
 def test_bwd_bf16_cuda_core_path():
     """bf16 with a headdim that is no multiple of 8 (P 12): the CUDA-core
     gradient kernel."""
