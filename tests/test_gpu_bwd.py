@@ -83,6 +83,13 @@ def test_bwd_bf16_tensor_core_head_slices():
                             chunk=128, dtype="bf16", seed=66), seed=5)
 
 
+def test_bwd_bf16_tensor_core_without_optional_inputs():
+    """The tensor-core path with no D, no initial state and no dL/dfinal."""
+    _check(I.small_workload(batch=1, seqlen=140, nheads=3, headdim=64, dstate=128, ngroups=1,
+                            chunk=128, dtype="bf16", init="zero", seed=67),
+           use_D=False, use_init=False, use_dfinal=False, seed=6)
+
+
 def test_bwd_bf16_cuda_core_path():
     """bf16 with a headdim that is no multiple of 8 (P 12): the CUDA-core
     gradient kernel."""
