@@ -35,14 +35,14 @@
 //
 // Kernels (fp32 accumulation; the products on tensor cores take fp32
 // operands as bf16 hi/lo pairs, hi = rn(v), lo = rn(v - hi)):
-//   bwd_outer_kernel<F>  per (chunk, group, slice of up to 8 of the group's
+//   bwd_outer_kernel<F>  per (chunk, group, slice of up to 10 of the group's
 //                        heads): the chunk states sum_j w_j x_j B_j^T and
 //                        exp(cum_last), warp MMAs;
 //   bwd_outer_kernel<R>  the same for sum_i exp(cum_i) dy_i C_i^T;
 //   bwd_pass_kernel      per (row, head, state element): the states entering
 //                        each chunk (forwards) / the adjoints leaving each
 //                        chunk (backwards), in place; dinit;
-//   bwd_grad_tc_kernel   per (chunk, group, slice of up to 8 heads), bf16
+//   bwd_grad_tc_kernel   per (chunk, group, slice of up to 10 heads), bf16
 //                        inputs with headdim and dstate multiples of 8:
 //                        every gradient above on tcgen05 MMAs (M = 64), dB
 //                        and dC summed over the slice in tensor memory;
@@ -272,7 +272,7 @@ __device__ __forceinline__ void store_split4(__nv_bfloat16* dh, __nv_bfloat16* d
 // p.vec the rows move as 16-byte vectors: the next head's U rows are copied
 // asynchronously into a staging buffer (and its dt loaded) while the current
 // head's product runs.
-constexpr int kHS = 8;  // heads of a group per block (outer sums and gradients)
+constexpr int kHS = 10;  // heads of a group per block (outer sums and gradients); 80 heads make 8 slices
 
 constexpr size_t kStage = sizeof(float) * kQb * kPmax;  // raw U rows of one head
 
@@ -914,10 +914,10 @@ constexpr uint32_t oB = 0, oC = 2 * kAtom, oX = 4 * kAtom, oWXh = 5 * kAtom, oWX
                    oMh = 19 * kAtom, oMl = 20 * kAtom, oGh = 21 * kAtom, oGl = 22 * kAtom,
                    oTab = 23 * kAtom;
 // tables (floats): two buffers of (log2e cum, exp(cum), w, exp(cum_last -
-// cum)) [64]; per head of the slice dt [8][64]; per head the partial decay
+// cum)) [64]; per head of the slice dt [kHS][64]; per head the partial decay
 // sums, each slot with one writer: dL/dcum by row and column group [4][64],
 // the direct dt terms by row and column group [4][64] and by column and row
-// group [4][64]; and (log2e cum_last, <dH, H>, sum_j w_j v_j, dD) [8][4]
+// group [4][64]; and (log2e cum_last, <dH, H>, sum_j w_j v_j, dD) [kHS][4]
 constexpr uint32_t kPart = 3 * 4 * kQb;  // partial sums per head
 constexpr uint32_t kTabFloats = 2 * 4 * kQb + kHS * kQb + kHS * kPart + 4 * kHS;
 constexpr uint32_t oBar = oTab + 4 * kTabFloats;
@@ -1011,9 +1011,9 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   const uint32_t sb = (raw_s + 1023u) & ~1023u;
   unsigned char* base = tsm_raw + (sb - raw_s);
   float* tabs = reinterpret_cast<float*>(base + oTab);
-  float* dtsH = tabs + 8 * kQb;          // [8][64] dt per head
-  float* partH = dtsH + kHS * kQb;       // [8][kPart] partial decay sums per head
-  float* hsum = partH + kHS * kPart;     // [8][4] per head
+  float* dtsH = tabs + 8 * kQb;          // [kHS][64] dt per head (after the two 4 x 64 table buffers)
+  float* partH = dtsH + kHS * kQb;       // [kHS][kPart] partial decay sums per head
+  float* hsum = partH + kHS * kPart;     // [kHS][4] per head
   // mbarriers, one phase per head each: C B^T (once), dS, group 1, group 2,
   // Xi; then the drain of the last MMAs (once)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);
