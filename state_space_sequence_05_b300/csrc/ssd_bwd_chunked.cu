@@ -1539,30 +1539,33 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
 // ---------------------------------------------------------------- state scans, tcgen05
 // The states entering each chunk (forwards from init) and the adjoints
 // leaving each chunk (backwards from dL/dfinal) for the tcgen05 gradient
-// kernel: one block per (head, batch row, direction) walks the row's chunks
-// in order with the state in registers, so every state is written once.
-// Storage is transposed: st, ad [chunk][head][n][q] (dstate rows of headdim
-// values); dinit [batch][head][q][n].  Per chunk the local sum
+// kernel: one block per (head, batch row, direction, half of headdim) walks
+// the row's chunks in order with its 128 x 32 part of the state in
+// registers, so every state is written once.  Storage is transposed: st, ad
+// [chunk][head][n][q] (dstate rows of headdim values); dinit
+// [batch][head][q][n].  Per chunk the local sum
 //   forwards:  sum_j B_j (w_j x_j)^T,       w_j = exp(cum_last - cum_j) dt_j
 //   backwards: sum_i C_i (exp(cum_i) dy_i)^T
-// is one M = 128 (n) x N = 128 tcgen05 product over the chunk's 64 tokens:
-// B^T (or C^T) read MN-major, times the weighted rows as [hi | lo] (64
-// columns each, MN-major); the state then becomes exp(cum_last) state + hi +
-// lo.  Warps 0-3 hold the state (row n = TMEM lane n) and write it out
-// through two 128B-swizzled shared-memory tiles with TMA stores, warps 4-7 stage and
-// convert the operands of a two-slot ring, warp 8 issues the MMAs into a
-// double-buffered accumulator.  Every wait is bounded (SSD_ERR_TIMEOUT).
+// over the block's 32 columns is one M = 128 (n) x N = 64 tcgen05 product
+// over the chunk's 64 tokens: B^T (or C^T) read MN-major, times the weighted
+// rows as [hi | lo] (32 columns each) in one MN-major tile; the state then
+// becomes exp(cum_last) state + hi + lo.  Warps 0-3 hold the state (row n =
+// TMEM lane n) and write it out through a 128B-swizzled shared tile with a
+// TMA store, warps 4-7 stage and convert the operands of a two-slot ring,
+// warp 8 issues the MMAs into a double-buffered accumulator.  Three blocks
+// fit on an SM.  Every wait is bounded (SSD_ERR_TIMEOUT).
 namespace sc {
 constexpr int kStages = 2;
-constexpr uint32_t kAtom = 8192;        // 64 rows x 128 bytes
-constexpr uint32_t kSlotBytes = 4 * kAtom;  // U hi, U lo (64 tokens x 64 q), V (64 tokens x 128 n)
+constexpr int kQH = 32;                     // headdim columns per block (half of 64)
+constexpr uint32_t kAtom = 8192;            // 64 rows x 128 bytes
+constexpr uint32_t kSlotBytes = 3 * kAtom;  // U (64 tokens x [hi 32 | lo 32]), V (64 tokens x 128 n)
 constexpr int kThreads = 32 * 9;
 constexpr int kTabF = 144;  // floats per (chunk, head) of the weight table
 constexpr uint32_t oTab = kStages * kSlotBytes;  // [2][64] the slots' row weights
-constexpr uint32_t oStg = oTab + 1024;  // two [128 rows][32 fp32] 128B-swizzled tiles: the state out
-constexpr uint32_t oBar = oStg + 2 * 16384;  // full[2], empty[2], acc full[2], acc free[2]; TMEM base
+constexpr uint32_t oStg = oTab + 1024;           // [128 rows][32 fp32] 128B-swizzled tile: the state out
+constexpr uint32_t oBar = oStg + 16384;  // full[2], empty[2], acc full[2], acc free[2], drain; TMEM base
 constexpr uint32_t kSmem = oBar + 128 + 1024;
-constexpr uint32_t kId = tc::idesc_bf16(128, 128, true, true);
+constexpr uint32_t kId = tc::idesc_bf16(128, 64, true, true);
 }  // namespace sc
 
 // The weight table of the tensor-core path, per (chunk, head): the forward
@@ -1595,11 +1598,15 @@ __global__ void __launch_bounds__(256) bwd_tab_kernel(BP p) {
   if (lane == 0) row[128] = tc::fast_exp2(lst);
 }
 
-__global__ void __launch_bounds__(sc::kThreads, 2)
+__global__ void __launch_bounds__(sc::kThreads, 3)
     bwd_scan_kernel(BP p, const __grid_constant__ CUtensorMap map_st,
                     const __grid_constant__ CUtensorMap map_ad) {
   using namespace sc;
   using tc::f2;
+  const int h = blockIdx.x, b = blockIdx.y, dir = blockIdx.z >> 1, qh = blockIdx.z & 1;
+  const int P = p.P, N = p.N, nc = p.nc;
+  const int q0 = kQH * qh;  // this block's headdim columns q0 .. q0 + 31
+  if (q0 >= P) return;      // (the whole block: headdim <= 32 needs one half)
   extern __shared__ unsigned char ssm_raw[];
   const uint32_t raw_s = tc::smem_u32(ssm_raw);
   const uint32_t sb = (raw_s + 1023u) & ~1023u;
@@ -1607,9 +1614,7 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);
   uint32_t* tptr = reinterpret_cast<uint32_t*>(base + oBar + 80);  // bars[8]: the drain
   volatile int* abort_f = reinterpret_cast<volatile int*>(base + oBar + 84);
-  const int h = blockIdx.x, b = blockIdx.y, dir = blockIdx.z;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int P = p.P, N = p.N, nc = p.nc;
   const int g = (int)((long long)h * p.G / p.H);
   bool ok = true;
   const auto chunk_at = [&](int s) { return b * nc + (dir == 0 ? s : nc - 1 - s); };
@@ -1625,7 +1630,7 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
       tc::fence_mbar_init();
     }
     __syncwarp();
-    tc::tmem_alloc(tptr, 256);
+    tc::tmem_alloc(tptr, 128);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -1634,8 +1639,8 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
   const uint32_t tm = *tptr;
 
   if (w >= 4 && w < 8) {
-    // ---- converters: copies of step s into slot s % 3, then w o x (or
-    //      exp(cum) o dy) as hi/lo tiles
+    // ---- converters: copies of step s into slot s % 2, then w o x (or
+    //      exp(cum) o dy) for the block's 32 columns as [hi | lo] in one tile
     const int ct = t - 128;
     const void* vsrc = dir == 0 ? p.B : p.C;
     const auto issue = [&](int s) {
@@ -1647,26 +1652,27 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
         const int e = ct + 128 * r, j = e >> 4, n8 = (e & 15) * 8;
         const bool okc = j < k.len && n8 < N;
         const __nv_bfloat16* src = vg + ((k.tok0 + (okc ? j : 0)) * p.G + g) * N + (okc ? n8 : 0);
-        tc::cp_async16_zfill(st + 2 * kAtom + tg::swo(j, n8), src, okc);
+        tc::cp_async16_zfill(st + kAtom + tg::swo(j, n8), src, okc);
       }
       if (ct < 16)  // the step's row weights
         tc::cp_async16(base + oTab + 256 * (s % kStages) + 16 * ct,
                        tabh + (long long)chunk_at(s) * p.H * kTabF + 64 * dir + 4 * ct);
-      if (dir == 0) {  // x rows (bf16) straight into the hi tile
+      if (dir == 0) {  // x (bf16), 32 columns, straight into the hi half of the tile
         const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int e = ct + 128 * r, j = e >> 3, q8 = (e & 7) * 8;
-          const bool okc = j < k.len && q8 < P;
-          const __nv_bfloat16* src = xg + ((k.tok0 + (okc ? j : 0)) * p.H + h) * P + (okc ? q8 : 0);
+        for (int r = 0; r < 2; ++r) {
+          const int e = ct + 128 * r, j = e >> 2, q8 = (e & 3) * 8;
+          const bool okc = j < k.len && q0 + q8 < P;
+          const __nv_bfloat16* src =
+              xg + ((k.tok0 + (okc ? j : 0)) * p.H + h) * P + (okc ? q0 + q8 : 0);
           tc::cp_async16_zfill(st + tg::swo(j, q8), src, okc);
         }
-      } else {  // dy rows (fp32) as they are over both tiles: row j at 256 j
+      } else {  // dy (fp32), 32 columns, as they are over the tile: row j at 128 j
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int e = ct + 128 * r, j = e >> 4, q4 = (e & 15) * 4;
-          const bool okc = j < k.len && q4 < P;
-          const float* src = p.dy + ((k.tok0 + (okc ? j : 0)) * p.H + h) * P + (okc ? q4 : 0);
+        for (int r = 0; r < 4; ++r) {
+          const int e = ct + 128 * r, j = e >> 3, q4 = (e & 7) * 4;
+          const bool okc = j < k.len && q0 + q4 < P;
+          const float* src = p.dy + ((k.tok0 + (okc ? j : 0)) * p.H + h) * P + (okc ? q0 + q4 : 0);
           tc::cp_async16_zfill(st + 16 * e, src, okc);
         }
       }
@@ -1687,35 +1693,33 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
       unsigned char* st = base + slot * kSlotBytes;
       if (dir == 0) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int e = ct + 128 * r, j = e >> 3, q8 = (e & 7) * 8;
+        for (int r = 0; r < 2; ++r) {
+          const int e = ct + 128 * r, j = e >> 2, q8 = (e & 3) * 8;
           const float wj = wrow[j];
-          const uint32_t o = tg::swo(j, q8);
-          const uint4 xv = *reinterpret_cast<const uint4*>(st + o);
+          const uint4 xv = *reinterpret_cast<const uint4*>(st + tg::swo(j, q8));
           const f2 ww{wj, wj};
           const f2 v[4] = {tc::mul2(tc::bf2(xv.x), ww), tc::mul2(tc::bf2(xv.y), ww),
                            tc::mul2(tc::bf2(xv.z), ww), tc::mul2(tc::bf2(xv.w), ww)};
           uint4 hi, lo;
           tg::split8(v, hi, lo);
-          *reinterpret_cast<uint4*>(st + o) = hi;
-          *reinterpret_cast<uint4*>(st + kAtom + o) = lo;
+          *reinterpret_cast<uint4*>(st + tg::swo(j, q8)) = hi;
+          *reinterpret_cast<uint4*>(st + tg::swo(j, kQH + q8)) = lo;
         }
       } else {
-        float4 raw[8];
+        float4 raw[4];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) raw[r] = *reinterpret_cast<const float4*>(st + 16 * (ct + 128 * r));
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the raw rows are read before the tiles overwrite them
+        for (int r = 0; r < 4; ++r) raw[r] = *reinterpret_cast<const float4*>(st + 16 * (ct + 128 * r));
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the raw rows are read before the tile overwrites them
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int e = ct + 128 * r, j = e >> 4, q4 = (e & 15) * 4;
+        for (int r = 0; r < 4; ++r) {
+          const int e = ct + 128 * r, j = e >> 3, q4 = (e & 7) * 4;
           const float wj = wrow[j];
-          const uint32_t o = tg::swo(j, q4);
           float4 v = raw[r];
           v.x *= wj;
           v.y *= wj;
           v.z *= wj;
           v.w *= wj;
-          tg::split4_at(st + o, st + kAtom + o, v);
+          tg::split4_at(st + tg::swo(j, q4), st + tg::swo(j, kQH + q4), v);
         }
       }
       tc::fence_proxy_async_smem();
@@ -1730,13 +1734,13 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
       tc::tc_fence_after();
       if (tc::elect_one()) {
         const uint32_t s0 = sb + slot * kSlotBytes;
-        const uint64_t dv = tc::sdesc_sw128(s0 + 2 * kAtom, kAtom, 1024);  // V^T, MN-major
-        const uint64_t du = tc::sdesc_sw128(s0, kAtom, 1024);              // [U hi | U lo], MN-major
+        const uint64_t dv = tc::sdesc_sw128(s0 + kAtom, kAtom, 1024);  // V^T, MN-major
+        const uint64_t du = tc::sdesc_sw128(s0, kAtom, 1024);          // [U hi | U lo], MN-major
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16(tm + 128 * a, dv + kk * 128, du + kk * 128, kId, kk > 0);
+          tc::mma_bf16(tm + 64 * a, dv + kk * 128, du + kk * 128, kId, kk > 0);
         tc::mma_commit(&bars[2 + slot]);
-        if (!(p.hold == 2 && s == 0 && h == 0 && b == 0 && dir == 0))
+        if (!(p.hold == 2 && s == 0 && h == 0 && b == 0 && dir == 0 && qh == 0))
           tc::mma_commit(&bars[4 + a]);  // (the test hook holds back the first one of one block)
       }
       __syncwarp();
@@ -1746,43 +1750,40 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
     __syncwarp();
     tc::mbar_wait(&bars[8], 0);
   } else {
-    // ---- state warps: row n of the transposed state, headdim values
+    // ---- state warps: row n of the transposed state, the block's 32 columns
     const int n = 32 * w + lane;
     const uint32_t lb = (uint32_t)(32 * w) << 16;
-    float S[kPmax];
+    float S[kQH];
     const float* s0 = dir == 0 ? p.init : p.dfinal;
 #pragma unroll
-    for (int q = 0; q < kPmax; ++q)
-      S[q] = (s0 && q < P && n < N) ? s0[(((long long)b * p.H + h) * P + q) * N + n] : 0.f;
+    for (int q = 0; q < kQH; ++q)
+      S[q] = (s0 && q0 + q < P && n < N) ? s0[(((long long)b * p.H + h) * P + q0 + q) * N + n] : 0.f;
     // the chunks' decays, loaded four steps ahead
     float dcur[4], dnext[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) dcur[i] = i < nc ? tabh[(long long)chunk_at(i) * p.H * kTabF + 128] : 1.f;
-    for (int s0 = 0; s0 < nc; s0 += 4) {
+    for (int s0i = 0; s0i < nc; s0i += 4) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        dnext[i] = s0 + 4 + i < nc ? tabh[(long long)chunk_at(s0 + 4 + i) * p.H * kTabF + 128] : 1.f;
+        dnext[i] = s0i + 4 + i < nc ? tabh[(long long)chunk_at(s0i + 4 + i) * p.H * kTabF + 128] : 1.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int s = s0 + i;
+        const int s = s0i + i;
         if (s >= nc) break;
         const int a = s & 1;
         const long long c = chunk_at(s);
-        {  // S out: row n into the two swizzled stage tiles, then two TMA stores
+        {  // S out: row n into the swizzled stage tile, then one TMA store
           unsigned char* stg = base + oStg;
-          if (t == 0) tc::bulk_wait_read<0>();  // the previous step's stores have read the stage
+          if (t == 0) tc::bulk_wait_read<0>();  // the previous step's store has read the stage
           asm volatile("bar.sync 2, 128;" ::: "memory");
 #pragma unroll
-          for (int q = 0; q < kPmax; q += 4)
-            *reinterpret_cast<float4*>(stg + (q >> 5) * 16384 + tc::sw128_offset(n, (q & 31) >> 2)) =
+          for (int q = 0; q < kQH; q += 4)
+            *reinterpret_cast<float4*>(stg + tc::sw128_offset(n, q >> 2)) =
                 make_float4(S[q], S[q + 1], S[q + 2], S[q + 3]);
           tc::fence_proxy_async_smem();
           asm volatile("bar.sync 2, 128;" ::: "memory");
           if (t == 0) {
-            const CUtensorMap* map = dir == 0 ? &map_st : &map_ad;
-            const int row0 = (int)((c * p.H + h) * N);
-            tc::tma_store_2d(map, stg, 0, row0);
-            if (P > 32) tc::tma_store_2d(map, stg + 16384, 32, row0);
+            tc::tma_store_2d(dir == 0 ? &map_st : &map_ad, stg, q0, (int)((c * p.H + h) * N));
             tc::bulk_commit();
           }
         }
@@ -1790,11 +1791,11 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
         ok &= bwait(&bars[4 + a], (s >> 1) & 1, abort_f, p.wait_polls);
         tc::tc_fence_after();
 #pragma unroll
-        for (int qb = 0; qb < kPmax; qb += 8) {  // columns qb.. of the hi half, 64 + qb.. of the lo half
+        for (int qb = 0; qb < kQH; qb += 8) {  // columns qb.. of the hi half, 32 + qb.. of the lo half
           float vh[8], vl[8];
-          const uint32_t col = tm + lb + 128 * a + qb;
+          const uint32_t col = tm + lb + 64 * a + qb;
           tc::tmem_ld8(col, vh);
-          tc::tmem_ld8(col + 64, vl);
+          tc::tmem_ld8(col + kQH, vl);
           tc::tmem_ld_wait();
           tc::tie8(vh);
           tc::tie8(vl);
@@ -1810,14 +1811,14 @@ __global__ void __launch_bounds__(sc::kThreads, 2)
     if (t == 0) tc::bulk_wait<0>();  // the state stores are complete
     if (dir == 1 && p.dinit && n < N) {
 #pragma unroll
-      for (int q = 0; q < kPmax; ++q)
-        if (q < P) p.dinit[(((long long)b * p.H + h) * P + q) * N + n] = S[q];
+      for (int q = 0; q < kQH; ++q)
+        if (q0 + q < P) p.dinit[(((long long)b * p.H + h) * P + q0 + q) * N + n] = S[q];
     }
   }
   if (!ok && p.status) atomicCAS(p.status, 0, (int)SSD_ERR_TIMEOUT);
   tc::tc_fence_before();
   __syncthreads();
-  if (w == 8) tc::tmem_dealloc(tm, 256);
+  if (w == 8) tc::tmem_dealloc(tm, 128);
 }
 
 }  // namespace
@@ -1910,7 +1911,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
     if (!tc_make_map_f32_sw128(&map_st, p.st, srows, a.P, a.N) ||
         !tc_make_map_f32_sw128(&map_ad, p.ad, srows, a.P, a.N))
       return SSD_ERR_CUDA;
-    bwd_scan_kernel<<<dim3((unsigned)a.H, (unsigned)a.batch, 2), sc::kThreads, sc::kSmem, a.stream>>>(
+    bwd_scan_kernel<<<dim3((unsigned)a.H, (unsigned)a.batch, 4), sc::kThreads, sc::kSmem, a.stream>>>(
         p, map_st, map_ad);
     bwd_grad_tc_kernel<<<ggrid, tg::kThreads, tg::kSmem, a.stream>>>(p);
     count_launches(3);
