@@ -919,7 +919,7 @@ constexpr uint32_t oB = 0, oC = 2 * kAtom, oX = 4 * kAtom, oWXh = 5 * kAtom, oWX
 // the direct dt terms by row and column group [4][64] and by column and row
 // group [4][64]; and (log2e cum_last, <dH, H>, sum_j w_j v_j, dD) [kHS][4]
 constexpr uint32_t kPart = 3 * 4 * kQb;  // partial sums per head
-constexpr uint32_t kTabFloats = 2 * 4 * kQb + kHS * kQb + kHS * kPart + 4 * kHS;
+constexpr uint32_t kTabFloats = 2 * 4 * kQb + kHS * kQb + kHS * kPart + 4 * kHS + kHS;
 constexpr uint32_t oBar = oTab + 4 * kTabFloats;
 constexpr uint32_t kSmem = oBar + 64 + 1024;  // + alignment of the tiles to 1024 bytes
 static_assert(kSmem <= 232448, "shared memory per block");
@@ -1014,6 +1014,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   float* dtsH = tabs + 8 * kQb;          // [kHS][64] dt per head (after the two 4 x 64 table buffers)
   float* partH = dtsH + kHS * kQb;       // [kHS][kPart] partial decay sums per head
   float* hsum = partH + kHS * kPart;     // [kHS][4] per head
+  float* atab = hsum + 4 * kHS;          // [kHS] log2e A per head
   // mbarriers, one phase per head each: C B^T (once), dS, group 1, group 2,
   // Xi; then the drain of the last MMAs (once)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);
@@ -1072,17 +1073,20 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     }
   };
   // One warp: the decay tables of slice head hh into buffer hh % 2 (lane l:
-  // rows 2l, 2l+1), its dt and log2e cum_last.
-  const auto tables = [&](int hh) {
+  // rows 2l, 2l+1) and its log2e cum_last, from the head's dt and A staged in
+  // shared memory by the prologue (head 0: from global memory, `fromg`).
+  const auto tables = [&](int hh, bool fromg) {
     const int h = hb + hh;
     float* c2 = tabs + 4 * (hh & 1) * kQb;
     float* ec = c2 + kQb;
     float* wt = ec + kQb;
     float* el = wt + kQb;
-    const float Ah = p.A[h] * kLog2e;
+    const float Ah = fromg ? p.A[h] * kLog2e : atab[hh];
     const int j0 = 2 * lane, j1 = j0 + 1;
-    const float d0 = j0 < len ? ldin<true>(p.dt, (k.tok0 + j0) * p.H + h) : 0.f;
-    const float d1 = j1 < len ? ldin<true>(p.dt, (k.tok0 + j1) * p.H + h) : 0.f;
+    const float d0 = fromg ? (j0 < len ? ldin<true>(p.dt, (k.tok0 + j0) * p.H + h) : 0.f)
+                           : dtsH[hh * kQb + j0];
+    const float d1 = fromg ? (j1 < len ? ldin<true>(p.dt, (k.tok0 + j1) * p.H + h) : 0.f)
+                           : dtsH[hh * kQb + j1];
     const float a1 = d1 * Ah;
     float s = d0 * Ah + a1;
 #pragma unroll
@@ -1178,7 +1182,15 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
       *reinterpret_cast<uint4*>(base + oC + swo(j, n)) = vc[r];
     }
     for (int e = t; e < (int)(kHS * kPart + 4 * kHS); e += kMathThreads) partH[e] = 0.f;  // partial sums
-    if (w == 0) tables(0);
+    if (w == 0) {
+      tables(0, true);
+    } else {  // the other heads' dt and A, for their tables later
+      for (int e = t - 32; e < (nh - 1) * kQb; e += kMathThreads - 32) {
+        const int hh = 1 + e / kQb, j = e % kQb;
+        dtsH[hh * kQb + j] = j < len ? ldin<true>(p.dt, (k.tok0 + j) * p.H + hb + hh) : 0.f;
+      }
+      if (t - 32 < nh) atab[t - 32] = p.A[hb + t - 32] * kLog2e;
+    }
     tc::fence_proxy_async_smem();
   } else {
     if (lane == 0) {
@@ -1346,7 +1358,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
           for (int o = 4; o < 32; o <<= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
           if (gq == 0) dcol[c16 + 8 * tt + 2 * tq + e] = b;
         }
-      if (w == 4 && hh + 1 < nh) tables(hh + 1);  // a warp whose dS block is masked
+      if (w == 4 && hh + 1 < nh) tables(hh + 1, false);  // a warp whose dS block is masked
       // the next head's x, dy, H, dH into registers (this head's are in shared memory)
       if (hh + 1 < nh) {
         load_head(h + 1);
