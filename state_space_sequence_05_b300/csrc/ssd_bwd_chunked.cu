@@ -83,6 +83,9 @@ struct BP {
   int hold;             // test hook: 1 / 2 hold back one MMA completion (gradients / scans)
   float* st;   // [chunks][H][P N]: chunk states, then the states entering each chunk
   float* ad;   // [chunks][H][P N]: local adjoint sums, then the adjoints leaving each chunk
+  // tensor-core path: the same two buffers hold the transposed states as bf16
+  // hi/lo pairs, [chunks][H][N][P] each (st = sth | stl, ad = adh | adl)
+  __nv_bfloat16 *sth, *stl, *adh, *adl;
   float* dec;  // [chunks][H]: exp(cum_last)
   float* tab;  // [chunks][H][144] (tensor-core path): forward weights, adjoint weights, decay
   int T, H, P, N, G, nc;  // nc: chunks per batch row
@@ -890,17 +893,17 @@ __global__ void __launch_bounds__(kThr) bwd_grad_kernel(BP p) {
 // headdim and dstate multiples of 8).  Per block (chunk, group, slice of up
 // to kHS heads of the group), 16 math warps and one MMA warp.  Operands are
 // 128-byte-swizzled bf16 tiles of 64 rows (exact for x, B, C; hi/lo pairs
-// for dy, exp(cum) dy, w x, H_c, dH_{c+1}, M and dG; H_c and dH_{c+1} as
-// stored by the state scans, transposed: 128 rows of dstate), zero-padded to
-// headdim 64 and dstate 128, read by the MMAs K-major or MN-major as each
-// product needs.  Accumulators (M = 64: row r in TMEM lane 32 (r / 16) + r % 16):
+// for dy, exp(cum) dy, w x, H_c, dH_{c+1}, M and dG; H_c and dH_{c+1} come
+// split and transposed, 128 rows of dstate, from the state scans by TMA
+// loads a head ahead), zero-padded to headdim 64 and dstate 128, read by the
+// MMAs K-major or MN-major as each product needs.  Accumulators (M = 64: row r in TMEM lane 32 (r / 16) + r % 16):
 //   dC (128 columns) += exp(cum) dY H + dG B       summed over the slice's heads
 //   dB (128 columns) += (w o X) dH + dG^T C
 //   S  = dY X^T (the first head's C B^T before it)   V = B dH^T
 //   Xi = M^T dY (D on M's diagonal: + D dy)          U = C H^T
 // Per head: operands -> smem; MMAs dS, V, U, dC, dB; the dS epilogue writes M
 // and dG; MMAs Xi, dC, dB; the epilogue of V, U, Xi writes dx and the decay
-// terms; warp 0 closes ddt and dA.  Every wait is bounded: one that runs out
+// terms, and the next head's H, dH loads start; warp 0 closes ddt and dA.  Every wait is bounded: one that runs out
 // records SSD_ERR_TIMEOUT and the block goes on (its results are then
 // undefined) and waits once more for its last MMAs before freeing TMEM.
 namespace tg {
@@ -1003,7 +1006,11 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile i
   return false;
 }
 
-__global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
+__global__ void __launch_bounds__(tg::kThreads, 1)
+    bwd_grad_tc_kernel(BP p, const __grid_constant__ CUtensorMap map_hh,
+                       const __grid_constant__ CUtensorMap map_hl,
+                       const __grid_constant__ CUtensorMap map_dh,
+                       const __grid_constant__ CUtensorMap map_dl) {
   using namespace tg;
   using tc::f2;
   extern __shared__ unsigned char tsm_raw[];
@@ -1016,10 +1023,11 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   float* hsum = partH + kHS * kPart;     // [kHS][4] per head
   float* atab = hsum + 4 * kHS;          // [kHS] log2e A per head
   // mbarriers, one phase per head each: C B^T (once), dS, group 1, group 2,
-  // Xi; then the drain of the last MMAs (once)
+  // Xi; then the drain of the last MMAs (once); and the TMA loads of H, dH
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);
   uint32_t* tptr = reinterpret_cast<uint32_t*>(base + oBar + 48);
   volatile int* abort_f = reinterpret_cast<volatile int*>(base + oBar + 52);
+  uint64_t* hdbar = reinterpret_cast<uint64_t*>(base + oBar + 56);
   const int c = blockIdx.x, g = blockIdx.y;
   const Chunk k = chunk_of(p, c);
   const int P = p.P, N = p.N, len = k.len;
@@ -1035,36 +1043,42 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   const __nv_bfloat16* xg = reinterpret_cast<const __nv_bfloat16*>(p.x);
   bool ok = true;  // every wait of this thread completed
 
-  // One head's x, dy, H_c, dH_{c+1} in registers (zero outside the valid
-  // rows, headdim and dstate), loaded a head ahead of their use.  Math
-  // thread t: x and dy of row t / 8, columns 8 (t % 8)..; float4 r of the
-  // transposed H and dH ([n][q]) at row (t + 512 r) / 16, columns
-  // 4 ((t + 512 r) % 16)..
+  // One head's x and dy in registers (zero outside the valid rows and
+  // headdim), loaded a head ahead of their use.  Math thread t: row t / 8,
+  // columns 8 (t % 8)..
   uint4 vx = make_uint4(0, 0, 0, 0);
-  float4 vy[2], vh[4], vd[4];
+  float4 vy[2];
   const auto load_head = [&](int h) {
-    const long long sOff = ((long long)c * p.H + h) * (long long)(P * N);
     const int j = t >> 3, q = (t & 7) * 8;
     const bool okr = j < len && q < P;
     const long long row = ((k.tok0 + j) * p.H + h) * P + q;
     vx = okr ? *reinterpret_cast<const uint4*>(xg + row) : make_uint4(0, 0, 0, 0);
     vy[0] = okr ? *reinterpret_cast<const float4*>(p.dy + row) : make_float4(0.f, 0.f, 0.f, 0.f);
     vy[1] = okr ? *reinterpret_cast<const float4*>(p.dy + row + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e4 = t + kMathThreads * r, n = e4 >> 4, qq = (e4 & 15) * 4;
-      const bool okh = n < N && qq < P;
-      vh[r] = okh ? __ldcg(reinterpret_cast<const float4*>(p.st + sOff + n * P + qq))
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-      vd[r] = okh ? __ldcg(reinterpret_cast<const float4*>(p.ad + sOff + n * P + qq))
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
   };
+  // H_c and dH_{c+1} of slice head hh (bf16 hi/lo pairs of the transposed
+  // states, as the state scans stored them) into their operand tiles by TMA,
+  // zero past dstate and headdim; completes phase hh of hdbar.  One thread.
+  const auto load_hd = [&](int hh) {
+    const int slab = (int)((long long)c * p.H + hb + hh);
+    tc::mbar_arrive_expect_tx(hdbar, 8u * kAtom);
+    tc::tma_load_3d(base + oHh, &map_hh, hdbar, 0, 0, slab);
+    tc::tma_load_3d(base + oHh + kAtom, &map_hh, hdbar, 0, 64, slab);
+    tc::tma_load_3d(base + oHl, &map_hl, hdbar, 0, 0, slab);
+    tc::tma_load_3d(base + oHl + kAtom, &map_hl, hdbar, 0, 64, slab);
+    tc::tma_load_3d(base + oDh, &map_dh, hdbar, 0, 0, slab);
+    tc::tma_load_3d(base + oDh + kAtom, &map_dh, hdbar, 0, 64, slab);
+    tc::tma_load_3d(base + oDl, &map_dl, hdbar, 0, 0, slab);
+    tc::tma_load_3d(base + oDl + kAtom, &map_dl, hdbar, 0, 64, slab);
+  };
+  int hd_issued = 0;  // thread 0: heads whose H, dH loads it issued
   const auto prefetch_head = [&](int h) {
     const long long sOff = ((long long)c * p.H + h) * (long long)(P * N);
     if (t == 0) {
-      tc::bulk_prefetch_l2(p.st + sOff, (uint32_t)(P * N * 4));
-      tc::bulk_prefetch_l2(p.ad + sOff, (uint32_t)(P * N * 4));
+      tc::bulk_prefetch_l2(p.sth + sOff, (uint32_t)(P * N * 2));
+      tc::bulk_prefetch_l2(p.stl + sOff, (uint32_t)(P * N * 2));
+      tc::bulk_prefetch_l2(p.adh + sOff, (uint32_t)(P * N * 2));
+      tc::bulk_prefetch_l2(p.adl + sOff, (uint32_t)(P * N * 2));
     } else if (t >= 32 && t < 32 + kQb && t - 32 < len) {
       const long long row = (k.tok0 + (t - 32)) * p.H + h;
       tc::prefetch_l2(xg + row * P);
@@ -1110,10 +1124,9 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     if (lane == 0) hsum[4 * hh] = lst;
   };
 
-  // The operands of slice head hh read only by the first MMA group: H_c,
-  // dH_{c+1} (hi/lo), w o x and exp(cum) o dy (hi/lo) from the registers
-  // (x, dy, H, dH of that head) and its tables; the block sums <dH, H> and
-  // dD of the head.  Math threads.
+  // The operands of slice head hh read only by the first MMA group besides
+  // H and dH: w o x and exp(cum) o dy (hi/lo) from the registers (x, dy of
+  // that head) and its tables; the block sum dD of the head.  Math threads.
   const auto store_early = [&](int hh) {
     const float* ec = tabs + (4 * (hh & 1) + 1) * kQb;
     const float* wt = ec + kQb;
@@ -1137,27 +1150,36 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     split8(sy, hi, lo);
     *reinterpret_cast<uint4*>(base + oEYh + o8) = hi;
     *reinterpret_cast<uint4*>(base + oEYl + o8) = lo;
-    f2 hd2{0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e4 = t + kMathThreads * r, n = e4 >> 4, qq = (e4 & 15) * 4;
-      const uint32_t o = swo(n, qq);
-      split4_at(base + oHh + o, base + oHl + o, vh[r]);
-      split4_at(base + oDh + o, base + oDl + o, vd[r]);
-      hd2 = tc::fma2(f2{vh[r].x, vh[r].y}, f2{vd[r].x, vd[r].y}, hd2);
-      hd2 = tc::fma2(f2{vh[r].z, vh[r].w}, f2{vd[r].z, vd[r].w}, hd2);
-    }
     tc::fence_proxy_async_smem();
-    float hdot = hd2.x + hd2.y, dd = dd2.x + dd2.y;
+    float dd = dd2.x + dd2.y;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      hdot += __shfl_xor_sync(0xffffffffu, hdot, o);
-      dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    for (int o = 16; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    if (lane == 0) atomicAdd(&hsum[4 * hh + 3], dd);
+  };
+  // <dH_{c+1}, H_c> of slice head hh from its operand tiles (hi + lo; both
+  // tiles share one layout, so equal offsets hold matching elements).  Math
+  // threads, after the tiles' TMA loads completed.
+  const auto hdot_tiles = [&](int hh) {
+    float hd = 0.f;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint32_t o = 16u * (uint32_t)(t + kMathThreads * r);
+      const uint4 a = *reinterpret_cast<const uint4*>(base + oHh + o);
+      const uint4 b = *reinterpret_cast<const uint4*>(base + oHl + o);
+      const uint4 d = *reinterpret_cast<const uint4*>(base + oDh + o);
+      const uint4 e = *reinterpret_cast<const uint4*>(base + oDl + o);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+      const uint32_t dw[4] = {d.x, d.y, d.z, d.w}, ew[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const f2 hv = tc::add2(tc::bf2(aw[i]), tc::bf2(bw[i]));
+        const f2 dv = tc::add2(tc::bf2(dw[i]), tc::bf2(ew[i]));
+        hd = fmaf(hv.x, dv.x, fmaf(hv.y, dv.y, hd));
+      }
     }
-    if (lane == 0) {
-      atomicAdd(&hsum[4 * hh + 1], hdot);
-      atomicAdd(&hsum[4 * hh + 3], dd);
-    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
+    if (lane == 0) atomicAdd(&hsum[4 * hh + 1], hd);
   };
 
   // ---- prologue: B, C tiles; the first head's operands and tables; TMEM; C B^T
@@ -1196,6 +1218,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     if (lane == 0) {
 #pragma unroll
       for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
+      tc::mbar_init(hdbar, 1);
       *abort_f = 0;
       tc::fence_mbar_init();
     }
@@ -1207,6 +1230,10 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tm = *tptr;
+  if (t == 0) {  // the first head's H, dH
+    load_hd(0);
+    hd_issued = 1;
+  }
   // operand descriptors: one K-major and one MN-major base, the tiles at
   // constant offsets from it (start-address field, 16-byte units)
   const uint64_t kd0 = tc::sdesc_sw128(sb, 16, 1024), md0 = tc::sdesc_sw128(sb, kAtom, 1024);
@@ -1269,6 +1296,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
         }
         if (!(p.hold == 1 && hh == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0))
           tc::mma_commit(&bars[1]);  // (the test hook holds back the first one of block 0)
+        ok &= bwait(hdbar, par, abort_f, p.wait_polls);  // this head's H, dH in their tiles
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const bool acc = hh > 0 || kk > 0;
@@ -1358,6 +1386,8 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
           for (int o = 4; o < 32; o <<= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
           if (gq == 0) dcol[c16 + 8 * tt + 2 * tq + e] = b;
         }
+      ok &= bwait(hdbar, par, abort_f, p.wait_polls);
+      hdot_tiles(hh);
       if (w == 4 && hh + 1 < nh) tables(hh + 1, false);  // a warp whose dS block is masked
       // the next head's x, dy, H, dH into registers (this head's are in shared memory)
       if (hh + 1 < nh) {
@@ -1393,6 +1423,14 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
       // ---- V, U: the state terms of the decay; then dx = Xi + w_j V
       ok &= bwait(&bars[2], par, abort_f, p.wait_polls);
       tc::tc_fence_after();
+      // group 1 and the <dH, H> sums are done with the H, dH tiles: the next
+      // head's go in (after this head's loads completed, so that the phases
+      // of hdbar never overlap, even after an expired wait)
+      if (t == 0 && hh + 1 < nh && hd_issued == hh + 1 &&
+          tc::mbar_wait(hdbar, (uint32_t)(hh & 1), p.wait_polls)) {
+        load_hd(hh + 1);
+        hd_issued = hh + 2;
+      }
       float va[8], ua[8];
       ld_frag2(tm + lanebase + cV + c16, va);
       ld_frag2(tm + lanebase + cU + c16, ua);
@@ -1536,6 +1574,9 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
     }
   }
   if (!ok && p.status) atomicCAS(p.status, 0, (int)SSD_ERR_TIMEOUT);
+  // the last H, dH loads complete before the block's shared memory goes
+  // (they all did unless a wait expired; bounded)
+  if (t == 0 && hd_issued > 0) (void)tc::mbar_wait(hdbar, (uint32_t)((hd_issued - 1) & 1), p.wait_polls);
   tc::tc_fence_before();
   __syncthreads();
   if (!math) {  // every MMA of the block complete before its tensor memory is freed
@@ -1553,17 +1594,19 @@ __global__ void __launch_bounds__(tg::kThreads, 1) bwd_grad_tc_kernel(BP p) {
 // leaving each chunk (backwards from dL/dfinal) for the tcgen05 gradient
 // kernel: one block per (head, batch row, direction, half of headdim) walks
 // the row's chunks in order with its 128 x 32 part of the state in
-// registers, so every state is written once.  Storage is transposed: st, ad
-// [chunk][head][n][q] (dstate rows of headdim values); dinit
-// [batch][head][q][n].  Per chunk the local sum
+// registers, so every state is written once.  Storage is transposed and
+// split for the gradient kernel's operands: bf16 hi/lo pairs (hi = rn(v), lo
+// = rn(v - hi)), each [chunk][head][n][q] (dstate rows of headdim values), in
+// the workspace of the fp32 states; dinit [batch][head][q][n] in fp32.  Per
+// chunk the local sum
 //   forwards:  sum_j B_j (w_j x_j)^T,       w_j = exp(cum_last - cum_j) dt_j
 //   backwards: sum_i C_i (exp(cum_i) dy_i)^T
 // over the block's 32 columns is one M = 128 (n) x N = 64 tcgen05 product
 // over the chunk's 64 tokens: B^T (or C^T) read MN-major, times the weighted
 // rows as [hi | lo] (32 columns each) in one MN-major tile; the state then
 // becomes exp(cum_last) state + hi + lo.  Warps 0-3 hold the state (row n =
-// TMEM lane n) and write it out through a 128B-swizzled shared tile with a
-// TMA store, warps 4-7 stage and convert the operands of a two-slot ring,
+// TMEM lane n) and write it out through two 64B-swizzled shared tiles (hi,
+// lo) with TMA stores, warps 4-7 stage and convert the operands of a two-slot ring,
 // warp 8 issues the MMAs into a double-buffered accumulator.  Three blocks
 // fit on an SM.  Every wait is bounded (SSD_ERR_TIMEOUT).
 namespace sc {
@@ -1574,7 +1617,8 @@ constexpr uint32_t kSlotBytes = 3 * kAtom;  // U (64 tokens x [hi 32 | lo 32]), 
 constexpr int kThreads = 32 * 9;
 constexpr int kTabF = 144;  // floats per (chunk, head) of the weight table
 constexpr uint32_t oTab = kStages * kSlotBytes;  // [2][64] the slots' row weights
-constexpr uint32_t oStg = oTab + 1024;           // [128 rows][32 fp32] 128B-swizzled tile: the state out
+constexpr uint32_t oStg = oTab + 1024;  // [2][128 rows][32 bf16] 64B-swizzled tiles: the state out (hi, lo)
+constexpr uint32_t kStgHalf = 8192;
 constexpr uint32_t oBar = oStg + 16384;  // full[2], empty[2], acc full[2], acc free[2], drain; TMEM base
 constexpr uint32_t kSmem = oBar + 128 + 1024;
 constexpr uint32_t kId = tc::idesc_bf16(128, 64, true, true);
@@ -1611,8 +1655,10 @@ __global__ void __launch_bounds__(256) bwd_tab_kernel(BP p) {
 }
 
 __global__ void __launch_bounds__(sc::kThreads, 3)
-    bwd_scan_kernel(BP p, const __grid_constant__ CUtensorMap map_st,
-                    const __grid_constant__ CUtensorMap map_ad) {
+    bwd_scan_kernel(BP p, const __grid_constant__ CUtensorMap map_sth,
+                    const __grid_constant__ CUtensorMap map_stl,
+                    const __grid_constant__ CUtensorMap map_adh,
+                    const __grid_constant__ CUtensorMap map_adl) {
   using namespace sc;
   using tc::f2;
   const int h = blockIdx.x, b = blockIdx.y, dir = blockIdx.z >> 1, qh = blockIdx.z & 1;
@@ -1784,18 +1830,27 @@ __global__ void __launch_bounds__(sc::kThreads, 3)
         if (s >= nc) break;
         const int a = s & 1;
         const long long c = chunk_at(s);
-        {  // S out: row n into the swizzled stage tile, then one TMA store
+        {  // S out as bf16 hi/lo pairs (the gradient kernel's operand split):
+           // row n into two 64-byte-swizzled stage tiles, then two TMA stores
           unsigned char* stg = base + oStg;
-          if (t == 0) tc::bulk_wait_read<0>();  // the previous step's store has read the stage
+          if (t == 0) tc::bulk_wait_read<0>();  // the previous step's stores have read the stage
           asm volatile("bar.sync 2, 128;" ::: "memory");
 #pragma unroll
-          for (int q = 0; q < kQH; q += 4)
-            *reinterpret_cast<float4*>(stg + tc::sw128_offset(n, q >> 2)) =
-                make_float4(S[q], S[q + 1], S[q + 2], S[q + 3]);
+          for (int cq = 0; cq < kQH / 8; ++cq) {
+            const f2 v[4] = {f2{S[8 * cq], S[8 * cq + 1]}, f2{S[8 * cq + 2], S[8 * cq + 3]},
+                             f2{S[8 * cq + 4], S[8 * cq + 5]}, f2{S[8 * cq + 6], S[8 * cq + 7]}};
+            uint4 hi, lo;
+            tg::split8(v, hi, lo);
+            const uint32_t o = (uint32_t)n * 64u + ((uint32_t)(cq ^ ((n >> 1) & 3)) << 4);
+            *reinterpret_cast<uint4*>(stg + o) = hi;
+            *reinterpret_cast<uint4*>(stg + kStgHalf + o) = lo;
+          }
           tc::fence_proxy_async_smem();
           asm volatile("bar.sync 2, 128;" ::: "memory");
           if (t == 0) {
-            tc::tma_store_2d(dir == 0 ? &map_st : &map_ad, stg, q0, (int)((c * p.H + h) * N));
+            const int row = (int)((c * p.H + h) * N);
+            tc::tma_store_2d(dir == 0 ? &map_sth : &map_adh, stg, q0, row);
+            tc::tma_store_2d(dir == 0 ? &map_stl : &map_adl, stg + kStgHalf, q0, row);
             tc::bulk_commit();
           }
         }
@@ -1918,14 +1973,22 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
                    al(a.dinit, 3);
   if (tcp) {
     bwd_tab_kernel<<<dim3((unsigned)nch, (unsigned)((a.H + 7) / 8)), 256, 0, a.stream>>>(p);
-    CUtensorMap map_st, map_ad;
-    const long long srows = nch * a.H * a.N;
-    if (!tc_make_map_f32_sw128(&map_st, p.st, srows, a.P, a.N) ||
-        !tc_make_map_f32_sw128(&map_ad, p.ad, srows, a.P, a.N))
-      return SSD_ERR_CUDA;
+    // the transposed states as bf16 hi/lo pairs: stored by the scans (32
+    // columns x N rows per step), loaded by the gradient kernel (64 x 64 tiles)
+    const long long selems = nch * a.H * a.N * a.P, slabs = nch * a.H;
+    p.sth = reinterpret_cast<__nv_bfloat16*>(p.st);
+    p.stl = p.sth + selems;
+    p.adh = reinterpret_cast<__nv_bfloat16*>(p.ad);
+    p.adl = p.adh + selems;
+    CUtensorMap ms[4], ml[4];
+    __nv_bfloat16* const sp[4] = {p.sth, p.stl, p.adh, p.adl};
+    for (int i = 0; i < 4; ++i)
+      if (!tc_make_map_bf16_sw64(&ms[i], sp[i], slabs * a.N, a.P, a.N) ||
+          !tc_make_map_bf16_slab_sw128(&ml[i], sp[i], slabs, a.N, a.P))
+        return SSD_ERR_CUDA;
     bwd_scan_kernel<<<dim3((unsigned)a.H, (unsigned)a.batch, 4), sc::kThreads, sc::kSmem, a.stream>>>(
-        p, map_st, map_ad);
-    bwd_grad_tc_kernel<<<ggrid, tg::kThreads, tg::kSmem, a.stream>>>(p);
+        p, ms[0], ms[1], ms[2], ms[3]);
+    bwd_grad_tc_kernel<<<ggrid, tg::kThreads, tg::kSmem, a.stream>>>(p, ml[0], ml[1], ml[2], ml[3]);
     count_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
   }

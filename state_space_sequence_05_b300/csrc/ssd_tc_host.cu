@@ -151,6 +151,37 @@ bool tc_make_map_f32_sw128(CUtensorMap* m, float* ptr, long long rows, long long
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 [rows][cols] (the backward's hi/lo state tiles as the state scans
+// store them): a box is 32 columns (64 bytes) x box_rows rows, 64-byte swizzle.
+bool tc_make_map_bf16_sw64(CUtensorMap* m, void* ptr, long long rows, long long cols,
+                           int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 [slabs][rows][cols] (the same tiles as the gradient kernel loads
+// them): a box is 64 columns (128 bytes) x 64 rows of one slab, 128-byte
+// swizzle; elements past rows or cols read as zero.
+bool tc_make_map_bf16_slab_sw128(CUtensorMap* m, const void* ptr, long long slabs, long long rows,
+                                 long long cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)slabs};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(cols * rows) * 2};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // bf16 y (the fused-epilogue option): a box is 16 columns (32 bytes) x 32
 // rows, unswizzled.
 bool tc_make_map_y_bf16(CUtensorMap* m, void* ptr, long long rows, long long cols) {

@@ -40,6 +40,15 @@ bool tc_make_map_y_f32(CUtensorMap* m, float* ptr, long long rows, long long col
 // swizzle (the backward's state tiles; box_rows <= 256).
 bool tc_make_map_f32_sw128(CUtensorMap* m, float* ptr, long long rows, long long cols,
                            int box_rows);
+// bf16 [rows][cols]: 32-column (64-byte) x box_rows-row boxes, 64-byte
+// swizzle (the backward's state tiles as stored; box_rows <= 256).
+bool tc_make_map_bf16_sw64(CUtensorMap* m, void* ptr, long long rows, long long cols,
+                           int box_rows);
+// bf16 [slabs][rows][cols] as a 3-D tensor: 64-column (128-byte) x 64-row x
+// 1-slab boxes, 128-byte swizzle, zero fill past rows and cols (the
+// backward's state tiles as loaded into the MMA operands).
+bool tc_make_map_bf16_slab_sw128(CUtensorMap* m, const void* ptr, long long slabs, long long rows,
+                                 long long cols);
 // bf16 y: 16-column (32-byte) x 32-row boxes, unswizzled.
 bool tc_make_map_y_bf16(CUtensorMap* m, void* ptr, long long rows, long long cols);
 
