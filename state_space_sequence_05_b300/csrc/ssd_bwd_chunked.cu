@@ -1157,13 +1157,13 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
     if (lane == 0) atomicAdd(&hsum[4 * hh + 3], dd);
   };
   // <dH_{c+1}, H_c> of slice head hh from its operand tiles (hi + lo; both
-  // tiles share one layout, so equal offsets hold matching elements).  Math
-  // threads, after the tiles' TMA loads completed.
-  const auto hdot_tiles = [&](int hh) {
+  // tiles share one layout, so equal offsets hold matching elements), by
+  // five warps (index iw), after the tiles' TMA loads completed.
+  const auto hdot_tiles = [&](int hh, int iw) {
     float hd = 0.f;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const uint32_t o = 16u * (uint32_t)(t + kMathThreads * r);
+#pragma unroll 1
+    for (int k16 = 32 * iw + lane; k16 < (int)(2 * kAtom / 16); k16 += 5 * 32) {
+      const uint32_t o = 16u * (uint32_t)k16;
       const uint4 a = *reinterpret_cast<const uint4*>(base + oHh + o);
       const uint4 b = *reinterpret_cast<const uint4*>(base + oHl + o);
       const uint4 d = *reinterpret_cast<const uint4*>(base + oDh + o);
@@ -1204,6 +1204,9 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
       *reinterpret_cast<uint4*>(base + oC + swo(j, n)) = vc[r];
     }
     for (int e = t; e < (int)(kHS * kPart + 4 * kHS); e += kMathThreads) partH[e] = 0.f;  // partial sums
+    // M and dG: the blocks above the diagonal stay zero (no warp writes them)
+    for (int e = t; e < (int)(4 * kAtom / 16); e += kMathThreads)
+      *reinterpret_cast<uint4*>(base + oMh + 16 * e) = make_uint4(0, 0, 0, 0);
     if (w == 0) {
       tables(0, true);
     } else {  // the other heads' dt and A, for their tables later
@@ -1319,77 +1322,83 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
       __syncwarp();
     } else {
       // ---- dS epilogue: M = G L dt (+ D on the diagonal), dG = dS L dt;
-      //      the decay terms of the quadratic form (rows r16.., columns c16..)
-      ok &= bwait(&bars[1], par, abort_f, p.wait_polls);
-      tc::tc_fence_after();
-      float sa[8];
-      ld_frag2(tm + lanebase + cS + c16, sa);
-      tc::tmem_ld_wait();
-      tc::tie8(sa);
-      const float Dd = p.D ? p.D[h] : 0.f;
-      float rowT[2] = {0.f, 0.f}, colU[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-      const float c2i[2] = {c2[r16 + gq], c2[r16 + gq + 8]};
-      float c2j[4], dtj[4];
+      //      the decay terms of the quadratic form (rows r16.., columns
+      //      c16..), by the warps whose block meets the causal mask; of the
+      //      others, warp 4 makes the next head's tables and five sum <dH, H>
+      if (cg <= qd) {
+        ok &= bwait(&bars[1], par, abort_f, p.wait_polls);
+        tc::tc_fence_after();
+        float sa[8];
+        ld_frag2(tm + lanebase + cS + c16, sa);
+        tc::tmem_ld_wait();
+        tc::tie8(sa);
+        const float Dd = p.D ? p.D[h] : 0.f;
+        float rowT[2] = {0.f, 0.f}, colU[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        const float c2i[2] = {c2[r16 + gq], c2[r16 + gq + 8]};
+        float c2j[4], dtj[4];
 #pragma unroll
-      for (int f = 0; f < 4; ++f) {
-        const int j = c16 + 8 * (f >> 1) + 2 * tq + (f & 1);
-        c2j[f] = c2[j];
-        dtj[f] = dts[j];
-      }
+        for (int f = 0; f < 4; ++f) {
+          const int j = c16 + 8 * (f >> 1) + 2 * tq + (f & 1);
+          c2j[f] = c2[j];
+          dtj[f] = dts[j];
+        }
 #pragma unroll
-      for (int tt = 0; tt < 2; ++tt) {
+        for (int tt = 0; tt < 2; ++tt) {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int i = r16 + gq + 8 * hf;
+            float mv[2], dv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int j = c16 + 8 * tt + 2 * tq + e;
+              const int f = 4 * tt + 2 * hf + e;
+              mv[e] = dv[e] = 0.f;
+              if (j <= i && i < len) {
+                const float L = tc::fast_exp2(c2i[hf] - c2j[2 * tt + e]);
+                const float GL = gr[f] * L;
+                mv[e] = GL * dtj[2 * tt + e];
+                dv[e] = sa[f] * L * dtj[2 * tt + e];
+                rowT[hf] = fmaf(sa[f], mv[e], rowT[hf]);
+                colU[tt][e] = fmaf(sa[f], GL, colU[tt][e]);
+                if (i == j) mv[e] += Dd;
+              }
+            }
+            uint32_t mh, ml, gh, gl;
+            split2rn(f2{mv[0], mv[1]}, mh, ml);
+            split2rn(f2{dv[0], dv[1]}, gh, gl);
+            const uint32_t o = swo(i, c16 + 8 * tt + 2 * tq);
+            *reinterpret_cast<uint32_t*>(base + oMh + o) = mh;
+            *reinterpret_cast<uint32_t*>(base + oMl + o) = ml;
+            *reinterpret_cast<uint32_t*>(base + oGh + o) = gh;
+            *reinterpret_cast<uint32_t*>(base + oGl + o) = gl;
+          }
+        }
+        tc::fence_proxy_async_smem();
+        // partial sums, one writer per slot: rows (quad sums) and columns
+        // (column j: sum_i dS M = dt_j sum_i dS G L; sums over the warp's rows)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          const int i = r16 + gq + 8 * hf;
-          float mv[2], dv[2];
+          float v = rowT[hf];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          if (tq == 0) rrow[r16 + gq + 8 * hf] = v;
+        }
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int j = c16 + 8 * tt + 2 * tq + e;
-            const int f = 4 * tt + 2 * hf + e;
-            mv[e] = dv[e] = 0.f;
-            if (j <= i && i < len) {
-              const float L = tc::fast_exp2(c2i[hf] - c2j[2 * tt + e]);
-              const float GL = gr[f] * L;
-              mv[e] = GL * dtj[2 * tt + e];
-              dv[e] = sa[f] * L * dtj[2 * tt + e];
-              rowT[hf] = fmaf(sa[f], mv[e], rowT[hf]);
-              colU[tt][e] = fmaf(sa[f], GL, colU[tt][e]);
-              if (i == j) mv[e] += Dd;
-            }
+            float b = colU[tt][e];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+            if (gq == 0) dcol[c16 + 8 * tt + 2 * tq + e] = b;
           }
-          uint32_t mh, ml, gh, gl;
-          split2rn(f2{mv[0], mv[1]}, mh, ml);
-          split2rn(f2{dv[0], dv[1]}, gh, gl);
-          const uint32_t o = swo(i, c16 + 8 * tt + 2 * tq);
-          *reinterpret_cast<uint32_t*>(base + oMh + o) = mh;
-          *reinterpret_cast<uint32_t*>(base + oMl + o) = ml;
-          *reinterpret_cast<uint32_t*>(base + oGh + o) = gh;
-          *reinterpret_cast<uint32_t*>(base + oGl + o) = gl;
-        }
+      } else if (w != 4) {
+        ok &= bwait(hdbar, par, abort_f, p.wait_polls);
+        hdot_tiles(hh, cg == 2 ? qd : 2 + qd);
+      } else if (hh + 1 < nh) {
+        tables(hh + 1, false);
       }
-      tc::fence_proxy_async_smem();
-      // partial sums, one writer per slot: rows (quad sums) and columns
-      // (column j: sum_i dS M = dt_j sum_i dS G L; sums over the warp's rows)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float v = rowT[hf];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        if (tq == 0) rrow[r16 + gq + 8 * hf] = v;
-      }
-#pragma unroll
-      for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float b = colU[tt][e];
-#pragma unroll
-          for (int o = 4; o < 32; o <<= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
-          if (gq == 0) dcol[c16 + 8 * tt + 2 * tq + e] = b;
-        }
-      ok &= bwait(hdbar, par, abort_f, p.wait_polls);
-      hdot_tiles(hh);
-      if (w == 4 && hh + 1 < nh) tables(hh + 1, false);  // a warp whose dS block is masked
-      // the next head's x, dy, H, dH into registers (this head's are in shared memory)
+      // the next head's x, dy into registers (this head's are in shared memory)
       if (hh + 1 < nh) {
         load_head(h + 1);
         if (hh + 2 < nh) prefetch_head(h + 2);
