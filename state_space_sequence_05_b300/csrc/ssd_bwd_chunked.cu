@@ -920,9 +920,11 @@ constexpr uint32_t oB = 0, oC = 2 * kAtom, oX = 4 * kAtom, oWXh = 5 * kAtom, oWX
 // cum)) [64]; per head of the slice dt [kHS][64]; per head the partial decay
 // sums, each slot with one writer: dL/dcum by row and column group [4][64],
 // the direct dt terms by row and column group [4][64] and by column and row
-// group [4][64]; and (log2e cum_last, <dH, H>, sum_j w_j v_j, dD) [kHS][4]
+// group [4][64]; log2e cum_last [kHS][4] (every fourth); log2e A [kHS]; and
+// per warp (one writer each) the partial sums of <dH, H>, sum_j w_j v_j and
+// dD [kHS][3][16]
 constexpr uint32_t kPart = 3 * 4 * kQb;  // partial sums per head
-constexpr uint32_t kTabFloats = 2 * 4 * kQb + kHS * kQb + kHS * kPart + 4 * kHS + kHS;
+constexpr uint32_t kTabFloats = 2 * 4 * kQb + kHS * kQb + kHS * kPart + 4 * kHS + kHS + 48 * kHS;
 constexpr uint32_t oBar = oTab + 4 * kTabFloats;
 constexpr uint32_t kSmem = oBar + 64 + 1024;  // + alignment of the tiles to 1024 bytes
 static_assert(kSmem <= 232448, "shared memory per block");
@@ -1022,6 +1024,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
   float* partH = dtsH + kHS * kQb;       // [kHS][kPart] partial decay sums per head
   float* hsum = partH + kHS * kPart;     // [kHS][4] per head
   float* atab = hsum + 4 * kHS;          // [kHS] log2e A per head
+  float* wsum = atab + kHS;              // [kHS][3][16] per-warp sums: <dH, H>, sum w v, dD
   // mbarriers, one phase per head each: C B^T (once), dS, group 1, group 2,
   // Xi; then the drain of the last MMAs (once); and the TMA loads of H, dH
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + oBar);
@@ -1071,7 +1074,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
     tc::tma_load_3d(base + oDl, &map_dl, hdbar, 0, 0, slab);
     tc::tma_load_3d(base + oDl + kAtom, &map_dl, hdbar, 0, 64, slab);
   };
-  int hd_issued = 0;  // thread 0: heads whose H, dH loads it issued
+  int hd_issued = 0;  // MMA warp, lane 0: heads whose H, dH loads it issued
   const auto prefetch_head = [&](int h) {
     const long long sOff = ((long long)c * p.H + h) * (long long)(P * N);
     if (t == 0) {
@@ -1154,7 +1157,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
     float dd = dd2.x + dd2.y;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
-    if (lane == 0) atomicAdd(&hsum[4 * hh + 3], dd);
+    if (lane == 0) wsum[(hh * 3 + 2) * 16 + w] = dd;
   };
   // <dH_{c+1}, H_c> of slice head hh from its operand tiles (hi + lo; both
   // tiles share one layout, so equal offsets hold matching elements), by
@@ -1179,7 +1182,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
-    if (lane == 0) atomicAdd(&hsum[4 * hh + 1], hd);
+    if (lane == 0) wsum[hh * 3 * 16 + iw] = hd;
   };
 
   // ---- prologue: B, C tiles; the first head's operands and tables; TMEM; C B^T
@@ -1233,7 +1236,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tm = *tptr;
-  if (t == 0) {  // the first head's H, dH
+  if (w == kMathWarps && lane == 0) {  // the first head's H, dH
     load_hd(0);
     hd_issued = 1;
   }
@@ -1428,18 +1431,21 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
         tc::mma_commit(&bars[3]);
       }
       __syncwarp();
-    } else {
-      // ---- V, U: the state terms of the decay; then dx = Xi + w_j V
-      ok &= bwait(&bars[2], par, abort_f, p.wait_polls);
-      tc::tc_fence_after();
-      // group 1 and the <dH, H> sums are done with the H, dH tiles: the next
-      // head's go in (after this head's loads completed, so that the phases
-      // of hdbar never overlap, even after an expired wait)
-      if (t == 0 && hh + 1 < nh && hd_issued == hh + 1 &&
+      // once group 1 completed (the <dH, H> sums were done before the second
+      // barrier), the H, dH tiles are free: the next head's go in, after this
+      // head's loads completed (the phases of hdbar never overlap, even after
+      // an expired wait)
+      if (lane == 0 && hh + 1 < nh && hd_issued == hh + 1 &&
+          tc::mbar_wait(&bars[2], par, p.wait_polls) &&
           tc::mbar_wait(hdbar, (uint32_t)(hh & 1), p.wait_polls)) {
         load_hd(hh + 1);
         hd_issued = hh + 2;
       }
+      __syncwarp();
+    } else {
+      // ---- V, U: the state terms of the decay; then dx = Xi + w_j V
+      ok &= bwait(&bars[2], par, abort_f, p.wait_polls);
+      tc::tc_fence_after();
       float va[8], ua[8];
       ld_frag2(tm + lanebase + cV + c16, va);
       ld_frag2(tm + lanebase + cU + c16, ua);
@@ -1477,7 +1483,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) wv_sum += __shfl_xor_sync(0xffffffffu, wv_sum, o);
-      if (lane == 0) atomicAdd(&hsum[4 * hh + 2], wv_sum);
+      if (lane == 0) wsum[(hh * 3 + 1) * 16 + w] = wv_sum;
       // the first group is done with H, dH, w o x and exp(cum) o dy: the next
       // head's go in now (its tables came with the second barrier)
       if (hh + 1 < nh) store_early(hh + 1);
@@ -1527,14 +1533,24 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
       dc = r - dts[j] * cu;
       dd = d + cu;
     };
-    const float extra = tc::fast_exp2(hsum[4 * hh]) * hsum[4 * hh + 1] + hsum[4 * hh + 2];
+    // the per-warp sums: <dH, H> (five warps), sum_j w_j v_j and dD (sixteen)
+    const float* ws = wsum + hh * 48;
+    float s_hd = lane < 5 ? ws[lane] : 0.f, s_wv = lane < 16 ? ws[16 + lane] : 0.f;
+    float s_dd = lane < 16 ? ws[32 + lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s_hd += __shfl_xor_sync(0xffffffffu, s_hd, o);
+      s_wv += __shfl_xor_sync(0xffffffffu, s_wv, o);
+      s_dd += __shfl_xor_sync(0xffffffffu, s_dd, o);
+    }
+    const float extra = tc::fast_exp2(hsum[4 * hh]) * s_hd + s_wv;
     const int j1 = kQb - 1 - 2 * lane, j2 = j1 - 1;  // lane l: entries 63 - 2l, 62 - 2l
     float dc1, dd1, dc2, dd2;
     sums(j1, dc1, dd1);
     sums(j2, dc2, dd2);
     const float a1 = dc1 + (j1 == len - 1 ? extra : 0.f);
     const float a2 = dc2 + (j2 == len - 1 ? extra : 0.f);
-    if (lane == 0 && p.dD) atomicAdd(p.dD + h, hsum[4 * hh + 3]);
+    if (lane == 0 && p.dD) atomicAdd(p.dD + h, s_dd);
     float v = a1 + a2;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1585,7 +1601,8 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
   if (!ok && p.status) atomicCAS(p.status, 0, (int)SSD_ERR_TIMEOUT);
   // the last H, dH loads complete before the block's shared memory goes
   // (they all did unless a wait expired; bounded)
-  if (t == 0 && hd_issued > 0) (void)tc::mbar_wait(hdbar, (uint32_t)((hd_issued - 1) & 1), p.wait_polls);
+  if (!math && lane == 0 && hd_issued > 0)
+    (void)tc::mbar_wait(hdbar, (uint32_t)((hd_issued - 1) & 1), p.wait_polls);
   tc::tc_fence_before();
   __syncthreads();
   if (!math) {  // every MMA of the block complete before its tensor memory is freed
