@@ -896,9 +896,12 @@ __global__ void __launch_bounds__(kThr) bwd_grad_kernel(BP p) {
 // for dy, exp(cum) dy, w x, H_c, dH_{c+1}, M and dG; H_c and dH_{c+1} come
 // split and transposed, 128 rows of dstate, from the state scans by TMA
 // loads a head ahead), zero-padded to headdim 64 and dstate 128, read by the
-// MMAs K-major or MN-major as each product needs.  Accumulators (M = 64: row r in TMEM lane 32 (r / 16) + r % 16):
-//   dC (128 columns) += exp(cum) dY H + dG B       summed over the slice's heads
-//   dB (128 columns) += (w o X) dH + dG^T C
+// MMAs K-major or MN-major as each product needs.  Accumulators, summed
+// over the slice's heads, transposed (M = 128: dstate row n in TMEM lane n;
+// 128 columns, token j in columns j and 64 + j, the products with the two
+// halves of a stacked hi/lo operand):
+//   dC^T += H^T (exp(cum) dY)^T + B^T dG^T          dB^T += dH^T (w o X)^T + C^T dG
+// and per head (M = 64: row r in TMEM lane 32 (r / 16) + r % 16):
 //   S  = dY X^T (the first head's C B^T before it)   V = B dH^T
 //   Xi = M^T dY (D on M's diagonal: + D dy)          U = C H^T
 // Per head: operands -> smem; MMAs dS, V, U, dC, dB; the dS epilogue writes M
@@ -931,9 +934,12 @@ static_assert(kSmem <= 232448, "shared memory per block");
 constexpr uint32_t cDC = 0, cDB = 128, cS = 256, cX = 320, cV = 384, cU = 448;  // TMEM columns
 constexpr uint32_t kIdKK64 = tc::idesc_bf16(64, 64, false, false);
 constexpr uint32_t kIdNN64 = tc::idesc_bf16(64, 64, true, true);
-constexpr uint32_t kIdKN128 = tc::idesc_bf16(64, 128, false, true);
-constexpr uint32_t kIdNN128 = tc::idesc_bf16(64, 128, true, true);
-constexpr uint32_t kIdKK128 = tc::idesc_bf16(64, 128, false, false);
+// the transposed dC, dB products: M = 128 (dstate), N = 128 (a stacked hi/lo
+// operand) or 64
+constexpr uint32_t kIdT128 = tc::idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdT64 = tc::idesc_bf16(128, 64, false, false);
+constexpr uint32_t kIdTMK = tc::idesc_bf16(128, 128, true, false);
+constexpr uint32_t kIdTMM = tc::idesc_bf16(128, 128, true, true);
 constexpr uint32_t kIdKN64 = tc::idesc_bf16(64, 64, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -957,19 +963,6 @@ __device__ __forceinline__ void ld_frag2(uint32_t taddr, float (&v)[8]) {
                : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-// the same for 32 columns (blocks b = 0..3)
-__device__ __forceinline__ void ld_frag4(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 // a pair of fp32 -> bf16 hi = rn(v), lo = rn(v - hi), packed (x in the low half)
 __device__ __forceinline__ void split2rn(tc::f2 v, uint32_t& hi, uint32_t& lo) {
@@ -1041,7 +1034,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
   const bool math = w < kMathWarps;
   const int gq = lane >> 2, tq = lane & 3;
   const int qd = w & 3, cg = w >> 2;  // math warps: TMEM lane quadrant (rows 16 qd..), column group
-  const int r16 = 16 * qd, c16 = 16 * cg, c32 = 32 * cg;
+  const int r16 = 16 * qd, c16 = 16 * cg;
   const uint32_t lanebase = (uint32_t)(32 * qd) << 16;
   const __nv_bfloat16* xg = reinterpret_cast<const __nv_bfloat16*>(p.x);
   bool ok = true;  // every wait of this thread completed
@@ -1292,7 +1285,8 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
     __syncthreads();
     tc::tc_fence_after();
 
-    // ---- group 1: dS = dY X^T; V = B dH^T; U = C H^T; dC += (ec o dY) H; dB += (w o X) dH
+    // ---- group 1: dS = dY X^T; V = B dH^T; U = C H^T; dC^T += H^T (ec o dY)^T;
+    //      dB^T += dH^T (w o X)^T
     if (!math) {
       if (tc::elect_one()) {
 #pragma unroll
@@ -1303,15 +1297,16 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
         if (!(p.hold == 1 && hh == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0))
           tc::mma_commit(&bars[1]);  // (the test hook holds back the first one of block 0)
         ok &= bwait(hdbar, par, abort_f, p.wait_polls);  // this head's H, dH in their tiles
+        // (H^T and dH^T are the tiles as stored, K-major over headdim; the hi
+        // and lo tiles of exp(cum) dy and of w x are adjacent: one operand of
+        // N = 128)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const bool acc = hh > 0 || kk > 0;
-          tc::mma_bf16(tm + cDC, KD(oEYh, kk), KD(oHh, kk), kIdKK128, acc);
-          tc::mma_bf16(tm + cDC, KD(oEYl, kk), KD(oHh, kk), kIdKK128, true);
-          tc::mma_bf16(tm + cDC, KD(oEYh, kk), KD(oHl, kk), kIdKK128, true);
-          tc::mma_bf16(tm + cDB, KD(oWXh, kk), KD(oDh, kk), kIdKK128, acc);
-          tc::mma_bf16(tm + cDB, KD(oWXl, kk), KD(oDh, kk), kIdKK128, true);
-          tc::mma_bf16(tm + cDB, KD(oWXh, kk), KD(oDl, kk), kIdKK128, true);
+          tc::mma_bf16(tm + cDC, KD(oHh, kk), KD(oEYh, kk), kIdT128, acc);
+          tc::mma_bf16(tm + cDC, KD(oHl, kk), KD(oEYh, kk), kIdT64, true);
+          tc::mma_bf16(tm + cDB, KD(oDh, kk), KD(oWXh, kk), kIdT128, acc);
+          tc::mma_bf16(tm + cDB, KD(oDl, kk), KD(oWXh, kk), kIdT64, true);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -1411,7 +1406,7 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
     __syncthreads();
     tc::tc_fence_after();
 
-    // ---- group 2: Xi = M^T dY; dC += dG B; dB += dG^T C
+    // ---- group 2: Xi = M^T dY; dC^T += B^T dG^T; dB^T += C^T dG
     if (!math) {
       if (tc::elect_one()) {
 #pragma unroll
@@ -1421,12 +1416,12 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
           tc::mma_bf16(tm + cX, MD(oMh, kk), MD(oYl, kk), kIdNN64, true);
         }
         tc::mma_commit(&bars[4]);
+        // (B^T, C^T: the tiles read MN-major; dG hi and lo adjacent: one
+        // operand of N = 128, K-major for dC, MN-major for dB)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          tc::mma_bf16(tm + cDC, KD(oGh, kk), MD(oB, kk), kIdKN128, true);
-          tc::mma_bf16(tm + cDC, KD(oGl, kk), MD(oB, kk), kIdKN128, true);
-          tc::mma_bf16(tm + cDB, MD(oGh, kk), MD(oC, kk), kIdNN128, true);
-          tc::mma_bf16(tm + cDB, MD(oGl, kk), MD(oC, kk), kIdNN128, true);
+          tc::mma_bf16(tm + cDC, MD(oB, kk), KD(oGh, kk), kIdTMK, true);
+          tc::mma_bf16(tm + cDB, MD(oC, kk), MD(oGh, kk), kIdTMM, true);
         }
         tc::mma_commit(&bars[3]);
       }
@@ -1572,28 +1567,28 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
     for (int o = 16; o > 0; o >>= 1) da += __shfl_xor_sync(0xffffffffu, da, o);
     if (lane == 0) atomicAdd(p.dA + h, da);
   }
-  // ---- dB, dC of the slice's heads (rows r16.., columns c32..)
+  // ---- dB, dC of the slice's heads: warp w, dstate rows 32 (w % 4) + lane,
+  //      tokens 16 (w / 4).. (columns j and 64 + j summed)
   if (math) {
-    float vc[16], vb[16];
-    ld_frag4(tm + lanebase + cDC + c32, vc);
-    ld_frag4(tm + lanebase + cDB + c32, vb);
+    float c0[16], c1[16], b0[16], b1[16];
+    tc::tmem_ld16(tm + lanebase + cDC + c16, c0);
+    tc::tmem_ld16(tm + lanebase + cDC + 64 + c16, c1);
+    tc::tmem_ld16(tm + lanebase + cDB + c16, b0);
+    tc::tmem_ld16(tm + lanebase + cDB + 64 + c16, b1);
     tc::tmem_ld_wait();
-    tc::tie16(vc);
-    tc::tie16(vb);
+    tc::tie16(c0);
+    tc::tie16(c1);
+    tc::tie16(b0);
+    tc::tie16(b1);
+    const int n = 32 * qd + lane;
+    if (n < N) {
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int j = r16 + gq + 8 * hf;
-      if (j < len) {
-        float* db = p.dB + ((k.tok0 + j) * p.G + g) * N;
-        float* dc = p.dC + ((k.tok0 + j) * p.G + g) * N;
-#pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-          const int n = c32 + 8 * tt + 2 * tq;
-          const int f = 4 * tt + 2 * hf;
-          if (n < N) {
-            atomicAdd(reinterpret_cast<float2*>(db + n), make_float2(vb[f], vb[f + 1]));
-            atomicAdd(reinterpret_cast<float2*>(dc + n), make_float2(vc[f], vc[f + 1]));
-          }
+      for (int e = 0; e < 16; ++e) {
+        const int j = c16 + e;
+        if (j < len) {
+          const long long row = ((k.tok0 + j) * p.G + g) * N + n;
+          atomicAdd(p.dC + row, c0[e] + c1[e]);
+          atomicAdd(p.dB + row, b0[e] + b1[e]);
         }
       }
     }
