@@ -908,9 +908,11 @@ def measure_epilogue(fi, wl, dev, d, A, D, init, ws, flush, peaks, reps=20):
 
 def measure_backward(fi, wl, dev, d, A, D, init, peaks, reps=3):
     """ssd_chunk_scan_bwd on the same layer with a seeded fp32 dL/dy: median of
-    `reps` calls (inputs larger than L2).  Algorithmic bytes: x, dt, B, C
-    (input dtype) and dy read once; dx, ddt, dB, dC, dinit and the two
-    per-head sums written once."""
+    `reps` calls, each bracketed by its own events after an L2 flush, with no
+    host synchronisation between them (as the forward steps are timed: the
+    host enqueues a call while the GPU runs the flush before it).
+    Algorithmic bytes: x, dt, B, C (input dtype) and dy read once; dx, ddt,
+    dB, dC, dinit and the two per-head sums written once."""
     import numpy as np
     import torch
     from state_space_sequence_05_b300 import ssd
@@ -928,17 +930,21 @@ def measure_backward(fi, wl, dev, d, A, D, init, peaks, reps=3):
         ssd.ssd_chunk_scan_bwd(d["x"], d["dt"], A, d["B"], d["C"], D, init, dy, workspace=ws,
                                dev_status=status, stream=stream)
 
+    flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
     call()
     torch.cuda.synchronize()
-    us = []
+    ev = []
     l0 = ssd.kernel_launches()
     for _ in range(reps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
         e0.record(stream)
         call()
         e1.record(stream)
-        torch.cuda.synchronize()
-        us.append(1e3 * e0.elapsed_time(e1))
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    us = [1e3 * e0.elapsed_time(e1) for e0, e1 in ev]
+    del flush
     if int(status.item()) != 0:
         raise RuntimeError(f"backward: device status {int(status.item())}")
     med = statistics.median(us)
