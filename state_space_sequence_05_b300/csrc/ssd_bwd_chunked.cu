@@ -1679,7 +1679,11 @@ __global__ void __launch_bounds__(sc::kThreads, 3)
     bwd_scan_kernel(BP p, const __grid_constant__ CUtensorMap map_sth,
                     const __grid_constant__ CUtensorMap map_stl,
                     const __grid_constant__ CUtensorMap map_adh,
-                    const __grid_constant__ CUtensorMap map_adl) {
+                    const __grid_constant__ CUtensorMap map_adl,
+                    const __grid_constant__ CUtensorMap map_b,
+                    const __grid_constant__ CUtensorMap map_c,
+                    const __grid_constant__ CUtensorMap map_x,
+                    const __grid_constant__ CUtensorMap map_dy) {
   using namespace sc;
   using tc::f2;
   const int h = blockIdx.x, b = blockIdx.y, dir = blockIdx.z >> 1, qh = blockIdx.z & 1;
@@ -1705,6 +1709,7 @@ __global__ void __launch_bounds__(sc::kThreads, 3)
       for (int i = 2; i < 6; ++i) tc::mbar_init(&bars[i], 1);    // empty, acc full: MMA commits
       for (int i = 6; i < 8; ++i) tc::mbar_init(&bars[i], 128);  // acc free: state threads
       tc::mbar_init(&bars[8], 1);                                // drain of the last MMAs
+      for (int i = 11; i < 13; ++i) tc::mbar_init(&bars[i], 1);  // copies landed (TMA)
       *abort_f = 0;
       tc::fence_mbar_init();
     }
@@ -1718,69 +1723,73 @@ __global__ void __launch_bounds__(sc::kThreads, 3)
   const uint32_t tm = *tptr;
 
   if (w >= 4 && w < 8) {
-    // ---- converters: copies of step s into slot s % 2, then w o x (or
-    //      exp(cum) o dy) for the block's 32 columns as [hi | lo] in one tile
+    // ---- converters: step s arrives in slot s % 2 by TMA (B or C rows, x or
+    //      dy rows, the row weights; one thread issues, bars[11 + slot] count
+    //      the bytes), then w o x (or exp(cum) o dy) for the block's 32
+    //      columns as [hi | lo] in one tile
     const int ct = t - 128;
-    const void* vsrc = dir == 0 ? p.B : p.C;
+    uint64_t* cfull = &bars[11];
+    int issued = 0;  // thread ct == 0: the steps whose copies it issued
     const auto issue = [&](int s) {
+      const int sl = s % kStages;
       const Chunk k = chunk_of(p, chunk_at(s));
-      unsigned char* st = base + (s % kStages) * kSlotBytes;
-      const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(vsrc);
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int e = ct + 128 * r, j = e >> 4, n8 = (e & 15) * 8;
-        const bool okc = j < k.len && n8 < N;
-        const __nv_bfloat16* src = vg + ((k.tok0 + (okc ? j : 0)) * p.G + g) * N + (okc ? n8 : 0);
-        tc::cp_async16_zfill(st + kAtom + tg::swo(j, n8), src, okc);
-      }
-      if (ct < 16)  // the step's row weights
-        tc::cp_async16(base + oTab + 256 * (s % kStages) + 16 * ct,
-                       tabh + (long long)chunk_at(s) * p.H * kTabF + 64 * dir + 4 * ct);
-      if (dir == 0) {  // x (bf16), 32 columns, straight into the hi half of the tile
-        const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x);
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int e = ct + 128 * r, j = e >> 2, q8 = (e & 3) * 8;
-          const bool okc = j < k.len && q0 + q8 < P;
-          const __nv_bfloat16* src =
-              xg + ((k.tok0 + (okc ? j : 0)) * p.H + h) * P + (okc ? q0 + q8 : 0);
-          tc::cp_async16_zfill(st + tg::swo(j, q8), src, okc);
-        }
-      } else {  // dy (fp32), 32 columns, as they are over the tile: row j at 128 j
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int e = ct + 128 * r, j = e >> 3, q4 = (e & 7) * 4;
-          const bool okc = j < k.len && q0 + q4 < P;
-          const float* src = p.dy + ((k.tok0 + (okc ? j : 0)) * p.H + h) * P + (okc ? q0 + q4 : 0);
-          tc::cp_async16_zfill(st + 16 * e, src, okc);
-        }
-      }
+      unsigned char* st = base + sl * kSlotBytes;
+      tc::mbar_arrive_expect_tx(&cfull[sl], 2 * kAtom + (dir == 0 ? kAtom / 2 : kAtom) + 256);
+      const CUtensorMap* mv = dir == 0 ? &map_b : &map_c;  // [tokens][G][N]: 64 tokens x 64 n
+      tc::tma_load_3d(st + kAtom, mv, &cfull[sl], 0, g, (int)k.tok0);
+      tc::tma_load_3d(st + 2 * kAtom, mv, &cfull[sl], 64, g, (int)k.tok0);
+      // x (bf16) or dy (fp32), 32 columns of 64 tokens, row j at 64 j (x) or 128 j (dy)
+      tc::tma_load_3d(st, dir == 0 ? &map_x : &map_dy, &cfull[sl], q0, h, (int)k.tok0);
+      tc::bulk_load(base + oTab + 256 * sl, tabh + (long long)chunk_at(s) * p.H * kTabF + 64 * dir,
+                    256, &cfull[sl]);
     };
-    issue(0);
-    tc::cp_async_commit();
+    // a slot's earlier copies complete (bounded) before it is refilled, so that
+    // the phases of its barrier never overlap, even after an expired wait
+    const auto issue_next = [&](int s) {
+      if (issued != s) return;
+      if (s >= kStages && !tc::mbar_wait(&cfull[s % kStages], ((s / kStages) - 1) & 1, p.wait_polls))
+        return;
+      issue(s);
+      issued = s + 1;
+    };
+    if (ct == 0) issue_next(0);
     for (int s = 0; s < nc; ++s) {
       const int slot = s % kStages;
       if (s + 1 < nc) {  // the next step's copies into the other slot, once its product is done
         const int s1 = s + 1;
         if (s1 >= kStages) ok &= bwait(&bars[2 + s1 % kStages], ((s1 / kStages) - 1) & 1, abort_f, p.wait_polls);
-        issue(s1);
+        if (ct == 0) issue_next(s1);
       }
-      tc::cp_async_commit();
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // every converter's copies of step s
+      ok &= bwait(&cfull[slot], (s / kStages) & 1, abort_f, p.wait_polls);
+      const int len = chunk_of(p, chunk_at(s)).len;
       const float* wrow = reinterpret_cast<const float*>(base + oTab + 256 * slot);
       unsigned char* st = base + slot * kSlotBytes;
+      if (len < kQb) {  // rows past a short chunk's end (the next tokens' B or C) read as zero
+        for (int e = ct; e < (kQb - len) * 16; e += 128) {
+          const int j = len + (e >> 4), c = e & 15;
+          *reinterpret_cast<uint4*>(st + kAtom + (c >> 3) * kAtom + 128 * j + 16 * (c & 7)) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
       if (dir == 0) {
+        uint4 xr[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int e = ct + 128 * r, j = e >> 2, q8 = (e & 3) * 8;
-          const float wj = wrow[j];
-          const uint4 xv = *reinterpret_cast<const uint4*>(st + tg::swo(j, q8));
+          xr[r] = *reinterpret_cast<const uint4*>(st + 64 * j + 2 * q8);
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the raw rows are read before the tile overwrites them
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int e = ct + 128 * r, j = e >> 2, q8 = (e & 3) * 8;
+          const float wj = j < len ? wrow[j] : 0.f;
+          const uint4 xv = xr[r];
           const f2 ww{wj, wj};
           const f2 v[4] = {tc::mul2(tc::bf2(xv.x), ww), tc::mul2(tc::bf2(xv.y), ww),
                            tc::mul2(tc::bf2(xv.z), ww), tc::mul2(tc::bf2(xv.w), ww)};
           uint4 hi, lo;
           tg::split8(v, hi, lo);
+          if (j >= len) hi = lo = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(st + tg::swo(j, q8)) = hi;
           *reinterpret_cast<uint4*>(st + tg::swo(j, kQH + q8)) = lo;
         }
@@ -1794,16 +1803,24 @@ __global__ void __launch_bounds__(sc::kThreads, 3)
           const int e = ct + 128 * r, j = e >> 3, q4 = (e & 7) * 4;
           const float wj = wrow[j];
           float4 v = raw[r];
-          v.x *= wj;
-          v.y *= wj;
-          v.z *= wj;
-          v.w *= wj;
+          if (j < len) {
+            v.x *= wj;
+            v.y *= wj;
+            v.z *= wj;
+            v.w *= wj;
+          } else {
+            v = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
           tg::split4_at(st + tg::swo(j, q4), st + tg::swo(j, kQH + q4), v);
         }
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars[slot]);
     }
+    // the last copies landed before the block's shared memory goes (bounded)
+    if (ct == 0)
+      for (int s = max(0, issued - kStages); s < issued; ++s)
+        (void)tc::mbar_wait(&cfull[s % kStages], (s / kStages) & 1, p.wait_polls);
   } else if (w == 8) {
     // ---- MMA warp
     for (int s = 0; s < nc; ++s) {
@@ -2007,8 +2024,17 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
       if (!tc_make_map_bf16_sw64(&ms[i], sp[i], slabs * a.N, a.P, a.N) ||
           !tc_make_map_bf16_slab_sw128(&ml[i], sp[i], slabs, a.N, a.P))
         return SSD_ERR_CUDA;
+    // the scans' per-step operands: B or C rows of one group (64 tokens x 64 of
+    // dstate, 128-byte swizzle), x or dy rows of one head (64 tokens x 32 of headdim)
+    CUtensorMap mb, mc, mx, mdy;
+    const long long ntok = (long long)a.batch * a.seqlen;
+    if (!tc_make_map_3d(&mb, a.B, 2, a.N, a.G, ntok, 64, 1, 64, true) ||
+        !tc_make_map_3d(&mc, a.C, 2, a.N, a.G, ntok, 64, 1, 64, true) ||
+        !tc_make_map_3d(&mx, a.x, 2, a.P, a.H, ntok, 32, 1, 64, false) ||
+        !tc_make_map_3d(&mdy, a.dy, 4, a.P, a.H, ntok, 32, 1, 64, false))
+      return SSD_ERR_CUDA;
     bwd_scan_kernel<<<dim3((unsigned)a.H, (unsigned)a.batch, 4), sc::kThreads, sc::kSmem, a.stream>>>(
-        p, ms[0], ms[1], ms[2], ms[3]);
+        p, ms[0], ms[1], ms[2], ms[3], mb, mc, mx, mdy);
     bwd_grad_tc_kernel<<<ggrid, tg::kThreads, tg::kSmem, a.stream>>>(p, ml[0], ml[1], ml[2], ml[3]);
     count_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;

@@ -182,6 +182,22 @@ bool tc_make_map_bf16_slab_sw128(CUtensorMap* m, const void* ptr, long long slab
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 3-D bf16 or fp32 tensor (the backward scans' per-step operands: B or C
+// rows of one group, x or dy rows of one head).
+bool tc_make_map_3d(CUtensorMap* m, const void* ptr, int elem_bytes, long long d0, long long d1,
+                    long long d2, int b0, int b1, int b2, bool sw128) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t strides[2] = {(cuuint64_t)(d0 * elem_bytes), (cuuint64_t)(d0 * d1 * elem_bytes)};
+  cuuint32_t box[3] = {(cuuint32_t)b0, (cuuint32_t)b1, (cuuint32_t)b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+             3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // bf16 y (the fused-epilogue option): a box is 16 columns (32 bytes) x 32
 // rows, unswizzled.
 bool tc_make_map_y_bf16(CUtensorMap* m, void* ptr, long long rows, long long cols) {

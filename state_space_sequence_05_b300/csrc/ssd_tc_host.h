@@ -49,6 +49,11 @@ bool tc_make_map_bf16_sw64(CUtensorMap* m, void* ptr, long long rows, long long 
 // backward's state tiles as loaded into the MMA operands).
 bool tc_make_map_bf16_slab_sw128(CUtensorMap* m, const void* ptr, long long slabs, long long rows,
                                  long long cols);
+// A 3-D tensor of bf16 (elem_bytes 2) or fp32 (4) values, dims d0 (innermost)
+// .. d2, with b0 x b1 x b2 boxes, unswizzled or 128-byte swizzled; zero fill
+// past the dims.
+bool tc_make_map_3d(CUtensorMap* m, const void* ptr, int elem_bytes, long long d0, long long d1,
+                    long long d2, int b0, int b1, int b2, bool sw128);
 // bf16 y: 16-column (32-byte) x 32-row boxes, unswizzled.
 bool tc_make_map_y_bf16(CUtensorMap* m, void* ptr, long long rows, long long cols);
 
