@@ -1722,44 +1722,39 @@ __global__ void __launch_bounds__(sc::kThreads, 3)
   tc::tc_fence_after();
   const uint32_t tm = *tptr;
 
+  // Step s arrives in slot s % 2 by TMA (B or C rows, x or dy rows, the row
+  // weights; bars[11 + slot] count the bytes), issued by the MMA warp: steps
+  // 0 and 1 at once, step s + 2 when the product of step s has completed.
+  uint64_t* cfull = &bars[11];
+  int issued = 0;  // MMA warp, lane 0: the steps whose copies it issued
+  const auto issue = [&](int s) {
+    const int sl = s % kStages;
+    const Chunk k = chunk_of(p, chunk_at(s));
+    unsigned char* st = base + sl * kSlotBytes;
+    tc::mbar_arrive_expect_tx(&cfull[sl], 2 * kAtom + (dir == 0 ? kAtom / 2 : kAtom) + 256);
+    const CUtensorMap* mv = dir == 0 ? &map_b : &map_c;  // [tokens][G][N]: 64 tokens x 64 n
+    tc::tma_load_3d(st + kAtom, mv, &cfull[sl], 0, g, (int)k.tok0);
+    tc::tma_load_3d(st + 2 * kAtom, mv, &cfull[sl], 64, g, (int)k.tok0);
+    // x (bf16) or dy (fp32), 32 columns of 64 tokens, row j at 64 j (x) or 128 j (dy)
+    tc::tma_load_3d(st, dir == 0 ? &map_x : &map_dy, &cfull[sl], q0, h, (int)k.tok0);
+    tc::bulk_load(base + oTab + 256 * sl, tabh + (long long)chunk_at(s) * p.H * kTabF + 64 * dir,
+                  256, &cfull[sl]);
+  };
+  // a slot's earlier copies complete (bounded) before it is refilled, so that
+  // the phases of its barrier never overlap, even after an expired wait
+  const auto issue_next = [&](int s) {
+    if (issued != s) return;
+    if (s >= kStages && !tc::mbar_wait(&cfull[s % kStages], ((s / kStages) - 1) & 1, p.wait_polls))
+      return;
+    issue(s);
+    issued = s + 1;
+  };
   if (w >= 4 && w < 8) {
-    // ---- converters: step s arrives in slot s % 2 by TMA (B or C rows, x or
-    //      dy rows, the row weights; one thread issues, bars[11 + slot] count
-    //      the bytes), then w o x (or exp(cum) o dy) for the block's 32
-    //      columns as [hi | lo] in one tile
+    // ---- converters: step s has arrived in slot s % 2 by TMA; w o x (or
+    //      exp(cum) o dy) for the block's 32 columns as [hi | lo] in one tile
     const int ct = t - 128;
-    uint64_t* cfull = &bars[11];
-    int issued = 0;  // thread ct == 0: the steps whose copies it issued
-    const auto issue = [&](int s) {
-      const int sl = s % kStages;
-      const Chunk k = chunk_of(p, chunk_at(s));
-      unsigned char* st = base + sl * kSlotBytes;
-      tc::mbar_arrive_expect_tx(&cfull[sl], 2 * kAtom + (dir == 0 ? kAtom / 2 : kAtom) + 256);
-      const CUtensorMap* mv = dir == 0 ? &map_b : &map_c;  // [tokens][G][N]: 64 tokens x 64 n
-      tc::tma_load_3d(st + kAtom, mv, &cfull[sl], 0, g, (int)k.tok0);
-      tc::tma_load_3d(st + 2 * kAtom, mv, &cfull[sl], 64, g, (int)k.tok0);
-      // x (bf16) or dy (fp32), 32 columns of 64 tokens, row j at 64 j (x) or 128 j (dy)
-      tc::tma_load_3d(st, dir == 0 ? &map_x : &map_dy, &cfull[sl], q0, h, (int)k.tok0);
-      tc::bulk_load(base + oTab + 256 * sl, tabh + (long long)chunk_at(s) * p.H * kTabF + 64 * dir,
-                    256, &cfull[sl]);
-    };
-    // a slot's earlier copies complete (bounded) before it is refilled, so that
-    // the phases of its barrier never overlap, even after an expired wait
-    const auto issue_next = [&](int s) {
-      if (issued != s) return;
-      if (s >= kStages && !tc::mbar_wait(&cfull[s % kStages], ((s / kStages) - 1) & 1, p.wait_polls))
-        return;
-      issue(s);
-      issued = s + 1;
-    };
-    if (ct == 0) issue_next(0);
     for (int s = 0; s < nc; ++s) {
       const int slot = s % kStages;
-      if (s + 1 < nc) {  // the next step's copies into the other slot, once its product is done
-        const int s1 = s + 1;
-        if (s1 >= kStages) ok &= bwait(&bars[2 + s1 % kStages], ((s1 / kStages) - 1) & 1, abort_f, p.wait_polls);
-        if (ct == 0) issue_next(s1);
-      }
       ok &= bwait(&cfull[slot], (s / kStages) & 1, abort_f, p.wait_polls);
       const int len = chunk_of(p, chunk_at(s)).len;
       const float* wrow = reinterpret_cast<const float*>(base + oTab + 256 * slot);
@@ -1817,12 +1812,10 @@ __global__ void __launch_bounds__(sc::kThreads, 3)
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&bars[slot]);
     }
-    // the last copies landed before the block's shared memory goes (bounded)
-    if (ct == 0)
-      for (int s = max(0, issued - kStages); s < issued; ++s)
-        (void)tc::mbar_wait(&cfull[s % kStages], (s / kStages) & 1, p.wait_polls);
   } else if (w == 8) {
     // ---- MMA warp
+    if (lane == 0)
+      for (int s = 0; s < kStages && s < nc; ++s) issue_next(s);
     for (int s = 0; s < nc; ++s) {
       const int slot = s % kStages, a = s & 1;
       ok &= bwait(&bars[slot], (s / kStages) & 1, abort_f, p.wait_polls);
@@ -1840,11 +1833,20 @@ __global__ void __launch_bounds__(sc::kThreads, 3)
           tc::mma_commit(&bars[4 + a]);  // (the test hook holds back the first one of one block)
       }
       __syncwarp();
+      // the slot's next copies, once this product has read it (bounded)
+      if (lane == 0 && s + kStages < nc &&
+          tc::mbar_wait(&bars[2 + slot], (uint32_t)((s / kStages) & 1), p.wait_polls))
+        issue_next(s + kStages);
+      __syncwarp();
     }
-    // every MMA of the block complete before its tensor memory is freed
+    // every MMA of the block complete before its tensor memory is freed, and
+    // the last copies landed before its shared memory goes (bounded)
     if (tc::elect_one()) tc::mma_commit(&bars[8]);
     __syncwarp();
     tc::mbar_wait(&bars[8], 0);
+    if (lane == 0)
+      for (int s = max(0, issued - kStages); s < issued; ++s)
+        (void)tc::mbar_wait(&cfull[s % kStages], (s / kStages) & 1, p.wait_polls);
   } else {
     // ---- state warps: row n of the transposed state, the block's 32 columns
     const int n = 32 * w + lane;
