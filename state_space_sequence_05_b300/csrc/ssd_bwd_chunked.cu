@@ -1627,9 +1627,11 @@ __global__ void __launch_bounds__(tg::kThreads, 1)
 // rows as [hi | lo] (32 columns each) in one MN-major tile; the state then
 // becomes exp(cum_last) state + hi + lo.  Warps 0-3 hold the state (row n =
 // TMEM lane n) and write it out through two 64B-swizzled shared tiles (hi,
-// lo) with TMA stores, warps 4-7 stage and convert the operands of a two-slot ring,
-// warp 8 issues the MMAs into a double-buffered accumulator.  Three blocks
-// fit on an SM.  Every wait is bounded (SSD_ERR_TIMEOUT).
+// lo) with TMA stores; warps 4-7 convert the operands of a two-slot ring
+// whose rows arrive by TMA; warp 8 issues those copies (a slot's next ones
+// once its product has read it, with an L2 prefetch of the x or dy rows two
+// steps further) and the MMAs into a double-buffered accumulator.  Three
+// blocks fit on an SM.  Every wait is bounded (SSD_ERR_TIMEOUT).
 namespace sc {
 constexpr int kStages = 2;
 constexpr int kQH = 32;                     // headdim columns per block (half of 64)
@@ -1739,6 +1741,10 @@ __global__ void __launch_bounds__(sc::kThreads, 3)
     tc::tma_load_3d(st, dir == 0 ? &map_x : &map_dy, &cfull[sl], q0, h, (int)k.tok0);
     tc::bulk_load(base + oTab + 256 * sl, tabh + (long long)chunk_at(s) * p.H * kTabF + 64 * dir,
                   256, &cfull[sl]);
+    if (s + 2 < nc) {  // the x or dy rows of two steps later into L2 (B and C rows are there)
+      const Chunk kp = chunk_of(p, chunk_at(s + 2));
+      tc::tma_prefetch_3d(dir == 0 ? &map_x : &map_dy, q0, h, (int)kp.tok0);
+    }
   };
   // a slot's earlier copies complete (bounded) before it is refilled, so that
   // the phases of its barrier never overlap, even after an expired wait
