@@ -229,7 +229,9 @@ ssd_status_t ssd_state_update(float *state, const void *x, const void *dt, const
  *   aligned, owned by the caller.  With headdim <= 64 and dstate <= 128
  *   (the chunked path, 64-token chunks): the state entering each chunk and
  *   the adjoint leaving it, [chunks][nheads] x headdim x dstate float32
- *   each, and per (chunk, head) its decay and a 144-float weight row; other
+ *   each (on the tensor-core path the same bytes hold each as a bf16
+ *   hi/lo pair of [chunks][nheads][dstate][headdim] arrays), and per
+ *   (chunk, head) its decay and a 144-float weight row; other
  *   shapes (the step-by-step path): one stored state every 64 steps and the
  *   64 states of one chunk, per (batch row, head).
  * Supported: headdim * dstate <= 16384, either input dtype; no cu_seqlens.
