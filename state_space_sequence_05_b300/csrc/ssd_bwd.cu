@@ -248,19 +248,12 @@ ssd_status_t bwd(const BwdArgs& a) {
   p.G = a.G;
   p.nck = (a.seqlen + kCk - 1) / kCk;
   p.nslice = (a.P + kRows - 1) / kRows;
-  const long long ntok = (long long)a.batch * a.seqlen;
-  // the accumulated gradients start at zero
-  if (cudaMemsetAsync(a.dA, 0, sizeof(float) * a.H, a.stream) != cudaSuccess ||
-      (ntok > 0 && cudaMemsetAsync(a.ddt, 0, sizeof(float) * ntok * a.H, a.stream) != cudaSuccess) ||
-      (a.dD && cudaMemsetAsync(a.dD, 0, sizeof(float) * a.H, a.stream) != cudaSuccess) ||
-      (ntok > 0 &&
-       (cudaMemsetAsync(a.dB, 0, sizeof(float) * ntok * a.G * a.N, a.stream) != cudaSuccess ||
-        cudaMemsetAsync(a.dC, 0, sizeof(float) * ntok * a.G * a.N, a.stream) != cudaSuccess)))
-    return SSD_ERR_CUDA;
+  // the chunked path zeroes the accumulated gradients itself
   auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
   if (a.seqlen > 0 && bwd_chunked_supported(a.P, a.N) && a16(a.init) && a16(a.dfinal) &&
       a16(a.dinit))
     return bwd_chunked(a);
+  if (bwd_zero_grads(a) != cudaSuccess) return SSD_ERR_CUDA;
   if (a.seqlen == 0) {
     // no steps: dinit = dL/dfinal
     if (a.dinit) {
@@ -281,6 +274,18 @@ ssd_status_t bwd(const BwdArgs& a) {
   k<<<a.batch * a.H * p.nslice, kBwdThreads, smem, a.stream>>>(p);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+cudaError_t bwd_zero_grads(const BwdArgs& a) {
+  const long long ntok = (long long)a.batch * a.seqlen;
+  cudaError_t e = cudaMemsetAsync(a.dA, 0, sizeof(float) * a.H, a.stream);
+  if (e == cudaSuccess && ntok > 0) e = cudaMemsetAsync(a.ddt, 0, sizeof(float) * ntok * a.H, a.stream);
+  if (e == cudaSuccess && a.dD) e = cudaMemsetAsync(a.dD, 0, sizeof(float) * a.H, a.stream);
+  if (e == cudaSuccess && ntok > 0)
+    e = cudaMemsetAsync(a.dB, 0, sizeof(float) * ntok * a.G * a.N, a.stream);
+  if (e == cudaSuccess && ntok > 0)
+    e = cudaMemsetAsync(a.dC, 0, sizeof(float) * ntok * a.G * a.N, a.stream);
+  return e;
 }
 
 }  // namespace ssd

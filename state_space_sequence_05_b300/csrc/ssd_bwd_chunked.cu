@@ -1654,6 +1654,21 @@ constexpr uint32_t kId = tc::idesc_bf16(128, 64, true, true);
 __global__ void __launch_bounds__(256) bwd_tab_kernel(BP p) {
   const int c = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 8 + w;
+  {  // the accumulated gradients start at zero (dB, dC in pairs: dstate is even)
+    const long long ntok = (long long)(gridDim.x / p.nc) * p.T;
+    const long long nth = (long long)gridDim.x * gridDim.y * blockDim.x;
+    const long long i0 = ((long long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long nbc = ntok * p.G * p.N / 2;
+    for (long long i = i0; i < nbc; i += nth) {
+      reinterpret_cast<float2*>(p.dB)[i] = make_float2(0.f, 0.f);
+      reinterpret_cast<float2*>(p.dC)[i] = make_float2(0.f, 0.f);
+    }
+    for (long long i = i0; i < ntok * p.H; i += nth) p.ddt[i] = 0.f;
+    if (i0 < p.H) {
+      p.dA[i0] = 0.f;
+      if (p.dD) p.dD[i0] = 0.f;
+    }
+  }
   if (h >= p.H) return;
   const Chunk k = chunk_of(p, c);
   const float Ah2 = p.A[h] * tg::kLog2e;
@@ -2018,6 +2033,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
                    al(a.C, 15) && al(a.dy, 15) && al(a.dx, 7) && al(a.dB, 7) && al(a.dC, 7) &&
                    al(a.dinit, 3);
   if (tcp) {
+    // (the table kernel also zeroes dA, ddt, dD, dB and dC)
     bwd_tab_kernel<<<dim3((unsigned)nch, (unsigned)((a.H + 7) / 8)), 256, 0, a.stream>>>(p);
     // the transposed states as bf16 hi/lo pairs: stored by the scans (32
     // columns x N rows per step), loaded by the gradient kernel (64 x 64 tiles)
@@ -2047,6 +2063,7 @@ ssd_status_t bwd_chunked(const BwdArgs& a) {
     count_launches(3);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
   }
+  if (bwd_zero_grads(a) != cudaSuccess) return SSD_ERR_CUDA;
   if (bf) {
     bwd_outer_kernel<true, 0><<<ggrid, kThr, outer_smem<true>(), a.stream>>>(p);
     bwd_outer_kernel<true, 1><<<ggrid, kThr, outer_smem<true>(), a.stream>>>(p);

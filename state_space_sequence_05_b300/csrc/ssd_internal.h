@@ -121,6 +121,9 @@ ssd_status_t bwd(const BwdArgs& a);
 bool bwd_chunked_supported(int P, int N);
 size_t bwd_chunked_workspace_bytes(int batch, int T, int H, int P, int N);
 ssd_status_t bwd_chunked(const BwdArgs& a);
+// dA, ddt, dD, dB and dC zeroed on the call's stream (the gradients that
+// the backward kernels accumulate).
+cudaError_t bwd_zero_grads(const BwdArgs& a);
 
 // Context parallelism: per-slice log-decay sums and the composition of the
 // slices' affine state maps.
