@@ -241,7 +241,8 @@ ssd_status_t ssd_state_update(float *state, const void *x, const void *dt, const
  *   of 8: three launches (a weight table, tcgen05 state scans, the tcgen05
  *   gradient kernel); other chunked shapes: five (warp-MMA chunk states,
  *   two state passes, the CUDA-core gradient kernel); the step-by-step
- *   path: one.  dA, dB, dC and dD are zeroed first.
+ *   path: one.  dA, ddt, dB, dC and dD are zeroed first (on the tensor-core
+ *   path by the weight-table launch, elsewhere by memsets).
  * dev_status: as for the forward (NULL allowed): zeroed by the call on its
  *   stream; a device wait that runs out writes SSD_ERR_TIMEOUT there and the
  *   outputs are undefined.

@@ -49,8 +49,9 @@
 //   bwd_grad_kernel      the same on CUDA cores for fp32 inputs and other
 //                        shapes, dB and dC summed over the slice in
 //                        registers.
-// dB, dC, dA and dD are added with atomics into buffers the entry point
-// zeroed.
+// dB, dC, dA and dD are added with atomics into zeroed buffers: on the
+// tensor-core path the weight-table kernel clears them (and ddt) first, on
+// the CUDA-core path memsets do.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
