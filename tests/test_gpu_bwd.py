@@ -103,6 +103,19 @@ def test_bwd_without_optional_inputs():
            use_D=False, use_init=False, use_dfinal=False, seed=2)
 
 
+def test_bwd_step_by_step_path():
+    """headdim 128 is past the chunked path's 64: the step-by-step kernel,
+    bf16 inputs, two batch rows, a ragged 64-step stretch at the end."""
+    _check(I.small_workload(batch=2, seqlen=90, nheads=2, headdim=128, dstate=32, ngroups=1,
+                            chunk=64, dtype="bf16", init="normal", seed=65), seed=7)
+
+
+def test_bwd_no_tokens():
+    """seqlen 0: dinit is dL/dfinal, every other gradient is zero."""
+    _check(I.small_workload(batch=2, seqlen=0, nheads=2, headdim=64, dstate=128, ngroups=1,
+                            chunk=64, dtype="bf16", init="normal", seed=66), seed=8)
+
+
 def test_bwd_l8k_shape_sampled_heads():
     """The metric's layer length (b1 T8192 H80 P64 N128, bf16, init, D):
     128 chunks of the chunked backward.  The fp64 oracle walks one head at a
