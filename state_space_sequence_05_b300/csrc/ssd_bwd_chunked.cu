@@ -42,10 +42,18 @@
 //   bwd_pass_kernel      per (row, head, state element): the states entering
 //                        each chunk (forwards) / the adjoints leaving each
 //                        chunk (backwards), in place; dinit;
+//   bwd_tab_kernel       per (chunk, head): the forward and adjoint weights
+//                        and the chunk decay; it also zeroes the gradients
+//                        the other kernels accumulate;
+//   bwd_scan_kernel      per (head, batch row, direction, half of headdim):
+//                        the states entering and the adjoints leaving every
+//                        chunk (tcgen05 chunk sums, operands by TMA), written
+//                        as bf16 hi/lo pairs;
 //   bwd_grad_tc_kernel   per (chunk, group, slice of up to 10 heads), bf16
 //                        inputs with headdim and dstate multiples of 8:
-//                        every gradient above on tcgen05 MMAs (M = 64), dB
-//                        and dC summed over the slice in tensor memory;
+//                        every gradient above on tcgen05 MMAs (M = 64 per
+//                        head), dB and dC transposed (M = 128) and summed
+//                        over the slice in tensor memory;
 //   bwd_grad_kernel      the same on CUDA cores for fp32 inputs and other
 //                        shapes, dB and dC summed over the slice in
 //                        registers.
